@@ -1,0 +1,281 @@
+/*
+ * oracle.c -- plain, single-threaded CPU definition of the weight-quantized
+ * decode linear layer (W4A8 and W8A16).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: only the tests, the smoke check and the CPU-baseline leg
+ * of the benchmark do.  It shares no code, header, table or constant
+ * generator with the CUDA library.
+ *
+ * Sources (pages that define the method):
+ *  [P1] "Jetson Orin AGX 上的 INT4 量化推理实践：从 9 tok/s 到 19.6 tok/s",
+ *       sections 当前实现方式 (row-wise INT4 weight with one scale per row;
+ *       activation dynamically quantized to INT8 before every linear;
+ *       output = int32 accumulate * weight_scale * activation_scale) and
+ *       正确方向 (INT4 weight, INT8 activation, int32 accumulate, float out).
+ *  [P2] "TPU-MLIR W8A16 for ChatGLM2-6B", section 2 (per-channel INT8
+ *       weights) and section 4 (the five steps: load, cast INT8 to F16,
+ *       multiply by the scale, matrix multiply with the activation, store).
+ * Where the pages leave a step open, the reading used is stated at the
+ * function (symmetric codes, divisors 7 and 127, round half away from zero,
+ * true division, low-nibble-first two's-complement packing, fp32 rescale in
+ * the order (acc * s_w) * s_a).
+ *
+ * Build: gcc -std=c11 -O2 -ffp-contract=off -fPIC -shared (no fast-math, no
+ * FMA contraction, so every float operation is one IEEE binary32 operation).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_SHAPE 3
+#define ORACLE_ERR_OVERFLOW 6
+
+/* ------------------------------------------------------------------------ */
+/* IEEE 754 binary16 <-> binary32, written from the format's definition.      */
+/* ------------------------------------------------------------------------ */
+
+/* binary16 bits -> float (always exact). */
+float oracle_half_to_float(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    float v;
+    if (e == 0x1F) {
+        v = m ? NAN : INFINITY;
+    } else if (e == 0) {
+        v = ldexpf((float)m, -24);          /* subnormal: m * 2^-24 */
+    } else {
+        v = ldexpf((float)(1024 + m), e - 25); /* (1 + m/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* float -> binary16 bits, round to nearest, ties to even. */
+uint16_t oracle_float_to_half(float f)
+{
+    uint32_t x;
+    memcpy(&x, &f, 4);
+    uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    uint32_t ax = x & 0x7FFFFFFFu;
+    if (ax > 0x7F800000u) return (uint16_t)(sign | 0x7E00u);   /* NaN */
+    if (ax == 0x7F800000u) return (uint16_t)(sign | 0x7C00u);  /* inf */
+    if (ax < 0x00800000u) return sign;  /* float subnormal: far below 2^-25 */
+
+    int e = (int)(ax >> 23) - 127;               /* |f| = m24 * 2^(e-23) */
+    uint32_t m24 = (ax & 0x7FFFFFu) | 0x800000u;
+    int eh = e < -14 ? -14 : e;                  /* binary16 exponent used */
+    /* quantum of the result is 2^(eh-10); n = |f| / quantum = m24 >> shift */
+    int shift = 13 + eh - e;
+    uint32_t n;
+    if (shift >= 32) {
+        n = 0;
+    } else {
+        n = m24 >> shift;
+        uint32_t rem = m24 & ((1u << shift) - 1u);
+        uint32_t half = 1u << (shift - 1);
+        if (rem > half || (rem == half && (n & 1u))) n += 1;
+    }
+    /* eh == -14: n is the full encoding (subnormal, or 0x400 = 2^-14).
+       otherwise n in [1024, 2048]; a carry to 2048 moves to the next
+       exponent naturally. */
+    uint32_t bits = (eh == -14) ? n : ((uint32_t)(eh + 15) << 10) + (n - 1024u);
+    if (bits >= 0x7C00u) bits = 0x7C00u;         /* overflow -> inf */
+    return (uint16_t)(sign | bits);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Symmetric rounding quantizer shared by the definitions below.             */
+/* ------------------------------------------------------------------------ */
+
+/* q = clamp(round_half_away(v / s), -qmax, qmax); s == 0 gives 0.
+   [P1 当前实现方式] weight_float ~ int4_value * weight_scale; the divisor,
+   rounding and clamp are the reading stated in the file header. */
+static int quant_code(float v, float s, int qmax)
+{
+    if (s == 0.0f) return 0;
+    float t = v / s;             /* one IEEE division */
+    float r = roundf(t);         /* halves go away from zero */
+    if (r > (float)qmax) r = (float)qmax;
+    if (r < (float)-qmax) r = (float)-qmax;
+    return (int)r;
+}
+
+static float row_absmax(const float* row, int64_t K)
+{
+    float m = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+        float a = fabsf(row[k]);
+        if (a > m) m = a;
+    }
+    return m;
+}
+
+/* ------------------------------------------------------------------------ */
+/* a1: row-wise INT4 weight quantizer + packing  [P1 当前实现方式]            */
+/* ------------------------------------------------------------------------ */
+
+/* W[N][K] fp32 -> Wq[N][K/2] packed nibbles + sw[N] fp32.
+   Per output row n: s = max|W[n,:]| / 7, q = clamp(round(W/s), -7, 7).
+   Byte j of a row holds q[2j] in bits 0..3 and q[2j+1] in bits 4..7,
+   each as a 4-bit two's-complement code. */
+int oracle_w4_quantize(const float* W, int64_t N, int64_t K, uint8_t* Wq, float* sw)
+{
+    if (N < 0 || K < 0 || (K & 1)) return ORACLE_ERR_SHAPE;
+    for (int64_t n = 0; n < N; ++n) {
+        const float* row = W + n * K;
+        float s = row_absmax(row, K) / 7.0f;
+        sw[n] = s;
+        for (int64_t j = 0; j < K / 2; ++j) {
+            int q0 = quant_code(row[2 * j], s, 7);
+            int q1 = quant_code(row[2 * j + 1], s, 7);
+            Wq[n * (K / 2) + j] = (uint8_t)((q0 & 0xF) | ((q1 & 0xF) << 4));
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Decode one 4-bit two's-complement code. */
+static int nibble_value(unsigned v)
+{
+    return v >= 8 ? (int)v - 16 : (int)v;
+}
+
+/* Wq[N][K/2] -> q[N][K] int8 codes (inverse of the packing above). */
+int oracle_w4_unpack(const uint8_t* Wq, int64_t N, int64_t K, int8_t* q)
+{
+    if (N < 0 || K < 0 || (K & 1)) return ORACLE_ERR_SHAPE;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t j = 0; j < K / 2; ++j) {
+            uint8_t b = Wq[n * (K / 2) + j];
+            q[n * K + 2 * j] = (int8_t)nibble_value(b & 0xFu);
+            q[n * K + 2 * j + 1] = (int8_t)nibble_value(b >> 4);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* a2: dynamic per-row INT8 activation quantizer  [P1 正确方向, 当前实现方式] */
+/* ------------------------------------------------------------------------ */
+
+/* X[M][K] binary16 -> Xq[M][K] int8 + sa[M] fp32.
+   Per activation row m: s_a = max|x| / 127, q = clamp(round(x/s_a), -127, 127). */
+int oracle_act_quantize(const uint16_t* X, int64_t M, int64_t K, int8_t* Xq, float* sa)
+{
+    if (M < 0 || K < 0) return ORACLE_ERR_SHAPE;
+    for (int64_t m = 0; m < M; ++m) {
+        float mx = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(oracle_half_to_float(X[m * K + k]));
+            if (a > mx) mx = a;
+        }
+        float s = mx / 127.0f;
+        sa[m] = s;
+        for (int64_t k = 0; k < K; ++k)
+            Xq[m * K + k] = (int8_t)quant_code(oracle_half_to_float(X[m * K + k]), s, 127);
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* a3+a4: integer dot products  [P1 正确方向: int8 x int8 -> int32]           */
+/* ------------------------------------------------------------------------ */
+
+/* acc[m][n] = sum_k Xq[m][k] * qw[n][k], summed in int64 and checked to fit
+   the int32 accumulator the pages name. */
+int oracle_w4a8_dot(const int8_t* Xq, int64_t M, int64_t K, const uint8_t* Wq, int64_t N,
+                    int32_t* acc)
+{
+    if (M < 0 || N < 0 || K < 0 || (K & 1)) return ORACLE_ERR_SHAPE;
+    int status = ORACLE_OK;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            int64_t s = 0;
+            for (int64_t j = 0; j < K / 2; ++j) {
+                uint8_t b = Wq[n * (K / 2) + j];
+                s += (int64_t)Xq[m * K + 2 * j] * nibble_value(b & 0xFu);
+                s += (int64_t)Xq[m * K + 2 * j + 1] * nibble_value(b >> 4);
+            }
+            if (s > INT32_MAX || s < INT32_MIN) status = ORACLE_ERR_OVERFLOW;
+            acc[m * N + n] = (int32_t)s;
+        }
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* a5: rescale  [P1 当前实现方式: output = acc * weight_scale * act_scale]    */
+/* ------------------------------------------------------------------------ */
+
+/* Y[m][n] = ((float)acc * sw[n]) * sa[m]; two fp32 round-to-nearest
+   multiplies in this order. */
+void oracle_w4a8_rescale(const int32_t* acc, const float* sw, const float* sa, int64_t M,
+                         int64_t N, float* Y)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            float t = (float)acc[m * N + n] * sw[n];
+            Y[m * N + n] = t * sa[m];
+        }
+    }
+}
+
+/* a-f: the whole W4A8 linear as the pages describe it: quantize the
+   activation, integer dot, rescale.  Xq_out / sa_out / acc_out receive the
+   intermediates (all required here; the oracle is for checking). */
+int oracle_w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                       const float* sw, int64_t N, float* Y, int8_t* Xq_out, float* sa_out,
+                       int32_t* acc_out)
+{
+    int st = oracle_act_quantize(X, M, K, Xq_out, sa_out);
+    if (st != ORACLE_OK) return st;
+    st = oracle_w4a8_dot(Xq_out, M, K, Wq, N, acc_out);
+    oracle_w4a8_rescale(acc_out, sw, sa_out, M, N, Y);
+    return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* b1: per-output-channel INT8 weight quantizer  [P2 sections 2 and 3]       */
+/* ------------------------------------------------------------------------ */
+
+/* W[N][K] fp32 -> Wq8[N][K] int8 + sw16[N] binary16.
+   Per output channel n: s = fp16(max|W[n,:]| / 127); the codes are taken
+   with that rounded scale: q = clamp(round(W / float(s)), -127, 127). */
+int oracle_w8_quantize(const float* W, int64_t N, int64_t K, int8_t* Wq8, uint16_t* sw16)
+{
+    if (N < 0 || K < 0) return ORACLE_ERR_SHAPE;
+    for (int64_t n = 0; n < N; ++n) {
+        const float* row = W + n * K;
+        uint16_t h = oracle_float_to_half(row_absmax(row, K) / 127.0f);
+        float s = oracle_half_to_float(h);
+        sw16[n] = h;
+        for (int64_t k = 0; k < K; ++k) Wq8[n * K + k] = (int8_t)quant_code(row[k], s, 127);
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* b2: W8A16 product, fp64 reference  [P2 section 4, steps 2-4]              */
+/* ------------------------------------------------------------------------ */
+
+/* Y[m][n] = sum_k (q[n][k] * s[n]) * x[m][k], every product and sum in
+   binary64: step 2 casts the code, step 3 multiplies by the scale
+   (dequantize), step 4 multiplies with the activation. */
+void oracle_w8a16_ref(const uint16_t* X, int64_t M, int64_t K, const int8_t* Wq8,
+                      const uint16_t* sw16, int64_t N, double* Y)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double s = (double)oracle_half_to_float(sw16[n]);
+            double y = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double w = (double)Wq8[n * K + k] * s;
+                y += w * (double)oracle_half_to_float(X[m * K + k]);
+            }
+            Y[m * N + n] = y;
+        }
+    }
+}

@@ -1,0 +1,435 @@
+"""Pins for the CPU oracle: checks against what the pages and mathematics fix.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with something other than itself: hand-derived
+closed forms from ``tests/golden/``, sizes printed on the pages, exhaustive
+comparisons with numpy's IEEE binary16 conversion, exact rational arithmetic,
+numpy integer/fp64 matrix products on decoded codes, invariants of
+round-to-nearest quantization and a deterministic end-to-end error bound.
+
+The same functions run against deliberately broken copies of ``oracle.c`` in
+``test_oracle_mutations.py``: every planted mistake must trip at least one pin.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def read_cases(name):
+    """Parse a golden file made of ``case <name>`` blocks of ``key: values``."""
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            if line.startswith("case "):
+                cur = {"name": line[5:].strip()}
+                cases.append(cur)
+            else:
+                key, val = line.split(":", 1)
+                cur[key.strip()] = val.split()
+    return cases
+
+
+def read_kv(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                k, v = line.split(":", 1)
+                out[k.strip()] = float(v)
+    return out
+
+
+def f32_nearest(fr: Fraction) -> np.float32:
+    """Exact round-to-nearest-even of a rational into binary32 (normal range)."""
+    if fr == 0:
+        return np.float32(0.0)
+    neg = fr < 0
+    a = -fr if neg else fr
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    assert -126 <= e <= 127
+    scaled = a / Fraction(2) ** (e - 23)          # in [2^23, 2^24)
+    n = scaled.numerator // scaled.denominator
+    rem = scaled - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    v = math.ldexp(float(n), e - 23)
+    return np.float32(-v if neg else v)
+
+
+def round_half_away(v: float) -> int:
+    a = abs(v)
+    r = math.floor(a + 0.5) if a - math.floor(a) != 0.5 else math.floor(a) + 1
+    return int(math.copysign(r, v)) if r else 0
+
+
+def decode_nibbles(Wq: np.ndarray) -> np.ndarray:
+    """Independent decode used only to feed numpy products (pinned by golden bytes)."""
+    lo = (Wq & 0x0F).astype(np.int16)
+    hi = (Wq >> 4).astype(np.int16)
+    lo = np.where(lo >= 8, lo - 16, lo)
+    hi = np.where(hi >= 8, hi - 16, hi)
+    out = np.empty((Wq.shape[0], Wq.shape[1] * 2), np.int64)
+    out[:, 0::2] = lo
+    out[:, 1::2] = hi
+    return out
+
+
+# --------------------------------------------------------------------------
+# binary16
+# --------------------------------------------------------------------------
+
+def pin_half_decode_exhaustive(o):
+    """All 65536 binary16 patterns decode exactly as numpy's IEEE conversion."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([o.half_to_float(int(b)) for b in bits], dtype=np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def pin_half_encode(o):
+    """Round-to-nearest-even float->binary16 agrees with numpy on edge values
+    (ties, overflow threshold, subnormal boundaries) and random bit patterns."""
+    edges = [0.0, -0.0, 1.0, 65504.0, 65519.996, 65520.0, 65536.0, 1e9, -65520.0,
+             2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -26, 2.0 ** -14,
+             2.0 ** -14 - 2.0 ** -25, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11,
+             2049.0, 2051.0, 1e-30, -1e-30, float("inf"), -float("inf"), 5.9604645e-08,
+             8.940697e-08, 0.33325195, 1.0 / 3.0]
+    rng = np.random.Generator(np.random.PCG64(12345))
+    rand_bits = rng.integers(0, 2 ** 32, size=60000, dtype=np.uint64).astype(np.uint32)
+    # bias the random set towards the binary16 range (exponents 100..150)
+    near = (rng.integers(100, 150, size=60000).astype(np.uint32) << 23) | (
+        rng.integers(0, 2 ** 23, size=60000).astype(np.uint32)) | (
+        rng.integers(0, 2, size=60000).astype(np.uint32) << 31)
+    vals = np.concatenate([np.array(edges, np.float32), rand_bits.view(np.float32),
+                           near.view(np.float32)])
+    with np.errstate(over="ignore", invalid="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([o.float_to_half(float(v)) for v in vals], dtype=np.uint16)
+    nan = np.isnan(vals)
+    assert np.all((got[nan] & 0x7C00) == 0x7C00) and np.all((got[nan] & 0x3FF) != 0)
+    bad = np.nonzero(got[~nan] != ref[~nan])[0]
+    assert bad.size == 0, "first mismatch at %r" % (vals[~nan][bad[:3]],)
+
+
+# --------------------------------------------------------------------------
+# a1: INT4 weight quantizer and packing
+# --------------------------------------------------------------------------
+
+def pin_w4_golden(o):
+    """Hand-derived closed forms: scale, codes, packed bytes, decode."""
+    for c in read_cases("w4_quant_closed_forms.txt"):
+        row = np.array([float(v) for v in c["row"]], np.float32)[None, :]
+        Wq, sw = o.w4_quantize(row)
+        assert sw[0] == np.float32(float(c["scale"][0])), c["name"]
+        want = np.array([int(b, 16) for b in c["bytes"]], np.uint8)
+        assert np.array_equal(Wq[0], want), (c["name"], Wq[0], want)
+        codes = np.array([int(v) for v in c["codes"]], np.int8)
+        assert np.array_equal(o.w4_unpack(Wq, row.shape[1])[0], codes), c["name"]
+
+
+def pin_w4_all_code_pairs(o):
+    """Every pair of codes in [-7, 7] survives quantize -> pack -> unpack, and
+    the byte equals the two's-complement nibbles, low nibble first."""
+    codes = np.array([(a, b) for a in range(-7, 8) for b in range(-7, 8)], np.int64).ravel()
+    row = np.concatenate([[7.0], codes.astype(np.float64), [0.0]]).astype(np.float32)[None, :]
+    Wq, sw = o.w4_quantize(row)
+    assert sw[0] == 1.0
+    q = o.w4_unpack(Wq, row.shape[1])[0]
+    assert np.array_equal(q[1:-1], codes)
+    # byte j holds codes 2j (low) and 2j+1 (high); shift by one for the leading 7
+    b = Wq[0]
+    assert np.array_equal(decode_nibbles(Wq)[0], q.astype(np.int64))
+    lows = [(int(v) & 0xF) for v in q[0::2]]
+    highs = [(int(v) & 0xF) for v in q[1::2]]
+    assert list(b) == [lo | (hi << 4) for lo, hi in zip(lows, highs)]
+
+
+def pin_w4_true_division(o):
+    """Codes follow round(fl(w / s)) with a correctly rounded IEEE quotient,
+    checked in exact rational arithmetic on near-tie inputs."""
+    rng = np.random.Generator(np.random.PCG64(7))
+    rows = []
+    for _ in range(400):
+        mx = np.float32(rng.uniform(0.01, 1.0))
+        s = f32_nearest(Fraction(float(mx)) / 7)
+        r = [mx]
+        for k in range(-6, 7):
+            t = Fraction(2 * k + 1, 2)  # a .5 tie of the quotient
+            w = np.float32(float(t * Fraction(float(s))))
+            for d in (-2, -1, 0, 1, 2):
+                v = w
+                for _ in range(abs(d)):
+                    v = np.nextafter(v, np.float32(np.inf if d > 0 else -np.inf), dtype=np.float32)
+                r.append(v)
+        rows.append(r[:64] if len(r) >= 64 else r + [0.0] * (64 - len(r)))
+    W = np.array(rows, np.float32)
+    Wq, sw = o.w4_quantize(W)
+    q = o.w4_unpack(Wq, W.shape[1])
+    for n in range(W.shape[0]):
+        s = Fraction(float(sw[n]))
+        assert sw[n] == f32_nearest(Fraction(float(np.max(np.abs(W[n])))) / 7)
+        for k in range(W.shape[1]):
+            t = f32_nearest(Fraction(float(W[n, k])) / s) if W[n, k] != 0 else np.float32(0)
+            want = max(-7, min(7, round_half_away(float(t))))
+            assert q[n, k] == want, (n, k, float(W[n, k]), float(sw[n]), q[n, k], want)
+
+
+def pin_w4_invariants(o):
+    """On seeded N(0, 0.02) rows (with a few x20 outliers): |w - q*s| <= s/2,
+    the row's largest |w| gets code +-7 with its sign, codes stay in [-7, 7]."""
+    W = synth.normal(11, (48, 896), 0.02)
+    W[5, 100] *= 20.0
+    W[9, :] = 0.0
+    W[17, 3] = -0.5
+    Wq, sw = o.w4_quantize(W)
+    q = o.w4_unpack(Wq, W.shape[1]).astype(np.float64)
+    s = sw.astype(np.float64)[:, None]
+    err = np.abs(W.astype(np.float64) - q * s)
+    assert np.all(err <= s / 2 * (1 + 2 ** -20) + 1e-45)
+    assert np.all(np.abs(q) <= 7)
+    for n in range(W.shape[0]):
+        if sw[n] == 0:
+            assert not W[n].any() and not q[n].any()
+            continue
+        k = int(np.argmax(np.abs(W[n])))
+        assert q[n, k] == 7 * np.sign(W[n, k])
+        assert abs(float(sw[n]) * 7 - float(np.max(np.abs(W[n])))) <= 4e-7 * float(np.max(np.abs(W[n])))
+
+
+# --------------------------------------------------------------------------
+# a2: activation quantizer
+# --------------------------------------------------------------------------
+
+def pin_act_golden(o):
+    for c in read_cases("act_quant_closed_forms.txt"):
+        x = np.array([float(v) for v in c["x"]], np.float16)[None, :]
+        assert np.array_equal(x.astype(np.float64)[0], [float(v) for v in c["x"]])
+        Xq, sa = o.act_quantize(x)
+        assert sa[0] == np.float32(float(c["scale"][0])), c["name"]
+        assert np.array_equal(Xq[0], np.array([int(v) for v in c["codes"]], np.int8)), c["name"]
+
+
+def pin_act_invariants(o):
+    """|x - q*s_a| <= s_a/2, max |x| -> +-127, codes within [-127, 127], per row."""
+    X = synth.activation(21, 6, 3584, outlier_frac=0.001)
+    X[2] = 0
+    Xq, sa = o.act_quantize(X)
+    x = X.astype(np.float64)
+    s = sa.astype(np.float64)[:, None]
+    assert np.all(np.abs(x - Xq.astype(np.float64) * s) <= s / 2 * (1 + 2 ** -20) + 1e-45)
+    assert np.all(np.abs(Xq.astype(np.int64)) <= 127)
+    for m in range(X.shape[0]):
+        if sa[m] == 0:
+            assert not Xq[m].any()
+            continue
+        k = int(np.argmax(np.abs(x[m])))
+        assert Xq[m, k] == 127 * np.sign(x[m, k])
+        assert sa[m] == f32_nearest(Fraction(float(np.max(np.abs(x[m])))) / 127)
+
+
+# --------------------------------------------------------------------------
+# a3+a4: integer dot
+# --------------------------------------------------------------------------
+
+def pin_dot_closed_forms(o):
+    K = 96
+    W = np.full((2, K // 2), 0x77, np.uint8)          # every code +7
+    X = np.full((1, K), 127, np.int8)
+    assert np.all(o.w4a8_dot(X, W) == 889 * K)
+    X2 = np.tile(np.array([127, -127], np.int8), K // 2)[None, :]
+    assert np.all(o.w4a8_dot(X2, W) == 0)
+    # asymmetric byte: low code 7, high code 1; activation only on even k
+    W3 = np.full((1, K // 2), 0x17, np.uint8)
+    X3 = np.tile(np.array([1, 0], np.int8), K // 2)[None, :]
+    assert o.w4a8_dot(X3, W3)[0, 0] == 7 * (K // 2)
+    X4 = np.tile(np.array([0, 1], np.int8), K // 2)[None, :]
+    assert o.w4a8_dot(X4, W3)[0, 0] == 1 * (K // 2)
+    # one-hot activations recover every code at its index
+    W5 = np.frombuffer(bytes(range(0, 256, 3))[:K // 2], np.uint8)[None, :].copy()
+    q = decode_nibbles(W5)[0]
+    for k in range(K):
+        e = np.zeros((1, K), np.int8)
+        e[0, k] = -127
+        assert o.w4a8_dot(e, W5)[0, 0] == -127 * q[k]
+    # extreme magnitudes: -8 codes (legal on input) with -127 activations
+    W6 = np.full((1, K // 2), 0x88, np.uint8)
+    assert o.w4a8_dot(np.full((1, K), -127, np.int8), W6)[0, 0] == 8 * 127 * K
+
+
+def pin_dot_bruteforce(o):
+    """acc equals numpy's int64 matrix product of the decoded codes."""
+    for (M, N, K, seed) in [(1, 7, 64, 1), (3, 5, 32, 2), (4, 9, 160, 3)]:
+        W = synth.normal(seed, (N, K), 0.02)
+        Wq, _ = o.w4_quantize(W)
+        Xq, _ = o.act_quantize(synth.activation(seed + 100, M, K))
+        ref = Xq.astype(np.int64) @ decode_nibbles(Wq).T
+        assert np.array_equal(o.w4a8_dot(Xq, Wq).astype(np.int64), ref)
+
+
+# --------------------------------------------------------------------------
+# a5: rescale
+# --------------------------------------------------------------------------
+
+def pin_rescale_powers_of_two(o):
+    """With power-of-two scales the result is exact: Y[m][n] = acc * 2^-(n+3) * 2^-(4m)."""
+    M, N = 3, 6
+    acc = (np.arange(M * N, dtype=np.int64).reshape(M, N) * 7919 - 40000).astype(np.int32)
+    sw = np.array([2.0 ** -(n + 3) for n in range(N)], np.float32)
+    sa = np.array([2.0 ** -(4 * m) for m in range(M)], np.float32)
+    Y = o.w4a8_rescale(acc, sw, sa)
+    want = np.array([[acc[m, n] * 2.0 ** -(n + 3) * 2.0 ** -(4 * m) for n in range(N)]
+                     for m in range(M)])
+    assert np.array_equal(Y.astype(np.float64), want)
+
+
+def pin_rescale_order(o):
+    """The fixed contract: (float(acc) * s_w) * s_a, each product rounded to
+    binary32; checked with exact rationals on values where orders differ."""
+    rng = np.random.Generator(np.random.PCG64(3))
+    acc = rng.integers(-2 ** 30, 2 ** 30, size=(4, 64)).astype(np.int32)
+    sw = rng.uniform(1e-4, 1e-2, size=64).astype(np.float32)
+    sa = rng.uniform(1e-3, 1.0, size=4).astype(np.float32)
+    Y = o.w4a8_rescale(acc, sw, sa)
+    differs = 0
+    for m in range(4):
+        for n in range(64):
+            a = f32_nearest(Fraction(int(acc[m, n])))
+            t = f32_nearest(Fraction(float(a)) * Fraction(float(sw[n])))
+            y = f32_nearest(Fraction(float(t)) * Fraction(float(sa[m])))
+            assert Y[m, n] == y
+            other = f32_nearest(Fraction(float(a)) *
+                                Fraction(float(f32_nearest(Fraction(float(sw[n])) * Fraction(float(sa[m]))))))
+            differs += int(other != y)
+    assert differs > 0  # the inputs do separate the two orders
+
+
+# --------------------------------------------------------------------------
+# a-f: end to end
+# --------------------------------------------------------------------------
+
+def pin_linear_error_bound(o):
+    """Quantized linear vs fp64 unquantized GEMV within the deterministic bound
+    sum_k(|w| s_a/2 + |x| s_w/2 + 3 s_w s_a/4)(1+2^-18) + 3*2^-24 |Y|."""
+    for (M, N, K, seed) in [(1, 64, 896, 5), (2, 16, 3584, 6)]:
+        W = synth.normal(seed, (N, K), 0.02)
+        X = synth.activation(seed + 50, M, K, outlier_frac=0.001)
+        Wq, sw = o.w4_quantize(W)
+        Y, Xq, sa, acc = o.w4a8_linear(X, Wq, sw)
+        ref = X.astype(np.float64) @ W.astype(np.float64).T
+        s_w = sw.astype(np.float64)[None, :]
+        s_a = sa.astype(np.float64)[:, None]
+        bound = ((np.abs(X).astype(np.float64).sum(1)[:, None] * s_w / 2
+                  + np.abs(W).astype(np.float64).sum(1)[None, :] * s_a / 2
+                  + K * 3 * s_w * s_a / 4) * (1 + 2 ** -18) + 3 * 2.0 ** -24 * np.abs(Y))
+        assert np.all(np.abs(Y.astype(np.float64) - ref) <= bound)
+        # sanity: row-wise INT4 keeps the output's direction (measured ~0.985)
+        cos = float((Y.astype(np.float64) * ref).sum() /
+                    np.sqrt((Y.astype(np.float64) ** 2).sum() * (ref ** 2).sum()))
+        assert cos > 0.97
+
+
+# --------------------------------------------------------------------------
+# b1/b2: W8A16
+# --------------------------------------------------------------------------
+
+def pin_w8_quantize(o):
+    """Scale is binary16(max|w|/127) (numpy's conversion); codes satisfy
+    |w - q*s| <= s/2 unless clamped at +-127; the largest |w| maps to +-127."""
+    W = synth.normal(31, (40, 4096), 0.02)
+    W[3] = 0
+    W[7] *= 1e-3          # scale lands among binary16 subnormals: clamping matters
+    W[8, 11] = 1e-5
+    Wq8, sw16 = o.w8_quantize(W)
+    for n in range(W.shape[0]):
+        mx = np.float32(np.max(np.abs(W[n])))
+        assert sw16[n] == (mx / np.float32(127.0)).astype(np.float16)
+    s = sw16.astype(np.float64)[:, None]
+    q = Wq8.astype(np.float64)
+    w = W.astype(np.float64)
+    assert np.all(np.abs(q) <= 127)
+    free = np.abs(w) < 127.5 * s * (1 - 2 ** -20)
+    ok = np.abs(w - q * s) <= s / 2 * (1 + 2 ** -20) + 1e-45
+    assert np.all(ok | ~free)
+    assert np.all(np.where(~free & (s > 0), np.abs(q) == 127, True))
+    for n in range(W.shape[0]):
+        if sw16[n] == 0:
+            assert not Wq8[n].any()
+        else:
+            k = int(np.argmax(np.abs(W[n])))
+            assert Wq8[n, k] == 127 * np.sign(W[n, k])
+
+
+def pin_w8_sizes(o):
+    """Page 2 section 3: 4096 x 27392 -> 214 MB F16, 107 MB INT8, scale 0.008 MB."""
+    g = read_kv("w8a16_sizes.txt")
+    K, N = int(g["K"]), int(g["N"])
+    W = synth.normal(1, (2, K), 0.02)
+    Wq8, sw16 = o.w8_quantize(W)
+    assert Wq8.itemsize == 1 and sw16.itemsize == 2
+    mib = 2.0 ** 20
+    assert K * N * 2 / mib == g["f16_weight_mib"]
+    assert K * N * Wq8.itemsize / mib == g["int8_weight_mib"]
+    assert round(g["page_scale_count"] * sw16.itemsize / 1e6, 3) == g["page_scale_mb"] or \
+        round(g["page_scale_count"] * sw16.itemsize / mib, 3) == g["page_scale_mb"]
+
+
+def pin_w8a16_closed_form(o):
+    """Integer weights with row max 127 have scale exactly 1: y = sum of codes * x."""
+    K = 64
+    W = np.zeros((3, K), np.float32)
+    W[0, :] = 127
+    W[1, :] = np.arange(K) - 32
+    W[1, 0] = 127
+    W[2, 5] = -127
+    Wq8, sw16 = o.w8_quantize(W)
+    assert np.all(sw16 == 1.0) and np.array_equal(Wq8.astype(np.float32), W)
+    X = np.ones((1, K), np.float16)
+    Y = o.w8a16_ref(X, Wq8, sw16)
+    assert np.array_equal(Y[0], W.astype(np.float64).sum(1))
+    X2 = np.zeros((1, K), np.float16)
+    X2[0, 5] = 0.5
+    assert np.array_equal(o.w8a16_ref(X2, Wq8, sw16)[0], W[:, 5].astype(np.float64) * 0.5)
+
+
+def pin_w8a16_bruteforce_and_bound(o):
+    """fp64 reference equals numpy's fp64 product of the dequantized matrix, is
+    within sum_k |x| s/2 of the unquantized product, and cosine > 0.99 (page 2
+    section 2 reports > 99% cosine similarity against F16)."""
+    for (M, N, K, seed) in [(1, 32, 4096, 41), (3, 8, 1024, 42)]:
+        W = synth.normal(seed, (N, K), 0.02)
+        X = synth.activation(seed + 1, M, K)
+        Wq8, sw16 = o.w8_quantize(W)
+        Y = o.w8a16_ref(X, Wq8, sw16)
+        deq = Wq8.astype(np.float64) * sw16.astype(np.float64)[:, None]
+        ref = X.astype(np.float64) @ deq.T
+        assert np.allclose(Y, ref, rtol=1e-12, atol=1e-12)
+        exact = X.astype(np.float64) @ W.astype(np.float64).T
+        bound = np.abs(X).astype(np.float64).sum(1)[:, None] * sw16.astype(np.float64)[None, :] / 2
+        assert np.all(np.abs(Y - exact) <= bound * (1 + 1e-9) + 1e-12)
+        cos = float((Y * exact).sum() / np.sqrt((Y ** 2).sum() * (exact ** 2).sum()))
+        assert cos > 0.99
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,70 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and check that
+at least one pin catches each.  This is what makes the pins a check of the
+oracle rather than a restatement of it."""
+import os
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(os.path.abspath(oracle.__file__)), "oracle.c")
+
+# (name, exact text in oracle.c, replacement)
+MUTATIONS = [
+    ("round_half_even", "float r = roundf(t);", "float r = rintf(t);"),
+    ("round_toward_zero", "float r = roundf(t);", "float r = truncf(t);"),
+    ("reciprocal_multiply", "float t = v / s;", "float t = v * (1.0f / s);"),
+    ("nibble_order_pack",
+     "(uint8_t)((q0 & 0xF) | ((q1 & 0xF) << 4))", "(uint8_t)((q1 & 0xF) | ((q0 & 0xF) << 4))"),
+    ("nibble_unsigned", "return v >= 8 ? (int)v - 16 : (int)v;", "return (int)v;"),
+    ("nibble_sign_offset", "return v >= 8 ? (int)v - 16 : (int)v;", "return v >= 8 ? (int)v - 15 : (int)v;"),
+    ("w4_divisor_8", "row_absmax(row, K) / 7.0f", "row_absmax(row, K) / 8.0f"),
+    ("act_divisor_128", "float s = mx / 127.0f;", "float s = mx / 128.0f;"),
+    ("absmax_without_abs", "float a = fabsf(row[k]);", "float a = row[k];"),
+    ("act_row_index", "quant_code(oracle_half_to_float(X[m * K + k]), s, 127)",
+     "quant_code(oracle_half_to_float(X[k]), s, 127)"),
+    ("dot_nibble_swap",
+     "s += (int64_t)Xq[m * K + 2 * j] * nibble_value(b & 0xFu);\n"
+     "                s += (int64_t)Xq[m * K + 2 * j + 1] * nibble_value(b >> 4);",
+     "s += (int64_t)Xq[m * K + 2 * j] * nibble_value(b >> 4);\n"
+     "                s += (int64_t)Xq[m * K + 2 * j + 1] * nibble_value(b & 0xFu);"),
+    ("dot_dropped_high", "s += (int64_t)Xq[m * K + 2 * j + 1] * nibble_value(b >> 4);", ""),
+    ("dot_transposed_act", "(int64_t)Xq[m * K + 2 * j]", "(int64_t)Xq[n * K + 2 * j]"),
+    ("rescale_swapped_index", "float t = (float)acc[m * N + n] * sw[n];\n            Y[m * N + n] = t * sa[m];",
+     "float t = (float)acc[m * N + n] * sa[m];\n            Y[m * N + n] = t * sw[n];"),
+    ("rescale_dropped_sa", "Y[m * N + n] = t * sa[m];", "Y[m * N + n] = t;"),
+    ("rescale_sw_row_index", "* sw[n];", "* sw[m];"),
+    ("clamp_dropped", "if (r > (float)qmax) r = (float)qmax;", ""),
+    ("w8_unrounded_scale", "float s = oracle_half_to_float(h);", "float s = row_absmax(row, K) / 127.0f;"),
+    ("w8a16_scale_twice", "double w = (double)Wq8[n * K + k] * s;", "double w = (double)Wq8[n * K + k] * s * s;"),
+    ("w8a16_scale_dropped", "double w = (double)Wq8[n * K + k] * s;", "double w = (double)Wq8[n * K + k];"),
+    ("half_subnormal_exponent", "v = ldexpf((float)m, -24);", "v = ldexpf((float)m, -25);"),
+    ("half_normal_bias", "ldexpf((float)(1024 + m), e - 25)", "ldexpf((float)(1024 + m), e - 24)"),
+    ("half_encode_ties_up", "if (rem > half || (rem == half && (n & 1u))) n += 1;", "if (rem >= half) n += 1;"),
+    ("half_encode_truncate", "if (rem > half || (rem == half && (n & 1u))) n += 1;", ""),
+    ("half_encode_overflow", "if (bits >= 0x7C00u) bits = 0x7C00u;", ""),
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_mutation_is_caught(tmp_path, source, name, old, new):
+    assert source.count(old) >= 1, "mutation %s no longer matches oracle.c" % name
+    path = tmp_path / "oracle_mut.c"
+    path.write_text(source.replace(old, new))
+    lib = oracle.compile_oracle(str(path), str(tmp_path / "liboracle_mut.so"))
+    mut = oracle.Oracle(lib)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(mut)
+        except (AssertionError, ValueError, OverflowError, IndexError):
+            caught.append(pin.__name__)
+            break
+    assert caught, "planted mistake %r passed every pin" % name
