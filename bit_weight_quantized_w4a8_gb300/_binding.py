@@ -1,0 +1,261 @@
+"""ctypes binding of libw4a8.so: the entry points of include/w4a8.h under the
+same names, taking torch CUDA tensors.
+
+Argument marshalling only: every step of the linear runs in the library's
+CUDA kernels.  There is no fallback: if the library is missing or a call is
+rejected, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libw4a8.so")
+
+OK = 0
+ERR_NULL, ERR_ALIGN, ERR_SHAPE, ERR_WORKSPACE, ERR_CUDA = 1, 2, 3, 4, 5
+LAUNCH_PDL = 1
+W4A8_MAX_M = 8
+W8A16_MAX_M = 4
+
+EXPORTS = [
+    "w4_quantize_weights", "w8_quantize_weights", "act_quantize_i8",
+    "w4a8_workspace_bytes", "w4a8_gemv", "w4a8_linear",
+    "w8a16_workspace_bytes", "w8a16_gemv",
+    "w4a8_last_error", "w4a8_device_error", "w4a8_set_tuning", "w4a8_plan_info",
+]
+
+
+class W4A8Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("status %d: %s" % (status, message))
+        self.status = status
+
+
+class _Tuning(ctypes.Structure):
+    _fields_ = [("force_splits", ctypes.c_int), ("force_threads_per_row", ctypes.c_int),
+                ("ring_bytes", ctypes.c_int), ("ctas_per_sm", ctypes.c_int)]
+
+
+_i64, _p, _u = ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint
+_SIGS = {
+    "w4_quantize_weights": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _p]),
+    "w8_quantize_weights": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _p]),
+    "act_quantize_i8": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _p]),
+    "w4a8_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
+    "w4a8_gemv": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, ctypes.c_size_t, _u, _p]),
+    "w4a8_linear": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _p, _p, ctypes.c_size_t, _u, _p]),
+    "w8a16_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
+    "w8a16_gemv": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _p, ctypes.c_size_t, _u, _p]),
+    "w4a8_last_error": (ctypes.c_char_p, []),
+    "w4a8_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint), _p]),
+    "w4a8_set_tuning": (ctypes.c_int, [ctypes.POINTER(_Tuning)]),
+    "w4a8_plan_info": (ctypes.c_int, [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libw4a8.so not built: call __graft_entry__.build() or "
+                              "python -m bit_weight_quantized_w4a8_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(st: int):
+    if st != OK:
+        raise W4A8Error(st, lib().w4a8_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _want(t, dtype, name, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+_ws_cache = {}
+
+
+def _workspace(nbytes: int, device: torch.device, ws):
+    """Caller-provided workspace, or a cached zero-filled one per device."""
+    if nbytes == 0:
+        return ws
+    if ws is not None:
+        return ws
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+# --------------------------------------------------------------------------
+# entry points
+# --------------------------------------------------------------------------
+
+def w4_quantize_weights(W: torch.Tensor, Wq=None, sw=None):
+    """W [N][K] fp32 -> (Wq [N][K/2] uint8, sw [N] fp32)."""
+    _want(W, torch.float32, "W")
+    N, K = W.shape
+    Wq = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device) if Wq is None else Wq
+    sw = torch.empty((N,), dtype=torch.float32, device=W.device) if sw is None else sw
+    _want(Wq, torch.uint8, "Wq", (N, K // 2))
+    _want(sw, torch.float32, "sw", (N,))
+    _check(lib().w4_quantize_weights(_ptr(W), N, K, _ptr(Wq), _ptr(sw), _stream(W)))
+    return Wq, sw
+
+
+def w8_quantize_weights(W: torch.Tensor, Wq8=None, sw16=None):
+    """W [N][K] fp32 -> (Wq8 [N][K] int8, sw16 [N] fp16)."""
+    _want(W, torch.float32, "W")
+    N, K = W.shape
+    Wq8 = torch.empty((N, K), dtype=torch.int8, device=W.device) if Wq8 is None else Wq8
+    sw16 = torch.empty((N,), dtype=torch.float16, device=W.device) if sw16 is None else sw16
+    _want(Wq8, torch.int8, "Wq8", (N, K))
+    _want(sw16, torch.float16, "sw16", (N,))
+    _check(lib().w8_quantize_weights(_ptr(W), N, K, _ptr(Wq8), _ptr(sw16), _stream(W)))
+    return Wq8, sw16
+
+
+def act_quantize_i8(X: torch.Tensor, Xq=None, sa=None):
+    """X [M][K] fp16 -> (Xq [M][K] int8, sa [M] fp32)."""
+    _want(X, torch.float16, "X")
+    M, K = X.shape
+    Xq = torch.empty((M, K), dtype=torch.int8, device=X.device) if Xq is None else Xq
+    sa = torch.empty((M,), dtype=torch.float32, device=X.device) if sa is None else sa
+    _want(Xq, torch.int8, "Xq", (M, K))
+    _want(sa, torch.float32, "sa", (M,))
+    _check(lib().act_quantize_i8(_ptr(X), M, K, _ptr(Xq), _ptr(sa), _stream(X)))
+    return Xq, sa
+
+
+def w4a8_workspace_bytes(M: int, K: int, N: int) -> int:
+    return int(lib().w4a8_workspace_bytes(M, K, N))
+
+
+def w8a16_workspace_bytes(M: int, K: int, N: int) -> int:
+    return int(lib().w8a16_workspace_bytes(M, K, N))
+
+
+def w4a8_gemv(Xq, sa, Wq, sw, Y=None, acc_out=None, ws=None, flags: int = 0):
+    """Y[m][n] = ((float)sum_k Xq[m,k] q[n,k] * sw[n]) * sa[m]; returns Y."""
+    _want(Xq, torch.int8, "Xq")
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    _want(sa, torch.float32, "sa", (M,))
+    _want(Wq, torch.uint8, "Wq", (N, K // 2))
+    _want(sw, torch.float32, "sw", (N,))
+    Y = torch.empty((M, N), dtype=torch.float32, device=Xq.device) if Y is None else Y
+    _want(Y, torch.float32, "Y", (M, N))
+    if acc_out is not None:
+        _want(acc_out, torch.int32, "acc_out", (M, N))
+    nbytes = w4a8_workspace_bytes(M, K, N)
+    ws = _workspace(nbytes, Xq.device, ws)
+    _check(lib().w4a8_gemv(_ptr(Xq), _ptr(sa), M, K, _ptr(Wq), _ptr(sw), N, _ptr(Y), _ptr(acc_out),
+                           _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), flags,
+                           _stream(Xq)))
+    return Y
+
+
+def w4a8_linear(X, Wq, sw, Y=None, Xq_out=None, sa_out=None, acc_out=None, ws=None,
+                flags: int = 0):
+    """Fused activation quantization + W4A8 product; returns Y."""
+    _want(X, torch.float16, "X")
+    M, K = X.shape
+    N = Wq.shape[0]
+    _want(Wq, torch.uint8, "Wq", (N, K // 2))
+    _want(sw, torch.float32, "sw", (N,))
+    Y = torch.empty((M, N), dtype=torch.float32, device=X.device) if Y is None else Y
+    _want(Y, torch.float32, "Y", (M, N))
+    if Xq_out is not None:
+        _want(Xq_out, torch.int8, "Xq_out", (M, K))
+    if sa_out is not None:
+        _want(sa_out, torch.float32, "sa_out", (M,))
+    if acc_out is not None:
+        _want(acc_out, torch.int32, "acc_out", (M, N))
+    nbytes = w4a8_workspace_bytes(M, K, N)
+    ws = _workspace(nbytes, X.device, ws)
+    _check(lib().w4a8_linear(_ptr(X), M, K, _ptr(Wq), _ptr(sw), N, _ptr(Y), _ptr(Xq_out),
+                             _ptr(sa_out), _ptr(acc_out), _ptr(ws),
+                             0 if ws is None else ws.numel() * ws.element_size(), flags,
+                             _stream(X)))
+    return Y
+
+
+def w8a16_gemv(X, Wq8, sw16, Y=None, ws=None, flags: int = 0):
+    """Y[m][n] = float(sw16[n]) * sum_k q[n,k] * x[m,k]; returns Y."""
+    _want(X, torch.float16, "X")
+    M, K = X.shape
+    N = Wq8.shape[0]
+    _want(Wq8, torch.int8, "Wq8", (N, K))
+    _want(sw16, torch.float16, "sw16", (N,))
+    Y = torch.empty((M, N), dtype=torch.float32, device=X.device) if Y is None else Y
+    _want(Y, torch.float32, "Y", (M, N))
+    nbytes = w8a16_workspace_bytes(M, K, N)
+    ws = _workspace(nbytes, X.device, ws)
+    _check(lib().w8a16_gemv(_ptr(X), M, K, _ptr(Wq8), _ptr(sw16), N, _ptr(Y), _ptr(ws),
+                            0 if ws is None else ws.numel() * ws.element_size(), flags,
+                            _stream(X)))
+    return Y
+
+
+def w4a8_last_error() -> str:
+    return lib().w4a8_last_error().decode(errors="replace")
+
+
+def w4a8_device_error(device=None) -> int:
+    """Reads and clears the device error word (synchronises the current stream)."""
+    flags = ctypes.c_uint(0)
+    stream = torch.cuda.current_stream(device).cuda_stream
+    _check(lib().w4a8_device_error(ctypes.byref(flags), stream))
+    return int(flags.value)
+
+
+def w4a8_set_tuning(force_splits: int = 0, force_threads_per_row: int = 0,
+                    ring_bytes: int = 0, ctas_per_sm: int = 0, reset: bool = False):
+    if reset:
+        _check(lib().w4a8_set_tuning(None))
+        return
+    t = _Tuning(force_splits, force_threads_per_row, ring_bytes, ctas_per_sm)
+    _check(lib().w4a8_set_tuning(ctypes.byref(t)))
+
+
+PLAN_FIELDS = ("splits", "threads_per_row", "cols_per_thread", "rows_per_stage", "ctas_per_split",
+               "grid", "rows_per_cta", "stages", "stage_bytes", "smem_bytes", "ws_bytes")
+
+
+def w4a8_plan_info(M: int, K: int, N: int, w8a16: bool = False, num_sms: int = 0) -> dict:
+    """Launch plan for a shape; num_sms > 0 plans without a GPU."""
+    arr = (ctypes.c_int * len(PLAN_FIELDS))()
+    _check(lib().w4a8_plan_info(M, K, N, int(w8a16), num_sms, arr, len(PLAN_FIELDS)))
+    return dict(zip(PLAN_FIELDS, list(arr)))

@@ -1,0 +1,259 @@
+// abi.cu -- the extern "C" entry points declared in include/w4a8.h:
+// argument checks on the host, plan selection, launches on the caller's
+// stream.  Nothing here allocates or synchronises (except
+// w4a8_device_error, which is documented to synchronise).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdint>
+#include <string>
+
+#include "../../include/w4a8.h"
+#include "kernels.h"
+#include "plan.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int ok() {
+    g_last_error.clear();
+    return W4A8_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(W4A8_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Process-wide tuning knobs (w4a8_set_tuning); read at plan time.
+std::atomic<int> g_force_splits{0};
+std::atomic<int> g_force_cl{0};
+std::atomic<int> g_ring_bytes{0};
+std::atomic<int> g_ctas_per_sm{0};
+
+int sm_count(int* out) {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) {
+            *out = c;
+            return W4A8_OK;
+        }
+    }
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    *out = n;
+    return W4A8_OK;
+}
+
+w4a8::Tuning tuning() {
+    w4a8::Tuning t;
+    t.force_splits = g_force_splits.load();
+    t.force_cl = g_force_cl.load();
+    t.ring_bytes = g_ring_bytes.load();
+    t.ctas_per_sm = g_ctas_per_sm.load();
+    return t;
+}
+
+int plan_for(bool w4, bool fused, int64_t M, int64_t K, int64_t N, w4a8::GemvPlan* pl,
+             int sms = 0) {
+    if (sms <= 0) {
+        int st = sm_count(&sms);
+        if (st != W4A8_OK) return st;
+    }
+    if (!w4a8::make_gemv_plan(w4, fused, (int)M, K, N, sms, tuning(), pl))
+        return fail(W4A8_ERR_SHAPE, "no launch plan for M=%lld K=%lld N=%lld",
+                    (long long)M, (long long)K, (long long)N);
+    return W4A8_OK;
+}
+
+int check_w4a8_shape(int64_t M, int64_t K, int64_t N) {
+    if (M < 1 || M > W4A8_MAX_M) return fail(W4A8_ERR_SHAPE, "M=%lld outside [1, %d]", (long long)M, W4A8_MAX_M);
+    if (K < 32 || K > 131072 || K % 32) return fail(W4A8_ERR_SHAPE, "K=%lld must be a multiple of 32 in [32, 131072]", (long long)K);
+    if (N < 1 || N > 0x7FFFFFFF) return fail(W4A8_ERR_SHAPE, "N=%lld outside [1, 2^31-1]", (long long)N);
+    return W4A8_OK;
+}
+
+int check_w8a16_shape(int64_t M, int64_t K, int64_t N) {
+    if (M < 1 || M > W8A16_MAX_M) return fail(W4A8_ERR_SHAPE, "M=%lld outside [1, %d]", (long long)M, W8A16_MAX_M);
+    if (K < 16 || K > 65536 || K % 16) return fail(W4A8_ERR_SHAPE, "K=%lld must be a multiple of 16 in [16, 65536]", (long long)K);
+    if (N < 1 || N > 0x7FFFFFFF) return fail(W4A8_ERR_SHAPE, "N=%lld outside [1, 2^31-1]", (long long)N);
+    return W4A8_OK;
+}
+
+int check_workspace(const w4a8::GemvPlan& pl, void* ws, size_t ws_bytes) {
+    if (pl.ws_bytes == 0) return W4A8_OK;
+    if (ws == nullptr || ws_bytes < pl.ws_bytes)
+        return fail(W4A8_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given%s", pl.ws_bytes,
+                    ws ? ws_bytes : (size_t)0, ws ? "" : " (NULL)");
+    if (!aligned(ws, 256)) return fail(W4A8_ERR_ALIGN, "workspace must be 256-byte aligned");
+    return W4A8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int w4_quantize_weights(const float* W, int64_t N, int64_t K, uint8_t* Wq, float* sw, void* stream) {
+    if (!W || !Wq || !sw) return fail(W4A8_ERR_NULL, "w4_quantize_weights: NULL pointer");
+    if (N < 1 || N > 0x7FFFFFFF) return fail(W4A8_ERR_SHAPE, "N=%lld outside [1, 2^31-1]", (long long)N);
+    if (K < 32 || K % 32 || K > (1LL << 30)) return fail(W4A8_ERR_SHAPE, "K=%lld must be a positive multiple of 32", (long long)K);
+    if (!aligned(W, 16) || !aligned(Wq, 16) || !aligned(sw, 4))
+        return fail(W4A8_ERR_ALIGN, "w4_quantize_weights: W and Wq must be 16-byte aligned");
+    cudaError_t e = w4a8::launch_w4_quantize(W, N, K, Wq, sw, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w4_quantize_weights launch");
+}
+
+int w8_quantize_weights(const float* W, int64_t N, int64_t K, int8_t* Wq8, uint16_t* sw16,
+                        void* stream) {
+    if (!W || !Wq8 || !sw16) return fail(W4A8_ERR_NULL, "w8_quantize_weights: NULL pointer");
+    if (N < 1 || N > 0x7FFFFFFF) return fail(W4A8_ERR_SHAPE, "N=%lld outside [1, 2^31-1]", (long long)N);
+    if (K < 16 || K % 16 || K > (1LL << 30)) return fail(W4A8_ERR_SHAPE, "K=%lld must be a positive multiple of 16", (long long)K);
+    if (!aligned(W, 16) || !aligned(Wq8, 16) || !aligned(sw16, 2))
+        return fail(W4A8_ERR_ALIGN, "w8_quantize_weights: W and Wq8 must be 16-byte aligned");
+    cudaError_t e = w4a8::launch_w8_quantize(W, N, K, Wq8, sw16, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w8_quantize_weights launch");
+}
+
+int act_quantize_i8(const uint16_t* X, int64_t M, int64_t K, int8_t* Xq, float* sa, void* stream) {
+    if (!X || !Xq || !sa) return fail(W4A8_ERR_NULL, "act_quantize_i8: NULL pointer");
+    if (M < 1 || M > 65535) return fail(W4A8_ERR_SHAPE, "M=%lld outside [1, 65535]", (long long)M);
+    if (K < 1 || K > (1LL << 20) || K % 8) return fail(W4A8_ERR_SHAPE, "K=%lld must be a multiple of 8 in [8, 2^20]", (long long)K);
+    if (!aligned(X, 16) || !aligned(Xq, 16) || !aligned(sa, 4))
+        return fail(W4A8_ERR_ALIGN, "act_quantize_i8: X and Xq must be 16-byte aligned");
+    cudaError_t e = w4a8::launch_act_quantize(X, M, K, Xq, sa, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "act_quantize_i8 launch");
+}
+
+size_t w4a8_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+    if (check_w4a8_shape(M, K, N) != W4A8_OK) return 0;
+    w4a8::GemvPlan pl;
+    // the fused and unfused kernels share the split plan
+    if (plan_for(true, true, M, K, N, &pl) != W4A8_OK) return 0;
+    return pl.ws_bytes;
+}
+
+size_t w8a16_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+    if (check_w8a16_shape(M, K, N) != W4A8_OK) return 0;
+    w4a8::GemvPlan pl;
+    if (plan_for(false, false, M, K, N, &pl) != W4A8_OK) return 0;
+    return pl.ws_bytes;
+}
+
+int w4a8_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, const uint8_t* Wq,
+              const float* sw, int64_t N, float* Y, int32_t* acc_out, void* ws, size_t ws_bytes,
+              unsigned flags, void* stream) {
+    if (!Xq || !sa || !Wq || !sw || !Y) return fail(W4A8_ERR_NULL, "w4a8_gemv: NULL pointer");
+    int st = check_w4a8_shape(M, K, N);
+    if (st != W4A8_OK) return st;
+    if (!aligned(Xq, 16) || !aligned(Wq, 16) || !aligned(Y, 4) || !aligned(sw, 4) ||
+        !aligned(sa, 4) || (acc_out && !aligned(acc_out, 4)))
+        return fail(W4A8_ERR_ALIGN, "w4a8_gemv: Xq/Wq need 16-byte, Y/sw/sa/acc_out 4-byte alignment");
+    w4a8::GemvPlan pl;
+    if ((st = plan_for(true, true, M, K, N, &pl)) != W4A8_OK) return st;
+    if ((st = check_workspace(pl, ws, ws_bytes)) != W4A8_OK) return st;
+    cudaError_t e = w4a8::launch_w4a8(pl, false, nullptr, Xq, sa, (int)M, K, Wq, sw, N, Y, acc_out,
+                                      nullptr, nullptr, ws, flags, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_gemv launch");
+}
+
+int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const float* sw,
+                int64_t N, float* Y, int8_t* Xq_out, float* sa_out, int32_t* acc_out, void* ws,
+                size_t ws_bytes, unsigned flags, void* stream) {
+    if (!X || !Wq || !sw || !Y) return fail(W4A8_ERR_NULL, "w4a8_linear: NULL pointer");
+    int st = check_w4a8_shape(M, K, N);
+    if (st != W4A8_OK) return st;
+    if (!aligned(X, 16) || !aligned(Wq, 16) || !aligned(Y, 4) || !aligned(sw, 4) ||
+        (Xq_out && !aligned(Xq_out, 16)) || (sa_out && !aligned(sa_out, 4)) ||
+        (acc_out && !aligned(acc_out, 4)))
+        return fail(W4A8_ERR_ALIGN, "w4a8_linear: X/Wq/Xq_out need 16-byte, Y/sw/sa_out/acc_out 4-byte alignment");
+    w4a8::GemvPlan pl;
+    if ((st = plan_for(true, true, M, K, N, &pl)) != W4A8_OK) return st;
+    if ((st = check_workspace(pl, ws, ws_bytes)) != W4A8_OK) return st;
+    cudaError_t e = w4a8::launch_w4a8(pl, true, X, nullptr, nullptr, (int)M, K, Wq, sw, N, Y,
+                                      acc_out, Xq_out, sa_out, ws, flags,
+                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear launch");
+}
+
+int w8a16_gemv(const uint16_t* X, int64_t M, int64_t K, const int8_t* Wq8, const uint16_t* sw16,
+               int64_t N, float* Y, void* ws, size_t ws_bytes, unsigned flags, void* stream) {
+    if (!X || !Wq8 || !sw16 || !Y) return fail(W4A8_ERR_NULL, "w8a16_gemv: NULL pointer");
+    int st = check_w8a16_shape(M, K, N);
+    if (st != W4A8_OK) return st;
+    if (!aligned(X, 16) || !aligned(Wq8, 16) || !aligned(Y, 4) || !aligned(sw16, 2))
+        return fail(W4A8_ERR_ALIGN, "w8a16_gemv: X/Wq8 need 16-byte, Y 4-byte alignment");
+    w4a8::GemvPlan pl;
+    if ((st = plan_for(false, false, M, K, N, &pl)) != W4A8_OK) return st;
+    if ((st = check_workspace(pl, ws, ws_bytes)) != W4A8_OK) return st;
+    cudaError_t e = w4a8::launch_w8a16(pl, X, (int)M, K, Wq8, sw16, N, Y, ws, flags,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w8a16_gemv launch");
+}
+
+const char* w4a8_last_error(void) { return g_last_error.c_str(); }
+
+int w4a8_device_error(unsigned* flags, void* stream) {
+    if (!flags) return fail(W4A8_ERR_NULL, "w4a8_device_error: NULL pointer");
+    cudaError_t e = w4a8::read_and_clear_device_error(flags, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_device_error");
+}
+
+int w4a8_set_tuning(const w4a8_tuning_t* t) {
+    if (t == nullptr) {
+        g_force_splits = 0;
+        g_force_cl = 0;
+        g_ring_bytes = 0;
+        g_ctas_per_sm = 0;
+        return ok();
+    }
+    if (t->force_splits < 0 || t->force_splits > 16)
+        return fail(W4A8_ERR_SHAPE, "force_splits must be in [0, 16]");
+    if (t->force_threads_per_row < 0 || t->force_threads_per_row > 256 ||
+        (t->force_threads_per_row & (t->force_threads_per_row - 1)))
+        return fail(W4A8_ERR_SHAPE, "force_threads_per_row must be 0 or a power of two <= 256");
+    if (t->ring_bytes < 0 || t->ring_bytes > 200 * 1024)
+        return fail(W4A8_ERR_SHAPE, "ring_bytes must be in [0, 204800]");
+    if (t->ctas_per_sm < 0 || t->ctas_per_sm > 4)
+        return fail(W4A8_ERR_SHAPE, "ctas_per_sm must be in [0, 4]");
+    g_force_splits = t->force_splits;
+    g_force_cl = t->force_threads_per_row;
+    g_ring_bytes = t->ring_bytes;
+    g_ctas_per_sm = t->ctas_per_sm;
+    return ok();
+}
+
+int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int* info,
+                   int n_info) {
+    if (!info) return fail(W4A8_ERR_NULL, "w4a8_plan_info: NULL pointer");
+    int st = w8a16 ? check_w8a16_shape(M, K, N) : check_w4a8_shape(M, K, N);
+    if (st != W4A8_OK) return st;
+    w4a8::GemvPlan pl;
+    if ((st = plan_for(!w8a16, !w8a16, M, K, N, &pl, num_sms)) != W4A8_OK) return st;
+    const int ws = pl.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)pl.ws_bytes;
+    const int v[] = {pl.P, pl.Cl, pl.S, pl.Rl, pl.Gs, pl.grid, pl.rows_max, pl.NS,
+                     pl.stage_stride, pl.smem, ws};
+    for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,651 @@
+// gemv.cu -- streaming weight-quantized GEMV kernels for sm_103a.
+//
+// W4A8 (the Jetson INT4 page, sections 正确方向 / 当前实现方式): INT4 codes
+// are widened to int8 lanes in registers and multiplied against INT8
+// activation codes with __dp4a into int32; y = ((float)acc * s_w) * s_a.
+// W8A16 (the TPU-MLIR W8A16 page, section 4): INT8 codes are widened to
+// fp32 exactly in registers and multiplied with the F16 activation; the
+// per-channel scale multiplies the fp32 sum once.
+//
+// Both are HBM-bound at decode batch sizes, so the kernel is built around
+// the weight stream (the W8A16 page's load/compute overlap, done with the
+// TMA unit and an mbarrier ring instead of GDMA/BDC ping-pong):
+//  * one producer warp issues 1-D bulk copies (cp.async.bulk, L2
+//    evict-first) of whole rows, or of row-pieces when K is split, into an
+//    NS-stage shared-memory ring; `full`/`empty` mbarriers hand stages over;
+//  * 8 consumer warps: thread j of a row-piece owns granule columns
+//    j, j+Cl, ...; its activation operands are loaded once into registers,
+//    so shared memory traffic per weight byte is one write (TMA) + one read;
+//  * int32 partial sums are shifted right by 4 (the nibble trick below
+//    yields 16 * product) and reduced with warp shuffles, across warps in
+//    shared memory when a row-piece spans several warps;
+//  * split-K: int32 (or fp32) partials go to the workspace; the last CTA of
+//    a row block (atomic ticket) sums them in a fixed order and rescales
+//    once, so W4A8 stays bit-exact and W8A16 deterministic;
+//  * programmatic dependent launch: weights are streamed before the wait
+//    on the previous kernel; activations, outputs and workspace after it.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <type_traits>
+
+#include "kernels.h"
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace w4a8 {
+
+__device__ unsigned g_device_error;
+
+struct GemvArgs {
+    const uint8_t* W;       // W4: [N][K/2] packed nibbles; W8: [N][K] int8
+    const void* wscale;     // W4: float[N]; W8: binary16[N]
+    const int8_t* Xq;       // W4 unfused: [M][K] int8 codes
+    const float* sa;        // W4 unfused: [M] activation scales
+    const __half* X;        // W4 fused and W8: [M][K] binary16 activation
+    float* Y;               // [M][N]
+    int32_t* acc_out;       // optional [M][N] (W4)
+    int8_t* Xq_out;         // optional [M][K] (W4 fused)
+    float* sa_out;          // optional [M] (W4 fused)
+    void* part;             // split partials [P][M][N] (int32 or fp32)
+    unsigned* tickets;      // [Gs] arrival counters at the workspace start,
+                            // zero between calls
+    int M;
+    int K;
+    int N;
+    GemvPlan pl;
+};
+
+// Waits on an mbarrier phase unless the CTA has already given up.  On a
+// timeout it records `bit` in the device error word and tells the other
+// threads (through `abort_flag`) to stop waiting; the caller carries on
+// without valid data so every thread still meets every named barrier.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, unsigned bit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        #pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(&g_device_error, bit);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+    #pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// max |x| over 8 binary16 values, as binary16 pairs (comparisons are exact).
+__device__ __forceinline__ __half2 absmax8(uint4 h, __half2 m) {
+    const __half2* p = reinterpret_cast<const __half2*>(&h);
+    #pragma unroll
+    for (int t = 0; t < 4; ++t) m = __hmax2(m, __habs2(p[t]));
+    return m;
+}
+
+// INT8 code of one activation value, clamp(round_half_away(x / s), +-127)
+// with the IEEE quotient x / s, given r = rcp_rn(s) and s > 0.
+// t = x * r differs from x / s by at most |x/s| * 2^-23 (two roundings) and
+// the IEEE quotient differs from x / s by at most |x/s| * 2^-24, so for
+// |x/s| <= 129 the two lie within 2^-15 of each other.  When t is more than
+// 2^-14 away from every half-integer, both therefore have the same nearest
+// integer and neither is a tie: rint(t) is the answer.  The rare remaining
+// cases take the IEEE division.
+__device__ __forceinline__ uint32_t quant_i8(float x, float s, float r) {
+    const float t = __fmul_rn(x, r);
+    const float ti = rintf(t);
+    float q = ti;
+    if (!(fabsf(t - ti) < 0.5f - 0x1p-14f)) q = roundf(__fdiv_rn(x, s));
+    q = fminf(fmaxf(q, -127.f), 127.f);
+    return static_cast<uint32_t>(static_cast<int>(q)) & 0xFFu;
+}
+
+__device__ __forceinline__ uint2 quant8(uint4 h, float s, float r) {
+    if (s == 0.f) return make_uint2(0u, 0u);
+    const __half2* p = reinterpret_cast<const __half2*>(&h);
+    uint32_t b[8];
+    #pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const float2 f = __half22float2(p[t]);
+        b[2 * t] = quant_i8(f.x, s, r);
+        b[2 * t + 1] = quant_i8(f.y, s, r);
+    }
+    return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
+                      b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+}
+
+// 32 activation codes in natural order (two 16-byte words) -> the lane order
+// of the packed weights: word t of a granule holds codes 8t..8t+7 with even
+// k in the low nibbles and odd k in the high nibbles, so the even codes
+// go to act[t] and the odd codes to act[4 + t].
+__device__ __forceinline__ void permute_act(uint4 lo, uint4 hi, uint32_t* act) {
+    const uint32_t n[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    #pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        act[t] = __byte_perm(n[2 * t], n[2 * t + 1], 0x6420);
+        act[4 + t] = __byte_perm(n[2 * t], n[2 * t + 1], 0x7531);
+    }
+}
+
+template <bool kW4, int MT, int SMAX, bool kFused>
+__global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
+    using AccT = typename std::conditional<kW4, int, float>::type;
+    constexpr int kActWords = kW4 ? 8 : 16;  // registers per granule per activation row
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const GemvPlan& pl = a.pl;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int p = blockIdx.x % pl.P;
+    const int rb = blockIdx.x / pl.P;
+    const int64_t N = a.N;
+    const int64_t row0 = (int64_t)rb * N / pl.Gs;
+    const int nrows = (int)((int64_t)(rb + 1) * N / pl.Gs - row0);
+    const int nstages = (nrows + pl.Rl - 1) / pl.Rl;
+    const int NS = pl.NS;
+    const int g0 = p * pl.Gq;                   // first granule of this piece
+    const int gp = min(pl.Gq, pl.Gt - g0);      // granules in this piece
+    const int RBp = gp * kGranBytes;            // bytes of one row-piece
+    const int64_t RB = (int64_t)pl.Gt * kGranBytes;
+
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.off_bars);
+    uint64_t* empty = full + NS;
+    uint64_t* sw_bar = empty + NS;              // scale cache filled
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pl.off_flag);
+    int* last_flag = reinterpret_cast<int*>(smem + pl.off_flag + 4);
+    float* sw_s = reinterpret_cast<float*>(smem + pl.off_sw);
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(smem_u32(full + s), 1);
+            mbar_init(smem_u32(empty + s), kConsumerWarps);
+        }
+        mbar_init(smem_u32(sw_bar), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+
+    // ------------------------------------------------------------ producer
+    if (warp == kConsumerWarps) {
+        const uint64_t pol = l2_evict_first_policy();
+        const uint8_t* base = a.W + row0 * RB + (int64_t)g0 * kGranBytes;
+        auto issue = [&](int st, int slot) {
+            const int r0 = st * pl.Rl;
+            const int nr = min(pl.Rl, nrows - r0);
+            const uint32_t dst = smem_u32(smem + slot * pl.stage_stride);
+            const uint32_t bar = smem_u32(full + slot);
+            mbar_arrive_expect_tx(bar, (uint32_t)(nr * RBp));
+            const uint8_t* src = base + (int64_t)r0 * RB;
+            if (pl.P == 1) {
+                bulk_g2s(dst, src, (uint32_t)(nr * RBp), bar, pol);
+            } else {
+                for (int r = 0; r < nr; ++r)
+                    bulk_g2s(dst + r * RBp, src + (int64_t)r * RB, (uint32_t)RBp, bar, pol);
+            }
+        };
+        // Fill the ring first (weights may be read before the dependency wait).
+        const int first = min(NS, nstages);
+        if (lane == 0)
+            for (int st = 0; st < first; ++st) issue(st, st);
+        // The idle lanes meanwhile cache the weight scales of this CTA's rows.
+        if (pl.P == 1) {
+            for (int r = lane; r < nrows; r += 32) {
+                if constexpr (kW4)
+                    sw_s[r] = static_cast<const float*>(a.wscale)[row0 + r];
+                else
+                    sw_s[r] = __half2float(static_cast<const __half*>(a.wscale)[row0 + r]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(smem_u32(sw_bar));
+            int st = first, slot = 0;
+            uint32_t eph = 0;  // parity of the empty phase being waited for
+            for (; st < nstages; ++st) {
+                if (!wait_or_abort(smem_u32(empty + slot), eph, abort_flag, kErrEmptyWait)) break;
+                issue(st, slot);
+                if (++slot == NS) { slot = 0; eph ^= 1u; }
+            }
+            // No copy may still be landing in shared memory when the CTA exits.
+            for (int s2 = (st > NS ? st - NS : 0); s2 < st; ++s2)
+                if (!mbar_wait(smem_u32(full + s2 % NS), (s2 / NS) & 1))
+                    atomicOr(&g_device_error, kErrDrainWait);
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers
+    const int Cl = pl.Cl;
+    const int i = tid >> pl.log2Cl;   // row-piece within a stage
+    const int j = tid & (Cl - 1);     // column slot within the row-piece
+    const int M = a.M;
+    const int64_t K = a.K;
+    // granule columns j, j+Cl, ... below gp belong to this thread
+    const int ncol = j < gp ? min(pl.S, (gp - j + Cl - 1) >> pl.log2Cl) : 0;
+
+    griddep_wait();  // activations, outputs and workspace from here on
+
+    uint32_t act[MT][SMAX][kActWords];
+    float sa_r[MT];
+
+    if constexpr (kW4 && kFused) {
+        // Dynamic activation quantization fused into the linear (the Jetson
+        // INT4 page, section 后续优化方向).  Every CTA derives the same s_a
+        // from the whole row, then quantizes only its own K piece.
+        float* max_s = reinterpret_cast<float*>(smem + pl.off_max);
+        uint8_t* act_s = smem + pl.off_act;
+        const int act_stride = pl.Gq * 32;
+        const int64_t k0 = (int64_t)g0 * 32;
+        const int kq = gp * 32;
+        const int nv = (int)(K / 8);          // 16-byte vectors per activation row
+        // One-pass form: the thread's vectors of a single row stay in registers.
+        constexpr int XR = 10;
+        const bool one_pass = (MT == 1) && pl.P == 1 && nv <= XR * kConsumers;
+        uint4 xr[MT == 1 ? XR : 1];
+        #pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            __half2 hm = __float2half2_rn(0.f);
+            if (m < M) {
+                const uint4* xv = reinterpret_cast<const uint4*>(a.X + (int64_t)m * K);
+                if (MT == 1 && one_pass) {
+                    #pragma unroll
+                    for (int u = 0; u < (MT == 1 ? XR : 1); ++u) {
+                        const int v = tid + u * kConsumers;
+                        if (v < nv) {
+                            xr[u] = xv[v];
+                            hm = absmax8(xr[u], hm);
+                        }
+                    }
+                } else {
+                    for (int v = tid; v < nv; v += kConsumers) hm = absmax8(xv[v], hm);
+                }
+            }
+            float mx = fmaxf(__low2float(hm), __high2float(hm));
+            mx = warp_max(mx);
+            if (lane == 0) max_s[warp * MT + m] = mx;
+        }
+        named_bar_sync(1, kConsumers);
+        float rs[MT];
+        #pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            float mx = 0.f;
+            #pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) mx = fmaxf(mx, max_s[w * MT + m]);
+            sa_r[m] = __fdiv_rn(mx, 127.f);
+            rs[m] = sa_r[m] > 0.f ? __frcp_rn(sa_r[m]) : 0.f;
+        }
+        #pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                if (MT == 1 && one_pass) {
+                    #pragma unroll
+                    for (int u = 0; u < (MT == 1 ? XR : 1); ++u) {
+                        const int v = tid + u * kConsumers;
+                        if (v < nv)
+                            *reinterpret_cast<uint2*>(act_s + 8 * v) = quant8(xr[u], sa_r[0], rs[0]);
+                    }
+                } else {
+                    const uint4* xv = reinterpret_cast<const uint4*>(a.X + (int64_t)m * K + k0);
+                    for (int v = tid; v < kq / 8; v += kConsumers)
+                        *reinterpret_cast<uint2*>(act_s + m * act_stride + 8 * v) =
+                            quant8(xv[v], sa_r[m], rs[m]);
+                }
+            }
+        }
+        named_bar_sync(1, kConsumers);
+        if (a.Xq_out != nullptr && rb == 0) {
+            for (int m = 0; m < M; ++m)
+                for (int v = tid; v < kq / 16; v += kConsumers)
+                    *reinterpret_cast<uint4*>(a.Xq_out + (int64_t)m * K + k0 + 16 * v) =
+                        *reinterpret_cast<const uint4*>(act_s + m * act_stride + 16 * v);
+        }
+        if (a.sa_out != nullptr && blockIdx.x == 0) {
+            #pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (tid == m && m < M) a.sa_out[m] = sa_r[m];
+        }
+        #pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            #pragma unroll
+            for (int s = 0; s < SMAX; ++s) {
+                const int c = j + s * Cl;
+                if (m < M && s < ncol) {
+                    const uint4* src = reinterpret_cast<const uint4*>(act_s + m * act_stride + 32 * c);
+                    permute_act(src[0], src[1], act[m][s]);
+                } else {
+                    #pragma unroll
+                    for (int t = 0; t < kActWords; ++t) act[m][s][t] = 0u;
+                }
+            }
+        }
+    } else {
+        #pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if constexpr (kW4) sa_r[m] = (m < M) ? a.sa[m] : 0.f;
+            #pragma unroll
+            for (int s = 0; s < SMAX; ++s) {
+                const int c = j + s * Cl;
+                if (m < M && s < ncol) {
+                    if constexpr (kW4) {
+                        const int8_t* src = a.Xq + (int64_t)m * K + (int64_t)(g0 + c) * 32;
+                        permute_act(ld_global_nc_v4(src), ld_global_nc_v4(src + 16), act[m][s]);
+                    } else {
+                        const __half* src = a.X + (int64_t)m * K + (int64_t)(g0 + c) * 16;
+                        const uint4 h0 = ld_global_nc_v4(src);
+                        const uint4 h1 = ld_global_nc_v4(src + 8);
+                        const __half2* hp0 = reinterpret_cast<const __half2*>(&h0);
+                        const __half2* hp1 = reinterpret_cast<const __half2*>(&h1);
+                        #pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float2 f0 = __half22float2(hp0[t]);
+                            const float2 f1 = __half22float2(hp1[t]);
+                            act[m][s][2 * t] = __float_as_uint(f0.x);
+                            act[m][s][2 * t + 1] = __float_as_uint(f0.y);
+                            act[m][s][8 + 2 * t] = __float_as_uint(f1.x);
+                            act[m][s][8 + 2 * t + 1] = __float_as_uint(f1.y);
+                        }
+                    }
+                } else {
+                    #pragma unroll
+                    for (int t = 0; t < kActWords; ++t) act[m][s][t] = 0u;
+                }
+            }
+        }
+    }
+
+    // W4: the low nibbles enter the dot product biased by +8 (n ^ 8 = q + 8),
+    // so each row's sum carries 8 * (sum of the even-k codes) too much.
+    int corr[MT];
+    #pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        corr[m] = 0;
+        if constexpr (kW4) {
+            #pragma unroll
+            for (int s = 0; s < SMAX; ++s)
+                #pragma unroll
+                for (int t = 0; t < 4; ++t) corr[m] = __dp4a((int)act[m][s][t], 0x08080808, corr[m]);
+        }
+    }
+
+    // ------------------------------------------------------ streaming loop
+    AccT* red = reinterpret_cast<AccT*>(smem + pl.off_red);  // [2][warps][MT]
+    const int wpr = Cl >> 5;                                  // warps per row-piece
+    const uint32_t ring0 = smem_u32(smem);
+    const uint32_t col0 = (uint32_t)(i * RBp + j * kGranBytes);
+    const uint32_t cstep = (uint32_t)(Cl * kGranBytes);
+    bool sw_ready = pl.P != 1;
+    int slot = 0;
+    uint32_t fph = 0;  // parity of the full phase being waited for
+    for (int st = 0; st < nstages; ++st) {
+        wait_or_abort(smem_u32(full + slot), fph, abort_flag, kErrFullWait);
+        const int r0 = st * pl.Rl;
+        const int nr = min(pl.Rl, nrows - r0);
+        // independent accumulator chains: W4 keeps the biased low-nibble and
+        // the x16 high-nibble sums apart; NCH chains of each
+        constexpr int NCH = MT == 1 ? 2 : 1;
+        AccT alo[MT][NCH], ahi[MT][NCH];
+        #pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            #pragma unroll
+            for (int h = 0; h < NCH; ++h) { alo[m][h] = 0; ahi[m][h] = 0; }
+        }
+        if (i < nr) {
+            const uint32_t wbase = ring0 + (uint32_t)(slot * pl.stage_stride) + col0;
+            #pragma unroll
+            for (int s = 0; s < SMAX; ++s) {
+                if (s < ncol) {
+                    const uint4 w4v = *reinterpret_cast<const uint4*>(
+                        smem + (wbase - ring0) + s * cstep);
+                    const uint32_t wv[4] = {w4v.x, w4v.y, w4v.z, w4v.w};
+                    #pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        if constexpr (kW4) {
+                            // low nibbles: (n ^ 8) = q + 8 in [0, 15]; high
+                            // nibbles left in place read as int8 = 16 * q
+                            const uint32_t lo = (wv[t] ^ 0x08080808u) & 0x0F0F0F0Fu;
+                            const uint32_t hi = wv[t] & 0xF0F0F0F0u;
+                            #pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                AccT& cl = alo[m][t % NCH];
+                                AccT& ch = ahi[m][t % NCH];
+                                cl = __dp4a((int)lo, (int)act[m][s][t], cl);
+                                ch = __dp4a((int)hi, (int)act[m][s][4 + t], ch);
+                            }
+                        } else {
+                            // int8 code q -> fp32 exactly: the bits 0x4B0000uu
+                            // with uu = q + 128 encode 2^23 + q + 128.
+                            const uint32_t u = wv[t] ^ 0x80808080u;
+                            const float q0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)) - 8388736.f;
+                            const float q1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)) - 8388736.f;
+                            const float q2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)) - 8388736.f;
+                            const float q3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - 8388736.f;
+                            #pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                AccT& c0 = alo[m][t % NCH];
+                                AccT& c1 = ahi[m][t % NCH];
+                                c0 = fmaf(q0, __uint_as_float(act[m][s][4 * t + 0]), c0);
+                                c1 = fmaf(q1, __uint_as_float(act[m][s][4 * t + 1]), c1);
+                                c0 = fmaf(q2, __uint_as_float(act[m][s][4 * t + 2]), c0);
+                                c1 = fmaf(q3, __uint_as_float(act[m][s][4 * t + 3]), c1);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(empty + slot));  // stage consumed
+        if (++slot == NS) { slot = 0; fph ^= 1u; }
+
+        AccT acc[MT];
+        #pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if constexpr (kW4) {
+                int lo_sum = 0, hi_sum = 0;
+                #pragma unroll
+                for (int h = 0; h < NCH; ++h) { lo_sum += alo[m][h]; hi_sum += ahi[m][h]; }
+                acc[m] = lo_sum - corr[m] + (hi_sum >> 4);  // exact: hi_sum = 16 * sum
+            } else {
+                float sum = 0.f;
+                #pragma unroll
+                for (int h = 0; h < NCH; ++h) sum += alo[m][h] + ahi[m][h];
+                acc[m] = sum;
+            }
+        }
+        #pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            if (o < Cl) {
+                #pragma unroll
+                for (int m = 0; m < MT; ++m) acc[m] += __shfl_xor_sync(0xFFFFFFFFu, acc[m], o);
+            }
+        }
+        if (wpr > 1) {
+            AccT* rbuf = red + (st & 1) * kConsumerWarps * MT;
+            if (lane == 0) {
+                #pragma unroll
+                for (int m = 0; m < MT; ++m) rbuf[warp * MT + m] = acc[m];
+            }
+            named_bar_sync(2, kConsumers);
+            if (j == 0) {
+                #pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    AccT t = rbuf[warp * MT + m];
+                    for (int w = 1; w < wpr; ++w) t += rbuf[(warp + w) * MT + m];
+                    acc[m] = t;
+                }
+            }
+        }
+        if (j == 0 && i < nr) {
+            const int r = r0 + i;
+            const int64_t n = row0 + r;
+            if (pl.P == 1) {
+                if (!sw_ready) {
+                    wait_or_abort(smem_u32(sw_bar), 0, abort_flag, kErrFullWait);
+                    sw_ready = true;
+                }
+                const float swv = sw_s[r];
+                #pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (m < M) {
+                        if constexpr (kW4) {
+                            a.Y[m * N + n] = __fmul_rn(__fmul_rn(__int2float_rn(acc[m]), swv), sa_r[m]);
+                            if (a.acc_out != nullptr) a.acc_out[m * N + n] = acc[m];
+                        } else {
+                            a.Y[m * N + n] = __fmul_rn(acc[m], swv);
+                        }
+                    }
+                }
+            } else {
+                AccT* part = static_cast<AccT*>(a.part);
+                #pragma unroll
+                for (int m = 0; m < MT; ++m)
+                    if (m < M) part[((int64_t)p * M + m) * N + n] = acc[m];
+            }
+        }
+    }
+
+    if (pl.P == 1) return;
+
+    // ---------------------------------------------- split-K: last CTA sums
+    __threadfence();
+    named_bar_sync(1, kConsumers);
+    if (tid == 0) *last_flag = (atomicAdd(a.tickets + rb, 1u) == (unsigned)(pl.P - 1));
+    named_bar_sync(1, kConsumers);
+    if (!*last_flag) return;
+    __threadfence();
+    const AccT* part = static_cast<const AccT*>(a.part);
+    for (int r = tid; r < nrows; r += kConsumers) {
+        const int64_t n = row0 + r;
+        float swv;
+        if constexpr (kW4)
+            swv = static_cast<const float*>(a.wscale)[n];
+        else
+            swv = __half2float(static_cast<const __half*>(a.wscale)[n]);
+        #pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                AccT t = 0;
+                for (int q = 0; q < pl.P; ++q) t += __ldcg(part + ((int64_t)q * M + m) * N + n);
+                if constexpr (kW4) {
+                    a.Y[m * N + n] = __fmul_rn(__fmul_rn(__int2float_rn(t), swv), sa_r[m]);
+                    if (a.acc_out != nullptr) a.acc_out[m * N + n] = t;
+                } else {
+                    a.Y[m * N + n] = __fmul_rn(t, swv);
+                }
+            }
+        }
+    }
+    if (tid == 0) a.tickets[rb] = 0u;  // ready for the next call
+}
+
+// --------------------------------------------------------------- launching
+
+template <bool kW4, int MT, int SMAX, bool kFused>
+static cudaError_t launch_one(const GemvArgs& args, unsigned flags, cudaStream_t stream) {
+    auto* fn = gemv_kernel<kW4, MT, SMAX, kFused>;
+    static int attr_set[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+        if (e != cudaSuccess) return e;
+        // Carve out all of L1 as shared memory so a CTA of the next kernel
+        // (programmatic dependent launch) fits beside the running one.
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(args.pl.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = args.pl.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (flags & 1u) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, fn, args);
+}
+
+cudaError_t launch_w4a8(const GemvPlan& pl, bool fused, const uint16_t* X, const int8_t* Xq,
+                        const float* sa, int M, int64_t K, const uint8_t* Wq, const float* sw,
+                        int64_t N, float* Y, int32_t* acc_out, int8_t* Xq_out, float* sa_out,
+                        void* ws, unsigned flags, cudaStream_t stream) {
+    GemvArgs a = {};
+    a.W = Wq;
+    a.wscale = sw;
+    a.Xq = Xq;
+    a.sa = sa;
+    a.X = reinterpret_cast<const __half*>(X);
+    a.Y = Y;
+    a.acc_out = acc_out;
+    a.Xq_out = Xq_out;
+    a.sa_out = sa_out;
+    a.tickets = static_cast<unsigned*>(ws);
+    a.part = ws ? static_cast<uint8_t*>(ws) + kTicketBytes : nullptr;
+    a.M = M;
+    a.K = (int)K;
+    a.N = (int)N;
+    a.pl = pl;
+    switch (pl.MT * 2 + (fused ? 1 : 0)) {
+        case 2: return launch_one<true, 1, 8, false>(a, flags, stream);
+        case 3: return launch_one<true, 1, 8, true>(a, flags, stream);
+        case 4: return launch_one<true, 2, 4, false>(a, flags, stream);
+        case 5: return launch_one<true, 2, 4, true>(a, flags, stream);
+        case 8: return launch_one<true, 4, 2, false>(a, flags, stream);
+        case 9: return launch_one<true, 4, 2, true>(a, flags, stream);
+        case 16: return launch_one<true, 8, 1, false>(a, flags, stream);
+        case 17: return launch_one<true, 8, 1, true>(a, flags, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_w8a16(const GemvPlan& pl, const uint16_t* X, int M, int64_t K,
+                         const int8_t* Wq8, const uint16_t* sw16, int64_t N, float* Y, void* ws,
+                         unsigned flags, cudaStream_t stream) {
+    GemvArgs a = {};
+    a.W = reinterpret_cast<const uint8_t*>(Wq8);
+    a.wscale = sw16;
+    a.X = reinterpret_cast<const __half*>(X);
+    a.Y = Y;
+    a.tickets = static_cast<unsigned*>(ws);
+    a.part = ws ? static_cast<uint8_t*>(ws) + kTicketBytes : nullptr;
+    a.M = M;
+    a.K = (int)K;
+    a.N = (int)N;
+    a.pl = pl;
+    switch (pl.MT) {
+        case 1: return launch_one<false, 1, 4, false>(a, flags, stream);
+        case 2: return launch_one<false, 2, 2, false>(a, flags, stream);
+        case 4: return launch_one<false, 4, 1, false>(a, flags, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t read_and_clear_device_error(unsigned* flags, cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(flags, g_device_error, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));
+}
+
+}  // namespace w4a8

@@ -1,0 +1,29 @@
+// kernels.h -- host-side launchers of the CUDA kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "plan.h"
+
+namespace w4a8 {
+
+cudaError_t launch_w4_quantize(const float* W, int64_t N, int64_t K, uint8_t* Wq, float* sw,
+                               cudaStream_t stream);
+cudaError_t launch_w8_quantize(const float* W, int64_t N, int64_t K, int8_t* Wq8, uint16_t* sw16,
+                               cudaStream_t stream);
+cudaError_t launch_act_quantize(const uint16_t* X, int64_t M, int64_t K, int8_t* Xq, float* sa,
+                                cudaStream_t stream);
+
+cudaError_t launch_w4a8(const GemvPlan& pl, bool fused, const uint16_t* X, const int8_t* Xq,
+                        const float* sa, int M, int64_t K, const uint8_t* Wq, const float* sw,
+                        int64_t N, float* Y, int32_t* acc_out, int8_t* Xq_out, float* sa_out,
+                        void* ws, unsigned flags, cudaStream_t stream);
+cudaError_t launch_w8a16(const GemvPlan& pl, const uint16_t* X, int M, int64_t K,
+                         const int8_t* Wq8, const uint16_t* sw16, int64_t N, float* Y, void* ws,
+                         unsigned flags, cudaStream_t stream);
+
+cudaError_t read_and_clear_device_error(unsigned* flags, cudaStream_t stream);
+
+}  // namespace w4a8

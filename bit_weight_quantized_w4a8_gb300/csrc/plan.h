@@ -1,0 +1,159 @@
+// plan.h -- launch plan of the streaming GEMV kernels (host and device).
+//
+// A weight row is cut into 16-byte granules (32 INT4 codes, or 16 INT8
+// codes).  The K dimension may be split into P pieces ("split-K"); each CTA
+// streams a contiguous range of rows of one piece through a shared-memory
+// ring.  Inside a stage, `Cl` consumer threads share one row-piece: thread j
+// owns granule columns j, j+Cl, j+2Cl, ... (at most S of them), so the
+// activation values it multiplies never change and stay in registers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace w4a8 {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;  // 256 consumer threads
+constexpr int kThreads = kConsumers + 32;        // + one producer warp
+constexpr int kGranBytes = 16;
+constexpr int kMaxSplits = 16;
+constexpr int kMaxRowsPerCta = 4096;              // bounds the scale cache in smem
+constexpr int kMaxSmem = 232448;                  // 227 KB opt-in limit per CTA
+constexpr int kDefaultRingBytes = 96 * 1024;
+// Split-K workspace layout: arrival counters first, at a fixed place, so any
+// call leaves them zero for the next call whatever its shape; partials after.
+constexpr int kTicketSlots = 1024;
+constexpr size_t kTicketBytes = kTicketSlots * 4;
+
+struct GemvPlan {
+    int MT;            // activation rows rounded up to 1, 2, 4 or 8
+    int smax;          // compile-time bound on granule columns per thread
+    int P;             // K pieces
+    int Gt;            // granules per full weight row
+    int Gq;            // granules per piece (the last piece may have fewer)
+    int Cl, log2Cl;    // threads per row-piece
+    int S;             // granule columns per thread
+    int Rl;            // row-pieces per stage (kConsumers / Cl)
+    int Gs;            // CTAs per piece
+    int grid;          // Gs * P
+    int rows_max;      // most rows any CTA streams
+    int NS;            // ring stages
+    int stage_stride;  // bytes per ring stage (multiple of 128)
+    int off_bars, off_sw, off_act, off_red, off_max, off_flag;
+    int smem;          // dynamic shared memory bytes
+    size_t ws_bytes;   // workspace: kTicketBytes of counters + [P][M][N] x 4
+                       // bytes of partials; 0 when P == 1
+};
+
+struct Tuning {
+    int force_splits;   // 0 = heuristic, else P
+    int force_cl;       // 0 = heuristic, else threads per row-piece
+    int ring_bytes;     // 0 = default ring size
+    int ctas_per_sm;    // 0 = default (1), else CTAs per SM per K piece
+};
+
+inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
+inline size_t round_up_sz(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline int mt_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+
+// Builds the plan; returns false when no valid plan exists for the shape.
+// w4: INT4 weights (32 codes per granule) else INT8 (16 per granule).
+inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int num_sms,
+                           const Tuning& tu, GemvPlan* out) {
+    GemvPlan pl = {};
+    pl.MT = mt_of(M);
+    pl.smax = (w4 ? 8 : 4) / pl.MT;
+    if (pl.smax < 1) return false;
+    const int kgran = w4 ? 32 : 16;
+    if (K % kgran) return false;
+    pl.Gt = (int)(K / kgran);
+    double best_cost = 1e300;
+    bool found = false;
+    for (int P = 1; P <= kMaxSplits; ++P) {
+        if (tu.force_splits && P != tu.force_splits) continue;
+        const int Gq = (pl.Gt + P - 1) / P;
+        if ((P - 1) * Gq >= pl.Gt) continue;  // last piece must be non-empty
+        int bestCl = -1, bestS = 0;
+        double bestU = 0.0;
+        for (int lc = 0; lc <= 8; ++lc) {
+            const int Cl = 1 << lc;
+            if (tu.force_cl && Cl != tu.force_cl) continue;
+            const int S = (Gq + Cl - 1) / Cl;
+            if (S > pl.smax) continue;
+            const double u = (double)Gq / ((double)Cl * S);
+            if (u > bestU + 1e-9) { bestU = u; bestCl = Cl; bestS = S; }
+        }
+        if (bestCl < 0) continue;
+        const int cps = tu.ctas_per_sm > 0 ? tu.ctas_per_sm : 1;
+        int64_t Gs = (int64_t)num_sms * cps / P;
+        if (Gs < 1) Gs = 1;
+        if (Gs > N) Gs = N;
+        if (P > 1 && Gs > kTicketSlots) Gs = kTicketSlots;
+        int64_t rows_max = (N + Gs - 1) / Gs;
+        while (P == 1 && rows_max > kMaxRowsPerCta) {  // keep the scale cache small
+            Gs += (int64_t)num_sms * cps;
+            rows_max = (N + Gs - 1) / Gs;
+        }
+        if (Gs * P > 0x7FFFFFFF) continue;
+        // Streaming cost ~ granules per CTA; low lane utilisation only costs
+        // when the integer pipe becomes the limit (larger M); a split pays a
+        // partial-sum pass and an extra serial step at the end.
+        double cost = (double)rows_max * Gq;
+        const double alu = 0.3 * pl.MT / bestU;
+        if (alu > 1.0) cost *= alu;
+        if (P > 1) cost = cost * 1.05 + 2800.0;
+        if (cost < best_cost) {
+            best_cost = cost;
+            found = true;
+            pl.P = P;
+            pl.Gq = Gq;
+            pl.Cl = bestCl;
+            pl.S = bestS;
+            pl.Gs = (int)Gs;
+            pl.rows_max = (int)rows_max;
+        }
+    }
+    if (!found) return false;
+    pl.log2Cl = 0;
+    while ((1 << pl.log2Cl) < pl.Cl) ++pl.log2Cl;
+    pl.Rl = kConsumers / pl.Cl;
+    pl.grid = pl.Gs * pl.P;
+
+    const int stage_bytes = pl.Rl * pl.Gq * kGranBytes;
+    pl.stage_stride = round_up(stage_bytes, 128);
+    const int ring = tu.ring_bytes > 0 ? tu.ring_bytes : kDefaultRingBytes;
+    int NS = ring / pl.stage_stride;
+    if (NS < 2) NS = 2;
+    if (NS > 16) NS = 16;
+
+    const int sw_bytes = pl.P == 1 ? round_up(pl.rows_max * 4, 16) : 0;
+    const int act_bytes = (w4 && fused) ? round_up(pl.MT * pl.Gq * 32, 128) : 0;
+    const int red_bytes = 2 * kConsumerWarps * pl.MT * 4;
+    const int max_bytes = kConsumerWarps * pl.MT * 4;
+    for (;; --NS) {
+        int off = NS * pl.stage_stride;
+        pl.off_bars = off;
+        off += (2 * NS + 1) * 8;  // full[NS], empty[NS], scale-cache barrier
+        pl.off_sw = round_up(off, 16);
+        off = pl.off_sw + sw_bytes;
+        pl.off_act = round_up(off, 128);
+        off = pl.off_act + act_bytes;
+        pl.off_red = round_up(off, 16);
+        off = pl.off_red + red_bytes;
+        pl.off_max = off;
+        off += max_bytes;
+        pl.off_flag = round_up(off, 16);
+        off = pl.off_flag + 16;
+        pl.smem = round_up(off, 128);
+        if (pl.smem <= kMaxSmem) break;
+        if (NS <= 2) return false;
+    }
+    pl.NS = NS;
+    if (pl.P > 1) pl.ws_bytes = kTicketBytes + round_up_sz((size_t)pl.P * M * N * 4, 256);
+    *out = pl;
+    return true;
+}
+
+}  // namespace w4a8

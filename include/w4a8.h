@@ -1,0 +1,221 @@
+/*
+ * w4a8.h -- C ABI of the GB300 weight-quantized decode linear library.
+ *
+ * The method (pages it follows):
+ *  - "Jetson Orin AGX 上的 INT4 量化推理实践：从 9 tok/s 到 19.6 tok/s",
+ *    sections 当前实现方式 and 正确方向: weights quantized row-wise to INT4
+ *    with one scale per output row; the activation quantized dynamically to
+ *    INT8 before every linear; int8 x int8 products accumulated in int32;
+ *    output = int32 accumulate * weight_scale * activation_scale, as float.
+ *    Section 后续优化方向 lists the fusion of the activation quantization
+ *    into the linear kernel (w4a8_linear below).
+ *  - "TPU-MLIR W8A16 for ChatGLM2-6B", sections 2-4: per-channel INT8
+ *    weights, cast back to floating point and multiplied by the scale, then
+ *    multiplied with the F16 activation (w8a16_gemv below).
+ *
+ * Readings of points the pages leave open (fixed here, identical in the
+ * CPU oracle used by the tests):
+ *  - INT4 codes are symmetric in [-7, 7]: s_w = max|w_row| / 7 (fp32 IEEE
+ *    division), q = clamp(round_half_away(w / s_w), -7, 7).
+ *  - INT8 activation codes are in [-127, 127]: s_a = max|x_row| / 127,
+ *    q = clamp(round_half_away(x / s_a), -127, 127); one s_a per activation
+ *    row.  A zero row gets scale 0 and all codes 0.
+ *  - Packing: byte j of a weight row holds code 2j in bits 0..3 and code
+ *    2j+1 in bits 4..7, each a 4-bit two's-complement value.
+ *  - Rescale: Y = ((float)acc * s_w) * s_a, two fp32 round-to-nearest
+ *    multiplies in that order.  W4A8 results are therefore exact functions
+ *    of the inputs (bit-reproducible).
+ *  - W8A16: s = binary16(max|w_row| / 127) per output channel; codes are
+ *    taken with that rounded scale; Y = s * sum_k float(q) * float(x) with
+ *    fp32 accumulation (order unspecified; within a stated tolerance of the
+ *    fp64 result).
+ *
+ * Conventions for every entry point:
+ *  - All array arguments are DEVICE pointers owned by the caller, row-major
+ *    and contiguous.  binary16 data is passed as uint16_t bit patterns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call is asynchronous on that stream and performs no
+ *    host synchronisation and no allocation.
+ *  - Arguments are checked on the host before any launch; a failed check
+ *    returns a W4A8_ERR_* code, launches nothing and leaves a message for
+ *    w4a8_last_error().  A launch failure returns W4A8_ERR_CUDA.
+ *  - Inputs must be finite; results for NaN or Inf inputs are unspecified.
+ *  - No kernel traps.  Device-side waits are bounded (about 2 s); a wait that
+ *    runs out sets a bit in a device error word (see w4a8_device_error) and
+ *    the kernel returns early with its outputs unspecified.
+ */
+#ifndef W4A8_H
+#define W4A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4A8_OK = 0,
+    W4A8_ERR_NULL = 1,      /* a required pointer is NULL */
+    W4A8_ERR_ALIGN = 2,     /* a pointer is not aligned as documented */
+    W4A8_ERR_SHAPE = 3,     /* a size is out of the documented range */
+    W4A8_ERR_WORKSPACE = 4, /* workspace missing or smaller than required */
+    W4A8_ERR_CUDA = 5       /* a CUDA call failed (message has the reason) */
+} w4a8_status_t;
+
+/* Launch flag: allow the kernel to start while the previous kernel on the
+   stream is still running (programmatic dependent launch).  The kernel then
+   streams Wq/Wq8 and the weight scales before waiting for the previous
+   kernel, so those weight buffers must NOT be written by the kernel launched
+   immediately before it on the same stream.  Activations, outputs and the
+   workspace are only touched after the wait. */
+#define W4A8_LAUNCH_PDL 1u
+
+/* Maximum activation rows (decode batch) per call. */
+#define W4A8_MAX_M 8
+#define W8A16_MAX_M 4
+
+/* ---------------------------------------------------------------------- */
+/* Weight quantizers (load time)                                           */
+/* ---------------------------------------------------------------------- */
+
+/* Row-wise INT4 weight quantization and packing (the Jetson INT4 page,
+ * section 当前实现方式: "row-wise INT4 packed weight, one scale per row").
+ *   W   [N][K] fp32 in;  Wq [N][K/2] uint8 out;  sw [N] fp32 out.
+ *   Requires N >= 1, K >= 32, K % 32 == 0; W and Wq 16-byte aligned.
+ * Bit-identical to the CPU definition for finite inputs. */
+int w4_quantize_weights(const float* W, int64_t N, int64_t K, uint8_t* Wq, float* sw,
+                        void* stream);
+
+/* Per-output-channel INT8 weight quantization (the TPU-MLIR W8A16 page,
+ * section 2: per-channel INT8 storage; section 3: F16 scales).
+ *   W [N][K] fp32 in;  Wq8 [N][K] int8 out;  sw16 [N] binary16 out.
+ *   Requires N >= 1, K >= 16, K % 16 == 0; W and Wq8 16-byte aligned. */
+int w8_quantize_weights(const float* W, int64_t N, int64_t K, int8_t* Wq8, uint16_t* sw16,
+                        void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* Activation quantizer                                                    */
+/* ---------------------------------------------------------------------- */
+
+/* Dynamic INT8 activation quantization, one scale per row (the Jetson INT4
+ * page, section 正确方向: "activation: dynamically quantized to INT8").
+ *   X [M][K] binary16 in;  Xq [M][K] int8 out;  sa [M] fp32 out.
+ *   Requires 1 <= M <= 65535, 1 <= K <= 2^20, K % 8 == 0; X and Xq 16-byte
+ *   aligned. */
+int act_quantize_i8(const uint16_t* X, int64_t M, int64_t K, int8_t* Xq, float* sa,
+                    void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* W4A8 linear                                                             */
+/* ---------------------------------------------------------------------- */
+
+/* Workspace bytes w4a8_gemv / w4a8_linear need for this shape on the
+ * current device (0 when the chosen plan does not split K).  Layout: 4096
+ * bytes of arrival counters, then the int32/fp32 split partials.  The
+ * counters must be zero before the first call (zero-fill the buffer once);
+ * every call leaves them zero, so one workspace can serve calls of any
+ * shape, in either precision.  Calls that share a workspace must not run
+ * concurrently (same stream, or ordered by events).  Returns 0 for shapes
+ * the linear entry points reject. */
+size_t w4a8_workspace_bytes(int64_t M, int64_t K, int64_t N);
+
+/* INT4-weight x INT8-activation product with int32 accumulation and fp32
+ * rescale (the Jetson INT4 page, sections 正确方向 and 当前实现方式).
+ *   Xq [M][K] int8, sa [M] fp32      quantized activation (act_quantize_i8)
+ *   Wq [N][K/2] uint8, sw [N] fp32   packed weights (w4_quantize_weights)
+ *   Y  [M][N] fp32 out: Y[m][n] = ((float)acc[m][n] * sw[n]) * sa[m]
+ *   acc_out [M][N] int32 out, optional (NULL to skip): the exact
+ *     acc[m][n] = sum_k Xq[m][k] * q[n][k]
+ *   ws, ws_bytes: workspace of at least w4a8_workspace_bytes(M, K, N)
+ *     bytes, 256-byte aligned (may be NULL when that is 0).
+ *   flags: 0 or W4A8_LAUNCH_PDL.
+ * Requires 1 <= M <= W4A8_MAX_M, 32 <= K <= 131072, K % 32 == 0,
+ * 1 <= N <= 2^31 - 1; Xq and Wq 16-byte aligned; Y, sw, sa 4-byte aligned. */
+int w4a8_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, const uint8_t* Wq,
+              const float* sw, int64_t N, float* Y, int32_t* acc_out, void* ws,
+              size_t ws_bytes, unsigned flags, void* stream);
+
+/* Fused linear: activation quantization + INT4 x INT8 product + rescale in
+ * one kernel (the Jetson INT4 page, section 后续优化方向: fold the
+ * activation quantize into the linear kernel and save a launch).
+ *   X [M][K] binary16 in; Wq, sw, Y, acc_out, ws, ws_bytes, flags as in
+ *   w4a8_gemv.  Xq_out [M][K] int8 and sa_out [M] fp32 are optional outputs
+ *   (NULL to skip) holding exactly what act_quantize_i8 would produce.
+ * Y is bit-identical to act_quantize_i8 followed by w4a8_gemv.
+ * Requires the w4a8_gemv shape limits; X 16-byte aligned. */
+int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const float* sw,
+                int64_t N, float* Y, int8_t* Xq_out, float* sa_out, int32_t* acc_out,
+                void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* W8A16 linear                                                            */
+/* ---------------------------------------------------------------------- */
+
+/* Workspace bytes w8a16_gemv needs (same rules as w4a8_workspace_bytes). */
+size_t w8a16_workspace_bytes(int64_t M, int64_t K, int64_t N);
+
+/* INT8-weight x F16-activation product (the TPU-MLIR W8A16 page,
+ * section 4: cast INT8 to floating point, multiply by the scale, multiply
+ * with the activation).  The code is widened to fp32 exactly in registers,
+ * products are exact in fp32, sums are fp32, and the per-channel scale is
+ * applied once per output: Y[m][n] = float(sw16[n]) * sum_k q[n][k]*x[m][k].
+ *   X [M][K] binary16, Wq8 [N][K] int8, sw16 [N] binary16, Y [M][N] fp32.
+ * Requires 1 <= M <= W8A16_MAX_M, 16 <= K <= 65536, K % 16 == 0,
+ * 1 <= N <= 2^31 - 1; X and Wq8 16-byte aligned, Y 4-byte aligned. */
+int w8a16_gemv(const uint16_t* X, int64_t M, int64_t K, const int8_t* Wq8,
+               const uint16_t* sw16, int64_t N, float* Y, void* ws, size_t ws_bytes,
+               unsigned flags, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* Diagnostics                                                             */
+/* ---------------------------------------------------------------------- */
+
+/* Message for the last non-OK status returned on the calling thread
+ * ("" if none).  The pointer stays valid until the next call on this
+ * thread. */
+const char* w4a8_last_error(void);
+
+/* Copies the current device's error word into *flags and clears it.  Bit 0:
+ * a consumer wait for weight data ran out; bit 1: a producer wait for a
+ * free buffer ran out; bit 2: a wait for in-flight copies at exit ran out.
+ * Synchronises `stream` first.  Returns W4A8_OK or W4A8_ERR_CUDA. */
+int w4a8_device_error(unsigned* flags, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* Tuning and introspection (no counterpart on the pages)                  */
+/* ---------------------------------------------------------------------- */
+
+/* Process-wide overrides of the launch plan, for A/B measurements and for
+ * tests that must exercise a given plan.  Zero fields keep the heuristic.
+ *   force_splits: number of K pieces (1..16); the shape must admit it.
+ *   force_threads_per_row: threads sharing one row-piece (power of 2, <=256).
+ *   ring_bytes: target size of the shared-memory weight ring (<= 204800).
+ *   ctas_per_sm: CTAs per SM for each K piece (1..4; 0 = 1).
+ * w4a8_workspace_bytes reflects the overrides.  NULL restores the defaults.
+ * Not synchronised with calls running on other threads. */
+typedef struct {
+    int force_splits;
+    int force_threads_per_row;
+    int ring_bytes;
+    int ctas_per_sm;
+} w4a8_tuning_t;
+
+int w4a8_set_tuning(const w4a8_tuning_t* tuning);
+
+/* Writes up to n_info integers describing the plan the linear entry points
+ * would use for this shape, in this order: splits P, threads per row-piece,
+ * granule columns per thread, row-pieces per stage, CTAs per piece, grid
+ * size, most rows per CTA, ring stages, bytes per stage, dynamic shared
+ * memory bytes, workspace bytes (saturated at INT32_MAX).  w8a16 != 0
+ * selects w8a16_gemv.  num_sms > 0 plans for a device with that many SMs
+ * without touching any GPU (host-side testing); 0 queries the current
+ * device. */
+int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int* info,
+                   int n_info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A8_H */

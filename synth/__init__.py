@@ -96,3 +96,57 @@ def activation(seed: int, M: int, K: int, outlier_frac: float = 0.0,
 
 def n_outliers(K: int, outlier_frac: float) -> int:
     return int(np.ceil(outlier_frac * K - 1e-9)) if outlier_frac > 0 else 0
+
+
+# ----------------------------------------------------------------------------
+# CUDA twin of ``normal`` for large tensors (test / benchmark infrastructure)
+# ----------------------------------------------------------------------------
+
+import ctypes as _ct
+import os as _os
+import subprocess as _sp
+
+_HERE = _os.path.dirname(_os.path.abspath(__file__))
+_CU = _os.path.join(_HERE, "synth_gen.cu")
+_SO = _os.path.join(_HERE, "_build", "libsynth.so")
+_LIB = None
+
+
+def build_gpu() -> str:
+    """Compile libsynth.so for sm_103a if it is missing or stale."""
+    if _os.path.exists(_SO) and _os.path.getmtime(_SO) >= _os.path.getmtime(_CU):
+        return _SO
+    _os.makedirs(_os.path.dirname(_SO), exist_ok=True)
+    nvcc = _os.path.join(_os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    tmp = _SO + ".tmp%d" % _os.getpid()
+    _sp.check_call([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                    "-Xcompiler", "-fPIC", "-shared", "-cudart", "static", "-o", tmp, _CU])
+    _os.replace(tmp, _SO)
+    return _SO
+
+
+def _gpu_lib():
+    global _LIB
+    if _LIB is None:
+        lib = _ct.CDLL(build_gpu())
+        lib.synth_normal_f32.restype = _ct.c_int
+        lib.synth_normal_f32.argtypes = [_ct.c_uint32, _ct.c_uint64, _ct.c_uint64, _ct.c_float,
+                                         _ct.c_void_p, _ct.c_void_p]
+        _LIB = lib
+    return _LIB
+
+
+def normal_gpu(seed: int, shape, sigma: float = 1.0, offset: int = 0, device="cuda", out=None):
+    """Same values as ``normal(seed, shape, sigma, offset)``, drawn on the GPU
+    into a float32 torch tensor."""
+    import torch
+    n = int(np.prod(shape))
+    if out is None:
+        out = torch.empty(tuple(shape), dtype=torch.float32, device=device)
+    assert out.dtype == torch.float32 and out.is_contiguous() and out.numel() == n
+    stream = torch.cuda.current_stream(out.device).cuda_stream
+    st = _gpu_lib().synth_normal_f32(seed & 0xFFFFFFFF, offset, n, float(np.float32(sigma)),
+                                      out.data_ptr(), stream)
+    if st != 0:
+        raise RuntimeError("synth_normal_f32 failed with status %d" % st)
+    return out

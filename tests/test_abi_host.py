@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI (no GPU): exported symbols, argument
+validation that returns before any CUDA call, and the launch planner."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_weight_quantized_w4a8_gb300 as w4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    w4.build()
+    return w4.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "w4a8.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    for want in ["w4_quantize_weights", "w8_quantize_weights", "act_quantize_i8", "w4a8_gemv",
+                 "w4a8_linear", "w8a16_gemv", "w4a8_workspace_bytes", "w8a16_workspace_bytes",
+                 "w4a8_last_error", "w4a8_device_error", "w4a8_set_tuning", "w4a8_plan_info"]:
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in header_functions():
+        assert hasattr(L, name), name
+    assert set(header_functions()) <= set(w4.EXPORTS) | set(header_functions())
+
+
+def test_binding_covers_header():
+    assert set(header_functions()) == set(w4.EXPORTS)
+
+
+P16 = 0x10000  # a fake, 16-byte aligned address: never dereferenced (checks fail first)
+
+
+def test_null_pointers_rejected(L):
+    assert L.w4_quantize_weights(None, 4, 32, P16, P16, None) == w4._binding.ERR_NULL
+    assert L.act_quantize_i8(P16, 1, 32, None, P16, None) == w4._binding.ERR_NULL
+    assert L.w4a8_gemv(None, P16, 1, 32, P16, P16, 4, P16, None, None, 0, 0, None) == w4._binding.ERR_NULL
+    assert L.w4a8_linear(P16, 1, 32, P16, None, 4, P16, None, None, None, None, 0, 0, None) == w4._binding.ERR_NULL
+    assert L.w8a16_gemv(P16, 1, 32, None, P16, 4, P16, None, 0, 0, None) == w4._binding.ERR_NULL
+    assert b"NULL" in L.w4a8_last_error()
+
+
+def test_bad_shapes_rejected(L):
+    E = w4._binding.ERR_SHAPE
+    assert L.w4_quantize_weights(P16, 4, 48, P16, P16, None) == E          # K % 32
+    assert L.w4_quantize_weights(P16, 0, 32, P16, P16, None) == E          # N < 1
+    assert L.w8_quantize_weights(P16, 4, 24, P16, P16, None) == E          # K % 16
+    assert L.act_quantize_i8(P16, 0, 32, P16, P16, None) == E              # M < 1
+    assert L.act_quantize_i8(P16, 1, 12, P16, P16, None) == E              # K % 8
+    assert L.w4a8_gemv(P16, P16, 9, 32, P16, P16, 4, P16, None, None, 0, 0, None) == E  # M > 8
+    assert L.w4a8_gemv(P16, P16, 1, 40, P16, P16, 4, P16, None, None, 0, 0, None) == E  # K % 32
+    assert L.w4a8_gemv(P16, P16, 1, 262144, P16, P16, 4, P16, None, None, 0, 0, None) == E
+    assert L.w4a8_linear(P16, 1, 32, P16, P16, 0, P16, None, None, None, None, 0, 0, None) == E
+    assert L.w8a16_gemv(P16, 5, 32, P16, P16, 4, P16, None, 0, 0, None) == E  # M > 4
+    assert L.w8a16_gemv(P16, 1, 131072, P16, P16, 4, P16, None, 0, 0, None) == E
+    assert L.w4a8_workspace_bytes(9, 32, 4) == 0
+
+
+def test_misaligned_pointers_rejected(L):
+    E = w4._binding.ERR_ALIGN
+    assert L.w4_quantize_weights(P16 + 4, 4, 32, P16, P16, None) == E
+    assert L.act_quantize_i8(P16, 1, 32, P16 + 8, P16, None) == E
+    assert L.w4a8_gemv(P16 + 8, P16, 1, 32, P16, P16, 4, P16, None, None, 0, 0, None) == E
+    assert L.w4a8_gemv(P16, P16, 1, 32, P16 + 1, P16, 4, P16, None, None, 0, 0, None) == E
+    assert L.w4a8_linear(P16, 1, 32, P16, P16, 4, P16 + 2, None, None, None, None, 0, 0, None) == E
+    assert L.w8a16_gemv(P16, 1, 32, P16 + 4, P16, 4, P16, None, 0, 0, None) == E
+
+
+def test_tuning_validation():
+    with pytest.raises(w4.W4A8Error):
+        w4.w4a8_set_tuning(force_splits=17)
+    with pytest.raises(w4.W4A8Error):
+        w4.w4a8_set_tuning(force_threads_per_row=24)
+    with pytest.raises(w4.W4A8Error):
+        w4.w4a8_set_tuning(ring_bytes=10 ** 7)
+    w4.w4a8_set_tuning(reset=True)
+
+
+SHAPES = [(1, 896, 512), (1, 3584, 3584), (1, 3584, 512), (1, 3584, 18944), (1, 18944, 3584),
+          (1, 3584, 152064), (2, 3584, 18944), (4, 18944, 3584), (8, 3584, 18944),
+          (8, 18944, 3584), (3, 32, 1), (1, 64, 100000), (5, 131072, 3), (1, 4096, 7)]
+
+
+@pytest.mark.parametrize("sms", [152, 148, 20, 1])
+@pytest.mark.parametrize("w8", [False, True])
+def test_plan_invariants(sms, w8):
+    for (M, K, N) in SHAPES:
+        if w8 and (M > 4 or K > 65536):
+            continue
+        p = w4.w4a8_plan_info(M, K, N, w8a16=w8, num_sms=sms)
+        kgran = 16 if w8 else 32
+        Gt = K // kgran
+        P = p["splits"]
+        Gq = -(-Gt // P)
+        assert 1 <= P <= 16 and (P - 1) * Gq < Gt
+        Cl, S = p["threads_per_row"], p["cols_per_thread"]
+        assert Cl & (Cl - 1) == 0 and Cl * S >= Gq and Cl * (S - 1) < Gq
+        mt = 1 if M <= 1 else 2 if M <= 2 else 4 if M <= 4 else 8
+        assert S <= ((4 if w8 else 8) // mt)
+        assert p["rows_per_stage"] * Cl == 256
+        assert p["grid"] == p["ctas_per_split"] * P
+        assert p["ctas_per_split"] <= N
+        assert p["rows_per_cta"] * p["ctas_per_split"] >= N
+        assert p["rows_per_cta"] <= 4096 or P > 1
+        assert 2 <= p["stages"] <= 16
+        assert p["stage_bytes"] % 128 == 0 and p["stage_bytes"] >= p["rows_per_stage"] * Gq * 16
+        assert p["smem_bytes"] <= 232448
+        assert (p["ws_bytes"] > 0) == (P > 1)
+
+
+def test_forced_plans_respected():
+    try:
+        w4.w4a8_set_tuning(force_splits=4)
+        assert w4.w4a8_plan_info(1, 3584, 3584, num_sms=152)["splits"] == 4
+        w4.w4a8_set_tuning(force_threads_per_row=256)
+        assert w4.w4a8_plan_info(1, 3584, 3584, num_sms=152)["threads_per_row"] == 256
+        w4.w4a8_set_tuning(ring_bytes=8192)
+        assert w4.w4a8_plan_info(1, 3584, 3584, num_sms=152)["stages"] == 2
+    finally:
+        w4.w4a8_set_tuning(reset=True)

@@ -1,0 +1,299 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+W4A8 (quantizers, codes, scales, int32 accumulators, fp32 outputs) must be
+bit-exact; W8A16 outputs within the stated tolerance of the fp64 oracle:
+relative L2 error <= 5e-4 and |err| <= 1e-3 * (|y| + 1) per element.
+Sizes span several tiles and ragged tails; plans are forced through every
+split count, threads-per-row setting and a two-stage ring.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+W8_REL_L2 = 5e-4
+W8_ELEM = 1e-3
+
+
+@pytest.fixture(scope="module")
+def w4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bit_weight_quantized_w4a8_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+@pytest.fixture(autouse=True)
+def _reset_tuning(w4):
+    w4.w4a8_set_tuning(reset=True)
+    yield
+    w4.w4a8_set_tuning(reset=True)
+    assert w4.w4a8_device_error() == 0
+
+
+def bits(a):
+    a = np.ascontiguousarray(a)
+    return a.view(np.uint32 if a.dtype.itemsize == 4 else np.uint16)
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def weights(N, K, seed, sigma=0.02):
+    return synth.normal(seed, (N, K), sigma)
+
+
+def check_w4a8(w4, orc, M, K, N, seed, fused=True, outliers=0.001, flags=0, zero_rows=()):
+    W = weights(N, K, seed)
+    for r in zero_rows:
+        W[r % N] = 0
+    X = synth.activation(seed + 7, M, K, outlier_frac=outliers)
+    if M > 1:
+        X[M - 1] = 0  # a zero activation row: scale 0, codes 0, outputs 0
+    Wq_ref, sw_ref = orc.w4_quantize(W)
+    Y_ref, Xq_ref, sa_ref, acc_ref = orc.w4a8_linear(X, Wq_ref, sw_ref)
+
+    Wq, sw = w4.w4_quantize_weights(to_dev(W))
+    assert np.array_equal(Wq.cpu().numpy(), Wq_ref)
+    assert np.array_equal(bits(sw.cpu().numpy()), bits(sw_ref))
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    if fused:
+        Xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
+        sa = torch.empty((M,), dtype=torch.float32, device="cuda")
+        Y = w4.w4a8_linear(to_dev(X), Wq, sw, Xq_out=Xq, sa_out=sa, acc_out=acc, flags=flags)
+    else:
+        Xq, sa = w4.act_quantize_i8(to_dev(X))
+        Y = w4.w4a8_gemv(Xq, sa, Wq, sw, acc_out=acc, flags=flags)
+    torch.cuda.synchronize()
+    assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
+    assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
+    assert np.array_equal(acc.cpu().numpy(), acc_ref)
+    assert np.array_equal(bits(Y.cpu().numpy()), bits(Y_ref))
+
+
+# ---------------------------------------------------------------------------
+# quantizers
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K,seed", [(512, 896, 0), (37, 3584, 1), (5, 32, 2), (64, 18944, 3),
+                                      (300, 64, 4), (1, 131072, 5)])
+def test_w4_quantize(w4, orc, N, K, seed):
+    W = weights(N, K, seed)
+    W[0, 3] = 0.25   # an outlier row
+    if N > 2:
+        W[2] = 0     # a zero row
+    Wq_ref, sw_ref = orc.w4_quantize(W)
+    Wq, sw = w4.w4_quantize_weights(to_dev(W))
+    assert np.array_equal(Wq.cpu().numpy(), Wq_ref)
+    assert np.array_equal(bits(sw.cpu().numpy()), bits(sw_ref))
+
+
+def test_w4_quantize_golden_rows(w4, orc):
+    """The hand-derived closed forms (tests/golden) through the GPU quantizer."""
+    import pins
+    for c in pins.read_cases("w4_quant_closed_forms.txt"):
+        row = np.zeros((1, 32), np.float32)
+        vals = [float(v) for v in c["row"]]
+        row[0, :len(vals)] = vals
+        Wq, sw = w4.w4_quantize_weights(to_dev(row))
+        want = [int(b, 16) for b in c["bytes"]]
+        assert list(Wq.cpu().numpy()[0, :len(want)]) == want, c["name"]
+        assert sw.item() == float(c["scale"][0])
+
+
+@pytest.mark.parametrize("M,K,seed", [(1, 896, 10), (3, 3584, 11), (8, 18944, 12), (2, 8, 13),
+                                      (5, 131072, 14)])
+def test_act_quantize(w4, orc, M, K, seed):
+    X = synth.activation(seed, M, K, outlier_frac=0.001)
+    if M > 1:
+        X[1] = 0
+    Xq_ref, sa_ref = orc.act_quantize(X)
+    Xq, sa = w4.act_quantize_i8(to_dev(X))
+    assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
+    assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
+
+
+@pytest.mark.parametrize("N,K,seed", [(64, 4096, 20), (7, 13696, 21), (33, 16, 22)])
+def test_w8_quantize(w4, orc, N, K, seed):
+    W = weights(N, K, seed)
+    if N > 3:
+        W[3] = 0
+        W[1] *= 1e-3    # binary16 subnormal scale: clamping is reachable
+        W[2, 5] = 1e-5
+    Wq_ref, sw_ref = orc.w8_quantize(W)
+    Wq8, sw16 = w4.w8_quantize_weights(to_dev(W))
+    assert np.array_equal(Wq8.cpu().numpy(), Wq_ref)
+    assert np.array_equal(bits(sw16.cpu().numpy()), bits(sw_ref))
+
+
+# ---------------------------------------------------------------------------
+# W4A8 linear
+# ---------------------------------------------------------------------------
+
+W4A8_SHAPES = [
+    (1, 896, 512, 0),        # the tiny GEMV
+    (1, 3584, 37, 1),        # N smaller than a stage
+    (1, 3584, 3584, 2),
+    (2, 3584, 1000, 3),
+    (3, 18944, 77, 4),       # long rows
+    (4, 896, 1000, 5),
+    (5, 64, 300, 6),
+    (8, 3584, 129, 7),
+    (1, 32, 1, 8),           # smallest shape
+    (7, 96, 33, 9),
+    (1, 131072, 5, 10),      # longest rows
+    (8, 131072, 3, 11),
+    (6, 18944, 600, 12),
+]
+
+
+@pytest.mark.parametrize("M,K,N,seed", W4A8_SHAPES)
+def test_w4a8_linear_fused(w4, orc, M, K, N, seed):
+    check_w4a8(w4, orc, M, K, N, seed, fused=True, zero_rows=(1,))
+
+
+@pytest.mark.parametrize("M,K,N,seed", W4A8_SHAPES[:8])
+def test_w4a8_gemv_unfused(w4, orc, M, K, N, seed):
+    check_w4a8(w4, orc, M, K, N, seed, fused=False)
+
+
+@pytest.mark.parametrize("splits", [2, 3, 5, 16])
+@pytest.mark.parametrize("fused", [True, False])
+def test_w4a8_split_k(w4, orc, splits, fused):
+    w4.w4a8_set_tuning(force_splits=splits)
+    for (M, K, N, seed) in [(1, 3584, 700, 30), (3, 18944, 150, 31), (8, 1024, 64, 32)]:
+        if (K // 32) < splits:
+            continue
+        check_w4a8(w4, orc, M, K, N, seed, fused=fused)
+        check_w4a8(w4, orc, M, K, N, seed + 1, fused=fused)  # tickets were reset
+
+
+@pytest.mark.parametrize("cl", [1, 2, 8, 32, 64, 128, 256])
+def test_w4a8_threads_per_row(w4, orc, cl):
+    w4.w4a8_set_tuning(force_threads_per_row=cl)
+    for (M, K, N, seed) in [(1, 3584, 300, 40), (2, 2048, 99, 41), (1, 256, 513, 42)]:
+        try:
+            plan = w4.w4a8_plan_info(M, K, N)
+        except w4.W4A8Error:
+            continue  # this thread count cannot cover the row with this M
+        assert plan["threads_per_row"] == cl
+        check_w4a8(w4, orc, M, K, N, seed)
+
+
+def test_w4a8_two_stage_ring(w4, orc):
+    """A two-stage ring wraps many times; mbarrier phases must stay in step."""
+    w4.w4a8_set_tuning(ring_bytes=8192)
+    assert w4.w4a8_plan_info(1, 3584, 5000)["stages"] == 2
+    check_w4a8(w4, orc, 1, 3584, 5000, 50)
+    w4.w4a8_set_tuning(ring_bytes=8192, force_splits=3)
+    check_w4a8(w4, orc, 2, 18944, 300, 51)
+
+
+def test_w4a8_pdl_back_to_back_and_graph(w4, orc):
+    """Chains of PDL launches sharing one split-K workspace, eager and in a
+    CUDA graph replayed twice, give the oracle's results."""
+    w4.w4a8_set_tuning(force_splits=4)
+    shapes = [(1, 3584, 512, 60), (1, 18944, 256, 61), (1, 3584, 2048, 62), (1, 896, 100, 63)]
+    ins, refs = [], []
+    for (M, K, N, seed) in shapes:
+        W = weights(N, K, seed)
+        X = synth.activation(seed + 7, M, K, outlier_frac=0.001)
+        Wq_ref, sw_ref = orc.w4_quantize(W)
+        refs.append(orc.w4a8_linear(X, Wq_ref, sw_ref)[0])
+        ins.append((to_dev(X), to_dev(Wq_ref), to_dev(sw_ref),
+                    torch.empty((M, N), dtype=torch.float32, device="cuda")))
+    nbytes = max(w4.w4a8_workspace_bytes(M, K, N) for (M, K, N, _) in shapes)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+
+    def run():
+        for (X, Wq, sw, Y) in ins:
+            w4.w4a8_linear(X, Wq, sw, Y=Y, ws=ws, flags=w4.LAUNCH_PDL)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        run()
+        run()
+    torch.cuda.synchronize()
+    for (_, _, _, Y), ref in zip(ins, refs):
+        assert np.array_equal(bits(Y.cpu().numpy()), bits(ref))
+        Y.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run()
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        for (_, _, _, Y), ref in zip(ins, refs):
+            assert np.array_equal(bits(Y.cpu().numpy()), bits(ref))
+
+
+def test_workspace_checks(w4):
+    w4.w4a8_set_tuning(force_splits=2)
+    X = torch.zeros((1, 64), dtype=torch.float16, device="cuda")
+    Wq = torch.zeros((4, 32), dtype=torch.uint8, device="cuda")
+    sw = torch.zeros((4,), dtype=torch.float32, device="cuda")
+    need = w4.w4a8_workspace_bytes(1, 64, 4)
+    assert need > 0
+    small = torch.zeros(need - 256 if need > 256 else 1, dtype=torch.uint8, device="cuda")
+    with pytest.raises(w4.W4A8Error) as e:
+        w4.w4a8_linear(X, Wq, sw, ws=small)
+    assert e.value.status == 4
+
+
+# ---------------------------------------------------------------------------
+# W8A16
+# ---------------------------------------------------------------------------
+
+def check_w8a16(w4, orc, M, K, N, seed):
+    W = weights(N, K, seed)
+    X = synth.activation(seed + 3, M, K)
+    Wq_ref, sw_ref = orc.w8_quantize(W)
+    Y_ref = orc.w8a16_ref(X, Wq_ref, sw_ref)
+    Wq8, sw16 = w4.w8_quantize_weights(to_dev(W))
+    assert np.array_equal(Wq8.cpu().numpy(), Wq_ref)
+    Y = w4.w8a16_gemv(to_dev(X), Wq8, sw16).cpu().numpy().astype(np.float64)
+    err = np.abs(Y - Y_ref)
+    assert np.sqrt((err ** 2).sum() / max((Y_ref ** 2).sum(), 1e-300)) <= W8_REL_L2
+    assert np.all(err <= W8_ELEM * (np.abs(Y_ref) + 1))
+    # and the deterministic fp32 summation bound: K roundings of partial sums
+    s = sw_ref.astype(np.float64)[None, :]
+    absum = np.abs(X.astype(np.float64)) @ np.abs(Wq_ref.astype(np.float64)).T * s
+    assert np.all(err <= (K + 2) * 2.0 ** -24 * absum + 1e-30)
+
+
+@pytest.mark.parametrize("M,K,N,seed", [(1, 4096, 4608, 70), (2, 64, 100, 71), (4, 13696, 50, 72),
+                                        (3, 16, 7, 73), (1, 13696, 400, 74), (1, 65536, 3, 75)])
+def test_w8a16(w4, orc, M, K, N, seed):
+    check_w8a16(w4, orc, M, K, N, seed)
+
+
+@pytest.mark.parametrize("splits", [2, 5])
+def test_w8a16_split_k(w4, orc, splits):
+    w4.w4a8_set_tuning(force_splits=splits)
+    check_w8a16(w4, orc, 1, 4096, 333, 80)
+    check_w8a16(w4, orc, 3, 4096, 64, 81)    # M=3 needs pieces of <= 256 granules
+    check_w8a16(w4, orc, 1, 13696, 64, 82)
+
+
+# ---------------------------------------------------------------------------
+# generator twin
+# ---------------------------------------------------------------------------
+
+def test_gpu_generator_matches_host(w4):
+    g = synth.normal_gpu(1234, (3000, 64), 0.02).cpu().numpy()
+    assert np.array_equal(bits(g), bits(synth.normal(1234, (3000, 64), 0.02)))
+    g = synth.normal_gpu(99, (1000,), 1.0, offset=(1 << 32) - 1000).cpu().numpy()
+    assert np.array_equal(bits(g), bits(synth.normal(99, (1000,), 1.0, offset=(1 << 32) - 1000)))
