@@ -26,6 +26,7 @@ EXPORTS = [
     "w4a8_workspace_bytes", "w4a8_gemv", "w4a8_linear",
     "w8a16_workspace_bytes", "w8a16_gemv",
     "w4a8_last_error", "w4a8_device_error", "w4a8_set_tuning", "w4a8_plan_info",
+    "w4a8_linear_noalloc",
 ]
 
 
@@ -48,6 +49,7 @@ _SIGS = {
     "w4a8_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
     "w4a8_gemv": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, ctypes.c_size_t, _u, _p]),
     "w4a8_linear": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _p, _p, ctypes.c_size_t, _u, _p]),
+    "w4a8_linear_noalloc": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _u, _p]),
     "w8a16_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
     "w8a16_gemv": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _p, ctypes.c_size_t, _u, _p]),
     "w4a8_last_error": (ctypes.c_char_p, []),
@@ -209,6 +211,23 @@ def w4a8_linear(X, Wq, sw, Y=None, Xq_out=None, sa_out=None, acc_out=None, ws=No
                              _ptr(sa_out), _ptr(acc_out), _ptr(ws),
                              0 if ws is None else ws.numel() * ws.element_size(), flags,
                              _stream(X)))
+    return Y
+
+
+def w4a8_linear_noalloc(X, Wq, sw, Y=None, flags: int = 0):
+    """w4a8_linear for callers that cannot provide workspace memory: the
+    split-K scratch is the library's static per-GPU array (see the C header
+    for its limit and for why calls overlapping on the GPU must be avoided).
+    Allocates nothing when Y is given."""
+    _want(X, torch.float16, "X")
+    M, K = X.shape
+    N = Wq.shape[0]
+    _want(Wq, torch.uint8, "Wq", (N, K // 2))
+    _want(sw, torch.float32, "sw", (N,))
+    Y = torch.empty((M, N), dtype=torch.float32, device=X.device) if Y is None else Y
+    _want(Y, torch.float32, "Y", (M, N))
+    _check(lib().w4a8_linear_noalloc(_ptr(X), M, K, _ptr(Wq), _ptr(sw), N, _ptr(Y), flags,
+                                     _stream(X)))
     return Y
 
 

@@ -257,3 +257,68 @@ int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int*
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// w4a8_linear_noalloc: the fused linear with its split-K scratch in a static
+// device array, for callers that cannot provide workspace memory.
+// ---------------------------------------------------------------------------
+
+#include <mutex>
+
+namespace {
+
+// Scratch of the split-K kernel: 4096 bytes of arrival counters, then the
+// int32 partial sums.  Every GPU that loads this library holds it until exit.
+constexpr size_t kNoAllocScratchBytes = W4A8_NOALLOC_SCRATCH;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of this device's scratch array.  The first call on a device
+// looks it up (the host-side symbol is only a stand-in, never a device
+// address) and clears the arrival counters on `stream`.
+int noalloc_scratch(cudaStream_t stream, void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(W4A8_ERR_CUDA, "device ordinal %d not supported", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+        e = cudaMemsetAsync(p, 0, w4a8::kTicketBytes, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch counters");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return W4A8_OK;
+}
+
+}  // namespace
+
+extern "C" int w4a8_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                                   const float* sw, int64_t N, float* Y, unsigned flags,
+                                   void* stream) {
+    if (!X || !Wq || !sw || !Y) return fail(W4A8_ERR_NULL, "w4a8_linear_noalloc: NULL pointer");
+    int st = check_w4a8_shape(M, K, N);
+    if (st != W4A8_OK) return st;
+    if (!aligned(X, 16) || !aligned(Wq, 16) || !aligned(Y, 4) || !aligned(sw, 4))
+        return fail(W4A8_ERR_ALIGN, "w4a8_linear_noalloc: X/Wq need 16-byte, Y/sw 4-byte alignment");
+    w4a8::GemvPlan pl;
+    if ((st = plan_for(true, true, M, K, N, &pl)) != W4A8_OK) return st;
+    if (pl.ws_bytes > kNoAllocScratchBytes)
+        return fail(W4A8_ERR_WORKSPACE,
+                    "w4a8_linear_noalloc: this shape needs %zu bytes of split-K scratch, more than "
+                    "the %zu-byte static scratch; use w4a8_linear with a workspace",
+                    pl.ws_bytes, kNoAllocScratchBytes);
+    void* scratch = nullptr;
+    if (pl.ws_bytes > 0 &&
+        (st = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch)) != W4A8_OK)
+        return st;
+    cudaError_t e = w4a8::launch_w4a8(pl, true, X, nullptr, nullptr, (int)M, K, Wq, sw, N, Y,
+                                      nullptr, nullptr, nullptr, scratch, flags,
+                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear_noalloc launch");
+}

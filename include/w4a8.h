@@ -148,6 +148,29 @@ int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, cons
                 int64_t N, float* Y, int8_t* Xq_out, float* sa_out, int32_t* acc_out,
                 void* ws, size_t ws_bytes, unsigned flags, void* stream);
 
+/* Fused linear that allocates nothing and takes no workspace.  The pages
+ * have no counterpart; this is a calling convention for callers that cannot
+ * provide device memory: code paths that must not allocate, such as an
+ * engine's per-token execute step or a framework plugin whose enqueue
+ * function is not allowed to, because cudaMalloc can synchronise the device
+ * and take unbounded time.
+ *   Same arguments and results as w4a8_linear without the optional outputs:
+ *   Y is bit-identical to w4a8_linear's for the same plan.
+ * The split-K scratch is a static 4 MiB device array (W4A8_NOALLOC_SCRATCH
+ * bytes: 4096 bytes of arrival counters, then int32 partials) that every GPU
+ * loading the library holds until the process exits.  Shapes whose plan
+ * needs more scratch are rejected with W4A8_ERR_WORKSPACE (at M = 1 and four
+ * K pieces that is N > 261,888).  The first call on a device that needs
+ * scratch looks up the array's device address and clears its counters on
+ * `stream`; make that first call before any stream capture.  Every call on a
+ * device shares the one array, which keeps the last call's contents; the
+ * kernels leave the counters at zero, so calls in order on one stream are
+ * fine, but calls whose executions overlap on the GPU (different streams
+ * without ordering between them) race and give wrong results. */
+#define W4A8_NOALLOC_SCRATCH (4u << 20)
+int w4a8_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                        const float* sw, int64_t N, float* Y, unsigned flags, void* stream);
+
 /* ---------------------------------------------------------------------- */
 /* W8A16 linear                                                            */
 /* ---------------------------------------------------------------------- */
