@@ -1,13 +1,14 @@
 #!/usr/bin/env python
 """Benchmark: the Qwen2-7B-shaped decode linear set at M=1, W4A8.
 
-One step = one pass of the whole hot path over one decode token: for each of
-the eight linears (q, k, v, o, gate, up, down, lm_head) the fused kernel
+One step = one pass of the whole hot path over one decode token: for the
+eight linears (q, k, v, o, gate, up, down, lm_head) the fused kernel
 quantizes the fp16 activation to INT8, streams the packed INT4 weights,
-accumulates in int32 and rescales to fp32.  Weights (389.8 MB per set) are
-resident in HBM; two copies alternate between steps, so nothing is reused
-from the 129 MB L2.  The set is replayed as a CUDA graph of eight
-programmatically dependent launches.
+accumulates in int32 and rescales to fp32.  Projections that read the same
+activation in the model share one grouped launch (q/k/v; gate/up), so a step
+is five launches.  Weights (389.8 MB per set) are resident in HBM; two copies
+alternate between steps, so nothing is reused from the 129 MB L2.  The step is
+replayed as a CUDA graph of programmatically dependent launches.
 
 Reported (one JSON line, rank 0):
   value     effective weight GB/s (packed INT4 + fp32 scales per set / time)
@@ -41,6 +42,10 @@ METRIC = "µs/decode-step linear set & effective weight GB/s (% of GB300 HBM pea
 LINEARS = [("q", 3584, 3584), ("k", 3584, 512), ("v", 3584, 512), ("o", 3584, 3584),
            ("gate", 3584, 18944), ("up", 3584, 18944), ("down", 18944, 3584),
            ("lm_head", 3584, 152064)]
+# Launches of one decode step: projections that read the same activation share
+# one grouped launch (q/k/v; gate/up), as they do in the model.
+LAUNCHES = [("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")),
+            ("down", ("down",)), ("lm_head", ("lm_head",))]
 WEIGHT_SEED0 = 1000
 ACT_SEED_OFFSET = 500
 OUTLIER_FRAC = 0.001
@@ -50,6 +55,13 @@ WORKLOAD = ("Qwen2-7B-shaped decode linear set, M=1, W4A8: q 3584->3584, k 3584-
             "v 3584->512, o 3584->3584, gate 3584->18944, up 3584->18944, down 18944->3584, "
             "lm_head 3584->152064; weights N(0,0.02), x N(0,1) fp16 with 0.1% outliers x20")
 CPU_SAMPLE_STRIDE = 8
+
+
+def activation_seed(name: str) -> int:
+    """Seed of the activation read by linear `name` (shared inside a launch)."""
+    names = [l[0] for l in LINEARS]
+    first = next(members[0] for _, members in LAUNCHES if name in members)
+    return WEIGHT_SEED0 + names.index(first) + ACT_SEED_OFFSET
 
 
 def weight_bytes(K: int, N: int) -> int:
@@ -221,7 +233,7 @@ def cpu_sample_inputs(dev):
         W_rows = W[::CPU_SAMPLE_STRIDE].cpu().numpy()
         del W
         Wq, sw = orc.w4_quantize(W_rows)
-        X = synth.activation(seed + ACT_SEED_OFFSET, 1, K, outlier_frac=OUTLIER_FRAC)
+        X = synth.activation(activation_seed(name), 1, K, outlier_frac=OUTLIER_FRAC)
         out.append((X, Wq, sw, N))
     return orc, out
 
@@ -298,15 +310,18 @@ def run_ours(args, world, rank):
     stream = torch.cuda.Stream(dev)
     PDL = w4.LAUNCH_PDL
 
-    # --- inputs: activations in one buffer, outputs in one buffer ----------
-    k_off = np.cumsum([0] + [K for _, K, _ in LINEARS])
+    # --- inputs: one activation per launch, outputs in one buffer -----------
+    names = [l[0] for l in LINEARS]
+    lin = {name: (i, K, N) for i, (name, K, N) in enumerate(LINEARS)}
+    act_K = [lin[members[0]][1] for _, members in LAUNCHES]
+    k_off = np.cumsum([0] + act_K)
     n_off = np.cumsum([0] + [N for _, _, N in LINEARS])
-    X_host = np.concatenate([synth.activation(WEIGHT_SEED0 + i + ACT_SEED_OFFSET, 1, K,
-                                              outlier_frac=OUTLIER_FRAC)[0]
-                             for i, (_, K, _) in enumerate(LINEARS)])
+    X_host = np.concatenate([
+        synth.activation(activation_seed(members[0]), 1, lin[members[0]][1],
+                         outlier_frac=OUTLIER_FRAC)[0] for _, members in LAUNCHES])
     X_all = torch.from_numpy(X_host).to(dev)
     Y_all = torch.zeros(int(n_off[-1]), dtype=torch.float32, device=dev)
-    Xs = [X_all[k_off[i]:k_off[i + 1]].view(1, -1) for i in range(len(LINEARS))]
+    Xs = [X_all[k_off[j]:k_off[j + 1]].view(1, -1) for j in range(len(LAUNCHES))]
     Ys = [Y_all[n_off[i]:n_off[i + 1]].view(1, -1) for i in range(len(LINEARS))]
 
     # --- weights: generated on the GPU, quantized by the library -----------
@@ -320,14 +335,23 @@ def run_ours(args, world, rank):
             Wqs.append(Wq)
             sws.append(sw)
         copies.append((Wqs, sws))
-    ws_bytes = max(w4.w4a8_workspace_bytes(1, K, N) for _, K, N in LINEARS)
-    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    ws_bytes = max(w4.w4a8_workspace_bytes(1, act_K[j], sum(lin[n][2] for n in members))
+                   for j, (_, members) in enumerate(LAUNCHES))
+    ws = torch.zeros(max(ws_bytes, 4096), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
-    def launch_set(c):
+    def launch(c, j, flags):
         Wqs, sws = copies[c]
-        for i in range(len(LINEARS)):
-            w4.w4a8_linear(Xs[i], Wqs[i], sws[i], Y=Ys[i], ws=ws, flags=PDL)
+        idx = [lin[n][0] for n in LAUNCHES[j][1]]
+        if len(idx) == 1:
+            w4.w4a8_linear(Xs[j], Wqs[idx[0]], sws[idx[0]], Y=Ys[idx[0]], ws=ws, flags=flags)
+        else:
+            w4.w4a8_linear_grouped(Xs[j], [Wqs[i] for i in idx], [sws[i] for i in idx],
+                                   Ys=[Ys[i] for i in idx], ws=ws, flags=flags)
+
+    def launch_set(c):
+        for j in range(len(LAUNCHES)):
+            launch(c, j, PDL)
 
     # eager warm-up (sets kernel attributes), then graphs per weight copy
     with torch.cuda.stream(stream):
@@ -376,17 +400,16 @@ def run_ours(args, world, rank):
     barrier(world)
     ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
 
-    # --- dominant kernel: lm_head, per-launch CUDA events --------------------
-    li = len(LINEARS) - 1
-    _, K_lm, N_lm = LINEARS[li]
+    # --- dominant kernel: lm_head, CUDA events around each launch ------------
+    jl = [l[0] for l in LAUNCHES].index("lm_head")
+    _, K_lm, N_lm = LINEARS[lin["lm_head"][0]]
     n_lm = max(20, min(args.steps, 400))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_lm)]
     with torch.cuda.stream(stream):
         for k in range(n_lm):
-            Wqs, sws = copies[k % 2]
             evs[k][0].record(stream)
-            w4.w4a8_linear(Xs[li], Wqs[li], sws[li], Y=Ys[li], ws=ws, flags=0)
+            launch(k % 2, jl, 0)
             evs[k][1].record(stream)
     torch.cuda.synchronize()
     lm_ms = float(np.mean([a.elapsed_time(b) for a, b in evs[2:]]))
@@ -407,19 +430,25 @@ def run_ours(args, world, rank):
     Y_check = Y_pin.numpy()
     assert np.isfinite(Y_check).all()
 
-    # --- per-linear times (eager, one launch each, events) ------------------
-    per_linear = {}
-    with torch.cuda.stream(stream):
-        for i, (name, K, N) in enumerate(LINEARS):
-            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                     for _ in range(20)]
-            for k, (a, b) in enumerate(pairs):
-                Wqs, sws = copies[k % 2]
-                a.record(stream)
-                w4.w4a8_linear(Xs[i], Wqs[i], sws[i], Y=Ys[i], ws=ws, flags=0)
-                b.record(stream)
-            torch.cuda.synchronize()
-            per_linear[name] = round(float(np.mean([a.elapsed_time(b) for a, b in pairs[2:]])) * 1e3, 2)
+    # --- per-launch times: a graph of 20 launches of one kind (no PDL) -------
+    per_launch = {}
+    for j, (lname, members) in enumerate(LAUNCHES):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(20):
+                launch(k % 2, j, 0)
+        with torch.cuda.stream(stream):
+            g.replay()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(5):
+                g.replay()
+            a1.record(stream)
+        torch.cuda.synchronize()
+        us = a0.elapsed_time(a1) / 100 * 1e3
+        nbytes = sum(weight_bytes(lin[n][1], lin[n][2]) for n in members)
+        per_launch[lname] = {"us": round(us, 2), "GBps": round(nbytes / us / 1e3, 1)}
+        del g
     errors = w4.w4a8_device_error()
     if errors:
         raise SystemExit("device error word %#x" % errors)
@@ -436,7 +465,7 @@ def run_ours(args, world, rank):
         "dtype": "int4xint8->int32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "set_weight_bytes": SET_BYTES,
                    "l2": "two weight copies alternate (780 MB > 129 MB L2)",
-                   "launch": "CUDA graph of 8 fused linears with programmatic dependent launch",
+                   "launch": "CUDA graph of 5 fused launches (q/k/v and gate/up grouped) with programmatic dependent launch",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "us_per_set": round(ms_step * 1e3, 2),
         "pct_hbm_peak": {"of_measured": round(SET_BYTES / (ms_step * 1e-3) / 1e9 / peak, 4),
@@ -450,10 +479,10 @@ def run_ours(args, world, rank):
                 "us_per_set": round(e2e_ms * 1e3, 2),
                 "h2d_bytes_per_step": int(X_pin.numel() * X_pin.element_size()),
                 "d2h_bytes_per_step": int(Y_pin.numel() * Y_pin.element_size()),
-                "how": "CUDA graph: pinned H2D of the 8 activations, 8 fused linears, D2H of the 8 outputs"},
+                "how": "CUDA graph: pinned H2D of the 5 activations, 5 fused launches, D2H of the 8 outputs"},
         "clocks": clk,
-        "gpu_launches": len(LINEARS) * args.steps,
-        "per_linear_us_eager": per_linear,
+        "gpu_launches": len(LAUNCHES) * args.steps,
+        "per_launch_no_pdl": per_launch,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         orc, inputs = cpu_sample_inputs(dev)

@@ -6,7 +6,7 @@ include/w4a8.h); this package is its thin Python binding.
 from ._binding import (  # noqa: F401
     EXPORTS, LAUNCH_PDL, LIB_PATH, PLAN_FIELDS, W4A8_MAX_M, W8A16_MAX_M, W4A8Error,
     act_quantize_i8, lib, w4_quantize_weights, w4a8_device_error, w4a8_gemv,
-    w4a8_last_error, w4a8_linear, w4a8_linear_noalloc, w4a8_plan_info, w4a8_set_tuning, w4a8_workspace_bytes,
+    w4a8_last_error, w4a8_linear, w4a8_linear_grouped, w4a8_linear_noalloc, w4a8_plan_info, w4a8_set_tuning, w4a8_workspace_bytes,
     w8_quantize_weights, w8a16_gemv, w8a16_workspace_bytes,
 )
 from .build import build  # noqa: F401

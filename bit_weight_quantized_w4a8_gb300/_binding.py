@@ -26,7 +26,7 @@ EXPORTS = [
     "w4a8_workspace_bytes", "w4a8_gemv", "w4a8_linear",
     "w8a16_workspace_bytes", "w8a16_gemv",
     "w4a8_last_error", "w4a8_device_error", "w4a8_set_tuning", "w4a8_plan_info",
-    "w4a8_linear_noalloc",
+    "w4a8_linear_noalloc", "w4a8_linear_grouped",
 ]
 
 
@@ -50,6 +50,8 @@ _SIGS = {
     "w4a8_gemv": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, ctypes.c_size_t, _u, _p]),
     "w4a8_linear": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _p, _p, ctypes.c_size_t, _u, _p]),
     "w4a8_linear_noalloc": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _u, _p]),
+    "w4a8_linear_grouped": (ctypes.c_int, [_p, _i64, _i64, ctypes.c_int, _p, _p, _p, _p, _p,
+                                           ctypes.c_size_t, _u, _p]),
     "w8a16_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
     "w8a16_gemv": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _p, ctypes.c_size_t, _u, _p]),
     "w4a8_last_error": (ctypes.c_char_p, []),
@@ -212,6 +214,38 @@ def w4a8_linear(X, Wq, sw, Y=None, Xq_out=None, sa_out=None, acc_out=None, ws=No
                              0 if ws is None else ws.numel() * ws.element_size(), flags,
                              _stream(X)))
     return Y
+
+
+def w4a8_linear_grouped(X, Wqs, sws, Ys=None, ws=None, flags: int = 0):
+    """One launch for several weight matrices sharing X (e.g. q/k/v); returns
+    the list of outputs, each bit-identical to w4a8_linear on its own."""
+    _want(X, torch.float16, "X")
+    M, K = X.shape
+    G = len(Wqs)
+    if G != len(sws) or not 1 <= G <= 4:
+        raise ValueError("need 1..4 weight matrices with one scale vector each")
+    Ns = [int(w.shape[0]) for w in Wqs]
+    for g in range(G):
+        _want(Wqs[g], torch.uint8, "Wq[%d]" % g, (Ns[g], K // 2))
+        _want(sws[g], torch.float32, "sw[%d]" % g, (Ns[g],))
+    if Ys is None:
+        Ys = [torch.empty((M, n), dtype=torch.float32, device=X.device) for n in Ns]
+    for g in range(G):
+        _want(Ys[g], torch.float32, "Y[%d]" % g, (M, Ns[g]))
+    arr_p = ctypes.c_void_p * G
+    wq_a = arr_p(*[w.data_ptr() for w in Wqs])
+    sw_a = arr_p(*[s.data_ptr() for s in sws])
+    y_a = arr_p(*[y.data_ptr() for y in Ys])
+    n_a = (ctypes.c_int64 * G)(*Ns)
+    nbytes = w4a8_workspace_bytes(M, K, sum(Ns))
+    ws = _workspace(nbytes, X.device, ws)
+    _check(lib().w4a8_linear_grouped(_ptr(X), M, K, G, ctypes.cast(wq_a, ctypes.c_void_p),
+                                     ctypes.cast(sw_a, ctypes.c_void_p),
+                                     ctypes.cast(n_a, ctypes.c_void_p),
+                                     ctypes.cast(y_a, ctypes.c_void_p), _ptr(ws),
+                                     0 if ws is None else ws.numel() * ws.element_size(), flags,
+                                     _stream(X)))
+    return Ys
 
 
 def w4a8_linear_noalloc(X, Wq, sw, Y=None, flags: int = 0):

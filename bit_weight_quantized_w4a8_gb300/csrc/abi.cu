@@ -195,6 +195,31 @@ int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, cons
     return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear launch");
 }
 
+int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const uint8_t* const* Wq,
+                        const float* const* sw, const int64_t* N, float* const* Y, void* ws,
+                        size_t ws_bytes, unsigned flags, void* stream) {
+    if (!X || !Wq || !sw || !N || !Y) return fail(W4A8_ERR_NULL, "w4a8_linear_grouped: NULL pointer");
+    if (G < 1 || G > W4A8_MAX_GROUP)
+        return fail(W4A8_ERR_SHAPE, "G=%d outside [1, %d]", G, W4A8_MAX_GROUP);
+    int64_t total = 0;
+    for (int g = 0; g < G; ++g) {
+        if (!Wq[g] || !sw[g] || !Y[g]) return fail(W4A8_ERR_NULL, "w4a8_linear_grouped: NULL pointer in group %d", g);
+        if (N[g] < 1) return fail(W4A8_ERR_SHAPE, "N[%d]=%lld < 1", g, (long long)N[g]);
+        if (!aligned(Wq[g], 16) || !aligned(sw[g], 4) || !aligned(Y[g], 4))
+            return fail(W4A8_ERR_ALIGN, "w4a8_linear_grouped: Wq[%d] needs 16-byte, sw/Y 4-byte alignment", g);
+        total += N[g];
+    }
+    int st = check_w4a8_shape(M, K, total);
+    if (st != W4A8_OK) return st;
+    if (!aligned(X, 16)) return fail(W4A8_ERR_ALIGN, "w4a8_linear_grouped: X needs 16-byte alignment");
+    w4a8::GemvPlan pl;
+    if ((st = plan_for(true, true, M, K, total, &pl)) != W4A8_OK) return st;
+    if ((st = check_workspace(pl, ws, ws_bytes)) != W4A8_OK) return st;
+    cudaError_t e = w4a8::launch_w4a8_grouped(pl, X, (int)M, K, G, Wq, sw, N, Y, ws, flags,
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear_grouped launch");
+}
+
 int w8a16_gemv(const uint16_t* X, int64_t M, int64_t K, const int8_t* Wq8, const uint16_t* sw16,
                int64_t N, float* Y, void* ws, size_t ws_bytes, unsigned flags, void* stream) {
     if (!X || !Wq8 || !sw16 || !Y) return fail(W4A8_ERR_NULL, "w8a16_gemv: NULL pointer");

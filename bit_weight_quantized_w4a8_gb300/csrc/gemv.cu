@@ -38,14 +38,19 @@ namespace w4a8 {
 
 __device__ unsigned g_device_error;
 
+constexpr int kMaxSegments = 4;
+
 struct GemvArgs {
-    const uint8_t* W;       // W4: [N][K/2] packed nibbles; W8: [N][K] int8
-    const void* wscale;     // W4: float[N]; W8: binary16[N]
+    // Up to kMaxSegments weight matrices sharing the activation; their rows
+    // are concatenated: segment g holds rows off[g] .. off[g+1]-1 of N.
+    const uint8_t* W[kMaxSegments];   // W4: [N_g][K/2] packed nibbles; W8: [N_g][K] int8
+    const void* wscale[kMaxSegments]; // W4: float[N_g]; W8: binary16[N_g]
+    float* Yg[kMaxSegments];          // [M][N_g]
+    int64_t off[kMaxSegments + 1];    // segment row offsets; off[G..] = N
     const int8_t* Xq;       // W4 unfused: [M][K] int8 codes
     const float* sa;        // W4 unfused: [M] activation scales
     const __half* X;        // W4 fused and W8: [M][K] binary16 activation
-    float* Y;               // [M][N]
-    int32_t* acc_out;       // optional [M][N] (W4)
+    int32_t* acc_out;       // optional [M][N] (W4, one segment)
     int8_t* Xq_out;         // optional [M][K] (W4 fused)
     float* sa_out;          // optional [M] (W4 fused)
     void* part;             // split partials [P][M][N] (int32 or fp32)
@@ -99,28 +104,37 @@ __device__ __forceinline__ __half2 absmax8(uint4 h, __half2 m) {
 // |x/s| <= 129 the two lie within 2^-15 of each other.  When t is more than
 // 2^-14 away from every half-integer, both therefore have the same nearest
 // integer and neither is a tie: rint(t) is the answer.  The rare remaining
-// cases take the IEEE division.
-__device__ __forceinline__ uint32_t quant_i8(float x, float s, float r) {
-    const float t = __fmul_rn(x, r);
-    const float ti = rintf(t);
-    float q = ti;
-    if (!(fabsf(t - ti) < 0.5f - 0x1p-14f)) q = roundf(__fdiv_rn(x, s));
-    q = fminf(fmaxf(q, -127.f), 127.f);
-    return static_cast<uint32_t>(static_cast<int>(q)) & 0xFFu;
+// cases take the IEEE division.  rint(t) for |t| < 2^22 is (t + 1.5*2^23)
+// - 1.5*2^23 in round-to-nearest, and the integer sits in the low bits of
+// t + 1.5*2^23, so no conversion instruction is needed.
+__device__ __noinline__ int quant_near_tie(float x, float s) {
+    return static_cast<int>(roundf(__fdiv_rn(x, s)));  // kept out of line: rarely taken
 }
 
+__device__ __forceinline__ int quant_i8(float x, float s, float r) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    const float t = __fmul_rn(x, r);
+    const float y = __fadd_rn(t, kMagic);
+    const float ti = __fsub_rn(y, kMagic);
+    int q = __float_as_int(y) - 0x4B400000;
+    if (!(fabsf(__fsub_rn(t, ti)) < 0.5f - 0x1p-14f)) q = quant_near_tie(x, s);
+    return min(max(q, -127), 127);
+}
+
+// 8 binary16 values -> 8 INT8 codes, packed in order.
 __device__ __forceinline__ uint2 quant8(uint4 h, float s, float r) {
     if (s == 0.f) return make_uint2(0u, 0u);
     const __half2* p = reinterpret_cast<const __half2*>(&h);
-    uint32_t b[8];
+    int q[8];
     #pragma unroll
     for (int t = 0; t < 4; ++t) {
         const float2 f = __half22float2(p[t]);
-        b[2 * t] = quant_i8(f.x, s, r);
-        b[2 * t + 1] = quant_i8(f.y, s, r);
+        q[2 * t] = quant_i8(f.x, s, r);
+        q[2 * t + 1] = quant_i8(f.y, s, r);
     }
-    return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
-                      b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+    const uint32_t lo = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
+    const uint32_t hi = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
+    return make_uint2(lo, hi);
 }
 
 // 32 activation codes in natural order (two 16-byte words) -> the lane order
@@ -134,6 +148,13 @@ __device__ __forceinline__ void permute_act(uint4 lo, uint4 hi, uint32_t* act) {
         act[t] = __byte_perm(n[2 * t], n[2 * t + 1], 0x6420);
         act[4 + t] = __byte_perm(n[2 * t], n[2 * t + 1], 0x7531);
     }
+}
+
+__device__ __forceinline__ int segment_of(const GemvArgs& a, int64_t n) {
+    int g = 0;
+    #pragma unroll
+    for (int k = 1; k < kMaxSegments; ++k) g += (n >= a.off[k]) ? 1 : 0;
+    return g;
 }
 
 template <bool kW4, int MT, int SMAX, bool kFused>
@@ -159,74 +180,52 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
     const int64_t RB = (int64_t)pl.Gt * kGranBytes;
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.off_bars);
-    uint64_t* empty = full + NS;
-    uint64_t* sw_bar = empty + NS;              // scale cache filled
+    uint64_t* sw_bar = full + NS;                       // scale cache landed
+    int* released = reinterpret_cast<int*>(sw_bar + 1);  // warps done with each slot
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pl.off_flag);
     int* last_flag = reinterpret_cast<int*>(smem + pl.off_flag + 4);
     float* sw_s = reinterpret_cast<float*>(smem + pl.off_sw);
 
+    // Stage `st` of this CTA's weight stream into ring slot `slot`: one 1-D
+    // bulk copy of whole rows, or one per row-piece when K is split.
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int st, int slot) {
+        const int r0 = st * pl.Rl;
+        const int nr = min(pl.Rl, nrows - r0);
+        const uint32_t dst = smem_u32(smem + slot * pl.stage_stride);
+        const uint32_t bar = smem_u32(full + slot);
+        mbar_arrive_expect_tx(bar, (uint32_t)(nr * RBp));
+        // rows row0+r0 .. row0+r0+nr-1, cut where a segment ends
+        int64_t n = row0 + r0;
+        const int64_t n_end = n + nr;
+        while (n < n_end) {
+            const int sg = segment_of(a, n);
+            const int64_t run = min(n_end, a.off[sg + 1]) - n;
+            const uint8_t* src = a.W[sg] + (n - a.off[sg]) * RB + (int64_t)g0 * kGranBytes;
+            const uint32_t d = dst + (uint32_t)((n - row0 - r0) * RBp);
+            if (pl.P == 1) {
+                bulk_g2s(d, src, (uint32_t)(run * RBp), bar, pol);
+            } else {
+                for (int r = 0; r < run; ++r)
+                    bulk_g2s(d + r * RBp, src + (int64_t)r * RB, (uint32_t)RBp, bar, pol);
+            }
+            n += run;
+        }
+    };
+
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(full + s), 1);
-            mbar_init(smem_u32(empty + s), kConsumerWarps);
+            released[s] = 0;
         }
-        mbar_init(smem_u32(sw_bar), 1);
+        mbar_init(smem_u32(sw_bar), kConsumers);
         *abort_flag = 0;
         fence_mbar_init();
+        // Fill the ring (weights may be read before the dependency wait).
+        for (int st = 0; st < min(NS, nstages); ++st) issue(st, st);
     }
-    __syncthreads();
     griddep_launch_dependents();
 
-    // ------------------------------------------------------------ producer
-    if (warp == kConsumerWarps) {
-        const uint64_t pol = l2_evict_first_policy();
-        const uint8_t* base = a.W + row0 * RB + (int64_t)g0 * kGranBytes;
-        auto issue = [&](int st, int slot) {
-            const int r0 = st * pl.Rl;
-            const int nr = min(pl.Rl, nrows - r0);
-            const uint32_t dst = smem_u32(smem + slot * pl.stage_stride);
-            const uint32_t bar = smem_u32(full + slot);
-            mbar_arrive_expect_tx(bar, (uint32_t)(nr * RBp));
-            const uint8_t* src = base + (int64_t)r0 * RB;
-            if (pl.P == 1) {
-                bulk_g2s(dst, src, (uint32_t)(nr * RBp), bar, pol);
-            } else {
-                for (int r = 0; r < nr; ++r)
-                    bulk_g2s(dst + r * RBp, src + (int64_t)r * RB, (uint32_t)RBp, bar, pol);
-            }
-        };
-        // Fill the ring first (weights may be read before the dependency wait).
-        const int first = min(NS, nstages);
-        if (lane == 0)
-            for (int st = 0; st < first; ++st) issue(st, st);
-        // The idle lanes meanwhile cache the weight scales of this CTA's rows.
-        if (pl.P == 1) {
-            for (int r = lane; r < nrows; r += 32) {
-                if constexpr (kW4)
-                    sw_s[r] = static_cast<const float*>(a.wscale)[row0 + r];
-                else
-                    sw_s[r] = __half2float(static_cast<const __half*>(a.wscale)[row0 + r]);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(smem_u32(sw_bar));
-            int st = first, slot = 0;
-            uint32_t eph = 0;  // parity of the empty phase being waited for
-            for (; st < nstages; ++st) {
-                if (!wait_or_abort(smem_u32(empty + slot), eph, abort_flag, kErrEmptyWait)) break;
-                issue(st, slot);
-                if (++slot == NS) { slot = 0; eph ^= 1u; }
-            }
-            // No copy may still be landing in shared memory when the CTA exits.
-            for (int s2 = (st > NS ? st - NS : 0); s2 < st; ++s2)
-                if (!mbar_wait(smem_u32(full + s2 % NS), (s2 / NS) & 1))
-                    atomicOr(&g_device_error, kErrDrainWait);
-        }
-        return;
-    }
-
-    // ----------------------------------------------------------- consumers
     const int Cl = pl.Cl;
     const int i = tid >> pl.log2Cl;   // row-piece within a stage
     const int j = tid & (Cl - 1);     // column slot within the row-piece
@@ -234,6 +233,23 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
     const int64_t K = a.K;
     // granule columns j, j+Cl, ... below gp belong to this thread
     const int ncol = j < gp ? min(pl.S, (gp - j + Cl - 1) >> pl.log2Cl) : 0;
+
+    __syncthreads();  // barrier init visible to every thread
+    // Weight scales of this CTA's rows (weights may be read before the wait):
+    // asynchronous 4-byte copies whose completion arrives on sw_bar; only the
+    // threads that write outputs wait for it, right before their first one.
+    if constexpr (kW4) {
+        if (pl.P == 1)
+            for (int r = tid; r < nrows; r += kConsumers)
+            {
+                const int64_t n = row0 + r;
+                const int sg = segment_of(a, n);
+                cp_async_4(smem_u32(sw_s + r), static_cast<const float*>(a.wscale[sg]) + (n - a.off[sg]));
+            }
+        cp_async_mbar_arrive(smem_u32(sw_bar));
+    } else {
+        mbar_arrive(smem_u32(sw_bar));
+    }
 
     griddep_wait();  // activations, outputs and workspace from here on
 
@@ -250,10 +266,12 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
         const int64_t k0 = (int64_t)g0 * 32;
         const int kq = gp * 32;
         const int nv = (int)(K / 8);          // 16-byte vectors per activation row
-        // One-pass form: the thread's vectors of a single row stay in registers.
-        constexpr int XR = 10;
+        // One-pass form: all of the thread's vectors of the (single) row are
+        // loaded at once and stay in registers for the quantization.
+        constexpr int XR = MT == 1 ? 10 : 1;
         const bool one_pass = (MT == 1) && pl.P == 1 && nv <= XR * kConsumers;
-        uint4 xr[MT == 1 ? XR : 1];
+        const int nu = (nv + kConsumers - 1) / kConsumers;  // vectors per thread (uniform)
+        uint4 xr[XR];
         #pragma unroll
         for (int m = 0; m < MT; ++m) {
             __half2 hm = __float2half2_rn(0.f);
@@ -261,14 +279,18 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                 const uint4* xv = reinterpret_cast<const uint4*>(a.X + (int64_t)m * K);
                 if (MT == 1 && one_pass) {
                     #pragma unroll
-                    for (int u = 0; u < (MT == 1 ? XR : 1); ++u) {
+                    for (int u = 0; u < XR; ++u) {
+                        if (u >= nu) break;  // uniform: skips the unused unrolled steps
                         const int v = tid + u * kConsumers;
-                        if (v < nv) {
-                            xr[u] = xv[v];
-                            hm = absmax8(xr[u], hm);
-                        }
+                        xr[u] = v < nv ? xv[v] : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    #pragma unroll
+                    for (int u = 0; u < XR; ++u) {
+                        if (u >= nu) break;
+                        hm = absmax8(xr[u], hm);
                     }
                 } else {
+                    #pragma unroll 4
                     for (int v = tid; v < nv; v += kConsumers) hm = absmax8(xv[v], hm);
                 }
             }
@@ -291,13 +313,15 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
             if (m < M) {
                 if (MT == 1 && one_pass) {
                     #pragma unroll
-                    for (int u = 0; u < (MT == 1 ? XR : 1); ++u) {
+                    for (int u = 0; u < XR; ++u) {
+                        if (u >= nu) break;
                         const int v = tid + u * kConsumers;
-                        if (v < nv)
-                            *reinterpret_cast<uint2*>(act_s + 8 * v) = quant8(xr[u], sa_r[0], rs[0]);
+                        const uint2 qv = quant8(xr[u], sa_r[0], rs[0]);
+                        if (v < nv) *reinterpret_cast<uint2*>(act_s + 8 * v) = qv;
                     }
                 } else {
                     const uint4* xv = reinterpret_cast<const uint4*>(a.X + (int64_t)m * K + k0);
+                    #pragma unroll 4
                     for (int v = tid; v < kq / 8; v += kConsumers)
                         *reinterpret_cast<uint2*>(act_s + m * act_stride + 8 * v) =
                             quant8(xv[v], sa_r[m], rs[m]);
@@ -365,6 +389,13 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
         }
     }
 
+    if constexpr (!kW4) {
+        if (pl.P == 1)
+            for (int r = tid; r < nrows; r += kConsumers)
+                sw_s[r] = __half2float(static_cast<const __half*>(a.wscale[0])[row0 + r]);
+        named_bar_sync(1, kConsumers);  // scale cache visible to every thread
+    }
+
     // W4: the low nibbles enter the dot product biased by +8 (n ^ 8 = q + 8),
     // so each row's sum carries 8 * (sum of the even-k codes) too much.
     int corr[MT];
@@ -379,143 +410,186 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
         }
     }
 
+    // the weight-scale cache must have landed before any output is written
+    wait_or_abort(smem_u32(sw_bar), 0, abort_flag, kErrFullWait);
+
     // ------------------------------------------------------ streaming loop
-    AccT* red = reinterpret_cast<AccT*>(smem + pl.off_red);  // [2][warps][MT]
+    // Stages are consumed in batches of kBatch: per stage each thread only
+    // multiplies and accumulates; the cross-thread reduction and the outputs
+    // of a whole batch follow together, so their latencies overlap.
+    constexpr int kBatch = 4;
+    constexpr int NCH = MT == 1 ? 2 : 1;       // independent chains per sum
+    AccT* red = reinterpret_cast<AccT*>(smem + pl.off_red);  // [2][warps][kBatch][MT]
     const int wpr = Cl >> 5;                                  // warps per row-piece
-    const uint32_t ring0 = smem_u32(smem);
-    const uint32_t col0 = (uint32_t)(i * RBp + j * kGranBytes);
-    const uint32_t cstep = (uint32_t)(Cl * kGranBytes);
-    bool sw_ready = pl.P != 1;
+    // Every thread loads SMAX granules per row-piece; columns past this
+    // thread's last valid one are clamped to a valid address and multiply
+    // zero activations, so the loads need no branch and can all be issued
+    // before the arithmetic.
+    int coff[SMAX];
+    #pragma unroll
+    for (int s = 0; s < SMAX; ++s)
+        coff[s] = i * RBp + min(j + s * Cl, gp - 1) * kGranBytes;
     int slot = 0;
     uint32_t fph = 0;  // parity of the full phase being waited for
-    for (int st = 0; st < nstages; ++st) {
-        wait_or_abort(smem_u32(full + slot), fph, abort_flag, kErrFullWait);
-        const int r0 = st * pl.Rl;
-        const int nr = min(pl.Rl, nrows - r0);
-        // independent accumulator chains: W4 keeps the biased low-nibble and
-        // the x16 high-nibble sums apart; NCH chains of each
-        constexpr int NCH = MT == 1 ? 2 : 1;
-        AccT alo[MT][NCH], ahi[MT][NCH];
+    for (int sb = 0; sb < nstages; sb += kBatch) {
+        AccT part[kBatch][MT];
         #pragma unroll
-        for (int m = 0; m < MT; ++m) {
+        for (int d = 0; d < kBatch; ++d) {
             #pragma unroll
-            for (int h = 0; h < NCH; ++h) { alo[m][h] = 0; ahi[m][h] = 0; }
-        }
-        if (i < nr) {
-            const uint32_t wbase = ring0 + (uint32_t)(slot * pl.stage_stride) + col0;
-            #pragma unroll
-            for (int s = 0; s < SMAX; ++s) {
-                if (s < ncol) {
-                    const uint4 w4v = *reinterpret_cast<const uint4*>(
-                        smem + (wbase - ring0) + s * cstep);
-                    const uint32_t wv[4] = {w4v.x, w4v.y, w4v.z, w4v.w};
+            for (int m = 0; m < MT; ++m) part[d][m] = 0;
+            if (sb + d < nstages) {  // uniform over the CTA
+                wait_or_abort(smem_u32(full + slot), fph, abort_flag, kErrFullWait);
+                const uint8_t* stage = smem + slot * pl.stage_stride;
+                uint4 wg[SMAX];
+                #pragma unroll
+                for (int s = 0; s < SMAX; ++s)
+                    wg[s] = *reinterpret_cast<const uint4*>(stage + coff[s]);
+                __syncwarp();
+                if (lane == 0) {
+                    // the last warp done with this slot refills it with the
+                    // stage NS further on
+                    __threadfence_block();
+                    if (atomicAdd(released + slot, 1) == kConsumerWarps - 1) {
+                        released[slot] = 0;
+                        __threadfence_block();
+                        if (sb + d + NS < nstages && !*abort_flag) issue(sb + d + NS, slot);
+                    }
+                }
+                if (++slot == NS) { slot = 0; fph ^= 1u; }
+
+                AccT alo[MT][NCH], ahi[MT][NCH];
+                #pragma unroll
+                for (int m = 0; m < MT; ++m) {
                     #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        if constexpr (kW4) {
-                            // low nibbles: (n ^ 8) = q + 8 in [0, 15]; high
-                            // nibbles left in place read as int8 = 16 * q
-                            const uint32_t lo = (wv[t] ^ 0x08080808u) & 0x0F0F0F0Fu;
-                            const uint32_t hi = wv[t] & 0xF0F0F0F0u;
-                            #pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                AccT& cl = alo[m][t % NCH];
-                                AccT& ch = ahi[m][t % NCH];
-                                cl = __dp4a((int)lo, (int)act[m][s][t], cl);
-                                ch = __dp4a((int)hi, (int)act[m][s][4 + t], ch);
-                            }
-                        } else {
-                            // int8 code q -> fp32 exactly: the bits 0x4B0000uu
-                            // with uu = q + 128 encode 2^23 + q + 128.
-                            const uint32_t u = wv[t] ^ 0x80808080u;
-                            const float q0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)) - 8388736.f;
-                            const float q1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)) - 8388736.f;
-                            const float q2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)) - 8388736.f;
-                            const float q3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - 8388736.f;
-                            #pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                AccT& c0 = alo[m][t % NCH];
-                                AccT& c1 = ahi[m][t % NCH];
-                                c0 = fmaf(q0, __uint_as_float(act[m][s][4 * t + 0]), c0);
-                                c1 = fmaf(q1, __uint_as_float(act[m][s][4 * t + 1]), c1);
-                                c0 = fmaf(q2, __uint_as_float(act[m][s][4 * t + 2]), c0);
-                                c1 = fmaf(q3, __uint_as_float(act[m][s][4 * t + 3]), c1);
+                    for (int h = 0; h < NCH; ++h) { alo[m][h] = 0; ahi[m][h] = 0; }
+                }
+                #pragma unroll
+                for (int s = 0; s < SMAX; ++s) {
+                    if (s < pl.S) {  // uniform over the CTA
+                        const uint32_t wv[4] = {wg[s].x, wg[s].y, wg[s].z, wg[s].w};
+                        #pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            if constexpr (kW4) {
+                                // low nibbles: (n ^ 8) = q + 8 in [0, 15]; high
+                                // nibbles left in place read as int8 = 16 * q
+                                const uint32_t lo = (wv[t] ^ 0x08080808u) & 0x0F0F0F0Fu;
+                                const uint32_t hi = wv[t] & 0xF0F0F0F0u;
+                                #pragma unroll
+                                for (int m = 0; m < MT; ++m) {
+                                    AccT& cl = alo[m][t % NCH];
+                                    AccT& ch = ahi[m][t % NCH];
+                                    cl = __dp4a((int)lo, (int)act[m][s][t], cl);
+                                    ch = __dp4a((int)hi, (int)act[m][s][4 + t], ch);
+                                }
+                            } else {
+                                // int8 code q -> fp32 exactly: the bits 0x4B0000uu
+                                // with uu = q + 128 encode 2^23 + q + 128.
+                                const uint32_t u = wv[t] ^ 0x80808080u;
+                                const float q0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)) - 8388736.f;
+                                const float q1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)) - 8388736.f;
+                                const float q2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)) - 8388736.f;
+                                const float q3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - 8388736.f;
+                                #pragma unroll
+                                for (int m = 0; m < MT; ++m) {
+                                    AccT& c0 = alo[m][t % NCH];
+                                    AccT& c1 = ahi[m][t % NCH];
+                                    c0 = fmaf(q0, __uint_as_float(act[m][s][4 * t + 0]), c0);
+                                    c1 = fmaf(q1, __uint_as_float(act[m][s][4 * t + 1]), c1);
+                                    c0 = fmaf(q2, __uint_as_float(act[m][s][4 * t + 2]), c0);
+                                    c1 = fmaf(q3, __uint_as_float(act[m][s][4 * t + 3]), c1);
+                                }
                             }
                         }
                     }
                 }
+                #pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if constexpr (kW4) {
+                        int lo_sum = 0, hi_sum = 0;
+                        #pragma unroll
+                        for (int h = 0; h < NCH; ++h) { lo_sum += alo[m][h]; hi_sum += ahi[m][h]; }
+                        part[d][m] = lo_sum - corr[m] + (hi_sum >> 4);  // exact: hi_sum = 16 * sum
+                    } else {
+                        float sum = 0.f;
+                        #pragma unroll
+                        for (int h = 0; h < NCH; ++h) sum += alo[m][h] + ahi[m][h];
+                        part[d][m] = sum;
+                    }
+                }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(empty + slot));  // stage consumed
-        if (++slot == NS) { slot = 0; fph ^= 1u; }
 
-        AccT acc[MT];
-        #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if constexpr (kW4) {
-                int lo_sum = 0, hi_sum = 0;
-                #pragma unroll
-                for (int h = 0; h < NCH; ++h) { lo_sum += alo[m][h]; hi_sum += ahi[m][h]; }
-                acc[m] = lo_sum - corr[m] + (hi_sum >> 4);  // exact: hi_sum = 16 * sum
-            } else {
-                float sum = 0.f;
-                #pragma unroll
-                for (int h = 0; h < NCH; ++h) sum += alo[m][h] + ahi[m][h];
-                acc[m] = sum;
-            }
-        }
+        // reduce the batch across the Cl threads of each row-piece
         #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
             if (o < Cl) {
                 #pragma unroll
-                for (int m = 0; m < MT; ++m) acc[m] += __shfl_xor_sync(0xFFFFFFFFu, acc[m], o);
+                for (int d = 0; d < kBatch; ++d)
+                    #pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        part[d][m] += __shfl_xor_sync(0xFFFFFFFFu, part[d][m], o);
             }
         }
         if (wpr > 1) {
-            AccT* rbuf = red + (st & 1) * kConsumerWarps * MT;
+            AccT* rbuf = red + ((sb / kBatch) & 1) * kConsumerWarps * kBatch * MT;
             if (lane == 0) {
                 #pragma unroll
-                for (int m = 0; m < MT; ++m) rbuf[warp * MT + m] = acc[m];
+                for (int d = 0; d < kBatch; ++d)
+                    #pragma unroll
+                    for (int m = 0; m < MT; ++m) rbuf[(warp * kBatch + d) * MT + m] = part[d][m];
             }
             named_bar_sync(2, kConsumers);
             if (j == 0) {
                 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    AccT t = rbuf[warp * MT + m];
-                    for (int w = 1; w < wpr; ++w) t += rbuf[(warp + w) * MT + m];
-                    acc[m] = t;
-                }
+                for (int d = 0; d < kBatch; ++d)
+                    #pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        AccT t = rbuf[(warp * kBatch + d) * MT + m];
+                        for (int w = 1; w < wpr; ++w) t += rbuf[((warp + w) * kBatch + d) * MT + m];
+                        part[d][m] = t;
+                    }
             }
         }
-        if (j == 0 && i < nr) {
-            const int r = r0 + i;
-            const int64_t n = row0 + r;
-            if (pl.P == 1) {
-                if (!sw_ready) {
-                    wait_or_abort(smem_u32(sw_bar), 0, abort_flag, kErrFullWait);
-                    sw_ready = true;
-                }
-                const float swv = sw_s[r];
-                #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (m < M) {
-                        if constexpr (kW4) {
-                            a.Y[m * N + n] = __fmul_rn(__fmul_rn(__int2float_rn(acc[m]), swv), sa_r[m]);
-                            if (a.acc_out != nullptr) a.acc_out[m * N + n] = acc[m];
-                        } else {
-                            a.Y[m * N + n] = __fmul_rn(acc[m], swv);
+        if (j == 0) {
+            #pragma unroll
+            for (int d = 0; d < kBatch; ++d) {
+                const int r = (sb + d) * pl.Rl + i;   // row within this CTA's range
+                if (sb + d < nstages && r < nrows) {
+                    const int64_t n = row0 + r;
+                    if (pl.P == 1) {
+                        const float swv = sw_s[r];
+                        const int sg = segment_of(a, n);
+                        const int64_t Ng = a.off[sg + 1] - a.off[sg];
+                        float* Yp = a.Yg[sg] + (n - a.off[sg]);
+                        #pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            if (m < M) {
+                                if constexpr (kW4) {
+                                    Yp[m * Ng] = __fmul_rn(__fmul_rn(__int2float_rn(part[d][m]), swv), sa_r[m]);
+                                    if (a.acc_out != nullptr) a.acc_out[m * N + n] = part[d][m];
+                                } else {
+                                    Yp[m * Ng] = __fmul_rn(part[d][m], swv);
+                                }
+                            }
                         }
+                    } else {
+                        AccT* pbuf = static_cast<AccT*>(a.part);
+                        #pragma unroll
+                        for (int m = 0; m < MT; ++m)
+                            if (m < M) pbuf[((int64_t)p * M + m) * N + n] = part[d][m];
                     }
                 }
-            } else {
-                AccT* part = static_cast<AccT*>(a.part);
-                #pragma unroll
-                for (int m = 0; m < MT; ++m)
-                    if (m < M) part[((int64_t)p * M + m) * N + n] = acc[m];
             }
         }
     }
 
+    // After an abandoned wait, copies may still be landing: wait for them
+    // (bounded) so that none writes shared memory after the CTA exits.
+    if (*abort_flag && tid == 0) {
+        for (int s2 = (nstages > NS ? nstages - NS : 0); s2 < nstages; ++s2)
+            if (!mbar_wait(smem_u32(full + s2 % NS), (s2 / NS) & 1))
+                atomicOr(&g_device_error, kErrDrainWait);
+    }
     if (pl.P == 1) return;
 
     // ---------------------------------------------- split-K: last CTA sums
@@ -528,21 +602,24 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
     const AccT* part = static_cast<const AccT*>(a.part);
     for (int r = tid; r < nrows; r += kConsumers) {
         const int64_t n = row0 + r;
+        const int sg = segment_of(a, n);
+        const int64_t ng = n - a.off[sg];
+        const int64_t Ng = a.off[sg + 1] - a.off[sg];
         float swv;
         if constexpr (kW4)
-            swv = static_cast<const float*>(a.wscale)[n];
+            swv = static_cast<const float*>(a.wscale[sg])[ng];
         else
-            swv = __half2float(static_cast<const __half*>(a.wscale)[n]);
+            swv = __half2float(static_cast<const __half*>(a.wscale[sg])[ng]);
         #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m < M) {
                 AccT t = 0;
                 for (int q = 0; q < pl.P; ++q) t += __ldcg(part + ((int64_t)q * M + m) * N + n);
                 if constexpr (kW4) {
-                    a.Y[m * N + n] = __fmul_rn(__fmul_rn(__int2float_rn(t), swv), sa_r[m]);
+                    a.Yg[sg][m * Ng + ng] = __fmul_rn(__fmul_rn(__int2float_rn(t), swv), sa_r[m]);
                     if (a.acc_out != nullptr) a.acc_out[m * N + n] = t;
                 } else {
-                    a.Y[m * N + n] = __fmul_rn(t, swv);
+                    a.Yg[sg][m * Ng + ng] = __fmul_rn(t, swv);
                 }
             }
         }
@@ -584,17 +661,56 @@ static cudaError_t launch_one(const GemvArgs& args, unsigned flags, cudaStream_t
     return cudaLaunchKernelEx(&cfg, fn, args);
 }
 
+static void set_segments(GemvArgs& a, int G, const uint8_t* const* W, const void* const* s,
+                         const int64_t* Ns, float* const* Y) {
+    int64_t off = 0;
+    for (int k = 0; k < kMaxSegments; ++k) {
+        a.off[k] = off;
+        if (k < G) {
+            a.W[k] = W[k];
+            a.wscale[k] = s[k];
+            a.Yg[k] = Y[k];
+            off += Ns[k];
+        }
+    }
+    a.off[kMaxSegments] = off;
+    for (int k = G; k < kMaxSegments; ++k) a.off[k] = off;  // empty tail segments
+}
+
+cudaError_t launch_w4a8_grouped(const GemvPlan& pl, const uint16_t* X, int M, int64_t K, int G,
+                                const uint8_t* const* Wq, const float* const* sw,
+                                const int64_t* Ns, float* const* Y, void* ws, unsigned flags,
+                                cudaStream_t stream) {
+    GemvArgs a = {};
+    const void* s[kMaxSegments] = {};
+    for (int k = 0; k < G; ++k) s[k] = sw[k];
+    set_segments(a, G, Wq, s, Ns, Y);
+    a.X = reinterpret_cast<const __half*>(X);
+    a.tickets = static_cast<unsigned*>(ws);
+    a.part = ws ? static_cast<uint8_t*>(ws) + kTicketBytes : nullptr;
+    a.M = M;
+    a.K = (int)K;
+    a.N = (int)a.off[kMaxSegments];
+    a.pl = pl;
+    switch (pl.MT) {
+        case 1: return launch_one<true, 1, 8, true>(a, flags, stream);
+        case 2: return launch_one<true, 2, 4, true>(a, flags, stream);
+        case 4: return launch_one<true, 4, 2, true>(a, flags, stream);
+        case 8: return launch_one<true, 8, 1, true>(a, flags, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_w4a8(const GemvPlan& pl, bool fused, const uint16_t* X, const int8_t* Xq,
                         const float* sa, int M, int64_t K, const uint8_t* Wq, const float* sw,
                         int64_t N, float* Y, int32_t* acc_out, int8_t* Xq_out, float* sa_out,
                         void* ws, unsigned flags, cudaStream_t stream) {
     GemvArgs a = {};
-    a.W = Wq;
-    a.wscale = sw;
+    const void* s0 = sw;
+    set_segments(a, 1, &Wq, &s0, &N, &Y);
     a.Xq = Xq;
     a.sa = sa;
     a.X = reinterpret_cast<const __half*>(X);
-    a.Y = Y;
     a.acc_out = acc_out;
     a.Xq_out = Xq_out;
     a.sa_out = sa_out;
@@ -621,10 +737,10 @@ cudaError_t launch_w8a16(const GemvPlan& pl, const uint16_t* X, int M, int64_t K
                          const int8_t* Wq8, const uint16_t* sw16, int64_t N, float* Y, void* ws,
                          unsigned flags, cudaStream_t stream) {
     GemvArgs a = {};
-    a.W = reinterpret_cast<const uint8_t*>(Wq8);
-    a.wscale = sw16;
+    const uint8_t* w0 = reinterpret_cast<const uint8_t*>(Wq8);
+    const void* s0 = sw16;
+    set_segments(a, 1, &w0, &s0, &N, &Y);
     a.X = reinterpret_cast<const __half*>(X);
-    a.Y = Y;
     a.tickets = static_cast<unsigned*>(ws);
     a.part = ws ? static_cast<uint8_t*>(ws) + kTicketBytes : nullptr;
     a.M = M;

@@ -20,6 +20,10 @@ cudaError_t launch_w4a8(const GemvPlan& pl, bool fused, const uint16_t* X, const
                         const float* sa, int M, int64_t K, const uint8_t* Wq, const float* sw,
                         int64_t N, float* Y, int32_t* acc_out, int8_t* Xq_out, float* sa_out,
                         void* ws, unsigned flags, cudaStream_t stream);
+cudaError_t launch_w4a8_grouped(const GemvPlan& pl, const uint16_t* X, int M, int64_t K, int G,
+                                const uint8_t* const* Wq, const float* const* sw,
+                                const int64_t* Ns, float* const* Y, void* ws, unsigned flags,
+                                cudaStream_t stream);
 cudaError_t launch_w8a16(const GemvPlan& pl, const uint16_t* X, int M, int64_t K,
                          const int8_t* Wq8, const uint16_t* sw16, int64_t N, float* Y, void* ws,
                          unsigned flags, cudaStream_t stream);

@@ -15,7 +15,7 @@ namespace w4a8 {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;  // 256 consumer threads
-constexpr int kThreads = kConsumers + 32;        // + one producer warp
+constexpr int kThreads = kConsumers;             // thread 0 also issues the copies
 constexpr int kGranBytes = 16;
 constexpr int kMaxSplits = 16;
 constexpr int kMaxRowsPerCta = 4096;              // bounds the scale cache in smem
@@ -86,7 +86,14 @@ inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int
             if (u > bestU + 1e-9) { bestU = u; bestCl = Cl; bestS = S; }
         }
         if (bestCl < 0) continue;
-        const int cps = tu.ctas_per_sm > 0 ? tu.ctas_per_sm : 1;
+        // Two CTAs per SM double the consumer warps that hide the per-stage
+        // latency; keep one when a CTA would get fewer than two stages.
+        int cps = tu.ctas_per_sm;
+        if (cps <= 0) {
+            const int64_t gs2 = (int64_t)num_sms * 2 / P;
+            const int rl = kConsumers / bestCl;
+            cps = (gs2 >= 1 && N / gs2 >= 2 * rl) ? 2 : 1;
+        }
         int64_t Gs = (int64_t)num_sms * cps / P;
         if (Gs < 1) Gs = 1;
         if (Gs > N) Gs = N;
@@ -100,7 +107,7 @@ inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int
         // Streaming cost ~ granules per CTA; low lane utilisation only costs
         // when the integer pipe becomes the limit (larger M); a split pays a
         // partial-sum pass and an extra serial step at the end.
-        double cost = (double)rows_max * Gq;
+        double cost = (double)rows_max * Gq * cps / 2.0;  // per-SM share of the stream
         const double alu = 0.3 * pl.MT / bestU;
         if (alu > 1.0) cost *= alu;
         if (P > 1) cost = cost * 1.05 + 2800.0;
@@ -130,12 +137,12 @@ inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int
 
     const int sw_bytes = pl.P == 1 ? round_up(pl.rows_max * 4, 16) : 0;
     const int act_bytes = (w4 && fused) ? round_up(pl.MT * pl.Gq * 32, 128) : 0;
-    const int red_bytes = 2 * kConsumerWarps * pl.MT * 4;
+    const int red_bytes = 2 * kConsumerWarps * 4 * pl.MT * 4;  // [2][warps][batch 4][MT]
     const int max_bytes = kConsumerWarps * pl.MT * 4;
     for (;; --NS) {
         int off = NS * pl.stage_stride;
         pl.off_bars = off;
-        off += (2 * NS + 1) * 8;  // full[NS], empty[NS], scale-cache barrier
+        off += NS * 8 + 8 + NS * 4;  // full[NS], scale-cache mbarrier, released[NS]
         pl.off_sw = round_up(off, 16);
         off = pl.off_sw + sw_bytes;
         pl.off_act = round_up(off, 128);

@@ -148,6 +148,21 @@ int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, cons
                 int64_t N, float* Y, int8_t* Xq_out, float* sa_out, int32_t* acc_out,
                 void* ws, size_t ws_bytes, unsigned flags, void* stream);
 
+/* Grouped fused linear: G weight matrices that read the same activation
+ * (the query/key/value projections, or the gate and up projections of an
+ * MLP) in one launch, quantizing the activation once (the Jetson INT4 page,
+ * section 后续优化方向: cut the repeated quantization in QKV and the MLP).
+ *   X [M][K] binary16 in;  for g < G: Wq[g] [N[g]][K/2] uint8, sw[g] [N[g]]
+ *   fp32, Y[g] [M][N[g]] fp32 out; Wq, sw, N, Y are HOST arrays of G device
+ *   pointers / sizes.  Y[g] is bit-identical to w4a8_linear(X, Wq[g], sw[g]).
+ *   ws, ws_bytes: at least w4a8_workspace_bytes(M, K, N[0] + ... + N[G-1]).
+ * Requires 1 <= G <= W4A8_MAX_GROUP and the w4a8_linear limits with
+ * N = the sum of N[g]; X and every Wq[g] 16-byte aligned. */
+#define W4A8_MAX_GROUP 4
+int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const uint8_t* const* Wq,
+                        const float* const* sw, const int64_t* N, float* const* Y, void* ws,
+                        size_t ws_bytes, unsigned flags, void* stream);
+
 /* Fused linear that allocates nothing and takes no workspace.  The pages
  * have no counterpart; this is a calling convention for callers that cannot
  * provide device memory: code paths that must not allocate, such as an

@@ -79,6 +79,21 @@ def test_misaligned_pointers_rejected(L):
     assert L.w8a16_gemv(P16, 1, 32, P16 + 4, P16, 4, P16, None, 0, 0, None) == E
 
 
+def test_grouped_argument_checks(L):
+    import ctypes
+    arr = (ctypes.c_void_p * 2)(P16, P16)
+    ns = (ctypes.c_int64 * 2)(4, 4)
+    null_arr = (ctypes.c_void_p * 2)(P16, None)
+    assert L.w4a8_linear_grouped(P16, 1, 32, 0, arr, arr, ns, arr, None, 0, 0, None) == w4._binding.ERR_SHAPE
+    assert L.w4a8_linear_grouped(P16, 1, 32, 5, arr, arr, ns, arr, None, 0, 0, None) == w4._binding.ERR_SHAPE
+    assert L.w4a8_linear_grouped(P16, 1, 32, 2, arr, null_arr, ns, arr, None, 0, 0, None) == w4._binding.ERR_NULL
+    bad_n = (ctypes.c_int64 * 2)(4, 0)
+    assert L.w4a8_linear_grouped(P16, 1, 32, 2, arr, arr, bad_n, arr, None, 0, 0, None) == w4._binding.ERR_SHAPE
+    mis = (ctypes.c_void_p * 2)(P16, P16 + 8)
+    assert L.w4a8_linear_grouped(P16, 1, 32, 2, mis, arr, ns, arr, None, 0, 0, None) == w4._binding.ERR_ALIGN
+    assert L.w4a8_linear_grouped(None, 1, 32, 2, arr, arr, ns, arr, None, 0, 0, None) == w4._binding.ERR_NULL
+
+
 def test_tuning_validation():
     with pytest.raises(w4.W4A8Error):
         w4.w4a8_set_tuning(force_splits=17)

@@ -84,6 +84,40 @@ def test_qwen2_7b_linear_set_m1(w4, orc, idx):
     assert w4.w4a8_device_error() == 0
 
 
+def test_decode_step_as_benchmarked(w4, orc):
+    """One step exactly as bench.py runs it (grouped q/k/v and gate/up, PDL),
+    sampled rows of every output checked against the oracle."""
+    import bench
+    names = [l[0] for l in bench.LINEARS]
+    Wqs, sws, Ys = {}, {}, {}
+    for i, (name, K, N) in enumerate(bench.LINEARS):
+        W = synth.normal_gpu(bench.WEIGHT_SEED0 + i, (N, K), 0.02)
+        Wqs[name], sws[name] = w4.w4_quantize_weights(W)
+        del W
+    Xs = {}
+    for lname, members in bench.LAUNCHES:
+        K = bench.LINEARS[names.index(members[0])][1]
+        X = synth.activation(bench.activation_seed(members[0]), 1, K, outlier_frac=bench.OUTLIER_FRAC)
+        Xs[lname] = X
+        Xd = torch.from_numpy(X).cuda()
+        if len(members) == 1:
+            Ys[members[0]] = w4.w4a8_linear(Xd, Wqs[members[0]], sws[members[0]], flags=w4.LAUNCH_PDL)
+        else:
+            out = w4.w4a8_linear_grouped(Xd, [Wqs[n] for n in members], [sws[n] for n in members],
+                                         flags=w4.LAUNCH_PDL)
+            Ys.update(dict(zip(members, out)))
+    torch.cuda.synchronize()
+    for lname, members in bench.LAUNCHES:
+        for name in members:
+            i = names.index(name)
+            _, K, N = bench.LINEARS[i]
+            rows = sample_rows(N, 7000 + i, n=24)
+            Wq_ref, sw_ref = orc.w4_quantize(synth.weight_rows(bench.WEIGHT_SEED0 + i, N, K, rows))
+            Y_ref = orc.w4a8_linear(Xs[lname], Wq_ref, sw_ref)[0]
+            assert np.array_equal(bits(Ys[name].cpu().numpy()[:, rows]), bits(Y_ref)), name
+    assert w4.w4a8_device_error() == 0
+
+
 @pytest.mark.parametrize("M", [1, 2, 4, 8])
 @pytest.mark.parametrize("name", ["gate", "down"])
 def test_skinny_batch_sweep(w4, orc, M, name):

@@ -297,3 +297,46 @@ def test_gpu_generator_matches_host(w4):
     assert np.array_equal(bits(g), bits(synth.normal(1234, (3000, 64), 0.02)))
     g = synth.normal_gpu(99, (1000,), 1.0, offset=(1 << 32) - 1000).cpu().numpy()
     assert np.array_equal(bits(g), bits(synth.normal(99, (1000,), 1.0, offset=(1 << 32) - 1000)))
+
+
+# ---------------------------------------------------------------------------
+# grouped launch: several weight matrices sharing the activation
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,Ns,splits", [
+    (1, 3584, (3584, 512, 512), 0),      # q/k/v shaped
+    (3, 896, (5, 77, 300, 1), 0),        # ragged, a one-row segment
+    (2, 1024, (33, 600), 3),             # split-K partials span segments
+    (1, 3584, (100, 7, 2000), 4),
+    (8, 64, (17, 1, 40, 9), 0),
+    (1, 18944, (300, 50), 0),
+])
+def test_w4a8_linear_grouped(w4, orc, M, K, Ns, splits):
+    w4.w4a8_set_tuning(force_splits=splits)
+    X = synth.activation(500 + K, M, K, outlier_frac=0.001)
+    refs, Wqs, sws = [], [], []
+    for g, N in enumerate(Ns):
+        W = weights(N, K, 600 + 7 * g + N)
+        Wq_ref, sw_ref = orc.w4_quantize(W)
+        refs.append(orc.w4a8_linear(X, Wq_ref, sw_ref)[0])
+        Wq, sw = w4.w4_quantize_weights(to_dev(W))
+        Wqs.append(Wq)
+        sws.append(sw)
+    for rep in range(2):
+        Ys = w4.w4a8_linear_grouped(to_dev(X), Wqs, sws, flags=w4.LAUNCH_PDL if rep else 0)
+        torch.cuda.synchronize()
+        for Y, ref in zip(Ys, refs):
+            assert np.array_equal(bits(Y.cpu().numpy()), bits(ref))
+
+
+def test_w4a8_linear_grouped_rejects_bad_groups(w4):
+    X = torch.zeros((1, 64), dtype=torch.float16, device="cuda")
+    Wq = torch.zeros((4, 32), dtype=torch.uint8, device="cuda")
+    sw = torch.zeros((4,), dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        w4.w4a8_linear_grouped(X, [Wq] * 5, [sw] * 5)
+    flat = torch.zeros(4 * 32 + 8, dtype=torch.uint8, device="cuda")
+    Wq_mis = flat[8:].view(4, 32)                                  # 8 bytes off 16
+    with pytest.raises(w4.W4A8Error) as e:
+        w4.w4a8_linear_grouped(X, [Wq, Wq_mis], [sw, sw])
+    assert e.value.status == 2
