@@ -81,6 +81,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-busy-s", type=float, default=0.6,
                     help="keep the GPU busy at least this long before timing (clock samples)")
+    ap.add_argument("--only", choices=[l[0] for l in LAUNCHES], default=None,
+                    help="profiling aid: time one launch kind alone, eagerly, without PDL "
+                         "(not the headline metric)")
     return ap.parse_args()
 
 
@@ -496,9 +499,66 @@ def run_ours(args, world, rank):
         print(json.dumps(line), flush=True)
 
 
+def run_only(args, lname):
+    """Profiling aid: `warmup` then `steps` eager launches of one launch kind on
+    two alternating weight copies, CUDA events around the timed launches."""
+    import torch
+    import synth
+    import bit_weight_quantized_w4a8_gb300 as w4
+    w4.build()
+    w4.w4a8_set_tuning(reset=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    members = dict(LAUNCHES)[lname]
+    names = [l[0] for l in LINEARS]
+    idx = [names.index(n) for n in members]
+    K = LINEARS[idx[0]][1]
+    X = torch.from_numpy(synth.activation(activation_seed(members[0]), 1, K,
+                                          outlier_frac=OUTLIER_FRAC)).to(dev)
+    copies = []
+    for c in range(2):
+        ws_, ss_ = [], []
+        for i in idx:
+            W = synth.normal_gpu(WEIGHT_SEED0 + i, (LINEARS[i][2], K), 0.02, device=dev)
+            Wq, sw = w4.w4_quantize_weights(W)
+            del W
+            ws_.append(Wq)
+            ss_.append(sw)
+        copies.append((ws_, ss_))
+    Ys = [torch.empty((1, LINEARS[i][2]), dtype=torch.float32, device=dev) for i in idx]
+    wsb = torch.zeros(max(w4.w4a8_workspace_bytes(1, K, sum(LINEARS[i][2] for i in idx)), 4096),
+                      dtype=torch.uint8, device=dev)
+
+    def one(k):
+        Wqs, sws = copies[k % 2]
+        if len(idx) == 1:
+            w4.w4a8_linear(X, Wqs[0], sws[0], Y=Ys[0], ws=wsb)
+        else:
+            w4.w4a8_linear_grouped(X, Wqs, sws, Ys=Ys, ws=wsb)
+
+    for k in range(args.warmup):
+        one(k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(args.steps):
+        one(k)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / args.steps * 1e3
+    nbytes = sum(weight_bytes(K, LINEARS[i][2]) for i in idx)
+    print(json.dumps({"only": lname, "members": list(members), "steps": args.steps,
+                      "us_per_launch": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+                      "note": "eager launches, host launch gaps included; profiling aid"}),
+          flush=True)
+
+
 def main():
     args = parse()
     world, rank, _ = dist_setup(args)
+    if args.only is not None:
+        if rank == 0:
+            run_only(args, args.only)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
     else:
