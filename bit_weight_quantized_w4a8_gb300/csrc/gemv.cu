@@ -97,44 +97,57 @@ __device__ __forceinline__ __half2 absmax8(uint4 h, __half2 m) {
     return m;
 }
 
-// INT8 code of one activation value, clamp(round_half_away(x / s), +-127)
-// with the IEEE quotient x / s, given r = rcp_rn(s) and s > 0.
-// t = x * r differs from x / s by at most |x/s| * 2^-23 (two roundings) and
-// the IEEE quotient differs from x / s by at most |x/s| * 2^-24, so for
-// |x/s| <= 129 the two lie within 2^-15 of each other.  When t is more than
-// 2^-14 away from every half-integer, both therefore have the same nearest
-// integer and neither is a tie: rint(t) is the answer.  The rare remaining
-// cases take the IEEE division.  rint(t) for |t| < 2^22 is (t + 1.5*2^23)
-// - 1.5*2^23 in round-to-nearest, and the integer sits in the low bits of
-// t + 1.5*2^23, so no conversion instruction is needed.
-__device__ __noinline__ int quant_near_tie(float x, float s) {
-    return static_cast<int>(roundf(__fdiv_rn(x, s)));  // kept out of line: rarely taken
+// Activation codes, clamp(round_half_away(x / s), +-127) with the IEEE
+// quotient x / s, for 8 binary16 values at once, split by parity: .x holds
+// the codes of elements 0, 2, 4, 6 and .y those of 1, 3, 5, 7 (low byte
+// first), the order in which the packed weights present them.
+//
+// Exact slow form: one IEEE division and roundf per value.
+__device__ __noinline__ uint2 quant8_split_exact(uint4 h, float s) {
+    if (!(s > 0.f)) return make_uint2(0u, 0u);
+    const __half* p = reinterpret_cast<const __half*>(&h);
+    uint32_t w[2] = {0u, 0u};
+    #pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        int q = static_cast<int>(roundf(__fdiv_rn(__half2float(p[k]), s)));
+        q = min(max(q, -127), 127);
+        w[k & 1] |= (uint32_t)(q & 0xFF) << (8 * (k >> 1));
+    }
+    return make_uint2(w[0], w[1]);
 }
 
-__device__ __forceinline__ int quant_i8(float x, float s, float r) {
+// Fast form, given r_lo and r_hi, rcp_rn(s) scaled by 1 -+ 2^-21 and
+// rounded (both 0 when s = 0).  They bracket 1/s with a relative margin of
+// more than 2^-22 on each side, so for x != 0 the IEEE quotient x / s (within
+// 2^-24 relative of the exact one) lies strictly between x * r_lo and
+// x * r_hi.  With M = 1.5 * 2^23, fma(x, r, M) holds rint(x * r) of the exact
+// product in the low bits of its encoding (|x * r| < 2^22).  When the two
+// ends round to the same integer k, both lie in [k - 1/2, k + 1/2] and the
+// quotient strictly inside, so k is the code and no tie is involved; since
+// |x| <= 127 * s up to one rounding of s, |k| <= 127 needs no clamp.  A
+// vector in which some value's ends disagree (a half-integer between them,
+// about one value in 10^4 at most) takes the exact form.
+__device__ __forceinline__ uint2 quant8_split(uint4 h, float s, float r_lo, float r_hi) {
     constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    const float t = __fmul_rn(x, r);
-    const float y = __fadd_rn(t, kMagic);
-    const float ti = __fsub_rn(y, kMagic);
-    int q = __float_as_int(y) - 0x4B400000;
-    if (!(fabsf(__fsub_rn(t, ti)) < 0.5f - 0x1p-14f)) q = quant_near_tie(x, s);
-    return min(max(q, -127), 127);
-}
-
-// 8 binary16 values -> 8 INT8 codes, packed in order.
-__device__ __forceinline__ uint2 quant8(uint4 h, float s, float r) {
-    if (s == 0.f) return make_uint2(0u, 0u);
     const __half2* p = reinterpret_cast<const __half2*>(&h);
-    int q[8];
+    uint32_t y[8];
+    uint32_t diff = 0u;
     #pragma unroll
     for (int t = 0; t < 4; ++t) {
         const float2 f = __half22float2(p[t]);
-        q[2 * t] = quant_i8(f.x, s, r);
-        q[2 * t + 1] = quant_i8(f.y, s, r);
+        const uint32_t a0 = __float_as_uint(__fmaf_rn(f.x, r_lo, kMagic));
+        const uint32_t b0 = __float_as_uint(__fmaf_rn(f.x, r_hi, kMagic));
+        const uint32_t a1 = __float_as_uint(__fmaf_rn(f.y, r_lo, kMagic));
+        const uint32_t b1 = __float_as_uint(__fmaf_rn(f.y, r_hi, kMagic));
+        diff |= (a0 ^ b0) | (a1 ^ b1);
+        y[2 * t] = a0;
+        y[2 * t + 1] = a1;
     }
-    const uint32_t lo = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
-    const uint32_t hi = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
-    return make_uint2(lo, hi);
+    if (diff != 0u) return quant8_split_exact(h, s);
+    // the low byte of y is k modulo 256, the code's two's complement byte
+    const uint32_t ev = __byte_perm(__byte_perm(y[0], y[2], 0x0040), __byte_perm(y[4], y[6], 0x0040), 0x5410);
+    const uint32_t od = __byte_perm(__byte_perm(y[1], y[3], 0x0040), __byte_perm(y[5], y[7], 0x0040), 0x5410);
+    return make_uint2(ev, od);
 }
 
 // 32 activation codes in natural order (two 16-byte words) -> the lane order
@@ -225,6 +238,15 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
         for (int st = 0; st < min(NS, nstages); ++st) issue(st, st);
     }
     griddep_launch_dependents();
+    // Warm the L2 with the activation lines: a prefetch binds no value, so
+    // it is safe before the dependency wait even if the previous kernel
+    // is still writing them.
+    {
+        const void* xp = (kW4 && !kFused) ? static_cast<const void*>(a.Xq) : static_cast<const void*>(a.X);
+        const int64_t xbytes = (int64_t)a.M * a.K * ((kW4 && !kFused) ? 1 : 2);
+        for (int64_t o = (int64_t)threadIdx.x * 128; o < xbytes; o += (int64_t)kThreads * 128)
+            prefetch_l2(static_cast<const uint8_t*>(xp) + o);
+    }
 
     const int Cl = pl.Cl;
     const int i = tid >> pl.log2Cl;   // row-piece within a stage
@@ -259,81 +281,97 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
     if constexpr (kW4 && kFused) {
         // Dynamic activation quantization fused into the linear (the Jetson
         // INT4 page, section 后续优化方向).  Every CTA derives the same s_a
-        // from the whole row, then quantizes only its own K piece.
+        // from the whole row, then quantizes only its own K piece into
+        // shared memory, already in the lane order of the packed weights:
+        // per row piece, plane 0 holds granule c's even-k codes as 16 bytes
+        // at 16c, plane 1 its odd-k codes at 16 (Gq + c), so that threads of
+        // consecutive columns read consecutive 16-byte words.
         float* max_s = reinterpret_cast<float*>(smem + pl.off_max);
-        uint8_t* act_s = smem + pl.off_act;
-        const int act_stride = pl.Gq * 32;
-        const int64_t k0 = (int64_t)g0 * 32;
-        const int kq = gp * 32;
-        const int nv = (int)(K / 8);          // 16-byte vectors per activation row
-        // One-pass form: all of the thread's vectors of the (single) row are
-        // loaded at once and stay in registers for the quantization.
-        constexpr int XR = MT == 1 ? 10 : 1;
-        const bool one_pass = (MT == 1) && pl.P == 1 && nv <= XR * kConsumers;
-        const int nu = (nv + kConsumers - 1) / kConsumers;  // vectors per thread (uniform)
-        uint4 xr[XR];
-        #pragma unroll
-        for (int m = 0; m < MT; ++m) {
+        uint32_t* act_w = reinterpret_cast<uint32_t*>(smem + pl.off_act);
+        const int act_words = pl.Gq * 8;       // words per activation row piece
+        const int plane = pl.Gq * 4;           // words per plane
+        const int nv = (int)(K / 8);           // 16-byte vectors per activation row
+        const int v0 = g0 * 4;                 // first vector of this piece
+        const int nvq = gp * 4;                // vectors in this piece
+        uint4* x_s = reinterpret_cast<uint4*>(smem + pl.off_x);
+        // vector v of the piece = codes 8t..8t+7 of granule v / 4: its even
+        // codes are word v of plane 0, its odd codes word v of plane 1
+        auto quant_piece = [&](const uint4* src, uint32_t* dst, float sa, float r_lo, float r_hi) {
+            #pragma unroll 2
+            for (int v = tid; v < nvq; v += kConsumers) {
+                const uint2 q = quant8_split(src[v], sa, r_lo, r_hi);
+                dst[v] = q.x;
+                dst[plane + v] = q.y;
+            }
+        };
+        const bool staged = MT == 1 && pl.x_bytes > 0;
+        if (staged) {
+            // M == 1, short row: all loads in flight at once, the row kept
+            // in shared memory for the quantization pass
+            constexpr int XR = kMaxXStage / 16 / kConsumers;
+            const uint4* xv = reinterpret_cast<const uint4*>(a.X);
+            uint4 xr[XR];
+            #pragma unroll
+            for (int u = 0; u < XR; ++u) {
+                if (u * kConsumers >= nv) break;  // uniform
+                const int v = tid + u * kConsumers;
+                if (v < nv) xr[u] = xv[v];
+            }
             __half2 hm = __float2half2_rn(0.f);
-            if (m < M) {
-                const uint4* xv = reinterpret_cast<const uint4*>(a.X + (int64_t)m * K);
-                if (MT == 1 && one_pass) {
-                    #pragma unroll
-                    for (int u = 0; u < XR; ++u) {
-                        if (u >= nu) break;  // uniform: skips the unused unrolled steps
-                        const int v = tid + u * kConsumers;
-                        xr[u] = v < nv ? xv[v] : make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    #pragma unroll
-                    for (int u = 0; u < XR; ++u) {
-                        if (u >= nu) break;
-                        hm = absmax8(xr[u], hm);
-                    }
-                } else {
-                    #pragma unroll 4
-                    for (int v = tid; v < nv; v += kConsumers) hm = absmax8(xv[v], hm);
+            #pragma unroll
+            for (int u = 0; u < XR; ++u) {
+                if (u * kConsumers >= nv) break;
+                const int v = tid + u * kConsumers;
+                if (v < nv) {
+                    hm = absmax8(xr[u], hm);
+                    x_s[v] = xr[u];
                 }
             }
             float mx = fmaxf(__low2float(hm), __high2float(hm));
             mx = warp_max(mx);
-            if (lane == 0) max_s[warp * MT + m] = mx;
+            if (lane == 0) max_s[warp] = mx;
+        } else {
+            #pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                __half2 hm = __float2half2_rn(0.f);
+                if (m < M) {
+                    const uint4* xv = reinterpret_cast<const uint4*>(a.X + (int64_t)m * K);
+                    #pragma unroll 4
+                    for (int v = tid; v < nv; v += kConsumers) hm = absmax8(xv[v], hm);
+                }
+                float mx = fmaxf(__low2float(hm), __high2float(hm));
+                mx = warp_max(mx);
+                if (lane == 0) max_s[warp * MT + m] = mx;
+            }
         }
         named_bar_sync(1, kConsumers);
-        float rs[MT];
         #pragma unroll
         for (int m = 0; m < MT; ++m) {
             float mx = 0.f;
             #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) mx = fmaxf(mx, max_s[w * MT + m]);
             sa_r[m] = __fdiv_rn(mx, 127.f);
-            rs[m] = sa_r[m] > 0.f ? __frcp_rn(sa_r[m]) : 0.f;
-        }
-        #pragma unroll
-        for (int m = 0; m < MT; ++m) {
+            const float rs = sa_r[m] > 0.f ? __frcp_rn(sa_r[m]) : 0.f;
+            const float r_lo = __fmul_rn(rs, 1.f - 0x1p-21f);
+            const float r_hi = __fmul_rn(rs, 1.f + 0x1p-21f);
             if (m < M) {
-                if (MT == 1 && one_pass) {
-                    #pragma unroll
-                    for (int u = 0; u < XR; ++u) {
-                        if (u >= nu) break;
-                        const int v = tid + u * kConsumers;
-                        const uint2 qv = quant8(xr[u], sa_r[0], rs[0]);
-                        if (v < nv) *reinterpret_cast<uint2*>(act_s + 8 * v) = qv;
-                    }
-                } else {
-                    const uint4* xv = reinterpret_cast<const uint4*>(a.X + (int64_t)m * K + k0);
-                    #pragma unroll 4
-                    for (int v = tid; v < kq / 8; v += kConsumers)
-                        *reinterpret_cast<uint2*>(act_s + m * act_stride + 8 * v) =
-                            quant8(xv[v], sa_r[m], rs[m]);
-                }
+                if (staged)
+                    quant_piece(x_s + v0, act_w, sa_r[m], r_lo, r_hi);
+                else
+                    quant_piece(reinterpret_cast<const uint4*>(a.X + (int64_t)m * K) + v0,
+                                act_w + m * act_words, sa_r[m], r_lo, r_hi);
             }
         }
         named_bar_sync(1, kConsumers);
         if (a.Xq_out != nullptr && rb == 0) {
-            for (int m = 0; m < M; ++m)
-                for (int v = tid; v < kq / 16; v += kConsumers)
-                    *reinterpret_cast<uint4*>(a.Xq_out + (int64_t)m * K + k0 + 16 * v) =
-                        *reinterpret_cast<const uint4*>(act_s + m * act_stride + 16 * v);
+            for (int m = 0; m < M; ++m) {
+                const uint32_t* src = act_w + m * act_words;
+                for (int v = tid; v < nvq; v += kConsumers) {
+                    const uint32_t e = src[v], o = src[plane + v];
+                    *reinterpret_cast<uint2*>(a.Xq_out + (int64_t)m * K + 8 * (int64_t)(v0 + v)) =
+                        make_uint2(__byte_perm(e, o, 0x5140), __byte_perm(e, o, 0x7362));
+                }
+            }
         }
         if (a.sa_out != nullptr && blockIdx.x == 0) {
             #pragma unroll
@@ -346,8 +384,10 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
             for (int s = 0; s < SMAX; ++s) {
                 const int c = j + s * Cl;
                 if (m < M && s < ncol) {
-                    const uint4* src = reinterpret_cast<const uint4*>(act_s + m * act_stride + 32 * c);
-                    permute_act(src[0], src[1], act[m][s]);
+                    const uint4* src = reinterpret_cast<const uint4*>(act_w + m * act_words);
+                    const uint4 e = src[c], o = src[pl.Gq + c];
+                    act[m][s][0] = e.x; act[m][s][1] = e.y; act[m][s][2] = e.z; act[m][s][3] = e.w;
+                    act[m][s][4] = o.x; act[m][s][5] = o.y; act[m][s][6] = o.z; act[m][s][7] = o.w;
                 } else {
                     #pragma unroll
                     for (int t = 0; t < kActWords; ++t) act[m][s][t] = 0u;

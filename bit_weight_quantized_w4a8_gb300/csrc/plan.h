@@ -20,6 +20,10 @@ constexpr int kGranBytes = 16;
 constexpr int kMaxSplits = 16;
 constexpr int kMaxRowsPerCta = 4096;              // bounds the scale cache in smem
 constexpr int kMaxSmem = 232448;                  // 227 KB opt-in limit per CTA
+constexpr int kMaxSmem2 = 233472 / 2 - 1024;      // per CTA with two CTAs on an SM
+// A single fp16 activation row up to this size is staged in shared memory
+// (fused W4A8, M == 1).
+constexpr int kMaxXStage = 40960;
 constexpr int kDefaultRingBytes = 96 * 1024;
 // Split-K workspace layout: arrival counters first, at a fixed place, so any
 // call leaves them zero for the next call whatever its shape; partials after.
@@ -40,7 +44,9 @@ struct GemvPlan {
     int rows_max;      // most rows any CTA streams
     int NS;            // ring stages
     int stage_stride;  // bytes per ring stage (multiple of 128)
-    int off_bars, off_sw, off_act, off_red, off_max, off_flag;
+    int cps;           // CTAs per SM the grid was sized for
+    int x_bytes;       // staged activation row (0: read from global memory)
+    int off_bars, off_sw, off_x, off_act, off_red, off_max, off_flag;
     int smem;          // dynamic shared memory bytes
     size_t ws_bytes;   // workspace: kTicketBytes of counters + [P][M][N] x 4
                        // bytes of partials; 0 when P == 1
@@ -114,6 +120,7 @@ inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int
         if (cost < best_cost) {
             best_cost = cost;
             found = true;
+            pl.cps = cps;
             pl.P = P;
             pl.Gq = Gq;
             pl.Cl = bestCl;
@@ -137,14 +144,20 @@ inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int
 
     const int sw_bytes = pl.P == 1 ? round_up(pl.rows_max * 4, 16) : 0;
     const int act_bytes = (w4 && fused) ? round_up(pl.MT * pl.Gq * 32, 128) : 0;
+    pl.x_bytes = (w4 && fused && pl.MT == 1 && 2 * K <= kMaxXStage) ? (int)(2 * K) : 0;
     const int red_bytes = 2 * kConsumerWarps * 4 * pl.MT * 4;  // [2][warps][batch 4][MT]
     const int max_bytes = kConsumerWarps * pl.MT * 4;
+    // Shrink the ring until the CTA fits beside its sibling(s) on an SM; if
+    // even two stages do not fit, fall back to the one-CTA limit.
+    const int limit = (pl.cps >= 2) ? kMaxSmem2 : kMaxSmem;
     for (;; --NS) {
         int off = NS * pl.stage_stride;
         pl.off_bars = off;
         off += NS * 8 + 8 + NS * 4;  // full[NS], scale-cache mbarrier, released[NS]
         pl.off_sw = round_up(off, 16);
         off = pl.off_sw + sw_bytes;
+        pl.off_x = round_up(off, 128);
+        off = pl.off_x + pl.x_bytes;
         pl.off_act = round_up(off, 128);
         off = pl.off_act + act_bytes;
         pl.off_red = round_up(off, 16);
@@ -154,7 +167,7 @@ inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int
         pl.off_flag = round_up(off, 16);
         off = pl.off_flag + 16;
         pl.smem = round_up(off, 128);
-        if (pl.smem <= kMaxSmem) break;
+        if (pl.smem <= limit || (NS <= 2 && pl.smem <= kMaxSmem)) break;
         if (NS <= 2) return false;
     }
     pl.NS = NS;

@@ -7,8 +7,7 @@
 namespace w4a8 {
 
 // Device error word bits (see w4a8_device_error in the C header).
-constexpr unsigned kErrFullWait = 1u;   // consumer waited too long for data
-constexpr unsigned kErrEmptyWait = 2u;  // producer waited too long for a slot
+constexpr unsigned kErrFullWait = 1u;   // consumer waited too long for weight data
 constexpr unsigned kErrDrainWait = 4u;  // exit wait for in-flight copies ran out
 
 // Every device-side wait gives up after this many nanoseconds.
@@ -82,6 +81,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// Brings the 128-byte line holding `p` into L2; no value is read.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // Programmatic dependent launch: block until the preceding kernel on the

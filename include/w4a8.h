@@ -215,8 +215,8 @@ int w8a16_gemv(const uint16_t* X, int64_t M, int64_t K, const int8_t* Wq8,
 const char* w4a8_last_error(void);
 
 /* Copies the current device's error word into *flags and clears it.  Bit 0:
- * a consumer wait for weight data ran out; bit 1: a producer wait for a
- * free buffer ran out; bit 2: a wait for in-flight copies at exit ran out.
+ * a wait for weight data ran out; bit 1: unused; bit 2: a wait for
+ * in-flight copies at exit ran out.
  * Synchronises `stream` first.  Returns W4A8_OK or W4A8_ERR_CUDA. */
 int w4a8_device_error(unsigned* flags, void* stream);
 

@@ -181,6 +181,43 @@ def test_w4a8_split_k(w4, orc, splits, fused):
         check_w4a8(w4, orc, M, K, N, seed + 1, fused=fused)  # tickets were reset
 
 
+def tie_activation(M, K, seed):
+    """Activation rows whose scale is exactly 1/128 (max|x| = 127/128) and
+    whose values are mostly exact half-integers of that scale, (2k+1)/256,
+    so x / s_a lands on a tie; the rest are ordinary values."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ties = (2 * rng.integers(0, 127, size=(M, K)) + 1) / 256.0 * rng.choice([-1.0, 1.0], size=(M, K))
+    plain = np.clip(rng.normal(0.0, 0.3, size=(M, K)), -0.98, 0.98)
+    X = np.where(rng.random((M, K)) < 0.5, ties, plain).astype(np.float16)
+    X[:, rng.integers(0, K)] = np.float16(127.0 / 128.0)
+    return X
+
+
+@pytest.mark.parametrize("M,K,N,splits", [(1, 3584, 300, 0), (1, 3584, 300, 3), (2, 896, 200, 0),
+                                          (1, 131072, 4, 0)])
+def test_w4a8_fused_ties(w4, orc, M, K, N, splits):
+    """Ties (and vectors mixing ties with ordinary values) take the exact
+    division path of the fused quantizer; every code must match the oracle,
+    halves rounded away from zero."""
+    if splits:
+        w4.w4a8_set_tuning(force_splits=splits)
+    X = tie_activation(M, K, 90 + K + M)
+    W = weights(N, K, 91)
+    Wq_ref, sw_ref = orc.w4_quantize(W)
+    Y_ref, Xq_ref, sa_ref, _ = orc.w4a8_linear(X, Wq_ref, sw_ref)
+    assert np.all(sa_ref == np.float32(1.0 / 128.0))
+    Wq, sw = w4.w4_quantize_weights(to_dev(W))
+    Xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    sa = torch.empty((M,), dtype=torch.float32, device="cuda")
+    Y = w4.w4a8_linear(to_dev(X), Wq, sw, Xq_out=Xq, sa_out=sa)
+    Xq2, sa2 = w4.act_quantize_i8(to_dev(X))
+    torch.cuda.synchronize()
+    assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
+    assert np.array_equal(Xq2.cpu().numpy(), Xq_ref)
+    assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
+    assert np.array_equal(bits(Y.cpu().numpy()), bits(Y_ref))
+
+
 @pytest.mark.parametrize("cl", [1, 2, 8, 32, 64, 128, 256])
 def test_w4a8_threads_per_row(w4, orc, cl):
     w4.w4a8_set_tuning(force_threads_per_row=cl)
