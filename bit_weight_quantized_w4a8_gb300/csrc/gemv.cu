@@ -170,7 +170,40 @@ __device__ __forceinline__ int segment_of(const GemvArgs& a, int64_t n) {
     return g;
 }
 
-template <bool kW4, int MT, int SMAX, bool kFused>
+// Stage `st` of a CTA's weight stream (rows row0 + st * Rl ...) into ring
+// slot `slot`: one 1-D bulk copy per run of whole rows, cut where a segment
+// ends, or one copy per row-piece when K is split.  (Inlined: a call on the
+// refill path costs register spills and delays the refill.)
+__device__ __forceinline__ void issue_stage(const GemvArgs& a, uint8_t* smem, int st, int slot,
+                                         int64_t row0, int nrows, int g0, uint64_t pol) {
+    const GemvPlan& pl = a.pl;
+    const int RBp = min(pl.Gq, pl.Gt - g0) * kGranBytes;  // bytes of one row-piece
+    const int64_t RB = (int64_t)pl.Gt * kGranBytes;
+    const int r0 = st * pl.Rl;
+    const int nr = min(pl.Rl, nrows - r0);
+    const uint32_t dst = smem_u32(smem + slot * pl.stage_stride);
+    const uint32_t bar = smem_u32(smem + pl.off_bars + 8 * slot);
+    mbar_arrive_expect_tx(bar, (uint32_t)(nr * RBp));
+    int64_t n = row0 + r0;
+    const int64_t n_end = n + nr;
+    while (n < n_end) {
+        const int sg = segment_of(a, n);
+        const int64_t run = min(n_end, a.off[sg + 1]) - n;
+        const uint8_t* src = a.W[sg] + (n - a.off[sg]) * RB + (int64_t)g0 * kGranBytes;
+        const uint32_t d = dst + (uint32_t)((n - row0 - r0) * RBp);
+        if (pl.P == 1) {
+            bulk_g2s(d, src, (uint32_t)(run * RBp), bar, pol);
+        } else {
+            for (int r = 0; r < run; ++r)
+                bulk_g2s(d + r * RBp, src + (int64_t)r * RB, (uint32_t)RBp, bar, pol);
+        }
+        n += run;
+    }
+}
+
+// SMAX bounds the granule columns per thread; kExactS says the plan uses
+// exactly SMAX of them (no per-column test in the loop).
+template <bool kW4, int MT, int SMAX, bool kFused, bool kExactS>
 __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
     using AccT = typename std::conditional<kW4, int, float>::type;
     constexpr int kActWords = kW4 ? 8 : 16;  // registers per granule per activation row
@@ -190,7 +223,6 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
     const int g0 = p * pl.Gq;                   // first granule of this piece
     const int gp = min(pl.Gq, pl.Gt - g0);      // granules in this piece
     const int RBp = gp * kGranBytes;            // bytes of one row-piece
-    const int64_t RB = (int64_t)pl.Gt * kGranBytes;
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.off_bars);
     uint64_t* sw_bar = full + NS;                       // scale cache landed
@@ -199,32 +231,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
     int* last_flag = reinterpret_cast<int*>(smem + pl.off_flag + 4);
     float* sw_s = reinterpret_cast<float*>(smem + pl.off_sw);
 
-    // Stage `st` of this CTA's weight stream into ring slot `slot`: one 1-D
-    // bulk copy of whole rows, or one per row-piece when K is split.
     const uint64_t pol = l2_evict_first_policy();
-    auto issue = [&](int st, int slot) {
-        const int r0 = st * pl.Rl;
-        const int nr = min(pl.Rl, nrows - r0);
-        const uint32_t dst = smem_u32(smem + slot * pl.stage_stride);
-        const uint32_t bar = smem_u32(full + slot);
-        mbar_arrive_expect_tx(bar, (uint32_t)(nr * RBp));
-        // rows row0+r0 .. row0+r0+nr-1, cut where a segment ends
-        int64_t n = row0 + r0;
-        const int64_t n_end = n + nr;
-        while (n < n_end) {
-            const int sg = segment_of(a, n);
-            const int64_t run = min(n_end, a.off[sg + 1]) - n;
-            const uint8_t* src = a.W[sg] + (n - a.off[sg]) * RB + (int64_t)g0 * kGranBytes;
-            const uint32_t d = dst + (uint32_t)((n - row0 - r0) * RBp);
-            if (pl.P == 1) {
-                bulk_g2s(d, src, (uint32_t)(run * RBp), bar, pol);
-            } else {
-                for (int r = 0; r < run; ++r)
-                    bulk_g2s(d + r * RBp, src + (int64_t)r * RB, (uint32_t)RBp, bar, pol);
-            }
-            n += run;
-        }
-    };
+    auto issue = [&](int st, int slot) { issue_stage(a, smem, st, slot, row0, nrows, g0, pol); };
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -306,27 +314,16 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
         };
         const bool staged = MT == 1 && pl.x_bytes > 0;
         if (staged) {
-            // M == 1, short row: all loads in flight at once, the row kept
-            // in shared memory for the quantization pass
-            constexpr int XR = kMaxXStage / 16 / kConsumers;
+            // M == 1, short row: every thread copies its 16-byte vectors to
+            // shared memory asynchronously (all in flight at once), then
+            // takes the max over the vectors it copied
             const uint4* xv = reinterpret_cast<const uint4*>(a.X);
-            uint4 xr[XR];
-            #pragma unroll
-            for (int u = 0; u < XR; ++u) {
-                if (u * kConsumers >= nv) break;  // uniform
-                const int v = tid + u * kConsumers;
-                if (v < nv) xr[u] = xv[v];
-            }
+            #pragma unroll 1
+            for (int v = tid; v < nv; v += kConsumers) cp_async_16(smem_u32(x_s + v), xv + v);
+            cp_async_wait_all();
             __half2 hm = __float2half2_rn(0.f);
-            #pragma unroll
-            for (int u = 0; u < XR; ++u) {
-                if (u * kConsumers >= nv) break;
-                const int v = tid + u * kConsumers;
-                if (v < nv) {
-                    hm = absmax8(xr[u], hm);
-                    x_s[v] = xr[u];
-                }
-            }
+            #pragma unroll 2
+            for (int v = tid; v < nv; v += kConsumers) hm = absmax8(x_s[v], hm);
             float mx = fmaxf(__low2float(hm), __high2float(hm));
             mx = warp_max(mx);
             if (lane == 0) max_s[warp] = mx;
@@ -457,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
     // Stages are consumed in batches of kBatch: per stage each thread only
     // multiplies and accumulates; the cross-thread reduction and the outputs
     // of a whole batch follow together, so their latencies overlap.
-    constexpr int kBatch = 4;
+    constexpr int kBatch = 2;
     constexpr int NCH = MT == 1 ? 2 : 1;       // independent chains per sum
     AccT* red = reinterpret_cast<AccT*>(smem + pl.off_red);  // [2][warps][kBatch][MT]
     const int wpr = Cl >> 5;                                  // warps per row-piece
@@ -505,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                 }
                 #pragma unroll
                 for (int s = 0; s < SMAX; ++s) {
-                    if (s < pl.S) {  // uniform over the CTA
+                    if (kExactS || s < pl.S) {  // uniform over the CTA
                         const uint32_t wv[4] = {wg[s].x, wg[s].y, wg[s].z, wg[s].w};
                         #pragma unroll
                         for (int t = 0; t < 4; ++t) {
@@ -669,9 +666,9 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
 
 // --------------------------------------------------------------- launching
 
-template <bool kW4, int MT, int SMAX, bool kFused>
+template <bool kW4, int MT, int SMAX, bool kFused, bool kExactS = false>
 static cudaError_t launch_one(const GemvArgs& args, unsigned flags, cudaStream_t stream) {
-    auto* fn = gemv_kernel<kW4, MT, SMAX, kFused>;
+    auto* fn = gemv_kernel<kW4, MT, SMAX, kFused, kExactS>;
     static int attr_set[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -699,6 +696,14 @@ static cudaError_t launch_one(const GemvArgs& args, unsigned flags, cudaStream_t
         cfg.numAttrs = 1;
     }
     return cudaLaunchKernelEx(&cfg, fn, args);
+}
+
+// M == 1 fused W4A8: the common column counts get kernels with exactly that
+// many columns (7: K = 3584 at 16 threads per row; 5: K = 18944 at 128).
+static cudaError_t launch_w4a8_m1_fused(const GemvArgs& a, unsigned flags, cudaStream_t stream) {
+    if (a.pl.S == 7) return launch_one<true, 1, 7, true, true>(a, flags, stream);
+    if (a.pl.S == 5) return launch_one<true, 1, 5, true, true>(a, flags, stream);
+    return launch_one<true, 1, 8, true>(a, flags, stream);
 }
 
 static void set_segments(GemvArgs& a, int G, const uint8_t* const* W, const void* const* s,
@@ -733,7 +738,7 @@ cudaError_t launch_w4a8_grouped(const GemvPlan& pl, const uint16_t* X, int M, in
     a.N = (int)a.off[kMaxSegments];
     a.pl = pl;
     switch (pl.MT) {
-        case 1: return launch_one<true, 1, 8, true>(a, flags, stream);
+        case 1: return launch_w4a8_m1_fused(a, flags, stream);
         case 2: return launch_one<true, 2, 4, true>(a, flags, stream);
         case 4: return launch_one<true, 4, 2, true>(a, flags, stream);
         case 8: return launch_one<true, 8, 1, true>(a, flags, stream);
@@ -762,7 +767,7 @@ cudaError_t launch_w4a8(const GemvPlan& pl, bool fused, const uint16_t* X, const
     a.pl = pl;
     switch (pl.MT * 2 + (fused ? 1 : 0)) {
         case 2: return launch_one<true, 1, 8, false>(a, flags, stream);
-        case 3: return launch_one<true, 1, 8, true>(a, flags, stream);
+        case 3: return launch_w4a8_m1_fused(a, flags, stream);
         case 4: return launch_one<true, 2, 4, false>(a, flags, stream);
         case 5: return launch_one<true, 2, 4, true>(a, flags, stream);
         case 8: return launch_one<true, 4, 2, false>(a, flags, stream);

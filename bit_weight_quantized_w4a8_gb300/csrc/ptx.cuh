@@ -108,6 +108,14 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+// 16-byte asynchronous global -> shared copy through L1 (not the TMA unit).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Waits until all of this thread's cp.async copies have landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
 // Arrive on `bar` once all of this thread's earlier cp.async copies landed
 // (the barrier's expected count covers this arrival).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
