@@ -18,8 +18,8 @@ LIB_PATH = os.path.join(_PKG, "_build", "libw4a8.so")
 OK = 0
 ERR_NULL, ERR_ALIGN, ERR_SHAPE, ERR_WORKSPACE, ERR_CUDA = 1, 2, 3, 4, 5
 LAUNCH_PDL = 1
-W4A8_MAX_M = 8
-W8A16_MAX_M = 4
+W4A8_MAX_M = 64
+W8A16_MAX_M = 64
 
 EXPORTS = [
     "w4_quantize_weights", "w8_quantize_weights", "act_quantize_i8",

@@ -100,6 +100,22 @@ int check_w8a16_shape(int64_t M, int64_t K, int64_t N) {
     return W4A8_OK;
 }
 
+// One kernel launch handles up to this many activation rows; calls with
+// more rows run one launch per group of rows (each streams the weights).
+constexpr int kRowGroupW4 = 8;
+constexpr int kRowGroupW8 = 4;
+
+// Plans of the row groups of an M-row call: `full` for groups of `rg`
+// rows, `tail` for a shorter last group (equal to `full` when there is none).
+int plan_row_groups(bool w4, bool fused, int64_t M, int64_t K, int64_t N, int rg,
+                    w4a8::GemvPlan* full, w4a8::GemvPlan* tail, int sms = 0) {
+    int st = plan_for(w4, fused, M < rg ? M : rg, K, N, full, sms);
+    if (st != W4A8_OK) return st;
+    *tail = *full;
+    if (M > rg && M % rg) st = plan_for(w4, fused, M % rg, K, N, tail, sms);
+    return st;
+}
+
 int check_workspace(const w4a8::GemvPlan& pl, void* ws, size_t ws_bytes) {
     if (pl.ws_bytes == 0) return W4A8_OK;
     if (ws == nullptr || ws_bytes < pl.ws_bytes)
@@ -146,17 +162,17 @@ int act_quantize_i8(const uint16_t* X, int64_t M, int64_t K, int8_t* Xq, float* 
 
 size_t w4a8_workspace_bytes(int64_t M, int64_t K, int64_t N) {
     if (check_w4a8_shape(M, K, N) != W4A8_OK) return 0;
-    w4a8::GemvPlan pl;
+    w4a8::GemvPlan pf, pt;
     // the fused and unfused kernels share the split plan
-    if (plan_for(true, true, M, K, N, &pl) != W4A8_OK) return 0;
-    return pl.ws_bytes;
+    if (plan_row_groups(true, true, M, K, N, kRowGroupW4, &pf, &pt) != W4A8_OK) return 0;
+    return pf.ws_bytes > pt.ws_bytes ? pf.ws_bytes : pt.ws_bytes;
 }
 
 size_t w8a16_workspace_bytes(int64_t M, int64_t K, int64_t N) {
     if (check_w8a16_shape(M, K, N) != W4A8_OK) return 0;
-    w4a8::GemvPlan pl;
-    if (plan_for(false, false, M, K, N, &pl) != W4A8_OK) return 0;
-    return pl.ws_bytes;
+    w4a8::GemvPlan pf, pt;
+    if (plan_row_groups(false, false, M, K, N, kRowGroupW8, &pf, &pt) != W4A8_OK) return 0;
+    return pf.ws_bytes > pt.ws_bytes ? pf.ws_bytes : pt.ws_bytes;
 }
 
 int w4a8_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, const uint8_t* Wq,
@@ -168,12 +184,20 @@ int w4a8_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, const uin
     if (!aligned(Xq, 16) || !aligned(Wq, 16) || !aligned(Y, 4) || !aligned(sw, 4) ||
         !aligned(sa, 4) || (acc_out && !aligned(acc_out, 4)))
         return fail(W4A8_ERR_ALIGN, "w4a8_gemv: Xq/Wq need 16-byte, Y/sw/sa/acc_out 4-byte alignment");
-    w4a8::GemvPlan pl;
-    if ((st = plan_for(true, true, M, K, N, &pl)) != W4A8_OK) return st;
-    if ((st = check_workspace(pl, ws, ws_bytes)) != W4A8_OK) return st;
-    cudaError_t e = w4a8::launch_w4a8(pl, false, nullptr, Xq, sa, (int)M, K, Wq, sw, N, Y, acc_out,
-                                      nullptr, nullptr, ws, flags, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_gemv launch");
+    w4a8::GemvPlan pf, pt;
+    if ((st = plan_row_groups(true, true, M, K, N, kRowGroupW4, &pf, &pt)) != W4A8_OK) return st;
+    if ((st = check_workspace(pf, ws, ws_bytes)) != W4A8_OK) return st;
+    if ((st = check_workspace(pt, ws, ws_bytes)) != W4A8_OK) return st;
+    for (int64_t m0 = 0; m0 < M; m0 += kRowGroupW4) {
+        const int64_t mg = M - m0 < kRowGroupW4 ? M - m0 : kRowGroupW4;
+        cudaError_t e = w4a8::launch_w4a8(mg == kRowGroupW4 || M < kRowGroupW4 ? pf : pt, false,
+                                          nullptr, Xq + m0 * K, sa + m0, (int)mg, K, Wq, sw, N,
+                                          Y + m0 * N, acc_out ? acc_out + m0 * N : nullptr,
+                                          nullptr, nullptr, ws, flags,
+                                          static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "w4a8_gemv launch");
+    }
+    return ok();
 }
 
 int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const float* sw,
@@ -186,13 +210,21 @@ int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, cons
         (Xq_out && !aligned(Xq_out, 16)) || (sa_out && !aligned(sa_out, 4)) ||
         (acc_out && !aligned(acc_out, 4)))
         return fail(W4A8_ERR_ALIGN, "w4a8_linear: X/Wq/Xq_out need 16-byte, Y/sw/sa_out/acc_out 4-byte alignment");
-    w4a8::GemvPlan pl;
-    if ((st = plan_for(true, true, M, K, N, &pl)) != W4A8_OK) return st;
-    if ((st = check_workspace(pl, ws, ws_bytes)) != W4A8_OK) return st;
-    cudaError_t e = w4a8::launch_w4a8(pl, true, X, nullptr, nullptr, (int)M, K, Wq, sw, N, Y,
-                                      acc_out, Xq_out, sa_out, ws, flags,
-                                      static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear launch");
+    w4a8::GemvPlan pf, pt;
+    if ((st = plan_row_groups(true, true, M, K, N, kRowGroupW4, &pf, &pt)) != W4A8_OK) return st;
+    if ((st = check_workspace(pf, ws, ws_bytes)) != W4A8_OK) return st;
+    if ((st = check_workspace(pt, ws, ws_bytes)) != W4A8_OK) return st;
+    for (int64_t m0 = 0; m0 < M; m0 += kRowGroupW4) {
+        const int64_t mg = M - m0 < kRowGroupW4 ? M - m0 : kRowGroupW4;
+        cudaError_t e = w4a8::launch_w4a8(mg == kRowGroupW4 || M < kRowGroupW4 ? pf : pt, true,
+                                          X + m0 * K, nullptr, nullptr, (int)mg, K, Wq, sw, N,
+                                          Y + m0 * N, acc_out ? acc_out + m0 * N : nullptr,
+                                          Xq_out ? Xq_out + m0 * K : nullptr,
+                                          sa_out ? sa_out + m0 : nullptr, ws, flags,
+                                          static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "w4a8_linear launch");
+    }
+    return ok();
 }
 
 int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const uint8_t* const* Wq,
@@ -212,12 +244,20 @@ int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const ui
     int st = check_w4a8_shape(M, K, total);
     if (st != W4A8_OK) return st;
     if (!aligned(X, 16)) return fail(W4A8_ERR_ALIGN, "w4a8_linear_grouped: X needs 16-byte alignment");
-    w4a8::GemvPlan pl;
-    if ((st = plan_for(true, true, M, K, total, &pl)) != W4A8_OK) return st;
-    if ((st = check_workspace(pl, ws, ws_bytes)) != W4A8_OK) return st;
-    cudaError_t e = w4a8::launch_w4a8_grouped(pl, X, (int)M, K, G, Wq, sw, N, Y, ws, flags,
-                                              static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear_grouped launch");
+    w4a8::GemvPlan pf, pt;
+    if ((st = plan_row_groups(true, true, M, K, total, kRowGroupW4, &pf, &pt)) != W4A8_OK) return st;
+    if ((st = check_workspace(pf, ws, ws_bytes)) != W4A8_OK) return st;
+    if ((st = check_workspace(pt, ws, ws_bytes)) != W4A8_OK) return st;
+    float* Yg[W4A8_MAX_GROUP];
+    for (int64_t m0 = 0; m0 < M; m0 += kRowGroupW4) {
+        const int64_t mg = M - m0 < kRowGroupW4 ? M - m0 : kRowGroupW4;
+        for (int g = 0; g < G; ++g) Yg[g] = Y[g] + m0 * N[g];
+        cudaError_t e = w4a8::launch_w4a8_grouped(mg == kRowGroupW4 || M < kRowGroupW4 ? pf : pt,
+                                                  X + m0 * K, (int)mg, K, G, Wq, sw, N, Yg, ws,
+                                                  flags, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "w4a8_linear_grouped launch");
+    }
+    return ok();
 }
 
 int w8a16_gemv(const uint16_t* X, int64_t M, int64_t K, const int8_t* Wq8, const uint16_t* sw16,
@@ -227,12 +267,18 @@ int w8a16_gemv(const uint16_t* X, int64_t M, int64_t K, const int8_t* Wq8, const
     if (st != W4A8_OK) return st;
     if (!aligned(X, 16) || !aligned(Wq8, 16) || !aligned(Y, 4) || !aligned(sw16, 2))
         return fail(W4A8_ERR_ALIGN, "w8a16_gemv: X/Wq8 need 16-byte, Y 4-byte alignment");
-    w4a8::GemvPlan pl;
-    if ((st = plan_for(false, false, M, K, N, &pl)) != W4A8_OK) return st;
-    if ((st = check_workspace(pl, ws, ws_bytes)) != W4A8_OK) return st;
-    cudaError_t e = w4a8::launch_w8a16(pl, X, (int)M, K, Wq8, sw16, N, Y, ws, flags,
-                                       static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? ok() : cuda_fail(e, "w8a16_gemv launch");
+    w4a8::GemvPlan pf, pt;
+    if ((st = plan_row_groups(false, false, M, K, N, kRowGroupW8, &pf, &pt)) != W4A8_OK) return st;
+    if ((st = check_workspace(pf, ws, ws_bytes)) != W4A8_OK) return st;
+    if ((st = check_workspace(pt, ws, ws_bytes)) != W4A8_OK) return st;
+    for (int64_t m0 = 0; m0 < M; m0 += kRowGroupW8) {
+        const int64_t mg = M - m0 < kRowGroupW8 ? M - m0 : kRowGroupW8;
+        cudaError_t e = w4a8::launch_w8a16(mg == kRowGroupW8 || M < kRowGroupW8 ? pf : pt,
+                                           X + m0 * K, (int)mg, K, Wq8, sw16, N, Y + m0 * N, ws,
+                                           flags, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "w8a16_gemv launch");
+    }
+    return ok();
 }
 
 const char* w4a8_last_error(void) { return g_last_error.c_str(); }
@@ -272,9 +318,13 @@ int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int*
     if (!info) return fail(W4A8_ERR_NULL, "w4a8_plan_info: NULL pointer");
     int st = w8a16 ? check_w8a16_shape(M, K, N) : check_w4a8_shape(M, K, N);
     if (st != W4A8_OK) return st;
-    w4a8::GemvPlan pl;
-    if ((st = plan_for(!w8a16, !w8a16, M, K, N, &pl, num_sms)) != W4A8_OK) return st;
-    const int ws = pl.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)pl.ws_bytes;
+    // the plan of the first row group; workspace for the whole call
+    w4a8::GemvPlan pl, pt;
+    if ((st = plan_row_groups(!w8a16, !w8a16, M, K, N, w8a16 ? kRowGroupW8 : kRowGroupW4, &pl,
+                              &pt, num_sms)) != W4A8_OK)
+        return st;
+    const size_t wsb = pl.ws_bytes > pt.ws_bytes ? pl.ws_bytes : pt.ws_bytes;
+    const int ws = wsb > 0x7FFFFFFF ? 0x7FFFFFFF : (int)wsb;
     const int v[] = {pl.P, pl.Cl, pl.S, pl.Rl, pl.Gs, pl.grid, pl.rows_max, pl.NS,
                      pl.stage_stride, pl.smem, ws};
     for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
@@ -329,6 +379,8 @@ extern "C" int w4a8_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, cons
     if (!X || !Wq || !sw || !Y) return fail(W4A8_ERR_NULL, "w4a8_linear_noalloc: NULL pointer");
     int st = check_w4a8_shape(M, K, N);
     if (st != W4A8_OK) return st;
+    if (M > kRowGroupW4)
+        return fail(W4A8_ERR_SHAPE, "w4a8_linear_noalloc: M=%lld outside [1, %d]", (long long)M, kRowGroupW4);
     if (!aligned(X, 16) || !aligned(Wq, 16) || !aligned(Y, 4) || !aligned(sw, 4))
         return fail(W4A8_ERR_ALIGN, "w4a8_linear_noalloc: X/Wq need 16-byte, Y/sw 4-byte alignment");
     w4a8::GemvPlan pl;

@@ -71,9 +71,13 @@ typedef enum {
    workspace are only touched after the wait. */
 #define W4A8_LAUNCH_PDL 1u
 
-/* Maximum activation rows (decode batch) per call. */
-#define W4A8_MAX_M 8
-#define W8A16_MAX_M 4
+/* Maximum activation rows (decode batch) per call.  One kernel launch
+ * handles up to 8 rows (W8A16: 4); a call with more rows runs one launch
+ * per group of that many rows, in order on `stream`, and each of them
+ * streams the whole weight matrix again.  w4a8_linear_noalloc takes at
+ * most 8 rows. */
+#define W4A8_MAX_M 64
+#define W8A16_MAX_M 64
 
 /* ---------------------------------------------------------------------- */
 /* Weight quantizers (load time)                                           */

@@ -5,7 +5,7 @@ those weight rows from the counter-based generator).
 * Qwen2-7B-shaped decode linear set, M=1, W4A8 (q, k, v, o, gate, up, down,
   lm_head), activations with 0.1% x20 outliers, fused activation quantization,
   programmatic dependent launch.
-* Skinny-batch sweep on gate and down, M in {1, 2, 4, 8}.
+* Skinny-batch sweep on gate and down, M in {1, 2, 4, 8, 16, 32, 64}.
 * ChatGLM2-6B-shaped W8A16 GEMVs.
 """
 import numpy as np
@@ -118,7 +118,7 @@ def test_decode_step_as_benchmarked(w4, orc):
     assert w4.w4a8_device_error() == 0
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
 @pytest.mark.parametrize("name", ["gate", "down"])
 def test_skinny_batch_sweep(w4, orc, M, name):
     idx = [s[0] for s in QWEN2_7B_SET].index(name)
@@ -127,7 +127,7 @@ def test_skinny_batch_sweep(w4, orc, M, name):
 
 
 def test_batch_above_limit_rejected(w4):
-    X = torch.zeros((16, 3584), dtype=torch.float16, device="cuda")
+    X = torch.zeros((65, 3584), dtype=torch.float16, device="cuda")
     Wq = torch.zeros((64, 1792), dtype=torch.uint8, device="cuda")
     sw = torch.zeros((64,), dtype=torch.float32, device="cuda")
     with pytest.raises(w4.W4A8Error) as e:

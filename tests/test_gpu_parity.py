@@ -157,6 +157,10 @@ W4A8_SHAPES = [
     (1, 131072, 5, 10),      # longest rows
     (8, 131072, 3, 11),
     (6, 18944, 600, 12),
+    (9, 896, 100, 13),       # row groups: 8 + 1
+    (16, 3584, 77, 14),      # 8 + 8
+    (37, 256, 50, 15),       # 8 * 4 + 5
+    (64, 1024, 40, 16),      # the largest batch
 ]
 
 
@@ -165,7 +169,7 @@ def test_w4a8_linear_fused(w4, orc, M, K, N, seed):
     check_w4a8(w4, orc, M, K, N, seed, fused=True, zero_rows=(1,))
 
 
-@pytest.mark.parametrize("M,K,N,seed", W4A8_SHAPES[:8])
+@pytest.mark.parametrize("M,K,N,seed", W4A8_SHAPES[:8] + W4A8_SHAPES[-3:-1])
 def test_w4a8_gemv_unfused(w4, orc, M, K, N, seed):
     check_w4a8(w4, orc, M, K, N, seed, fused=False)
 
@@ -312,7 +316,8 @@ def check_w8a16(w4, orc, M, K, N, seed):
 
 
 @pytest.mark.parametrize("M,K,N,seed", [(1, 4096, 4608, 70), (2, 64, 100, 71), (4, 13696, 50, 72),
-                                        (3, 16, 7, 73), (1, 13696, 400, 74), (1, 65536, 3, 75)])
+                                        (3, 16, 7, 73), (1, 13696, 400, 74), (1, 65536, 3, 75),
+                                        (5, 4096, 64, 76), (16, 512, 90, 77), (64, 128, 20, 78)])
 def test_w8a16(w4, orc, M, K, N, seed):
     check_w8a16(w4, orc, M, K, N, seed)
 
@@ -347,6 +352,8 @@ def test_gpu_generator_matches_host(w4):
     (1, 3584, (100, 7, 2000), 4),
     (8, 64, (17, 1, 40, 9), 0),
     (1, 18944, (300, 50), 0),
+    (12, 512, (40, 7), 0),               # row groups 8 + 4
+    (20, 256, (9, 30, 3), 2),
 ])
 def test_w4a8_linear_grouped(w4, orc, M, K, Ns, splits):
     w4.w4a8_set_tuning(force_splits=splits)
