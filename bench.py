@@ -7,8 +7,9 @@ quantizes the fp16 activation to INT8, streams the packed INT4 weights,
 accumulates in int32 and rescales to fp32.  Projections that read the same
 activation in the model share one grouped launch (q/k/v; gate/up), so a step
 is five launches.  Weights (389.8 MB per set) are resident in HBM; two copies
-alternate between steps, so nothing is reused from the 129 MB L2.  The step is
-replayed as a CUDA graph of programmatically dependent launches.
+alternate between steps, so nothing is reused from the 129 MB L2.  Steps are
+replayed as CUDA graphs of two steps each (copy 0, then copy 1) whose launches
+are programmatically dependent.
 
 Reported (one JSON line, rank 0):
   value     effective weight GB/s (packed INT4 + fp32 scales per set / time)
@@ -16,6 +17,10 @@ Reported (one JSON line, rank 0):
             and the outputs read back, every step, inside the timed region
   roofline  the dominant kernel (lm_head, 273 MB) against measured HBM peak
   cpu_baseline  the CPU oracle timed on the host on a sample of the set
+  decode_step_28_layers  a full 28-layer decode step of the same shapes
+            (linear layers only) plus lm_head: ms per token
+  skinny_batch  gate and down at M = 1 ... 64 activation rows
+  w8a16_set the ChatGLM2-6B-shaped W8A16 GEMVs at M=1
 
 `--impl reference` times the CPU oracle alone (the reference arm).
 Under torchrun with N > 1 every rank runs an independent replica (weak
@@ -79,6 +84,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the 28-layer step, the skinny-batch sweep and the W8A16 set")
     ap.add_argument("--min-busy-s", type=float, default=0.6,
                     help="keep the GPU busy at least this long before timing (clock samples)")
     ap.add_argument("--only", choices=[l[0] for l in LAUNCHES], default=None,
@@ -356,26 +363,38 @@ def run_ours(args, world, rank):
         for j in range(len(LAUNCHES)):
             launch(c, j, PDL)
 
-    # eager warm-up (sets kernel attributes), then graphs per weight copy
+    X_pin = torch.from_numpy(X_host).pin_memory()
+    Y_pin = torch.empty(int(n_off[-1]), dtype=torch.float32).pin_memory()
+
+    def e2e_set(c):
+        X_all.copy_(X_pin, non_blocking=True)
+        launch_set(c)
+        Y_pin.copy_(Y_all, non_blocking=True)
+
+    # eager warm-up (sets kernel attributes), then graphs: a pair of steps
+    # (weight copy 0, then copy 1) and a single step for an odd remainder
     with torch.cuda.stream(stream):
         launch_set(0)
         launch_set(1)
     torch.cuda.synchronize()
-    graphs, e2e_graphs = [], []
-    X_pin = torch.from_numpy(X_host).pin_memory()
-    Y_pin = torch.empty(int(n_off[-1]), dtype=torch.float32).pin_memory()
-    for c in range(2):
+
+    def capture(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            launch_set(c)
-        graphs.append(g)
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g2, stream=stream):
-            X_all.copy_(X_pin, non_blocking=True)
-            launch_set(c)
-            Y_pin.copy_(Y_all, non_blocking=True)
-        e2e_graphs.append(g2)
+            fn()
+        return g
+
+    pair = capture(lambda: (launch_set(0), launch_set(1)))
+    single = capture(lambda: launch_set(0))
+    e2e_pair = capture(lambda: (e2e_set(0), e2e_set(1)))
+    e2e_single = capture(lambda: e2e_set(0))
     torch.cuda.synchronize()
+
+    def run_steps(n, two, one):
+        for _ in range(n // 2):
+            two.replay()
+        if n % 2:
+            one.replay()
 
     clocks = ClockSampler(gpu_uuid())
     clocks.start()
@@ -384,9 +403,9 @@ def run_ours(args, world, rank):
         t_end = time.time() + args.min_busy_s
         k = 0
         while k < args.warmup or time.time() < t_end:
-            graphs[k % 2].replay()
-            k += 1
-            if k % 200 == 0:
+            pair.replay()
+            k += 2
+            if k % 400 == 0:
                 stream.synchronize()
     stream.synchronize()
 
@@ -396,8 +415,7 @@ def run_ours(args, world, rank):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for k in range(args.steps):
-            graphs[k % 2].replay()
+        run_steps(args.steps, pair, single)
         ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -419,13 +437,11 @@ def run_ours(args, world, rank):
 
     # --- e2e: pinned host in, results out, every step ---------------------
     with torch.cuda.stream(stream):
-        for k in range(max(3, args.warmup)):
-            e2e_graphs[k % 2].replay()
+        run_steps(max(4, args.warmup), e2e_pair, e2e_single)
         stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for k in range(args.steps):
-            e2e_graphs[k % 2].replay()
+        run_steps(args.steps, e2e_pair, e2e_single)
         e1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -452,11 +468,19 @@ def run_ours(args, world, rank):
         nbytes = sum(weight_bytes(lin[n][1], lin[n][2]) for n in members)
         per_launch[lname] = {"us": round(us, 2), "GBps": round(nbytes / us / 1e3, 1)}
         del g
+    peak, peak_kind = measured_peak()
+    extra = {}
+    if not args.no_extra:
+        extra["skinny_batch"] = measure_skinny(torch, w4, synth, dev, stream, copies, lin)
+        extra["w8a16_set"] = measure_w8a16(torch, w4, synth, dev, stream)
+        del copies
+        torch.cuda.empty_cache()
+        extra["decode_step_28_layers"] = measure_decode_step(torch, w4, synth, dev, stream, ws,
+                                                             peak)
     errors = w4.w4a8_device_error()
     if errors:
         raise SystemExit("device error word %#x" % errors)
 
-    peak, peak_kind = measured_peak()
     value = SET_BYTES * world / (ms_step * 1e-3) / 1e9
     lm_bytes = weight_bytes(K_lm, N_lm)
     achieved = lm_bytes / (lm_ms * 1e-3) / 1e9
@@ -468,7 +492,7 @@ def run_ours(args, world, rank):
         "dtype": "int4xint8->int32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "set_weight_bytes": SET_BYTES,
                    "l2": "two weight copies alternate (780 MB > 129 MB L2)",
-                   "launch": "CUDA graph of 5 fused launches (q/k/v and gate/up grouped) with programmatic dependent launch",
+                   "launch": "CUDA graphs of two steps (weight copy 0, then 1; a one-step graph for an odd count), 5 fused launches a step (q/k/v and gate/up grouped), programmatic dependent launch",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "us_per_set": round(ms_step * 1e3, 2),
         "pct_hbm_peak": {"of_measured": round(SET_BYTES / (ms_step * 1e-3) / 1e9 / peak, 4),
@@ -482,11 +506,12 @@ def run_ours(args, world, rank):
                 "us_per_set": round(e2e_ms * 1e3, 2),
                 "h2d_bytes_per_step": int(X_pin.numel() * X_pin.element_size()),
                 "d2h_bytes_per_step": int(Y_pin.numel() * Y_pin.element_size()),
-                "how": "CUDA graph: pinned H2D of the 5 activations, 5 fused launches, D2H of the 8 outputs"},
+                "how": "CUDA graphs of two steps: per step pinned H2D of the 5 activations, 5 fused launches, D2H of the 8 outputs"},
         "clocks": clk,
         "gpu_launches": len(LAUNCHES) * args.steps,
         "per_launch_no_pdl": per_launch,
     }
+    line.update(extra)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         orc, inputs = cpu_sample_inputs(dev)
         t_set, reps = time_oracle_sample(orc, inputs)
@@ -497,6 +522,144 @@ def run_ours(args, world, rank):
                       % (CPU_SAMPLE_STRIDE, reps)}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def _graph_us(torch, stream, fn, per_replay, reps=5):
+    """Captures fn() as one CUDA graph, replays it once untimed and `reps`
+    times timed; returns microseconds per unit (per_replay units a replay)."""
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        g.replay()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        a1.record(stream)
+    torch.cuda.synchronize()
+    return a0.elapsed_time(a1) / (reps * per_replay) * 1e3
+
+
+DECODE_LAYERS = 28
+
+
+def measure_decode_step(torch, w4, synth, dev, stream, ws, peak):
+    """A full 28-layer Qwen2-7B-shaped decode step, linear layers only: per
+    layer q/k/v (grouped), o, gate/up (grouped), down, then lm_head once;
+    per-layer weights (seed 1000 * (layer + 1) + index), 3.54 GB resident;
+    activations pre-generated per launch (the linears do not chain without
+    attention and norms); one CUDA graph of 113 dependent launches."""
+    names = [l[0] for l in LINEARS]
+    layers = []
+    for layer in range(DECODE_LAYERS):
+        Wq, sw = {}, {}
+        for i, (n, K, N) in enumerate(LINEARS[:-1]):
+            W = synth.normal_gpu(1000 * (layer + 1) + i, (N, K), 0.02, device=dev)
+            Wq[n], sw[n] = w4.w4_quantize_weights(W)
+            del W
+        Xs = {}
+        for lname, members in LAUNCHES[:-1]:
+            K = LINEARS[names.index(members[0])][1]
+            Xs[lname] = torch.from_numpy(synth.activation(
+                1000 * (layer + 1) + names.index(members[0]) + ACT_SEED_OFFSET, 1, K,
+                outlier_frac=OUTLIER_FRAC)).to(dev)
+        layers.append((Wq, sw, Xs))
+    i_lm = names.index("lm_head")
+    _, K_lm, N_lm = LINEARS[i_lm]
+    W = synth.normal_gpu(WEIGHT_SEED0 + i_lm, (N_lm, K_lm), 0.02, device=dev)
+    Wq_lm, sw_lm = w4.w4_quantize_weights(W)
+    del W
+    X_lm = torch.from_numpy(synth.activation(activation_seed("lm_head"), 1, K_lm,
+                                             outlier_frac=OUTLIER_FRAC)).to(dev)
+    Ys = {n: torch.empty((1, N), dtype=torch.float32, device=dev) for n, _, N in LINEARS}
+    torch.cuda.synchronize()
+
+    def step():
+        for Wq, sw, Xs in layers:
+            for lname, members in LAUNCHES[:-1]:
+                if len(members) == 1:
+                    w4.w4a8_linear(Xs[lname], Wq[members[0]], sw[members[0]], Y=Ys[members[0]],
+                                   ws=ws, flags=w4.LAUNCH_PDL)
+                else:
+                    w4.w4a8_linear_grouped(Xs[lname], [Wq[n] for n in members],
+                                           [sw[n] for n in members], Ys=[Ys[n] for n in members],
+                                           ws=ws, flags=w4.LAUNCH_PDL)
+        w4.w4a8_linear(X_lm, Wq_lm, sw_lm, Y=Ys["lm_head"], ws=ws, flags=w4.LAUNCH_PDL)
+
+    us = _graph_us(torch, stream, step, 1, reps=10)
+    nbytes = DECODE_LAYERS * sum(weight_bytes(K, N) for _, K, N in LINEARS[:-1]) + \
+        weight_bytes(K_lm, N_lm)
+    del layers
+    return {"workload": "28 layers x (q/k/v, o, gate/up, down) + lm_head, M=1, W4A8",
+            "launches": DECODE_LAYERS * (len(LAUNCHES) - 1) + 1, "weight_bytes": nbytes,
+            "ms_per_token": round(us / 1e3, 4), "tok_per_s": round(1e6 / us, 1),
+            "GBps": round(nbytes / us / 1e3, 1), "of_measured_peak": round(nbytes / us / 1e3 / peak, 4)}
+
+
+SKINNY_M = (1, 2, 4, 8, 16, 32, 64)
+
+
+def measure_skinny(torch, w4, synth, dev, stream, copies, lin):
+    """gate 3584->18944 and down 18944->3584 at M = 1 ... 64 rows: a graph of
+    ten calls on the two alternating weight copies; more than 8 rows run as
+    consecutive launches of 8-row groups."""
+    out = {}
+    for name in ("gate", "down"):
+        i, K, N = lin[name]
+        res = {}
+        for M in SKINNY_M:
+            X = torch.from_numpy(synth.activation(WEIGHT_SEED0 + i + ACT_SEED_OFFSET, M, K,
+                                                  outlier_frac=OUTLIER_FRAC)).to(dev)
+            Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            ws = torch.zeros(max(w4.w4a8_workspace_bytes(M, K, N), 4096), dtype=torch.uint8,
+                             device=dev)
+
+            def calls():
+                for k in range(10):
+                    Wqs, sws = copies[k % 2]
+                    w4.w4a8_linear(X, Wqs[i], sws[i], Y=Y, ws=ws, flags=w4.LAUNCH_PDL)
+
+            us = _graph_us(torch, stream, calls, 10)
+            res[str(M)] = {"us": round(us, 2), "GBps": round(weight_bytes(K, N) / us / 1e3, 1)}
+        out[name] = res
+    return out
+
+
+W8A16_SET = [("h_to_4h", 4096, 27392), ("qkv", 4096, 4608), ("4h_to_h", 13696, 4096)]
+
+
+def measure_w8a16(torch, w4, synth, dev, stream):
+    """ChatGLM2-6B-shaped W8A16 GEMVs at M=1 (per-channel INT8 weights, fp16
+    scale, fp16 activation): two weight copies alternate, one graph."""
+    copies = []
+    for c in range(2):
+        cp = []
+        for j, (_, K, N) in enumerate(W8A16_SET):
+            W = synth.normal_gpu(2000 + j, (N, K), 0.02, device=dev)
+            cp.append(w4.w8_quantize_weights(W))
+            del W
+        copies.append(cp)
+    Xs = [torch.from_numpy(synth.activation(2500 + j, 1, K)).to(dev)
+          for j, (_, K, _) in enumerate(W8A16_SET)]
+    Ys = [torch.empty((1, N), dtype=torch.float32, device=dev) for _, _, N in W8A16_SET]
+    ws = torch.zeros(max(max(w4.w8a16_workspace_bytes(1, K, N) for _, K, N in W8A16_SET), 4096),
+                     dtype=torch.uint8, device=dev)
+
+    def sets():
+        for c in range(2):
+            for j in range(len(W8A16_SET)):
+                Wq8, sw16 = copies[c][j]
+                w4.w8a16_gemv(Xs[j], Wq8, sw16, Y=Ys[j], ws=ws, flags=w4.LAUNCH_PDL)
+
+    us = _graph_us(torch, stream, sets, 2, reps=10)
+    nbytes = sum(N * K + 2 * N for _, K, N in W8A16_SET)
+    del copies
+    return {"workload": "W8A16 GEMVs 4096->27392, 4096->4608, 13696->4096, M=1",
+            "weight_bytes": nbytes, "us_per_set": round(us, 2), "GBps": round(nbytes / us / 1e3, 1)}
 
 
 def run_only(args, lname):
