@@ -44,6 +44,9 @@ std::atomic<int> g_force_splits{0};
 std::atomic<int> g_force_cl{0};
 std::atomic<int> g_ring_bytes{0};
 std::atomic<int> g_ctas_per_sm{0};
+std::atomic<int> g_mma_min_m{0};
+// Batch rows from which the W4A8 entry points take the tensor-core kernel.
+constexpr int kDefaultMmaMinM = 16;
 
 int sm_count(int* out) {
     static std::atomic<int> cache[64];
@@ -97,6 +100,23 @@ int check_w8a16_shape(int64_t M, int64_t K, int64_t N) {
     if (M < 1 || M > W8A16_MAX_M) return fail(W4A8_ERR_SHAPE, "M=%lld outside [1, %d]", (long long)M, W8A16_MAX_M);
     if (K < 16 || K > 65536 || K % 16) return fail(W4A8_ERR_SHAPE, "K=%lld must be a multiple of 16 in [16, 65536]", (long long)K);
     if (N < 1 || N > 0x7FFFFFFF) return fail(W4A8_ERR_SHAPE, "N=%lld outside [1, 2^31-1]", (long long)N);
+    return W4A8_OK;
+}
+
+// Tensor-core plan for an M-row W4A8 call, or false when the dp4a path
+// serves it (fewer rows than the threshold, or no tensor-core plan).
+bool mma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::MmaPlan* pl, int sms = 0) {
+    const int t = g_mma_min_m.load();
+    if (M < (t > 0 ? t : kDefaultMmaMinM)) return false;
+    if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
+    return w4a8::make_mma_plan((int)M, K, N, sms, pl);
+}
+
+int check_mma_workspace(const w4a8::MmaPlan& pl, void* ws, size_t ws_bytes) {
+    if (ws == nullptr || ws_bytes < pl.ws_bytes)
+        return fail(W4A8_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given%s", pl.ws_bytes,
+                    ws ? ws_bytes : (size_t)0, ws ? "" : " (NULL)");
+    if (!aligned(ws, 256)) return fail(W4A8_ERR_ALIGN, "workspace must be 256-byte aligned");
     return W4A8_OK;
 }
 
@@ -162,6 +182,8 @@ int act_quantize_i8(const uint16_t* X, int64_t M, int64_t K, int8_t* Xq, float* 
 
 size_t w4a8_workspace_bytes(int64_t M, int64_t K, int64_t N) {
     if (check_w4a8_shape(M, K, N) != W4A8_OK) return 0;
+    w4a8::MmaPlan mp;
+    if (mma_plan_for(M, K, N, &mp)) return mp.ws_bytes;
     w4a8::GemvPlan pf, pt;
     // the fused and unfused kernels share the split plan
     if (plan_row_groups(true, true, M, K, N, kRowGroupW4, &pf, &pt) != W4A8_OK) return 0;
@@ -184,6 +206,14 @@ int w4a8_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, const uin
     if (!aligned(Xq, 16) || !aligned(Wq, 16) || !aligned(Y, 4) || !aligned(sw, 4) ||
         !aligned(sa, 4) || (acc_out && !aligned(acc_out, 4)))
         return fail(W4A8_ERR_ALIGN, "w4a8_gemv: Xq/Wq need 16-byte, Y/sw/sa/acc_out 4-byte alignment");
+    w4a8::MmaPlan mp;
+    if (mma_plan_for(M, K, N, &mp)) {
+        if ((st = check_mma_workspace(mp, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_mma(mp, nullptr, Xq, sa, (int)M, K, 1, &Wq, &sw, &N, &Y,
+                                              acc_out, nullptr, nullptr, ws, flags,
+                                              static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_gemv tensor-core launch");
+    }
     w4a8::GemvPlan pf, pt;
     if ((st = plan_row_groups(true, true, M, K, N, kRowGroupW4, &pf, &pt)) != W4A8_OK) return st;
     if ((st = check_workspace(pf, ws, ws_bytes)) != W4A8_OK) return st;
@@ -210,6 +240,14 @@ int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, cons
         (Xq_out && !aligned(Xq_out, 16)) || (sa_out && !aligned(sa_out, 4)) ||
         (acc_out && !aligned(acc_out, 4)))
         return fail(W4A8_ERR_ALIGN, "w4a8_linear: X/Wq/Xq_out need 16-byte, Y/sw/sa_out/acc_out 4-byte alignment");
+    w4a8::MmaPlan mp;
+    if (mma_plan_for(M, K, N, &mp)) {
+        if ((st = check_mma_workspace(mp, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_mma(mp, X, nullptr, nullptr, (int)M, K, 1, &Wq, &sw, &N,
+                                              &Y, acc_out, Xq_out, sa_out, ws, flags,
+                                              static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear tensor-core launch");
+    }
     w4a8::GemvPlan pf, pt;
     if ((st = plan_row_groups(true, true, M, K, N, kRowGroupW4, &pf, &pt)) != W4A8_OK) return st;
     if ((st = check_workspace(pf, ws, ws_bytes)) != W4A8_OK) return st;
@@ -244,6 +282,20 @@ int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const ui
     int st = check_w4a8_shape(M, K, total);
     if (st != W4A8_OK) return st;
     if (!aligned(X, 16)) return fail(W4A8_ERR_ALIGN, "w4a8_linear_grouped: X needs 16-byte alignment");
+    w4a8::MmaPlan mp;
+    if (mma_plan_for(M, K, total, &mp)) {
+        // one plan per matrix inside; the workspace bound covers every N[g] <= total
+        for (int g = 0; g < G; ++g) {
+            w4a8::MmaPlan pg;
+            if (!w4a8::make_mma_plan((int)M, K, N[g], mp.sms, &pg) || pg.ws_bytes > mp.ws_bytes)
+                return fail(W4A8_ERR_SHAPE, "no tensor-core plan for group %d", g);
+        }
+        if ((st = check_mma_workspace(mp, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_mma(mp, X, nullptr, nullptr, (int)M, K, G, Wq, sw, N, Y,
+                                              nullptr, nullptr, nullptr, ws, flags,
+                                              static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear_grouped tensor-core launch");
+    }
     w4a8::GemvPlan pf, pt;
     if ((st = plan_row_groups(true, true, M, K, total, kRowGroupW4, &pf, &pt)) != W4A8_OK) return st;
     if ((st = check_workspace(pf, ws, ws_bytes)) != W4A8_OK) return st;
@@ -286,6 +338,7 @@ const char* w4a8_last_error(void) { return g_last_error.c_str(); }
 int w4a8_device_error(unsigned* flags, void* stream) {
     if (!flags) return fail(W4A8_ERR_NULL, "w4a8_device_error: NULL pointer");
     cudaError_t e = w4a8::read_and_clear_device_error(flags, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = w4a8::read_and_clear_mma_error(flags, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_device_error");
 }
 
@@ -295,6 +348,7 @@ int w4a8_set_tuning(const w4a8_tuning_t* t) {
         g_force_cl = 0;
         g_ring_bytes = 0;
         g_ctas_per_sm = 0;
+        g_mma_min_m = 0;
         return ok();
     }
     if (t->force_splits < 0 || t->force_splits > 16)
@@ -309,7 +363,10 @@ int w4a8_set_tuning(const w4a8_tuning_t* t) {
     g_force_splits = t->force_splits;
     g_force_cl = t->force_threads_per_row;
     g_ring_bytes = t->ring_bytes;
+    if (t->mma_min_m != 0 && (t->mma_min_m < 2 || t->mma_min_m > 65))
+        return fail(W4A8_ERR_SHAPE, "mma_min_m must be 0 or in [2, 65]");
     g_ctas_per_sm = t->ctas_per_sm;
+    g_mma_min_m = t->mma_min_m;
     return ok();
 }
 
@@ -318,6 +375,16 @@ int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int*
     if (!info) return fail(W4A8_ERR_NULL, "w4a8_plan_info: NULL pointer");
     int st = w8a16 ? check_w8a16_shape(M, K, N) : check_w4a8_shape(M, K, N);
     if (st != W4A8_OK) return st;
+    if (!w8a16) {
+        w4a8::MmaPlan mp;
+        if (mma_plan_for(M, K, N, &mp, num_sms)) {
+            const int ws = mp.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)mp.ws_bytes;
+            const int v[] = {mp.P, 0, mp.BN, 128, mp.tiles, mp.grid, 128, mp.stages, mp.stage_bytes,
+                             mp.smem, ws, 1};
+            for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
+            return ok();
+        }
+    }
     // the plan of the first row group; workspace for the whole call
     w4a8::GemvPlan pl, pt;
     if ((st = plan_row_groups(!w8a16, !w8a16, M, K, N, w8a16 ? kRowGroupW8 : kRowGroupW4, &pl,
@@ -326,7 +393,7 @@ int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int*
     const size_t wsb = pl.ws_bytes > pt.ws_bytes ? pl.ws_bytes : pt.ws_bytes;
     const int ws = wsb > 0x7FFFFFFF ? 0x7FFFFFFF : (int)wsb;
     const int v[] = {pl.P, pl.Cl, pl.S, pl.Rl, pl.Gs, pl.grid, pl.rows_max, pl.NS,
-                     pl.stage_stride, pl.smem, ws};
+                     pl.stage_stride, pl.smem, ws, 0};
     for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
     return ok();
 }

@@ -30,4 +30,13 @@ cudaError_t launch_w8a16(const GemvPlan& pl, const uint16_t* X, int M, int64_t K
 
 cudaError_t read_and_clear_device_error(unsigned* flags, cudaStream_t stream);
 
+// Tensor-core path (mma.cu).  make_mma_plan is host-only and needs no GPU.
+bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out);
+cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* Xq, const float* sa,
+                            int M, int64_t K, int G, const uint8_t* const* Wq,
+                            const float* const* sw, const int64_t* Ns, float* const* Y,
+                            int32_t* acc_out, int8_t* Xq_out, float* sa_out, void* ws,
+                            unsigned flags, cudaStream_t stream);
+cudaError_t read_and_clear_mma_error(unsigned* flags, cudaStream_t stream);
+
 }  // namespace w4a8

@@ -1,0 +1,584 @@
+// mma.cu -- W4A8 linear on the sm_103a tensor cores, for decode batches
+// where the dp4a GEMV turns ALU-bound (the skinny-batch regime, 2..64 rows).
+//
+// The arithmetic is the W4A8 contract of the Jetson INT4 page (sections
+// 正确方向 / 当前实现方式): INT8 activation codes times INT4 weight codes,
+// summed exactly in integers, y = ((float)acc * s_w) * s_a.  Both code sets
+// are small integers and so exact in bf16; tcgen05.mma kind::f16 multiplies
+// them exactly and accumulates in fp32 in TMEM.  Every partial sum of one
+// K piece is an integer of magnitude <= 8 * 127 * 16384 < 2^24, so the fp32
+// accumulator holds it exactly whatever the summation order; pieces are
+// summed as int32 in a fixed order.  The result is bit-identical to the
+// integer definition.
+//
+// Two kernels:
+//  * act_codes_kernel (one CTA per activation row): the per-row INT8
+//    quantization (max|x|, s_a = max/127, IEEE division, round half away,
+//    clamp), written as bf16 codes [M][K] for the tensor cores (plus the
+//    optional int8 codes and scale outputs); or, for the unfused entry,
+//    the given int8 codes widened to bf16.
+//  * mma_kernel: one CTA per 128 weight rows and K piece.  Warp 0 streams
+//    packed INT4 tiles (128 rows x 64 K = 4 KB) with 2-D TMA into a deep
+//    ring; warp 2 streams the bf16 activation tiles (TMA, 128-byte
+//    swizzle) into their own ring; warp 1 issues the MMAs (M = 128 weight
+//    rows, N = 16..64 batch rows, K = 16, four per tile) into a TMEM
+//    accumulator; warps 3-10 widen each INT4 tile to bf16 in the same
+//    swizzled layout (nibble ^ 8 placed in the mantissa of 128.0, minus
+//    136), then read the accumulator back (tcgen05.ld), convert to int32
+//    and rescale, or store int32 partials for the split-K sum.  Every ring
+//    slot is handed back by a tcgen05.commit, so no thread waits for one
+//    MMA to finish before issuing the next.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "plan.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace w4a8 {
+
+__device__ unsigned g_mma_error;  // wait timeouts of the tensor-core path (same bits)
+
+namespace {
+
+constexpr int kTileRows = 128;                  // weight rows per CTA (MMA M)
+constexpr int kKBlock = 64;                     // K per tile: 128 bytes of bf16
+constexpr int kWBlocks = 4;                     // K blocks per weight load: 128 bytes of a row
+constexpr int kWStages = 4;                     // packed INT4 ring (16 KB a stage)
+constexpr int kAStages = 4;                     // bf16 weight tiles (16 KB each)
+constexpr int kBStages = 6;                     // bf16 activation tiles (<= 8 KB each)
+constexpr int kConvWarps = 8;
+constexpr int kFirstConvWarp = 3;
+constexpr int kWordsPerConv = 1024 / (kConvWarps * 32);  // packed words per converter a tile
+constexpr int kMmaThreads = (kFirstConvWarp + kConvWarps) * 32;
+constexpr int kWTileBytes = kTileRows * kKBlock / 2 * kWBlocks;  // 16384
+constexpr int kATileBytes = kTileRows * kKBlock * 2;    // 16384
+constexpr int kBTileMax = 64 * kKBlock * 2;             // 8192 (64 batch rows)
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kAStages * kATileBytes;
+constexpr int kOffW = kOffB + kBStages * kBTileMax;
+constexpr int kOffBars = kOffW + kWStages * kWTileBytes;
+constexpr int kNumBars = 2 * kWStages + 2 * kAStages + 2 * kBStages + 1;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kMmaSmem = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+constexpr int kAQThreads = 256;
+
+static_assert(kOffB % 1024 == 0 && kOffW % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+struct MmaArgs {
+    CUtensorMap tmW;        // packed weights [N][K/2] uint8, box 128 bytes x 128 rows
+    const uint8_t* codes;   // activation tiles [nkb][BN][64] bf16, pre-swizzled
+    const float* sw;        // [N]
+    const float* sa;        // [M]
+    float* Y;               // [M][N]
+    int32_t* acc_out;       // optional [M][N]
+    int32_t* part;          // [grid][M][128] when P > 1 (one block per CTA)
+    unsigned* tickets;      // [tiles] when P > 1, zero between calls
+    int M, N, K, BN, P, nkb, kbp;
+};
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        #pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(&g_mma_error, kErrFullWait);
+            return false;
+        }
+    }
+}
+
+// Waits (bounded, ignoring the abort flag) for a copy this thread issued,
+// so that nothing lands in shared memory after the CTA exits.
+__device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
+    if (!mbar_wait(bar, parity)) atomicOr(&g_mma_error, kErrDrainWait);
+}
+
+__device__ __forceinline__ int act_code(float v, float s) {
+    if (s == 0.f) return 0;
+    const float r = fminf(fmaxf(roundf(__fdiv_rn(v, s)), -127.f), 127.f);
+    return static_cast<int>(r);
+}
+
+// Activation codes for the tensor cores, in the order the MMA reads them:
+// K-block kb (64 codes of every row) is one contiguous [BN][64] bf16 tile of
+// BN * 128 bytes, already in the 128-byte swizzled layout (16-byte chunk c
+// of row m at m * 128 + ((c ^ (m % 8)) * 16)), so one 1-D bulk copy moves
+// a whole tile.  Rows M..BN-1 and codes past K are zero.  One CTA per row
+// (BN CTAs): X [M][K] binary16 quantized here (max|x|, s_a = max/127 by
+// IEEE division, round half away, clamp), or, when X is null, the given
+// int8 codes Xq and scales sa_in; optional int8 codes and scale outputs.
+__global__ void __launch_bounds__(kAQThreads) act_codes_kernel(
+    const __half* __restrict__ X, const int8_t* __restrict__ Xq, const float* __restrict__ sa_in,
+    int M, int64_t K, int BN, uint8_t* __restrict__ B, float* __restrict__ sa_ws,
+    int8_t* __restrict__ Xq_out, float* __restrict__ sa_out) {
+    __shared__ float red[kAQThreads / 32];
+    griddep_launch_dependents();
+    griddep_wait();
+    const int m = blockIdx.x;
+    const int64_t nchunks = (K + kKBlock - 1) / kKBlock * 8;  // 16-byte chunks incl. padding
+    const int64_t kchunks = K / 8;
+    const size_t tile_bytes = (size_t)BN * 128;
+    auto dst = [&](int64_t u) {
+        return reinterpret_cast<uint4*>(B + (u >> 3) * tile_bytes + (size_t)m * 128 +
+                                        ((((int)u & 7) ^ (m & 7)) << 4));
+    };
+    if (m >= M) {
+        for (int64_t u = threadIdx.x; u < nchunks; u += kAQThreads) *dst(u) = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    float s;
+    const uint4* xv = reinterpret_cast<const uint4*>(X + (int64_t)m * K);
+    if (X == nullptr) {
+        s = sa_in[m];
+    } else {
+        float mx = 0.f;
+        for (int64_t u = threadIdx.x; u < kchunks; u += kAQThreads) {
+            const uint4 h = xv[u];
+            const __half* hp = reinterpret_cast<const __half*>(&h);
+            #pragma unroll
+            for (int t = 0; t < 8; ++t) mx = fmaxf(mx, fabsf(__half2float(hp[t])));
+        }
+        #pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+        __syncthreads();
+        mx = 0.f;
+        #pragma unroll
+        for (int w = 0; w < kAQThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+        s = __fdiv_rn(mx, 127.f);
+    }
+    for (int64_t u = threadIdx.x; u < nchunks; u += kAQThreads) {
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        if (u < kchunks) {
+            int q[8];
+            if (X != nullptr) {
+                const uint4 h = xv[u];
+                const __half* hp = reinterpret_cast<const __half*>(&h);
+                uint32_t c8[2] = {0u, 0u};
+                #pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    q[t] = act_code(__half2float(hp[t]), s);
+                    c8[t >> 2] |= ((uint32_t)q[t] & 0xFFu) << (8 * (t & 3));
+                }
+                if (Xq_out != nullptr)
+                    *reinterpret_cast<uint2*>(Xq_out + (int64_t)m * K + 8 * u) = make_uint2(c8[0], c8[1]);
+            } else {
+                const uint2 c8 = *reinterpret_cast<const uint2*>(Xq + (int64_t)m * K + 8 * u);
+                #pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    q[t] = (int)(int8_t)(((t < 4 ? c8.x : c8.y) >> (8 * (t & 3))) & 0xFFu);
+            }
+            #pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const __nv_bfloat162 v = __floats2bfloat162_rn((float)q[2 * t], (float)q[2 * t + 1]);
+                o[t] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+        }
+        *dst(u) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (threadIdx.x == 0) {
+        sa_ws[m] = s;
+        if (sa_out != nullptr) sa_out[m] = s;
+    }
+}
+
+// One packed word (8 INT4 codes, low nibble first) -> 8 bf16 values.
+// n ^ 8 = q + 8 in [0, 15] placed in the mantissa of bf16 128.0 (0x4300)
+// is 136 + q exactly; subtracting 136 gives q.
+__device__ __forceinline__ uint4 int4x8_to_bf16(uint32_t w) {
+    const uint32_t u = w ^ 0x88888888u;
+    const uint32_t h = u >> 4;
+    const __nv_bfloat162 bias = __floats2bfloat162_rn(136.f, 136.f);
+    uint32_t o[4];
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        // byte j of u (even code 2j in its low nibble) to bits 0-3,
+        // byte j of u >> 4 (odd code 2j+1) to bits 16-19
+        const uint32_t x = (__byte_perm(u, h, (uint32_t)(j | ((4 + j) << 8))) & 0x000F000Fu) | 0x43004300u;
+        const __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&x), bias);
+        o[j] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_constant__ MmaArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned base for the swizzled tiles
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sbase = smem_u32(smem);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int tile = blockIdx.x / a.P;
+    const int p = blockIdx.x % a.P;
+    const int n0 = tile * kTileRows;
+    const int kb0 = p * a.kbp;
+    const int nk = min(a.nkb, kb0 + a.kbp) - kb0;  // >= 1 by the plan
+    const int BN = a.BN;
+    const uint32_t b_bytes = (uint32_t)BN * kKBlock * 2;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+    uint64_t* wfull = bars;
+    uint64_t* wempty = wfull + kWStages;
+    uint64_t* afull = wempty + kWStages;
+    uint64_t* aempty = afull + kAStages;
+    uint64_t* bfull = aempty + kAStages;
+    uint64_t* bempty = bfull + kBStages;
+    uint64_t* accfull = bempty + kBStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
+    // 256 of the SM's 512 TMEM columns: the accumulator needs BN <= 64 and
+    // the kernel runs one CTA per SM.
+    const uint32_t ncols = 256u;
+
+    if (tid == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(smem_u32(wfull + s), 1);
+            mbar_init(smem_u32(wempty + s), kConvWarps);
+        }
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(smem_u32(afull + s), kConvWarps);
+            mbar_init(smem_u32(aempty + s), 1);
+        }
+        for (int s = 0; s < kBStages; ++s) {
+            mbar_init(smem_u32(bfull + s), 1);
+            mbar_init(smem_u32(bempty + s), 1);
+        }
+        mbar_init(smem_u32(accfull), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), ncols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    griddep_launch_dependents();
+
+    if (warp == 0) {
+        // ---- producer: packed INT4 tiles (weights may be read before the
+        // dependency wait)
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            int issued = 0;
+            const int nw = (nk + kWBlocks - 1) / kWBlocks;  // loads of kWBlocks K blocks each
+            for (int i = 0; i < nw; ++i) {
+                const int s = i % kWStages;
+                if (i >= kWStages && !wait_bounded(smem_u32(wempty + s), ((i / kWStages) - 1) & 1, abort_flag))
+                    break;
+                mbar_arrive_expect_tx(smem_u32(wfull + s), kWTileBytes);
+                tma_load_2d_hint(sbase + kOffW + s * kWTileBytes, &a.tmW, (kb0 + kWBlocks * i) * (kKBlock / 2),
+                                 n0, smem_u32(wfull + s), pol);
+                issued = i + 1;
+            }
+            for (int i = max(0, issued - kWStages); i < issued; ++i)
+                drain(smem_u32(wfull + i % kWStages), (i / kWStages) & 1);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer (one lane)
+        if (lane == 0) {
+            const uint32_t idesc = bf16_idesc(kTileRows, BN);
+            for (int i = 0; i < nk; ++i) {
+                const int sa_ = i % kAStages, sb = i % kBStages;
+                if (!wait_bounded(smem_u32(afull + sa_), (i / kAStages) & 1, abort_flag)) break;
+                if (!wait_bounded(smem_u32(bfull + sb), (i / kBStages) & 1, abort_flag)) break;
+                tc_fence_after_sync();
+                const uint64_t ad = sw128_desc(sbase + kOffA + sa_ * kATileBytes);
+                const uint64_t bd = sw128_desc(sbase + kOffB + sb * kBTileMax);
+                #pragma unroll
+                for (int k = 0; k < kKBlock / 16; ++k)  // 32 bytes of K per MMA: +2 in the address field
+                    tc_mma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, i > 0 || k > 0);
+                tc_commit(smem_u32(aempty + sa_));  // both slots free once these MMAs are done
+                tc_commit(smem_u32(bempty + sb));
+            }
+            tc_commit(smem_u32(accfull));  // every MMA issued so far
+        }
+    } else if (warp == 2) {
+        // ---- activation tiles (one lane)
+        if (lane == 0) {
+            griddep_wait();  // the bf16 codes come from the previous kernel
+            const uint64_t pol = l2_evict_last_policy();
+            int issued = 0;
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % kBStages;
+                if (i >= kBStages && !wait_bounded(smem_u32(bempty + s), ((i / kBStages) - 1) & 1, abort_flag))
+                    break;
+                mbar_arrive_expect_tx(smem_u32(bfull + s), b_bytes);
+                bulk_g2s(sbase + kOffB + s * kBTileMax, a.codes + (size_t)(kb0 + i) * b_bytes, b_bytes,
+                         smem_u32(bfull + s), pol);
+                issued = i + 1;
+            }
+            for (int i = max(0, issued - kBStages); i < issued; ++i)
+                drain(smem_u32(bfull + i % kBStages), (i / kBStages) & 1);
+        }
+    } else {
+        // ---- converters: INT4 tile -> bf16 tile in the swizzled layout
+        const int ct = tid - kFirstConvWarp * 32;  // 0 .. 32 * kConvWarps - 1
+        for (int i = 0; i < nk; ++i) {
+            const int t = i / kWBlocks, sub = i % kWBlocks;
+            const int ws = t % kWStages;
+            // warp-uniform outcome: a lane may time out while another sees the phase
+            if (!__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(wfull + ws), (t / kWStages) & 1, abort_flag)))
+                break;
+            // row r of the load holds kWBlocks x 32 bytes; this stage's are at sub * 32
+            const uint32_t* wt = reinterpret_cast<const uint32_t*>(smem + kOffW + ws * kWTileBytes) + sub * 8;
+            uint32_t w[kWordsPerConv];
+            #pragma unroll
+            for (int q = 0; q < kWordsPerConv; ++q) {
+                const int idx = ct + kConvWarps * 32 * q;  // row idx / 8, word idx % 8
+                w[q] = wt[(idx >> 3) * (8 * kWBlocks) + (idx & 7)];
+            }
+            __syncwarp();
+            if (lane == 0 && (sub == kWBlocks - 1 || i == nk - 1)) mbar_arrive(smem_u32(wempty + ws));
+            const int s = i % kAStages;
+            if (i >= kAStages &&
+                !__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(aempty + s), ((i / kAStages) - 1) & 1, abort_flag)))
+                break;
+            uint8_t* at = smem + kOffA + s * kATileBytes;
+            #pragma unroll
+            for (int q = 0; q < kWordsPerConv; ++q) {
+                const int idx = ct + kConvWarps * 32 * q;
+                const int r = idx >> 3, c = idx & 7;
+                *reinterpret_cast<uint4*>(at + r * 128 + ((c ^ (r & 7)) << 4)) = int4x8_to_bf16(w[q]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(afull + s));
+        }
+
+        // ---- epilogue: TMEM lanes = weight rows, columns = batch rows
+        griddep_wait();  // scales and outputs
+        const bool ok = __all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(accfull), 0, abort_flag));
+        tc_fence_after_sync();
+        const int quarter = warp & 3;  // the TMEM lanes this warp may read
+        const int group = (warp - kFirstConvWarp) >> 2;  // warps with the same quarter split the columns
+        const int r = quarter * 32 + lane;
+        const int n = n0 + r;
+        const float swv = (ok && n < a.N) ? a.sw[n] : 0.f;
+        for (int ch = group; ch < BN / 8; ch += kConvWarps / 4) {
+            uint32_t v[8];
+            tmem_ld8(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(8 * ch), v);
+            if (!ok || n >= a.N) continue;
+            #pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int m = 8 * ch + t;
+                if (m >= a.M) break;
+                const int32_t acc = __float2int_rn(__uint_as_float(v[t]));
+                const int64_t o = (int64_t)m * a.N + n;
+                if (a.P == 1) {
+                    a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), swv), a.sa[m]);
+                    if (a.acc_out != nullptr) a.acc_out[o] = acc;
+                } else {
+                    a.part[((int64_t)blockIdx.x * a.M + m) * kTileRows + r] = acc;
+                }
+            }
+        }
+        if (a.P > 1) {
+            // the last CTA of this tile sums the pieces in a fixed order
+            __threadfence();
+            named_bar_sync(1, kConvWarps * 32);
+            if (ct == 0) *last_flag = (atomicAdd(a.tickets + tile, 1u) == (unsigned)(a.P - 1));
+            named_bar_sync(1, kConvWarps * 32);
+            if (*last_flag) {
+                __threadfence();
+                const int rows = min(kTileRows, a.N - n0);
+                for (int e = ct; e < a.M * rows; e += kConvWarps * 32) {
+                    const int m = e / rows, rr = e % rows, nn = n0 + rr;
+                    const int64_t o = (int64_t)m * a.N + nn;
+                    int32_t acc = 0;
+                    for (int q = 0; q < a.P; ++q)
+                        acc += __ldcg(a.part + ((int64_t)(tile * a.P + q) * a.M + m) * kTileRows + rr);
+                    a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), a.sw[nn]), a.sa[m]);
+                    if (a.acc_out != nullptr) a.acc_out[o] = acc;
+                }
+                if (ct == 0) a.tickets[tile] = 0u;  // ready for the next call
+            }
+        }
+    }
+
+    // every MMA has completed (accfull) before TMEM is released
+    if (tid == 32) drain(smem_u32(accfull), 0);
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, ncols);
+    }
+}
+
+// --------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swz) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       unsigned flags, void** args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (flags & 1u) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace
+
+bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out) {
+    if (M < 1 || M > 64 || K < 32 || K % 32 || N < 1 || N > 0x7FFFFFFF) return false;
+    MmaPlan pl = {};
+    pl.BN = (M + 15) / 16 * 16;
+    pl.tiles = (int)((N + kTileRows - 1) / kTileRows);
+    pl.nkb = (int)((K + kKBlock - 1) / kKBlock);
+    // split K when the tiles alone leave SMs idle; pieces of at most 256
+    // K-blocks (16384) keep every fp32 partial sum exact
+    int P = 1;
+    if (pl.tiles < num_sms * 4 / 5) P = num_sms / pl.tiles;
+    if (P < 1) P = 1;
+    const int pmin = (pl.nkb + 255) / 256;
+    if (P < pmin) P = pmin;
+    if (P > pl.nkb) P = pl.nkb;
+    if (P > 64) P = 64;
+    // pieces of whole weight loads (kWBlocks K blocks), none empty
+    pl.kbp = (pl.nkb + P - 1) / P;
+    pl.kbp = (pl.kbp + kWBlocks - 1) / kWBlocks * kWBlocks;
+    pl.P = (pl.nkb + pl.kbp - 1) / pl.kbp;
+    if (pl.kbp > 256) return false;
+    if (pl.P > 1 && pl.tiles > kTicketSlots) return false;
+    if ((int64_t)pl.tiles * pl.P > 0x7FFFFFFF) return false;
+    pl.grid = pl.tiles * pl.P;
+    pl.smem = kMmaSmem;
+    pl.sms = num_sms;
+    pl.stages = kWStages;
+    pl.stage_bytes = kWTileBytes;
+    // workspace: tickets, scales (64 floats), bf16 code tiles [nkb][BN][64], then an
+    // int32 [M][128] block per CTA for split-K partials.  The partial region
+    // is sized for any N' <= N on this device (grouped launches run one
+    // plan per weight matrix): a split plan has at most max(SMs, tiles *
+    // pieces forced by the 16384-wide exactness limit) CTAs.
+    pl.off_sa = kTicketBytes;
+    pl.off_codes = pl.off_sa + 256;
+    pl.off_part = round_up_sz(pl.off_codes + (size_t)pl.nkb * pl.BN * kKBlock * 2, 256);
+    const int64_t gmax = pmin > 1 ? ((int64_t)pl.tiles * pmin > num_sms ? (int64_t)pl.tiles * pmin : num_sms)
+                                  : num_sms;
+    pl.ws_bytes = pl.off_part + round_up_sz((size_t)gmax * M * kTileRows * 4, 256);
+    *out = pl;
+    return true;
+}
+
+cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* Xq, const float* sa,
+                            int M, int64_t K, int G, const uint8_t* const* Wq,
+                            const float* const* sw, const int64_t* Ns, float* const* Y,
+                            int32_t* acc_out, int8_t* Xq_out, float* sa_out, void* ws,
+                            unsigned flags, cudaStream_t stream) {
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    float* sa_ws = reinterpret_cast<float*>(wsb + pl.off_sa);
+    uint8_t* codes = wsb + pl.off_codes;
+    {
+        const __half* xh = reinterpret_cast<const __half*>(X);
+        int Mi = M, BNi = pl.BN;
+        int64_t Kk = K;
+        void* args[] = {&xh, &Xq, &sa, &Mi, &Kk, &BNi, &codes, &sa_ws, &Xq_out, &sa_out};
+        cudaError_t e = launch_pdl(reinterpret_cast<const void*>(act_codes_kernel), dim3(pl.BN),
+                                   dim3(kAQThreads), 0, stream, flags, args);
+        if (e != cudaSuccess) return e;
+    }
+    static int attr_set[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = 1;
+    }
+    for (int g = 0; g < G; ++g) {
+        MmaPlan pg;
+        if (!make_mma_plan(M, K, Ns[g], pl.sms, &pg)) return cudaErrorInvalidValue;
+        MmaArgs a;
+        memset(&a, 0, sizeof(a));
+        if (!encode_2d(&a.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq[g], (uint64_t)(K / 2), (uint64_t)Ns[g],
+                       (uint64_t)(K / 2), kWBlocks * kKBlock / 2, kTileRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+        a.codes = codes;
+        a.sw = sw[g];
+        a.sa = sa_ws;
+        a.Y = Y[g];
+        a.acc_out = (G == 1) ? acc_out : nullptr;
+        a.part = reinterpret_cast<int32_t*>(wsb + pg.off_part);
+        a.tickets = reinterpret_cast<unsigned*>(wsb);
+        a.M = M;
+        a.N = (int)Ns[g];
+        a.K = (int)K;
+        a.BN = pg.BN;
+        a.P = pg.P;
+        a.nkb = pg.nkb;
+        a.kbp = pg.kbp;
+        void* args[] = {&a};
+        e = launch_pdl(reinterpret_cast<const void*>(mma_kernel), dim3(pg.grid), dim3(kMmaThreads),
+                       kMmaSmem, stream, flags, args);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t read_and_clear_mma_error(unsigned* flags, cudaStream_t stream) {
+    unsigned v = 0, z = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_mma_error, sizeof(v), 0, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbolAsync(g_mma_error, &z, sizeof(z), 0, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    *flags |= v;
+    return e;
+}
+
+}  // namespace w4a8

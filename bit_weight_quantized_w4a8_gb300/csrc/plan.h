@@ -59,6 +59,18 @@ struct Tuning {
     int ctas_per_sm;    // 0 = default (1), else CTAs per SM per K piece
 };
 
+// Launch plan of the tensor-core path (csrc/mma.cu).
+struct MmaPlan {
+    int BN;            // batch rows padded to a multiple of 16 (the MMA's N)
+    int tiles;         // 128-row weight tiles
+    int nkb;           // 64-wide K blocks
+    int P, kbp;        // K pieces, K blocks per piece
+    int grid, smem, sms;
+    int stages, stage_bytes;             // weight ring
+    size_t off_sa, off_codes, off_part;  // workspace layout
+    size_t ws_bytes;
+};
+
 inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 inline size_t round_up_sz(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -71,11 +71,16 @@ typedef enum {
    workspace are only touched after the wait. */
 #define W4A8_LAUNCH_PDL 1u
 
-/* Maximum activation rows (decode batch) per call.  One kernel launch
- * handles up to 8 rows (W8A16: 4); a call with more rows runs one launch
- * per group of that many rows, in order on `stream`, and each of them
- * streams the whole weight matrix again.  w4a8_linear_noalloc takes at
- * most 8 rows. */
+/* Maximum activation rows (decode batch) per call.  W4A8 calls with at
+ * least 16 rows (see w4a8_tuning_t.mma_min_m) run on the tensor cores: an
+ * activation-quantization launch writes bf16 codes into the workspace, then
+ * tcgen05 MMAs of 128 weight rows x the batch accumulate the integer
+ * products exactly in fp32 (every partial sum of one K piece of at most
+ * 16384 is an integer below 2^24) and the rescale matches the dp4a path
+ * bit for bit.  Smaller batches use the dp4a kernel, one launch per group
+ * of up to 8 rows (W8A16: 4 rows, always dp4a-free fp32 FMAs), each
+ * streaming the whole weight matrix.  w4a8_linear_noalloc takes at most 8
+ * rows. */
 #define W4A8_MAX_M 64
 #define W8A16_MAX_M 64
 
@@ -234,6 +239,8 @@ int w4a8_device_error(unsigned* flags, void* stream);
  *   force_threads_per_row: threads sharing one row-piece (power of 2, <=256).
  *   ring_bytes: target size of the shared-memory weight ring (<= 204800).
  *   ctas_per_sm: CTAs per SM for each K piece (1..4; 0 = 1).
+ *   mma_min_m: activation rows from which the W4A8 entry points use the
+ *     tensor-core kernel (2..65; 0 = default, 65 = never).
  * w4a8_workspace_bytes reflects the overrides.  NULL restores the defaults.
  * Not synchronised with calls running on other threads. */
 typedef struct {
@@ -241,6 +248,7 @@ typedef struct {
     int force_threads_per_row;
     int ring_bytes;
     int ctas_per_sm;
+    int mma_min_m;
 } w4a8_tuning_t;
 
 int w4a8_set_tuning(const w4a8_tuning_t* tuning);
@@ -249,7 +257,10 @@ int w4a8_set_tuning(const w4a8_tuning_t* tuning);
  * would use for this shape, in this order: splits P, threads per row-piece,
  * granule columns per thread, row-pieces per stage, CTAs per piece, grid
  * size, most rows per CTA, ring stages, bytes per stage, dynamic shared
- * memory bytes, workspace bytes (saturated at INT32_MAX).  w8a16 != 0
+ * memory bytes, workspace bytes (saturated at INT32_MAX), and 1 when the
+ * tensor-core kernel serves the call (then the fields read: K pieces, 0,
+ * batch rows padded to 16, 128 weight rows per tile, tiles, grid, 128,
+ * ring stages, bytes per stage, shared memory, workspace).  w8a16 != 0
  * selects w8a16_gemv.  num_sms > 0 plans for a device with that many SMs
  * without touching any GPU (host-side testing); 0 queries the current
  * device. */

@@ -118,6 +118,9 @@ def test_plan_invariants(sms, w8):
         if w8 and K > 65536:
             continue
         p = w4.w4a8_plan_info(M, K, N, w8a16=w8, num_sms=sms)
+        if p["tensor_cores"]:
+            check_mma_plan(p, M, K, N, sms)
+            continue
         M = min(M, 4 if w8 else 8)  # the plan of the first launch of a row-group sequence
         kgran = 16 if w8 else 32
         Gt = K // kgran
@@ -138,6 +141,34 @@ def test_plan_invariants(sms, w8):
         assert p["smem_bytes"] <= 232448
         if P > 1:
             assert p["ws_bytes"] > 0
+
+
+def check_mma_plan(p, M, K, N, sms):
+    assert M >= 16
+    tiles = -(-N // 128)
+    nkb = -(-K // 64)
+    P = p["splits"]
+    assert p["cols_per_thread"] == -(-M // 16) * 16 <= 64      # the MMA's N
+    assert p["ctas_per_split"] == tiles and p["grid"] == tiles * P
+    kbp = -(-nkb // P)
+    assert kbp <= 256 and (P - 1) * kbp < nkb                   # pieces <= 16384, none empty
+    assert p["smem_bytes"] <= 232448
+    assert p["ws_bytes"] >= 4096 + 256 + M * K * 2
+
+
+def test_tensor_core_threshold():
+    try:
+        assert w4.w4a8_plan_info(15, 3584, 18944, num_sms=152)["tensor_cores"] == 0
+        assert w4.w4a8_plan_info(16, 3584, 18944, num_sms=152)["tensor_cores"] == 1
+        w4.w4a8_set_tuning(mma_min_m=65)
+        assert w4.w4a8_plan_info(64, 3584, 18944, num_sms=152)["tensor_cores"] == 0
+        w4.w4a8_set_tuning(mma_min_m=2)
+        assert w4.w4a8_plan_info(2, 3584, 18944, num_sms=152)["tensor_cores"] == 1
+        assert w4.w4a8_plan_info(1, 3584, 18944, num_sms=152)["tensor_cores"] == 0
+        with pytest.raises(w4.W4A8Error):
+            w4.w4a8_set_tuning(mma_min_m=1)
+    finally:
+        w4.w4a8_set_tuning(reset=True)
 
 
 def test_forced_plans_respected():

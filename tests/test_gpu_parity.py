@@ -222,6 +222,74 @@ def test_w4a8_fused_ties(w4, orc, M, K, N, splits):
     assert np.array_equal(bits(Y.cpu().numpy()), bits(Y_ref))
 
 
+# ---------------------------------------------------------------------------
+# tensor-core path (batches of 16+ rows by default; forced down to 2 here)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,N,seed", [(2, 3584, 300, 100), (5, 896, 129, 101), (15, 128, 256, 102),
+                                        (16, 18944, 200, 103), (24, 96, 1, 104), (64, 3584, 129, 105)])
+@pytest.mark.parametrize("fused", [True, False])
+def test_w4a8_tensor_cores(w4, orc, M, K, N, seed, fused):
+    w4.w4a8_set_tuning(mma_min_m=2)
+    assert w4.w4a8_plan_info(M, K, N)["tensor_cores"] == 1
+    check_w4a8(w4, orc, M, K, N, seed, fused=fused, zero_rows=(0,))
+
+
+def test_w4a8_tensor_cores_grouped(w4, orc):
+    w4.w4a8_set_tuning(mma_min_m=2)
+    M, K, Ns = 18, 1024, (300, 7, 129)
+    X = synth.activation(110, M, K, outlier_frac=0.001)
+    Wqs, sws, refs = [], [], []
+    for g, N in enumerate(Ns):
+        W = weights(N, K, 111 + g)
+        Wq_ref, sw_ref = orc.w4_quantize(W)
+        refs.append(orc.w4a8_linear(X, Wq_ref, sw_ref)[0])
+        Wq, sw = w4.w4_quantize_weights(to_dev(W))
+        Wqs.append(Wq)
+        sws.append(sw)
+    for rep in range(2):
+        Ys = w4.w4a8_linear_grouped(to_dev(X), Wqs, sws, flags=w4.LAUNCH_PDL if rep else 0)
+        torch.cuda.synchronize()
+        for Y, ref in zip(Ys, refs):
+            assert np.array_equal(bits(Y.cpu().numpy()), bits(ref))
+
+
+@pytest.mark.parametrize("K", [16384, 32768])
+def test_w4a8_tensor_cores_largest_sums(w4, K):
+    """Every weight code -8 (nibble 0x8, legal on input) against activation
+    codes +127 and -127: each K piece's partial sum reaches 8 * 127 * 16384 =
+    16,646,144, just below 2^24, which the fp32 accumulator must hold
+    exactly; the pieces are added as int32."""
+    w4.w4a8_set_tuning(mma_min_m=2)
+    M, N = 16, 130
+    Wq = torch.full((N, K // 2), 0x88, dtype=torch.uint8, device="cuda")
+    sw = torch.ones((N,), dtype=torch.float32, device="cuda")
+    Xq = torch.full((M, K), 127, dtype=torch.int8, device="cuda")
+    Xq[1::2] = -127
+    sa = torch.ones((M,), dtype=torch.float32, device="cuda")
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    Y = w4.w4a8_gemv(Xq, sa, Wq, sw, acc_out=acc)
+    torch.cuda.synchronize()
+    want = np.where(np.arange(M)[:, None] % 2 == 0, -1016 * K, 1016 * K) * np.ones((1, N), np.int64)
+    assert np.array_equal(acc.cpu().numpy(), want)
+    assert np.array_equal(Y.cpu().numpy(), want.astype(np.float32))
+
+
+def test_w4a8_tensor_cores_match_dp4a(w4, orc):
+    """The same call on both paths gives the same bits."""
+    M, K, N = 12, 3584, 1000
+    W = weights(N, K, 120)
+    X = to_dev(synth.activation(121, M, K, outlier_frac=0.001))
+    Wq, sw = w4.w4_quantize_weights(to_dev(W))
+    w4.w4a8_set_tuning(mma_min_m=65)
+    assert w4.w4a8_plan_info(M, K, N)["tensor_cores"] == 0
+    Y0 = w4.w4a8_linear(X, Wq, sw)
+    w4.w4a8_set_tuning(mma_min_m=2)
+    Y1 = w4.w4a8_linear(X, Wq, sw)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(Y0.cpu().numpy()), bits(Y1.cpu().numpy()))
+
+
 @pytest.mark.parametrize("cl", [1, 2, 8, 32, 64, 128, 256])
 def test_w4a8_threads_per_row(w4, orc, cl):
     w4.w4a8_set_tuning(force_threads_per_row=cl)
