@@ -22,12 +22,14 @@
 //    ring; warp 2 streams the bf16 activation tiles (TMA, 128-byte
 //    swizzle) into their own ring; warp 1 issues the MMAs (M = 128 weight
 //    rows, N = 16..64 batch rows, K = 16, four per tile) into a TMEM
-//    accumulator; warps 3-10 widen each INT4 tile to bf16 in the same
-//    swizzled layout (nibble ^ 8 placed in the mantissa of 128.0, minus
-//    136), then read the accumulator back (tcgen05.ld), convert to int32
-//    and rescale, or store int32 partials for the split-K sum.  Every ring
-//    slot is handed back by a tcgen05.commit, so no thread waits for one
-//    MMA to finish before issuing the next.
+//    accumulator; warps 3-10 widen each weight row's INT4 codes to bf16
+//    (nibble ^ 8 placed in the mantissa of 128.0, minus 136) straight into
+//    TMEM, where the MMA reads its A operand (so the widened weights never
+//    pass through shared memory, whose bandwidth would otherwise bound the
+//    kernel), then read the accumulator back (tcgen05.ld), convert to
+//    int32 and rescale, or store int32 partials for the split-K sum.  Every
+//    ring slot is handed back by a tcgen05.commit, so no thread waits for
+//    one MMA to finish before issuing the next.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -50,28 +52,32 @@ __device__ unsigned g_mma_error;  // wait timeouts of the tensor-core path (same
 namespace {
 
 constexpr int kTileRows = 128;                  // weight rows per CTA (MMA M)
-constexpr int kKBlock = 64;                     // K per tile: 128 bytes of bf16
+constexpr int kKBlock = 64;                     // K block: 128 bytes of bf16 per row
+constexpr int kStageK = 2;                      // K blocks per pipeline stage (8 MMAs, one commit)
 constexpr int kWBlocks = 4;                     // K blocks per weight load: 128 bytes of a row
-constexpr int kWStages = 4;                     // packed INT4 ring (16 KB a stage)
-constexpr int kAStages = 4;                     // bf16 weight tiles (16 KB each)
-constexpr int kBStages = 6;                     // bf16 activation tiles (<= 8 KB each)
-constexpr int kConvWarps = 8;
+constexpr int kWStages = 4;                     // packed INT4 ring (16 KB a load)
+constexpr int kStages = 4;                      // stage ring: A in TMEM, B in shared memory
+constexpr int kConvGroups = 2;                  // converter warp groups, alternating stages
+constexpr int kConvWarps = 4 * kConvGroups;     // one warp per TMEM lane quarter per group
 constexpr int kFirstConvWarp = 3;
-constexpr int kWordsPerConv = 1024 / (kConvWarps * 32);  // packed words per converter a tile
 constexpr int kMmaThreads = (kFirstConvWarp + kConvWarps) * 32;
 constexpr int kWTileBytes = kTileRows * kKBlock / 2 * kWBlocks;  // 16384
-constexpr int kATileBytes = kTileRows * kKBlock * 2;    // 16384
-constexpr int kBTileMax = 64 * kKBlock * 2;             // 8192 (64 batch rows)
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kAStages * kATileBytes;
-constexpr int kOffW = kOffB + kBStages * kBTileMax;
+constexpr int kBTileMax = 64 * kKBlock * 2;     // one K block of 64 batch rows: 8192
+constexpr int kBStageMax = kStageK * kBTileMax;
+constexpr uint32_t kTmemCols = 512;             // D: columns 0..63; A stage s: 64 + 64 s
+constexpr uint32_t kTmemA = 64;
+constexpr uint32_t kTmemAStage = 32 * kStageK;  // two bf16 per column
+constexpr int kOffB = 0;
+constexpr int kOffW = kOffB + kStages * kBStageMax;
 constexpr int kOffBars = kOffW + kWStages * kWTileBytes;
-constexpr int kNumBars = 2 * kWStages + 2 * kAStages + 2 * kBStages + 1;
+constexpr int kNumBars = 2 * kWStages + 3 * kStages + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kMmaSmem = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
 constexpr int kAQThreads = 256;
 
+static_assert(kWBlocks % kStageK == 0 && kStages % kConvGroups == 0, "stage geometry");
 static_assert(kOffB % 1024 == 0 && kOffW % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(kTmemA + kTmemAStage * kStages <= kTmemCols, "TMEM budget");
 
 struct MmaArgs {
     CUtensorMap tmW;        // packed weights [N][K/2] uint8, box 128 bytes x 128 rows
@@ -236,30 +242,25 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
     uint64_t* wfull = bars;
     uint64_t* wempty = wfull + kWStages;
-    uint64_t* afull = wempty + kWStages;
-    uint64_t* aempty = afull + kAStages;
-    uint64_t* bfull = aempty + kAStages;
-    uint64_t* bempty = bfull + kBStages;
-    uint64_t* accfull = bempty + kBStages;
+    uint64_t* afull = wempty + kWStages;  // A stage written (4 converter warps)
+    uint64_t* bfull = afull + kStages;    // B stage landed
+    uint64_t* sempty = bfull + kStages;   // stage consumed by the MMAs (commit)
+    uint64_t* accfull = sempty + kStages;
+    const int nst = (nk + kStageK - 1) / kStageK;  // stages of this piece
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
     int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
-    // 256 of the SM's 512 TMEM columns: the accumulator needs BN <= 64 and
-    // the kernel runs one CTA per SM.
-    const uint32_t ncols = 256u;
+    const uint32_t ncols = kTmemCols;  // of the SM's 512; one CTA per SM
 
     if (tid == 0) {
         for (int s = 0; s < kWStages; ++s) {
             mbar_init(smem_u32(wfull + s), 1);
-            mbar_init(smem_u32(wempty + s), kConvWarps);
+            mbar_init(smem_u32(wempty + s), 4 * (kWBlocks / kStageK));  // each stage read by 4 warps
         }
-        for (int s = 0; s < kAStages; ++s) {
-            mbar_init(smem_u32(afull + s), kConvWarps);
-            mbar_init(smem_u32(aempty + s), 1);
-        }
-        for (int s = 0; s < kBStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(afull + s), 4);  // the 4 lane quarters of one group
             mbar_init(smem_u32(bfull + s), 1);
-            mbar_init(smem_u32(bempty + s), 1);
+            mbar_init(smem_u32(sempty + s), 1);
         }
         mbar_init(smem_u32(accfull), 1);
         *abort_flag = 0;
@@ -292,73 +293,91 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
                 drain(smem_u32(wfull + i % kWStages), (i / kWStages) & 1);
         }
     } else if (warp == 1) {
-        // ---- MMA issuer (one lane)
+        // ---- MMA issuer (one lane): per stage up to kStageK K blocks of
+        // four K = 16 steps, then one commit that frees the stage
         if (lane == 0) {
             const uint32_t idesc = bf16_idesc(kTileRows, BN);
-            for (int i = 0; i < nk; ++i) {
-                const int sa_ = i % kAStages, sb = i % kBStages;
-                if (!wait_bounded(smem_u32(afull + sa_), (i / kAStages) & 1, abort_flag)) break;
-                if (!wait_bounded(smem_u32(bfull + sb), (i / kBStages) & 1, abort_flag)) break;
+            for (int st = 0; st < nst; ++st) {
+                const int s = st % kStages;
+                const uint32_t ph = (st / kStages) & 1;
+                if (!wait_bounded(smem_u32(afull + s), ph, abort_flag)) break;
+                if (!wait_bounded(smem_u32(bfull + s), ph, abort_flag)) break;
                 tc_fence_after_sync();
-                const uint64_t ad = sw128_desc(sbase + kOffA + sa_ * kATileBytes);
-                const uint64_t bd = sw128_desc(sbase + kOffB + sb * kBTileMax);
-                #pragma unroll
-                for (int k = 0; k < kKBlock / 16; ++k)  // 32 bytes of K per MMA: +2 in the address field
-                    tc_mma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, i > 0 || k > 0);
-                tc_commit(smem_u32(aempty + sa_));  // both slots free once these MMAs are done
-                tc_commit(smem_u32(bempty + sb));
+                const int nkb = min(kStageK, nk - kStageK * st);
+                const uint32_t at = tmem + kTmemA + kTmemAStage * s;
+                for (int j = 0; j < nkb; ++j) {
+                    const uint64_t bd = sw128_desc(sbase + kOffB + s * kBStageMax + j * b_bytes);
+                    #pragma unroll
+                    for (int k = 0; k < kKBlock / 16; ++k)  // 8 TMEM columns of A, 32 bytes of B a step
+                        tc_mma_bf16_tmem_a(tmem, at + 32 * j + 8 * k, bd + 2 * k, idesc, st > 0 || j > 0 || k > 0);
+                }
+                tc_commit(smem_u32(sempty + s));
             }
             tc_commit(smem_u32(accfull));  // every MMA issued so far
         }
     } else if (warp == 2) {
-        // ---- activation tiles (one lane)
+        // ---- activation tiles (one lane): the K blocks of a stage are
+        // adjacent in the tiled codes, one bulk copy each
         if (lane == 0) {
             griddep_wait();  // the bf16 codes come from the previous kernel
             const uint64_t pol = l2_evict_last_policy();
             int issued = 0;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % kBStages;
-                if (i >= kBStages && !wait_bounded(smem_u32(bempty + s), ((i / kBStages) - 1) & 1, abort_flag))
+            for (int st = 0; st < nst; ++st) {
+                const int s = st % kStages;
+                if (st >= kStages && !wait_bounded(smem_u32(sempty + s), ((st / kStages) - 1) & 1, abort_flag))
                     break;
-                mbar_arrive_expect_tx(smem_u32(bfull + s), b_bytes);
-                bulk_g2s(sbase + kOffB + s * kBTileMax, a.codes + (size_t)(kb0 + i) * b_bytes, b_bytes,
-                         smem_u32(bfull + s), pol);
-                issued = i + 1;
+                const uint32_t bytes = (uint32_t)min(kStageK, nk - kStageK * st) * b_bytes;
+                mbar_arrive_expect_tx(smem_u32(bfull + s), bytes);
+                bulk_g2s(sbase + kOffB + s * kBStageMax, a.codes + (size_t)(kb0 + kStageK * st) * b_bytes,
+                         bytes, smem_u32(bfull + s), pol);
+                issued = st + 1;
             }
-            for (int i = max(0, issued - kBStages); i < issued; ++i)
-                drain(smem_u32(bfull + i % kBStages), (i / kBStages) & 1);
+            for (int st = max(0, issued - kStages); st < issued; ++st)
+                drain(smem_u32(bfull + st % kStages), (st / kStages) & 1);
         }
     } else {
-        // ---- converters: INT4 tile -> bf16 tile in the swizzled layout
-        const int ct = tid - kFirstConvWarp * 32;  // 0 .. 32 * kConvWarps - 1
-        for (int i = 0; i < nk; ++i) {
-            const int t = i / kWBlocks, sub = i % kWBlocks;
+        // ---- converters: each thread widens its weight row's 64 codes of a
+        // stage to bf16 and stores them into the stage's TMEM columns (the
+        // MMA's A operand); the two groups take alternate stages
+        const int cg = (warp - kFirstConvWarp) >> 2;
+        const int q = warp & 3;         // TMEM lanes 32q .. 32q + 31
+        const int r = 32 * q + lane;    // weight row within the tile
+        for (int st = cg; st < nst; st += kConvGroups) {
+            const int kb = kStageK * st;  // first K block of the stage (within the piece)
+            const int t = kb / kWBlocks, sub = kb % kWBlocks;
             const int ws = t % kWStages;
             // warp-uniform outcome: a lane may time out while another sees the phase
             if (!__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(wfull + ws), (t / kWStages) & 1, abort_flag)))
                 break;
-            // row r of the load holds kWBlocks x 32 bytes; this stage's are at sub * 32
-            const uint32_t* wt = reinterpret_cast<const uint32_t*>(smem + kOffW + ws * kWTileBytes) + sub * 8;
-            uint32_t w[kWordsPerConv];
+            // 128-byte rows swizzled by the TMA: 16-byte chunk c of row r at (c ^ r % 8) * 16;
+            // K block sub + j of the load is chunks 2(sub + j) and 2(sub + j) + 1
+            const uint8_t* row = smem + kOffW + ws * kWTileBytes + r * 128;
+            uint4 c16[2 * kStageK];
             #pragma unroll
-            for (int q = 0; q < kWordsPerConv; ++q) {
-                const int idx = ct + kConvWarps * 32 * q;  // row idx / 8, word idx % 8
-                w[q] = wt[(idx >> 3) * (8 * kWBlocks) + (idx & 7)];
-            }
+            for (int c = 0; c < 2 * kStageK; ++c)
+                c16[c] = *reinterpret_cast<const uint4*>(row + (((2 * sub + c) ^ (r & 7)) << 4));
             __syncwarp();
-            if (lane == 0 && (sub == kWBlocks - 1 || i == nk - 1)) mbar_arrive(smem_u32(wempty + ws));
-            const int s = i % kAStages;
-            if (i >= kAStages &&
-                !__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(aempty + s), ((i / kAStages) - 1) & 1, abort_flag)))
+            if (lane == 0) mbar_arrive(smem_u32(wempty + ws));
+            const int s = st % kStages;
+            if (st >= kStages &&
+                !__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(sempty + s), ((st / kStages) - 1) & 1, abort_flag)))
                 break;
-            uint8_t* at = smem + kOffA + s * kATileBytes;
             #pragma unroll
-            for (int q = 0; q < kWordsPerConv; ++q) {
-                const int idx = ct + kConvWarps * 32 * q;
-                const int r = idx >> 3, c = idx & 7;
-                *reinterpret_cast<uint4*>(at + r * 128 + ((c ^ (r & 7)) << 4)) = int4x8_to_bf16(w[q]);
+            for (int j = 0; j < kStageK; ++j) {  // word w of K block j = codes 8w .. 8w+7 -> columns 4w .. 4w+3
+                const uint32_t w8[8] = {c16[2 * j].x, c16[2 * j].y, c16[2 * j].z, c16[2 * j].w,
+                                        c16[2 * j + 1].x, c16[2 * j + 1].y, c16[2 * j + 1].z, c16[2 * j + 1].w};
+                uint32_t v[32];
+                #pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const uint4 o = int4x8_to_bf16(w8[w]);
+                    v[4 * w] = o.x;
+                    v[4 * w + 1] = o.y;
+                    v[4 * w + 2] = o.z;
+                    v[4 * w + 3] = o.w;
+                }
+                tmem_st32(tmem + ((uint32_t)(32 * q) << 16) + kTmemA + kTmemAStage * s + 32 * j, v);
             }
-            fence_proxy_async_smem();
+            tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(afull + s));
         }
@@ -367,14 +386,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
         griddep_wait();  // scales and outputs
         const bool ok = __all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(accfull), 0, abort_flag));
         tc_fence_after_sync();
-        const int quarter = warp & 3;  // the TMEM lanes this warp may read
-        const int group = (warp - kFirstConvWarp) >> 2;  // warps with the same quarter split the columns
-        const int r = quarter * 32 + lane;
+        // the TMEM lanes this warp may read are its converter lanes (q, r);
+        // the two warps of a quarter split the columns
+        const int ct = tid - kFirstConvWarp * 32;
         const int n = n0 + r;
         const float swv = (ok && n < a.N) ? a.sw[n] : 0.f;
-        for (int ch = group; ch < BN / 8; ch += kConvWarps / 4) {
+        for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
             uint32_t v[8];
-            tmem_ld8(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(8 * ch), v);
+            tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(8 * ch), v);
             if (!ok || n >= a.N) continue;
             #pragma unroll
             for (int t = 0; t < 8; ++t) {
@@ -546,7 +565,7 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
         MmaArgs a;
         memset(&a, 0, sizeof(a));
         if (!encode_2d(&a.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq[g], (uint64_t)(K / 2), (uint64_t)Ns[g],
-                       (uint64_t)(K / 2), kWBlocks * kKBlock / 2, kTileRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+                       (uint64_t)(K / 2), kWBlocks * kKBlock / 2, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         a.codes = codes;
         a.sw = sw[g];
