@@ -40,6 +40,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "actq.cuh"
 #include "kernels.h"
 #include "plan.h"
 #include "ptx.cuh"
@@ -86,7 +87,7 @@ struct MmaArgs {
     const float* sa;        // [M]
     float* Y;               // [M][N]
     int32_t* acc_out;       // optional [M][N]
-    int32_t* part;          // [grid][M][128] when P > 1 (one block per CTA)
+    int32_t* part;          // [tiles][M][128] int32 accumulators when P > 1 (zeroed by the pre-pass)
     unsigned* tickets;      // [tiles] when P > 1, zero between calls
     int M, N, K, BN, P, nkb, kbp;
 };
@@ -113,37 +114,36 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
     if (!mbar_wait(bar, parity)) atomicOr(&g_mma_error, kErrDrainWait);
 }
 
-__device__ __forceinline__ int act_code(float v, float s) {
-    if (s == 0.f) return 0;
-    const float r = fminf(fmaxf(roundf(__fdiv_rn(v, s)), -127.f), 127.f);
-    return static_cast<int>(r);
-}
-
 // Activation codes for the tensor cores, in the order the MMA reads them:
 // K-block kb (64 codes of every row) is one contiguous [BN][64] bf16 tile of
 // BN * 128 bytes, already in the 128-byte swizzled layout (16-byte chunk c
 // of row m at m * 128 + ((c ^ (m % 8)) * 16)), so one 1-D bulk copy moves
-// a whole tile.  Rows M..BN-1 and codes past K are zero.  One CTA per row
-// (BN CTAs): X [M][K] binary16 quantized here (max|x|, s_a = max/127 by
-// IEEE division, round half away, clamp), or, when X is null, the given
-// int8 codes Xq and scales sa_in; optional int8 codes and scale outputs.
+// a whole tile.  Rows M..BN-1 and codes past K are zero.  Grid (BN rows,
+// pieces of 256 vectors of 8 codes): every CTA of a row takes the row's
+// max|x| (exact in binary16), s_a = max/127 by IEEE division, and quantizes
+// its piece with the fast exact quantizer (actq.cuh); when X is null it
+// widens the given int8 codes Xq instead.  Optional int8 codes and scale
+// outputs for the caller.  It also zeroes the int32 split-K accumulators.
 __global__ void __launch_bounds__(kAQThreads) act_codes_kernel(
     const __half* __restrict__ X, const int8_t* __restrict__ Xq, const float* __restrict__ sa_in,
     int M, int64_t K, int BN, uint8_t* __restrict__ B, float* __restrict__ sa_ws,
-    int8_t* __restrict__ Xq_out, float* __restrict__ sa_out) {
+    int8_t* __restrict__ Xq_out, float* __restrict__ sa_out, int32_t* __restrict__ acc,
+    int64_t acc_words) {
     __shared__ float red[kAQThreads / 32];
     griddep_launch_dependents();
     griddep_wait();
+    // clear the split-K accumulators of the launches that follow
+    for (int64_t e = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * kAQThreads + threadIdx.x; e < acc_words;
+         e += (int64_t)gridDim.x * gridDim.y * kAQThreads)
+        acc[e] = 0;
     const int m = blockIdx.x;
-    const int64_t nchunks = (K + kKBlock - 1) / kKBlock * 8;  // 16-byte chunks incl. padding
+    const int64_t u = (int64_t)blockIdx.y * kAQThreads + threadIdx.x;  // vector of 8 codes
+    const int64_t nchunks = (K + kKBlock - 1) / kKBlock * 8;           // incl. the padding to a K block
     const int64_t kchunks = K / 8;
-    const size_t tile_bytes = (size_t)BN * 128;
-    auto dst = [&](int64_t u) {
-        return reinterpret_cast<uint4*>(B + (u >> 3) * tile_bytes + (size_t)m * 128 +
-                                        ((((int)u & 7) ^ (m & 7)) << 4));
-    };
+    uint4* dst = reinterpret_cast<uint4*>(B + (u >> 3) * ((size_t)BN * 128) + (size_t)m * 128 +
+                                          ((((int)u & 7) ^ (m & 7)) << 4));
     if (m >= M) {
-        for (int64_t u = threadIdx.x; u < nchunks; u += kAQThreads) *dst(u) = make_uint4(0u, 0u, 0u, 0u);
+        if (u < nchunks) *dst = make_uint4(0u, 0u, 0u, 0u);
         return;
     }
     float s;
@@ -151,13 +151,15 @@ __global__ void __launch_bounds__(kAQThreads) act_codes_kernel(
     if (X == nullptr) {
         s = sa_in[m];
     } else {
-        float mx = 0.f;
-        for (int64_t u = threadIdx.x; u < kchunks; u += kAQThreads) {
-            const uint4 h = xv[u];
-            const __half* hp = reinterpret_cast<const __half*>(&h);
+        __half2 hm = __float2half2_rn(0.f);
+        #pragma unroll 4
+        for (int64_t v = threadIdx.x; v < kchunks; v += kAQThreads) {
+            const uint4 h = xv[v];
+            const __half2* p2 = reinterpret_cast<const __half2*>(&h);
             #pragma unroll
-            for (int t = 0; t < 8; ++t) mx = fmaxf(mx, fabsf(__half2float(hp[t])));
+            for (int t = 0; t < 4; ++t) hm = __hmax2(hm, __habs2(p2[t]));
         }
+        float mx = fmaxf(__low2float(hm), __high2float(hm));
         #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
         if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
@@ -167,36 +169,34 @@ __global__ void __launch_bounds__(kAQThreads) act_codes_kernel(
         for (int w = 0; w < kAQThreads / 32; ++w) mx = fmaxf(mx, red[w]);
         s = __fdiv_rn(mx, 127.f);
     }
-    for (int64_t u = threadIdx.x; u < nchunks; u += kAQThreads) {
+    if (u < nchunks) {
         uint32_t o[4] = {0u, 0u, 0u, 0u};
         if (u < kchunks) {
-            int q[8];
+            uint32_t c8[2];
             if (X != nullptr) {
-                const uint4 h = xv[u];
-                const __half* hp = reinterpret_cast<const __half*>(&h);
-                uint32_t c8[2] = {0u, 0u};
-                #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    q[t] = act_code(__half2float(hp[t]), s);
-                    c8[t >> 2] |= ((uint32_t)q[t] & 0xFFu) << (8 * (t & 3));
-                }
+                float r_lo, r_hi;
+                quant_bracket(s, &r_lo, &r_hi);
+                const uint2 q = quant8_split(xv[u], s, r_lo, r_hi);  // even / odd codes
+                c8[0] = __byte_perm(q.x, q.y, 0x5140);               // natural order
+                c8[1] = __byte_perm(q.x, q.y, 0x7362);
                 if (Xq_out != nullptr)
                     *reinterpret_cast<uint2*>(Xq_out + (int64_t)m * K + 8 * u) = make_uint2(c8[0], c8[1]);
             } else {
-                const uint2 c8 = *reinterpret_cast<const uint2*>(Xq + (int64_t)m * K + 8 * u);
-                #pragma unroll
-                for (int t = 0; t < 8; ++t)
-                    q[t] = (int)(int8_t)(((t < 4 ? c8.x : c8.y) >> (8 * (t & 3))) & 0xFFu);
+                const uint2 c = *reinterpret_cast<const uint2*>(Xq + (int64_t)m * K + 8 * u);
+                c8[0] = c.x;
+                c8[1] = c.y;
             }
             #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                const __nv_bfloat162 v = __floats2bfloat162_rn((float)q[2 * t], (float)q[2 * t + 1]);
+                const uint32_t w = c8[t >> 1] >> (16 * (t & 1));
+                const __nv_bfloat162 v = __floats2bfloat162_rn((float)(int8_t)(w & 0xFFu),
+                                                               (float)(int8_t)((w >> 8) & 0xFFu));
                 o[t] = *reinterpret_cast<const uint32_t*>(&v);
             }
         }
-        *dst(u) = make_uint4(o[0], o[1], o[2], o[3]);
+        *dst = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    if (threadIdx.x == 0) {
+    if (blockIdx.y == 0 && threadIdx.x == 0) {
         sa_ws[m] = s;
         if (sa_out != nullptr) sa_out[m] = s;
     }
@@ -405,12 +405,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
                     a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), swv), a.sa[m]);
                     if (a.acc_out != nullptr) a.acc_out[o] = acc;
                 } else {
-                    a.part[((int64_t)blockIdx.x * a.M + m) * kTileRows + r] = acc;
+                    atomicAdd(a.part + ((int64_t)tile * a.M + m) * kTileRows + r, acc);  // exact, order-free
                 }
             }
         }
         if (a.P > 1) {
-            // the last CTA of this tile sums the pieces in a fixed order
+            // the pieces' int32 sums were added atomically (integer addition
+            // is exact and order-free); the last CTA of the tile rescales them
             __threadfence();
             named_bar_sync(1, kConvWarps * 32);
             if (ct == 0) *last_flag = (atomicAdd(a.tickets + tile, 1u) == (unsigned)(a.P - 1));
@@ -418,14 +419,26 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
             if (*last_flag) {
                 __threadfence();
                 const int rows = min(kTileRows, a.N - n0);
-                for (int e = ct; e < a.M * rows; e += kConvWarps * 32) {
-                    const int m = e / rows, rr = e % rows, nn = n0 + rr;
-                    const int64_t o = (int64_t)m * a.N + nn;
-                    int32_t acc = 0;
-                    for (int q = 0; q < a.P; ++q)
-                        acc += __ldcg(a.part + ((int64_t)(tile * a.P + q) * a.M + m) * kTileRows + rr);
-                    a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), a.sw[nn]), a.sa[m]);
-                    if (a.acc_out != nullptr) a.acc_out[o] = acc;
+                int32_t* acc_t = a.part + (int64_t)tile * a.M * kTileRows;
+                constexpr int kBatch = 8;  // loads in flight per thread
+                for (int e0 = ct; e0 < a.M * kTileRows; e0 += kConvWarps * 32 * kBatch) {
+                    int32_t v[kBatch];
+                    #pragma unroll
+                    for (int b = 0; b < kBatch; ++b) {
+                        const int e = e0 + b * kConvWarps * 32;
+                        v[b] = e < a.M * kTileRows ? __ldcg(acc_t + e) : 0;
+                    }
+                    #pragma unroll
+                    for (int b = 0; b < kBatch; ++b) {
+                        const int e = e0 + b * kConvWarps * 32;
+                        if (e >= a.M * kTileRows) break;
+                        __stcg(acc_t + e, 0);  // clear for the next matrix of a grouped call
+                        const int m = e / kTileRows, rr = e % kTileRows, nn = n0 + rr;
+                        if (rr >= rows) continue;
+                        const int64_t o = (int64_t)m * a.N + nn;
+                        a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(v[b]), a.sw[nn]), a.sa[m]);
+                        if (a.acc_out != nullptr) a.acc_out[o] = v[b];
+                    }
                 }
                 if (ct == 0) a.tickets[tile] = 0u;  // ready for the next call
             }
@@ -518,17 +531,17 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out) {
     pl.sms = num_sms;
     pl.stages = kWStages;
     pl.stage_bytes = kWTileBytes;
-    // workspace: tickets, scales (64 floats), bf16 code tiles [nkb][BN][64], then an
-    // int32 [M][128] block per CTA for split-K partials.  The partial region
-    // is sized for any N' <= N on this device (grouped launches run one
-    // plan per weight matrix): a split plan has at most max(SMs, tiles *
-    // pieces forced by the 16384-wide exactness limit) CTAs.
+    // workspace: tickets, scales (64 floats), bf16 code tiles [nkb][BN][64], then
+    // int32 [M][128] accumulators per tile for split plans.  The region is
+    // sized for any N' <= N on this device (grouped launches run one plan
+    // per weight matrix): K is split when the exactness limit forces it
+    // (every tile) or when a matrix has fewer tiles than 4/5 of the SMs.
     pl.off_sa = kTicketBytes;
     pl.off_codes = pl.off_sa + 256;
     pl.off_part = round_up_sz(pl.off_codes + (size_t)pl.nkb * pl.BN * kKBlock * 2, 256);
-    const int64_t gmax = pmin > 1 ? ((int64_t)pl.tiles * pmin > num_sms ? (int64_t)pl.tiles * pmin : num_sms)
-                                  : num_sms;
-    pl.ws_bytes = pl.off_part + round_up_sz((size_t)gmax * M * kTileRows * 4, 256);
+    const int64_t small = num_sms * 4 / 5;
+    const int64_t tmax = pmin > 1 ? pl.tiles : (pl.tiles < small ? pl.tiles : small);
+    pl.ws_bytes = pl.off_part + round_up_sz((size_t)tmax * M * kTileRows * 4, 256);
     *out = pl;
     return true;
 }
@@ -545,8 +558,11 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
         const __half* xh = reinterpret_cast<const __half*>(X);
         int Mi = M, BNi = pl.BN;
         int64_t Kk = K;
-        void* args[] = {&xh, &Xq, &sa, &Mi, &Kk, &BNi, &codes, &sa_ws, &Xq_out, &sa_out};
-        cudaError_t e = launch_pdl(reinterpret_cast<const void*>(act_codes_kernel), dim3(pl.BN),
+        int32_t* acc = reinterpret_cast<int32_t*>(wsb + pl.off_part);
+        int64_t acc_words = (int64_t)((pl.ws_bytes - pl.off_part) / 4);
+        void* args[] = {&xh, &Xq, &sa, &Mi, &Kk, &BNi, &codes, &sa_ws, &Xq_out, &sa_out, &acc, &acc_words};
+        const unsigned pieces = (unsigned)(((int64_t)pl.nkb * 8 + kAQThreads - 1) / kAQThreads);
+        cudaError_t e = launch_pdl(reinterpret_cast<const void*>(act_codes_kernel), dim3(pl.BN, pieces),
                                    dim3(kAQThreads), 0, stream, flags, args);
         if (e != cudaSuccess) return e;
     }

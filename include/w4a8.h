@@ -121,10 +121,11 @@ int act_quantize_i8(const uint16_t* X, int64_t M, int64_t K, int8_t* Xq, float* 
 
 /* Workspace bytes w4a8_gemv / w4a8_linear need for this shape on the
  * current device (0 when the chosen plan does not split K).  Layout: 4096
- * bytes of arrival counters, then the int32/fp32 split partials.  The
- * counters must be zero before the first call (zero-fill the buffer once);
- * every call leaves them zero, so one workspace can serve calls of any
- * shape, in either precision.  Calls that share a workspace must not run
+ * bytes of arrival counters, then scratch (split partials; for the
+ * tensor-core path the activation codes and int32 accumulators, which its
+ * first kernel clears).  The counters must be zero before the first call
+ * (zero-fill the buffer once); every call leaves them zero, so one
+ * workspace can serve calls of any shape, in either precision.  Calls that share a workspace must not run
  * concurrently (same stream, or ordered by events).  Returns 0 for shapes
  * the linear entry points reject. */
 size_t w4a8_workspace_bytes(int64_t M, int64_t K, int64_t N);
