@@ -45,8 +45,9 @@ std::atomic<int> g_force_cl{0};
 std::atomic<int> g_ring_bytes{0};
 std::atomic<int> g_ctas_per_sm{0};
 std::atomic<int> g_mma_min_m{0};
-// Batch rows from which the W4A8 entry points take the tensor-core kernel.
-constexpr int kDefaultMmaMinM = 16;
+// Batch rows from which the W4A8 entry points take the tensor-core kernel
+// (measured on GB300: dp4a is faster at 1-2 rows, the tensor cores from 3).
+constexpr int kDefaultMmaMinM = 3;
 
 int sm_count(int* out) {
     static std::atomic<int> cache[64];

@@ -72,7 +72,7 @@ typedef enum {
 #define W4A8_LAUNCH_PDL 1u
 
 /* Maximum activation rows (decode batch) per call.  W4A8 calls with at
- * least 16 rows (see w4a8_tuning_t.mma_min_m) run on the tensor cores: an
+ * least 3 rows (see w4a8_tuning_t.mma_min_m) run on the tensor cores: an
  * activation-quantization launch writes bf16 codes into the workspace, then
  * tcgen05 MMAs of 128 weight rows x the batch accumulate the integer
  * products exactly in fp32 (every partial sum of one K piece of at most

@@ -144,7 +144,7 @@ def test_plan_invariants(sms, w8):
 
 
 def check_mma_plan(p, M, K, N, sms):
-    assert M >= 16
+    assert M >= 3
     tiles = -(-N // 128)
     nkb = -(-K // 64)
     P = p["splits"]
@@ -158,8 +158,8 @@ def check_mma_plan(p, M, K, N, sms):
 
 def test_tensor_core_threshold():
     try:
-        assert w4.w4a8_plan_info(15, 3584, 18944, num_sms=152)["tensor_cores"] == 0
-        assert w4.w4a8_plan_info(16, 3584, 18944, num_sms=152)["tensor_cores"] == 1
+        assert w4.w4a8_plan_info(2, 3584, 18944, num_sms=152)["tensor_cores"] == 0
+        assert w4.w4a8_plan_info(3, 3584, 18944, num_sms=152)["tensor_cores"] == 1
         w4.w4a8_set_tuning(mma_min_m=65)
         assert w4.w4a8_plan_info(64, 3584, 18944, num_sms=152)["tensor_cores"] == 0
         w4.w4a8_set_tuning(mma_min_m=2)

@@ -164,20 +164,26 @@ W4A8_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("path", ["default", "dp4a"])
 @pytest.mark.parametrize("M,K,N,seed", W4A8_SHAPES)
-def test_w4a8_linear_fused(w4, orc, M, K, N, seed):
+def test_w4a8_linear_fused(w4, orc, M, K, N, seed, path):
+    if path == "dp4a":
+        w4.w4a8_set_tuning(mma_min_m=65)  # batches of 3+ rows would take the tensor cores
     check_w4a8(w4, orc, M, K, N, seed, fused=True, zero_rows=(1,))
 
 
+@pytest.mark.parametrize("path", ["default", "dp4a"])
 @pytest.mark.parametrize("M,K,N,seed", W4A8_SHAPES[:8] + W4A8_SHAPES[-3:-1])
-def test_w4a8_gemv_unfused(w4, orc, M, K, N, seed):
+def test_w4a8_gemv_unfused(w4, orc, M, K, N, seed, path):
+    if path == "dp4a":
+        w4.w4a8_set_tuning(mma_min_m=65)
     check_w4a8(w4, orc, M, K, N, seed, fused=False)
 
 
 @pytest.mark.parametrize("splits", [2, 3, 5, 16])
 @pytest.mark.parametrize("fused", [True, False])
 def test_w4a8_split_k(w4, orc, splits, fused):
-    w4.w4a8_set_tuning(force_splits=splits)
+    w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65)  # the dp4a kernel's split plans
     for (M, K, N, seed) in [(1, 3584, 700, 30), (3, 18944, 150, 31), (8, 1024, 64, 32)]:
         if (K // 32) < splits:
             continue
@@ -424,7 +430,7 @@ def test_gpu_generator_matches_host(w4):
     (20, 256, (9, 30, 3), 2),
 ])
 def test_w4a8_linear_grouped(w4, orc, M, K, Ns, splits):
-    w4.w4a8_set_tuning(force_splits=splits)
+    w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65 if splits else 0)
     X = synth.activation(500 + K, M, K, outlier_frac=0.001)
     refs, Wqs, sws = [], [], []
     for g, N in enumerate(Ns):
