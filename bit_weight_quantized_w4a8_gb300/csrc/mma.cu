@@ -56,8 +56,8 @@ constexpr int kTileRows = 128;                  // weight rows per CTA (MMA M)
 constexpr int kKBlock = 64;                     // K block: 128 bytes of bf16 per row
 constexpr int kStageK = 2;                      // K blocks per pipeline stage (8 MMAs, one commit)
 constexpr int kWBlocks = 4;                     // K blocks per weight load: 128 bytes of a row
-constexpr int kWStages = 4;                     // packed INT4 ring (16 KB a load)
-constexpr int kStages = 4;                      // stage ring: A in TMEM, B in shared memory
+constexpr int kWStages = 3;                     // packed INT4 ring (16 KB a load)
+constexpr int kStages = 3;                      // stage ring: A in TMEM, B in shared memory
 constexpr int kConvGroups = 2;                  // converter warp groups, alternating stages
 constexpr int kConvWarps = 4 * kConvGroups;     // one warp per TMEM lane quarter per group
 constexpr int kFirstConvWarp = 3;
@@ -65,7 +65,7 @@ constexpr int kMmaThreads = (kFirstConvWarp + kConvWarps) * 32;
 constexpr int kWTileBytes = kTileRows * kKBlock / 2 * kWBlocks;  // 16384
 constexpr int kBTileMax = 64 * kKBlock * 2;     // one K block of 64 batch rows: 8192
 constexpr int kBStageMax = kStageK * kBTileMax;
-constexpr uint32_t kTmemCols = 512;             // D: columns 0..63; A stage s: 64 + 64 s
+constexpr uint32_t kTmemCols = 256;             // D: columns 0..63; A stage s: 64 + 64 s
 constexpr uint32_t kTmemA = 64;
 constexpr uint32_t kTmemAStage = 32 * kStageK;  // two bf16 per column
 constexpr int kOffB = 0;
@@ -76,7 +76,7 @@ constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kMmaSmem = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
 constexpr int kAQThreads = 256;
 
-static_assert(kWBlocks % kStageK == 0 && kStages % kConvGroups == 0, "stage geometry");
+static_assert(kWBlocks % kStageK == 0, "stage geometry");
 static_assert(kOffB % 1024 == 0 && kOffW % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kTmemA + kTmemAStage * kStages <= kTmemCols, "TMEM budget");
 
@@ -221,7 +221,10 @@ __device__ __forceinline__ uint4 int4x8_to_bf16(uint32_t w) {
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_constant__ MmaArgs a) {
+// Two CTAs per SM (shared memory < 113 KB, 256 TMEM columns, <= 93
+// registers): the SM's tensor core then interleaves two MMA streams, each at
+// the issue rate of one.
+__global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_constant__ MmaArgs a) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles
     const uint32_t raw = smem_u32(smem_raw);
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
     int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
-    const uint32_t ncols = kTmemCols;  // of the SM's 512; one CTA per SM
+    const uint32_t ncols = kTmemCols;  // half of the SM's 512: two CTAs per SM
 
     if (tid == 0) {
         for (int s = 0; s < kWStages; ++s) {
@@ -513,7 +516,8 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out) {
     // split K when the tiles alone leave SMs idle; pieces of at most 256
     // K-blocks (16384) keep every fp32 partial sum exact
     int P = 1;
-    if (pl.tiles < num_sms * 4 / 5) P = num_sms / pl.tiles;
+    const int slots = 2 * num_sms;  // resident CTAs
+    if (pl.tiles < slots * 4 / 5) P = slots / pl.tiles;
     if (P < 1) P = 1;
     const int pmin = (pl.nkb + 255) / 256;
     if (P < pmin) P = pmin;
@@ -535,11 +539,11 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out) {
     // int32 [M][128] accumulators per tile for split plans.  The region is
     // sized for any N' <= N on this device (grouped launches run one plan
     // per weight matrix): K is split when the exactness limit forces it
-    // (every tile) or when a matrix has fewer tiles than 4/5 of the SMs.
+    // (every tile) or when a matrix has fewer tiles than 4/5 of the CTA slots.
     pl.off_sa = kTicketBytes;
     pl.off_codes = pl.off_sa + 256;
     pl.off_part = round_up_sz(pl.off_codes + (size_t)pl.nkb * pl.BN * kKBlock * 2, 256);
-    const int64_t small = num_sms * 4 / 5;
+    const int64_t small = 2 * num_sms * 4 / 5;
     const int64_t tmax = pmin > 1 ? pl.tiles : (pl.tiles < small ? pl.tiles : small);
     pl.ws_bytes = pl.off_part + round_up_sz((size_t)tmax * M * kTileRows * 4, 256);
     *out = pl;
