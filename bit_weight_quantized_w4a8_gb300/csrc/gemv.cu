@@ -4,8 +4,9 @@
 // are widened to int8 lanes in registers and multiplied against INT8
 // activation codes with __dp4a into int32; y = ((float)acc * s_w) * s_a.
 // W8A16 (the TPU-MLIR W8A16 page, section 4): INT8 codes are widened to
-// fp32 exactly in registers and multiplied with the F16 activation; the
-// per-channel scale multiplies the fp32 sum once.
+// binary16 exactly in registers and multiplied with the F16 activation by
+// f16 x f16 -> f32 FMAs (exact products, fp32 sums); the per-channel scale
+// multiplies the fp32 sum once.
 //
 // Both are HBM-bound at decode batch sizes, so the kernel is built around
 // the weight stream (the W8A16 page's load/compute overlap, done with the
@@ -111,6 +112,18 @@ __device__ __forceinline__ void permute_act(uint4 lo, uint4 hi, uint32_t* act) {
     }
 }
 
+// c0 += lo(q) * lo(x), c1 += hi(q) * hi(x): binary16 products, exact in
+// fp32, accumulated in fp32 (one instruction each, at the FFMA rate).
+__device__ __forceinline__ void fma_f16_f32x2(float& c0, float& c1, uint32_t q, uint32_t x) {
+    asm("{\n\t.reg .f16 ql, qh, xl, xh;\n\t"
+        "mov.b32 {ql, qh}, %2;\n\t"
+        "mov.b32 {xl, xh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, ql, xl, %0;\n\t"
+        "fma.rn.f32.f16 %1, qh, xh, %1;\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "r"(q), "r"(x));
+}
+
 __device__ __forceinline__ int segment_of(const GemvArgs& a, int64_t n) {
     int g = 0;
     #pragma unroll
@@ -154,7 +167,7 @@ __device__ __forceinline__ void issue_stage(const GemvArgs& a, uint8_t* smem, in
 template <bool kW4, int MT, int SMAX, bool kFused, bool kExactS>
 __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
     using AccT = typename std::conditional<kW4, int, float>::type;
-    constexpr int kActWords = kW4 ? 8 : 16;  // registers per granule per activation row
+    constexpr int kActWords = 8;  // registers per granule per activation row (W8: binary16 pairs)
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const GemvPlan& pl = a.pl;
@@ -351,20 +364,12 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                         const int8_t* src = a.Xq + (int64_t)m * K + (int64_t)(g0 + c) * 32;
                         permute_act(ld_global_nc_v4(src), ld_global_nc_v4(src + 16), act[m][s]);
                     } else {
+                        // the 16 binary16 values of the granule, kept as pairs
                         const __half* src = a.X + (int64_t)m * K + (int64_t)(g0 + c) * 16;
                         const uint4 h0 = ld_global_nc_v4(src);
                         const uint4 h1 = ld_global_nc_v4(src + 8);
-                        const __half2* hp0 = reinterpret_cast<const __half2*>(&h0);
-                        const __half2* hp1 = reinterpret_cast<const __half2*>(&h1);
-                        #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const float2 f0 = __half22float2(hp0[t]);
-                            const float2 f1 = __half22float2(hp1[t]);
-                            act[m][s][2 * t] = __float_as_uint(f0.x);
-                            act[m][s][2 * t + 1] = __float_as_uint(f0.y);
-                            act[m][s][8 + 2 * t] = __float_as_uint(f1.x);
-                            act[m][s][8 + 2 * t + 1] = __float_as_uint(f1.y);
-                        }
+                        act[m][s][0] = h0.x; act[m][s][1] = h0.y; act[m][s][2] = h0.z; act[m][s][3] = h0.w;
+                        act[m][s][4] = h1.x; act[m][s][5] = h1.y; act[m][s][6] = h1.z; act[m][s][7] = h1.w;
                     }
                 } else {
                     #pragma unroll
@@ -467,21 +472,23 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                                     ch = __dp4a((int)hi, (int)act[m][s][4 + t], ch);
                                 }
                             } else {
-                                // int8 code q -> fp32 exactly: the bits 0x4B0000uu
-                                // with uu = q + 128 encode 2^23 + q + 128.
+                                // int8 code q -> binary16 exactly: the byte uu = q + 128
+                                // under the high byte 0x64 encodes 1024 + q + 128; one
+                                // packed subtraction of 1152 leaves q (|q| <= 128)
                                 const uint32_t u = wv[t] ^ 0x80808080u;
-                                const float q0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)) - 8388736.f;
-                                const float q1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)) - 8388736.f;
-                                const float q2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)) - 8388736.f;
-                                const float q3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - 8388736.f;
+                                const uint32_t p01 = __byte_perm(u, 0x64646464u, 0x4140);
+                                const uint32_t p23 = __byte_perm(u, 0x64646464u, 0x4342);
+                                const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));
+                                const __half2 h01 = __hsub2(*reinterpret_cast<const __half2*>(&p01), bias);
+                                const __half2 h23 = __hsub2(*reinterpret_cast<const __half2*>(&p23), bias);
+                                const uint32_t q01 = *reinterpret_cast<const uint32_t*>(&h01);
+                                const uint32_t q23 = *reinterpret_cast<const uint32_t*>(&h23);
                                 #pragma unroll
                                 for (int m = 0; m < MT; ++m) {
                                     AccT& c0 = alo[m][t % NCH];
                                     AccT& c1 = ahi[m][t % NCH];
-                                    c0 = fmaf(q0, __uint_as_float(act[m][s][4 * t + 0]), c0);
-                                    c1 = fmaf(q1, __uint_as_float(act[m][s][4 * t + 1]), c1);
-                                    c0 = fmaf(q2, __uint_as_float(act[m][s][4 * t + 2]), c0);
-                                    c1 = fmaf(q3, __uint_as_float(act[m][s][4 * t + 3]), c1);
+                                    fma_f16_f32x2(c0, c1, q01, act[m][s][2 * t]);      // codes 4t, 4t+1
+                                    fma_f16_f32x2(c0, c1, q23, act[m][s][2 * t + 1]);  // codes 4t+2, 4t+3
                                 }
                             }
                         }
