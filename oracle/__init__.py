@@ -71,12 +71,17 @@ class Oracle:
             "oracle_w4a8_dot": [_p, _i64, _i64, _p, _i64, _p],
             "oracle_w4a8_linear": [_p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _p],
             "oracle_w8_quantize": [_p, _i64, _i64, _p, _p],
+            "oracle_w4g_quantize": [_p, _i64, _i64, _i64, _p, _p],
+            "oracle_w4a8g_ref": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p],
+            "oracle_w4a8g_linear": [_p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _p, _p],
         }.items():
             f = getattr(lib, name)
             f.restype = ctypes.c_int
             f.argtypes = args
         lib.oracle_w4a8_rescale.restype = None
         lib.oracle_w4a8_rescale.argtypes = [_p, _p, _p, _i64, _i64, _p]
+        lib.oracle_w4g_scale_stride.restype = _i64
+        lib.oracle_w4g_scale_stride.argtypes = [_i64, _i64]
         lib.oracle_w8a16_ref.restype = None
         lib.oracle_w8a16_ref.argtypes = [_p, _i64, _i64, _p, _p, _i64, _p]
 
@@ -155,6 +160,56 @@ class Oracle:
         if st != OK:
             raise OverflowError("oracle_w4a8_linear status %d" % st)
         return Y, Xq, sa, acc
+
+    # -- group-wise W4A8 --------------------------------------------------
+    def w4g_scale_stride(self, K: int, gs: int) -> int:
+        return int(self._lib.oracle_w4g_scale_stride(K, gs))
+
+    def w4g_quantize(self, W: np.ndarray, gs: int):
+        """Returns (Wq [N][K/2] uint8, sg [N][stride] float32)."""
+        W = np.ascontiguousarray(W, dtype=np.float32)
+        N, K = W.shape
+        Wq = np.empty((N, K // 2), np.uint8)
+        sg = np.empty((N, max(1, self.w4g_scale_stride(K, gs))), np.float32)
+        st = self._lib.oracle_w4g_quantize(_ptr(W), N, K, gs, _ptr(Wq), _ptr(sg))
+        if st != OK:
+            raise ValueError("oracle_w4g_quantize status %d" % st)
+        return Wq, sg
+
+    def w4a8g_ref(self, Xq: np.ndarray, sa: np.ndarray, Wq: np.ndarray, sg: np.ndarray, gs: int):
+        """Returns (Y, B) in float64: the product and its rounding magnitude."""
+        Xq = np.ascontiguousarray(Xq, dtype=np.int8)
+        sa = np.ascontiguousarray(sa, dtype=np.float32)
+        Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+        sg = np.ascontiguousarray(sg, dtype=np.float32)
+        M, K = Xq.shape
+        N = Wq.shape[0]
+        assert Wq.shape[1] * 2 == K and sg.shape == (N, self.w4g_scale_stride(K, gs))
+        Y = np.empty((M, N), np.float64)
+        B = np.empty((M, N), np.float64)
+        st = self._lib.oracle_w4a8g_ref(_ptr(Xq), _ptr(sa), M, K, gs, _ptr(Wq), _ptr(sg), N,
+                                        _ptr(Y), _ptr(B))
+        if st != OK:
+            raise ValueError("oracle_w4a8g_ref status %d" % st)
+        return Y, B
+
+    def w4a8g_linear(self, X: np.ndarray, Wq: np.ndarray, sg: np.ndarray, gs: int):
+        """Returns (Y, B, Xq, sa)."""
+        X = np.ascontiguousarray(X, dtype=np.float16)
+        Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+        sg = np.ascontiguousarray(sg, dtype=np.float32)
+        M, K = X.shape
+        N = Wq.shape[0]
+        assert Wq.shape[1] * 2 == K and sg.shape == (N, self.w4g_scale_stride(K, gs))
+        Y = np.empty((M, N), np.float64)
+        B = np.empty((M, N), np.float64)
+        Xq = np.empty((M, K), np.int8)
+        sa = np.empty(M, np.float32)
+        st = self._lib.oracle_w4a8g_linear(_ptr(X), M, K, gs, _ptr(Wq), _ptr(sg), N, _ptr(Y),
+                                           _ptr(B), _ptr(Xq), _ptr(sa))
+        if st != OK:
+            raise ValueError("oracle_w4a8g_linear status %d" % st)
+        return Y, B, Xq, sa
 
     # -- W8A16 ------------------------------------------------------------
     def w8_quantize(self, W: np.ndarray):

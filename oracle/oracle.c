@@ -12,14 +12,17 @@
  *       sections 当前实现方式 (row-wise INT4 weight with one scale per row;
  *       activation dynamically quantized to INT8 before every linear;
  *       output = int32 accumulate * weight_scale * activation_scale) and
- *       正确方向 (INT4 weight, INT8 activation, int32 accumulate, float out).
+ *       正确方向 (INT4 weight, INT8 activation, int32 accumulate, float out),
+ *       and 后续优化方向 (group-wise scales, listed as the next step: read
+ *       as the row-wise definition applied to each group of gs codes).
  *  [P2] "TPU-MLIR W8A16 for ChatGLM2-6B", section 2 (per-channel INT8
  *       weights) and section 4 (the five steps: load, cast INT8 to F16,
  *       multiply by the scale, matrix multiply with the activation, store).
  * Where the pages leave a step open, the reading used is stated at the
  * function (symmetric codes, divisors 7 and 127, round half away from zero,
  * true division, low-nibble-first two's-complement packing, fp32 rescale in
- * the order (acc * s_w) * s_a).
+ * the order (acc * s_w) * s_a; for group scales a binary64 reference plus
+ * the magnitude that bounds any fp32 evaluation of it).
  *
  * Build: gcc -std=c11 -O2 -ffp-contract=off -fPIC -shared (no fast-math, no
  * FMA contraction, so every float operation is one IEEE binary32 operation).
@@ -278,4 +281,103 @@ void oracle_w8a16_ref(const uint16_t* X, int64_t M, int64_t K, const int8_t* Wq8
             Y[m * N + n] = y;
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* g1: group-wise INT4 weight quantizer  [P1 后续优化方向: group-wise scale,  */
+/*     the row-wise definition of 当前实现方式 applied to each group of a row] */
+/* ------------------------------------------------------------------------ */
+
+/* Floats per row of the group-scale matrix: K / gs rounded up to a multiple
+   of 4, so that every scale row starts on a 16-byte boundary.  The pages fix
+   no storage layout; this is the library's documented one. */
+int64_t oracle_w4g_scale_stride(int64_t K, int64_t gs)
+{
+    if (gs <= 0 || K < 0) return 0;
+    int64_t groups = K / gs;
+    return (groups + 3) / 4 * 4;
+}
+
+/* W[N][K] fp32 -> Wq[N][K/2] packed nibbles (same packing as the row-wise
+   quantizer) + sg[N][stride] fp32.  Group g of row n covers the codes
+   k = g*gs .. g*gs+gs-1; its scale is s = max|W over the group| / 7 and its
+   codes q = clamp(round(W / s), -7, 7).  Padding entries of sg are 0.
+   With gs == K this is the row-wise quantizer. */
+int oracle_w4g_quantize(const float* W, int64_t N, int64_t K, int64_t gs, uint8_t* Wq,
+                        float* sg)
+{
+    if (N < 0 || K < 0 || gs < 2 || (gs & 1) || K % gs) return ORACLE_ERR_SHAPE;
+    int64_t groups = K / gs;
+    int64_t ld = oracle_w4g_scale_stride(K, gs);
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t g = 0; g < ld; ++g) {
+            if (g >= groups) {
+                sg[n * ld + g] = 0.0f;
+                continue;
+            }
+            const float* grp = W + n * K + g * gs;
+            float s = row_absmax(grp, gs) / 7.0f;
+            sg[n * ld + g] = s;
+            for (int64_t j = 0; j < gs / 2; ++j) {
+                int q0 = quant_code(grp[2 * j], s, 7);
+                int q1 = quant_code(grp[2 * j + 1], s, 7);
+                Wq[n * (K / 2) + g * (gs / 2) + j] = (uint8_t)((q0 & 0xF) | ((q1 & 0xF) << 4));
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* g2: group-wise W4A8 product, binary64 reference  [P1 当前实现方式: output */
+/*     = int32 accumulate * weight_scale * activation_scale, per group]      */
+/* ------------------------------------------------------------------------ */
+
+/* For every (m, n):
+     acc_g = sum over group g of Xq[m][k] * q_w[n][k]          (int64, exact)
+     Y[m][n] = s_a[m] * sum_g s_g[n][g] * acc_g                (binary64)
+     B[m][n] = s_a[m] * sum_g s_g[n][g] * sum over g of |Xq * q_w|
+   B is the magnitude in which the rounding error of an fp32 evaluation of Y
+   is bounded.  Every product s_g * acc_g is exact in binary64 (a 24-bit
+   significand times an integer below 2^26 for gs <= 2^16); only the sums
+   and the final product round. */
+int oracle_w4a8g_ref(const int8_t* Xq, const float* sa, int64_t M, int64_t K, int64_t gs,
+                     const uint8_t* Wq, const float* sg, int64_t N, double* Y, double* B)
+{
+    if (M < 0 || N < 0 || K < 0 || gs < 2 || (gs & 1) || K % gs || gs > 65536)
+        return ORACLE_ERR_SHAPE;
+    int64_t groups = K / gs;
+    int64_t ld = oracle_w4g_scale_stride(K, gs);
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double y = 0.0, b = 0.0;
+            for (int64_t g = 0; g < groups; ++g) {
+                int64_t acc = 0, mag = 0;
+                for (int64_t j = g * (gs / 2); j < (g + 1) * (gs / 2); ++j) {
+                    uint8_t byte = Wq[n * (K / 2) + j];
+                    int64_t p0 = (int64_t)Xq[m * K + 2 * j] * nibble_value(byte & 0xFu);
+                    int64_t p1 = (int64_t)Xq[m * K + 2 * j + 1] * nibble_value(byte >> 4);
+                    acc += p0 + p1;
+                    mag += (p0 < 0 ? -p0 : p0) + (p1 < 0 ? -p1 : p1);
+                }
+                double s = (double)sg[n * ld + g];
+                y += s * (double)acc;
+                b += s * (double)mag;
+            }
+            Y[m * N + n] = (double)sa[m] * y;
+            B[m * N + n] = (double)sa[m] * b;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* The whole group-wise linear: the per-row activation quantizer of a2, then
+   the reference above. */
+int oracle_w4a8g_linear(const uint16_t* X, int64_t M, int64_t K, int64_t gs, const uint8_t* Wq,
+                        const float* sg, int64_t N, double* Y, double* B, int8_t* Xq_out,
+                        float* sa_out)
+{
+    int st = oracle_act_quantize(X, M, K, Xq_out, sa_out);
+    if (st != ORACLE_OK) return st;
+    return oracle_w4a8g_ref(Xq_out, sa_out, M, K, gs, Wq, sg, N, Y, B);
 }

@@ -351,6 +351,138 @@ def pin_linear_error_bound(o):
 
 
 # --------------------------------------------------------------------------
+# g1/g2: group-wise INT4 scales
+# --------------------------------------------------------------------------
+
+def pin_w4g_golden(o):
+    """Hand-derived closed forms: per-group scales (with the zero padding of
+    the scale row), codes and packed bytes."""
+    for c in read_cases("w4g_quant_closed_forms.txt"):
+        gs = int(c["gs"][0])
+        row = np.array([float(v) for v in c["row"]], np.float32)[None, :]
+        Wq, sg = o.w4g_quantize(row, gs)
+        want_s = np.array([float(v) for v in c["scales"]], np.float32)
+        assert np.array_equal(sg[0], want_s), (c["name"], sg[0], want_s)
+        want = np.array([int(b, 16) for b in c["bytes"]], np.uint8)
+        assert np.array_equal(Wq[0], want), (c["name"], Wq[0], want)
+        codes = np.array([int(v) for v in c["codes"]], np.int64)
+        assert np.array_equal(decode_nibbles(Wq)[0], codes), c["name"]
+
+
+def pin_w4g_scale_stride(o):
+    """Scale rows hold K/gs entries rounded up to a multiple of four."""
+    for K, gs, want in [(896, 128, 8), (3584, 128, 28), (18944, 128, 148), (64, 32, 4),
+                        (4096, 4096, 4), (512, 64, 8), (96, 32, 4), (160, 32, 8)]:
+        assert o.w4g_scale_stride(K, gs) == want, (K, gs)
+
+
+def pin_w4g_reduces_to_rowwise(o):
+    """One group per row (gs = K) gives exactly the row-wise codes and scales,
+    and the reference product agrees with the row-wise rescale (two fp32
+    roundings) to 2^-23 relative."""
+    for (M, N, K, seed) in [(2, 24, 256, 41), (1, 9, 896, 42)]:
+        W = synth.normal(seed, (N, K), 0.02)
+        W[3, :] = 0.0
+        Wq_r, sw = o.w4_quantize(W)
+        Wq_g, sg = o.w4g_quantize(W, K)
+        assert np.array_equal(Wq_g, Wq_r)
+        assert np.array_equal(sg[:, 0], sw) and not sg[:, 1:].any()
+        X = synth.activation(seed + 7, M, K, outlier_frac=0.001)
+        Y_r, Xq, sa, _ = o.w4a8_linear(X, Wq_r, sw)
+        Y_g, B, Xq_g, sa_g = o.w4a8g_linear(X, Wq_g, sg, K)
+        assert np.array_equal(Xq_g, Xq) and np.array_equal(sa_g, sa)
+        assert np.all(np.abs(Y_r.astype(np.float64) - Y_g) <= 2.0 ** -23 * np.abs(Y_g) + 1e-300)
+        assert np.all(B >= np.abs(Y_g) * (1 - 1e-15))
+
+
+def pin_w4g_invariants(o):
+    """Seeded N(0, 0.02) rows, gs = 128: |w - q*s_g| <= s_g/2 per element, the
+    largest |w| of every group gets code +-7 with its sign, an all-zero group
+    gets scale 0 and codes 0 inside a non-zero row, codes stay in [-7, 7]."""
+    gs = 128
+    W = synth.normal(13, (24, 896), 0.02)
+    W[4, 130] *= 20.0
+    W[7, 256:384] = 0.0
+    Wq, sg = o.w4g_quantize(W, gs)
+    G = 896 // gs
+    assert sg.shape == (24, 8) and not sg[:, G:].any()
+    q = decode_nibbles(Wq).astype(np.float64)
+    s = np.repeat(sg[:, :G].astype(np.float64), gs, axis=1)
+    err = np.abs(W.astype(np.float64) - q * s)
+    assert np.all(err <= s / 2 * (1 + 2 ** -20) + 1e-45)
+    assert np.all(np.abs(q) <= 7)
+    for n in range(W.shape[0]):
+        for g in range(G):
+            grp = W[n, g * gs:(g + 1) * gs]
+            if sg[n, g] == 0:
+                assert not grp.any() and not q[n, g * gs:(g + 1) * gs].any()
+                continue
+            k = int(np.argmax(np.abs(grp)))
+            assert q[n, g * gs + k] == 7 * np.sign(grp[k])
+            assert sg[n, g] == f32_nearest(Fraction(float(np.max(np.abs(grp)))) / 7)
+    assert sg[7, 2] == 0 and sg[7, 1] > 0
+
+
+def pin_w4a8g_closed_forms(o):
+    """Every code +7 with group scales 2^-g and every activation code +127:
+    Y = s_a * 889 * gs * sum_g 2^-g exactly (one binary64 rounding) and B = Y;
+    alternating activation signs cancel inside each group: Y = 0, B unchanged."""
+    gs, G = 32, 5
+    K = gs * G
+    W = np.concatenate([np.full(gs, 7.0 * 2.0 ** -g) for g in range(G)]).astype(np.float32)
+    W = np.stack([W, -W])
+    Wq, sg = o.w4g_quantize(W, gs)
+    assert np.array_equal(sg[0, :G], [2.0 ** -g for g in range(G)])
+    for X, sign in [(np.ones((1, K), np.float16), 1), (np.tile(np.array([1, -1], np.float16), K // 2)[None, :], 0)]:
+        Y, B, Xq, sa = o.w4a8g_linear(X, Wq, sg, gs)
+        assert sa[0] == f32_nearest(Fraction(1, 127))
+        mag = Fraction(float(sa[0])) * 889 * gs * sum(Fraction(1, 2 ** g) for g in range(G))
+        want = float(mag) * sign
+        assert Y[0, 0] == want and Y[0, 1] == -want, (Y, want)
+        assert B[0, 0] == float(mag) and B[0, 1] == float(mag)
+
+
+def pin_w4a8g_bruteforce(o):
+    """The reference equals numpy's binary64 product of the dequantized
+    operands element by element (w_k = q_k * s_g(k), x_k = q_k * s_a), and B
+    equals the same sum over |products|."""
+    for (M, N, K, gs, seed) in [(1, 7, 128, 32, 51), (3, 5, 256, 64, 52), (2, 6, 896, 128, 53)]:
+        W = synth.normal(seed, (N, K), 0.02)
+        Wq, sg = o.w4g_quantize(W, gs)
+        Xq, sa = o.act_quantize(synth.activation(seed + 100, M, K))
+        Y, B = o.w4a8g_ref(Xq, sa, Wq, sg, gs)
+        w = decode_nibbles(Wq).astype(np.float64) * np.repeat(sg[:, :K // gs].astype(np.float64), gs, axis=1)
+        x = Xq.astype(np.float64) * sa.astype(np.float64)[:, None]
+        ref = x @ w.T
+        mag = np.abs(x) @ np.abs(w).T
+        assert np.all(np.abs(Y - ref) <= 1e-12 * mag + 1e-300)
+        assert np.all(np.abs(B - mag) <= 1e-12 * mag + 1e-300)
+
+
+def pin_w4a8g_error_bound(o):
+    """Quantized group-wise linear vs the fp64 unquantized GEMV within the
+    deterministic bound sum_k(|x| s_g/2 + |w| s_a/2 + s_g s_a/4)(1 + 2^-18),
+    and closer to it than row-wise scales on the same seeded operands."""
+    for (M, N, K, gs, seed) in [(1, 64, 896, 128, 61), (2, 16, 3584, 128, 62)]:
+        W = synth.normal(seed, (N, K), 0.02)
+        X = synth.activation(seed + 50, M, K, outlier_frac=0.001)
+        Wq, sg = o.w4g_quantize(W, gs)
+        Y, B, Xq, sa = o.w4a8g_linear(X, Wq, sg, gs)
+        ref = X.astype(np.float64) @ W.astype(np.float64).T
+        s_g = np.repeat(sg[:, :K // gs].astype(np.float64), gs, axis=1)   # [N][K]
+        s_a = sa.astype(np.float64)[:, None]
+        ax = np.abs(X).astype(np.float64)
+        bound = ((ax @ s_g.T) / 2 + np.abs(W).astype(np.float64).sum(1)[None, :] * s_a / 2
+                 + s_g.sum(1)[None, :] * s_a / 4) * (1 + 2 ** -18)
+        assert np.all(np.abs(Y - ref) <= bound)
+        Wq_r, sw = o.w4_quantize(W)
+        Y_r = o.w4a8_linear(X, Wq_r, sw)[0].astype(np.float64)
+        err_g = np.linalg.norm(Y - ref) / np.linalg.norm(ref)
+        err_r = np.linalg.norm(Y_r - ref) / np.linalg.norm(ref)
+        assert err_g < err_r, (err_g, err_r)
+
+
+# --------------------------------------------------------------------------
 # b1/b2: W8A16
 # --------------------------------------------------------------------------
 

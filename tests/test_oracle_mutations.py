@@ -44,6 +44,16 @@ MUTATIONS = [
     ("half_encode_ties_up", "if (rem > half || (rem == half && (n & 1u))) n += 1;", "if (rem >= half) n += 1;"),
     ("half_encode_truncate", "if (rem > half || (rem == half && (n & 1u))) n += 1;", ""),
     ("half_encode_overflow", "if (bits >= 0x7C00u) bits = 0x7C00u;", ""),
+    ("w4g_row_max", "float s = row_absmax(grp, gs) / 7.0f;", "float s = row_absmax(W + n * K, K) / 7.0f;"),
+    ("w4g_divisor_8", "row_absmax(grp, gs) / 7.0f", "row_absmax(grp, gs) / 8.0f"),
+    ("w4g_pack_group_offset", "Wq[n * (K / 2) + g * (gs / 2) + j]", "Wq[n * (K / 2) + j]"),
+    ("w4g_stride_unpadded", "return (groups + 3) / 4 * 4;", "return groups;"),
+    ("w4g_ref_scale_group0", "double s = (double)sg[n * ld + g];", "double s = (double)sg[n * ld];"),
+    ("w4g_ref_dropped_sa", "Y[m * N + n] = (double)sa[m] * y;", "Y[m * N + n] = y;"),
+    ("w4g_ref_signed_magnitude", "mag += (p0 < 0 ? -p0 : p0) + (p1 < 0 ? -p1 : p1);", "mag += p0 + p1;"),
+    ("w4g_ref_group_bytes", "for (int64_t j = g * (gs / 2); j < (g + 1) * (gs / 2); ++j)",
+     "for (int64_t j = 0; j < gs / 2; ++j)"),
+    ("w4g_ref_dropped_high", "acc += p0 + p1;", "acc += p0;"),
 ]
 
 
