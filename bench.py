@@ -21,6 +21,7 @@ Reported (one JSON line, rank 0):
             (linear layers only) plus lm_head: ms per token
   skinny_batch  gate and down at M = 1 ... 64 activation rows
   w8a16_set the ChatGLM2-6B-shaped W8A16 GEMVs at M=1
+  group_scale_set  the M=1 set with group-wise INT4 scales (group 128)
 
 `--impl reference` times the CPU oracle alone (the reference arm).
 Under torchrun with N > 1 every rank runs an independent replica (weak
@@ -473,6 +474,7 @@ def run_ours(args, world, rank):
     if not args.no_extra:
         extra["skinny_batch"] = measure_skinny(torch, w4, synth, dev, stream, copies, lin)
         extra["w8a16_set"] = measure_w8a16(torch, w4, synth, dev, stream)
+        extra["group_scale_set"] = measure_group_set(torch, w4, synth, dev, stream, lin)
         del copies
         torch.cuda.empty_cache()
         extra["decode_step_28_layers"] = measure_decode_step(torch, w4, synth, dev, stream, ws,
@@ -627,6 +629,60 @@ def measure_skinny(torch, w4, synth, dev, stream, copies, lin):
             res[str(M)] = {"us": round(us, 2), "GBps": round(weight_bytes(K, N) / us / 1e3, 1)}
         out[name] = res
     return out
+
+
+GROUP_SIZE = 128
+
+
+def measure_group_set(torch, w4, synth, dev, stream, lin, gs=GROUP_SIZE):
+    """The headline set with group-wise INT4 scales (one fp32 scale per 128
+    codes): same shapes, seeds, activations and launch structure (five
+    launches, q/k/v and gate/up grouped, PDL, two weight copies alternating
+    in graphs of two steps).  Bytes per linear: N * (K/2 + 4 * stride)."""
+    names = [l[0] for l in LINEARS]
+    copies = []
+    for c in range(2):
+        Wqs, sgs = [], []
+        for i, (_, K, N) in enumerate(LINEARS):
+            W = synth.normal_gpu(WEIGHT_SEED0 + i, (N, K), 0.02, device=dev)
+            Wq, sg = w4.w4g_quantize_weights(W, gs)
+            del W
+            Wqs.append(Wq)
+            sgs.append(sg)
+        copies.append((Wqs, sgs))
+    Xs, Ys = [], [torch.empty((1, N), dtype=torch.float32, device=dev) for _, _, N in LINEARS]
+    for _, members in LAUNCHES:
+        K = lin[members[0]][1]
+        Xs.append(torch.from_numpy(synth.activation(activation_seed(members[0]), 1, K,
+                                                    outlier_frac=OUTLIER_FRAC)).to(dev))
+    ws_bytes = max(w4.w4a8g_workspace_bytes(1, lin[m[0]][1], sum(lin[n][2] for n in m), gs)
+                   for _, m in LAUNCHES)
+    ws = torch.zeros(max(ws_bytes, 4096), dtype=torch.uint8, device=dev)
+
+    def launch(c, j, flags):
+        Wqs, sgs = copies[c]
+        idx = [names.index(n) for n in LAUNCHES[j][1]]
+        if len(idx) == 1:
+            w4.w4a8g_linear(Xs[j], Wqs[idx[0]], sgs[idx[0]], gs, Y=Ys[idx[0]], ws=ws, flags=flags)
+        else:
+            w4.w4a8g_linear_grouped(Xs[j], [Wqs[i] for i in idx], [sgs[i] for i in idx], gs,
+                                    Ys=[Ys[i] for i in idx], ws=ws, flags=flags)
+
+    def pair():
+        for c in range(2):
+            for j in range(len(LAUNCHES)):
+                launch(c, j, w4.LAUNCH_PDL)
+
+    us = _graph_us(torch, stream, pair, 2, reps=20)
+    nbytes = sum(N * (K // 2 + 4 * w4.w4g_scale_stride(K, gs)) for _, K, N in LINEARS)
+    jl = [l[0] for l in LAUNCHES].index("lm_head")
+    us_lm = _graph_us(torch, stream, lambda: [launch(k % 2, jl, 0) for k in range(20)], 20)
+    _, K_lm, N_lm = LINEARS[names.index("lm_head")]
+    lm_bytes = N_lm * (K_lm // 2 + 4 * w4.w4g_scale_stride(K_lm, gs))
+    del copies
+    return {"workload": "the M=1 set above with group-wise INT4 scales, group %d" % gs,
+            "weight_bytes": nbytes, "us_per_set": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+            "lm_head_in_chain": {"us": round(us_lm, 2), "GBps": round(lm_bytes / us_lm / 1e3, 1)}}
 
 
 W8A16_SET = [("h_to_4h", 4096, 27392), ("qkv", 4096, 4608), ("4h_to_h", 13696, 4096)]

@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) weight-quantized decode linear: W4A8 and W8A16.
+"""GB300 (sm_103a) weight-quantized decode linear: W4A8 (row-wise or
+group-wise INT4 scales) and W8A16.
 
 The compute lives in libw4a8.so (CUDA kernels behind the C ABI of
 include/w4a8.h); this package is its thin Python binding.
@@ -8,5 +9,7 @@ from ._binding import (  # noqa: F401
     act_quantize_i8, lib, w4_quantize_weights, w4a8_device_error, w4a8_gemv,
     w4a8_last_error, w4a8_linear, w4a8_linear_grouped, w4a8_linear_noalloc, w4a8_plan_info, w4a8_set_tuning, w4a8_workspace_bytes,
     w8_quantize_weights, w8a16_gemv, w8a16_workspace_bytes,
+    GROUP_PLAN_FIELDS, w4g_quantize_weights, w4g_scale_stride, w4a8g_gemv, w4a8g_linear,
+    w4a8g_linear_grouped, w4a8g_plan_info, w4a8g_workspace_bytes,
 )
 from .build import build  # noqa: F401

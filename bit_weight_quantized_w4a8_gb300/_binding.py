@@ -27,6 +27,8 @@ EXPORTS = [
     "w8a16_workspace_bytes", "w8a16_gemv",
     "w4a8_last_error", "w4a8_device_error", "w4a8_set_tuning", "w4a8_plan_info",
     "w4a8_linear_noalloc", "w4a8_linear_grouped",
+    "w4g_quantize_weights", "w4a8g_workspace_bytes", "w4a8g_gemv", "w4a8g_linear",
+    "w4a8g_linear_grouped", "w4a8g_plan_info",
 ]
 
 
@@ -60,6 +62,16 @@ _SIGS = {
     "w4a8_set_tuning": (ctypes.c_int, [ctypes.POINTER(_Tuning)]),
     "w4a8_plan_info": (ctypes.c_int, [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int,
                                       ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
+    "w4g_quantize_weights": (ctypes.c_int, [_p, _i64, _i64, _i64, _p, _p, _p]),
+    "w4a8g_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, _i64]),
+    "w4a8g_gemv": (ctypes.c_int, [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, ctypes.c_size_t,
+                                  _u, _p]),
+    "w4a8g_linear": (ctypes.c_int, [_p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _p, _p,
+                                    ctypes.c_size_t, _u, _p]),
+    "w4a8g_linear_grouped": (ctypes.c_int, [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _p, _p,
+                                            _p, ctypes.c_size_t, _u, _p]),
+    "w4a8g_plan_info": (ctypes.c_int, [_i64, _i64, _i64, _i64, ctypes.c_int,
+                                       ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
 }
 
 _lib = None
@@ -283,6 +295,103 @@ def w8a16_gemv(X, Wq8, sw16, Y=None, ws=None, flags: int = 0):
     return Y
 
 
+# -- group-wise INT4 scales -------------------------------------------------
+
+def w4g_scale_stride(K: int, group: int) -> int:
+    """Floats per row of the group-scale matrix: K/group rounded up to a
+    multiple of 4 (the W4G_SCALE_STRIDE layout of the C header)."""
+    return (K // group + 3) // 4 * 4
+
+
+def w4g_quantize_weights(W: torch.Tensor, group: int, Wq=None, sg=None):
+    """W [N][K] fp32 -> (Wq [N][K/2] uint8, sg [N][stride] fp32)."""
+    _want(W, torch.float32, "W")
+    N, K = W.shape
+    ld = w4g_scale_stride(K, group) if group > 0 else 0
+    Wq = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device) if Wq is None else Wq
+    sg = torch.empty((N, ld), dtype=torch.float32, device=W.device) if sg is None else sg
+    _want(Wq, torch.uint8, "Wq", (N, K // 2))
+    _want(sg, torch.float32, "sg", (N, ld))
+    _check(lib().w4g_quantize_weights(_ptr(W), N, K, group, _ptr(Wq), _ptr(sg), _stream(W)))
+    return Wq, sg
+
+
+def w4a8g_workspace_bytes(M: int, K: int, N: int, group: int) -> int:
+    return int(lib().w4a8g_workspace_bytes(M, K, N, group))
+
+
+def _want_group(Wq, sg, N, K, group, name=""):
+    _want(Wq, torch.uint8, "Wq" + name, (N, K // 2))
+    _want(sg, torch.float32, "sg" + name, (N, w4g_scale_stride(K, group) if group > 0 else 0))
+
+
+def w4a8g_gemv(Xq, sa, Wq, sg, group: int, Y=None, ws=None, flags: int = 0):
+    """Y[m][n] = sa[m] * sum_g sg[n][g] * acc_g[m][n] (group-wise scales); returns Y."""
+    _want(Xq, torch.int8, "Xq")
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    _want(sa, torch.float32, "sa", (M,))
+    _want_group(Wq, sg, N, K, group)
+    Y = torch.empty((M, N), dtype=torch.float32, device=Xq.device) if Y is None else Y
+    _want(Y, torch.float32, "Y", (M, N))
+    ws = _workspace(w4a8g_workspace_bytes(M, K, N, group), Xq.device, ws)
+    _check(lib().w4a8g_gemv(_ptr(Xq), _ptr(sa), M, K, group, _ptr(Wq), _ptr(sg), N, _ptr(Y),
+                            _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), flags,
+                            _stream(Xq)))
+    return Y
+
+
+def w4a8g_linear(X, Wq, sg, group: int, Y=None, Xq_out=None, sa_out=None, ws=None,
+                 flags: int = 0):
+    """Fused activation quantization + group-scale W4A8 product; returns Y."""
+    _want(X, torch.float16, "X")
+    M, K = X.shape
+    N = Wq.shape[0]
+    _want_group(Wq, sg, N, K, group)
+    Y = torch.empty((M, N), dtype=torch.float32, device=X.device) if Y is None else Y
+    _want(Y, torch.float32, "Y", (M, N))
+    if Xq_out is not None:
+        _want(Xq_out, torch.int8, "Xq_out", (M, K))
+    if sa_out is not None:
+        _want(sa_out, torch.float32, "sa_out", (M,))
+    ws = _workspace(w4a8g_workspace_bytes(M, K, N, group), X.device, ws)
+    _check(lib().w4a8g_linear(_ptr(X), M, K, group, _ptr(Wq), _ptr(sg), N, _ptr(Y),
+                              _ptr(Xq_out), _ptr(sa_out), _ptr(ws),
+                              0 if ws is None else ws.numel() * ws.element_size(), flags,
+                              _stream(X)))
+    return Y
+
+
+def w4a8g_linear_grouped(X, Wqs, sgs, group: int, Ys=None, ws=None, flags: int = 0):
+    """One launch for several group-scale weight matrices sharing X; returns
+    the list of outputs."""
+    _want(X, torch.float16, "X")
+    M, K = X.shape
+    G = len(Wqs)
+    if G != len(sgs) or not 1 <= G <= 4:
+        raise ValueError("need 1..4 weight matrices with one scale matrix each")
+    Ns = [int(w.shape[0]) for w in Wqs]
+    for g in range(G):
+        _want_group(Wqs[g], sgs[g], Ns[g], K, group, "[%d]" % g)
+    if Ys is None:
+        Ys = [torch.empty((M, n), dtype=torch.float32, device=X.device) for n in Ns]
+    for g in range(G):
+        _want(Ys[g], torch.float32, "Y[%d]" % g, (M, Ns[g]))
+    arr_p = ctypes.c_void_p * G
+    wq_a = arr_p(*[w.data_ptr() for w in Wqs])
+    sg_a = arr_p(*[t.data_ptr() for t in sgs])
+    y_a = arr_p(*[y.data_ptr() for y in Ys])
+    n_a = (ctypes.c_int64 * G)(*Ns)
+    ws = _workspace(w4a8g_workspace_bytes(M, K, sum(Ns), group), X.device, ws)
+    _check(lib().w4a8g_linear_grouped(_ptr(X), M, K, group, G, ctypes.cast(wq_a, ctypes.c_void_p),
+                                      ctypes.cast(sg_a, ctypes.c_void_p),
+                                      ctypes.cast(n_a, ctypes.c_void_p),
+                                      ctypes.cast(y_a, ctypes.c_void_p), _ptr(ws),
+                                      0 if ws is None else ws.numel() * ws.element_size(), flags,
+                                      _stream(X)))
+    return Ys
+
+
 def w4a8_last_error() -> str:
     return lib().w4a8_last_error().decode(errors="replace")
 
@@ -315,3 +424,13 @@ def w4a8_plan_info(M: int, K: int, N: int, w8a16: bool = False, num_sms: int = 0
     arr = (ctypes.c_int * len(PLAN_FIELDS))()
     _check(lib().w4a8_plan_info(M, K, N, int(w8a16), num_sms, arr, len(PLAN_FIELDS)))
     return dict(zip(PLAN_FIELDS, list(arr)))
+
+
+GROUP_PLAN_FIELDS = PLAN_FIELDS + ("scale_window", "scale_stage_bytes")
+
+
+def w4a8g_plan_info(M: int, K: int, N: int, group: int, num_sms: int = 0) -> dict:
+    """Launch plan of the group-scale entry points; num_sms > 0 plans without a GPU."""
+    arr = (ctypes.c_int * len(GROUP_PLAN_FIELDS))()
+    _check(lib().w4a8g_plan_info(M, K, N, group, num_sms, arr, len(GROUP_PLAN_FIELDS)))
+    return dict(zip(GROUP_PLAN_FIELDS, list(arr)))

@@ -78,13 +78,14 @@ w4a8::Tuning tuning() {
     return t;
 }
 
+// gshift >= 0: group-wise scales, one per 2^gshift granules, rows of gld floats.
 int plan_for(bool w4, bool fused, int64_t M, int64_t K, int64_t N, w4a8::GemvPlan* pl,
-             int sms = 0) {
+             int sms = 0, int gshift = -1, int gld = 0) {
     if (sms <= 0) {
         int st = sm_count(&sms);
         if (st != W4A8_OK) return st;
     }
-    if (!w4a8::make_gemv_plan(w4, fused, (int)M, K, N, sms, tuning(), pl))
+    if (!w4a8::make_gemv_plan(w4, fused, (int)M, K, N, sms, tuning(), pl, gshift, gld))
         return fail(W4A8_ERR_SHAPE, "no launch plan for M=%lld K=%lld N=%lld",
                     (long long)M, (long long)K, (long long)N);
     return W4A8_OK;
@@ -129,12 +130,25 @@ constexpr int kRowGroupW8 = 4;
 // Plans of the row groups of an M-row call: `full` for groups of `rg`
 // rows, `tail` for a shorter last group (equal to `full` when there is none).
 int plan_row_groups(bool w4, bool fused, int64_t M, int64_t K, int64_t N, int rg,
-                    w4a8::GemvPlan* full, w4a8::GemvPlan* tail, int sms = 0) {
-    int st = plan_for(w4, fused, M < rg ? M : rg, K, N, full, sms);
+                    w4a8::GemvPlan* full, w4a8::GemvPlan* tail, int sms = 0, int gshift = -1,
+                    int gld = 0) {
+    int st = plan_for(w4, fused, M < rg ? M : rg, K, N, full, sms, gshift, gld);
     if (st != W4A8_OK) return st;
     *tail = *full;
-    if (M > rg && M % rg) st = plan_for(w4, fused, M % rg, K, N, tail, sms);
+    if (M > rg && M % rg) st = plan_for(w4, fused, M % rg, K, N, tail, sms, gshift, gld);
     return st;
+}
+
+// Group-wise scales: `group` a power of two in [32, K] dividing K.
+int check_group(int64_t K, int64_t group, int* gshift, int* gld) {
+    if (group < 32 || group > K || (group & (group - 1)) || K % group)
+        return fail(W4A8_ERR_SHAPE, "group=%lld must be a power of two in [32, K=%lld] dividing K",
+                    (long long)group, (long long)K);
+    int sh = 0;
+    while ((32LL << sh) < group) ++sh;
+    *gshift = sh;
+    *gld = (int)W4G_SCALE_STRIDE(K, group);
+    return W4A8_OK;
 }
 
 int check_workspace(const w4a8::GemvPlan& pl, void* ws, size_t ws_bytes) {
@@ -188,6 +202,31 @@ size_t w4a8_workspace_bytes(int64_t M, int64_t K, int64_t N) {
     w4a8::GemvPlan pf, pt;
     // the fused and unfused kernels share the split plan
     if (plan_row_groups(true, true, M, K, N, kRowGroupW4, &pf, &pt) != W4A8_OK) return 0;
+    return pf.ws_bytes > pt.ws_bytes ? pf.ws_bytes : pt.ws_bytes;
+}
+
+int w4g_quantize_weights(const float* W, int64_t N, int64_t K, int64_t group, uint8_t* Wq,
+                         float* sg, void* stream) {
+    if (!W || !Wq || !sg) return fail(W4A8_ERR_NULL, "w4g_quantize_weights: NULL pointer");
+    if (N < 1 || N > 0x7FFFFFFF) return fail(W4A8_ERR_SHAPE, "N=%lld outside [1, 2^31-1]", (long long)N);
+    if (K < 32 || K % 32 || K > (1LL << 30)) return fail(W4A8_ERR_SHAPE, "K=%lld must be a positive multiple of 32", (long long)K);
+    int gshift, gld;
+    int st = check_group(K, group, &gshift, &gld);
+    if (st != W4A8_OK) return st;
+    if (!aligned(W, 16) || !aligned(Wq, 16) || !aligned(sg, 16))
+        return fail(W4A8_ERR_ALIGN, "w4g_quantize_weights: W, Wq and sg must be 16-byte aligned");
+    cudaError_t e = w4a8::launch_w4g_quantize(W, N, K, (int)group, gld, Wq, sg,
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w4g_quantize_weights launch");
+}
+
+size_t w4a8g_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t group) {
+    if (check_w4a8_shape(M, K, N) != W4A8_OK) return 0;
+    int gshift, gld;
+    if (check_group(K, group, &gshift, &gld) != W4A8_OK) return 0;
+    w4a8::GemvPlan pf, pt;
+    if (plan_row_groups(true, true, M, K, N, kRowGroupW4, &pf, &pt, 0, gshift, gld) != W4A8_OK)
+        return 0;
     return pf.ws_bytes > pt.ws_bytes ? pf.ws_bytes : pt.ws_bytes;
 }
 
@@ -313,6 +352,80 @@ int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const ui
     return ok();
 }
 
+}  // extern "C"
+
+namespace {
+
+// Shared body of the group-scale entry points: X (fused) or Xq + sa.
+int w4a8g_run(const char* name, const uint16_t* X, const int8_t* Xq, const float* sa, int64_t M,
+              int64_t K, int64_t group, int G, const uint8_t* const* Wq, const float* const* sg,
+              const int64_t* N, float* const* Y, int8_t* Xq_out, float* sa_out, void* ws,
+              size_t ws_bytes, unsigned flags, void* stream) {
+    if (G < 1 || G > W4A8_MAX_GROUP)
+        return fail(W4A8_ERR_SHAPE, "%s: G=%d outside [1, %d]", name, G, W4A8_MAX_GROUP);
+    int64_t total = 0;
+    for (int g = 0; g < G; ++g) {
+        if (!Wq[g] || !sg[g] || !Y[g]) return fail(W4A8_ERR_NULL, "%s: NULL pointer in group %d", name, g);
+        if (N[g] < 1) return fail(W4A8_ERR_SHAPE, "%s: N[%d]=%lld < 1", name, g, (long long)N[g]);
+        if (!aligned(Wq[g], 16) || !aligned(sg[g], 16) || !aligned(Y[g], 4))
+            return fail(W4A8_ERR_ALIGN, "%s: Wq and sg need 16-byte, Y 4-byte alignment", name);
+        total += N[g];
+    }
+    int st = check_w4a8_shape(M, K, total);
+    if (st != W4A8_OK) return st;
+    int gshift, gld;
+    if ((st = check_group(K, group, &gshift, &gld)) != W4A8_OK) return st;
+    if ((X && !aligned(X, 16)) || (Xq && !aligned(Xq, 16)) || (sa && !aligned(sa, 4)) ||
+        (Xq_out && !aligned(Xq_out, 16)) || (sa_out && !aligned(sa_out, 4)))
+        return fail(W4A8_ERR_ALIGN, "%s: X/Xq/Xq_out need 16-byte, sa/sa_out 4-byte alignment", name);
+    w4a8::GemvPlan pf, pt;
+    if ((st = plan_row_groups(true, true, M, K, total, kRowGroupW4, &pf, &pt, 0, gshift, gld)) != W4A8_OK)
+        return st;
+    if ((st = check_workspace(pf, ws, ws_bytes)) != W4A8_OK) return st;
+    if ((st = check_workspace(pt, ws, ws_bytes)) != W4A8_OK) return st;
+    float* Yg[W4A8_MAX_GROUP];
+    for (int64_t m0 = 0; m0 < M; m0 += kRowGroupW4) {
+        const int64_t mg = M - m0 < kRowGroupW4 ? M - m0 : kRowGroupW4;
+        for (int g = 0; g < G; ++g) Yg[g] = Y[g] + m0 * N[g];
+        cudaError_t e = w4a8::launch_w4a8g(
+            mg == kRowGroupW4 || M < kRowGroupW4 ? pf : pt, X != nullptr,
+            X ? X + m0 * K : nullptr, Xq ? Xq + m0 * K : nullptr, sa ? sa + m0 : nullptr, (int)mg,
+            K, (int)group, G, Wq, sg, N, Yg, Xq_out ? Xq_out + m0 * K : nullptr,
+            sa_out ? sa_out + m0 : nullptr, ws, flags, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, name);
+    }
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int w4a8g_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, int64_t group,
+               const uint8_t* Wq, const float* sg, int64_t N, float* Y, void* ws,
+               size_t ws_bytes, unsigned flags, void* stream) {
+    if (!Xq || !sa || !Wq || !sg || !Y) return fail(W4A8_ERR_NULL, "w4a8g_gemv: NULL pointer");
+    return w4a8g_run("w4a8g_gemv", nullptr, Xq, sa, M, K, group, 1, &Wq, &sg, &N, &Y, nullptr,
+                     nullptr, ws, ws_bytes, flags, stream);
+}
+
+int w4a8g_linear(const uint16_t* X, int64_t M, int64_t K, int64_t group, const uint8_t* Wq,
+                 const float* sg, int64_t N, float* Y, int8_t* Xq_out, float* sa_out, void* ws,
+                 size_t ws_bytes, unsigned flags, void* stream) {
+    if (!X || !Wq || !sg || !Y) return fail(W4A8_ERR_NULL, "w4a8g_linear: NULL pointer");
+    return w4a8g_run("w4a8g_linear", X, nullptr, nullptr, M, K, group, 1, &Wq, &sg, &N, &Y,
+                     Xq_out, sa_out, ws, ws_bytes, flags, stream);
+}
+
+int w4a8g_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int64_t group, int G,
+                         const uint8_t* const* Wq, const float* const* sg, const int64_t* N,
+                         float* const* Y, void* ws, size_t ws_bytes, unsigned flags,
+                         void* stream) {
+    if (!X || !Wq || !sg || !N || !Y) return fail(W4A8_ERR_NULL, "w4a8g_linear_grouped: NULL pointer");
+    return w4a8g_run("w4a8g_linear_grouped", X, nullptr, nullptr, M, K, group, G, Wq, sg, N, Y,
+                     nullptr, nullptr, ws, ws_bytes, flags, stream);
+}
+
 int w8a16_gemv(const uint16_t* X, int64_t M, int64_t K, const int8_t* Wq8, const uint16_t* sw16,
                int64_t N, float* Y, void* ws, size_t ws_bytes, unsigned flags, void* stream) {
     if (!X || !Wq8 || !sw16 || !Y) return fail(W4A8_ERR_NULL, "w8a16_gemv: NULL pointer");
@@ -340,6 +453,7 @@ int w4a8_device_error(unsigned* flags, void* stream) {
     if (!flags) return fail(W4A8_ERR_NULL, "w4a8_device_error: NULL pointer");
     cudaError_t e = w4a8::read_and_clear_device_error(flags, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = w4a8::read_and_clear_mma_error(flags, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = w4a8::read_and_clear_group_error(flags, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_device_error");
 }
 
@@ -395,6 +509,25 @@ int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int*
     const int ws = wsb > 0x7FFFFFFF ? 0x7FFFFFFF : (int)wsb;
     const int v[] = {pl.P, pl.Cl, pl.S, pl.Rl, pl.Gs, pl.grid, pl.rows_max, pl.NS,
                      pl.stage_stride, pl.smem, ws, 0};
+    for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
+    return ok();
+}
+
+int w4a8g_plan_info(int64_t M, int64_t K, int64_t N, int64_t group, int num_sms, int* info,
+                    int n_info) {
+    if (!info) return fail(W4A8_ERR_NULL, "w4a8g_plan_info: NULL pointer");
+    int st = check_w4a8_shape(M, K, N);
+    if (st != W4A8_OK) return st;
+    int gshift, gld;
+    if ((st = check_group(K, group, &gshift, &gld)) != W4A8_OK) return st;
+    w4a8::GemvPlan pl, pt;
+    if ((st = plan_row_groups(true, true, M, K, N, kRowGroupW4, &pl, &pt, num_sms, gshift, gld)) !=
+        W4A8_OK)
+        return st;
+    const size_t wsb = pl.ws_bytes > pt.ws_bytes ? pl.ws_bytes : pt.ws_bytes;
+    const int ws = wsb > 0x7FFFFFFF ? 0x7FFFFFFF : (int)wsb;
+    const int v[] = {pl.P, pl.Cl, pl.S, pl.Rl, pl.Gs, pl.grid, pl.rows_max, pl.NS,
+                     pl.stage_stride, pl.smem, ws, 0, pl.gwin, pl.gstage};
     for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
     return ok();
 }

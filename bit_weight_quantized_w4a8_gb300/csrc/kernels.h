@@ -11,6 +11,8 @@ namespace w4a8 {
 
 cudaError_t launch_w4_quantize(const float* W, int64_t N, int64_t K, uint8_t* Wq, float* sw,
                                cudaStream_t stream);
+cudaError_t launch_w4g_quantize(const float* W, int64_t N, int64_t K, int gs, int64_t ld,
+                                uint8_t* Wq, float* sg, cudaStream_t stream);
 cudaError_t launch_w8_quantize(const float* W, int64_t N, int64_t K, int8_t* Wq8, uint16_t* sw16,
                                cudaStream_t stream);
 cudaError_t launch_act_quantize(const uint16_t* X, int64_t M, int64_t K, int8_t* Xq, float* sa,
@@ -29,6 +31,16 @@ cudaError_t launch_w8a16(const GemvPlan& pl, const uint16_t* X, int M, int64_t K
                          unsigned flags, cudaStream_t stream);
 
 cudaError_t read_and_clear_device_error(unsigned* flags, cudaStream_t stream);
+
+// Group-wise INT4 scales (gemv_group.cu): G weight matrices sharing the
+// activation (G = 1 for a single linear); X (fused) or Xq + sa (unfused).
+cudaError_t launch_w4a8g(const GemvPlan& pl, bool fused, const uint16_t* X, const int8_t* Xq,
+                         const float* sa, int M, int64_t K, int gs, int G,
+                         const uint8_t* const* Wq, const float* const* sg, const int64_t* Ns,
+                         float* const* Y, int8_t* Xq_out, float* sa_out, void* ws,
+                         unsigned flags, cudaStream_t stream);
+// ORs the group-scale kernels' device error word into *flags and clears it.
+cudaError_t read_and_clear_group_error(unsigned* flags, cudaStream_t stream);
 
 // Tensor-core path (mma.cu).  make_mma_plan is host-only and needs no GPU.
 bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out);

@@ -1,6 +1,7 @@
 // quant.cu -- weight and activation quantizer kernels for sm_103a.
 //
-// Row-wise INT4 weights (the Jetson INT4 page, section 当前实现方式),
+// Row-wise and group-wise INT4 weights (the Jetson INT4 page, sections
+// 当前实现方式 and 后续优化方向),
 // per-channel INT8 weights (the TPU-MLIR W8A16 page, sections 2-3) and the
 // dynamic per-row INT8 activation quantizer (the Jetson INT4 page, section
 // 正确方向).  One CTA per row: a max|.| reduction over the row, then every
@@ -64,6 +65,45 @@ __global__ void __launch_bounds__(kQThreads) w4_quantize_kernel(const float* __r
         for (int t = 0; t < 8; ++t)
             word |= (static_cast<uint32_t>(quant_code(v[t], s, 7.f)) & 0xFu) << (4 * t);
         out[u] = word;
+    }
+}
+
+// Group-wise INT4 (the Jetson INT4 page, section 后续优化方向: group-wise
+// scales): the row-wise rule applied to each group of gs codes of a row.
+// W [N][K] fp32 -> Wq [N][K/2] packed nibbles + sg [N][ld] fp32, ld = K/gs
+// rounded up to a multiple of 4 (padding written as 0).  One CTA per row,
+// one warp per group at a time; gs is a multiple of 32.
+__global__ void __launch_bounds__(kQThreads) w4g_quantize_kernel(const float* __restrict__ W,
+                                                                  int64_t K, int gs, int64_t ld,
+                                                                  uint8_t* __restrict__ Wq,
+                                                                  float* __restrict__ sg) {
+    const int64_t n = blockIdx.x;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t groups = K / gs;
+    for (int64_t g = warp; g < ld; g += kQThreads / 32) {
+        if (g >= groups) {
+            if (lane == 0) sg[n * ld + g] = 0.f;
+            continue;
+        }
+        const float4* grp = reinterpret_cast<const float4*>(W + n * K + g * gs);
+        float m = 0.f;
+        for (int v = lane; v < gs / 4; v += 32) m = fmaxf(m, absmax4(grp[v]));
+        #pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const float s = __fdiv_rn(m, 7.f);
+        if (lane == 0) sg[n * ld + g] = s;
+        uint32_t* out = reinterpret_cast<uint32_t*>(Wq + n * (K / 2) + g * (gs / 2));
+        for (int u = lane; u < gs / 8; u += 32) {  // 8 codes -> 4 bytes
+            const float4 a = grp[2 * u];
+            const float4 b = grp[2 * u + 1];
+            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            uint32_t word = 0;
+            #pragma unroll
+            for (int t = 0; t < 8; ++t)
+                word |= (static_cast<uint32_t>(quant_code(v[t], s, 7.f)) & 0xFu) << (4 * t);
+            out[u] = word;
+        }
     }
 }
 
@@ -133,6 +173,12 @@ __global__ void __launch_bounds__(kQThreads) act_quantize_kernel(const __half* _
 cudaError_t launch_w4_quantize(const float* W, int64_t N, int64_t K, uint8_t* Wq, float* sw,
                                cudaStream_t stream) {
     w4_quantize_kernel<<<dim3((unsigned)N), kQThreads, 0, stream>>>(W, K, Wq, sw);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_w4g_quantize(const float* W, int64_t N, int64_t K, int gs, int64_t ld,
+                                uint8_t* Wq, float* sg, cudaStream_t stream) {
+    w4g_quantize_kernel<<<dim3((unsigned)N), kQThreads, 0, stream>>>(W, K, gs, ld, Wq, sg);
     return cudaGetLastError();
 }
 

@@ -197,6 +197,76 @@ int w4a8_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, const uint8_t* 
                         const float* sw, int64_t N, float* Y, unsigned flags, void* stream);
 
 /* ---------------------------------------------------------------------- */
+/* W4A8 with group-wise weight scales                                      */
+/* ---------------------------------------------------------------------- */
+
+/* Group-wise scales (the Jetson INT4 page, section 后续优化方向, which names
+ * group-wise scales as the next step for precision): one fp32 scale per
+ * group of `group` consecutive codes of a weight row instead of one per row.
+ * `group` is a power of two from 32 to K that divides K.  Scale rows are
+ * padded to 16 bytes: sg is [N][W4G_SCALE_STRIDE(K, group)] fp32, the
+ * stride being K/group rounded up to a multiple of 4; w4g_quantize_weights
+ * writes the padding entries as 0 and the products never use them. */
+#define W4G_SCALE_STRIDE(K, group) ((((K) / (group)) + 3) / 4 * 4)
+
+/* Group-wise INT4 weight quantization: for each row n and group g,
+ * s = max|W over the group| / 7 (fp32 IEEE division),
+ * q = clamp(round_half_away(w / s), -7, 7), packed as w4_quantize_weights.
+ * With group == K the codes and scales are those of w4_quantize_weights.
+ *   W [N][K] fp32 in;  Wq [N][K/2] uint8 out;  sg [N][stride] fp32 out.
+ *   Requires N >= 1, K >= 32, K % 32 == 0, the group rule above; W, Wq
+ *   and sg 16-byte aligned.
+ * Bit-identical to the CPU definition for finite inputs. */
+int w4g_quantize_weights(const float* W, int64_t N, int64_t K, int64_t group, uint8_t* Wq,
+                         float* sg, void* stream);
+
+/* Workspace bytes of w4a8g_gemv / w4a8g_linear (rules of
+ * w4a8_workspace_bytes; 0 also for shapes those calls reject). */
+size_t w4a8g_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t group);
+
+/* INT4 x INT8 product with group-wise weight scales:
+ *   Y[m][n] = sa[m] * sum_g sg[n][g] * acc_g[m][n],
+ *   acc_g[m][n] = sum over the codes k of group g of Xq[m][k] * q[n][k].
+ * Arithmetic: the int32 sum of every 32-code granule is exact; it is
+ * multiplied by its group's scale and added into an fp32 sum with one
+ * fused multiply-add, the partial sums are added in fp32 in an order fixed
+ * by the launch plan (the same on every call with the same shape and
+ * device), and the total is multiplied by sa[m].  The result therefore
+ * lies within (K/32 + 4) * 2^-24 * sa[m] * sum_g sg[n][g] * |acc|_g of the
+ * exact value, |acc|_g being the sum of |Xq * q| over group g.
+ *   Xq [M][K] int8, sa [M] fp32    quantized activation (act_quantize_i8)
+ *   Wq [N][K/2] uint8, sg [N][stride] fp32   (w4g_quantize_weights)
+ *   Y [M][N] fp32 out; ws, ws_bytes (w4a8g_workspace_bytes) and flags as
+ *   in w4a8_gemv.
+ * Requires 1 <= M <= W4A8_MAX_M (one launch per group of up to 8 rows, on
+ * the dp4a kernel; the tensor-core kernel does not take group scales),
+ * the w4a8_gemv limits on K and N, the group rule above; Xq, Wq and sg
+ * 16-byte aligned; Y and sa 4-byte aligned. */
+int w4a8g_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, int64_t group,
+               const uint8_t* Wq, const float* sg, int64_t N, float* Y, void* ws,
+               size_t ws_bytes, unsigned flags, void* stream);
+
+/* Fused linear with group-wise scales: activation quantization and the
+ * product above in one kernel.  Xq_out [M][K] int8 and sa_out [M] fp32 are
+ * optional outputs (NULL to skip), bit-identical to act_quantize_i8's; Y is
+ * bit-identical to act_quantize_i8 followed by w4a8g_gemv.
+ * Requires the w4a8g_gemv limits; X 16-byte aligned. */
+int w4a8g_linear(const uint16_t* X, int64_t M, int64_t K, int64_t group, const uint8_t* Wq,
+                 const float* sg, int64_t N, float* Y, int8_t* Xq_out, float* sa_out, void* ws,
+                 size_t ws_bytes, unsigned flags, void* stream);
+
+/* Grouped fused linear with group-wise scales: G weight matrices reading
+ * the same activation in one launch, as w4a8_linear_grouped.  Wq, sg, N, Y
+ * are HOST arrays of G device pointers / sizes; ws covers
+ * w4a8g_workspace_bytes(M, K, N[0] + ... + N[G-1], group).  Y[g] is within
+ * the w4a8g_gemv bound of the exact product (its rounding may differ from
+ * w4a8g_linear's, whose launch plan differs). */
+int w4a8g_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int64_t group, int G,
+                         const uint8_t* const* Wq, const float* const* sg, const int64_t* N,
+                         float* const* Y, void* ws, size_t ws_bytes, unsigned flags,
+                         void* stream);
+
+/* ---------------------------------------------------------------------- */
 /* W8A16 linear                                                            */
 /* ---------------------------------------------------------------------- */
 
@@ -205,9 +275,10 @@ size_t w8a16_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
 /* INT8-weight x F16-activation product (the TPU-MLIR W8A16 page,
  * section 4: cast INT8 to floating point, multiply by the scale, multiply
- * with the activation).  The code is widened to fp32 exactly in registers,
- * products are exact in fp32, sums are fp32, and the per-channel scale is
- * applied once per output: Y[m][n] = float(sw16[n]) * sum_k q[n][k]*x[m][k].
+ * with the activation).  The code is widened to binary16 exactly in
+ * registers, each binary16 x binary16 product is exact in fp32, sums are
+ * fp32, and the per-channel scale is applied once per output:
+ * Y[m][n] = float(sw16[n]) * sum_k q[n][k]*x[m][k].
  *   X [M][K] binary16, Wq8 [N][K] int8, sw16 [N] binary16, Y [M][N] fp32.
  * Requires 1 <= M <= W8A16_MAX_M, 16 <= K <= 65536, K % 16 == 0,
  * 1 <= N <= 2^31 - 1; X and Wq8 16-byte aligned, Y 4-byte aligned. */
@@ -267,6 +338,12 @@ int w4a8_set_tuning(const w4a8_tuning_t* tuning);
  * device. */
 int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int* info,
                    int n_info);
+
+/* The same for w4a8g_gemv / w4a8g_linear (the last field is always 0),
+ * followed by two more: the widest scale window a K piece reads (floats
+ * per row) and the bytes of one ring slot's scale area. */
+int w4a8g_plan_info(int64_t M, int64_t K, int64_t N, int64_t group, int num_sms, int* info,
+                    int n_info);
 
 #ifdef __cplusplus
 }

@@ -181,3 +181,80 @@ def test_forced_plans_respected():
         assert w4.w4a8_plan_info(1, 3584, 3584, num_sms=152)["stages"] == 2
     finally:
         w4.w4a8_set_tuning(reset=True)
+
+
+# --------------------------------------------------------------------------
+# group-wise scales
+# --------------------------------------------------------------------------
+
+def test_group_argument_checks(L):
+    E_S, E_A, E_N = w4._binding.ERR_SHAPE, w4._binding.ERR_ALIGN, w4._binding.ERR_NULL
+    for gs in (16, 48, 96, 3584, 0, -32, 8192):   # below 32, not a power of two, > K
+        assert L.w4g_quantize_weights(P16, 4, 3584, gs, P16, P16, None) == E_S, gs
+        assert L.w4a8g_linear(P16, 1, 3584, gs, P16, P16, 4, P16, None, None, None, 0, 0, None) == E_S, gs
+        assert L.w4a8g_workspace_bytes(1, 3584, 4, gs) == 0
+    assert L.w4g_quantize_weights(P16, 4, 3584, 1024, P16, P16, None) == E_S   # 1024 does not divide 3584
+    assert L.w4g_quantize_weights(P16, 4, 3584, 128, P16, P16 + 4, None) == E_A  # scales 16-byte aligned
+    assert L.w4g_quantize_weights(None, 4, 3584, 128, P16, P16, None) == E_N
+    assert L.w4a8g_gemv(P16, P16, 1, 3584, 128, P16, P16 + 8, 4, P16, None, 0, 0, None) == E_A
+    assert L.w4a8g_gemv(P16, None, 1, 3584, 128, P16, P16, 4, P16, None, 0, 0, None) == E_N
+    assert L.w4a8g_gemv(P16, P16, 65, 3584, 128, P16, P16, 4, P16, None, 0, 0, None) == E_S
+    assert L.w4a8g_linear(P16 + 8, 1, 3584, 128, P16, P16, 4, P16, None, None, None, 0, 0, None) == E_A
+    arr = (ctypes.c_void_p * 2)(P16, P16)
+    mis = (ctypes.c_void_p * 2)(P16, P16 + 4)
+    ns = (ctypes.c_int64 * 2)(4, 4)
+    assert L.w4a8g_linear_grouped(P16, 1, 3584, 128, 0, arr, arr, ns, arr, None, 0, 0, None) == E_S
+    assert L.w4a8g_linear_grouped(P16, 1, 3584, 128, 2, arr, mis, ns, arr, None, 0, 0, None) == E_A
+
+
+def test_group_scale_stride_matches_header():
+    src = open(os.path.join(ROOT, "include", "w4a8.h")).read()
+    assert "#define W4G_SCALE_STRIDE(K, group) ((((K) / (group)) + 3) / 4 * 4)" in src
+    for K, gs, want in [(896, 128, 8), (3584, 128, 28), (18944, 128, 148), (4096, 4096, 4)]:
+        assert w4.w4g_scale_stride(K, gs) == want
+
+
+GROUP_SHAPES = [(1, 896, 512, 128), (1, 3584, 152064, 128), (1, 18944, 3584, 128),
+                (1, 3584, 37888, 64), (2, 3584, 18944, 256), (8, 18944, 3584, 32), (1, 32, 7, 32),
+                (3, 131072, 5, 1024), (1, 4096, 9, 4096), (64, 2048, 100, 512)]
+
+
+@pytest.mark.parametrize("sms", [152, 148, 20, 1])
+@pytest.mark.parametrize("splits", [0, 3, 7, 16])
+def test_group_plan_windows(sms, splits):
+    """Every K piece's scale window covers the groups of its granules, starts
+    and ends on 16-byte words inside the padded scale row, and the slot's
+    scale area holds a whole stage of rows."""
+    try:
+        w4.w4a8_set_tuning(force_splits=splits)
+        for (M, K, N, gs) in GROUP_SHAPES:
+            if splits and splits > K // 32:
+                continue
+            try:
+                p = w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)
+            except w4.W4A8Error:
+                assert splits, (M, K, N, gs)  # only a forced split may leave no plan
+                continue
+            P = p["splits"]
+            assert not splits or P == splits
+            Gt = K // 32
+            Gq = -(-Gt // P)
+            shift = (gs // 32).bit_length() - 1
+            ld = w4.w4g_scale_stride(K, gs)
+            win = p["scale_window"]
+            assert win % 4 == 0 and 4 <= win <= ld
+            for piece in range(P):
+                g0 = piece * Gq
+                gp = min(Gq, Gt - g0)
+                gb = (g0 >> shift) & ~3
+                first, last = g0 >> shift, (g0 + gp - 1) >> shift
+                assert gb <= first and last < gb + win or (gb + win == ld and last < ld)
+                assert gb % 4 == 0 and gb + min(win, ld - gb) <= ld
+            assert p["scale_stage_bytes"] % 16 == 0
+            assert p["scale_stage_bytes"] >= p["rows_per_stage"] * win * 4
+            assert p["smem_bytes"] <= 232448 and 2 <= p["stages"] <= 16
+            assert p["stage_bytes"] >= p["rows_per_stage"] * Gq * 16
+            assert (p["ws_bytes"] > 0) == (P > 1)
+            assert w4.w4a8g_workspace_bytes(M, K, N, gs) == p["ws_bytes"] or sms != 0
+    finally:
+        w4.w4a8_set_tuning(reset=True)

@@ -1,0 +1,281 @@
+"""Group-wise INT4 scales: CUDA path vs the CPU oracle through the C ABI.
+
+Codes, scales and the quantized activation are bit-exact.  The product is
+fp32 arithmetic on exact int32 granule sums, so Y is checked against the
+oracle's binary64 value within the bound the arithmetic gives:
+|Y - Y_ref| <= (K/32 + 4) * 2^-24 * B, B = s_a * sum_g s_g * sum |Xq * q|
+(K/32 granule terms, each folded with one rounding, the partial sums and the
+final multiply by s_a).  With power-of-two scales and integer activations
+every intermediate is exact and Y must equal the oracle bit for bit.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+U = 2.0 ** -24
+
+
+@pytest.fixture(scope="module")
+def w4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bit_weight_quantized_w4a8_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+@pytest.fixture(autouse=True)
+def _reset_tuning(w4):
+    w4.w4a8_set_tuning(reset=True)
+    yield
+    w4.w4a8_set_tuning(reset=True)
+    assert w4.w4a8_device_error() == 0
+
+
+def bits(a):
+    a = np.ascontiguousarray(a)
+    return a.view(np.uint32 if a.dtype.itemsize == 4 else np.uint16)
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def assert_within_bound(Y, Y_ref, B, K):
+    Y = Y.astype(np.float64)
+    bound = (K / 32 + 4) * U * B
+    err = np.abs(Y - Y_ref)
+    bad = np.argwhere(err > bound)
+    assert bad.size == 0, (bad[:5], Y[tuple(bad[0])], Y_ref[tuple(bad[0])], bound[tuple(bad[0])])
+    assert np.isfinite(Y).all()
+
+
+def make_operands(M, K, N, gs, seed):
+    W = synth.normal(seed, (N, K), 0.02)
+    W[1 % N] = 0.0                        # a zero row: every scale 0, outputs 0
+    if K // gs > 1:
+        W[0, gs:2 * gs] = 0.0             # a zero group inside a non-zero row
+    X = synth.activation(seed + 7, M, K, outlier_frac=0.001)
+    if M > 1:
+        X[M - 1] = 0                      # a zero activation row: s_a 0, outputs 0
+    return W, X
+
+
+def check_group(w4, orc, M, K, N, gs, seed, fused=True, flags=0):
+    W, X = make_operands(M, K, N, gs, seed)
+    Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
+    Y_ref, B, Xq_ref, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
+
+    Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
+    assert np.array_equal(Wq.cpu().numpy(), Wq_ref)
+    assert np.array_equal(bits(sg.cpu().numpy()), bits(sg_ref))
+    if fused:
+        Xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
+        sa = torch.empty((M,), dtype=torch.float32, device="cuda")
+        Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs, Xq_out=Xq, sa_out=sa, flags=flags)
+    else:
+        Xq, sa = w4.act_quantize_i8(to_dev(X))
+        Y = w4.w4a8g_gemv(Xq, sa, Wq, sg, gs, flags=flags)
+    torch.cuda.synchronize()
+    assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
+    assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
+    Yh = Y.cpu().numpy()
+    assert_within_bound(Yh, Y_ref, B, K)
+    assert not Yh[:, 1 % N].any()
+    if M > 1:
+        assert not Yh[M - 1].any()
+    return Yh
+
+
+@pytest.mark.parametrize("N,K,gs,seed", [(512, 896, 128, 0), (37, 3584, 128, 1), (5, 32, 32, 2),
+                                         (64, 18944, 128, 3), (9, 4096, 4096, 4), (17, 1024, 64, 5),
+                                         (3, 2048, 256, 6)])
+def test_w4g_quantize(w4, orc, N, K, gs, seed):
+    W = synth.normal(seed, (N, K), 0.02)
+    W[0, :gs] = 0.0
+    W[N - 1, K - 1] *= 30.0
+    Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
+    Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
+    torch.cuda.synchronize()
+    assert np.array_equal(Wq.cpu().numpy(), Wq_ref)
+    assert np.array_equal(bits(sg.cpu().numpy()), bits(sg_ref))
+
+
+def test_w4g_quantize_equals_rowwise_at_group_k(w4):
+    W = to_dev(synth.normal(8, (33, 4096), 0.02))
+    Wq_r, sw = w4.w4_quantize_weights(W)
+    Wq_g, sg = w4.w4g_quantize_weights(W, 4096)
+    torch.cuda.synchronize()
+    assert torch.equal(Wq_r, Wq_g)
+    assert torch.equal(sg[:, 0], sw) and not sg[:, 1:].any()
+
+
+GROUP_SHAPES = [
+    # M, K, N, gs, seed: several tiles, ragged N, every group size, odd group counts
+    (1, 896, 512, 128, 10), (1, 3584, 300, 128, 11), (1, 18944, 129, 128, 12),
+    (2, 3584, 260, 64, 13), (3, 1024, 77, 32, 14), (4, 3584, 1000, 256, 15),
+    (5, 896, 33, 128, 16), (8, 2048, 200, 512, 17), (1, 32, 7, 32, 18), (1, 4096, 64, 4096, 19),
+    (11, 896, 100, 128, 20), (64, 384, 96, 128, 21),
+]
+
+
+@pytest.mark.parametrize("M,K,N,gs,seed", GROUP_SHAPES)
+def test_w4a8g_linear(w4, orc, M, K, N, gs, seed):
+    check_group(w4, orc, M, K, N, gs, seed, fused=True)
+
+
+@pytest.mark.parametrize("M,K,N,gs,seed", GROUP_SHAPES[:6] + GROUP_SHAPES[-2:])
+def test_w4a8g_gemv_unfused(w4, orc, M, K, N, gs, seed):
+    check_group(w4, orc, M, K, N, gs, seed, fused=False)
+
+
+@pytest.mark.parametrize("splits", [2, 3, 5, 16])
+@pytest.mark.parametrize("fused", [True, False])
+def test_w4a8g_split_k(w4, orc, splits, fused):
+    # pieces that start inside a scale word: the windows are widened to whole
+    # 16-byte words and indexed from their remainder
+    w4.w4a8_set_tuning(force_splits=splits)
+    check_group(w4, orc, 2, 3584, 300, 128, 30 + splits, fused=fused)
+    check_group(w4, orc, 1, 18944, 70, 64, 40 + splits, fused=fused)
+
+
+@pytest.mark.parametrize("cl", [1, 4, 32, 256])
+def test_w4a8g_threads_per_row(w4, orc, cl):
+    w4.w4a8_set_tuning(force_threads_per_row=cl)
+    check_group(w4, orc, 1, 3584, 150, 128, 50)
+
+
+def test_w4a8g_two_stage_ring(w4, orc):
+    w4.w4a8_set_tuning(ring_bytes=8192)
+    check_group(w4, orc, 1, 3584, 700, 128, 51)
+
+
+def test_w4a8g_exact_powers_of_two(w4, orc):
+    """Group scales 2^-e (e in 0..3) and integer activations with max 127
+    (s_a = 1): every granule sum, product and partial sum is exact in fp32,
+    so Y equals the oracle's binary64 value bit for bit."""
+    M, K, N, gs = 3, 1024, 300, 64
+    rng = np.random.Generator(np.random.PCG64(77))
+    G = K // gs
+    q = rng.integers(-7, 8, size=(N, G, gs))
+    q[:, :, 0] = 7 * rng.choice([-1, 1], size=(N, G))
+    e = rng.integers(0, 4, size=(N, G, 1))
+    W = (q * 2.0 ** -e).reshape(N, K).astype(np.float32)
+    X = rng.integers(-126, 127, size=(M, K)).astype(np.float16)
+    X[:, 5] = 127
+    Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
+    Y_ref, B, _, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
+    assert np.all(sa_ref == 1.0)
+    for splits in (0, 3):
+        w4.w4a8_set_tuning(force_splits=splits)
+        Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
+        Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs)
+        torch.cuda.synchronize()
+        assert np.array_equal(Y.cpu().numpy().astype(np.float64), Y_ref)
+
+
+def test_w4a8g_deterministic(w4, orc):
+    W, X = make_operands(2, 3584, 5000, 128, 60)
+    Wq, sg = w4.w4g_quantize_weights(to_dev(W), 128)
+    Xd = to_dev(X)
+    Y1 = w4.w4a8g_linear(Xd, Wq, sg, 128).clone()
+    Y2 = w4.w4a8g_linear(Xd, Wq, sg, 128, flags=w4.LAUNCH_PDL)
+    torch.cuda.synchronize()
+    assert torch.equal(Y1, Y2)
+
+
+@pytest.mark.parametrize("M,K,Ns,gs,splits", [
+    (1, 3584, [3584, 512, 512], 128, 0), (1, 3584, [300, 17], 128, 3),
+    (2, 896, [64, 100, 33, 5], 128, 0), (4, 1024, [100, 60], 32, 2),
+])
+def test_w4a8g_linear_grouped(w4, orc, M, K, Ns, gs, splits):
+    w4.w4a8_set_tuning(force_splits=splits)
+    X = synth.activation(70 + len(Ns), M, K, outlier_frac=0.001)
+    Wqs, sgs, refs = [], [], []
+    for g, N in enumerate(Ns):
+        W = synth.normal(80 + g, (N, K), 0.02)
+        Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
+        refs.append(orc.w4a8g_linear(X, Wq_ref, sg_ref, gs))
+        Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
+        Wqs.append(Wq)
+        sgs.append(sg)
+    Ys = w4.w4a8g_linear_grouped(to_dev(X), Wqs, sgs, gs)
+    torch.cuda.synchronize()
+    for Y, (Y_ref, B, _, _) in zip(Ys, refs):
+        assert_within_bound(Y.cpu().numpy(), Y_ref, B, K)
+
+
+def test_w4a8g_rejects(w4):
+    X = torch.zeros((1, 3584), dtype=torch.float16, device="cuda")
+    Wq = torch.zeros((8, 1792), dtype=torch.uint8, device="cuda")
+    sg = torch.zeros((8, 28), dtype=torch.float32, device="cuda")
+    with pytest.raises(w4.W4A8Error):
+        w4.w4a8g_linear(X, Wq, torch.zeros((8, 4), dtype=torch.float32, device="cuda"), 3584)  # not a power of two
+    with pytest.raises(w4.W4A8Error):
+        w4.w4a8g_linear(X, Wq, torch.zeros((8, 4), dtype=torch.float32, device="cuda"), 1024)  # 1024 does not divide 3584
+    with pytest.raises(w4.W4A8Error):
+        w4.w4a8g_linear(X, Wq, torch.zeros((8, 224), dtype=torch.float32, device="cuda"), 16)  # below 32
+    base = torch.zeros(8 * 28 + 4, dtype=torch.float32, device="cuda")
+    Y = torch.empty((1, 8), dtype=torch.float32, device="cuda")
+    st = w4.lib().w4a8g_linear(X.data_ptr(), 1, 3584, 128, Wq.data_ptr(), base.data_ptr() + 4, 8,
+                               Y.data_ptr(), None, None, None, 0, 0, None)
+    assert st == w4._binding.ERR_ALIGN  # scale rows must start on 16-byte boundaries
+
+
+# --------------------------------------------------------------------------
+# full size: the Qwen2-7B-shaped linear set at M = 1 with group size 128,
+# in the launch configuration of the benchmark (grouped q/k/v and gate/up,
+# programmatic dependent launch), checked on sampled rows
+# --------------------------------------------------------------------------
+
+QWEN2_LAUNCHES = [[("q", 3584, 3584), ("k", 3584, 512), ("v", 3584, 512)], [("o", 3584, 3584)],
+                  [("gate", 3584, 18944), ("up", 3584, 18944)], [("down", 18944, 3584)],
+                  [("lm_head", 3584, 152064)]]
+
+
+def sample_rows(N, seed, n=40):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rows = set(rng.choice(N, size=min(n, N), replace=False).tolist()) | {0, N - 1}
+    return np.array(sorted(rows), np.int64)
+
+
+@pytest.mark.parametrize("li", range(len(QWEN2_LAUNCHES)), ids=["qkv", "o", "gate_up", "down", "lm_head"])
+def test_w4a8g_qwen2_fullsize(w4, orc, li):
+    gs = 128
+    mats = QWEN2_LAUNCHES[li]
+    K = mats[0][1]
+    seed0 = 2000 + 10 * li
+    X = synth.activation(seed0 + 500, 1, K, outlier_frac=0.001)
+    Wqs, sgs, rows_all = [], [], []
+    for g, (_, _, N) in enumerate(mats):
+        W = synth.normal_gpu(seed0 + g, (N, K), 0.02)
+        Wq, sg = w4.w4g_quantize_weights(W, gs)
+        del W
+        Wqs.append(Wq)
+        sgs.append(sg)
+    if len(mats) == 1:
+        Ys = [w4.w4a8g_linear(to_dev(X), Wqs[0], sgs[0], gs, flags=w4.LAUNCH_PDL)]
+    else:
+        Ys = w4.w4a8g_linear_grouped(to_dev(X), Wqs, sgs, gs, flags=w4.LAUNCH_PDL)
+    torch.cuda.synchronize()
+    for g, (_, _, N) in enumerate(mats):
+        rows = sample_rows(N, seed0 + g)
+        W_rows = synth.weight_rows(seed0 + g, N, K, rows)
+        Wq_ref, sg_ref = orc.w4g_quantize(W_rows, gs)
+        idx = torch.from_numpy(rows).cuda()
+        assert np.array_equal(Wqs[g][idx].cpu().numpy(), Wq_ref)
+        assert np.array_equal(bits(sgs[g][idx].cpu().numpy()), bits(sg_ref))
+        Y_ref, B, _, _ = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
+        assert_within_bound(Ys[g].cpu().numpy()[:, rows], Y_ref, B, K)
