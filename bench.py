@@ -92,6 +92,8 @@ def parse():
     ap.add_argument("--only", choices=[l[0] for l in LAUNCHES], default=None,
                     help="profiling aid: time one launch kind alone, eagerly, without PDL "
                          "(not the headline metric)")
+    ap.add_argument("--group", type=int, default=0,
+                    help="with --only: group-wise INT4 scales of this group size")
     return ap.parse_args()
 
 
@@ -212,7 +214,7 @@ def measured_peak():
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_weight_quantized_w4a8_gb300", "csrc")
-    for name in ("gemv.cu", "plan.h", "ptx.cuh"):
+    for name in ("gemv_kernel.cuh", "gemv.cu", "gemv_group.cu", "plan.h", "ptx.cuh", "actq.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -733,23 +735,29 @@ def run_only(args, lname):
     K = LINEARS[idx[0]][1]
     X = torch.from_numpy(synth.activation(activation_seed(members[0]), 1, K,
                                           outlier_frac=OUTLIER_FRAC)).to(dev)
+    gs = args.group
     copies = []
     for c in range(2):
         ws_, ss_ = [], []
         for i in idx:
             W = synth.normal_gpu(WEIGHT_SEED0 + i, (LINEARS[i][2], K), 0.02, device=dev)
-            Wq, sw = w4.w4_quantize_weights(W)
+            Wq, sw = w4.w4g_quantize_weights(W, gs) if gs else w4.w4_quantize_weights(W)
             del W
             ws_.append(Wq)
             ss_.append(sw)
         copies.append((ws_, ss_))
     Ys = [torch.empty((1, LINEARS[i][2]), dtype=torch.float32, device=dev) for i in idx]
-    wsb = torch.zeros(max(w4.w4a8_workspace_bytes(1, K, sum(LINEARS[i][2] for i in idx)), 4096),
-                      dtype=torch.uint8, device=dev)
+    N_all = sum(LINEARS[i][2] for i in idx)
+    nws = w4.w4a8g_workspace_bytes(1, K, N_all, gs) if gs else w4.w4a8_workspace_bytes(1, K, N_all)
+    wsb = torch.zeros(max(nws, 4096), dtype=torch.uint8, device=dev)
 
     def one(k):
         Wqs, sws = copies[k % 2]
-        if len(idx) == 1:
+        if gs and len(idx) == 1:
+            w4.w4a8g_linear(X, Wqs[0], sws[0], gs, Y=Ys[0], ws=wsb)
+        elif gs:
+            w4.w4a8g_linear_grouped(X, Wqs, sws, gs, Ys=Ys, ws=wsb)
+        elif len(idx) == 1:
             w4.w4a8_linear(X, Wqs[0], sws[0], Y=Ys[0], ws=wsb)
         else:
             w4.w4a8_linear_grouped(X, Wqs, sws, Ys=Ys, ws=wsb)
@@ -764,8 +772,11 @@ def run_only(args, lname):
     e1.record()
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) / args.steps * 1e3
-    nbytes = sum(weight_bytes(K, LINEARS[i][2]) for i in idx)
-    print(json.dumps({"only": lname, "members": list(members), "steps": args.steps,
+    if gs:
+        nbytes = sum(LINEARS[i][2] * (K // 2 + 4 * w4.w4g_scale_stride(K, gs)) for i in idx)
+    else:
+        nbytes = sum(weight_bytes(K, LINEARS[i][2]) for i in idx)
+    print(json.dumps({"only": lname, "members": list(members), "group": gs, "steps": args.steps,
                       "us_per_launch": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                       "note": "eager launches, host launch gaps included; profiling aid"}),
           flush=True)
