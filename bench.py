@@ -89,7 +89,8 @@ def parse():
                     help="skip the 28-layer step, the skinny-batch sweep and the W8A16 set")
     ap.add_argument("--min-busy-s", type=float, default=0.6,
                     help="keep the GPU busy at least this long before timing (clock samples)")
-    ap.add_argument("--only", choices=[l[0] for l in LAUNCHES], default=None,
+    ap.add_argument("--only", choices=[l[0] for l in LAUNCHES] + ["w8_" + l[0] for l in W8A16_SET],
+                    default=None,
                     help="profiling aid: time one launch kind alone, eagerly, without PDL "
                          "(not the headline metric)")
     ap.add_argument("--group", type=int, default=0,
@@ -729,6 +730,8 @@ def run_only(args, lname):
     w4.build()
     w4.w4a8_set_tuning(reset=True)
     dev = torch.device("cuda", torch.cuda.current_device())
+    if lname.startswith("w8_"):
+        return run_only_w8(args, lname[3:], torch, synth, w4, dev)
     members = dict(LAUNCHES)[lname]
     names = [l[0] for l in LINEARS]
     idx = [names.index(n) for n in members]
@@ -780,6 +783,38 @@ def run_only(args, lname):
                       "us_per_launch": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                       "note": "eager launches, host launch gaps included; profiling aid"}),
           flush=True)
+
+
+def run_only_w8(args, name, torch, synth, w4, dev):
+    """Profiling aid for one W8A16 GEMV of the ChatGLM2-6B-shaped set."""
+    j = [l[0] for l in W8A16_SET].index(name)
+    _, K, N = W8A16_SET[j]
+    copies = []
+    for c in range(2):
+        W = synth.normal_gpu(2000 + j, (N, K), 0.02, device=dev)
+        copies.append(w4.w8_quantize_weights(W))
+        del W
+    X = torch.from_numpy(synth.activation(2500 + j, 1, K)).to(dev)
+    Y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    wsb = torch.zeros(max(w4.w8a16_workspace_bytes(1, K, N), 4096), dtype=torch.uint8, device=dev)
+
+    def one(k):
+        Wq8, sw16 = copies[k % 2]
+        w4.w8a16_gemv(X, Wq8, sw16, Y=Y, ws=wsb)
+
+    for k in range(args.warmup):
+        one(k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(args.steps):
+        one(k)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / args.steps * 1e3
+    print(json.dumps({"only": "w8_" + name, "steps": args.steps, "us_per_launch": round(us, 2),
+                      "GBps": round((N * K + 2 * N) / us / 1e3, 1),
+                      "note": "eager launches, host launch gaps included; profiling aid"}), flush=True)
 
 
 def main():

@@ -83,9 +83,12 @@ cudaError_t launch_w8a16(const GemvPlan& pl, const uint16_t* X, int M, int64_t K
     a.N = (int)N;
     a.pl = pl;
     switch (pl.MT) {
-        case 1: return launch_one<false, 1, 4, false>(a, flags, stream);
-        case 2: return launch_one<false, 2, 2, false>(a, flags, stream);
-        case 4: return launch_one<false, 4, 1, false>(a, flags, stream);
+        case 1:  // exact column counts for K = 4096 (8 at 32 threads per row) and 13696 (7 at 128)
+            if (pl.S == 8) return launch_one<false, 1, 8, false, true>(a, flags, stream);
+            if (pl.S == 7) return launch_one<false, 1, 7, false, true>(a, flags, stream);
+            return launch_one<false, 1, 8, false>(a, flags, stream);
+        case 2: return launch_one<false, 2, 4, false>(a, flags, stream);
+        case 4: return launch_one<false, 4, 2, false>(a, flags, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -283,6 +283,20 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                 cp_async_4(smem_u32(sw_s + r), static_cast<const float*>(a.wscale[sg]) + (n - a.off[sg]));
             }
         cp_async_mbar_arrive(smem_u32(sw_bar));
+    } else if constexpr (!kW4) {
+        // binary16 scales (one segment): the 4-byte words covering rows
+        // row0 & ~1 ... row0 + nrows - 1; a word past the last scale reads
+        // only its first half
+        if (pl.P == 1) {
+            const uint16_t* s16 = static_cast<const uint16_t*>(a.wscale[0]);
+            const int64_t base = row0 & ~(int64_t)1;
+            const int words = (int)((row0 + nrows - base + 1) >> 1);
+            for (int w = tid; w < words; w += kConsumers) {
+                const int64_t e = base + 2 * w;
+                cp_async_4_partial(smem_u32(sw_s + w), s16 + e, e + 1 < N ? 4u : 2u);
+            }
+        }
+        cp_async_mbar_arrive(smem_u32(sw_bar));
     } else {
         mbar_arrive(smem_u32(sw_bar));
     }
@@ -398,6 +412,19 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
             }
         }
     } else {
+        if constexpr (!kW4) {
+            // W8: this piece of every activation row, copied once per CTA
+            if (pl.x_bytes > 0) {
+                uint4* x_s = reinterpret_cast<uint4*>(smem + pl.off_x);
+                const int nvp = gp * 2;  // 16-byte vectors per row piece
+                for (int v = tid; v < M * nvp; v += kConsumers) {
+                    const int m = v / nvp, u = v - m * nvp;
+                    cp_async_16(smem_u32(x_s + v), a.X + (int64_t)m * K + (int64_t)g0 * 16 + 8 * u);
+                }
+                cp_async_wait_all();
+                named_bar_sync(1, kConsumers);
+            }
+        }
         #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if constexpr (kW4) sa_r[m] = (m < M) ? a.sa[m] : 0.f;
@@ -410,9 +437,12 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                         permute_act(ld_global_nc_v4(src), ld_global_nc_v4(src + 16), act[m][s]);
                     } else {
                         // the 16 binary16 values of the granule, kept as pairs
-                        const __half* src = a.X + (int64_t)m * K + (int64_t)(g0 + c) * 16;
-                        const uint4 h0 = ld_global_nc_v4(src);
-                        const uint4 h1 = ld_global_nc_v4(src + 8);
+                        // (from the staged piece when there is one)
+                        const uint4* src = pl.x_bytes > 0
+                            ? reinterpret_cast<const uint4*>(smem + pl.off_x) + (m * gp + c) * 2
+                            : reinterpret_cast<const uint4*>(a.X + (int64_t)m * K + (int64_t)(g0 + c) * 16);
+                        const uint4 h0 = src[0];
+                        const uint4 h1 = src[1];
                         act[m][s][0] = h0.x; act[m][s][1] = h0.y; act[m][s][2] = h0.z; act[m][s][3] = h0.w;
                         act[m][s][4] = h1.x; act[m][s][5] = h1.y; act[m][s][6] = h1.z; act[m][s][7] = h1.w;
                     }
@@ -424,12 +454,6 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
         }
     }
 
-    if constexpr (!kW4) {
-        if (pl.P == 1)
-            for (int r = tid; r < nrows; r += kConsumers)
-                sw_s[r] = __half2float(static_cast<const __half*>(a.wscale[0])[row0 + r]);
-        named_bar_sync(1, kConsumers);  // scale cache visible to every thread
-    }
 
     // W4: the low nibbles enter the dot product biased by +8 (n ^ 8 = q + 8),
     // so each row's sum carries 8 * (sum of the even-k codes) too much: per
@@ -620,7 +644,9 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                     #pragma unroll
                     for (int m = 0; m < MT; ++m) rbuf[(warp * kBatch + d) * MT + m] = part[d][m];
             }
-            named_bar_sync(2, kConsumers);
+            // only the wpr warps of this row-piece meet (barrier 2 + i; at
+            // most 4 row-pieces when a row-piece spans warps)
+            named_bar_sync(2 + i, Cl);
             if (j == 0) {
                 #pragma unroll
                 for (int d = 0; d < kBatch; ++d)
@@ -639,7 +665,9 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                 if (sb + d < nstages && r < nrows) {
                     const int64_t n = row0 + r;
                     if (pl.P == 1) {
-                        const float swv = kG ? 0.f : sw_s[r];
+                        const float swv = kG ? 0.f
+                                        : kW4 ? sw_s[r]
+                                              : __half2float(reinterpret_cast<const __half*>(sw_s)[r + (row0 & 1)]);
                         const int sg = segment_of(a, n);
                         const int64_t Ng = a.off[sg + 1] - a.off[sg];
                         float* Yp = a.Yg[sg] + (n - a.off[sg]);

@@ -103,7 +103,7 @@ inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int
     if (gshift >= 0 && (!w4 || gld <= 0 || gld % 4)) return false;
     GemvPlan pl = {};
     pl.MT = mt_of(M);
-    pl.smax = (w4 ? 8 : 4) / pl.MT;
+    pl.smax = 8 / pl.MT;  // 8 activation registers per granule and row (W4 codes, W8 binary16 pairs)
     if (pl.smax < 1) return false;
     const int kgran = w4 ? 32 : 16;
     if (K % kgran) return false;
@@ -175,13 +175,16 @@ inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int
     if (NS < 2) NS = 2;
     if (NS > 16) NS = 16;
 
-    const int sw_bytes = (pl.P == 1 && gshift < 0) ? round_up(pl.rows_max * 4, 16) : 0;
+    const int sw_bytes = (pl.P == 1 && gshift < 0) ? round_up(pl.rows_max * 4 + 8, 16) : 0;
     if (gshift >= 0) {
         pl.gwin = group_window_max(pl, gshift, gld);
         pl.gstage = round_up(pl.Rl * pl.gwin * 4, 128);
     }
     const int act_bytes = (w4 && fused) ? round_up(pl.MT * pl.Gq * 32, 128) : 0;
-    pl.x_bytes = (w4 && fused && pl.MT == 1 && 2 * K <= kMaxXStage) ? (int)(2 * K) : 0;
+    // the K piece of the activation rows a W8 CTA reads, staged once per CTA
+    const int w8_x = w4 ? 0 : M * pl.Gq * kGranBytes * 2;
+    pl.x_bytes = (w4 && fused && pl.MT == 1 && 2 * K <= kMaxXStage) ? (int)(2 * K)
+               : (!w4 && w8_x <= kMaxXStage) ? w8_x : 0;
     const int red_bytes = 2 * kConsumerWarps * 4 * pl.MT * 4;  // [2][warps][batch 4][MT]
     const int max_bytes = kConsumerWarps * pl.MT * 4;
     // Shrink the ring until the CTA fits beside its sibling(s) on an SM; if

@@ -130,7 +130,7 @@ def test_plan_invariants(sms, w8):
         Cl, S = p["threads_per_row"], p["cols_per_thread"]
         assert Cl & (Cl - 1) == 0 and Cl * S >= Gq and Cl * (S - 1) < Gq
         mt = 1 if M <= 1 else 2 if M <= 2 else 4 if M <= 4 else 8
-        assert S <= ((4 if w8 else 8) // mt)
+        assert S <= 8 // mt
         assert p["rows_per_stage"] * Cl == 256
         assert p["grid"] == p["ctas_per_split"] * P
         assert p["ctas_per_split"] <= N
