@@ -74,6 +74,8 @@ class Oracle:
             "oracle_w4g_quantize": [_p, _i64, _i64, _i64, _p, _p],
             "oracle_w4a8g_ref": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p],
             "oracle_w4a8g_linear": [_p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _p, _p],
+            "oracle_isx_lut": [ctypes.c_int, ctypes.c_double, _p],
+            "oracle_index_softmax": [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p],
         }.items():
             f = getattr(lib, name)
             f.restype = ctypes.c_int
@@ -82,6 +84,8 @@ class Oracle:
         lib.oracle_w4a8_rescale.argtypes = [_p, _p, _p, _i64, _i64, _p]
         lib.oracle_w4g_scale_stride.restype = _i64
         lib.oracle_w4g_scale_stride.argtypes = [_i64, _i64]
+        lib.oracle_isx_c_int.restype = _i64
+        lib.oracle_isx_c_int.argtypes = [ctypes.c_double, _i64, ctypes.c_float, ctypes.c_float]
         lib.oracle_w8a16_ref.restype = None
         lib.oracle_w8a16_ref.argtypes = [_p, _i64, _i64, _p, _p, _i64, _p]
 
@@ -210,6 +214,28 @@ class Oracle:
         if st != OK:
             raise ValueError("oracle_w4a8g_linear status %d" % st)
         return Y, B, Xq, sa
+
+    # -- IndexSoftmax -----------------------------------------------------
+    def isx_lut(self, b: int = 5, c: float = 6.6) -> np.ndarray:
+        lut = np.empty(1 << b, np.uint8)
+        st = self._lib.oracle_isx_lut(b, c, _ptr(lut))
+        if st != OK:
+            raise ValueError("oracle_isx_lut status %d" % st)
+        return lut
+
+    def isx_c_int(self, c: float, d: int, s_q: float, s_k: float) -> int:
+        return int(self._lib.oracle_isx_c_int(c, d, float(np.float32(s_q)), float(np.float32(s_k))))
+
+    def index_softmax(self, A: np.ndarray, c_int: int, b: int = 5, lut=None) -> np.ndarray:
+        """int32 logits [rows][cols] -> UINT8 probabilities (same shape)."""
+        A = np.ascontiguousarray(A, dtype=np.int32)
+        rows, cols = A.shape
+        lut = self.isx_lut(b) if lut is None else np.ascontiguousarray(lut, dtype=np.uint8)
+        P = np.empty((rows, cols), np.uint8)
+        st = self._lib.oracle_index_softmax(_ptr(A), rows, cols, c_int, b, _ptr(lut), _ptr(P))
+        if st != OK:
+            raise ValueError("oracle_index_softmax status %d" % st)
+        return P
 
     # -- W8A16 ------------------------------------------------------------
     def w8_quantize(self, W: np.ndarray):

@@ -1,6 +1,6 @@
 /*
  * oracle.c -- plain, single-threaded CPU definition of the weight-quantized
- * decode linear layer (W4A8 and W8A16).
+ * decode linear layer (W4A8 and W8A16) and of the IndexSoftmax operator.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
  * calls this file: only the tests, the smoke check and the CPU-baseline leg
@@ -18,6 +18,10 @@
  *  [P2] "TPU-MLIR W8A16 for ChatGLM2-6B", section 2 (per-channel INT8
  *       weights) and section 4 (the five steps: load, cast INT8 to F16,
  *       multiply by the scale, matrix multiply with the activation, store).
+ *  [P3] "【MLSys 2026】IntAttention：全整数注意力流水线，边缘推理的高效部署",
+ *       section 基准/方法设计 (IndexSoftmax: integer clipping of the row
+ *       distances, a 2^b-entry UINT8 exponent table, integer normalization
+ *       to UINT8 probabilities).
  * Where the pages leave a step open, the reading used is stated at the
  * function (symmetric codes, divisors 7 and 127, round half away from zero,
  * true division, low-nibble-first two's-complement packing, fp32 rescale in
@@ -380,4 +384,71 @@ int oracle_w4a8g_linear(const uint16_t* X, int64_t M, int64_t K, int64_t gs, con
     int st = oracle_act_quantize(X, M, K, Xq_out, sa_out);
     if (st != ORACLE_OK) return st;
     return oracle_w4a8g_ref(Xq_out, sa_out, M, K, gs, Wq, sg, N, Y, B);
+}
+
+/* ------------------------------------------------------------------------ */
+/* s1-s3: IndexSoftmax  [P3 "IntAttention: 全整数注意力流水线", section     */
+/*        基准/方法设计: IndexSoftmax 的三个机制]                            */
+/* ------------------------------------------------------------------------ */
+/* Readings where the page leaves a step open: the rounding bracket of every
+   formula is round to nearest with halves away from zero (all operands are
+   non-negative, so halves go up); LUT entries and c_int are computed in
+   binary64 with the C library's exp and sqrt; a row whose c_int is 0 clips
+   every distance to 0 and takes index 0 everywhere. */
+
+/* Mechanism 2: the 2^b-entry exponent table quantized to UINT8,
+   LUT[i] = round(255 * exp(-c * i / (2^b - 1))), the last entry forced to 0. */
+int oracle_isx_lut(int b, double c, uint8_t* lut)
+{
+    if (b < 1 || b > 8 || !(c > 0.0)) return ORACLE_ERR_SHAPE;
+    int n = 1 << b;
+    for (int i = 0; i < n - 1; ++i)
+        lut[i] = (uint8_t)round(255.0 * exp(-c * (double)i / (double)(n - 1)));
+    lut[n - 1] = 0;
+    return ORACLE_OK;
+}
+
+/* Mechanism 1's clipping threshold in integer logit units:
+   c_int = round(c * sqrt(d) / (s_Q * s_K)). */
+int64_t oracle_isx_c_int(double c, int64_t d, float s_q, float s_k)
+{
+    return (int64_t)llround(c * sqrt((double)d) / ((double)s_q * (double)s_k));
+}
+
+/* IndexSoftmax of the int32 logits A[rows][cols] into UINT8 probabilities
+   P[rows][cols], per row:
+     delta  = rowMax(A) - A                        (mechanism 1)
+     delta' = min(delta, c_int)
+     idx    = round(delta' * (2^b - 1) / c_int)    (mechanism 2)
+     E      = LUT[idx]
+     P      = round(255 * E / rowSum(E))           (mechanism 3)
+   All arithmetic is exact integer arithmetic (int64). */
+int oracle_index_softmax(const int32_t* A, int64_t rows, int64_t cols, int64_t c_int, int b,
+                         const uint8_t* lut, uint8_t* P)
+{
+    if (rows < 0 || cols < 1 || c_int < 0 || b < 1 || b > 8) return ORACLE_ERR_SHAPE;
+    int64_t top = (1 << b) - 1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const int32_t* a = A + r * cols;
+        int32_t mx = a[0];
+        for (int64_t k = 1; k < cols; ++k)
+            if (a[k] > mx) mx = a[k];
+        int64_t sum = 0;
+        for (int64_t k = 0; k < cols; ++k) {
+            int64_t delta = (int64_t)mx - (int64_t)a[k];
+            int64_t clipped = delta < c_int ? delta : c_int;
+            /* round(clipped * top / c_int), halves up: floor((2 x top + c) / 2c) */
+            int64_t idx = c_int > 0 ? (2 * clipped * top + c_int) / (2 * c_int) : 0;
+            sum += lut[idx];
+        }
+        for (int64_t k = 0; k < cols; ++k) {
+            int64_t delta = (int64_t)mx - (int64_t)a[k];
+            int64_t clipped = delta < c_int ? delta : c_int;
+            int64_t idx = c_int > 0 ? (2 * clipped * top + c_int) / (2 * c_int) : 0;
+            int64_t e = lut[idx];
+            /* round(255 e / sum), halves up; sum >= LUT[0] = 255 > 0 */
+            P[r * cols + k] = (uint8_t)((2 * 255 * e + sum) / (2 * sum));
+        }
+    }
+    return ORACLE_OK;
 }

@@ -483,6 +483,87 @@ def pin_w4a8g_error_bound(o):
 
 
 # --------------------------------------------------------------------------
+# s1-s3: IndexSoftmax
+# --------------------------------------------------------------------------
+
+def _decimal_lut(b, c):
+    """round(255 * exp(-c i / (2^b - 1))) with 50-digit decimal arithmetic
+    (c taken exactly as its binary64 value), last entry 0."""
+    import decimal
+    ctx = decimal.Context(prec=50)
+    n = 1 << b
+    out = []
+    for i in range(n - 1):
+        x = ctx.divide(ctx.multiply(decimal.Decimal(-c), i), n - 1)
+        v = ctx.multiply(255, ctx.exp(x))
+        out.append(int(v.quantize(decimal.Decimal(1), rounding=decimal.ROUND_HALF_UP)))
+    return out + [0]
+
+
+def pin_isx_lut(o):
+    """The UINT8 exponent table against 50-digit decimal exp, for the page's
+    (b, c) = (5, 6.6) and other points of its stable range."""
+    assert list(o.isx_lut(5, 6.6)) == _decimal_lut(5, 6.6)
+    for b, c in [(3, 5.5), (4, 7.7), (6, 6.6), (8, 5.5), (5, 4.0)]:
+        assert list(o.isx_lut(b, c)) == _decimal_lut(b, c), (b, c)
+    lut = o.isx_lut(5, 6.6)
+    assert lut[0] == 255 and lut[31] == 0 and len(lut) == 32
+    assert all(int(lut[i]) >= int(lut[i + 1]) for i in range(31))
+
+
+def pin_isx_c_int(o):
+    """c_int = round(c sqrt(d) / (s_Q s_K)) with halves away from zero."""
+    import decimal
+    assert o.isx_c_int(2.5, 1, 1.0, 1.0) == 3          # a half rounds up
+    assert o.isx_c_int(3.5, 4, 1.0, 1.0) == 7          # sqrt(4) = 2 exactly
+    assert o.isx_c_int(6.6, 128, 2.0 ** -5, 2.0 ** -5) == int(
+        (decimal.Decimal(6.6) * decimal.Decimal(128).sqrt() * 1024).quantize(
+            decimal.Decimal(1), rounding=decimal.ROUND_HALF_UP))
+    s = float(np.float32(4 / 127))
+    want = decimal.Decimal(6.6) * decimal.Decimal(128).sqrt() / (decimal.Decimal(s) * decimal.Decimal(s))
+    assert o.isx_c_int(6.6, 128, s, s) == int(want.quantize(decimal.Decimal(1),
+                                                             rounding=decimal.ROUND_HALF_UP))
+
+
+def pin_isx_golden(o):
+    for c in read_cases("index_softmax_closed_forms.txt"):
+        row = np.array([int(v) for v in c["row"]], np.int64).astype(np.int32)[None, :]
+        P = o.index_softmax(row, int(c["c_int"][0]))
+        want = np.array([int(v) for v in c["p"]], np.uint8)
+        assert np.array_equal(P[0], want), (c["name"], P[0], want)
+
+
+def pin_isx_invariants(o):
+    """Seeded int32 logits for d = 128 and per-tensor scales 4/127, spread
+    like trained attention (dequantized logits with standard deviation 4):
+    the row max gets the largest probability, probabilities do not increase
+    with the distance from the max, every distance at or past c_int gets 0,
+    the row sum is within cols/2 of 255, and P/255 keeps the direction of the
+    fp64 softmax of the dequantized logits (cosine > 0.99; flatter rows lose
+    more to the 8-bit probabilities, which the page names as its limit)."""
+    s = float(np.float32(4 / 127))
+    c_int = o.isx_c_int(6.6, 128, s, s)
+    rows, cols = 16, 1000
+    A = np.round(synth.normal(91, (rows, cols), 1.0) * (4.0 * math.sqrt(128) / (s * s))).astype(np.int32)
+    A[3, :] = A[3, 0]                                    # a constant row: 255/1000 rounds to 0
+    P = o.index_softmax(A, c_int).astype(np.int64)
+    delta = A.max(1, keepdims=True).astype(np.int64) - A
+    for r in range(rows):
+        order = np.argsort(delta[r], kind="stable")
+        assert np.all(np.diff(P[r][order]) <= 0)
+        assert P[r][np.argmax(A[r])] == P[r].max()
+        assert not P[r][delta[r] >= c_int].any()
+        assert abs(int(P[r].sum()) - 255) <= cols // 2
+    x = A.astype(np.float64) * s * s / math.sqrt(128)
+    e = np.exp(x - x.max(1, keepdims=True))
+    ref = e / e.sum(1, keepdims=True)
+    keep = np.arange(rows) != 3
+    cos = (P * ref).sum(1)[keep] / np.sqrt((P.astype(np.float64) ** 2).sum(1) * (ref ** 2).sum(1))[keep]
+    assert np.all(cos > 0.99), cos
+    assert not P[3].any()
+
+
+# --------------------------------------------------------------------------
 # b1/b2: W8A16
 # --------------------------------------------------------------------------
 

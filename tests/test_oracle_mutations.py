@@ -54,6 +54,15 @@ MUTATIONS = [
     ("w4g_ref_group_bytes", "for (int64_t j = g * (gs / 2); j < (g + 1) * (gs / 2); ++j)",
      "for (int64_t j = 0; j < gs / 2; ++j)"),
     ("w4g_ref_dropped_high", "acc += p0 + p1;", "acc += p0;"),
+    ("isx_lut_scale_254", "(uint8_t)round(255.0 * exp(", "(uint8_t)round(254.0 * exp("),
+    ("isx_lut_step_2b", "exp(-c * (double)i / (double)(n - 1))", "exp(-c * (double)i / (double)n)"),
+    ("isx_lut_last_not_zero", "lut[n - 1] = 0;", "lut[n - 1] = (uint8_t)round(255.0 * exp(-c));"),
+    ("isx_c_int_without_sqrt", "c * sqrt((double)d) /", "c * (double)d /"),
+    ("isx_c_int_truncated", "(int64_t)llround(c * sqrt", "(int64_t)(c * sqrt"),
+    ("isx_idx_floor", "(2 * clipped * top + c_int) / (2 * c_int)", "(clipped * top) / c_int"),
+    ("isx_sum_counts", "sum += lut[idx];", "sum += 255;"),
+    ("isx_p_floor", "(2 * 255 * e + sum) / (2 * sum)", "(255 * e) / sum"),
+    ("isx_p_scale_256", "(2 * 255 * e + sum) / (2 * sum)", "(2 * 256 * e + sum) / (2 * sum)"),
 ]
 
 
