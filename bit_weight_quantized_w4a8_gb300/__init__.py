@@ -1,5 +1,5 @@
 """GB300 (sm_103a) weight-quantized decode linear: W4A8 (row-wise or
-group-wise INT4 scales) and W8A16.
+group-wise INT4 scales) and W8A16; and the IndexSoftmax integer softmax.
 
 The compute lives in libw4a8.so (CUDA kernels behind the C ABI of
 include/w4a8.h); this package is its thin Python binding.
@@ -11,5 +11,6 @@ from ._binding import (  # noqa: F401
     w8_quantize_weights, w8a16_gemv, w8a16_workspace_bytes,
     GROUP_PLAN_FIELDS, w4g_quantize_weights, w4g_scale_stride, w4a8g_gemv, w4a8g_linear,
     w4a8g_linear_grouped, w4a8g_plan_info, w4a8g_workspace_bytes,
+    ISX_DEFAULT_B, ISX_DEFAULT_C, index_softmax_c_int, index_softmax_lut, index_softmax_u8,
 )
 from .build import build  # noqa: F401

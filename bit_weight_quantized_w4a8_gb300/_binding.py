@@ -29,6 +29,7 @@ EXPORTS = [
     "w4a8_linear_noalloc", "w4a8_linear_grouped",
     "w4g_quantize_weights", "w4a8g_workspace_bytes", "w4a8g_gemv", "w4a8g_linear",
     "w4a8g_linear_grouped", "w4a8g_plan_info",
+    "index_softmax_lut", "index_softmax_c_int", "index_softmax_u8",
 ]
 
 
@@ -72,6 +73,9 @@ _SIGS = {
                                             _p, ctypes.c_size_t, _u, _p]),
     "w4a8g_plan_info": (ctypes.c_int, [_i64, _i64, _i64, _i64, ctypes.c_int,
                                        ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
+    "index_softmax_lut": (ctypes.c_int, [ctypes.c_int, ctypes.c_double, _p]),
+    "index_softmax_c_int": (_i64, [ctypes.c_double, _i64, ctypes.c_float, ctypes.c_float]),
+    "index_softmax_u8": (ctypes.c_int, [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _p]),
 }
 
 _lib = None
@@ -390,6 +394,41 @@ def w4a8g_linear_grouped(X, Wqs, sgs, group: int, Ys=None, ws=None, flags: int =
                                       0 if ws is None else ws.numel() * ws.element_size(), flags,
                                       _stream(X)))
     return Ys
+
+
+# -- IndexSoftmax -------------------------------------------------------------
+
+ISX_DEFAULT_B = 5
+ISX_DEFAULT_C = 6.6
+
+
+def index_softmax_lut(b: int = ISX_DEFAULT_B, c: float = ISX_DEFAULT_C) -> bytes:
+    """The 2^b-entry UINT8 exponent table (computed on the host)."""
+    buf = (ctypes.c_uint8 * (1 << b))() if 1 <= b <= 8 else (ctypes.c_uint8 * 1)()
+    _check(lib().index_softmax_lut(b, c, ctypes.cast(buf, ctypes.c_void_p)))
+    return bytes(buf)
+
+
+def index_softmax_c_int(c: float, d: int, s_q: float, s_k: float) -> int:
+    v = int(lib().index_softmax_c_int(c, d, s_q, s_k))
+    if v < 0:
+        raise W4A8Error(ERR_SHAPE, "index_softmax_c_int: arguments out of range")
+    return v
+
+
+def index_softmax_u8(A, c_int: int, b: int = ISX_DEFAULT_B, lut: bytes = None, P=None):
+    """int32 logits [rows][cols] (CUDA) -> UINT8 probabilities; returns P."""
+    _want(A, torch.int32, "A")
+    rows, cols = A.shape
+    P = torch.empty((rows, cols), dtype=torch.uint8, device=A.device) if P is None else P
+    _want(P, torch.uint8, "P", (rows, cols))
+    lut = index_softmax_lut(b) if lut is None else bytes(lut)
+    if len(lut) != (1 << b):
+        raise ValueError("lut must have 2^b entries")
+    lut_buf = (ctypes.c_uint8 * len(lut)).from_buffer_copy(lut)
+    _check(lib().index_softmax_u8(_ptr(A), rows, cols, c_int, b,
+                                  ctypes.cast(lut_buf, ctypes.c_void_p), _ptr(P), _stream(A)))
+    return P
 
 
 def w4a8_last_error() -> str:

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdint>
@@ -445,6 +446,40 @@ int w8a16_gemv(const uint16_t* X, int64_t M, int64_t K, const int8_t* Wq8, const
         if (e != cudaSuccess) return cuda_fail(e, "w8a16_gemv launch");
     }
     return ok();
+}
+
+int index_softmax_lut(int b, double c, uint8_t* lut) {
+    if (!lut) return fail(W4A8_ERR_NULL, "index_softmax_lut: NULL pointer");
+    if (b < 1 || b > 8 || !(c > 0.0) || !(c < 1e300))
+        return fail(W4A8_ERR_SHAPE, "index_softmax_lut: need 1 <= b <= 8 and c > 0");
+    w4a8::isx_build_lut(b, c, lut);
+    return ok();
+}
+
+int64_t index_softmax_c_int(double c, int64_t d, float s_q, float s_k) {
+    if (!(c > 0.0) || d < 1 || !(s_q > 0.f) || !(s_k > 0.f)) return -1;
+    const double v = c * std::sqrt((double)d) / ((double)s_q * (double)s_k);
+    if (!(v < 2147483647.0)) return -1;
+    return w4a8::isx_c_int(c, d, s_q, s_k);
+}
+
+int index_softmax_u8(const int32_t* A, int64_t rows, int64_t cols, int64_t c_int, int b,
+                     const uint8_t* lut, uint8_t* P, void* stream) {
+    if (!A || !lut || !P) return fail(W4A8_ERR_NULL, "index_softmax_u8: NULL pointer");
+    if (rows < 1 || rows > 0x7FFFFFFF)
+        return fail(W4A8_ERR_SHAPE, "rows=%lld outside [1, 2^31-1]", (long long)rows);
+    if (cols < 1 || cols > ISX_MAX_COLS)
+        return fail(W4A8_ERR_SHAPE, "cols=%lld outside [1, %d]", (long long)cols, ISX_MAX_COLS);
+    if (c_int < 0 || c_int > 0x7FFFFFFF)
+        return fail(W4A8_ERR_SHAPE, "c_int=%lld outside [0, 2^31-1]", (long long)c_int);
+    if (b < 1 || b > 8) return fail(W4A8_ERR_SHAPE, "b=%d outside [1, 8]", b);
+    if (lut[0] < 1) return fail(W4A8_ERR_SHAPE, "lut[0] must be at least 1 (row sums stay positive)");
+    if (!aligned(A, 4)) return fail(W4A8_ERR_ALIGN, "index_softmax_u8: A needs 4-byte alignment");
+    uint32_t thr[w4a8::kIsxMaxEntries + 1];
+    w4a8::isx_thresholds((uint32_t)c_int, b, thr);
+    cudaError_t e = w4a8::launch_index_softmax(A, rows, cols, (uint32_t)c_int, b, lut, thr, P,
+                                               static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "index_softmax_u8 launch");
 }
 
 const char* w4a8_last_error(void) { return g_last_error.c_str(); }

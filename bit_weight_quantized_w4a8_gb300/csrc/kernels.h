@@ -51,4 +51,14 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
                             unsigned flags, cudaStream_t stream);
 cudaError_t read_and_clear_mma_error(unsigned* flags, cudaStream_t stream);
 
+// IndexSoftmax (isx.cu).  The host helpers need no GPU.
+constexpr int kIsxMaxEntries = 256;  // 2^b table entries, b <= 8
+void isx_build_lut(int b, double c, uint8_t* lut);
+int64_t isx_c_int(double c, int64_t d, float s_q, float s_k);
+void isx_thresholds(uint32_t c_int, int b, uint32_t* thr);
+int isx_kernel_kind(int64_t cols, bool vec_ok, int* q_needed);
+cudaError_t launch_index_softmax(const int32_t* A, int64_t rows, int64_t cols, uint32_t c_int,
+                                 int b, const uint8_t* lut, const uint32_t* thr, uint8_t* P,
+                                 cudaStream_t stream);
+
 }  // namespace w4a8

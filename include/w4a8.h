@@ -12,6 +12,8 @@
  *  - "TPU-MLIR W8A16 for ChatGLM2-6B", sections 2-4: per-channel INT8
  *    weights, cast back to floating point and multiplied by the scale, then
  *    multiplied with the F16 activation (w8a16_gemv below).
+ *  - "IntAttention" (MLSys 2026), section 基准/方法设计: the IndexSoftmax
+ *    integer softmax (index_softmax_u8 below).
  *
  * Readings of points the pages leave open (fixed here, identical in the
  * CPU oracle used by the tests):
@@ -285,6 +287,48 @@ size_t w8a16_workspace_bytes(int64_t M, int64_t K, int64_t N);
 int w8a16_gemv(const uint16_t* X, int64_t M, int64_t K, const int8_t* Wq8,
                const uint16_t* sw16, int64_t N, float* Y, void* ws, size_t ws_bytes,
                unsigned flags, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* IndexSoftmax (integer softmax of attention logits)                      */
+/* ---------------------------------------------------------------------- */
+
+/* IndexSoftmax (page "【MLSys 2026】IntAttention：全整数注意力流水线，边缘推理的高效部署",
+ * section 基准/方法设计, mechanisms 1-3): int32 attention logits (an INT8 x INT8
+ * QK^T product) to UINT8 probabilities without floating point, per row:
+ *   delta = rowMax(A) - A;  delta' = min(delta, c_int)
+ *   idx   = round(delta' * (2^b - 1) / c_int);  E = LUT[idx]
+ *   P     = round(255 * E / rowSum(E))
+ * Every rounding takes halves up (all operands are non-negative); c_int = 0
+ * clips every distance to 0.  P is bit-identical to the CPU definition. */
+
+/* The page's hyperparameters, b = 5 (a 32-entry table) and c = 6.6. */
+#define ISX_DEFAULT_B 5
+#define ISX_DEFAULT_C 6.6
+#define ISX_MAX_COLS (1 << 23)
+
+/* Host-only (no GPU): fills lut[0 .. 2^b - 1] with
+ * LUT[i] = round(255 * exp(-c * i / (2^b - 1))) in binary64, LUT[2^b - 1] = 0.
+ * Requires 1 <= b <= 8 and c > 0. */
+int index_softmax_lut(int b, double c, uint8_t* lut);
+
+/* Host-only: the clipping threshold in logit units,
+ * c_int = round(c * sqrt(d) / (s_q * s_k)) in binary64, for per-tensor INT8
+ * scales s_q, s_k and head dimension d.  Returns -1 unless c > 0, d >= 1,
+ * s_q > 0, s_k > 0 and the result fits in [0, 2^31 - 1]. */
+int64_t index_softmax_c_int(double c, int64_t d, float s_q, float s_k);
+
+/* P[rows][cols] = IndexSoftmax(A[rows][cols]) row by row.
+ *   A: int32 logits (device); P: UINT8 probabilities out (device).
+ *   c_int: threshold (index_softmax_c_int); b: table bits; lut: HOST array
+ *   of 2^b entries (index_softmax_lut, or any table with lut[0] >= 1, which
+ *   keeps every row sum positive), copied into the launch.
+ * Requires 1 <= rows <= 2^31 - 1, 1 <= cols <= ISX_MAX_COLS,
+ * 0 <= c_int <= 2^31 - 1, 1 <= b <= 8, lut[0] >= 1; A 4-byte aligned.
+ * cols % 4 == 0 with A 16-byte and P 4-byte aligned takes the vector path;
+ * rows of up to 8192 (vector path) or 2048 elements stay in registers (one
+ * read of A), longer rows are read three times. */
+int index_softmax_u8(const int32_t* A, int64_t rows, int64_t cols, int64_t c_int, int b,
+                     const uint8_t* lut, uint8_t* P, void* stream);
 
 /* ---------------------------------------------------------------------- */
 /* Diagnostics                                                             */

@@ -258,3 +258,39 @@ def test_group_plan_windows(sms, splits):
             assert w4.w4a8g_workspace_bytes(M, K, N, gs) == p["ws_bytes"] or sms != 0
     finally:
         w4.w4a8_set_tuning(reset=True)
+
+
+# --------------------------------------------------------------------------
+# IndexSoftmax host helpers and argument checks
+# --------------------------------------------------------------------------
+
+def test_isx_lut_and_c_int_match_oracle():
+    import oracle
+    o = oracle.load()
+    for b, c in [(5, 6.6), (3, 5.5), (4, 7.7), (8, 5.5), (1, 2.0)]:
+        assert w4.index_softmax_lut(b, c) == bytes(o.isx_lut(b, c)), (b, c)
+    for c, d, sq, sk in [(6.6, 128, 4 / 127, 4 / 127), (2.5, 1, 1.0, 1.0), (6.6, 64, 0.01, 0.02),
+                         (5.5, 128, 2.0 ** -5, 2.0 ** -5)]:
+        assert w4.index_softmax_c_int(c, d, sq, sk) == o.isx_c_int(c, d, sq, sk)
+    with pytest.raises(w4.W4A8Error):
+        w4.index_softmax_c_int(6.6, 128, 1e-6, 1e-6)    # beyond 2^31 - 1
+    with pytest.raises(w4.W4A8Error):
+        w4.index_softmax_lut(9, 6.6)
+
+
+def test_isx_argument_checks(L):
+    E_S, E_A, E_N = w4._binding.ERR_SHAPE, w4._binding.ERR_ALIGN, w4._binding.ERR_NULL
+    lut = (ctypes.c_uint8 * 32)(*w4.index_softmax_lut())
+    zero_lut = (ctypes.c_uint8 * 32)()
+    lp = ctypes.cast(lut, ctypes.c_void_p)
+    assert L.index_softmax_u8(None, 1, 8, 100, 5, lp, P16, None) == E_N
+    assert L.index_softmax_u8(P16, 1, 8, 100, 5, None, P16, None) == E_N
+    assert L.index_softmax_u8(P16, 0, 8, 100, 5, lp, P16, None) == E_S
+    assert L.index_softmax_u8(P16, 1, 0, 100, 5, lp, P16, None) == E_S
+    assert L.index_softmax_u8(P16, 1, (1 << 23) + 1, 100, 5, lp, P16, None) == E_S
+    assert L.index_softmax_u8(P16, 1, 8, -1, 5, lp, P16, None) == E_S
+    assert L.index_softmax_u8(P16, 1, 8, 1 << 31, 5, lp, P16, None) == E_S
+    assert L.index_softmax_u8(P16, 1, 8, 100, 0, lp, P16, None) == E_S
+    assert L.index_softmax_u8(P16, 1, 8, 100, 9, lp, P16, None) == E_S
+    assert L.index_softmax_u8(P16, 1, 8, 100, 5, ctypes.cast(zero_lut, ctypes.c_void_p), P16, None) == E_S
+    assert L.index_softmax_u8(P16 + 2, 1, 8, 100, 5, lp, P16, None) == E_A
