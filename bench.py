@@ -22,6 +22,8 @@ Reported (one JSON line, rank 0):
   skinny_batch  gate and down at M = 1 ... 64 activation rows
   w8a16_set the ChatGLM2-6B-shaped W8A16 GEMVs at M=1
   group_scale_set  the M=1 set with group-wise INT4 scales (group 128)
+  index_softmax  the IntAttention page's integer softmax on 32 x 1024 x 4096
+            int32 attention logits
 
 `--impl reference` times the CPU oracle alone (the reference arm).
 Under torchrun with N > 1 every rank runs an independent replica (weak
@@ -32,6 +34,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import subprocess
 import sys
@@ -478,6 +481,7 @@ def run_ours(args, world, rank):
         extra["skinny_batch"] = measure_skinny(torch, w4, synth, dev, stream, copies, lin)
         extra["w8a16_set"] = measure_w8a16(torch, w4, synth, dev, stream)
         extra["group_scale_set"] = measure_group_set(torch, w4, synth, dev, stream, lin)
+        extra["index_softmax"] = measure_index_softmax(torch, w4, synth, dev, stream, peak)
         del copies
         torch.cuda.empty_cache()
         extra["decode_step_28_layers"] = measure_decode_step(torch, w4, synth, dev, stream, ws,
@@ -686,6 +690,40 @@ def measure_group_set(torch, w4, synth, dev, stream, lin, gs=GROUP_SIZE):
     return {"workload": "the M=1 set above with group-wise INT4 scales, group %d" % gs,
             "weight_bytes": nbytes, "us_per_set": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
             "lm_head_in_chain": {"us": round(us_lm, 2), "GBps": round(lm_bytes / us_lm / 1e3, 1)}}
+
+
+ISX_HEADS, ISX_QUERIES, ISX_KEYS = 32, 1024, 4096
+
+
+def measure_index_softmax(torch, w4, synth, dev, stream, peak):
+    """IndexSoftmax on int32 attention logits of 32 heads x 1024 query rows x
+    4096 keys (d = 128, per-tensor INT8 scales 4/127, dequantized logits with
+    standard deviation 4): two logit buffers alternate (2 x 512 MB > L2), a
+    graph of 10 launches; bytes per launch = 4 per logit in + 1 per
+    probability out."""
+    rows, cols = ISX_HEADS * ISX_QUERIES, ISX_KEYS
+    s = float(np.float32(4 / 127))
+    scale = 4.0 * math.sqrt(128) / (s * s)
+    bufs = []
+    for c in range(2):
+        A = torch.empty((rows, cols), dtype=torch.int32, device=dev)
+        for r0 in range(0, rows, 2048):
+            z = synth.normal_gpu(4242 + c, (2048, cols), 1.0, offset=r0 * cols, device=dev)
+            A[r0:r0 + 2048] = torch.round(z.double() * scale).int()
+            del z
+        bufs.append(A)
+    P = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    c_int = w4.index_softmax_c_int(w4.ISX_DEFAULT_C, 128, s, s)
+    lut = w4.index_softmax_lut()
+    us = _graph_us(torch, stream, lambda: [w4.index_softmax_u8(bufs[k % 2], c_int, lut=lut, P=P)
+                                           for k in range(10)], 10)
+    nbytes = rows * cols * 5
+    del bufs
+    return {"workload": "IndexSoftmax (b=5, c=6.6) of int32 logits, %d heads x %d query rows x %d keys"
+                        % (ISX_HEADS, ISX_QUERIES, ISX_KEYS),
+            "bytes_per_launch": nbytes, "us": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+            "of_measured_peak": round(nbytes / us / 1e3 / peak, 4),
+            "Gelem_per_s": round(rows * cols / us / 1e3, 1)}
 
 
 W8A16_SET = [("h_to_4h", 4096, 27392), ("qkv", 4096, 4608), ("4h_to_h", 13696, 4096)]

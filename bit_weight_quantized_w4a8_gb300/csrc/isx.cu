@@ -15,10 +15,10 @@
 //
 // The index is exact without a division per element: idx is the number of
 // k in 1..top with delta' >= T[k], T[k] = ceil(c_int (2k - 1) / (2 top)) (the
-// smallest delta' that rounds to k or more).  An fp32 estimate
-// rint(delta' * top / c_int) is within 5e-5 of the exact quotient, so it is
-// off by at most one, next to a half; one comparison with T[est] and
-// T[est + 1] corrects it.
+// smallest delta' that rounds to k or more).  The fp32 quotient
+// x = delta' * top / c_int is within 5e-5 of the exact one, so the exact
+// index round(x) is floor(x) or floor(x) + 1 (or exactly floor(x) + 1 past a
+// half near an integer), and the single threshold T[floor(x) + 1] decides.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -85,11 +85,11 @@ __device__ __forceinline__ uint32_t isx_index(int a, int mx, uint32_t c_int, flo
                                               const uint32_t* thr) {
     const uint32_t delta = (uint32_t)mx - (uint32_t)a;  // mx >= a: exact as uint32
     const uint32_t cl = delta < c_int ? delta : c_int;
-    int est = __float2int_rn(__uint2float_rn(cl) * inv);
-    est = min(max(est, 0), top);
-    if (cl >= thr[est + 1]) ++est;
-    else if (cl < thr[est]) --est;
-    return (uint32_t)est;
+    // x = cl * top / c_int within 5e-5: the exact index is floor(x) or
+    // floor(x) + 1, decided by the one threshold between them
+    const float x = __uint2float_rn(cl) * inv;
+    const int j = min((int)x + 1, top);  // x >= 0: truncation is floor
+    return cl >= thr[j] ? (uint32_t)j : (uint32_t)(j - 1);
 }
 
 // Stages the launch's table, thresholds into shared memory.
