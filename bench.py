@@ -92,7 +92,8 @@ def parse():
                     help="skip the 28-layer step, the skinny-batch sweep and the W8A16 set")
     ap.add_argument("--min-busy-s", type=float, default=0.6,
                     help="keep the GPU busy at least this long before timing (clock samples)")
-    ap.add_argument("--only", choices=[l[0] for l in LAUNCHES] + ["w8_" + l[0] for l in W8A16_SET],
+    ap.add_argument("--only", choices=[l[0] for l in LAUNCHES] + ["w8_" + l[0] for l in W8A16_SET]
+                    + ["isx"],
                     default=None,
                     help="profiling aid: time one launch kind alone, eagerly, without PDL "
                          "(not the headline metric)")
@@ -770,6 +771,8 @@ def run_only(args, lname):
     dev = torch.device("cuda", torch.cuda.current_device())
     if lname.startswith("w8_"):
         return run_only_w8(args, lname[3:], torch, synth, w4, dev)
+    if lname == "isx":
+        return run_only_isx(args, torch, synth, w4, dev)
     members = dict(LAUNCHES)[lname]
     names = [l[0] for l in LINEARS]
     idx = [names.index(n) for n in members]
@@ -821,6 +824,33 @@ def run_only(args, lname):
                       "us_per_launch": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                       "note": "eager launches, host launch gaps included; profiling aid"}),
           flush=True)
+
+
+def run_only_isx(args, torch, synth, w4, dev):
+    """Profiling aid: eager IndexSoftmax launches on the benchmark's logits."""
+    rows, cols = ISX_HEADS * ISX_QUERIES, ISX_KEYS
+    s = float(np.float32(4 / 127))
+    A = torch.empty((rows, cols), dtype=torch.int32, device=dev)
+    for r0 in range(0, rows, 2048):
+        z = synth.normal_gpu(4242, (2048, cols), 1.0, offset=r0 * cols, device=dev)
+        A[r0:r0 + 2048] = torch.round(z.double() * (4.0 * math.sqrt(128) / (s * s))).int()
+        del z
+    P = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    c_int = w4.index_softmax_c_int(w4.ISX_DEFAULT_C, 128, s, s)
+    lut = w4.index_softmax_lut()
+    for _ in range(args.warmup):
+        w4.index_softmax_u8(A, c_int, lut=lut, P=P)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        w4.index_softmax_u8(A, c_int, lut=lut, P=P)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / args.steps * 1e3
+    print(json.dumps({"only": "isx", "steps": args.steps, "us_per_launch": round(us, 2),
+                      "GBps": round(rows * cols * 5 / us / 1e3, 1),
+                      "note": "eager launches on one logit buffer; profiling aid"}), flush=True)
 
 
 def run_only_w8(args, name, torch, synth, w4, dev):

@@ -15,10 +15,11 @@
 //
 // The index is exact without a division per element: idx is the number of
 // k in 1..top with delta' >= T[k], T[k] = ceil(c_int (2k - 1) / (2 top)) (the
-// smallest delta' that rounds to k or more).  The fp32 quotient
-// x = delta' * top / c_int is within 5e-5 of the exact one, so the exact
-// index round(x) is floor(x) or floor(x) + 1 (or exactly floor(x) + 1 past a
-// half near an integer), and the single threshold T[floor(x) + 1] decides.
+// smallest delta' that rounds to k or more).  An integer estimate
+// e = floor(delta' M / 2^32), M = ceil(2^32 top / c_int), is never below
+// floor(x), x = delta' top / c_int, and less than 1/2 above it, so the index
+// round(x) is e or e + 1 and the single threshold T[e + 1] decides; it is
+// packed with LUT[e] and LUT[e + 1] into one 8-byte shared-memory entry.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -40,7 +41,7 @@ struct IsxArgs {
     int cols;
     uint32_t c_int;
     int top;                   // 2^b - 1
-    float inv;                 // top / c_int (0 when c_int == 0)
+    uint32_t m_hi, m_lo;       // M = ceil(2^32 top / c_int) = m_hi 2^32 + m_lo (0 when c_int == 0)
     uint32_t thr[kIsxMaxEntries + 1];  // T[0] = 0, T[1..top], T[top + 1] = UINT32_MAX
     uint8_t lut[kIsxMaxEntries];
 };
@@ -57,60 +58,50 @@ __device__ __forceinline__ int warp_sum_i(int v) {
     return v;
 }
 
-// Block-wide max / sum over kIsxThreads threads (every thread gets the result).
-__device__ __forceinline__ int block_max_i(int v, int* red) {
-    v = warp_max_i(v);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    int m = red[0];
-    #pragma unroll
-    for (int w = 1; w < kIsxWarps; ++w) m = max(m, red[w]);
-    __syncthreads();  // red is reused
-    return m;
+// Shared table entry e (0 <= e <= top): T[e + 1], and LUT[e] | LUT[e + 1] << 8.
+__device__ __forceinline__ void isx_stage(const IsxArgs& a, uint2* tab) {
+    for (int e = threadIdx.x; e <= a.top; e += kIsxThreads) {
+        const uint32_t next = e < a.top ? a.lut[e + 1] : 0u;
+        tab[e] = make_uint2(a.thr[e + 1], (uint32_t)a.lut[e] | (next << 8));
+    }
 }
 
-__device__ __forceinline__ int block_sum_i(int v, int* red) {
-    v = warp_sum_i(v);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    int s = 0;
-    #pragma unroll
-    for (int w = 0; w < kIsxWarps; ++w) s += red[w];
-    __syncthreads();
-    return s;
-}
-
-// The exact table index of one logit given the row max.
-__device__ __forceinline__ uint32_t isx_index(int a, int mx, uint32_t c_int, float inv, int top,
-                                              const uint32_t* thr) {
+// The exact table index of one logit given the row max, and its entry E.
+// e = floor(cl M / 2^32) never undershoots floor(x), x = cl top / c_int, and
+// exceeds it by less than 1/2, so the index round(x) is e or e + 1 and
+// T[e + 1] decides (when e = floor(x) + 1, x is past its half and T[e + 1]
+// is out of reach).
+__device__ __forceinline__ uint32_t isx_lookup(int a, int mx, uint32_t c_int, uint32_t m_hi,
+                                               uint32_t m_lo, const uint2* tab, int* E) {
     const uint32_t delta = (uint32_t)mx - (uint32_t)a;  // mx >= a: exact as uint32
     const uint32_t cl = delta < c_int ? delta : c_int;
-    // x = cl * top / c_int within 5e-5: the exact index is floor(x) or
-    // floor(x) + 1, decided by the one threshold between them
-    const float x = __uint2float_rn(cl) * inv;
-    const int j = min((int)x + 1, top);  // x >= 0: truncation is floor
-    return cl >= thr[j] ? (uint32_t)j : (uint32_t)(j - 1);
-}
-
-// Stages the launch's table, thresholds into shared memory.
-__device__ __forceinline__ void isx_stage(const IsxArgs& a, uint32_t* thr_s, int* lut_s) {
-    for (int i = threadIdx.x; i <= a.top + 1; i += kIsxThreads) thr_s[i] = a.thr[i];
-    for (int i = threadIdx.x; i <= a.top; i += kIsxThreads) lut_s[i] = a.lut[i];
+    const uint32_t e = cl * m_hi + __umulhi(cl, m_lo);  // <= top: no overflow
+    const uint2 t = tab[e];
+    const bool up = cl >= t.x;
+    *E = (int)__byte_perm(t.y, 0u, up ? 0x4441u : 0x4440u);
+    return up ? e + 1u : e;
 }
 
 // Register-resident rows: each thread holds Q accesses of V consecutive
 // logits (V = 4: one 16-byte load, one 4-byte store of P; V = 1 otherwise).
+// Three barriers per row: the reduction slots and the probability table are
+// double-buffered by row parity, so no row waits for the previous one's
+// readers (a thread two rows ahead has passed barriers every other thread
+// reached only after finishing those reads).
 template <int V, int Q>
 __global__ void __launch_bounds__(kIsxThreads) isx_rows_kernel(const __grid_constant__ IsxArgs a) {
-    __shared__ uint32_t thr_s[kIsxMaxEntries + 1];
-    __shared__ int lut_s[kIsxMaxEntries];
-    __shared__ int ptab_s[kIsxMaxEntries];
-    __shared__ int red[kIsxWarps];
-    isx_stage(a, thr_s, lut_s);
+    __shared__ uint2 tab_s[kIsxMaxEntries];
+    __shared__ int ptab_s[2][kIsxMaxEntries];
+    __shared__ int red_max[2][kIsxWarps];
+    __shared__ int red_sum[2][kIsxWarps];
+    isx_stage(a, tab_s);
     __syncthreads();
 
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int nacc = a.cols / V;  // accesses per row (cols % V == 0)
-    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+    int par = 0;
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x, par ^= 1) {
         const int32_t* Ar = a.A + r * a.cols;
         int x[Q][V];
         int mx = INT32_MIN;
@@ -128,7 +119,12 @@ __global__ void __launch_bounds__(kIsxThreads) isx_rows_kernel(const __grid_cons
                 for (int u = 0; u < V; ++u) mx = max(mx, x[q][u]);
             }
         }
-        mx = block_max_i(mx, red);
+        mx = warp_max_i(mx);
+        if (lane == 0) red_max[par][warp] = mx;
+        __syncthreads();
+        mx = red_max[par][0];
+        #pragma unroll
+        for (int w = 1; w < kIsxWarps; ++w) mx = max(mx, red_max[par][w]);
 
         uint32_t idx[Q];  // V table indices per access, one byte each
         int sum = 0;
@@ -139,64 +135,85 @@ __global__ void __launch_bounds__(kIsxThreads) isx_rows_kernel(const __grid_cons
             if (k < nacc) {
                 #pragma unroll
                 for (int u = 0; u < V; ++u) {
-                    const uint32_t i = isx_index(x[q][u], mx, a.c_int, a.inv, a.top, thr_s);
-                    sum += lut_s[i];
+                    int E;
+                    const uint32_t i = isx_lookup(x[q][u], mx, a.c_int, a.m_hi, a.m_lo, tab_s, &E);
+                    sum += E;
                     idx[q] |= i << (8 * u);
                 }
             }
         }
-        const int S = block_sum_i(sum, red);  // >= LUT[0] > 0 (the max's entry)
+        sum = warp_sum_i(sum);
+        if (lane == 0) red_sum[par][warp] = sum;
+        __syncthreads();
+        int S = 0;  // >= LUT[0] > 0 (the max's entry)
+        #pragma unroll
+        for (int w = 0; w < kIsxWarps; ++w) S += red_sum[par][w];
         // the 2^b possible probabilities of this row, round(255 E / S) with
         // halves up, in uint32 (2 S < 2^32 for every row the ABI admits)
         for (int i = threadIdx.x; i <= a.top; i += kIsxThreads)
-            ptab_s[i] = (int)((2u * 255u * (uint32_t)lut_s[i] + (uint32_t)S) / (2u * (uint32_t)S));
+            ptab_s[par][i] = (int)((2u * 255u * (tab_s[i].y & 0xFFu) + (uint32_t)S) / (2u * (uint32_t)S));
         __syncthreads();
 
+        const int* pt = ptab_s[par];
         uint8_t* Pr = a.P + r * a.cols;
         #pragma unroll
         for (int q = 0; q < Q; ++q) {
             const int k = threadIdx.x + q * kIsxThreads;
             if (k < nacc) {
                 if constexpr (V == 4) {
-                    const uint32_t w = (uint32_t)ptab_s[idx[q] & 0xFF] |
-                                       ((uint32_t)ptab_s[(idx[q] >> 8) & 0xFF] << 8) |
-                                       ((uint32_t)ptab_s[(idx[q] >> 16) & 0xFF] << 16) |
-                                       ((uint32_t)ptab_s[idx[q] >> 24] << 24);
+                    const uint32_t w = (uint32_t)pt[idx[q] & 0xFF] |
+                                       ((uint32_t)pt[(idx[q] >> 8) & 0xFF] << 8) |
+                                       ((uint32_t)pt[(idx[q] >> 16) & 0xFF] << 16) |
+                                       ((uint32_t)pt[idx[q] >> 24] << 24);
                     __stcs(reinterpret_cast<uint32_t*>(Pr) + k, w);
                 } else {
-                    Pr[k] = (uint8_t)ptab_s[idx[q] & 0xFF];
+                    Pr[k] = (uint8_t)pt[idx[q] & 0xFF];
                 }
             }
         }
-        __syncthreads();  // ptab_s is rebuilt for the next row
     }
 }
 
 // Rows too long for registers: max, then sum, then output, each streaming
-// the row from global memory.
+// the row from global memory (same barrier scheme).
 __global__ void __launch_bounds__(kIsxThreads) isx_long_kernel(const __grid_constant__ IsxArgs a) {
-    __shared__ uint32_t thr_s[kIsxMaxEntries + 1];
-    __shared__ int lut_s[kIsxMaxEntries];
-    __shared__ int ptab_s[kIsxMaxEntries];
-    __shared__ int red[kIsxWarps];
-    isx_stage(a, thr_s, lut_s);
+    __shared__ uint2 tab_s[kIsxMaxEntries];
+    __shared__ int ptab_s[2][kIsxMaxEntries];
+    __shared__ int red_max[2][kIsxWarps];
+    __shared__ int red_sum[2][kIsxWarps];
+    isx_stage(a, tab_s);
     __syncthreads();
-    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int par = 0;
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x, par ^= 1) {
         const int32_t* Ar = a.A + r * a.cols;
         int mx = INT32_MIN;
         for (int k = threadIdx.x; k < a.cols; k += kIsxThreads) mx = max(mx, Ar[k]);
-        mx = block_max_i(mx, red);
+        mx = warp_max_i(mx);
+        if (lane == 0) red_max[par][warp] = mx;
+        __syncthreads();
+        mx = red_max[par][0];
+        for (int w = 1; w < kIsxWarps; ++w) mx = max(mx, red_max[par][w]);
         int sum = 0;
-        for (int k = threadIdx.x; k < a.cols; k += kIsxThreads)
-            sum += lut_s[isx_index(Ar[k], mx, a.c_int, a.inv, a.top, thr_s)];
-        const int S = block_sum_i(sum, red);
+        for (int k = threadIdx.x; k < a.cols; k += kIsxThreads) {
+            int E;
+            isx_lookup(Ar[k], mx, a.c_int, a.m_hi, a.m_lo, tab_s, &E);
+            sum += E;
+        }
+        sum = warp_sum_i(sum);
+        if (lane == 0) red_sum[par][warp] = sum;
+        __syncthreads();
+        int S = 0;
+        for (int w = 0; w < kIsxWarps; ++w) S += red_sum[par][w];
         for (int i = threadIdx.x; i <= a.top; i += kIsxThreads)
-            ptab_s[i] = (int)((2u * 255u * (uint32_t)lut_s[i] + (uint32_t)S) / (2u * (uint32_t)S));
+            ptab_s[par][i] = (int)((2u * 255u * (tab_s[i].y & 0xFFu) + (uint32_t)S) / (2u * (uint32_t)S));
         __syncthreads();
         uint8_t* Pr = a.P + r * a.cols;
-        for (int k = threadIdx.x; k < a.cols; k += kIsxThreads)
-            Pr[k] = (uint8_t)ptab_s[isx_index(Ar[k], mx, a.c_int, a.inv, a.top, thr_s)];
-        __syncthreads();
+        for (int k = threadIdx.x; k < a.cols; k += kIsxThreads) {
+            int E;
+            Pr[k] = (uint8_t)ptab_s[par][isx_lookup(Ar[k], mx, a.c_int, a.m_hi, a.m_lo, tab_s, &E)];
+        }
     }
 }
 
@@ -253,7 +270,10 @@ cudaError_t launch_index_softmax(const int32_t* A, int64_t rows, int64_t cols, u
     a.cols = (int)cols;
     a.c_int = c_int;
     a.top = (1 << b) - 1;
-    a.inv = c_int > 0 ? (float)a.top / (float)c_int : 0.f;
+    // M = ceil(2^32 top / c_int) < 2^40
+    const uint64_t m = c_int > 0 ? (((uint64_t)a.top << 32) + c_int - 1) / c_int : 0;
+    a.m_hi = (uint32_t)(m >> 32);
+    a.m_lo = (uint32_t)m;
     for (int i = 0; i <= a.top + 1; ++i) a.thr[i] = thr[i];
     for (int i = 0; i <= a.top; ++i) a.lut[i] = lut[i];
     const bool vec_ok = (cols % 4 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0) &&
