@@ -7,7 +7,9 @@
 // bit-identical to the CPU definition.
 //
 // HBM-bound (4 bytes in, 1 byte out per element), one pass over HBM: one
-// CTA per row keeps the row in registers (up to 8192 elements), takes the
+// CTA of 128 threads per row keeps the row in registers (up to 8192
+// elements; 128 threads leave each thread enough elements to amortize the
+// per-row reductions, 256 or 64 were measured slower), takes the
 // block max, the per-element table index (kept in registers as bytes), the
 // block sum, then writes P from a per-row table of the 2^b possible
 // probabilities, round(255 * LUT[i] / S), built once per row.  Rows longer
@@ -31,7 +33,7 @@
 namespace w4a8 {
 namespace {
 
-constexpr int kIsxThreads = 256;
+constexpr int kIsxThreads = 128;
 constexpr int kIsxWarps = kIsxThreads / 32;
 
 struct IsxArgs {
@@ -222,7 +224,8 @@ cudaError_t launch_rows(const IsxArgs& a, int q_needed, dim3 grid, cudaStream_t 
     if (q_needed <= 1) isx_rows_kernel<V, 1><<<grid, kIsxThreads, 0, stream>>>(a);
     else if (q_needed <= 2) isx_rows_kernel<V, 2><<<grid, kIsxThreads, 0, stream>>>(a);
     else if (q_needed <= 4) isx_rows_kernel<V, 4><<<grid, kIsxThreads, 0, stream>>>(a);
-    else isx_rows_kernel<V, 8><<<grid, kIsxThreads, 0, stream>>>(a);
+    else if (q_needed <= 8) isx_rows_kernel<V, 8><<<grid, kIsxThreads, 0, stream>>>(a);
+    else isx_rows_kernel<V, 16><<<grid, kIsxThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -256,7 +259,7 @@ int isx_kernel_kind(int64_t cols, bool vec_ok, int* q_needed) {
     const int64_t acc = cols / V;
     const int64_t q = (acc + kIsxThreads - 1) / kIsxThreads;
     *q_needed = (int)q;
-    if (q <= 8) return vec_ok ? 4 : 1;
+    if (q <= (vec_ok ? 16 : 8)) return vec_ok ? 4 : 1;
     return 0;  // streaming kernel
 }
 

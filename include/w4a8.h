@@ -325,7 +325,7 @@ int64_t index_softmax_c_int(double c, int64_t d, float s_q, float s_k);
  * Requires 1 <= rows <= 2^31 - 1, 1 <= cols <= ISX_MAX_COLS,
  * 0 <= c_int <= 2^31 - 1, 1 <= b <= 8, lut[0] >= 1; A 4-byte aligned.
  * cols % 4 == 0 with A 16-byte and P 4-byte aligned takes the vector path;
- * rows of up to 8192 (vector path) or 2048 elements stay in registers (one
+ * rows of up to 8192 (vector path) or 1024 elements stay in registers (one
  * read of A), longer rows are read three times. */
 int index_softmax_u8(const int32_t* A, int64_t rows, int64_t cols, int64_t c_int, int b,
                      const uint8_t* lut, uint8_t* P, void* stream);
