@@ -429,9 +429,15 @@ def run_ours(args, world, rank):
     barrier(world)
     ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
 
-    # --- dominant kernel: lm_head, CUDA events around each launch ------------
+    # --- dominant kernel: lm_head.  Its steady-state launch duration: CUDA
+    # events on the stream around replays of a graph of 20 back-to-back
+    # launches (PDL, the two weight copies alternating: 546 MB > L2), as it
+    # runs inside the set; and one launch on its own (ramp-up and tail
+    # included), for reference
     jl = [l[0] for l in LAUNCHES].index("lm_head")
     _, K_lm, N_lm = LINEARS[lin["lm_head"][0]]
+    lm_chain_us = _graph_us(torch, stream, lambda: [launch(k % 2, jl, PDL) for k in range(20)], 20,
+                            reps=10)
     n_lm = max(20, min(args.steps, 400))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_lm)]
@@ -493,7 +499,7 @@ def run_ours(args, world, rank):
 
     value = SET_BYTES * world / (ms_step * 1e-3) / 1e9
     lm_bytes = weight_bytes(K_lm, N_lm)
-    achieved = lm_bytes / (lm_ms * 1e-3) / 1e9
+    achieved = lm_bytes / (lm_chain_us * 1e-6) / 1e9
     traffic = profiled_traffic()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -511,7 +517,11 @@ def run_ours(args, world, rank):
         "roofline": {"bound": "hbm", "kernel": "gemv_kernel<W4A8, M=1, fused> on lm_head 3584->152064",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes": lm_bytes, "avg_launch_us": round(lm_ms * 1e3, 2)},
+                     "algorithmic_bytes": lm_bytes, "avg_launch_us": round(lm_chain_us, 2),
+                     "how": "graph of 20 back-to-back lm_head launches (PDL, two weight copies), "
+                            "CUDA events around 10 replays on the launching stream",
+                     "isolated_launch_us": round(lm_ms * 1e3, 2),
+                     "isolated_frac": round(lm_bytes / (lm_ms * 1e-3) / 1e9 / peak, 4)},
         "e2e": {"value": round(SET_BYTES * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "us_per_set": round(e2e_ms * 1e3, 2),
                 "h2d_bytes_per_step": int(X_pin.numel() * X_pin.element_size()),
