@@ -97,6 +97,8 @@ def parse():
                     default=None,
                     help="profiling aid: time one launch kind alone, eagerly, without PDL "
                          "(not the headline metric)")
+    ap.add_argument("--m", type=int, default=1,
+                    help="with --only: activation rows of the W4A8 launch (3..64 take the tensor cores)")
     ap.add_argument("--group", type=int, default=0,
                     help="with --only: group-wise INT4 scales of this group size")
     return ap.parse_args()
@@ -694,13 +696,14 @@ def measure_group_set(torch, w4, synth, dev, stream, lin, gs=GROUP_SIZE):
     us = _graph_us(torch, stream, pair, 2, reps=20)
     nbytes = sum(N * (K // 2 + 4 * w4.w4g_scale_stride(K, gs)) for _, K, N in LINEARS)
     jl = [l[0] for l in LAUNCHES].index("lm_head")
-    us_lm = _graph_us(torch, stream, lambda: [launch(k % 2, jl, 0) for k in range(20)], 20)
+    us_lm = _graph_us(torch, stream, lambda: [launch(k % 2, jl, w4.LAUNCH_PDL) for k in range(20)], 20)
     _, K_lm, N_lm = LINEARS[names.index("lm_head")]
     lm_bytes = N_lm * (K_lm // 2 + 4 * w4.w4g_scale_stride(K_lm, gs))
     del copies
     return {"workload": "the M=1 set above with group-wise INT4 scales, group %d" % gs,
             "weight_bytes": nbytes, "us_per_set": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
-            "lm_head_in_chain": {"us": round(us_lm, 2), "GBps": round(lm_bytes / us_lm / 1e3, 1)}}
+            "lm_head_in_chain": {"us": round(us_lm, 2), "GBps": round(lm_bytes / us_lm / 1e3, 1),
+                                 "how": "graph of 20 back-to-back launches, PDL, two weight copies"}}
 
 
 ISX_HEADS, ISX_QUERIES, ISX_KEYS = 32, 1024, 4096
@@ -787,7 +790,8 @@ def run_only(args, lname):
     names = [l[0] for l in LINEARS]
     idx = [names.index(n) for n in members]
     K = LINEARS[idx[0]][1]
-    X = torch.from_numpy(synth.activation(activation_seed(members[0]), 1, K,
+    M = args.m
+    X = torch.from_numpy(synth.activation(activation_seed(members[0]), M, K,
                                           outlier_frac=OUTLIER_FRAC)).to(dev)
     gs = args.group
     copies = []
@@ -800,9 +804,9 @@ def run_only(args, lname):
             ws_.append(Wq)
             ss_.append(sw)
         copies.append((ws_, ss_))
-    Ys = [torch.empty((1, LINEARS[i][2]), dtype=torch.float32, device=dev) for i in idx]
+    Ys = [torch.empty((M, LINEARS[i][2]), dtype=torch.float32, device=dev) for i in idx]
     N_all = sum(LINEARS[i][2] for i in idx)
-    nws = w4.w4a8g_workspace_bytes(1, K, N_all, gs) if gs else w4.w4a8_workspace_bytes(1, K, N_all)
+    nws = w4.w4a8g_workspace_bytes(M, K, N_all, gs) if gs else w4.w4a8_workspace_bytes(M, K, N_all)
     wsb = torch.zeros(max(nws, 4096), dtype=torch.uint8, device=dev)
 
     def one(k):
@@ -830,7 +834,7 @@ def run_only(args, lname):
         nbytes = sum(LINEARS[i][2] * (K // 2 + 4 * w4.w4g_scale_stride(K, gs)) for i in idx)
     else:
         nbytes = sum(weight_bytes(K, LINEARS[i][2]) for i in idx)
-    print(json.dumps({"only": lname, "members": list(members), "group": gs, "steps": args.steps,
+    print(json.dumps({"only": lname, "members": list(members), "M": M, "group": gs, "steps": args.steps,
                       "us_per_launch": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                       "note": "eager launches, host launch gaps included; profiling aid"}),
           flush=True)
