@@ -108,11 +108,16 @@ int check_w8a16_shape(int64_t M, int64_t K, int64_t N) {
 
 // Tensor-core plan for an M-row W4A8 call, or false when the dp4a path
 // serves it (fewer rows than the threshold, or no tensor-core plan).
-bool mma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::MmaPlan* pl, int sms = 0) {
+// group > 0: group-wise scales; the tensor cores take groups that are
+// whole 128-code stages of at most 16384 codes, smaller groups stay on the
+// dp4a kernel.
+bool mma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::MmaPlan* pl, int sms = 0,
+                  int64_t group = 0) {
     const int t = g_mma_min_m.load();
     if (M < (t > 0 ? t : kDefaultMmaMinM)) return false;
+    if (group > 0 && (group % 128 || group > 16384)) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
-    return w4a8::make_mma_plan((int)M, K, N, sms, pl);
+    return w4a8::make_mma_plan((int)M, K, N, sms, pl, (int)(group / 64));
 }
 
 int check_mma_workspace(const w4a8::MmaPlan& pl, void* ws, size_t ws_bytes) {
@@ -225,6 +230,8 @@ size_t w4a8g_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t group) {
     if (check_w4a8_shape(M, K, N) != W4A8_OK) return 0;
     int gshift, gld;
     if (check_group(K, group, &gshift, &gld) != W4A8_OK) return 0;
+    w4a8::MmaPlan mp;
+    if (mma_plan_for(M, K, N, &mp, 0, group)) return mp.ws_bytes;
     w4a8::GemvPlan pf, pt;
     if (plan_row_groups(true, true, M, K, N, kRowGroupW4, &pf, &pt, 0, gshift, gld) != W4A8_OK)
         return 0;
@@ -379,6 +386,21 @@ int w4a8g_run(const char* name, const uint16_t* X, const int8_t* Xq, const float
     if ((X && !aligned(X, 16)) || (Xq && !aligned(Xq, 16)) || (sa && !aligned(sa, 4)) ||
         (Xq_out && !aligned(Xq_out, 16)) || (sa_out && !aligned(sa_out, 4)))
         return fail(W4A8_ERR_ALIGN, "%s: X/Xq/Xq_out need 16-byte, sa/sa_out 4-byte alignment", name);
+    w4a8::MmaPlan mp;
+    if (mma_plan_for(M, K, total, &mp, 0, group)) {
+        // one plan per matrix inside; the workspace bound covers every N[g] <= total
+        for (int g = 0; g < G; ++g) {
+            w4a8::MmaPlan pg;
+            if (!w4a8::make_mma_plan((int)M, K, N[g], mp.sms, &pg, (int)(group / 64)) ||
+                pg.ws_bytes > mp.ws_bytes)
+                return fail(W4A8_ERR_SHAPE, "%s: no tensor-core plan for group %d", name, g);
+        }
+        if ((st = check_mma_workspace(mp, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_mma(mp, X, Xq, sa, (int)M, K, G, Wq, nullptr, N, Y, nullptr,
+                                              Xq_out, sa_out, ws, flags,
+                                              static_cast<cudaStream_t>(stream), (int)group, sg);
+        return e == cudaSuccess ? ok() : cuda_fail(e, name);
+    }
     w4a8::GemvPlan pf, pt;
     if ((st = plan_row_groups(true, true, M, K, total, kRowGroupW4, &pf, &pt, 0, gshift, gld)) != W4A8_OK)
         return st;
@@ -555,6 +577,14 @@ int w4a8g_plan_info(int64_t M, int64_t K, int64_t N, int64_t group, int num_sms,
     if (st != W4A8_OK) return st;
     int gshift, gld;
     if ((st = check_group(K, group, &gshift, &gld)) != W4A8_OK) return st;
+    w4a8::MmaPlan mp;
+    if (mma_plan_for(M, K, N, &mp, num_sms, group)) {
+        const int ws = mp.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)mp.ws_bytes;
+        const int v[] = {mp.P, 0, mp.BN, 128, mp.tiles, mp.grid, 128, mp.stages, mp.stage_bytes,
+                         mp.smem, ws, 1, 0, 0};
+        for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
+        return ok();
+    }
     w4a8::GemvPlan pl, pt;
     if ((st = plan_row_groups(true, true, M, K, N, kRowGroupW4, &pl, &pt, num_sms, gshift, gld)) !=
         W4A8_OK)

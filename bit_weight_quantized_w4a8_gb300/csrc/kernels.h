@@ -43,12 +43,16 @@ cudaError_t launch_w4a8g(const GemvPlan& pl, bool fused, const uint16_t* X, cons
 cudaError_t read_and_clear_group_error(unsigned* flags, cudaStream_t stream);
 
 // Tensor-core path (mma.cu).  make_mma_plan is host-only and needs no GPU.
-bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out);
+// gkb > 0: group-wise scales, groups of gkb 64-code K blocks (gs = 64 gkb).
+bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int gkb = 0);
+// gs > 0: group-wise scales sg[g] ([N][stride] fp32, gs a multiple of 128,
+// at most 16384); sw is then unused.
 cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* Xq, const float* sa,
                             int M, int64_t K, int G, const uint8_t* const* Wq,
                             const float* const* sw, const int64_t* Ns, float* const* Y,
                             int32_t* acc_out, int8_t* Xq_out, float* sa_out, void* ws,
-                            unsigned flags, cudaStream_t stream);
+                            unsigned flags, cudaStream_t stream, int gs = 0,
+                            const float* const* sg = nullptr);
 cudaError_t read_and_clear_mma_error(unsigned* flags, cudaStream_t stream);
 
 // IndexSoftmax (isx.cu).  The host helpers need no GPU.

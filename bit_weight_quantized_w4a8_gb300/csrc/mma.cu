@@ -71,7 +71,7 @@ constexpr uint32_t kTmemAStage = 32 * kStageK;  // two bf16 per column
 constexpr int kOffB = 0;
 constexpr int kOffW = kOffB + kStages * kBStageMax;
 constexpr int kOffBars = kOffW + kWStages * kWTileBytes;
-constexpr int kNumBars = 2 * kWStages + 3 * kStages + 1;
+constexpr int kNumBars = 2 * kWStages + 3 * kStages + 3;  // + accfull, dfull, dfree
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kMmaSmem = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
 constexpr int kAQThreads = 256;
@@ -79,6 +79,12 @@ constexpr int kAQThreads = 256;
 static_assert(kWBlocks % kStageK == 0, "stage geometry");
 static_assert(kOffB % 1024 == 0 && kOffW % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kTmemA + kTmemAStage * kStages <= kTmemCols, "TMEM budget");
+// Group scales: D (the integer sums of one group) at columns 0..63, F (the
+// fp32 running sums) at 64..127, two A stages at 128 + 64 s.
+constexpr int kStagesG = 2;
+constexpr uint32_t kTmemF = 64;
+constexpr uint32_t kTmemAG = 128;
+static_assert(kTmemAG + kTmemAStage * kStagesG <= kTmemCols, "TMEM budget (group scales)");
 
 struct MmaArgs {
     CUtensorMap tmW;        // packed weights [N][K/2] uint8, box 128 bytes x 128 rows
@@ -89,6 +95,11 @@ struct MmaArgs {
     int32_t* acc_out;       // optional [M][N]
     int32_t* part;          // [tiles][M][128] int32 accumulators when P > 1 (zeroed by the pre-pass)
     unsigned* tickets;      // [tiles] when P > 1, zero between calls
+    // group scales: sg [N][gld] fp32, gkb K blocks per group; fp32 partials
+    // [tiles][P][M][128] when P > 1
+    const float* sg;
+    float* part_f;
+    int gld, gkb;
     int M, N, K, BN, P, nkb, kbp;
 };
 
@@ -224,7 +235,18 @@ __device__ __forceinline__ uint4 int4x8_to_bf16(uint32_t w) {
 // Two CTAs per SM (shared memory < 113 KB, 256 TMEM columns, <= 93
 // registers): the SM's tensor core then interleaves two MMA streams, each at
 // the issue rate of one.
+//
+// kG: group-wise weight scales (groups of gkb K blocks, a whole number of
+// stages).  The MMAs of each group start a fresh accumulator D (exact
+// integer sums); when a group's last stage is committed (dfull), every
+// converter warp folds its share of D into fp32 running sums F in TMEM,
+// F += D * s_g with one fused multiply-add, and releases D (dfree) for the
+// next group.  A converter warp does the readout of a group before it
+// converts any later stage, so every wait points at earlier work.
+template <bool kG>
 __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_constant__ MmaArgs a) {
+    constexpr int S = kG ? kStagesG : kStages;          // stage ring in use
+    constexpr uint32_t kA0 = kG ? kTmemAG : kTmemA;     // first A stage column
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles
     const uint32_t raw = smem_u32(smem_raw);
@@ -249,7 +271,10 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
     uint64_t* bfull = afull + kStages;    // B stage landed
     uint64_t* sempty = bfull + kStages;   // stage consumed by the MMAs (commit)
     uint64_t* accfull = sempty + kStages;
+    uint64_t* dfull = accfull + 1;        // group scales: a group's sums are in D
+    uint64_t* dfree = dfull + 1;          // group scales: every converter warp has read D
     const int nst = (nk + kStageK - 1) / kStageK;  // stages of this piece
+    const int spg = kG ? a.gkb / kStageK : 1;      // stages per group
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
     int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
@@ -260,12 +285,14 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
             mbar_init(smem_u32(wfull + s), 1);
             mbar_init(smem_u32(wempty + s), 4 * (kWBlocks / kStageK));  // each stage read by 4 warps
         }
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(afull + s), 4);  // the 4 lane quarters of one group
             mbar_init(smem_u32(bfull + s), 1);
             mbar_init(smem_u32(sempty + s), 1);
         }
         mbar_init(smem_u32(accfull), 1);
+        mbar_init(smem_u32(dfull), 1);
+        mbar_init(smem_u32(dfree), kConvWarps);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -301,20 +328,28 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
         if (lane == 0) {
             const uint32_t idesc = bf16_idesc(kTileRows, BN);
             for (int st = 0; st < nst; ++st) {
-                const int s = st % kStages;
-                const uint32_t ph = (st / kStages) & 1;
+                const int s = st % S;
+                const uint32_t ph = (st / S) & 1;
+                // group scales: a group's first stage starts D afresh, once
+                // the converter warps have read the previous group's sums
+                const bool first = kG && (st % spg) == 0;
+                if (first && st > 0 && !wait_bounded(smem_u32(dfree), ((st / spg) - 1) & 1, abort_flag))
+                    break;
                 if (!wait_bounded(smem_u32(afull + s), ph, abort_flag)) break;
                 if (!wait_bounded(smem_u32(bfull + s), ph, abort_flag)) break;
                 tc_fence_after_sync();
                 const int nkb = min(kStageK, nk - kStageK * st);
-                const uint32_t at = tmem + kTmemA + kTmemAStage * s;
+                const uint32_t at = tmem + kA0 + kTmemAStage * s;
                 for (int j = 0; j < nkb; ++j) {
                     const uint64_t bd = sw128_desc(sbase + kOffB + s * kBStageMax + j * b_bytes);
                     #pragma unroll
-                    for (int k = 0; k < kKBlock / 16; ++k)  // 8 TMEM columns of A, 32 bytes of B a step
-                        tc_mma_bf16_tmem_a(tmem, at + 32 * j + 8 * k, bd + 2 * k, idesc, st > 0 || j > 0 || k > 0);
+                    for (int k = 0; k < kKBlock / 16; ++k) {  // 8 TMEM columns of A, 32 bytes of B a step
+                        const bool acc = kG ? !(first && j == 0 && k == 0) : (st > 0 || j > 0 || k > 0);
+                        tc_mma_bf16_tmem_a(tmem, at + 32 * j + 8 * k, bd + 2 * k, idesc, acc);
+                    }
                 }
                 tc_commit(smem_u32(sempty + s));
+                if (kG && (st % spg) == spg - 1) tc_commit(smem_u32(dfull));  // the group's D is complete
             }
             tc_commit(smem_u32(accfull));  // every MMA issued so far
         }
@@ -326,8 +361,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
             const uint64_t pol = l2_evict_last_policy();
             int issued = 0;
             for (int st = 0; st < nst; ++st) {
-                const int s = st % kStages;
-                if (st >= kStages && !wait_bounded(smem_u32(sempty + s), ((st / kStages) - 1) & 1, abort_flag))
+                const int s = st % S;
+                if (st >= S && !wait_bounded(smem_u32(sempty + s), ((st / S) - 1) & 1, abort_flag))
                     break;
                 const uint32_t bytes = (uint32_t)min(kStageK, nk - kStageK * st) * b_bytes;
                 mbar_arrive_expect_tx(smem_u32(bfull + s), bytes);
@@ -335,8 +370,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                          bytes, smem_u32(bfull + s), pol);
                 issued = st + 1;
             }
-            for (int st = max(0, issued - kStages); st < issued; ++st)
-                drain(smem_u32(bfull + st % kStages), (st / kStages) & 1);
+            for (int st = max(0, issued - S); st < issued; ++st)
+                drain(smem_u32(bfull + st % S), (st / S) & 1);
         }
     } else {
         // ---- converters: each thread widens its weight row's 64 codes of a
@@ -345,7 +380,44 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
         const int cg = (warp - kFirstConvWarp) >> 2;
         const int q = warp & 3;         // TMEM lanes 32q .. 32q + 31
         const int r = 32 * q + lane;    // weight row within the tile
+        const uint32_t lanes = tmem + ((uint32_t)(32 * q) << 16);
+        // group scales: fold group g's sums into F (this warp's lanes, its
+        // column chunks); false when a wait gave up
+        int next_g = 0;
+        const int ngroups = kG ? nst / spg : 0;
+        auto readout = [&](int g) -> bool {
+            const int n = n0 + r;
+            const float sc = n < a.N ? __ldg(a.sg + (int64_t)n * a.gld + kb0 / a.gkb + g) : 0.f;
+            if (!__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(dfull), g & 1, abort_flag))) return false;
+            tc_fence_after_sync();
+            for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
+                uint32_t d[8], f[8];
+                tmem_ld8(lanes + (uint32_t)(8 * ch), d);
+                if (g > 0) {
+                    tmem_ld8(lanes + kTmemF + (uint32_t)(8 * ch), f);
+                } else {
+                    #pragma unroll
+                    for (int t = 0; t < 8; ++t) f[t] = 0u;
+                }
+                #pragma unroll
+                for (int t = 0; t < 8; ++t)  // D holds an exact integer
+                    f[t] = __float_as_uint(__fmaf_rn(__uint_as_float(d[t]), sc, __uint_as_float(f[t])));
+                tmem_st8(lanes + kTmemF + (uint32_t)(8 * ch), f);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(dfree));
+            return true;
+        };
         for (int st = cg; st < nst; st += kConvGroups) {
+            if constexpr (kG) {  // groups that end before this stage
+                bool alive = true;
+                while (alive && next_g < ngroups && (next_g + 1) * spg - 1 < st) {
+                    alive = readout(next_g);
+                    if (alive) ++next_g;
+                }
+                if (!alive) break;
+            }
             const int kb = kStageK * st;  // first K block of the stage (within the piece)
             const int t = kb / kWBlocks, sub = kb % kWBlocks;
             const int ws = t % kWStages;
@@ -361,9 +433,9 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                 c16[c] = *reinterpret_cast<const uint4*>(row + (((2 * sub + c) ^ (r & 7)) << 4));
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(wempty + ws));
-            const int s = st % kStages;
-            if (st >= kStages &&
-                !__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(sempty + s), ((st / kStages) - 1) & 1, abort_flag)))
+            const int s = st % S;
+            if (st >= S &&
+                !__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(sempty + s), ((st / S) - 1) & 1, abort_flag)))
                 break;
             #pragma unroll
             for (int j = 0; j < kStageK; ++j) {  // word w of K block j = codes 8w .. 8w+7 -> columns 4w .. 4w+3
@@ -378,72 +450,118 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                     v[4 * w + 2] = o.z;
                     v[4 * w + 3] = o.w;
                 }
-                tmem_st32(tmem + ((uint32_t)(32 * q) << 16) + kTmemA + kTmemAStage * s + 32 * j, v);
+                tmem_st32(lanes + kA0 + kTmemAStage * s + 32 * j, v);
             }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(afull + s));
         }
 
-        // ---- epilogue: TMEM lanes = weight rows, columns = batch rows
-        griddep_wait();  // scales and outputs
-        const bool ok = __all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(accfull), 0, abort_flag));
-        tc_fence_after_sync();
-        // the TMEM lanes this warp may read are its converter lanes (q, r);
-        // the two warps of a quarter split the columns
-        const int ct = tid - kFirstConvWarp * 32;
-        const int n = n0 + r;
-        const float swv = (ok && n < a.N) ? a.sw[n] : 0.f;
-        for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
-            uint32_t v[8];
-            tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(8 * ch), v);
-            if (!ok || n >= a.N) continue;
-            #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int m = 8 * ch + t;
-                if (m >= a.M) break;
-                const int32_t acc = __float2int_rn(__uint_as_float(v[t]));
-                const int64_t o = (int64_t)m * a.N + n;
-                if (a.P == 1) {
-                    a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), swv), a.sa[m]);
-                    if (a.acc_out != nullptr) a.acc_out[o] = acc;
-                } else {
-                    atomicAdd(a.part + ((int64_t)tile * a.M + m) * kTileRows + r, acc);  // exact, order-free
+        if constexpr (kG) {
+            // ---- epilogue, group scales: the remaining groups, then
+            // Y = F * s_a, or this K piece's fp32 partials for the last CTA
+            while (next_g < ngroups && readout(next_g)) ++next_g;
+            griddep_wait();  // activation scales and outputs
+            const bool ok = __all_sync(0xFFFFFFFFu, next_g == ngroups);
+            tc_fence_after_sync();
+            const int ct = tid - kFirstConvWarp * 32;
+            const int n = n0 + r;
+            for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
+                uint32_t f[8];
+                tmem_ld8(lanes + kTmemF + (uint32_t)(8 * ch), f);
+                if (!ok || n >= a.N) continue;
+                #pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int m = 8 * ch + t;
+                    if (m >= a.M) break;
+                    const float v = __uint_as_float(f[t]);
+                    if (a.P == 1)
+                        a.Y[(int64_t)m * a.N + n] = __fmul_rn(v, a.sa[m]);
+                    else
+                        a.part_f[(((int64_t)tile * a.P + p) * a.M + m) * kTileRows + r] = v;
                 }
             }
-        }
-        if (a.P > 1) {
-            // the pieces' int32 sums were added atomically (integer addition
-            // is exact and order-free); the last CTA of the tile rescales them
-            __threadfence();
-            named_bar_sync(1, kConvWarps * 32);
-            if (ct == 0) *last_flag = (atomicAdd(a.tickets + tile, 1u) == (unsigned)(a.P - 1));
-            named_bar_sync(1, kConvWarps * 32);
-            if (*last_flag) {
+            if (a.P > 1) {
+                // the last CTA of the tile adds the pieces' partials in piece order
                 __threadfence();
-                const int rows = min(kTileRows, a.N - n0);
-                int32_t* acc_t = a.part + (int64_t)tile * a.M * kTileRows;
-                constexpr int kBatch = 8;  // loads in flight per thread
-                for (int e0 = ct; e0 < a.M * kTileRows; e0 += kConvWarps * 32 * kBatch) {
-                    int32_t v[kBatch];
-                    #pragma unroll
-                    for (int b = 0; b < kBatch; ++b) {
-                        const int e = e0 + b * kConvWarps * 32;
-                        v[b] = e < a.M * kTileRows ? __ldcg(acc_t + e) : 0;
-                    }
-                    #pragma unroll
-                    for (int b = 0; b < kBatch; ++b) {
-                        const int e = e0 + b * kConvWarps * 32;
-                        if (e >= a.M * kTileRows) break;
-                        __stcg(acc_t + e, 0);  // clear for the next matrix of a grouped call
-                        const int m = e / kTileRows, rr = e % kTileRows, nn = n0 + rr;
+                named_bar_sync(1, kConvWarps * 32);
+                if (ct == 0) *last_flag = (atomicAdd(a.tickets + tile, 1u) == (unsigned)(a.P - 1));
+                named_bar_sync(1, kConvWarps * 32);
+                if (*last_flag) {
+                    __threadfence();
+                    const int rows = min(kTileRows, a.N - n0);
+                    for (int e = ct; e < a.M * kTileRows; e += kConvWarps * 32) {
+                        const int m = e / kTileRows, rr = e % kTileRows;
                         if (rr >= rows) continue;
-                        const int64_t o = (int64_t)m * a.N + nn;
-                        a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(v[b]), a.sw[nn]), a.sa[m]);
-                        if (a.acc_out != nullptr) a.acc_out[o] = v[b];
+                        float t = 0.f;
+                        for (int pp = 0; pp < a.P; ++pp)
+                            t += __ldcg(a.part_f + (((int64_t)tile * a.P + pp) * a.M + m) * kTileRows + rr);
+                        a.Y[(int64_t)m * a.N + n0 + rr] = __fmul_rn(t, a.sa[m]);
+                    }
+                    if (ct == 0) a.tickets[tile] = 0u;  // ready for the next call
+                }
+            }
+        } else {
+            // ---- epilogue: TMEM lanes = weight rows, columns = batch rows
+            griddep_wait();  // scales and outputs
+            const bool ok = __all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(accfull), 0, abort_flag));
+            tc_fence_after_sync();
+            // the TMEM lanes this warp may read are its converter lanes (q, r);
+            // the two warps of a quarter split the columns
+            const int ct = tid - kFirstConvWarp * 32;
+            const int n = n0 + r;
+            const float swv = (ok && n < a.N) ? a.sw[n] : 0.f;
+            for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
+                uint32_t v[8];
+                tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(8 * ch), v);
+                if (!ok || n >= a.N) continue;
+                #pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int m = 8 * ch + t;
+                    if (m >= a.M) break;
+                    const int32_t acc = __float2int_rn(__uint_as_float(v[t]));
+                    const int64_t o = (int64_t)m * a.N + n;
+                    if (a.P == 1) {
+                        a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), swv), a.sa[m]);
+                        if (a.acc_out != nullptr) a.acc_out[o] = acc;
+                    } else {
+                        atomicAdd(a.part + ((int64_t)tile * a.M + m) * kTileRows + r, acc);  // exact, order-free
                     }
                 }
-                if (ct == 0) a.tickets[tile] = 0u;  // ready for the next call
+            }
+            if (a.P > 1) {
+                // the pieces' int32 sums were added atomically (integer addition
+                // is exact and order-free); the last CTA of the tile rescales them
+                __threadfence();
+                named_bar_sync(1, kConvWarps * 32);
+                if (ct == 0) *last_flag = (atomicAdd(a.tickets + tile, 1u) == (unsigned)(a.P - 1));
+                named_bar_sync(1, kConvWarps * 32);
+                if (*last_flag) {
+                    __threadfence();
+                    const int rows = min(kTileRows, a.N - n0);
+                    int32_t* acc_t = a.part + (int64_t)tile * a.M * kTileRows;
+                    constexpr int kBatch = 8;  // loads in flight per thread
+                    for (int e0 = ct; e0 < a.M * kTileRows; e0 += kConvWarps * 32 * kBatch) {
+                        int32_t v[kBatch];
+                        #pragma unroll
+                        for (int b = 0; b < kBatch; ++b) {
+                            const int e = e0 + b * kConvWarps * 32;
+                            v[b] = e < a.M * kTileRows ? __ldcg(acc_t + e) : 0;
+                        }
+                        #pragma unroll
+                        for (int b = 0; b < kBatch; ++b) {
+                            const int e = e0 + b * kConvWarps * 32;
+                            if (e >= a.M * kTileRows) break;
+                            __stcg(acc_t + e, 0);  // clear for the next matrix of a grouped call
+                            const int m = e / kTileRows, rr = e % kTileRows, nn = n0 + rr;
+                            if (rr >= rows) continue;
+                            const int64_t o = (int64_t)m * a.N + nn;
+                            a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(v[b]), a.sw[nn]), a.sa[m]);
+                            if (a.acc_out != nullptr) a.acc_out[o] = v[b];
+                        }
+                    }
+                    if (ct == 0) a.tickets[tile] = 0u;  // ready for the next call
+                }
             }
         }
     }
@@ -507,8 +625,12 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
 
 }  // namespace
 
-bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out) {
+bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int gkb) {
     if (M < 1 || M > 64 || K < 32 || K % 32 || N < 1 || N > 0x7FFFFFFF) return false;
+    // group scales: groups of gkb K blocks, whole stages, each group's sums
+    // exact in fp32 (at most 256 K blocks)
+    if (gkb != 0 && (gkb < kStageK || gkb % kStageK || gkb > 256 || K % ((int64_t)gkb * kKBlock)))
+        return false;
     MmaPlan pl = {};
     pl.BN = (M + 15) / 16 * 16;
     pl.tiles = (int)((N + kTileRows - 1) / kTileRows);
@@ -519,15 +641,18 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out) {
     const int slots = 2 * num_sms;  // resident CTAs
     if (pl.tiles < slots * 4 / 5) P = slots / pl.tiles;
     if (P < 1) P = 1;
-    const int pmin = (pl.nkb + 255) / 256;
+    // row-wise scales: pieces of at most 256 K blocks keep the integer sums
+    // exact; group scales: each group's D is exact on its own
+    const int pmin = gkb ? 1 : (pl.nkb + 255) / 256;
     if (P < pmin) P = pmin;
     if (P > pl.nkb) P = pl.nkb;
     if (P > 64) P = 64;
-    // pieces of whole weight loads (kWBlocks K blocks), none empty
+    // pieces of whole weight loads (kWBlocks K blocks) and whole groups, none empty
+    const int align = gkb > kWBlocks ? gkb : kWBlocks;
     pl.kbp = (pl.nkb + P - 1) / P;
-    pl.kbp = (pl.kbp + kWBlocks - 1) / kWBlocks * kWBlocks;
+    pl.kbp = (pl.kbp + align - 1) / align * align;
     pl.P = (pl.nkb + pl.kbp - 1) / pl.kbp;
-    if (pl.kbp > 256) return false;
+    if (!gkb && pl.kbp > 256) return false;
     if (pl.P > 1 && pl.tiles > kTicketSlots) return false;
     if ((int64_t)pl.tiles * pl.P > 0x7FFFFFFF) return false;
     pl.grid = pl.tiles * pl.P;
@@ -545,7 +670,10 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out) {
     pl.off_part = round_up_sz(pl.off_codes + (size_t)pl.nkb * pl.BN * kKBlock * 2, 256);
     const int64_t small = 2 * num_sms * 4 / 5;
     const int64_t tmax = pmin > 1 ? pl.tiles : (pl.tiles < small ? pl.tiles : small);
-    pl.ws_bytes = pl.off_part + round_up_sz((size_t)tmax * M * kTileRows * 4, 256);
+    // group scales: fp32 partials per tile and piece; a matrix split into
+    // P pieces has tiles * P <= the 2 * SMs CTA slots
+    const size_t part = gkb ? (size_t)(2 * num_sms) * M * kTileRows * 4 : (size_t)tmax * M * kTileRows * 4;
+    pl.ws_bytes = pl.off_part + round_up_sz(part, 256);
     *out = pl;
     return true;
 }
@@ -554,7 +682,8 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
                             int M, int64_t K, int G, const uint8_t* const* Wq,
                             const float* const* sw, const int64_t* Ns, float* const* Y,
                             int32_t* acc_out, int8_t* Xq_out, float* sa_out, void* ws,
-                            unsigned flags, cudaStream_t stream) {
+                            unsigned flags, cudaStream_t stream, int gs, const float* const* sg) {
+    const int gkb = gs > 0 ? gs / kKBlock : 0;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     float* sa_ws = reinterpret_cast<float*>(wsb + pl.off_sa);
     uint8_t* codes = wsb + pl.off_codes;
@@ -575,20 +704,28 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+        e = cudaFuncSetAttribute(mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = 1;
     }
     for (int g = 0; g < G; ++g) {
         MmaPlan pg;
-        if (!make_mma_plan(M, K, Ns[g], pl.sms, &pg)) return cudaErrorInvalidValue;
+        if (!make_mma_plan(M, K, Ns[g], pl.sms, &pg, gkb)) return cudaErrorInvalidValue;
         MmaArgs a;
         memset(&a, 0, sizeof(a));
         if (!encode_2d(&a.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq[g], (uint64_t)(K / 2), (uint64_t)Ns[g],
                        (uint64_t)(K / 2), kWBlocks * kKBlock / 2, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         a.codes = codes;
-        a.sw = sw[g];
+        a.sw = sw ? sw[g] : nullptr;
+        if (gkb) {
+            a.sg = sg[g];
+            a.gld = (int)((K / gs + 3) / 4 * 4);
+            a.gkb = gkb;
+            a.part_f = reinterpret_cast<float*>(wsb + pg.off_part);
+        }
         a.sa = sa_ws;
         a.Y = Y[g];
         a.acc_out = (G == 1) ? acc_out : nullptr;
@@ -602,7 +739,9 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
         a.nkb = pg.nkb;
         a.kbp = pg.kbp;
         void* args[] = {&a};
-        e = launch_pdl(reinterpret_cast<const void*>(mma_kernel), dim3(pg.grid), dim3(kMmaThreads),
+        const void* fn = gkb ? reinterpret_cast<const void*>(mma_kernel<true>)
+                             : reinterpret_cast<const void*>(mma_kernel<false>);
+        e = launch_pdl(fn, dim3(pg.grid), dim3(kMmaThreads),
                        kMmaSmem, stream, flags, args);
         if (e != cudaSuccess) return e;
     }

@@ -226,7 +226,7 @@ def test_group_plan_windows(sms, splits):
     and ends on 16-byte words inside the padded scale row, and the slot's
     scale area holds a whole stage of rows."""
     try:
-        w4.w4a8_set_tuning(force_splits=splits)
+        w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65)  # the dp4a kernel's plans
         for (M, K, N, gs) in GROUP_SHAPES:
             if splits and splits > K // 32:
                 continue
@@ -294,3 +294,33 @@ def test_isx_argument_checks(L):
     assert L.index_softmax_u8(P16, 1, 8, 100, 9, lp, P16, None) == E_S
     assert L.index_softmax_u8(P16, 1, 8, 100, 5, ctypes.cast(zero_lut, ctypes.c_void_p), P16, None) == E_S
     assert L.index_softmax_u8(P16 + 2, 1, 8, 100, 5, lp, P16, None) == E_A
+
+
+def test_group_tensor_core_plans():
+    """Group scales with 3..64 rows take the tensor cores when the group is a
+    whole number of 128-code stages (at most 16384 codes); the K pieces then
+    hold whole groups and whole weight loads, and the workspace covers the
+    fp32 partials of every piece."""
+    try:
+        for sms in (152, 148, 20):
+            for (M, K, N, gs) in [(3, 3584, 300, 128), (16, 3584, 18944, 128), (64, 18944, 3584, 128),
+                                  (4, 3584, 1000, 256), (8, 2048, 200, 512), (33, 896, 100, 128),
+                                  (5, 32768, 64, 16384)]:
+                p = w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)
+                assert p["tensor_cores"] == 1, (M, K, N, gs)
+                nkb = K // 64
+                P = p["splits"]
+                kbp = -(-nkb // P)
+                align = max(4, gs // 64)
+                # the plan's pieces: kbp rounded up to whole groups and loads
+                kbp_al = -(-kbp // align) * align
+                assert -(-nkb // kbp_al) == P or P == 1
+                assert p["grid"] == p["ctas_per_split"] * P
+                if P > 1:
+                    assert p["ws_bytes"] >= 4096 + 256 + M * K * 2 + p["grid"] * M * 128 * 4
+            for (M, K, N, gs) in [(3, 1024, 77, 32), (8, 3584, 100, 64), (2, 3584, 100, 128)]:
+                assert w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)["tensor_cores"] == 0
+        w4.w4a8_set_tuning(mma_min_m=65)
+        assert w4.w4a8g_plan_info(16, 3584, 18944, 128, num_sms=152)["tensor_cores"] == 0
+    finally:
+        w4.w4a8_set_tuning(reset=True)

@@ -131,14 +131,77 @@ GROUP_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("path", ["default", "dp4a"])
 @pytest.mark.parametrize("M,K,N,gs,seed", GROUP_SHAPES)
-def test_w4a8g_linear(w4, orc, M, K, N, gs, seed):
+def test_w4a8g_linear(w4, orc, M, K, N, gs, seed, path):
+    if path == "dp4a":
+        w4.w4a8_set_tuning(mma_min_m=65)
     check_group(w4, orc, M, K, N, gs, seed, fused=True)
 
 
+@pytest.mark.parametrize("path", ["default", "dp4a"])
 @pytest.mark.parametrize("M,K,N,gs,seed", GROUP_SHAPES[:6] + GROUP_SHAPES[-2:])
-def test_w4a8g_gemv_unfused(w4, orc, M, K, N, gs, seed):
+def test_w4a8g_gemv_unfused(w4, orc, M, K, N, gs, seed, path):
+    if path == "dp4a":
+        w4.w4a8_set_tuning(mma_min_m=65)
     check_group(w4, orc, M, K, N, gs, seed, fused=False)
+
+
+# the tensor-core path: groups of whole 128-code stages, 3..64 rows; small N
+# splits K into many pieces (fp32 partials summed by the last CTA)
+MMA_GROUP_SHAPES = [
+    (3, 3584, 300, 128, 90), (16, 3584, 1000, 128, 91), (64, 896, 129, 128, 92),
+    (33, 2048, 257, 256, 93), (8, 18944, 200, 128, 94), (5, 4096, 64, 4096, 95),
+    (24, 1024, 4096, 512, 96),
+]
+
+
+@pytest.mark.parametrize("M,K,N,gs,seed", MMA_GROUP_SHAPES)
+@pytest.mark.parametrize("fused", [True, False])
+def test_w4a8g_tensor_cores(w4, orc, M, K, N, gs, seed, fused):
+    assert w4.w4a8g_plan_info(M, K, N, gs)["tensor_cores"] == 1
+    check_group(w4, orc, M, K, N, gs, seed, fused=fused)
+
+
+@pytest.mark.parametrize("M,N", [(3, 300), (16, 5000), (64, 96)])
+def test_w4a8g_tensor_cores_exact(w4, orc, M, N):
+    """Power-of-two group scales and integer activations on the tensor cores:
+    each group's sums are exact in D and every fold is exact, so Y equals the
+    oracle bit for bit (small N: many K pieces and their fp32 partials)."""
+    K, gs = 1024, 128
+    rng = np.random.Generator(np.random.PCG64(78 + M))
+    G = K // gs
+    q = rng.integers(-7, 8, size=(N, G, gs))
+    q[:, :, 0] = 7 * rng.choice([-1, 1], size=(N, G))
+    e = rng.integers(0, 4, size=(N, G, 1))
+    W = (q * 2.0 ** -e).reshape(N, K).astype(np.float32)
+    X = rng.integers(-126, 127, size=(M, K)).astype(np.float16)
+    X[:, 5] = 127
+    Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
+    Y_ref, _, _, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
+    assert np.all(sa_ref == 1.0)
+    assert w4.w4a8g_plan_info(M, K, N, gs)["tensor_cores"] == 1
+    Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
+    Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs)
+    torch.cuda.synchronize()
+    assert np.array_equal(Y.cpu().numpy().astype(np.float64), Y_ref)
+
+
+def test_w4a8g_tensor_cores_grouped(w4, orc):
+    M, K, gs, Ns = 8, 3584, 128, [3584, 512, 512]
+    X = synth.activation(97, M, K, outlier_frac=0.001)
+    Wqs, sgs, refs = [], [], []
+    for g, N in enumerate(Ns):
+        W = synth.normal(180 + g, (N, K), 0.02)
+        Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
+        refs.append(orc.w4a8g_linear(X, Wq_ref, sg_ref, gs))
+        Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
+        Wqs.append(Wq)
+        sgs.append(sg)
+    Ys = w4.w4a8g_linear_grouped(to_dev(X), Wqs, sgs, gs, flags=w4.LAUNCH_PDL)
+    torch.cuda.synchronize()
+    for Y, (Y_ref, B, _, _) in zip(Ys, refs):
+        assert_within_bound(Y.cpu().numpy(), Y_ref, B, K)
 
 
 @pytest.mark.parametrize("splits", [2, 3, 5, 16])
