@@ -699,11 +699,30 @@ def measure_group_set(torch, w4, synth, dev, stream, lin, gs=GROUP_SIZE):
     us_lm = _graph_us(torch, stream, lambda: [launch(k % 2, jl, w4.LAUNCH_PDL) for k in range(20)], 20)
     _, K_lm, N_lm = LINEARS[names.index("lm_head")]
     lm_bytes = N_lm * (K_lm // 2 + 4 * w4.w4g_scale_stride(K_lm, gs))
+    # batches on gate and down (3..64 rows take the tensor cores)
+    skinny = {}
+    for name in ("gate", "down"):
+        i = names.index(name)
+        _, K, N = LINEARS[i]
+        res = {}
+        for M in (1, 4, 16, 64):
+            X = torch.from_numpy(synth.activation(WEIGHT_SEED0 + i + ACT_SEED_OFFSET, M, K,
+                                                  outlier_frac=OUTLIER_FRAC)).to(dev)
+            Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            wsm = torch.zeros(max(w4.w4a8g_workspace_bytes(M, K, N, gs), 4096), dtype=torch.uint8,
+                              device=dev)
+            us_m = _graph_us(torch, stream, lambda: [w4.w4a8g_linear(X, copies[k % 2][0][i], copies[k % 2][1][i],
+                                                                     gs, Y=Y, ws=wsm, flags=w4.LAUNCH_PDL)
+                                                     for k in range(10)], 10)
+            nb = N * (K // 2 + 4 * w4.w4g_scale_stride(K, gs))
+            res[str(M)] = {"us": round(us_m, 2), "GBps": round(nb / us_m / 1e3, 1)}
+        skinny[name] = res
     del copies
     return {"workload": "the M=1 set above with group-wise INT4 scales, group %d" % gs,
             "weight_bytes": nbytes, "us_per_set": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
             "lm_head_in_chain": {"us": round(us_lm, 2), "GBps": round(lm_bytes / us_lm / 1e3, 1),
-                                 "how": "graph of 20 back-to-back launches, PDL, two weight copies"}}
+                                 "how": "graph of 20 back-to-back launches, PDL, two weight copies"},
+            "skinny_batch": skinny}
 
 
 ISX_HEADS, ISX_QUERIES, ISX_KEYS = 32, 1024, 4096
