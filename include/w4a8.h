@@ -240,10 +240,14 @@ size_t w4a8g_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t group);
  *   Wq [N][K/2] uint8, sg [N][stride] fp32   (w4g_quantize_weights)
  *   Y [M][N] fp32 out; ws, ws_bytes (w4a8g_workspace_bytes) and flags as
  *   in w4a8_gemv.
- * Requires 1 <= M <= W4A8_MAX_M (one launch per group of up to 8 rows, on
- * the dp4a kernel; the tensor-core kernel does not take group scales),
- * the w4a8_gemv limits on K and N, the group rule above; Xq, Wq and sg
- * 16-byte aligned; Y and sa 4-byte aligned. */
+ * Calls with at least 3 rows (w4a8_tuning_t.mma_min_m) and a group of a
+ * multiple of 128 codes up to 16384 run on the tensor cores: each group's
+ * products are summed exactly in an fp32 TMEM accumulator, multiplied by
+ * the group scale and added into fp32 running sums with one fused
+ * multiply-add (the same bound holds); K pieces are added in a fixed order.
+ * Other calls run on the dp4a kernel, one launch per group of up to 8 rows.
+ * Requires 1 <= M <= W4A8_MAX_M, the w4a8_gemv limits on K and N, the group
+ * rule above; Xq, Wq and sg 16-byte aligned; Y and sa 4-byte aligned. */
 int w4a8g_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, int64_t group,
                const uint8_t* Wq, const float* sg, int64_t N, float* Y, void* ws,
                size_t ws_bytes, unsigned flags, void* stream);
