@@ -71,7 +71,7 @@ constexpr uint32_t kTmemAStage = 32 * kStageK;  // two bf16 per column
 constexpr int kOffB = 0;
 constexpr int kOffW = kOffB + kStages * kBStageMax;
 constexpr int kOffBars = kOffW + kWStages * kWTileBytes;
-constexpr int kNumBars = 2 * kWStages + 3 * kStages + 3;  // + accfull, dfull, dfree
+constexpr int kNumBars = 2 * kWStages + 3 * kStages + 5;  // + accfull, dfull[2], dfree[2]
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kMmaSmem = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
 constexpr int kAQThreads = 256;
@@ -79,8 +79,9 @@ constexpr int kAQThreads = 256;
 static_assert(kWBlocks % kStageK == 0, "stage geometry");
 static_assert(kOffB % 1024 == 0 && kOffW % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kTmemA + kTmemAStage * kStages <= kTmemCols, "TMEM budget");
-// Group scales: D (the integer sums of one group) at columns 0..63, F (the
-// fp32 running sums) at 64..127, two A stages at 128 + 64 s.
+// Group scales: D (the integer sums of one group) at columns 0..63 -- two
+// buffers of 32 columns when the batch has at most 32 rows --, F (the fp32
+// running sums) at 64..127, two A stages at 128 + 64 s.
 constexpr int kStagesG = 2;
 constexpr uint32_t kTmemF = 64;
 constexpr uint32_t kTmemAG = 128;
@@ -242,7 +243,8 @@ __device__ __forceinline__ uint4 int4x8_to_bf16(uint32_t w) {
 // converter warp folds its share of D into fp32 running sums F in TMEM,
 // F += D * s_g with one fused multiply-add, and releases D (dfree) for the
 // next group.  A converter warp does the readout of a group before it
-// converts any later stage, so every wait points at earlier work.
+// converts the stage `lag` stages past the group's end, so every wait
+// points at earlier work.
 template <bool kG>
 __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_constant__ MmaArgs a) {
     constexpr int S = kG ? kStagesG : kStages;          // stage ring in use
@@ -271,10 +273,18 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
     uint64_t* bfull = afull + kStages;    // B stage landed
     uint64_t* sempty = bfull + kStages;   // stage consumed by the MMAs (commit)
     uint64_t* accfull = sempty + kStages;
-    uint64_t* dfull = accfull + 1;        // group scales: a group's sums are in D
-    uint64_t* dfree = dfull + 1;          // group scales: every converter warp has read D
+    uint64_t* dfull = accfull + 1;        // group scales [buffer]: a group's sums are in D
+    uint64_t* dfree = dfull + 2;          // group scales [buffer]: every converter warp has read D
     const int nst = (nk + kStageK - 1) / kStageK;  // stages of this piece
     const int spg = kG ? a.gkb / kStageK : 1;      // stages per group
+    // group g uses D buffer g % nbuf (columns 32 (g % nbuf)); buffer b
+    // completes dfull[b] / dfree[b] phase g / nbuf.  The converter warps read
+    // group g out before converting stage last(g) + lag: with two buffers a
+    // stage later, so that a conversion never waits for the MMAs of the stage
+    // just before it (the next group's MMAs wait only for the readout of the
+    // group before the previous one).
+    const int nbuf = (kG && BN <= 32) ? 2 : 1;
+    const int lag = nbuf;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
     int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
@@ -291,8 +301,10 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
             mbar_init(smem_u32(sempty + s), 1);
         }
         mbar_init(smem_u32(accfull), 1);
-        mbar_init(smem_u32(dfull), 1);
-        mbar_init(smem_u32(dfree), kConvWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(dfull + b), 1);
+            mbar_init(smem_u32(dfree + b), kConvWarps);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -333,8 +345,11 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                 // group scales: a group's first stage starts D afresh, once
                 // the converter warps have read the previous group's sums
                 const bool first = kG && (st % spg) == 0;
-                if (first && st > 0 && !wait_bounded(smem_u32(dfree), ((st / spg) - 1) & 1, abort_flag))
+                const int g = kG ? st / spg : 0;
+                if (first && g >= nbuf &&
+                    !wait_bounded(smem_u32(dfree + g % nbuf), ((g / nbuf) - 1) & 1, abort_flag))
                     break;
+                const uint32_t d_tmem = tmem + (uint32_t)(32 * (g % nbuf));
                 if (!wait_bounded(smem_u32(afull + s), ph, abort_flag)) break;
                 if (!wait_bounded(smem_u32(bfull + s), ph, abort_flag)) break;
                 tc_fence_after_sync();
@@ -345,11 +360,11 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                     #pragma unroll
                     for (int k = 0; k < kKBlock / 16; ++k) {  // 8 TMEM columns of A, 32 bytes of B a step
                         const bool acc = kG ? !(first && j == 0 && k == 0) : (st > 0 || j > 0 || k > 0);
-                        tc_mma_bf16_tmem_a(tmem, at + 32 * j + 8 * k, bd + 2 * k, idesc, acc);
+                        tc_mma_bf16_tmem_a(d_tmem, at + 32 * j + 8 * k, bd + 2 * k, idesc, acc);
                     }
                 }
                 tc_commit(smem_u32(sempty + s));
-                if (kG && (st % spg) == spg - 1) tc_commit(smem_u32(dfull));  // the group's D is complete
+                if (kG && (st % spg) == spg - 1) tc_commit(smem_u32(dfull + g % nbuf));  // the group's D is complete
             }
             tc_commit(smem_u32(accfull));  // every MMA issued so far
         }
@@ -388,11 +403,13 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
         auto readout = [&](int g) -> bool {
             const int n = n0 + r;
             const float sc = n < a.N ? __ldg(a.sg + (int64_t)n * a.gld + kb0 / a.gkb + g) : 0.f;
-            if (!__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(dfull), g & 1, abort_flag))) return false;
+            const int b = g % nbuf;
+            if (!__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(dfull + b), (g / nbuf) & 1, abort_flag)))
+                return false;
             tc_fence_after_sync();
             for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
                 uint32_t d[8], f[8];
-                tmem_ld8(lanes + (uint32_t)(8 * ch), d);
+                tmem_ld8(lanes + (uint32_t)(32 * b + 8 * ch), d);
                 if (g > 0) {
                     tmem_ld8(lanes + kTmemF + (uint32_t)(8 * ch), f);
                 } else {
@@ -406,13 +423,13 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(dfree));
+            if (lane == 0) mbar_arrive(smem_u32(dfree + b));
             return true;
         };
         for (int st = cg; st < nst; st += kConvGroups) {
             if constexpr (kG) {  // groups that end before this stage
                 bool alive = true;
-                while (alive && next_g < ngroups && (next_g + 1) * spg - 1 < st) {
+                while (alive && next_g < ngroups && (next_g + 1) * spg - 1 + lag <= st) {
                     alive = readout(next_g);
                     if (alive) ++next_g;
                 }
