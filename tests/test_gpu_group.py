@@ -342,3 +342,14 @@ def test_w4a8g_qwen2_fullsize(w4, orc, li):
         assert np.array_equal(bits(sgs[g][idx].cpu().numpy()), bits(sg_ref))
         Y_ref, B, _, _ = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
         assert_within_bound(Ys[g].cpu().numpy()[:, rows], Y_ref, B, K)
+
+
+@pytest.mark.parametrize("M,K,N,gs,seed", [
+    (1, 131072, 5, 128, 110),     # longest rows, dp4a
+    (2, 131072, 3, 32, 111),      # longest rows, smallest groups, dp4a
+    (5, 131072, 7, 1024, 112),    # longest rows on the tensor cores
+    (4, 131072, 1, 16384, 113),   # largest tensor-core group, one output row
+    (1, 3584, 1, 128, 114),       # one output row
+])
+def test_w4a8g_maximum_sizes(w4, orc, M, K, N, gs, seed):
+    check_group(w4, orc, M, K, N, gs, seed)

@@ -145,3 +145,14 @@ def test_isx_attention_shape_sampled(w4, orc):
     assert np.array_equal(A[idx].cpu().numpy(), A_rows)
     P_ref = orc.index_softmax(A_rows, c_int)
     assert np.array_equal(P[idx].cpu().numpy(), P_ref)
+
+
+def test_isx_longest_rows(w4, orc):
+    """Rows of ISX_MAX_COLS = 2^23 logits (streaming path): a seeded row, and a
+    row of equal logits whose sum reaches 255 * 2^23, the largest the int32
+    row sum has to hold."""
+    cols = 1 << 23
+    c_int = orc.isx_c_int(6.6, 128, S_QK, S_QK)
+    A = np.concatenate([logits(120, 1, cols), np.full((1, cols), -5, np.int32)])
+    P = check(w4, orc, A, c_int)
+    assert not P[1].any()  # 255 * 255 / (255 * 2^23) rounds to 0
