@@ -46,6 +46,10 @@ std::atomic<int> g_force_cl{0};
 std::atomic<int> g_ring_bytes{0};
 std::atomic<int> g_ctas_per_sm{0};
 std::atomic<int> g_mma_min_m{0};
+std::atomic<int> g_rowdot_max_m{0};
+// Batch rows up to which row-wise W4A8 calls take the row-per-thread dp4a
+// kernel (from 2 rows).
+constexpr int kDefaultRowdotMaxM = 8;
 // Batch rows from which the W4A8 entry points take the tensor-core kernel
 // (measured on GB300: dp4a is faster at 1-2 rows, the tensor cores from 3).
 constexpr int kDefaultMmaMinM = 3;
@@ -118,6 +122,26 @@ bool mma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::MmaPlan* pl, int sms = 
     if (group > 0 && (group % 128 || group > 16384)) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
     return w4a8::make_mma_plan((int)M, K, N, sms, pl, (int)(group / 64));
+}
+
+// Row-per-thread plan for an M-row W4A8 call with row-wise scales, or false
+// when another kernel serves it.
+bool rowdot_plan_for(int64_t M, int64_t K, int64_t N, w4a8::RowdotPlan* pl, int sms = 0) {
+    const int t = g_rowdot_max_m.load();
+    const int hi = t > 0 ? t : kDefaultRowdotMaxM;
+    if (M < 2 || M > hi) return false;
+    if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
+    const int cl = g_force_cl.load();
+    return w4a8::make_rowdot_plan((int)M, K, N, sms, pl, (cl == 2 || cl == 4) ? cl : 0,
+                                  g_ctas_per_sm.load());
+}
+
+int check_ws(size_t need, void* ws, size_t ws_bytes) {
+    if (ws == nullptr || ws_bytes < need)
+        return fail(W4A8_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given%s", need,
+                    ws ? ws_bytes : (size_t)0, ws ? "" : " (NULL)");
+    if (!aligned(ws, 256)) return fail(W4A8_ERR_ALIGN, "workspace must be 256-byte aligned");
+    return W4A8_OK;
 }
 
 int check_mma_workspace(const w4a8::MmaPlan& pl, void* ws, size_t ws_bytes) {
@@ -203,6 +227,8 @@ int act_quantize_i8(const uint16_t* X, int64_t M, int64_t K, int8_t* Xq, float* 
 
 size_t w4a8_workspace_bytes(int64_t M, int64_t K, int64_t N) {
     if (check_w4a8_shape(M, K, N) != W4A8_OK) return 0;
+    w4a8::RowdotPlan rp;
+    if (rowdot_plan_for(M, K, N, &rp)) return rp.ws_bytes;
     w4a8::MmaPlan mp;
     if (mma_plan_for(M, K, N, &mp)) return mp.ws_bytes;
     w4a8::GemvPlan pf, pt;
@@ -254,6 +280,14 @@ int w4a8_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, const uin
     if (!aligned(Xq, 16) || !aligned(Wq, 16) || !aligned(Y, 4) || !aligned(sw, 4) ||
         !aligned(sa, 4) || (acc_out && !aligned(acc_out, 4)))
         return fail(W4A8_ERR_ALIGN, "w4a8_gemv: Xq/Wq need 16-byte, Y/sw/sa/acc_out 4-byte alignment");
+    w4a8::RowdotPlan rp;
+    if (rowdot_plan_for(M, K, N, &rp)) {
+        if ((st = check_ws(rp.ws_bytes, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_rowdot(rp, nullptr, Xq, sa, (int)M, K, 1, &Wq, &sw, &N, &Y,
+                                                 acc_out, nullptr, nullptr, ws, flags,
+                                                 static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_gemv row-per-thread launch");
+    }
     w4a8::MmaPlan mp;
     if (mma_plan_for(M, K, N, &mp)) {
         if ((st = check_mma_workspace(mp, ws, ws_bytes)) != W4A8_OK) return st;
@@ -288,6 +322,14 @@ int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, cons
         (Xq_out && !aligned(Xq_out, 16)) || (sa_out && !aligned(sa_out, 4)) ||
         (acc_out && !aligned(acc_out, 4)))
         return fail(W4A8_ERR_ALIGN, "w4a8_linear: X/Wq/Xq_out need 16-byte, Y/sw/sa_out/acc_out 4-byte alignment");
+    w4a8::RowdotPlan rp;
+    if (rowdot_plan_for(M, K, N, &rp)) {
+        if ((st = check_ws(rp.ws_bytes, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_rowdot(rp, X, nullptr, nullptr, (int)M, K, 1, &Wq, &sw, &N,
+                                                 &Y, acc_out, Xq_out, sa_out, ws, flags,
+                                                 static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear row-per-thread launch");
+    }
     w4a8::MmaPlan mp;
     if (mma_plan_for(M, K, N, &mp)) {
         if ((st = check_mma_workspace(mp, ws, ws_bytes)) != W4A8_OK) return st;
@@ -330,6 +372,21 @@ int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const ui
     int st = check_w4a8_shape(M, K, total);
     if (st != W4A8_OK) return st;
     if (!aligned(X, 16)) return fail(W4A8_ERR_ALIGN, "w4a8_linear_grouped: X needs 16-byte alignment");
+    w4a8::RowdotPlan rp;
+    if (rowdot_plan_for(M, K, total, &rp)) {
+        // one plan per matrix inside; the workspace bound covers every N[g] <= total
+        for (int g = 0; g < G; ++g) {
+            w4a8::RowdotPlan pg;
+            if (!w4a8::make_rowdot_plan((int)M, K, N[g], rp.sms, &pg, rp.tpr, rp.cps) ||
+                pg.ws_bytes > rp.ws_bytes)
+                return fail(W4A8_ERR_SHAPE, "no row-per-thread plan for group %d", g);
+        }
+        if ((st = check_ws(rp.ws_bytes, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_rowdot(rp, X, nullptr, nullptr, (int)M, K, G, Wq, sw, N, Y,
+                                                 nullptr, nullptr, nullptr, ws, flags,
+                                                 static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear_grouped row-per-thread launch");
+    }
     w4a8::MmaPlan mp;
     if (mma_plan_for(M, K, total, &mp)) {
         // one plan per matrix inside; the workspace bound covers every N[g] <= total
@@ -511,6 +568,7 @@ int w4a8_device_error(unsigned* flags, void* stream) {
     cudaError_t e = w4a8::read_and_clear_device_error(flags, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = w4a8::read_and_clear_mma_error(flags, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = w4a8::read_and_clear_group_error(flags, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = w4a8::read_and_clear_rowdot_error(flags, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_device_error");
 }
 
@@ -521,6 +579,7 @@ int w4a8_set_tuning(const w4a8_tuning_t* t) {
         g_ring_bytes = 0;
         g_ctas_per_sm = 0;
         g_mma_min_m = 0;
+        g_rowdot_max_m = 0;
         return ok();
     }
     if (t->force_splits < 0 || t->force_splits > 16)
@@ -537,8 +596,11 @@ int w4a8_set_tuning(const w4a8_tuning_t* t) {
     g_ring_bytes = t->ring_bytes;
     if (t->mma_min_m != 0 && (t->mma_min_m < 2 || t->mma_min_m > 65))
         return fail(W4A8_ERR_SHAPE, "mma_min_m must be 0 or in [2, 65]");
+    if (t->rowdot_max_m < 0 || t->rowdot_max_m > w4a8::kRowdotMaxM)
+        return fail(W4A8_ERR_SHAPE, "rowdot_max_m must be in [0, %d]", w4a8::kRowdotMaxM);
     g_ctas_per_sm = t->ctas_per_sm;
     g_mma_min_m = t->mma_min_m;
+    g_rowdot_max_m = t->rowdot_max_m;
     return ok();
 }
 
@@ -548,6 +610,14 @@ int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int*
     int st = w8a16 ? check_w8a16_shape(M, K, N) : check_w4a8_shape(M, K, N);
     if (st != W4A8_OK) return st;
     if (!w8a16) {
+        w4a8::RowdotPlan rp;
+        if (rowdot_plan_for(M, K, N, &rp, num_sms)) {
+            const int ws = rp.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)rp.ws_bytes;
+            const int v[] = {rp.P, rp.tpr, rp.MT, 128, rp.tiles, rp.grid, 128, rp.NS, 16384,
+                             rp.smem, ws, 2};
+            for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
+            return ok();
+        }
         w4a8::MmaPlan mp;
         if (mma_plan_for(M, K, N, &mp, num_sms)) {
             const int ws = mp.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)mp.ws_bytes;

@@ -54,6 +54,20 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
                             unsigned flags, cudaStream_t stream, int gs = 0,
                             const float* const* sg = nullptr);
 cudaError_t read_and_clear_mma_error(unsigned* flags, cudaStream_t stream);
+// Tensor map of packed INT4 weights [N][K/2] for 2-D TMA boxes of 128 bytes
+// (256 codes) x 128 rows, 128-byte swizzle; `map` is a 64-byte aligned
+// CUtensorMap.  Host-only; false when the driver entry point is missing.
+bool make_w4_tile_map(void* map, const uint8_t* Wq, int64_t K, int64_t N);
+
+// Row-per-thread dp4a kernel for small batches (rowdot.cu).
+bool make_rowdot_plan(int M, int64_t K, int64_t N, int num_sms, RowdotPlan* out, int tpr = 0,
+                      int cps = 0);
+cudaError_t launch_w4a8_rowdot(const RowdotPlan& pl, const uint16_t* X, const int8_t* Xq,
+                               const float* sa, int M, int64_t K, int G, const uint8_t* const* Wq,
+                               const float* const* sw, const int64_t* Ns, float* const* Y,
+                               int32_t* acc_out, int8_t* Xq_out, float* sa_out, void* ws,
+                               unsigned flags, cudaStream_t stream);
+cudaError_t read_and_clear_rowdot_error(unsigned* flags, cudaStream_t stream);
 
 // IndexSoftmax (isx.cu).  The host helpers need no GPU.
 constexpr int kIsxMaxEntries = 256;  // 2^b table entries, b <= 8

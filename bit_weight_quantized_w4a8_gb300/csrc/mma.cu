@@ -642,6 +642,12 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
 
 }  // namespace
 
+bool make_w4_tile_map(void* map, const uint8_t* Wq, int64_t K, int64_t N) {
+    return encode_2d(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2),
+                     (uint64_t)N, (uint64_t)(K / 2), kWBlocks * kKBlock / 2, kTileRows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int gkb) {
     if (M < 1 || M > 64 || K < 32 || K % 32 || N < 1 || N > 0x7FFFFFFF) return false;
     // group scales: groups of gkb K blocks, whole stages, each group's sums

@@ -73,7 +73,13 @@ typedef enum {
    workspace are only touched after the wait. */
 #define W4A8_LAUNCH_PDL 1u
 
-/* Maximum activation rows (decode batch) per call.  W4A8 calls with at
+/* Maximum activation rows (decode batch) per call.  Row-wise W4A8 calls
+ * with 2 to 8 rows (w4a8_tuning_t.rowdot_max_m) run on the row-per-thread
+ * integer kernel: an activation-quantization launch writes the codes into
+ * the workspace split by parity, then each weight row is walked by four
+ * threads (of four warps) that unpack its INT4 codes once for all batch rows and
+ * sum exact int32 dp4a products against activation words that the whole CTA
+ * reads as shared-memory broadcasts.  Other W4A8 calls with at
  * least 3 rows (see w4a8_tuning_t.mma_min_m) run on the tensor cores: an
  * activation-quantization launch writes bf16 codes into the workspace, then
  * tcgen05 MMAs of 128 weight rows x the batch accumulate the integer
@@ -358,9 +364,14 @@ int w4a8_device_error(unsigned* flags, void* stream);
  *   force_splits: number of K pieces (1..16); the shape must admit it.
  *   force_threads_per_row: threads sharing one row-piece (power of 2, <=256).
  *   ring_bytes: target size of the shared-memory weight ring (<= 204800).
- *   ctas_per_sm: CTAs per SM for each K piece (1..4; 0 = 1).
+ *   ctas_per_sm: CTAs per SM for each K piece (1..4; 0 = 1); for the
+ *     row-per-thread kernel, CTAs per SM (0 = 4 / its threads per row).
  *   mma_min_m: activation rows from which the W4A8 entry points use the
  *     tensor-core kernel (2..65; 0 = default, 65 = never).
+ *   rowdot_max_m: activation rows up to which row-wise W4A8 calls use the
+ *     row-per-thread kernel, from 2 rows (0 = default 8, 1 = never, <= 8);
+ *     it takes precedence over mma_min_m.  force_threads_per_row 2 or 4
+ *     sets that kernel's threads per weight row.
  * w4a8_workspace_bytes reflects the overrides.  NULL restores the defaults.
  * Not synchronised with calls running on other threads. */
 typedef struct {
@@ -369,6 +380,7 @@ typedef struct {
     int ring_bytes;
     int ctas_per_sm;
     int mma_min_m;
+    int rowdot_max_m;
 } w4a8_tuning_t;
 
 int w4a8_set_tuning(const w4a8_tuning_t* tuning);
@@ -380,7 +392,10 @@ int w4a8_set_tuning(const w4a8_tuning_t* tuning);
  * memory bytes, workspace bytes (saturated at INT32_MAX), and 1 when the
  * tensor-core kernel serves the call (then the fields read: K pieces, 0,
  * batch rows padded to 16, 128 weight rows per tile, tiles, grid, 128,
- * ring stages, bytes per stage, shared memory, workspace).  w8a16 != 0
+ * ring stages, bytes per stage, shared memory, workspace), or 2 when the
+ * row-per-thread kernel serves it (K pieces, threads per weight row, batch
+ * rows, 128, tiles, grid, 128, ring stages, 16384, shared memory,
+ * workspace).  w8a16 != 0
  * selects w8a16_gemv.  num_sms > 0 plans for a device with that many SMs
  * without touching any GPU (host-side testing); 0 queries the current
  * device. */

@@ -118,8 +118,11 @@ def test_plan_invariants(sms, w8):
         if w8 and K > 65536:
             continue
         p = w4.w4a8_plan_info(M, K, N, w8a16=w8, num_sms=sms)
-        if p["tensor_cores"]:
+        if p["kernel"] == 1:
             check_mma_plan(p, M, K, N, sms)
+            continue
+        if p["kernel"] == 2:
+            check_rowdot_plan(p, M, K, N, sms)
             continue
         M = min(M, 4 if w8 else 8)  # the plan of the first launch of a row-group sequence
         kgran = 16 if w8 else 32
@@ -156,15 +159,45 @@ def check_mma_plan(p, M, K, N, sms):
     assert p["ws_bytes"] >= 4096 + 256 + M * K * 2
 
 
-def test_tensor_core_threshold():
+def check_rowdot_plan(p, M, K, N, sms):
+    assert 2 <= M <= 8
+    tiles = -(-N // 128)
+    nbox = -(-K // 256)
+    P, tpr = p["splits"], p["threads_per_row"]
+    assert tpr in (2, 4) and p["cols_per_thread"] == M
+    assert p["ctas_per_split"] == tiles and p["grid"] == tiles * P
+    bpp = -(-nbox // P)
+    assert (P - 1) * bpp < nbox                                  # no empty piece
+    assert M * bpp * 256 <= 48 * 1024                            # the piece's activation planes
+    assert 1 <= p["stages"] <= min(8, bpp) and p["stage_bytes"] == 16384
+    assert p["smem_bytes"] >= p["stages"] * 16384 + M * bpp * 256
+    assert p["smem_bytes"] * (4 // tpr) <= 227 * 1024
+    assert P == 1 or tiles <= 1024
+    assert p["ws_bytes"] >= 4096 + 256 + M * nbox * 256 + (tiles * P * M * 512 if P > 1 else 0)
+
+
+def test_kernel_routing():
+    """Row-wise calls: 1 row on the dp4a GEMV, 2..8 rows on the
+    row-per-thread kernel, 9+ on the tensor cores; the tuning moves both
+    thresholds."""
     try:
-        assert w4.w4a8_plan_info(2, 3584, 18944, num_sms=152)["tensor_cores"] == 0
-        assert w4.w4a8_plan_info(3, 3584, 18944, num_sms=152)["tensor_cores"] == 1
-        w4.w4a8_set_tuning(mma_min_m=65)
-        assert w4.w4a8_plan_info(64, 3584, 18944, num_sms=152)["tensor_cores"] == 0
-        w4.w4a8_set_tuning(mma_min_m=2)
-        assert w4.w4a8_plan_info(2, 3584, 18944, num_sms=152)["tensor_cores"] == 1
-        assert w4.w4a8_plan_info(1, 3584, 18944, num_sms=152)["tensor_cores"] == 0
+        route = lambda M: w4.w4a8_plan_info(M, 3584, 18944, num_sms=152)["kernel"]
+        assert [route(M) for M in (1, 2, 3, 8, 9, 64)] == [0, 2, 2, 2, 1, 1]
+        w4.w4a8_set_tuning(rowdot_max_m=4)
+        assert [route(M) for M in (2, 4, 5)] == [2, 2, 1]
+        w4.w4a8_set_tuning(rowdot_max_m=1)
+        assert [route(M) for M in (2, 3)] == [0, 1]
+        w4.w4a8_set_tuning(force_threads_per_row=4)
+        assert w4.w4a8_plan_info(5, 3584, 18944, num_sms=152)["threads_per_row"] == 4
+        with pytest.raises(w4.W4A8Error):
+            w4.w4a8_set_tuning(rowdot_max_m=9)
+        # group scales never take the row-per-thread kernel
+        assert w4.w4a8g_plan_info(4, 3584, 18944, 128, num_sms=152)["kernel"] == 1
+        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
+        assert w4.w4a8_plan_info(64, 3584, 18944, num_sms=152)["kernel"] == 0
+        w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1)
+        assert w4.w4a8_plan_info(2, 3584, 18944, num_sms=152)["kernel"] == 1
+        assert w4.w4a8_plan_info(1, 3584, 18944, num_sms=152)["kernel"] == 0
         with pytest.raises(w4.W4A8Error):
             w4.w4a8_set_tuning(mma_min_m=1)
     finally:
@@ -226,7 +259,7 @@ def test_group_plan_windows(sms, splits):
     and ends on 16-byte words inside the padded scale row, and the slot's
     scale area holds a whole stage of rows."""
     try:
-        w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65)  # the dp4a kernel's plans
+        w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65, rowdot_max_m=1)  # the dp4a kernel's plans
         for (M, K, N, gs) in GROUP_SHAPES:
             if splits and splits > K // 32:
                 continue
@@ -307,7 +340,7 @@ def test_group_tensor_core_plans():
                                   (4, 3584, 1000, 256), (8, 2048, 200, 512), (33, 896, 100, 128),
                                   (5, 32768, 64, 16384)]:
                 p = w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)
-                assert p["tensor_cores"] == 1, (M, K, N, gs)
+                assert p["kernel"] == 1, (M, K, N, gs)
                 nkb = K // 64
                 P = p["splits"]
                 kbp = -(-nkb // P)
@@ -319,8 +352,8 @@ def test_group_tensor_core_plans():
                 if P > 1:
                     assert p["ws_bytes"] >= 4096 + 256 + M * K * 2 + p["grid"] * M * 128 * 4
             for (M, K, N, gs) in [(3, 1024, 77, 32), (8, 3584, 100, 64), (2, 3584, 100, 128)]:
-                assert w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)["tensor_cores"] == 0
-        w4.w4a8_set_tuning(mma_min_m=65)
-        assert w4.w4a8g_plan_info(16, 3584, 18944, 128, num_sms=152)["tensor_cores"] == 0
+                assert w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)["kernel"] == 0
+        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
+        assert w4.w4a8g_plan_info(16, 3584, 18944, 128, num_sms=152)["kernel"] == 0
     finally:
         w4.w4a8_set_tuning(reset=True)

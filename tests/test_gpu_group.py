@@ -135,7 +135,7 @@ GROUP_SHAPES = [
 @pytest.mark.parametrize("M,K,N,gs,seed", GROUP_SHAPES)
 def test_w4a8g_linear(w4, orc, M, K, N, gs, seed, path):
     if path == "dp4a":
-        w4.w4a8_set_tuning(mma_min_m=65)
+        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
     check_group(w4, orc, M, K, N, gs, seed, fused=True)
 
 
@@ -143,7 +143,7 @@ def test_w4a8g_linear(w4, orc, M, K, N, gs, seed, path):
 @pytest.mark.parametrize("M,K,N,gs,seed", GROUP_SHAPES[:6] + GROUP_SHAPES[-2:])
 def test_w4a8g_gemv_unfused(w4, orc, M, K, N, gs, seed, path):
     if path == "dp4a":
-        w4.w4a8_set_tuning(mma_min_m=65)
+        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
     check_group(w4, orc, M, K, N, gs, seed, fused=False)
 
 
@@ -159,7 +159,7 @@ MMA_GROUP_SHAPES = [
 @pytest.mark.parametrize("M,K,N,gs,seed", MMA_GROUP_SHAPES)
 @pytest.mark.parametrize("fused", [True, False])
 def test_w4a8g_tensor_cores(w4, orc, M, K, N, gs, seed, fused):
-    assert w4.w4a8g_plan_info(M, K, N, gs)["tensor_cores"] == 1
+    assert w4.w4a8g_plan_info(M, K, N, gs)["kernel"] == 1
     check_group(w4, orc, M, K, N, gs, seed, fused=fused)
 
 
@@ -180,7 +180,7 @@ def test_w4a8g_tensor_cores_exact(w4, orc, M, N):
     Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
     Y_ref, _, _, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
     assert np.all(sa_ref == 1.0)
-    assert w4.w4a8g_plan_info(M, K, N, gs)["tensor_cores"] == 1
+    assert w4.w4a8g_plan_info(M, K, N, gs)["kernel"] == 1
     Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
     Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs)
     torch.cuda.synchronize()

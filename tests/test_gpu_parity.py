@@ -168,7 +168,7 @@ W4A8_SHAPES = [
 @pytest.mark.parametrize("M,K,N,seed", W4A8_SHAPES)
 def test_w4a8_linear_fused(w4, orc, M, K, N, seed, path):
     if path == "dp4a":
-        w4.w4a8_set_tuning(mma_min_m=65)  # batches of 3+ rows would take the tensor cores
+        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)  # batches of 3+ rows would take the tensor cores
     check_w4a8(w4, orc, M, K, N, seed, fused=True, zero_rows=(1,))
 
 
@@ -176,14 +176,14 @@ def test_w4a8_linear_fused(w4, orc, M, K, N, seed, path):
 @pytest.mark.parametrize("M,K,N,seed", W4A8_SHAPES[:8] + W4A8_SHAPES[-3:-1])
 def test_w4a8_gemv_unfused(w4, orc, M, K, N, seed, path):
     if path == "dp4a":
-        w4.w4a8_set_tuning(mma_min_m=65)
+        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
     check_w4a8(w4, orc, M, K, N, seed, fused=False)
 
 
 @pytest.mark.parametrize("splits", [2, 3, 5, 16])
 @pytest.mark.parametrize("fused", [True, False])
 def test_w4a8_split_k(w4, orc, splits, fused):
-    w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65)  # the dp4a kernel's split plans
+    w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65, rowdot_max_m=1)  # the dp4a kernel's split plans
     for (M, K, N, seed) in [(1, 3584, 700, 30), (3, 18944, 150, 31), (8, 1024, 64, 32)]:
         if (K // 32) < splits:
             continue
@@ -236,13 +236,13 @@ def test_w4a8_fused_ties(w4, orc, M, K, N, splits):
                                         (16, 18944, 200, 103), (24, 96, 1, 104), (64, 3584, 129, 105)])
 @pytest.mark.parametrize("fused", [True, False])
 def test_w4a8_tensor_cores(w4, orc, M, K, N, seed, fused):
-    w4.w4a8_set_tuning(mma_min_m=2)
-    assert w4.w4a8_plan_info(M, K, N)["tensor_cores"] == 1
+    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1)
+    assert w4.w4a8_plan_info(M, K, N)["kernel"] == 1
     check_w4a8(w4, orc, M, K, N, seed, fused=fused, zero_rows=(0,))
 
 
 def test_w4a8_tensor_cores_grouped(w4, orc):
-    w4.w4a8_set_tuning(mma_min_m=2)
+    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1)
     M, K, Ns = 18, 1024, (300, 7, 129)
     X = synth.activation(110, M, K, outlier_frac=0.001)
     Wqs, sws, refs = [], [], []
@@ -266,7 +266,7 @@ def test_w4a8_tensor_cores_largest_sums(w4, K):
     codes +127 and -127: each K piece's partial sum reaches 8 * 127 * 16384 =
     16,646,144, just below 2^24, which the fp32 accumulator must hold
     exactly; the pieces are added as int32."""
-    w4.w4a8_set_tuning(mma_min_m=2)
+    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1)
     M, N = 16, 130
     Wq = torch.full((N, K // 2), 0x88, dtype=torch.uint8, device="cuda")
     sw = torch.ones((N,), dtype=torch.float32, device="cuda")
@@ -287,10 +287,10 @@ def test_w4a8_tensor_cores_match_dp4a(w4, orc):
     W = weights(N, K, 120)
     X = to_dev(synth.activation(121, M, K, outlier_frac=0.001))
     Wq, sw = w4.w4_quantize_weights(to_dev(W))
-    w4.w4a8_set_tuning(mma_min_m=65)
-    assert w4.w4a8_plan_info(M, K, N)["tensor_cores"] == 0
+    w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
+    assert w4.w4a8_plan_info(M, K, N)["kernel"] == 0
     Y0 = w4.w4a8_linear(X, Wq, sw)
-    w4.w4a8_set_tuning(mma_min_m=2)
+    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1)
     Y1 = w4.w4a8_linear(X, Wq, sw)
     torch.cuda.synchronize()
     assert np.array_equal(bits(Y0.cpu().numpy()), bits(Y1.cpu().numpy()))
@@ -298,7 +298,7 @@ def test_w4a8_tensor_cores_match_dp4a(w4, orc):
 
 @pytest.mark.parametrize("cl", [1, 2, 8, 32, 64, 128, 256])
 def test_w4a8_threads_per_row(w4, orc, cl):
-    w4.w4a8_set_tuning(force_threads_per_row=cl)
+    w4.w4a8_set_tuning(force_threads_per_row=cl, rowdot_max_m=1)  # the dp4a kernel's plans
     for (M, K, N, seed) in [(1, 3584, 300, 40), (2, 2048, 99, 41), (1, 256, 513, 42)]:
         try:
             plan = w4.w4a8_plan_info(M, K, N)
@@ -313,7 +313,7 @@ def test_w4a8_two_stage_ring(w4, orc):
     w4.w4a8_set_tuning(ring_bytes=8192)
     assert w4.w4a8_plan_info(1, 3584, 5000)["stages"] == 2
     check_w4a8(w4, orc, 1, 3584, 5000, 50)
-    w4.w4a8_set_tuning(ring_bytes=8192, force_splits=3)
+    w4.w4a8_set_tuning(ring_bytes=8192, force_splits=3, rowdot_max_m=1)
     check_w4a8(w4, orc, 2, 18944, 300, 51)
 
 
@@ -430,7 +430,8 @@ def test_gpu_generator_matches_host(w4):
     (20, 256, (9, 30, 3), 2),
 ])
 def test_w4a8_linear_grouped(w4, orc, M, K, Ns, splits):
-    w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65 if splits else 0)
+    w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65 if splits else 0,
+                      rowdot_max_m=1 if splits else 0)
     X = synth.activation(500 + K, M, K, outlier_frac=0.001)
     refs, Wqs, sws = [], [], []
     for g, N in enumerate(Ns):

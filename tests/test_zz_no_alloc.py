@@ -75,7 +75,7 @@ def test_noalloc_matches_workspace_path_twice(w4, M, K, N, splits):
 
 def test_noalloc_rejects_plans_beyond_the_static_scratch(w4):
     M, K, N = 8, 4096, 10000
-    w4.w4a8_set_tuning(force_splits=16, mma_min_m=65)  # the dp4a plan the entry point uses
+    w4.w4a8_set_tuning(force_splits=16, mma_min_m=65, rowdot_max_m=1)  # the dp4a plan the entry point uses
     try:
         assert w4.w4a8_workspace_bytes(M, K, N) > SCRATCH_BYTES
         X = torch.zeros((M, K), dtype=torch.float16, device="cuda")
