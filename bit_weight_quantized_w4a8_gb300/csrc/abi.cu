@@ -132,7 +132,7 @@ bool rowdot_plan_for(int64_t M, int64_t K, int64_t N, w4a8::RowdotPlan* pl, int 
     if (M < 2 || M > hi) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
     const int cl = g_force_cl.load();
-    return w4a8::make_rowdot_plan((int)M, K, N, sms, pl, (cl == 2 || cl == 4) ? cl : 0,
+    return w4a8::make_rowdot_plan((int)M, K, N, sms, pl, (cl == 2 || cl == 4 || cl == 8) ? cl : 0,
                                   g_ctas_per_sm.load());
 }
 

@@ -6,6 +6,7 @@
 #include <cstdint>
 
 #include "plan.h"
+#include "rowdot_plan.h"
 
 namespace w4a8 {
 

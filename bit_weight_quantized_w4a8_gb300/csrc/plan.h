@@ -74,21 +74,6 @@ struct MmaPlan {
     size_t ws_bytes;
 };
 
-// Launch plan of the row-per-thread dp4a kernel (csrc/rowdot.cu).
-constexpr int kRowdotMaxM = 8;        // batch rows the kernel is instantiated for: 2..8
-constexpr int kRowdotDefaultTPR = 4;  // threads per weight row (one CTA of 512 per SM)
-struct RowdotPlan {
-    int MT;            // activation rows (2..kRowdotMaxM)
-    int tpr, cps;      // threads per weight row, CTAs per SM (4 / tpr)
-    int tiles;         // 128-row weight tiles
-    int nbox;          // 256-code K boxes (K rounded up)
-    int P, bpp;        // K pieces, boxes per piece
-    int NS;            // weight ring slots of 16 KB
-    int grid, smem, sms;
-    size_t off_sa, off_codes, off_part;  // workspace layout
-    size_t ws_bytes;
-};
-
 inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 inline size_t round_up_sz(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

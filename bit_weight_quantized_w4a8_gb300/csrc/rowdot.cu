@@ -384,6 +384,15 @@ const void* kernel_for_rows(int M) {
     }
 }
 
+const void* kernel_for(int M, int tpr) {
+    switch (tpr) {
+        case 2: return kernel_for_rows<2>(M);
+        case 4: return kernel_for_rows<4>(M);
+        case 8: return kernel_for_rows<8>(M);
+        default: return nullptr;
+    }
+}
+
 // Opts every instantiation into its largest shared-memory plan (and the
 // full shared-memory carveout, so that the planned CTAs per SM fit), once
 // per device.
@@ -393,9 +402,9 @@ cudaError_t set_attributes() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && done[dev]) return cudaSuccess;
-    for (int tpr = 2; tpr <= 4; tpr += 2) {
+    for (int tpr = 2; tpr <= 8; tpr *= 2) {
         for (int M = 2; M <= kRowdotMaxM; ++M) {
-            const void* fn = tpr == 4 ? kernel_for_rows<4>(M) : kernel_for_rows<2>(M);
+            const void* fn = kernel_for(M, tpr);
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerSM - 1024);
             if (e != cudaSuccess) return e;
             e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -423,8 +432,8 @@ bool make_rowdot_plan(int M, int64_t K, int64_t N, int num_sms, RowdotPlan* out,
     if (M < 2 || M > kRowdotMaxM || K < 32 || K % 32 || K > 131072 || N < 1 || N > 0x7FFFFFFF)
         return false;
     if (tpr == 0) tpr = kRowdotDefaultTPR;
-    if (tpr != 2 && tpr != 4) return false;
-    if (cps == 0) cps = 4 / tpr;
+    if (tpr != 2 && tpr != 4 && tpr != 8) return false;
+    if (cps == 0) cps = tpr < 4 ? 4 / tpr : 1;
     if (cps < 1 || cps > 4) return false;
     RowdotPlan pl = {};
     pl.tpr = tpr;
@@ -485,7 +494,7 @@ cudaError_t launch_w4a8_rowdot(const RowdotPlan& pl, const uint16_t* X, const in
                                    dim3(kPreThreads), 0, stream, flags, args);
         if (e != cudaSuccess) return e;
     }
-    const void* fn = pl.tpr == 4 ? kernel_for_rows<4>(M) : kernel_for_rows<2>(M);
+    const void* fn = kernel_for(M, pl.tpr);
     if (fn == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = set_attributes();
     if (e != cudaSuccess) return e;

@@ -370,7 +370,7 @@ int w4a8_device_error(unsigned* flags, void* stream);
  *     tensor-core kernel (2..65; 0 = default, 65 = never).
  *   rowdot_max_m: activation rows up to which row-wise W4A8 calls use the
  *     row-per-thread kernel, from 2 rows (0 = default 8, 1 = never, <= 8);
- *     it takes precedence over mma_min_m.  force_threads_per_row 2 or 4
+ *     it takes precedence over mma_min_m.  force_threads_per_row 2, 4 or 8
  *     sets that kernel's threads per weight row.
  * w4a8_workspace_bytes reflects the overrides.  NULL restores the defaults.
  * Not synchronised with calls running on other threads. */

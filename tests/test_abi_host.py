@@ -164,14 +164,14 @@ def check_rowdot_plan(p, M, K, N, sms):
     tiles = -(-N // 128)
     nbox = -(-K // 256)
     P, tpr = p["splits"], p["threads_per_row"]
-    assert tpr in (2, 4) and p["cols_per_thread"] == M
+    assert tpr in (2, 4, 8) and p["cols_per_thread"] == M
     assert p["ctas_per_split"] == tiles and p["grid"] == tiles * P
     bpp = -(-nbox // P)
     assert (P - 1) * bpp < nbox                                  # no empty piece
     assert M * bpp * 256 <= 48 * 1024                            # the piece's activation planes
     assert 1 <= p["stages"] <= min(8, bpp) and p["stage_bytes"] == 16384
     assert p["smem_bytes"] >= p["stages"] * 16384 + M * bpp * 256
-    assert p["smem_bytes"] * (4 // tpr) <= 227 * 1024
+    assert p["smem_bytes"] * max(1, 4 // tpr) <= 227 * 1024
     assert P == 1 or tiles <= 1024
     assert p["ws_bytes"] >= 4096 + 256 + M * nbox * 256 + (tiles * P * M * 512 if P > 1 else 0)
 
@@ -187,8 +187,11 @@ def test_kernel_routing():
         assert [route(M) for M in (2, 4, 5)] == [2, 2, 1]
         w4.w4a8_set_tuning(rowdot_max_m=1)
         assert [route(M) for M in (2, 3)] == [0, 1]
-        w4.w4a8_set_tuning(force_threads_per_row=4)
-        assert w4.w4a8_plan_info(5, 3584, 18944, num_sms=152)["threads_per_row"] == 4
+        for tpr in (2, 4, 8):
+            w4.w4a8_set_tuning(force_threads_per_row=tpr)
+            p = w4.w4a8_plan_info(5, 3584, 18944, num_sms=152)
+            assert p["threads_per_row"] == tpr and p["kernel"] == 2
+            check_rowdot_plan(p, 5, 3584, 18944, 152)
         with pytest.raises(w4.W4A8Error):
             w4.w4a8_set_tuning(rowdot_max_m=9)
         # group scales never take the row-per-thread kernel

@@ -87,7 +87,7 @@ ROWDOT_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("tpr", [0, 2])
+@pytest.mark.parametrize("tpr", [0, 2, 8])
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("M,K,N,seed", ROWDOT_SHAPES)
 def test_rowdot_parity(w4, orc, M, K, N, seed, fused, tpr):
