@@ -126,14 +126,23 @@ bool mma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::MmaPlan* pl, int sms = 
 
 // Row-per-thread plan for an M-row W4A8 call with row-wise scales, or false
 // when another kernel serves it.
-bool rowdot_plan_for(int64_t M, int64_t K, int64_t N, w4a8::RowdotPlan* pl, int sms = 0) {
+// gshift >= 0: group-wise scales, groups of 2^gshift codes.
+bool rowdot_plan_for(int64_t M, int64_t K, int64_t N, w4a8::RowdotPlan* pl, int sms = 0,
+                     int gshift = -1) {
     const int t = g_rowdot_max_m.load();
     const int hi = t > 0 ? t : kDefaultRowdotMaxM;
     if (M < 2 || M > hi) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
     const int cl = g_force_cl.load();
     return w4a8::make_rowdot_plan((int)M, K, N, sms, pl, (cl == 2 || cl == 4 || cl == 8) ? cl : 0,
-                                  g_ctas_per_sm.load());
+                                  g_ctas_per_sm.load(), gshift);
+}
+
+// log2 of a group size already checked by check_group.
+int log2_group(int64_t group) {
+    int s = 0;
+    while ((1LL << s) < group) ++s;
+    return s;
 }
 
 int check_ws(size_t need, void* ws, size_t ws_bytes) {
@@ -256,6 +265,8 @@ size_t w4a8g_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t group) {
     if (check_w4a8_shape(M, K, N) != W4A8_OK) return 0;
     int gshift, gld;
     if (check_group(K, group, &gshift, &gld) != W4A8_OK) return 0;
+    w4a8::RowdotPlan rp;
+    if (rowdot_plan_for(M, K, N, &rp, 0, log2_group(group))) return rp.ws_bytes;
     w4a8::MmaPlan mp;
     if (mma_plan_for(M, K, N, &mp, 0, group)) return mp.ws_bytes;
     w4a8::GemvPlan pf, pt;
@@ -443,6 +454,21 @@ int w4a8g_run(const char* name, const uint16_t* X, const int8_t* Xq, const float
     if ((X && !aligned(X, 16)) || (Xq && !aligned(Xq, 16)) || (sa && !aligned(sa, 4)) ||
         (Xq_out && !aligned(Xq_out, 16)) || (sa_out && !aligned(sa_out, 4)))
         return fail(W4A8_ERR_ALIGN, "%s: X/Xq/Xq_out need 16-byte, sa/sa_out 4-byte alignment", name);
+    w4a8::RowdotPlan rp;
+    if (rowdot_plan_for(M, K, total, &rp, 0, log2_group(group))) {
+        // one plan per matrix inside; the workspace bound covers every N[g] <= total
+        for (int g = 0; g < G; ++g) {
+            w4a8::RowdotPlan pg;
+            if (!w4a8::make_rowdot_plan((int)M, K, N[g], rp.sms, &pg, rp.tpr, rp.cps, rp.gshift) ||
+                pg.ws_bytes > rp.ws_bytes)
+                return fail(W4A8_ERR_SHAPE, "%s: no row-per-thread plan for group %d", name, g);
+        }
+        if ((st = check_ws(rp.ws_bytes, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_rowdot(rp, X, Xq, sa, (int)M, K, G, Wq, nullptr, N, Y, nullptr,
+                                                 Xq_out, sa_out, ws, flags,
+                                                 static_cast<cudaStream_t>(stream), (int)group, sg);
+        return e == cudaSuccess ? ok() : cuda_fail(e, name);
+    }
     w4a8::MmaPlan mp;
     if (mma_plan_for(M, K, total, &mp, 0, group)) {
         // one plan per matrix inside; the workspace bound covers every N[g] <= total
@@ -647,6 +673,14 @@ int w4a8g_plan_info(int64_t M, int64_t K, int64_t N, int64_t group, int num_sms,
     if (st != W4A8_OK) return st;
     int gshift, gld;
     if ((st = check_group(K, group, &gshift, &gld)) != W4A8_OK) return st;
+    w4a8::RowdotPlan rp;
+    if (rowdot_plan_for(M, K, N, &rp, num_sms, log2_group(group))) {
+        const int ws = rp.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)rp.ws_bytes;
+        const int v[] = {rp.P, rp.tpr, rp.MT, 128, rp.tiles, rp.grid, 128, rp.NS, 16384,
+                         rp.smem, ws, 2, rp.gwin, rp.gstride * 128 * 4};
+        for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
+        return ok();
+    }
     w4a8::MmaPlan mp;
     if (mma_plan_for(M, K, N, &mp, num_sms, group)) {
         const int ws = mp.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)mp.ws_bytes;

@@ -62,12 +62,13 @@ bool make_w4_tile_map(void* map, const uint8_t* Wq, int64_t K, int64_t N);
 
 // Row-per-thread dp4a kernel for small batches (rowdot.cu).
 bool make_rowdot_plan(int M, int64_t K, int64_t N, int num_sms, RowdotPlan* out, int tpr = 0,
-                      int cps = 0);
+                      int cps = 0, int gshift = -1);
 cudaError_t launch_w4a8_rowdot(const RowdotPlan& pl, const uint16_t* X, const int8_t* Xq,
                                const float* sa, int M, int64_t K, int G, const uint8_t* const* Wq,
                                const float* const* sw, const int64_t* Ns, float* const* Y,
                                int32_t* acc_out, int8_t* Xq_out, float* sa_out, void* ws,
-                               unsigned flags, cudaStream_t stream);
+                               unsigned flags, cudaStream_t stream, int gs = 0,
+                               const float* const* sg = nullptr);
 cudaError_t read_and_clear_rowdot_error(unsigned* flags, cudaStream_t stream);
 
 // IndexSoftmax (isx.cu).  The host helpers need no GPU.

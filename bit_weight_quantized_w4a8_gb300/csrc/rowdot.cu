@@ -73,8 +73,12 @@ struct RowdotArgs {
     const float* sa;        // [M]
     float* Y;               // [M][N]
     int32_t* acc_out;       // optional [M][N]
-    int32_t* part;          // [tiles][P][M][128] int32 piece sums when P > 1
+    int32_t* part;          // [tiles][P][M][128] piece sums when P > 1 (int32; fp32 with group scales)
     unsigned* tickets;      // [tiles] when P > 1, zero between calls
+    // group scales: sg [N][gld] fp32, one per 2^gshift codes, ngroups = K >> gshift;
+    // a piece's window of gwin groups is staged per CTA as [128][gstride]
+    const float* sg;
+    int gshift, gld, ngroups, gwin, gstride;
     int M, N, kw, nbox, bpp, P, NS;
 };
 
@@ -158,9 +162,10 @@ __global__ void __launch_bounds__(kPreThreads) rowdot_codes_kernel(
 
 // Shared memory (base aligned to 1024 for the swizzled boxes): the weight
 // ring [NS][16384], the piece's activation codes [bpp][8][MT][32 bytes], the
-// cross-warp sums [TPR - 1][MT][128] int32, NS + 1 mbarriers (ring slots,
-// activations), and per slot the number of warps done with it and the last
-// box copied into it.
+// cross-warp sums [TPR - 1][MT][128] (int32; fp32 with group scales), with
+// group scales the piece's scale window [128][gstride] fp32, NS + 1 mbarriers
+// (ring slots, activations), and per slot the number of warps done with it
+// and the last box copied into it.
 //
 // Thread mapping: warp w takes the 16-byte chunks c = w / 4 + TPR * i of
 // every 128-byte box row, lane l the weight row r = (w % 4) * 32 + l.  With
@@ -168,7 +173,13 @@ __global__ void __launch_bounds__(kPreThreads) rowdot_codes_kernel(
 // * 16)) the eight lanes of each quarter-warp read eight different bank
 // groups (conflict-free), and every activation load of a warp is one
 // address (a broadcast).
-template <int MT, int TPR>
+//
+// kG (group-wise scales, groups of 2^gshift >= 32 codes): a 32-code chunk is
+// one granule of one group; its exact int32 sum v is folded into an fp32 sum
+// per batch row with one fma(v, s_g, sum), the four threads of a row add
+// their fp32 sums in a fixed order, pieces add theirs in piece order, and
+// the result is multiplied by s_a.
+template <int MT, int TPR, bool kG>
 __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_constant__ RowdotArgs a) {
     constexpr int kThreads = kTile * TPR;
     constexpr int kWarps = kThreads / 32;
@@ -182,7 +193,8 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
     uint8_t* ring = smem;
     uint8_t* act = smem + NS * kBoxBytes;
     int* red = reinterpret_cast<int*>(act + a.bpp * kBoxAct);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(red + (TPR - 1) * MT * kTile);  // full[NS], activations
+    float* sgs = reinterpret_cast<float*>(red + (TPR - 1) * MT * kTile);  // group scales
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sgs + (kG ? kTile * a.gstride : 0));  // full[NS], activations
     int* released = reinterpret_cast<int*>(bars + NS + 1);
     int* last_box = released + NS;
     volatile int* abort_flag = last_box + NS;
@@ -195,6 +207,7 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
     const int t = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint64_t pol = l2_evict_first_policy();
+    const int g0 = kG ? (box0 * kBoxCodes) >> a.gshift : 0;  // first group of the piece
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -217,6 +230,18 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
             last_box[i] = i;
         }
     }
+    if constexpr (kG) {
+        // the piece's scale window; zero for rows past N and groups past K
+        for (int e = tid; e < kTile * a.gwin; e += kThreads) {
+            const int rr = e / a.gwin, j = e - rr * a.gwin;
+            const int64_t n = (int64_t)tile * kTile + rr;
+            float* dst = sgs + rr * a.gstride + j;
+            if (n < a.N && g0 + j < a.ngroups)
+                cp_async_4(smem_u32(dst), a.sg + n * a.gld + g0 + j);
+            else
+                *dst = 0.f;
+        }
+    }
     griddep_wait();  // activation codes, scales, outputs and workspace from here on
     if (tid == 0) {
         const uint32_t bytes = (uint32_t)nb * kBoxAct;
@@ -224,10 +249,17 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
         bulk_g2s(smem_u32(act), reinterpret_cast<const uint8_t*>(a.codes) + (int64_t)box0 * kBoxAct, bytes,
                  smem_u32(bars + NS), l2_evict_last_policy());
     }
+    if constexpr (kG) {
+        cp_async_wait_all();
+        __syncthreads();
+    }
 
     int acc[MT][2];  // 16 x the even / odd products of each batch row
+    float gacc[kG ? MT : 1];  // group scales: fp32 sums of scaled granules
     #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = 0;
+    #pragma unroll
+    for (int m = 0; m < (kG ? MT : 1); ++m) gacc[m] = 0.f;
     const uint8_t* wrow = ring + r * 128;
     bool ok = wait_bounded(smem_u32(bars + NS), 0, abort_flag);
     int slot = 0;
@@ -262,13 +294,18 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
         const uint8_t* ab = act + i * kBoxAct;
         #pragma unroll
         for (int ci = 0; ci < CPT; ++ci) {
-            const uint8_t* ac = ab + (t + TPR * ci) * kChunkAct;
+            const int c = t + TPR * ci;
+            const uint8_t* ac = ab + c * kChunkAct;
             const uint32_t w[4] = {wv[ci].x, wv[ci].y, wv[ci].z, wv[ci].w};
             int lo[4], hi[4];
             #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 lo[j] = (int)((w[j] << 4) & 0xF0F0F0F0u);
                 hi[j] = (int)(w[j] & 0xF0F0F0F0u);
+            }
+            if constexpr (kG) {
+                #pragma unroll
+                for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = 0;
             }
             #pragma unroll
             for (int m = 0; m < MT; ++m) {
@@ -283,14 +320,28 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
                 acc[m][0] = __dp4a(lo[3], (int)a1.z, acc[m][0]);
                 acc[m][1] = __dp4a(hi[3], (int)a1.w, acc[m][1]);
             }
+            if constexpr (kG) {
+                // the granule's group scale; |v| <= 1016 * 32 is exact in fp32
+                const int g = (((box0 + i) * kBoxCodes + c * 32) >> a.gshift) - g0;
+                const float sgv = sgs[r * a.gstride + g];
+                #pragma unroll
+                for (int m = 0; m < MT; ++m)
+                    gacc[m] = __fmaf_rn(__int2float_rn((acc[m][0] >> 4) + (acc[m][1] >> 4)), sgv, gacc[m]);
+            }
         }
     }
 
-    // The row's integer dot products: the two sums are 16 x integers; the
-    // warps of chunk phases t > 0 hand theirs to phase 0 (exact).
+    // The row's sums: integers (the two dp4a sums are 16 x integers), or fp32
+    // with group scales; the warps of chunk phases t > 0 hand theirs to
+    // phase 0, which adds them in phase order.
     int v[MT];
-    #pragma unroll
-    for (int m = 0; m < MT; ++m) v[m] = (acc[m][0] >> 4) + (acc[m][1] >> 4);
+    if constexpr (kG) {
+        #pragma unroll
+        for (int m = 0; m < MT; ++m) v[m] = __float_as_int(gacc[m]);
+    } else {
+        #pragma unroll
+        for (int m = 0; m < MT; ++m) v[m] = (acc[m][0] >> 4) + (acc[m][1] >> 4);
+    }
     if (t > 0) {
         #pragma unroll
         for (int m = 0; m < MT; ++m) red[((t - 1) * MT + m) * kTile + r] = v[m];
@@ -308,17 +359,27 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
         #pragma unroll
         for (int tt = 1; tt < TPR; ++tt) {
             #pragma unroll
-            for (int m = 0; m < MT; ++m) v[m] += red[((tt - 1) * MT + m) * kTile + r];
+            for (int m = 0; m < MT; ++m) {
+                const int o = red[((tt - 1) * MT + m) * kTile + r];
+                if constexpr (kG)
+                    v[m] = __float_as_int(__fadd_rn(__int_as_float(v[m]), __int_as_float(o)));
+                else
+                    v[m] += o;
+            }
         }
     }
     const int n = tile * kTile + r;
     if (a.P == 1) {
         if (t == 0 && n < a.N) {
-            const float swv = a.sw[n];
+            const float swv = kG ? 0.f : a.sw[n];
             #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                a.Y[(int64_t)m * a.N + n] = __fmul_rn(__fmul_rn(__int2float_rn(v[m]), swv), a.sa[m]);
-                if (a.acc_out != nullptr) a.acc_out[(int64_t)m * a.N + n] = v[m];
+                if constexpr (kG) {
+                    a.Y[(int64_t)m * a.N + n] = __fmul_rn(__int_as_float(v[m]), a.sa[m]);
+                } else {
+                    a.Y[(int64_t)m * a.N + n] = __fmul_rn(__fmul_rn(__int2float_rn(v[m]), swv), a.sa[m]);
+                    if (a.acc_out != nullptr) a.acc_out[(int64_t)m * a.N + n] = v[m];
+                }
             }
         }
         return;
@@ -340,10 +401,17 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
     for (int e = tid; e < MT * kTile; e += kThreads) {
         const int m = e / kTile, rr = e % kTile, nn = tile * kTile + rr;
         if (nn >= a.N) continue;
-        int32_t sum = 0;
-        for (int q = 0; q < a.P; ++q) sum += __ldcg(src + (int64_t)q * MT * kTile + e);
-        a.Y[(int64_t)m * a.N + nn] = __fmul_rn(__fmul_rn(__int2float_rn(sum), a.sw[nn]), a.sa[m]);
-        if (a.acc_out != nullptr) a.acc_out[(int64_t)m * a.N + nn] = sum;
+        if constexpr (kG) {
+            float sum = 0.f;
+            for (int q = 0; q < a.P; ++q)
+                sum = __fadd_rn(sum, __int_as_float(__ldcg(src + (int64_t)q * MT * kTile + e)));
+            a.Y[(int64_t)m * a.N + nn] = __fmul_rn(sum, a.sa[m]);
+        } else {
+            int32_t sum = 0;
+            for (int q = 0; q < a.P; ++q) sum += __ldcg(src + (int64_t)q * MT * kTile + e);
+            a.Y[(int64_t)m * a.N + nn] = __fmul_rn(__fmul_rn(__int2float_rn(sum), a.sw[nn]), a.sa[m]);
+            if (a.acc_out != nullptr) a.acc_out[(int64_t)m * a.N + nn] = sum;
+        }
     }
     if (tid == 0) a.tickets[tile] = 0u;  // ready for the next call
 }
@@ -365,30 +433,32 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-template <int MT, int TPR>
+template <int MT, int TPR, bool kG>
 const void* kernel_for() {
-    return reinterpret_cast<const void*>(rowdot_kernel<MT, TPR>);
+    return reinterpret_cast<const void*>(rowdot_kernel<MT, TPR, kG>);
 }
 
-template <int TPR>
+template <int TPR, bool kG>
 const void* kernel_for_rows(int M) {
     switch (M) {
-        case 2: return kernel_for<2, TPR>();
-        case 3: return kernel_for<3, TPR>();
-        case 4: return kernel_for<4, TPR>();
-        case 5: return kernel_for<5, TPR>();
-        case 6: return kernel_for<6, TPR>();
-        case 7: return kernel_for<7, TPR>();
-        case 8: return kernel_for<8, TPR>();
+        case 2: return kernel_for<2, TPR, kG>();
+        case 3: return kernel_for<3, TPR, kG>();
+        case 4: return kernel_for<4, TPR, kG>();
+        case 5: return kernel_for<5, TPR, kG>();
+        case 6: return kernel_for<6, TPR, kG>();
+        case 7: return kernel_for<7, TPR, kG>();
+        case 8: return kernel_for<8, TPR, kG>();
         default: return nullptr;
     }
 }
 
-const void* kernel_for(int M, int tpr) {
+// Row-wise scales: 2, 4 or 8 threads per row; group scales: 4.
+const void* kernel_for(int M, int tpr, bool group) {
+    if (group) return tpr == 4 ? kernel_for_rows<4, true>(M) : nullptr;
     switch (tpr) {
-        case 2: return kernel_for_rows<2>(M);
-        case 4: return kernel_for_rows<4>(M);
-        case 8: return kernel_for_rows<8>(M);
+        case 2: return kernel_for_rows<2, false>(M);
+        case 4: return kernel_for_rows<4, false>(M);
+        case 8: return kernel_for_rows<8, false>(M);
         default: return nullptr;
     }
 }
@@ -402,9 +472,9 @@ cudaError_t set_attributes() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && done[dev]) return cudaSuccess;
-    for (int tpr = 2; tpr <= 8; tpr *= 2) {
+    for (int k = 0; k < 4; ++k) {
         for (int M = 2; M <= kRowdotMaxM; ++M) {
-            const void* fn = kernel_for(M, tpr);
+            const void* fn = k < 3 ? kernel_for(M, 2 << k, false) : kernel_for(M, 4, true);
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerSM - 1024);
             if (e != cudaSuccess) return e;
             e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -416,9 +486,10 @@ cudaError_t set_attributes() {
     return cudaSuccess;
 }
 
-size_t smem_bytes(int M, int NS, int bpp, int tpr) {
+size_t smem_bytes(int M, int NS, int bpp, int tpr, int gstride) {
     return 1024 + (size_t)NS * kBoxBytes + (size_t)M * bpp * kActBoxBytes +
-           (size_t)(tpr - 1) * M * kTile * 4 + (size_t)(NS + 1) * 8 + (size_t)(2 * NS + 2) * 4;
+           (size_t)(tpr - 1) * M * kTile * 4 + (size_t)kTile * gstride * 4 + (size_t)(NS + 1) * 8 +
+           (size_t)(2 * NS + 2) * 4;
 }
 
 }  // namespace
@@ -427,12 +498,16 @@ size_t smem_bytes(int M, int NS, int bpp, int tpr) {
 // cps CTAs per SM (0 = the defaults: 4 threads, 4 / TPR CTAs).  K is split
 // into pieces of whole 256-code boxes when the tiles alone leave CTA slots
 // idle, and so that a piece's activation codes fit in kActMax bytes.  The
-// ring takes what shared memory is left, up to kMaxNS boxes.
-bool make_rowdot_plan(int M, int64_t K, int64_t N, int num_sms, RowdotPlan* out, int tpr, int cps) {
+// ring takes what shared memory is left, up to kMaxNS boxes.  gshift >= 0:
+// group scales (groups of 2^gshift codes, 4 threads per row), the piece's
+// scale window staged per CTA.
+bool make_rowdot_plan(int M, int64_t K, int64_t N, int num_sms, RowdotPlan* out, int tpr, int cps,
+                      int gshift) {
     if (M < 2 || M > kRowdotMaxM || K < 32 || K % 32 || K > 131072 || N < 1 || N > 0x7FFFFFFF)
         return false;
-    if (tpr == 0) tpr = kRowdotDefaultTPR;
+    if (tpr == 0 || gshift >= 0) tpr = kRowdotDefaultTPR;
     if (tpr != 2 && tpr != 4 && tpr != 8) return false;
+    if (gshift >= 0 && (gshift < 5 || gshift > 17 || K % (1LL << gshift))) return false;
     if (cps == 0) cps = tpr < 4 ? 4 / tpr : 1;
     if (cps < 1 || cps > 4) return false;
     RowdotPlan pl = {};
@@ -452,16 +527,23 @@ bool make_rowdot_plan(int M, int64_t K, int64_t N, int num_sms, RowdotPlan* out,
     pl.P = (pl.nbox + pl.bpp - 1) / pl.bpp;
     if (pl.P > 1 && pl.tiles > kTicketSlots) return false;
     if ((int64_t)pl.tiles * pl.P > 0x7FFFFFFF) return false;
+    pl.gshift = gshift;
+    if (gshift >= 0) {
+        // groups a piece touches: whole groups when boxes hold whole groups,
+        // else the piece may start and end inside one
+        pl.gwin = (int)(((int64_t)pl.bpp * kBoxCodes) >> gshift) + 2;
+        pl.gstride = pl.gwin | 1;  // odd: the 32 rows of a warp hit 32 banks
+    }
     const int budget = kSmemPerSM / pl.cps - 1024;
     int NS = kMaxNS < pl.bpp ? kMaxNS : pl.bpp;
-    while (NS > 1 && smem_bytes(M, NS, pl.bpp, tpr) > (size_t)budget) --NS;
-    if (smem_bytes(M, NS, pl.bpp, tpr) > (size_t)budget) return false;
+    while (NS > 1 && smem_bytes(M, NS, pl.bpp, tpr, pl.gstride) > (size_t)budget) --NS;
+    if (smem_bytes(M, NS, pl.bpp, tpr, pl.gstride) > (size_t)budget) return false;
     pl.NS = NS;
-    pl.smem = (int)smem_bytes(M, NS, pl.bpp, tpr);
+    pl.smem = (int)smem_bytes(M, NS, pl.bpp, tpr, pl.gstride);
     pl.grid = pl.tiles * pl.P;
     pl.sms = num_sms;
     // workspace: tickets, scales, activation codes [nbox][8][M][32 bytes],
-    // then int32 piece sums [tiles][P][M][128].  Sized for any N' <= N
+    // then piece sums [tiles][P][M][128] (int32, or fp32 with group scales).  Sized for any N' <= N
     // (grouped launches plan each matrix on its own): a split matrix has
     // at most max(slots, tiles * pmin) tile pieces.
     pl.off_sa = kTicketBytes;
@@ -479,7 +561,8 @@ cudaError_t launch_w4a8_rowdot(const RowdotPlan& pl, const uint16_t* X, const in
                                const float* sa, int M, int64_t K, int G, const uint8_t* const* Wq,
                                const float* const* sw, const int64_t* Ns, float* const* Y,
                                int32_t* acc_out, int8_t* Xq_out, float* sa_out, void* ws,
-                               unsigned flags, cudaStream_t stream) {
+                               unsigned flags, cudaStream_t stream, int gs, const float* const* sg) {
+    const bool group = gs > 0;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     float* sa_ws = reinterpret_cast<float*>(wsb + pl.off_sa);
     uint2* codes = reinterpret_cast<uint2*>(wsb + pl.off_codes);
@@ -494,18 +577,26 @@ cudaError_t launch_w4a8_rowdot(const RowdotPlan& pl, const uint16_t* X, const in
                                    dim3(kPreThreads), 0, stream, flags, args);
         if (e != cudaSuccess) return e;
     }
-    const void* fn = kernel_for(M, pl.tpr);
-    if (fn == nullptr) return cudaErrorInvalidValue;
+    const void* fn = kernel_for(M, pl.tpr, group);
+    if (fn == nullptr || group != (pl.gshift >= 0)) return cudaErrorInvalidValue;
     cudaError_t e = set_attributes();
     if (e != cudaSuccess) return e;
     for (int g = 0; g < G; ++g) {
         RowdotPlan pg;
-        if (!make_rowdot_plan(M, K, Ns[g], pl.sms, &pg, pl.tpr, pl.cps)) return cudaErrorInvalidValue;
+        if (!make_rowdot_plan(M, K, Ns[g], pl.sms, &pg, pl.tpr, pl.cps, pl.gshift)) return cudaErrorInvalidValue;
         RowdotArgs a;
         memset(&a, 0, sizeof(a));
         if (!make_w4_tile_map(&a.tmW, Wq[g], K, Ns[g])) return cudaErrorInvalidValue;
         a.codes = codes;
-        a.sw = sw[g];
+        a.sw = group ? nullptr : sw[g];
+        if (group) {
+            a.sg = sg[g];
+            a.gshift = pg.gshift;
+            a.gld = (int)((K / gs + 3) / 4 * 4);
+            a.ngroups = (int)(K >> pg.gshift);
+            a.gwin = pg.gwin;
+            a.gstride = pg.gstride;
+        }
         a.sa = sa_ws;
         a.Y = Y[g];
         a.acc_out = (G == 1) ? acc_out : nullptr;

@@ -16,6 +16,8 @@ struct RowdotPlan {
     int nbox;          // 256-code K boxes (K rounded up)
     int P, bpp;        // K pieces, boxes per piece
     int NS;            // weight ring slots of 16 KB
+    int gshift;        // group scales: groups of 2^gshift codes (-1: row-wise)
+    int gwin, gstride; // groups staged per CTA, floats per staged row
     int grid, smem, sms;
     size_t off_sa, off_codes, off_part;  // workspace layout
     size_t ws_bytes;

@@ -246,7 +246,12 @@ size_t w4a8g_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t group);
  *   Wq [N][K/2] uint8, sg [N][stride] fp32   (w4g_quantize_weights)
  *   Y [M][N] fp32 out; ws, ws_bytes (w4a8g_workspace_bytes) and flags as
  *   in w4a8_gemv.
- * Calls with at least 3 rows (w4a8_tuning_t.mma_min_m) and a group of a
+ * Calls with 2 to 8 rows (w4a8_tuning_t.rowdot_max_m) run on the
+ * row-per-thread kernel (any group size): each 32-code granule's exact sum
+ * is folded with its group scale by one fused multiply-add per batch row,
+ * the four threads of a weight row and the K pieces add their fp32 sums in
+ * a fixed order.  Other calls with at least 3 rows
+ * (w4a8_tuning_t.mma_min_m) and a group of a
  * multiple of 128 codes up to 16384 run on the tensor cores: each group's
  * products are summed exactly in an fp32 TMEM accumulator, multiplied by
  * the group scale and added into fp32 running sums with one fused

@@ -194,8 +194,11 @@ def test_kernel_routing():
             check_rowdot_plan(p, 5, 3584, 18944, 152)
         with pytest.raises(w4.W4A8Error):
             w4.w4a8_set_tuning(rowdot_max_m=9)
-        # group scales never take the row-per-thread kernel
-        assert w4.w4a8g_plan_info(4, 3584, 18944, 128, num_sms=152)["kernel"] == 1
+        # group scales: the row-per-thread kernel at 2..8 rows, the tensor cores above
+        w4.w4a8_set_tuning()
+        assert w4.w4a8g_plan_info(4, 3584, 18944, 128, num_sms=152)["kernel"] == 2
+        assert w4.w4a8g_plan_info(9, 3584, 18944, 128, num_sms=152)["kernel"] == 1
+        assert w4.w4a8g_plan_info(4, 3584, 18944, 32, num_sms=152)["kernel"] == 2
         w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
         assert w4.w4a8_plan_info(64, 3584, 18944, num_sms=152)["kernel"] == 0
         w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1)
@@ -338,6 +341,7 @@ def test_group_tensor_core_plans():
     hold whole groups and whole weight loads, and the workspace covers the
     fp32 partials of every piece."""
     try:
+        w4.w4a8_set_tuning(rowdot_max_m=1)  # 2..8 rows would take the row-per-thread kernel
         for sms in (152, 148, 20):
             for (M, K, N, gs) in [(3, 3584, 300, 128), (16, 3584, 18944, 128), (64, 18944, 3584, 128),
                                   (4, 3584, 1000, 256), (8, 2048, 200, 512), (33, 896, 100, 128),
@@ -360,3 +364,22 @@ def test_group_tensor_core_plans():
         assert w4.w4a8g_plan_info(16, 3584, 18944, 128, num_sms=152)["kernel"] == 0
     finally:
         w4.w4a8_set_tuning(reset=True)
+
+
+def test_group_rowdot_plans():
+    """Group scales with 2..8 rows take the row-per-thread kernel for every
+    power-of-two group from 32: the staged scale window covers every group a
+    K piece touches and fits beside the ring."""
+    for sms in (152, 148, 20):
+        for (M, K, N, gs) in [(2, 3584, 1000, 128), (3, 1024, 77, 32), (8, 18944, 700, 128),
+                              (8, 4096, 64, 4096), (4, 2048, 5, 1024), (2, 131072, 3, 32),
+                              (5, 131072, 7, 1024)]:
+            p = w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)
+            assert p["kernel"] == 2, (M, K, N, gs)
+            check_rowdot_plan(p, M, K, N, sms)
+            nbox = -(-K // 256)
+            bpp = -(-nbox // p["splits"])
+            # groups touched by any piece: at most bpp * 256 / gs + 1
+            assert p["scale_window"] >= bpp * 256 // gs + 1
+            assert p["scale_stage_bytes"] >= 128 * p["scale_window"] * 4
+            assert p["smem_bytes"] >= p["stages"] * 16384 + M * bpp * 256 + p["scale_stage_bytes"]

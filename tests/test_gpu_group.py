@@ -159,6 +159,7 @@ MMA_GROUP_SHAPES = [
 @pytest.mark.parametrize("M,K,N,gs,seed", MMA_GROUP_SHAPES)
 @pytest.mark.parametrize("fused", [True, False])
 def test_w4a8g_tensor_cores(w4, orc, M, K, N, gs, seed, fused):
+    w4.w4a8_set_tuning(rowdot_max_m=1)  # 2..8 rows would take the row-per-thread kernel
     assert w4.w4a8g_plan_info(M, K, N, gs)["kernel"] == 1
     check_group(w4, orc, M, K, N, gs, seed, fused=fused)
 
@@ -180,6 +181,7 @@ def test_w4a8g_tensor_cores_exact(w4, orc, M, N):
     Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
     Y_ref, _, _, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
     assert np.all(sa_ref == 1.0)
+    w4.w4a8_set_tuning(rowdot_max_m=1)
     assert w4.w4a8g_plan_info(M, K, N, gs)["kernel"] == 1
     Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
     Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs)
@@ -188,6 +190,7 @@ def test_w4a8g_tensor_cores_exact(w4, orc, M, N):
 
 
 def test_w4a8g_tensor_cores_grouped(w4, orc):
+    w4.w4a8_set_tuning(rowdot_max_m=1)
     M, K, gs, Ns = 8, 3584, 128, [3584, 512, 512]
     X = synth.activation(97, M, K, outlier_frac=0.001)
     Wqs, sgs, refs = [], [], []
@@ -209,7 +212,7 @@ def test_w4a8g_tensor_cores_grouped(w4, orc):
 def test_w4a8g_split_k(w4, orc, splits, fused):
     # pieces that start inside a scale word: the windows are widened to whole
     # 16-byte words and indexed from their remainder
-    w4.w4a8_set_tuning(force_splits=splits)
+    w4.w4a8_set_tuning(force_splits=splits, rowdot_max_m=1)  # the dp4a kernel's split plans
     check_group(w4, orc, 2, 3584, 300, 128, 30 + splits, fused=fused)
     check_group(w4, orc, 1, 18944, 70, 64, 40 + splits, fused=fused)
 
@@ -225,7 +228,8 @@ def test_w4a8g_two_stage_ring(w4, orc):
     check_group(w4, orc, 1, 3584, 700, 128, 51)
 
 
-def test_w4a8g_exact_powers_of_two(w4, orc):
+@pytest.mark.parametrize("path", ["default", "dp4a"])
+def test_w4a8g_exact_powers_of_two(w4, orc, path):
     """Group scales 2^-e (e in 0..3) and integer activations with max 127
     (s_a = 1): every granule sum, product and partial sum is exact in fp32,
     so Y equals the oracle's binary64 value bit for bit."""
@@ -242,7 +246,11 @@ def test_w4a8g_exact_powers_of_two(w4, orc):
     Y_ref, B, _, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
     assert np.all(sa_ref == 1.0)
     for splits in (0, 3):
-        w4.w4a8_set_tuning(force_splits=splits)
+        if path == "dp4a":
+            w4.w4a8_set_tuning(force_splits=splits, rowdot_max_m=1, mma_min_m=65)
+        else:
+            w4.w4a8_set_tuning()
+            assert w4.w4a8g_plan_info(M, K, N, gs)["kernel"] == 2
         Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
         Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs)
         torch.cuda.synchronize()
@@ -344,12 +352,17 @@ def test_w4a8g_qwen2_fullsize(w4, orc, li):
         assert_within_bound(Ys[g].cpu().numpy()[:, rows], Y_ref, B, K)
 
 
+@pytest.mark.parametrize("path", ["default", "tensor_cores"])
 @pytest.mark.parametrize("M,K,N,gs,seed", [
     (1, 131072, 5, 128, 110),     # longest rows, dp4a
-    (2, 131072, 3, 32, 111),      # longest rows, smallest groups, dp4a
-    (5, 131072, 7, 1024, 112),    # longest rows on the tensor cores
+    (2, 131072, 3, 32, 111),      # longest rows, smallest groups (dp4a when forced)
+    (5, 131072, 7, 1024, 112),    # longest rows (row-per-thread; the tensor cores when forced)
     (4, 131072, 1, 16384, 113),   # largest tensor-core group, one output row
     (1, 3584, 1, 128, 114),       # one output row
 ])
-def test_w4a8g_maximum_sizes(w4, orc, M, K, N, gs, seed):
+def test_w4a8g_maximum_sizes(w4, orc, M, K, N, gs, seed, path):
+    if path == "tensor_cores":
+        if M == 1:
+            pytest.skip("one row runs on the dp4a kernel on both paths")
+        w4.w4a8_set_tuning(rowdot_max_m=1)
     check_group(w4, orc, M, K, N, gs, seed)
