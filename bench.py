@@ -699,13 +699,14 @@ def measure_group_set(torch, w4, synth, dev, stream, lin, gs=GROUP_SIZE):
     us_lm = _graph_us(torch, stream, lambda: [launch(k % 2, jl, w4.LAUNCH_PDL) for k in range(20)], 20)
     _, K_lm, N_lm = LINEARS[names.index("lm_head")]
     lm_bytes = N_lm * (K_lm // 2 + 4 * w4.w4g_scale_stride(K_lm, gs))
-    # batches on gate and down (3..64 rows take the tensor cores)
+    # batches on gate and down (2..8 rows take the row-per-thread kernel,
+    # 9..64 the tensor cores)
     skinny = {}
     for name in ("gate", "down"):
         i = names.index(name)
         _, K, N = LINEARS[i]
         res = {}
-        for M in (1, 4, 16, 64):
+        for M in (1, 2, 4, 8, 16, 64):
             X = torch.from_numpy(synth.activation(WEIGHT_SEED0 + i + ACT_SEED_OFFSET, M, K,
                                                   outlier_frac=OUTLIER_FRAC)).to(dev)
             Y = torch.empty((M, N), dtype=torch.float32, device=dev)
