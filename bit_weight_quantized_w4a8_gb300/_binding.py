@@ -42,7 +42,8 @@ class W4A8Error(RuntimeError):
 class _Tuning(ctypes.Structure):
     _fields_ = [("force_splits", ctypes.c_int), ("force_threads_per_row", ctypes.c_int),
                 ("ring_bytes", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("mma_min_m", ctypes.c_int), ("rowdot_max_m", ctypes.c_int)]
+                ("mma_min_m", ctypes.c_int), ("rowdot_max_m", ctypes.c_int),
+                ("mma_e4m3", ctypes.c_int)]
 
 
 _i64, _p, _u = ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint
@@ -445,12 +446,12 @@ def w4a8_device_error(device=None) -> int:
 
 def w4a8_set_tuning(force_splits: int = 0, force_threads_per_row: int = 0,
                     ring_bytes: int = 0, ctas_per_sm: int = 0, mma_min_m: int = 0,
-                    rowdot_max_m: int = 0, reset: bool = False):
+                    rowdot_max_m: int = 0, mma_e4m3: int = 0, reset: bool = False):
     if reset:
         _check(lib().w4a8_set_tuning(None))
         return
     t = _Tuning(force_splits, force_threads_per_row, ring_bytes, ctas_per_sm, mma_min_m,
-                rowdot_max_m)
+                rowdot_max_m, mma_e4m3)
     _check(lib().w4a8_set_tuning(ctypes.byref(t)))
 
 

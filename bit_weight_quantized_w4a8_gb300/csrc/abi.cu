@@ -47,6 +47,14 @@ std::atomic<int> g_ring_bytes{0};
 std::atomic<int> g_ctas_per_sm{0};
 std::atomic<int> g_mma_min_m{0};
 std::atomic<int> g_rowdot_max_m{0};
+std::atomic<int> g_mma_e4m3{0};
+// Row-wise tensor-core calls use bf16 operands by default (measured faster
+// than the e4m3 path at every batch size).
+constexpr bool kDefaultMmaE4m3 = false;
+bool mma_e4m3() {
+    const int v = g_mma_e4m3.load();
+    return v == 0 ? kDefaultMmaE4m3 : v == 2;
+}
 // Batch rows up to which row-wise W4A8 calls take the row-per-thread dp4a
 // kernel (from 2 rows).
 constexpr int kDefaultRowdotMaxM = 8;
@@ -304,7 +312,7 @@ int w4a8_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, const uin
         if ((st = check_mma_workspace(mp, ws, ws_bytes)) != W4A8_OK) return st;
         cudaError_t e = w4a8::launch_w4a8_mma(mp, nullptr, Xq, sa, (int)M, K, 1, &Wq, &sw, &N, &Y,
                                               acc_out, nullptr, nullptr, ws, flags,
-                                              static_cast<cudaStream_t>(stream));
+                                              static_cast<cudaStream_t>(stream), 0, nullptr, mma_e4m3());
         return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_gemv tensor-core launch");
     }
     w4a8::GemvPlan pf, pt;
@@ -346,7 +354,7 @@ int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, cons
         if ((st = check_mma_workspace(mp, ws, ws_bytes)) != W4A8_OK) return st;
         cudaError_t e = w4a8::launch_w4a8_mma(mp, X, nullptr, nullptr, (int)M, K, 1, &Wq, &sw, &N,
                                               &Y, acc_out, Xq_out, sa_out, ws, flags,
-                                              static_cast<cudaStream_t>(stream));
+                                              static_cast<cudaStream_t>(stream), 0, nullptr, mma_e4m3());
         return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear tensor-core launch");
     }
     w4a8::GemvPlan pf, pt;
@@ -409,7 +417,7 @@ int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const ui
         if ((st = check_mma_workspace(mp, ws, ws_bytes)) != W4A8_OK) return st;
         cudaError_t e = w4a8::launch_w4a8_mma(mp, X, nullptr, nullptr, (int)M, K, G, Wq, sw, N, Y,
                                               nullptr, nullptr, nullptr, ws, flags,
-                                              static_cast<cudaStream_t>(stream));
+                                              static_cast<cudaStream_t>(stream), 0, nullptr, mma_e4m3());
         return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear_grouped tensor-core launch");
     }
     w4a8::GemvPlan pf, pt;
@@ -606,6 +614,7 @@ int w4a8_set_tuning(const w4a8_tuning_t* t) {
         g_ctas_per_sm = 0;
         g_mma_min_m = 0;
         g_rowdot_max_m = 0;
+        g_mma_e4m3 = 0;
         return ok();
     }
     if (t->force_splits < 0 || t->force_splits > 16)
@@ -627,6 +636,8 @@ int w4a8_set_tuning(const w4a8_tuning_t* t) {
     g_ctas_per_sm = t->ctas_per_sm;
     g_mma_min_m = t->mma_min_m;
     g_rowdot_max_m = t->rowdot_max_m;
+    if (t->mma_e4m3 < 0 || t->mma_e4m3 > 2) return fail(W4A8_ERR_SHAPE, "mma_e4m3 must be 0, 1 or 2");
+    g_mma_e4m3 = t->mma_e4m3;
     return ok();
 }
 

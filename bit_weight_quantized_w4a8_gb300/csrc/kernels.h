@@ -53,7 +53,7 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
                             const float* const* sw, const int64_t* Ns, float* const* Y,
                             int32_t* acc_out, int8_t* Xq_out, float* sa_out, void* ws,
                             unsigned flags, cudaStream_t stream, int gs = 0,
-                            const float* const* sg = nullptr);
+                            const float* const* sg = nullptr, bool e4m3 = false);
 cudaError_t read_and_clear_mma_error(unsigned* flags, cudaStream_t stream);
 // Tensor map of packed INT4 weights [N][K/2] for 2-D TMA boxes of 128 bytes
 // (256 codes) x 128 rows, 128-byte swizzle; `map` is a 64-byte aligned

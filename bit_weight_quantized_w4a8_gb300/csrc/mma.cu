@@ -33,6 +33,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -86,6 +87,10 @@ constexpr int kStagesG = 2;
 constexpr uint32_t kTmemF = 64;
 constexpr uint32_t kTmemAG = 128;
 static_assert(kTmemAG + kTmemAStage * kStagesG <= kTmemCols, "TMEM budget (group scales)");
+// e4m3 path: D (2 x 64 columns: W.A_hi, W.A_lo) at 0..127, A stages of 32
+// columns at 128 + 32 s
+constexpr uint32_t kTmemAF8 = 128;
+static_assert(kTmemAF8 + 32 * kStages <= kTmemCols, "TMEM budget (e4m3)");
 
 struct MmaArgs {
     CUtensorMap tmW;        // packed weights [N][K/2] uint8, box 128 bytes x 128 rows
@@ -214,6 +219,112 @@ __global__ void __launch_bounds__(kAQThreads) act_codes_kernel(
     }
 }
 
+// The same for the e4m3 operand path: an INT8 code a = 16 a_hi + a_lo with
+// a_hi = a >> 4 in [-8, 7] and a_lo = a & 15 in [0, 15], both exact in
+// e4m3.  Per 128-code K tile t the B operand is [2 BN][128] bytes at
+// t * 2 BN * 128: rows 0..BN-1 hold a_hi of the batch rows, BN..2BN-1 a_lo,
+// 128-byte swizzled (16-byte chunk c of row m at m * 128 + (c ^ (m % 8)) * 16).
+// One MMA then yields W.A_hi and W.A_lo side by side in D, and the integer
+// product is 16 D_hi + D_lo.  Thread u handles 16 codes (one chunk).
+__device__ __forceinline__ uint32_t e4m3x4(int v0, int v1, int v2, int v3) {
+    return (uint32_t)__nv_cvt_float_to_fp8((float)v0, __NV_SATFINITE, __NV_E4M3) |
+           ((uint32_t)__nv_cvt_float_to_fp8((float)v1, __NV_SATFINITE, __NV_E4M3) << 8) |
+           ((uint32_t)__nv_cvt_float_to_fp8((float)v2, __NV_SATFINITE, __NV_E4M3) << 16) |
+           ((uint32_t)__nv_cvt_float_to_fp8((float)v3, __NV_SATFINITE, __NV_E4M3) << 24);
+}
+
+__global__ void __launch_bounds__(kAQThreads) act_codes_e4m3_kernel(
+    const __half* __restrict__ X, const int8_t* __restrict__ Xq, const float* __restrict__ sa_in,
+    int M, int64_t K, int BN, uint8_t* __restrict__ B, float* __restrict__ sa_ws,
+    int8_t* __restrict__ Xq_out, float* __restrict__ sa_out, int32_t* __restrict__ acc,
+    int64_t acc_words) {
+    __shared__ float red[kAQThreads / 32];
+    griddep_launch_dependents();
+    griddep_wait();
+    for (int64_t e = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * kAQThreads + threadIdx.x; e < acc_words;
+         e += (int64_t)gridDim.x * gridDim.y * kAQThreads)
+        acc[e] = 0;
+    const int m = blockIdx.x;
+    const int64_t u = (int64_t)blockIdx.y * kAQThreads + threadIdx.x;  // chunk of 16 codes
+    const int64_t nchunks = (K + 127) / 128 * 8;                        // incl. the padding to a K tile
+    const int64_t kchunks = K / 16;                                      // K % 32 == 0
+    const int64_t t = u >> 3;
+    const int c = (int)(u & 7);
+    const size_t tile = (size_t)t * 2 * BN * 128;
+    uint4* dhi = reinterpret_cast<uint4*>(B + tile + (size_t)m * 128 + ((c ^ (m & 7)) << 4));
+    const int ml = BN + m;
+    uint4* dlo = reinterpret_cast<uint4*>(B + tile + (size_t)ml * 128 + ((c ^ (ml & 7)) << 4));
+    if (m >= M) {
+        if (u < nchunks) *dhi = *dlo = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    float s;
+    const uint4* xv = reinterpret_cast<const uint4*>(X + (int64_t)m * K);
+    if (X == nullptr) {
+        s = sa_in[m];
+    } else {
+        __half2 hm = __float2half2_rn(0.f);
+        #pragma unroll 4
+        for (int64_t v = threadIdx.x; v < K / 8; v += kAQThreads) {
+            const uint4 h = xv[v];
+            const __half2* p2 = reinterpret_cast<const __half2*>(&h);
+            #pragma unroll
+            for (int q = 0; q < 4; ++q) hm = __hmax2(hm, __habs2(p2[q]));
+        }
+        float mx = fmaxf(__low2float(hm), __high2float(hm));
+        #pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+        __syncthreads();
+        mx = 0.f;
+        #pragma unroll
+        for (int w = 0; w < kAQThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+        s = __fdiv_rn(mx, 127.f);
+    }
+    if (u < nchunks) {
+        uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
+        if (u < kchunks) {
+            uint32_t c8[4];  // the 16 codes in natural order
+            if (X != nullptr) {
+                float r_lo, r_hi;
+                quant_bracket(s, &r_lo, &r_hi);
+                #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint2 q = quant8_split(xv[2 * u + h], s, r_lo, r_hi);  // even / odd codes
+                    c8[2 * h] = __byte_perm(q.x, q.y, 0x5140);
+                    c8[2 * h + 1] = __byte_perm(q.x, q.y, 0x7362);
+                }
+                if (Xq_out != nullptr)
+                    *reinterpret_cast<uint4*>(Xq_out + (int64_t)m * K + 16 * u) =
+                        make_uint4(c8[0], c8[1], c8[2], c8[3]);
+            } else {
+                const uint4 cq = *reinterpret_cast<const uint4*>(Xq + (int64_t)m * K + 16 * u);
+                c8[0] = cq.x;
+                c8[1] = cq.y;
+                c8[2] = cq.z;
+                c8[3] = cq.w;
+            }
+            uint32_t h4[4], l4[4];
+            #pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                int a[4];
+                #pragma unroll
+                for (int b = 0; b < 4; ++b) a[b] = (int)(int8_t)((c8[w] >> (8 * b)) & 0xFFu);
+                h4[w] = e4m3x4(a[0] >> 4, a[1] >> 4, a[2] >> 4, a[3] >> 4);
+                l4[w] = e4m3x4(a[0] & 15, a[1] & 15, a[2] & 15, a[3] & 15);
+            }
+            hi = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+            lo = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+        }
+        *dhi = hi;
+        *dlo = lo;
+    }
+    if (blockIdx.y == 0 && threadIdx.x == 0) {
+        sa_ws[m] = s;
+        if (sa_out != nullptr) sa_out[m] = s;
+    }
+}
+
 // One packed word (8 INT4 codes, low nibble first) -> 8 bf16 values.
 // n ^ 8 = q + 8 in [0, 15] placed in the mantissa of bf16 128.0 (0x4300)
 // is 136 + q exactly; subtracting 136 gives q.
@@ -233,6 +344,24 @@ __device__ __forceinline__ uint4 int4x8_to_bf16(uint32_t w) {
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// One packed word (8 INT4 codes) -> 8 e4m3 values in K order (two words):
+// each code pair as binary16 (n ^ 8 in the mantissa of 1024.0, minus 1032:
+// exact), then a pair conversion to e4m3 (exact for -8..7).
+__device__ __forceinline__ uint2 int4x8_to_e4m3(uint32_t w) {
+    const uint32_t u = w ^ 0x88888888u;
+    const uint32_t h = u >> 4;
+    const __half2 bias = __floats2half2_rn(1032.f, 1032.f);
+    uint32_t e[4];
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t x = (__byte_perm(u, h, (uint32_t)(j | ((4 + j) << 8))) & 0x000F000Fu) | 0x64006400u;
+        const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
+        e[j] = (uint32_t)__nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&v),
+                                                     __NV_SATFINITE, __NV_E4M3);
+    }
+    return make_uint2(e[0] | (e[1] << 16), e[2] | (e[3] << 16));
+}
+
 // Two CTAs per SM (shared memory < 113 KB, 256 TMEM columns, <= 93
 // registers): the SM's tensor core then interleaves two MMA streams, each at
 // the issue rate of one.
@@ -245,10 +374,19 @@ __device__ __forceinline__ uint4 int4x8_to_bf16(uint32_t w) {
 // next group.  A converter warp does the readout of a group before it
 // converts the stage `lag` stages past the group's end, so every wait
 // points at earlier work.
-template <bool kG>
+//
+// kF8 (row-wise scales only): the e4m3 operand path.  Weight codes are
+// widened to e4m3 (four per TMEM column, a stage of 128 codes in 32
+// columns), the activation tiles hold a_hi and a_lo as 2 BN rows, and each
+// MMA (kind::f8f6f4, K = 32) covers twice the weights of a kind::f16 MMA;
+// D holds W.A_hi in columns 0..BN-1 and W.A_lo in BN..2BN-1, both exact
+// integers in fp32, and acc = 16 D_hi + D_lo.
+template <bool kG, bool kF8>
 __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_constant__ MmaArgs a) {
+    static_assert(!(kG && kF8), "the e4m3 path has row-wise scales only");
     constexpr int S = kG ? kStagesG : kStages;          // stage ring in use
-    constexpr uint32_t kA0 = kG ? kTmemAG : kTmemA;     // first A stage column
+    constexpr uint32_t kA0 = kF8 ? kTmemAF8 : kG ? kTmemAG : kTmemA;  // first A stage column
+    constexpr uint32_t kAStage = kF8 ? 32 : kTmemAStage;               // A columns per stage
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles
     const uint32_t raw = smem_u32(smem_raw);
@@ -338,7 +476,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
         // ---- MMA issuer (one lane): per stage up to kStageK K blocks of
         // four K = 16 steps, then one commit that frees the stage
         if (lane == 0) {
-            const uint32_t idesc = bf16_idesc(kTileRows, BN);
+            const uint32_t idesc = kF8 ? e4m3_idesc(kTileRows, 2 * BN) : bf16_idesc(kTileRows, BN);
             for (int st = 0; st < nst; ++st) {
                 const int s = st % S;
                 const uint32_t ph = (st / S) & 1;
@@ -354,8 +492,15 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                 if (!wait_bounded(smem_u32(bfull + s), ph, abort_flag)) break;
                 tc_fence_after_sync();
                 const int nkb = min(kStageK, nk - kStageK * st);
-                const uint32_t at = tmem + kA0 + kTmemAStage * s;
-                for (int j = 0; j < nkb; ++j) {
+                const uint32_t at = tmem + kA0 + kAStage * s;
+                if constexpr (kF8) {
+                    // one [2 BN][128] e4m3 tile a stage (zero past K): four K = 32 steps
+                    const uint64_t bd = sw128_desc(sbase + kOffB + s * kBStageMax);
+                    #pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        tc_mma_e4m3_tmem_a(d_tmem, at + 8 * k, bd + 2 * k, idesc, st > 0 || k > 0);
+                }
+                for (int j = 0; j < (kF8 ? 0 : nkb); ++j) {
                     const uint64_t bd = sw128_desc(sbase + kOffB + s * kBStageMax + j * b_bytes);
                     #pragma unroll
                     for (int k = 0; k < kKBlock / 16; ++k) {  // 8 TMEM columns of A, 32 bytes of B a step
@@ -379,7 +524,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                 const int s = st % S;
                 if (st >= S && !wait_bounded(smem_u32(sempty + s), ((st / S) - 1) & 1, abort_flag))
                     break;
-                const uint32_t bytes = (uint32_t)min(kStageK, nk - kStageK * st) * b_bytes;
+                const uint32_t bytes = kF8 ? (uint32_t)kStageK * b_bytes
+                                           : (uint32_t)min(kStageK, nk - kStageK * st) * b_bytes;
                 mbar_arrive_expect_tx(smem_u32(bfull + s), bytes);
                 bulk_g2s(sbase + kOffB + s * kBStageMax, a.codes + (size_t)(kb0 + kStageK * st) * b_bytes,
                          bytes, smem_u32(bfull + s), pol);
@@ -454,8 +600,23 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
             if (st >= S &&
                 !__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(sempty + s), ((st / S) - 1) & 1, abort_flag)))
                 break;
+            if constexpr (kF8) {  // word w of K block j = codes 64 j + 8 w .. + 7 -> columns 16 j + 2 w, + 1
+                uint32_t v[32];
+                #pragma unroll
+                for (int j = 0; j < kStageK; ++j) {
+                    const uint32_t w8[8] = {c16[2 * j].x, c16[2 * j].y, c16[2 * j].z, c16[2 * j].w,
+                                            c16[2 * j + 1].x, c16[2 * j + 1].y, c16[2 * j + 1].z, c16[2 * j + 1].w};
+                    #pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const uint2 o = int4x8_to_e4m3(w8[w]);
+                        v[16 * j + 2 * w] = o.x;
+                        v[16 * j + 2 * w + 1] = o.y;
+                    }
+                }
+                tmem_st32(lanes + kA0 + kAStage * s, v);
+            }
             #pragma unroll
-            for (int j = 0; j < kStageK; ++j) {  // word w of K block j = codes 8w .. 8w+7 -> columns 4w .. 4w+3
+            for (int j = 0; j < (kF8 ? 0 : kStageK); ++j) {  // word w of K block j = codes 8w .. 8w+7 -> columns 4w .. 4w+3
                 const uint32_t w8[8] = {c16[2 * j].x, c16[2 * j].y, c16[2 * j].z, c16[2 * j].w,
                                         c16[2 * j + 1].x, c16[2 * j + 1].y, c16[2 * j + 1].z, c16[2 * j + 1].w};
                 uint32_t v[32];
@@ -467,7 +628,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                     v[4 * w + 2] = o.z;
                     v[4 * w + 3] = o.w;
                 }
-                tmem_st32(lanes + kA0 + kTmemAStage * s + 32 * j, v);
+                tmem_st32(lanes + kA0 + kAStage * s + 32 * j, v);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -529,14 +690,17 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
             const int n = n0 + r;
             const float swv = (ok && n < a.N) ? a.sw[n] : 0.f;
             for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
-                uint32_t v[8];
+                uint32_t v[8], vl[8];
                 tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(8 * ch), v);
+                if constexpr (kF8) tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN + 8 * ch), vl);
                 if (!ok || n >= a.N) continue;
                 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     const int m = 8 * ch + t;
                     if (m >= a.M) break;
-                    const int32_t acc = __float2int_rn(__uint_as_float(v[t]));
+                    const int32_t acc = kF8 ? 16 * __float2int_rn(__uint_as_float(v[t])) +
+                                                  __float2int_rn(__uint_as_float(vl[t]))
+                                            : __float2int_rn(__uint_as_float(v[t]));
                     const int64_t o = (int64_t)m * a.N + n;
                     if (a.P == 1) {
                         a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), swv), a.sa[m]);
@@ -690,7 +854,8 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int g
     // (every tile) or when a matrix has fewer tiles than 4/5 of the CTA slots.
     pl.off_sa = kTicketBytes;
     pl.off_codes = pl.off_sa + 256;
-    pl.off_part = round_up_sz(pl.off_codes + (size_t)pl.nkb * pl.BN * kKBlock * 2, 256);
+    // (K blocks rounded up to an even count: the e4m3 tiles cover 128 codes)
+    pl.off_part = round_up_sz(pl.off_codes + (size_t)((pl.nkb + 1) / 2 * 2) * pl.BN * kKBlock * 2, 256);
     const int64_t small = 2 * num_sms * 4 / 5;
     const int64_t tmax = pmin > 1 ? pl.tiles : (pl.tiles < small ? pl.tiles : small);
     // group scales: fp32 partials per tile and piece; a matrix split into
@@ -705,8 +870,10 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
                             int M, int64_t K, int G, const uint8_t* const* Wq,
                             const float* const* sw, const int64_t* Ns, float* const* Y,
                             int32_t* acc_out, int8_t* Xq_out, float* sa_out, void* ws,
-                            unsigned flags, cudaStream_t stream, int gs, const float* const* sg) {
+                            unsigned flags, cudaStream_t stream, int gs, const float* const* sg,
+                            bool e4m3) {
     const int gkb = gs > 0 ? gs / kKBlock : 0;
+    if (e4m3 && gkb) return cudaErrorInvalidValue;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     float* sa_ws = reinterpret_cast<float*>(wsb + pl.off_sa);
     uint8_t* codes = wsb + pl.off_codes;
@@ -717,9 +884,11 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
         int32_t* acc = reinterpret_cast<int32_t*>(wsb + pl.off_part);
         int64_t acc_words = (int64_t)((pl.ws_bytes - pl.off_part) / 4);
         void* args[] = {&xh, &Xq, &sa, &Mi, &Kk, &BNi, &codes, &sa_ws, &Xq_out, &sa_out, &acc, &acc_words};
-        const unsigned pieces = (unsigned)(((int64_t)pl.nkb * 8 + kAQThreads - 1) / kAQThreads);
-        cudaError_t e = launch_pdl(reinterpret_cast<const void*>(act_codes_kernel), dim3(pl.BN, pieces),
-                                   dim3(kAQThreads), 0, stream, flags, args);
+        const int64_t vecs = e4m3 ? (K + 127) / 128 * 8 : (int64_t)pl.nkb * 8;  // per batch row
+        const unsigned pieces = (unsigned)((vecs + kAQThreads - 1) / kAQThreads);
+        const void* pre = e4m3 ? reinterpret_cast<const void*>(act_codes_e4m3_kernel)
+                               : reinterpret_cast<const void*>(act_codes_kernel);
+        cudaError_t e = launch_pdl(pre, dim3(pl.BN, pieces), dim3(kAQThreads), 0, stream, flags, args);
         if (e != cudaSuccess) return e;
     }
     static int attr_set[64] = {0};
@@ -727,9 +896,11 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+        e = cudaFuncSetAttribute(mma_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+        e = cudaFuncSetAttribute(mma_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(mma_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = 1;
     }
@@ -762,8 +933,9 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
         a.nkb = pg.nkb;
         a.kbp = pg.kbp;
         void* args[] = {&a};
-        const void* fn = gkb ? reinterpret_cast<const void*>(mma_kernel<true>)
-                             : reinterpret_cast<const void*>(mma_kernel<false>);
+        const void* fn = gkb ? reinterpret_cast<const void*>(mma_kernel<true, false>)
+                       : e4m3 ? reinterpret_cast<const void*>(mma_kernel<false, true>)
+                              : reinterpret_cast<const void*>(mma_kernel<false, false>);
         e = launch_pdl(fn, dim3(pg.grid), dim3(kMmaThreads),
                        kMmaSmem, stream, flags, args);
         if (e != cudaSuccess) return e;

@@ -81,6 +81,19 @@ __device__ __forceinline__ void tc_mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_t
         : "memory");
 }
 
+// The same for kind::f8f6f4 with e4m3 operands: A (128 rows x 32 e4m3) in
+// TMEM, row i in lane i, four consecutive K values per 32-bit column (lowest
+// K in the low byte), so one K=32 step spans 8 columns.
+__device__ __forceinline__ void tc_mma_e4m3_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                   uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
 // Warp-collective store of 32 consecutive 32-bit columns into this warp's
 // 32 TMEM lanes (thread t writes lane base + t), then wait for it.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
@@ -143,6 +156,12 @@ __host__ __device__ constexpr uint64_t sw128_desc(uint32_t smem_addr) {
 __host__ __device__ constexpr uint32_t bf16_idesc(int m, int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(m >> 4) << 24);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with e4m3 A and B
+// (format code 0 in bits 7-9 and 10-12), D fp32, both K-major.
+__host__ __device__ constexpr uint32_t e4m3_idesc(int m, int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 }  // namespace w4a8

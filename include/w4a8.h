@@ -377,6 +377,9 @@ int w4a8_device_error(unsigned* flags, void* stream);
  *     row-per-thread kernel, from 2 rows (0 = default 8, 1 = never, <= 8);
  *     it takes precedence over mma_min_m.  force_threads_per_row 2, 4 or 8
  *     sets that kernel's threads per weight row.
+ *   mma_e4m3: operands of the row-wise tensor-core kernel: 0 = default,
+ *     1 = bf16 (kind::f16, K = 16 per MMA), 2 = e4m3 (kind::f8f6f4, K = 32
+ *     per MMA, activation codes split as 16 a_hi + a_lo).
  * w4a8_workspace_bytes reflects the overrides.  NULL restores the defaults.
  * Not synchronised with calls running on other threads. */
 typedef struct {
@@ -386,6 +389,7 @@ typedef struct {
     int ctas_per_sm;
     int mma_min_m;
     int rowdot_max_m;
+    int mma_e4m3;
 } w4a8_tuning_t;
 
 int w4a8_set_tuning(const w4a8_tuning_t* tuning);

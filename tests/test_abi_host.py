@@ -194,6 +194,10 @@ def test_kernel_routing():
             check_rowdot_plan(p, 5, 3584, 18944, 152)
         with pytest.raises(w4.W4A8Error):
             w4.w4a8_set_tuning(rowdot_max_m=9)
+        with pytest.raises(w4.W4A8Error):
+            w4.w4a8_set_tuning(mma_e4m3=3)
+        w4.w4a8_set_tuning(mma_e4m3=2, rowdot_max_m=1)  # operand type does not change the plan
+        assert w4.w4a8_plan_info(4, 3584, 18944, num_sms=152)["kernel"] == 1
         # group scales: the row-per-thread kernel at 2..8 rows, the tensor cores above
         w4.w4a8_set_tuning()
         assert w4.w4a8g_plan_info(4, 3584, 18944, 128, num_sms=152)["kernel"] == 2

@@ -235,14 +235,16 @@ def test_w4a8_fused_ties(w4, orc, M, K, N, splits):
 @pytest.mark.parametrize("M,K,N,seed", [(2, 3584, 300, 100), (5, 896, 129, 101), (15, 128, 256, 102),
                                         (16, 18944, 200, 103), (24, 96, 1, 104), (64, 3584, 129, 105)])
 @pytest.mark.parametrize("fused", [True, False])
-def test_w4a8_tensor_cores(w4, orc, M, K, N, seed, fused):
-    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1)
+@pytest.mark.parametrize("ops", [1, 2], ids=["bf16", "e4m3"])
+def test_w4a8_tensor_cores(w4, orc, M, K, N, seed, fused, ops):
+    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, mma_e4m3=ops)
     assert w4.w4a8_plan_info(M, K, N)["kernel"] == 1
     check_w4a8(w4, orc, M, K, N, seed, fused=fused, zero_rows=(0,))
 
 
-def test_w4a8_tensor_cores_grouped(w4, orc):
-    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1)
+@pytest.mark.parametrize("ops", [1, 2], ids=["bf16", "e4m3"])
+def test_w4a8_tensor_cores_grouped(w4, orc, ops):
+    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, mma_e4m3=ops)
     M, K, Ns = 18, 1024, (300, 7, 129)
     X = synth.activation(110, M, K, outlier_frac=0.001)
     Wqs, sws, refs = [], [], []
@@ -260,13 +262,14 @@ def test_w4a8_tensor_cores_grouped(w4, orc):
             assert np.array_equal(bits(Y.cpu().numpy()), bits(ref))
 
 
+@pytest.mark.parametrize("ops", [1, 2], ids=["bf16", "e4m3"])
 @pytest.mark.parametrize("K", [16384, 32768])
-def test_w4a8_tensor_cores_largest_sums(w4, K):
+def test_w4a8_tensor_cores_largest_sums(w4, K, ops):
     """Every weight code -8 (nibble 0x8, legal on input) against activation
     codes +127 and -127: each K piece's partial sum reaches 8 * 127 * 16384 =
     16,646,144, just below 2^24, which the fp32 accumulator must hold
     exactly; the pieces are added as int32."""
-    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1)
+    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, mma_e4m3=ops)
     M, N = 16, 130
     Wq = torch.full((N, K // 2), 0x88, dtype=torch.uint8, device="cuda")
     sw = torch.ones((N,), dtype=torch.float32, device="cuda")
