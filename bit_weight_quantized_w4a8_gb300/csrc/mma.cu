@@ -4,7 +4,7 @@
 // The arithmetic is the W4A8 contract of the Jetson INT4 page (sections
 // 正确方向 / 当前实现方式): INT8 activation codes times INT4 weight codes,
 // summed exactly in integers, y = ((float)acc * s_w) * s_a.  Both code sets
-// are small integers and so exact in bf16; tcgen05.mma kind::f16 multiplies
+// are small integers and so exact in binary16; tcgen05.mma kind::f16 multiplies
 // them exactly and accumulates in fp32 in TMEM.  Every partial sum of one
 // K piece is an integer of magnitude <= 8 * 127 * 16384 < 2^24, so the fp32
 // accumulator holds it exactly whatever the summation order; pieces are
@@ -14,16 +14,17 @@
 // Two kernels:
 //  * act_codes_kernel (one CTA per activation row): the per-row INT8
 //    quantization (max|x|, s_a = max/127, IEEE division, round half away,
-//    clamp), written as bf16 codes [M][K] for the tensor cores (plus the
+//    clamp), written as binary16 codes for the tensor cores (plus the
 //    optional int8 codes and scale outputs); or, for the unfused entry,
-//    the given int8 codes widened to bf16.
+//    the given int8 codes widened to binary16.
 //  * mma_kernel: one CTA per 128 weight rows and K piece.  Warp 0 streams
 //    packed INT4 tiles (128 rows x 64 K = 4 KB) with 2-D TMA into a deep
-//    ring; warp 2 streams the bf16 activation tiles (TMA, 128-byte
+//    ring; warp 2 streams the binary16 activation tiles (TMA, 128-byte
 //    swizzle) into their own ring; warp 1 issues the MMAs (M = 128 weight
 //    rows, N = 16..64 batch rows, K = 16, four per tile) into a TMEM
-//    accumulator; warps 3-10 widen each weight row's INT4 codes to bf16
-//    (nibble ^ 8 placed in the mantissa of 128.0, minus 136) straight into
+//    accumulator; warps 3-10 widen each weight row's INT4 codes to binary16
+//    (two nibbles at a time masked into the mantissa of 1024.0, in a K
+//    order permuted inside each 8-code group, as are the activations) straight into
 //    TMEM, where the MMA reads its A operand (so the widened weights never
 //    pass through shared memory, whose bandwidth would otherwise bound the
 //    kernel), then read the accumulator back (tcgen05.ld), convert to
@@ -203,11 +204,13 @@ __global__ void __launch_bounds__(kAQThreads) act_codes_kernel(
                 c8[0] = c.x;
                 c8[1] = c.y;
             }
+            // binary16 pairs in the permuted K order of the weight
+            // converters: pair t = codes (t, t + 4) of the 8
             #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                const uint32_t w = c8[t >> 1] >> (16 * (t & 1));
-                const __nv_bfloat162 v = __floats2bfloat162_rn((float)(int8_t)(w & 0xFFu),
-                                                               (float)(int8_t)((w >> 8) & 0xFFu));
+                const int lo = (int)(int8_t)((c8[0] >> (8 * t)) & 0xFFu);
+                const int hi = (int)(int8_t)((c8[1] >> (8 * t)) & 0xFFu);
+                const __half2 v = __floats2half2_rn((float)lo, (float)hi);
                 o[t] = *reinterpret_cast<const uint32_t*>(&v);
             }
         }
@@ -325,23 +328,29 @@ __global__ void __launch_bounds__(kAQThreads) act_codes_e4m3_kernel(
     }
 }
 
-// One packed word (8 INT4 codes, low nibble first) -> 8 bf16 values.
-// n ^ 8 = q + 8 in [0, 15] placed in the mantissa of bf16 128.0 (0x4300)
-// is 136 + q exactly; subtracting 136 gives q.
-__device__ __forceinline__ uint4 int4x8_to_bf16(uint32_t w) {
-    const uint32_t u = w ^ 0x88888888u;
-    const uint32_t h = u >> 4;
-    const __nv_bfloat162 bias = __floats2bfloat162_rn(136.f, 136.f);
-    uint32_t o[4];
-    #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        // byte j of u (even code 2j in its low nibble) to bits 0-3,
-        // byte j of u >> 4 (odd code 2j+1) to bits 16-19
-        const uint32_t x = (__byte_perm(u, h, (uint32_t)(j | ((4 + j) << 8))) & 0x000F000Fu) | 0x43004300u;
-        const __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&x), bias);
-        o[j] = *reinterpret_cast<const uint32_t*>(&v);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
+// One packed word (8 INT4 codes, low nibble first) -> 8 binary16 values in
+// the permuted K order (t, t + 4) per 32-bit pair, t = 0..3, the order the
+// activation tiles use too (a fixed permutation of K inside each 8-code
+// group leaves the dot product unchanged).  Nibbles 0 and 4 masked in place
+// and xor'ed into the mantissa of 1024.0 give 1024 + (n ^ 8) = 1032 + q;
+// nibbles 1 and 5 masked in place give 1024 + 16 (q + 8), scaled by 1/16
+// with one fma; the word shifted by 8 gives nibbles 2, 6 and 3, 7.  Every
+// step is exact: 4 mask-xor, 1 shift and 4 half2 operations per 8 codes.
+__device__ __forceinline__ uint4 int4x8_to_f16(uint32_t w) {
+    const uint32_t w2 = w >> 8;
+    const uint32_t x0 = (w & 0x000F000Fu) ^ 0x64086408u;   // codes 0, 4: 1032 + q
+    const uint32_t x1 = (w & 0x00F000F0u) ^ 0x64806480u;   // codes 1, 5: 1024 + 16 (q + 8)
+    const uint32_t x2 = (w2 & 0x000F000Fu) ^ 0x64086408u;  // codes 2, 6
+    const uint32_t x3 = (w2 & 0x00F000F0u) ^ 0x64806480u;  // codes 3, 7
+    const __half2 b0 = __floats2half2_rn(1032.f, 1032.f);
+    const __half2 s1 = __floats2half2_rn(0.0625f, 0.0625f);
+    const __half2 b1 = __floats2half2_rn(-72.f, -72.f);
+    const __half2 v0 = __hsub2(*reinterpret_cast<const __half2*>(&x0), b0);
+    const __half2 v1 = __hfma2(*reinterpret_cast<const __half2*>(&x1), s1, b1);
+    const __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&x2), b0);
+    const __half2 v3 = __hfma2(*reinterpret_cast<const __half2*>(&x3), s1, b1);
+    return make_uint4(*reinterpret_cast<const uint32_t*>(&v0), *reinterpret_cast<const uint32_t*>(&v1),
+                      *reinterpret_cast<const uint32_t*>(&v2), *reinterpret_cast<const uint32_t*>(&v3));
 }
 
 // One packed word (8 INT4 codes) -> 8 e4m3 values in K order (two words):
@@ -476,7 +485,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
         // ---- MMA issuer (one lane): per stage up to kStageK K blocks of
         // four K = 16 steps, then one commit that frees the stage
         if (lane == 0) {
-            const uint32_t idesc = kF8 ? e4m3_idesc(kTileRows, 2 * BN) : bf16_idesc(kTileRows, BN);
+            const uint32_t idesc = kF8 ? e4m3_idesc(kTileRows, 2 * BN) : f16_idesc(kTileRows, BN);
             for (int st = 0; st < nst; ++st) {
                 const int s = st % S;
                 const uint32_t ph = (st / S) & 1;
@@ -505,7 +514,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                     #pragma unroll
                     for (int k = 0; k < kKBlock / 16; ++k) {  // 8 TMEM columns of A, 32 bytes of B a step
                         const bool acc = kG ? !(first && j == 0 && k == 0) : (st > 0 || j > 0 || k > 0);
-                        tc_mma_bf16_tmem_a(d_tmem, at + 32 * j + 8 * k, bd + 2 * k, idesc, acc);
+                        tc_mma_f16_tmem_a(d_tmem, at + 32 * j + 8 * k, bd + 2 * k, idesc, acc);
                     }
                 }
                 tc_commit(smem_u32(sempty + s));
@@ -622,7 +631,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                 uint32_t v[32];
                 #pragma unroll
                 for (int w = 0; w < 8; ++w) {
-                    const uint4 o = int4x8_to_bf16(w8[w]);
+                    const uint4 o = int4x8_to_f16(w8[w]);
                     v[4 * w] = o.x;
                     v[4 * w + 1] = o.y;
                     v[4 * w + 2] = o.z;

@@ -69,9 +69,9 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
-// The same with the A operand (128 rows x 16 bf16) in TMEM: row i in lane
-// i, two bf16 per 32-bit column, so one K=16 step spans 8 columns.
-__device__ __forceinline__ void tc_mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+// The same with the A operand (128 rows x 16 16-bit values) in TMEM: row i
+// in lane i, two values per 32-bit column, so one K=16 step spans 8 columns.
+__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                    uint32_t idesc, bool accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -156,6 +156,11 @@ __host__ __device__ constexpr uint64_t sw128_desc(uint32_t smem_addr) {
 __host__ __device__ constexpr uint32_t bf16_idesc(int m, int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(m >> 4) << 24);
+}
+
+// The same with binary16 A and B (format code 0).
+__host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4 with e4m3 A and B
