@@ -89,6 +89,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sample-stride", type=int, default=CPU_SAMPLE_STRIDE,
+                    help="the oracle's sample: every n-th output row of each linear")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the 28-layer step, the skinny-batch sweep and the W8A16 set")
     ap.add_argument("--min-busy-s", type=float, default=0.6,
@@ -241,18 +243,22 @@ def profiled_traffic():
     return t.get("dram_bytes_per_launch")
 
 
-def cpu_sample_inputs(dev):
-    """Every CPU_SAMPLE_STRIDE-th output row of each linear, quantized by the
-    oracle on the host (weights drawn by the generator's GPU twin: same bits)."""
+def cpu_sample_inputs(dev, stride=CPU_SAMPLE_STRIDE):
+    """Every stride-th output row of each linear, quantized by the oracle on
+    the host (weights drawn by the generator's GPU twin, or on the host when
+    dev is None: the same bits)."""
     import oracle
     import synth
     orc = oracle.load()
     out = []
     for idx, (name, K, N) in enumerate(LINEARS):
         seed = WEIGHT_SEED0 + idx
-        W = synth.normal_gpu(seed, (N, K), 0.02, device=dev)
-        W_rows = W[::CPU_SAMPLE_STRIDE].cpu().numpy()
-        del W
+        if dev is None:
+            W_rows = synth.weight_rows(seed, N, K, range(0, N, stride))
+        else:
+            W = synth.normal_gpu(seed, (N, K), 0.02, device=dev)
+            W_rows = W[::stride].cpu().numpy()
+            del W
         Wq, sw = orc.w4_quantize(W_rows)
         X = synth.activation(activation_seed(name), 1, K, outlier_frac=OUTLIER_FRAC)
         out.append((X, Wq, sw, N))
@@ -307,15 +313,9 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     dev = torch.device("cuda") if torch.cuda.is_available() else None
-    import oracle
-    import synth
-    orc = oracle.load()
-    if dev is not None:
-        orc, inputs = cpu_sample_inputs(dev)
-        sample = "every %dth output row of each linear (%.1f%% of the set's weights)" % (
-            CPU_SAMPLE_STRIDE, 100.0 / CPU_SAMPLE_STRIDE)
-    else:
-        raise SystemExit(json.dumps({"impl": "reference", "unavailable": "no CUDA device for input generation"}))
+    orc, inputs = cpu_sample_inputs(dev, args.sample_stride)
+    sample = "every %dth output row of each linear (%.2f%% of the set's weights)" % (
+        args.sample_stride, 100.0 / args.sample_stride)
     for _ in range(args.warmup):
         for (X, Wq, sw, _) in inputs:
             orc.w4a8_linear(X, Wq, sw)
@@ -563,13 +563,13 @@ def run_ours(args, world, rank):
     }
     line.update(extra)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        orc, inputs = cpu_sample_inputs(dev)
+        orc, inputs = cpu_sample_inputs(dev, args.sample_stride)
         t_set, reps = time_oracle_sample(orc, inputs)
         line["cpu_baseline"] = {
             "value": round(SET_BYTES / t_set / 1e9, 4), "unit": "GB/s", "cores": 1,
             "kind": "oracle", "us_per_set": round(t_set * 1e6, 1),
             "sample": "every %dth output row of each linear, %d repetitions, scaled to the full set"
-                      % (CPU_SAMPLE_STRIDE, reps)}
+                      % (args.sample_stride, reps)}
         threads = os.cpu_count() or 1
         t_all, reps_all = time_oracle_sample_threads(orc, inputs, threads)
         line["cpu_baseline"]["all_cores"] = {
