@@ -180,6 +180,16 @@ def test_w4a8_gemv_unfused(w4, orc, M, K, N, seed, path):
     check_w4a8(w4, orc, M, K, N, seed, fused=False)
 
 
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("M,K,N,seed", [(1, 18944, 3584, 33), (1, 3584, 18944, 34), (1, 13696, 700, 35)])
+def test_w4a8_one_row_plans_fused_and_unfused(w4, orc, M, K, N, seed, fused):
+    """The fused and unfused one-row kernels share each shape's plan (ring
+    depth, staging, splits): both must run it to completion, bit-exact and
+    with no wait timing out, at the long-row and the wide shapes."""
+    check_w4a8(w4, orc, M, K, N, seed, fused=fused)
+    assert w4.w4a8_device_error() == 0
+
+
 @pytest.mark.parametrize("splits", [2, 3, 5, 16])
 @pytest.mark.parametrize("fused", [True, False])
 def test_w4a8_split_k(w4, orc, splits, fused):
