@@ -81,14 +81,15 @@ typedef enum {
  * sum exact int32 dp4a products against activation words that the whole CTA
  * reads as shared-memory broadcasts.  Other W4A8 calls with at
  * least 3 rows (see w4a8_tuning_t.mma_min_m) run on the tensor cores: an
- * activation-quantization launch writes bf16 codes into the workspace, then
+ * activation-quantization launch writes binary16 codes into the workspace, then
  * tcgen05 MMAs of 128 weight rows x the batch accumulate the integer
  * products exactly in fp32 (every partial sum of one K piece of at most
  * 16384 is an integer below 2^24) and the rescale matches the dp4a path
- * bit for bit.  Smaller batches use the dp4a kernel, one launch per group
- * of up to 8 rows (W8A16: 4 rows, always dp4a-free fp32 FMAs), each
- * streaming the whole weight matrix.  w4a8_linear_noalloc takes at most 8
- * rows. */
+ * bit for bit.  One row (and larger batches when the other kernels are
+ * switched off) runs on the dp4a GEMV, one launch per group of up to 8 rows
+ * (W8A16: 4 rows, always dp4a-free fp32 FMAs), each streaming the whole
+ * weight matrix.  w4a8_linear_noalloc takes at most 8 rows, always on the
+ * dp4a GEMV. */
 #define W4A8_MAX_M 64
 #define W8A16_MAX_M 64
 
@@ -370,7 +371,8 @@ int w4a8_device_error(unsigned* flags, void* stream);
  *   force_threads_per_row: threads sharing one row-piece (power of 2, <=256).
  *   ring_bytes: target size of the shared-memory weight ring (<= 204800).
  *   ctas_per_sm: CTAs per SM for each K piece (1..4; 0 = 1); for the
- *     row-per-thread kernel, CTAs per SM (0 = 4 / its threads per row).
+ *     row-per-thread kernel, CTAs per SM (0 = 1 at 4 or 8 threads per
+ *     row, 2 at 2).
  *   mma_min_m: activation rows from which the W4A8 entry points use the
  *     tensor-core kernel (2..65; 0 = default, 65 = never).
  *   rowdot_max_m: activation rows up to which row-wise W4A8 calls use the
