@@ -36,7 +36,9 @@
 //    once; each thread group accumulates its row's dot products with all
 //    MT batch rows; pieces are summed in int32 by the CTA that finishes a
 //    tile last (exact, so the result is bit-identical to the integer
-//    definition whatever the split).
+//    definition whatever the split).  With group-wise scales (kG) every
+//    32-code granule's exact sum is folded into an fp32 sum with its group
+//    scale (staged per CTA), and the sums are added in a fixed order.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
