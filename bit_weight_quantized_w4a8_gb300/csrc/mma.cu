@@ -32,7 +32,6 @@
 //    ring slot is handed back by a tcgen05.commit, so no thread waits for
 //    one MMA to finish before issuing the next.
 #include <cuda.h>
-#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>

@@ -7,19 +7,10 @@
 
 namespace w4a8 {
 
-// 2-D tiled TMA load of the box at (x, y) of `tmap` into shared memory;
-// completion is signalled as transaction bytes on `bar`.  x * element size
-// must be a multiple of 16 bytes (checked by the callers' plans).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// The same with an L2 cache policy (the weight stream: evict first).
+// 2-D tiled TMA load of the box at (x, y) of `tmap` into shared memory
+// with an L2 cache policy (the weight stream: evict first); completion is
+// signalled as transaction bytes on `bar`.  x * element size must be a
+// multiple of 16 bytes (checked by the callers' plans).
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap, int x, int y,
                                                  uint32_t bar, uint64_t policy) {
     asm volatile(
@@ -27,12 +18,6 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap,
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
-}
-
-// Makes this thread's generic-proxy shared-memory writes visible to the
-// async proxy (the tensor cores read operands through it).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // TMEM: one warp allocates `ncols` columns (a power of two >= 32) and
@@ -57,20 +42,9 @@ __device__ __forceinline__ void tc_fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 operands, fp32 D),
-// issued by one thread.
-__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-        : "memory");
-}
-
-// The same with the A operand (128 rows x 16 16-bit values) in TMEM: row i
-// in lane i, two values per 32-bit column, so one K=16 step spans 8 columns.
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (16-bit operands, fp32 D),
+// issued by one thread.  A (128 rows x 16 values) in TMEM: row i in lane i,
+// two values per 32-bit column, so one K=16 step spans 8 columns.
 __device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                    uint32_t idesc, bool accumulate) {
     asm volatile(
@@ -150,15 +124,9 @@ __host__ __device__ constexpr uint64_t sw128_desc(uint32_t smem_addr) {
            ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A and B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t bf16_idesc(int m, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-           ((uint32_t)(m >> 4) << 24);
-}
-
-// The same with binary16 A and B (format code 0).
+// Instruction descriptor of tcgen05.mma kind::f16 with binary16 A and B
+// (format code 0 in bits 7-9 and 10-12), D fp32 (bits 4-5 = 1), both
+// K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
