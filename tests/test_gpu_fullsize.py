@@ -5,7 +5,8 @@ those weight rows from the counter-based generator).
 * Qwen2-7B-shaped decode linear set, M=1, W4A8 (q, k, v, o, gate, up, down,
   lm_head), activations with 0.1% x20 outliers, fused activation quantization,
   programmatic dependent launch.
-* Skinny-batch sweep on gate and down, M in {1, 2, 4, 8, 16, 32, 64}.
+* Skinny-batch sweep on gate and down, M in {1, 2, 4, 8, 16, 32, 64}, and
+  lm_head at 3, 8 and 16 rows.
 * ChatGLM2-6B-shaped W8A16 GEMVs.
 """
 import numpy as np
@@ -123,6 +124,16 @@ def test_decode_step_as_benchmarked(w4, orc):
 def test_skinny_batch_sweep(w4, orc, M, name):
     idx = [s[0] for s in QWEN2_7B_SET].index(name)
     _, K, N = QWEN2_7B_SET[idx]
+    run_w4(w4, orc, K, N, M, WEIGHT_SEED0 + idx, flags=w4.LAUNCH_PDL)
+
+
+@pytest.mark.parametrize("M", [3, 8, 16])
+def test_lm_head_small_batches(w4, orc, M):
+    """lm_head at batch sizes that take the row-per-thread kernel (3, 8: a
+    1188-tile grid in several waves) and the tensor cores (16)."""
+    idx = [s[0] for s in QWEN2_7B_SET].index("lm_head")
+    _, K, N = QWEN2_7B_SET[idx]
+    assert w4.w4a8_plan_info(M, K, N)["kernel"] == (2 if M <= 8 else 1)
     run_w4(w4, orc, K, N, M, WEIGHT_SEED0 + idx, flags=w4.LAUNCH_PDL)
 
 
