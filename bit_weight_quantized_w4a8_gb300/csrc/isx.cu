@@ -73,11 +73,13 @@ __device__ __forceinline__ void isx_stage(const IsxArgs& a, uint2* tab) {
 // exceeds it by less than 1/2, so the index round(x) is e or e + 1 and
 // T[e + 1] decides (when e = floor(x) + 1, x is past its half and T[e + 1]
 // is out of reach).
+// kHi = false: M < 2^32 (m_hi = 0, every c_int >= top), one multiply-high.
+template <bool kHi = true>
 __device__ __forceinline__ uint32_t isx_lookup(int a, int mx, uint32_t c_int, uint32_t m_hi,
                                                uint32_t m_lo, const uint2* tab, int* E) {
     const uint32_t delta = (uint32_t)mx - (uint32_t)a;  // mx >= a: exact as uint32
     const uint32_t cl = delta < c_int ? delta : c_int;
-    const uint32_t e = cl * m_hi + __umulhi(cl, m_lo);  // <= top: no overflow
+    const uint32_t e = (kHi ? cl * m_hi : 0u) + __umulhi(cl, m_lo);  // <= top: no overflow
     const uint2 t = tab[e];
     const bool up = cl >= t.x;
     *E = (int)__byte_perm(t.y, 0u, up ? 0x4441u : 0x4440u);
@@ -90,7 +92,7 @@ __device__ __forceinline__ uint32_t isx_lookup(int a, int mx, uint32_t c_int, ui
 // double-buffered by row parity, so no row waits for the previous one's
 // readers (a thread two rows ahead has passed barriers every other thread
 // reached only after finishing those reads).
-template <int V, int Q>
+template <int V, int Q, bool kHi>
 __global__ void __launch_bounds__(kIsxThreads) isx_rows_kernel(const __grid_constant__ IsxArgs a) {
     __shared__ uint2 tab_s[kIsxMaxEntries];
     __shared__ int ptab_s[2][kIsxMaxEntries];
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(kIsxThreads) isx_rows_kernel(const __grid_cons
                 #pragma unroll
                 for (int u = 0; u < V; ++u) {
                     int E;
-                    const uint32_t i = isx_lookup(x[q][u], mx, a.c_int, a.m_hi, a.m_lo, tab_s, &E);
+                    const uint32_t i = isx_lookup<kHi>(x[q][u], mx, a.c_int, a.m_hi, a.m_lo, tab_s, &E);
                     sum += E;
                     idx[q] |= i << (8 * u);
                 }
@@ -219,14 +221,20 @@ __global__ void __launch_bounds__(kIsxThreads) isx_long_kernel(const __grid_cons
     }
 }
 
+template <int V, bool kHi>
+cudaError_t launch_rows_hi(const IsxArgs& a, int q_needed, dim3 grid, cudaStream_t stream) {
+    if (q_needed <= 1) isx_rows_kernel<V, 1, kHi><<<grid, kIsxThreads, 0, stream>>>(a);
+    else if (q_needed <= 2) isx_rows_kernel<V, 2, kHi><<<grid, kIsxThreads, 0, stream>>>(a);
+    else if (q_needed <= 4) isx_rows_kernel<V, 4, kHi><<<grid, kIsxThreads, 0, stream>>>(a);
+    else if (q_needed <= 8) isx_rows_kernel<V, 8, kHi><<<grid, kIsxThreads, 0, stream>>>(a);
+    else isx_rows_kernel<V, 16, kHi><<<grid, kIsxThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
 template <int V>
 cudaError_t launch_rows(const IsxArgs& a, int q_needed, dim3 grid, cudaStream_t stream) {
-    if (q_needed <= 1) isx_rows_kernel<V, 1><<<grid, kIsxThreads, 0, stream>>>(a);
-    else if (q_needed <= 2) isx_rows_kernel<V, 2><<<grid, kIsxThreads, 0, stream>>>(a);
-    else if (q_needed <= 4) isx_rows_kernel<V, 4><<<grid, kIsxThreads, 0, stream>>>(a);
-    else if (q_needed <= 8) isx_rows_kernel<V, 8><<<grid, kIsxThreads, 0, stream>>>(a);
-    else isx_rows_kernel<V, 16><<<grid, kIsxThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return a.m_hi ? launch_rows_hi<V, true>(a, q_needed, grid, stream)
+                  : launch_rows_hi<V, false>(a, q_needed, grid, stream);
 }
 
 }  // namespace
