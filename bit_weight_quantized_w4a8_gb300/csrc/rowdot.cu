@@ -545,15 +545,18 @@ bool make_rowdot_plan(int M, int64_t K, int64_t N, int num_sms, RowdotPlan* out,
     pl.grid = pl.tiles * pl.P;
     pl.sms = num_sms;
     // workspace: tickets, scales, activation codes [nbox][8][M][32 bytes],
-    // then piece sums [tiles][P][M][128] (int32, or fp32 with group scales).  Sized for any N' <= N
-    // (grouped launches plan each matrix on its own): a split matrix has
-    // at most max(slots, tiles * pmin) tile pieces.
+    // then piece sums [tiles][P][M][128] (int32, or fp32 with group scales).
+    // Sized for any N' <= N (grouped launches plan each matrix on its own):
+    // a matrix is split either because its tiles leave CTA slots idle
+    // (then tiles' * P' <= slots) or because a piece's codes must fit in
+    // kActMax (P' = pmin, tiles' <= tiles), so max(slots, tiles * pmin)
+    // tile pieces when pmin > 1, else slots.
     pl.off_sa = kTicketBytes;
     pl.off_codes = pl.off_sa + 256;
     pl.off_part = round_up_sz(pl.off_codes + (size_t)M * pl.nbox * kActBoxBytes, 256);
-    int64_t units = (int64_t)pl.tiles * pl.P;
-    if (units < slots) units = slots;
-    if (units < (int64_t)pl.tiles * pmin) units = (int64_t)pl.tiles * pmin;
+    int64_t units = slots;
+    if (pmin > 1 && units < (int64_t)pl.tiles * pmin) units = (int64_t)pl.tiles * pmin;
+    if (pl.P > 1 && units < (int64_t)pl.tiles * pl.P) units = (int64_t)pl.tiles * pl.P;
     pl.ws_bytes = pl.off_part + round_up_sz((size_t)units * M * kTile * 4, 256);
     *out = pl;
     return true;

@@ -387,3 +387,20 @@ def test_group_rowdot_plans():
             assert p["scale_window"] >= bpp * 256 // gs + 1
             assert p["scale_stage_bytes"] >= 128 * p["scale_window"] * 4
             assert p["smem_bytes"] >= p["stages"] * 16384 + M * bpp * 256 + p["scale_stage_bytes"]
+
+
+def test_rowdot_workspace_covers_grouped_matrices():
+    """A grouped call plans each matrix on its own inside the workspace sized
+    for the total rows: every smaller matrix's plan needs no more, and plans
+    that never split K do not reserve partial sums per tile."""
+    for sms in (152, 148, 20):
+        for (M, K) in [(2, 3584), (8, 3584), (8, 18944), (5, 131072), (3, 896)]:
+            N = 40000
+            full = w4.w4a8_plan_info(M, K, N, num_sms=sms)
+            assert full["kernel"] == 2
+            for Np in (1, 7, 128, 129, 1000, 4608, 18944, 39999):
+                p = w4.w4a8_plan_info(M, K, Np, num_sms=sms)
+                check_rowdot_plan(p, M, K, Np, sms)
+                assert p["ws_bytes"] <= full["ws_bytes"], (M, K, Np, sms)
+    p = w4.w4a8_plan_info(8, 3584, 152064, num_sms=152)  # lm_head: one piece per tile
+    assert p["splits"] == 1 and p["ws_bytes"] < 2 * 1024 * 1024
