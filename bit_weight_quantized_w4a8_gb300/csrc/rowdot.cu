@@ -62,7 +62,7 @@ namespace {
 constexpr int kTile = 128;             // weight rows per CTA
 constexpr int kBoxCodes = 256;         // K codes per TMA box (128 bytes of a row)
 constexpr int kBoxBytes = kTile * kBoxCodes / 2;  // 16384
-constexpr int kActBoxBytes = kBoxCodes;           // plane bytes of one batch row per box
+constexpr int kActBoxBytes = kBoxCodes;           // activation bytes of one batch row per box
 constexpr int kPreThreads = 256;
 constexpr int kMaxNS = 8;
 constexpr int kActMax = 48 * 1024;     // shared bytes for a piece's activation codes
@@ -81,7 +81,7 @@ struct RowdotArgs {
     // a piece's window of gwin groups is staged per CTA as [128][gstride]
     const float* sg;
     int gshift, gld, ngroups, gwin, gstride;
-    int M, N, kw, nbox, bpp, P, NS;
+    int M, N, nbox, bpp, P, NS;
 };
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -609,7 +609,6 @@ cudaError_t launch_w4a8_rowdot(const RowdotPlan& pl, const uint16_t* X, const in
         a.tickets = reinterpret_cast<unsigned*>(wsb);
         a.M = M;
         a.N = (int)Ns[g];
-        a.kw = (int)kw;
         a.nbox = pg.nbox;
         a.bpp = pg.bpp;
         a.P = pg.P;
