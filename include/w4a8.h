@@ -413,9 +413,11 @@ int w4a8_set_tuning(const w4a8_tuning_t* tuning);
 int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int* info,
                    int n_info);
 
-/* The same for w4a8g_gemv / w4a8g_linear (the last field is always 0),
- * followed by two more: the widest scale window a K piece reads (floats
- * per row) and the bytes of one ring slot's scale area. */
+/* The same for w4a8g_gemv / w4a8g_linear (the kernel field reads 0, 1 or
+ * 2 as above), followed by two more: the widest scale window a K piece
+ * reads (floats per row) and the bytes of one ring slot's scale area (the
+ * dp4a GEMV) or of the CTA's staged scale window (the row-per-thread
+ * kernel). */
 int w4a8g_plan_info(int64_t M, int64_t K, int64_t N, int64_t group, int num_sms, int* info,
                     int n_info);
 
