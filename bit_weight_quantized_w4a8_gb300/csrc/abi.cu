@@ -48,8 +48,8 @@ std::atomic<int> g_ctas_per_sm{0};
 std::atomic<int> g_mma_min_m{0};
 std::atomic<int> g_rowdot_max_m{0};
 std::atomic<int> g_mma_e4m3{0};
-// Row-wise tensor-core calls use bf16 operands by default (measured faster
-// than the e4m3 path at every batch size).
+// Row-wise tensor-core calls use binary16 operands by default (measured
+// faster than the e4m3 path at every batch size).
 constexpr bool kDefaultMmaE4m3 = false;
 bool mma_e4m3() {
     const int v = g_mma_e4m3.load();
@@ -59,7 +59,9 @@ bool mma_e4m3() {
 // kernel (from 2 rows).
 constexpr int kDefaultRowdotMaxM = 8;
 // Batch rows from which the W4A8 entry points take the tensor-core kernel
-// (measured on GB300: dp4a is faster at 1-2 rows, the tensor cores from 3).
+// when the row-per-thread kernel does not serve the call (measured on GB300:
+// the dp4a GEMV is faster at 1-2 rows, the tensor cores from 3; with the
+// row-per-thread kernel taking 2..8 rows, the tensor cores start at 9).
 constexpr int kDefaultMmaMinM = 3;
 
 int sm_count(int* out) {
@@ -132,9 +134,8 @@ bool mma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::MmaPlan* pl, int sms = 
     return w4a8::make_mma_plan((int)M, K, N, sms, pl, (int)(group / 64));
 }
 
-// Row-per-thread plan for an M-row W4A8 call with row-wise scales, or false
-// when another kernel serves it.
-// gshift >= 0: group-wise scales, groups of 2^gshift codes.
+// Row-per-thread plan for an M-row W4A8 call, or false when another kernel
+// serves it.  gshift >= 0: group-wise scales, groups of 2^gshift codes.
 bool rowdot_plan_for(int64_t M, int64_t K, int64_t N, w4a8::RowdotPlan* pl, int sms = 0,
                      int gshift = -1) {
     const int t = g_rowdot_max_m.load();
