@@ -378,7 +378,8 @@ int w4a8_device_error(unsigned* flags, void* stream);
  *   rowdot_max_m: activation rows up to which row-wise W4A8 calls use the
  *     row-per-thread kernel, from 2 rows (0 = default 8, 1 = never, <= 8);
  *     it takes precedence over mma_min_m.  force_threads_per_row 2, 4 or 8
- *     sets that kernel's threads per weight row.
+ *     sets that kernel's threads per weight row (row-wise scales; calls
+ *     with group-wise scales always use 4).
  *   mma_e4m3: operands of the row-wise tensor-core kernel: 0 = default,
  *     1 = bf16 (kind::f16, K = 16 per MMA), 2 = e4m3 (kind::f8f6f4, K = 32
  *     per MMA, activation codes split as 16 a_hi + a_lo).
