@@ -29,11 +29,12 @@ ERR_SHAPE = 3
 ERR_OVERFLOW = 6
 
 
-def compile_oracle(src: str = _SRC, out: str = _LIB) -> str:
-    """Compile ``src`` into the shared library ``out`` with gcc (no FMA contraction)."""
+def compile_oracle(src: str = _SRC, out: str = _LIB, extra=()) -> str:
+    """Compile ``src`` into the shared library ``out`` with gcc (no FMA
+    contraction); ``extra`` adds flags (e.g. sanitizers)."""
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = out + ".tmp%d" % os.getpid()
-    subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, src, "-lm"])
+    subprocess.check_call(["gcc", *CFLAGS, *extra, "-o", tmp, src, "-lm"])
     os.replace(tmp, out)
     return out
 
@@ -88,6 +89,10 @@ class Oracle:
         lib.oracle_isx_c_int.argtypes = [ctypes.c_double, _i64, ctypes.c_float, ctypes.c_float]
         lib.oracle_w8a16_ref.restype = None
         lib.oracle_w8a16_ref.argtypes = [_p, _i64, _i64, _p, _p, _i64, _p]
+        lib.oracle_double_to_half.restype = ctypes.c_uint16
+        lib.oracle_double_to_half.argtypes = [ctypes.c_double]
+        lib.oracle_silu_mul.restype = None
+        lib.oracle_silu_mul.argtypes = [_p, _p, _i64, _p, _p]
 
     # -- binary16 ---------------------------------------------------------
     def half_to_float(self, bits: int) -> float:
@@ -95,6 +100,20 @@ class Oracle:
 
     def float_to_half(self, x: float) -> int:
         return int(self._lib.oracle_float_to_half(float(np.float32(x))))
+
+    def double_to_half(self, x: float) -> int:
+        return int(self._lib.oracle_double_to_half(float(x)))
+
+    # -- the MLP's gated product ---------------------------------------------
+    def silu_mul(self, g: np.ndarray, u: np.ndarray):
+        """(v, h): v = silu(g) * u in binary64, h its binary16 bits (uint16)."""
+        g = np.ascontiguousarray(g, dtype=np.float32)
+        u = np.ascontiguousarray(u, dtype=np.float32)
+        assert g.shape == u.shape
+        v = np.empty(g.shape, np.float64)
+        h = np.empty(g.shape, np.uint16)
+        self._lib.oracle_silu_mul(_ptr(g), _ptr(u), g.size, _ptr(v), _ptr(h))
+        return v, h
 
     # -- W4A8 -------------------------------------------------------------
     def w4_quantize(self, W: np.ndarray):

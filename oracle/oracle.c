@@ -452,3 +452,47 @@ int oracle_index_softmax(const int32_t* A, int64_t rows, int64_t cols, int64_t c
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The MLP's gated product between gate/up and down                          */
+/* ------------------------------------------------------------------------ */
+
+/* binary64 -> binary16, round to nearest, ties to even, written from the
+   format's definition: the result's quantum is 2^(eh - 10) with
+   eh = max(floor(log2 |x|), -14) (subnormals share eh = -14); |x| / quantum
+   is an exact scaling, rounded once by rint (ties to even); a carry to 2048
+   moves to the next exponent, past 65504 (half an ulp included) to inf. */
+uint16_t oracle_double_to_half(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x)) return (uint16_t)(sign | 0x7E00u);
+    double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | 0x7C00u);
+    if (a == 0.0) return sign;
+    int e;
+    (void)frexp(a, &e);                  /* a = f * 2^e, f in [0.5, 1) */
+    int eh = e - 1 < -14 ? -14 : e - 1;  /* floor(log2 a), clamped */
+    if (eh > 15) return (uint16_t)(sign | 0x7C00u);
+    double n = rint(ldexp(a, 10 - eh));  /* a / 2^(eh - 10): exact, then one rounding */
+    /* n = 2048 carries into the exponent; at eh = 15 that is 0x7C00 = inf */
+    uint32_t bits = (eh == -14) ? (uint32_t)n : ((uint32_t)(eh + 15) << 10) + ((uint32_t)n - 1024u);
+    return (uint16_t)(sign | bits);
+}
+
+/* The gated product that the MLP of the INT4 page's model (a Qwen2-7B,
+   HIDDEN 3584 / INTERMEDIATE 18944: gate and up projections, then down)
+   feeds to the down projection, whose activation quantization the page's
+   section 后续优化方向 asks to make cheaper.  The pages do not print the
+   activation; the reading is that model family's SwiGLU:
+     v = silu(g) * u = g / (1 + exp(-g)) * u      in binary64 (exact inputs),
+     h = binary16(v)                               rounded to nearest even,
+   for i < n.  v is returned too, for the rounding-boundary check. */
+void oracle_silu_mul(const float* g, const float* u, int64_t n, double* v, uint16_t* h)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double x = (double)g[i];
+        double p = x / (1.0 + exp(-x)) * (double)u[i];
+        v[i] = p;
+        h[i] = oracle_double_to_half(p);
+    }
+}

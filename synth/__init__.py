@@ -150,3 +150,48 @@ def normal_gpu(seed: int, shape, sigma: float = 1.0, offset: int = 0, device="cu
     if st != 0:
         raise RuntimeError("synth_normal_f32 failed with status %d" % st)
     return out
+
+
+# ----------------------------------------------------------------------------
+# C twin of ``normal`` on the host, split over threads (test infrastructure)
+# ----------------------------------------------------------------------------
+
+_HOST_C = _os.path.join(_HERE, "synth_host.c")
+_HOST_SO = _os.path.join(_HERE, "_build", "libsynth_host.so")
+_HOST_LIB = None
+
+
+def build_host() -> str:
+    """Compile libsynth_host.so with gcc if it is missing or stale."""
+    if _os.path.exists(_HOST_SO) and _os.path.getmtime(_HOST_SO) >= _os.path.getmtime(_HOST_C):
+        return _HOST_SO
+    _os.makedirs(_os.path.dirname(_HOST_SO), exist_ok=True)
+    tmp = _HOST_SO + ".tmp%d" % _os.getpid()
+    _sp.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    "-o", tmp, _HOST_C])
+    _os.replace(tmp, _HOST_SO)
+    return _HOST_SO
+
+
+def _host_lib():
+    global _HOST_LIB
+    if _HOST_LIB is None:
+        lib = _ct.CDLL(build_host())
+        lib.synth_normal_f32_host.restype = _ct.c_int
+        lib.synth_normal_f32_host.argtypes = [_ct.c_uint32, _ct.c_uint64, _ct.c_uint64, _ct.c_float,
+                                              _ct.c_void_p, _ct.c_int]
+        _HOST_LIB = lib
+    return _HOST_LIB
+
+
+def normal_host(seed: int, shape, sigma: float = 1.0, offset: int = 0, threads: int = 0) -> np.ndarray:
+    """Same values as ``normal(seed, shape, sigma, offset)``, drawn by the C
+    twin over ``threads`` host threads (0 = every core)."""
+    n = int(np.prod(shape))
+    out = np.empty(n, np.float32)
+    th = threads if threads > 0 else (_os.cpu_count() or 1)
+    st = _host_lib().synth_normal_f32_host(seed & 0xFFFFFFFF, offset, n, float(np.float32(sigma)),
+                                           out.ctypes.data, th)
+    if st != 0:
+        raise ValueError("synth_normal_f32_host failed with status %d" % st)
+    return out.reshape(shape)

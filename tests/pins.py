@@ -645,4 +645,89 @@ def pin_w8a16_bruteforce_and_bound(o):
         assert cos > 0.99
 
 
+
+# --------------------------------------------------------------------------
+# the MLP's gated product: binary64 -> binary16 and silu(g) * u
+# --------------------------------------------------------------------------
+
+def pin_double_to_half(o):
+    """binary64 -> binary16 (round to nearest even) against numpy's IEEE
+    conversion: random values over the whole binary16 range and beyond,
+    exact ties in the normal and subnormal ranges, the overflow threshold."""
+    rng = np.random.Generator(np.random.PCG64(71))
+    mags = np.ldexp(rng.random(4000) + 0.5, rng.integers(-30, 18, size=4000))
+    xs = np.concatenate([mags, -mags, [0.0, -0.0, 65504.0, 65519.99, 65520.0, 65536.0, 1e300, 2.0 ** -24,
+                                       2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -14 - 2.0 ** -25, np.inf, -np.inf]])
+    # ties: (k + 1/2) quanta for random k, normal (quantum 2^(e-10)) and subnormal (2^-24)
+    k = rng.integers(1024, 2047, size=500).astype(np.float64)
+    e = rng.integers(-14, 16, size=500)
+    ties = np.ldexp(k + 0.5, e - 10)
+    sub = np.ldexp(rng.integers(0, 1023, size=200).astype(np.float64) + 0.5, -24)
+    xs = np.concatenate([xs, ties, -ties, sub, -sub])
+    want = xs.astype(np.float16).view(np.uint16)
+    got = np.array([o.double_to_half(x) for x in xs], np.uint16)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(xs[i], hex(got[i]), hex(want[i])) for i in bad[:5]]
+
+
+def _decimal_silu_mul(g, u):
+    """silu(g) * u with 50-digit decimal arithmetic (independent of the
+    binary64 evaluation)."""
+    import decimal
+    ctx = decimal.Context(prec=50)
+    x = decimal.Decimal(float(g))
+    return ctx.multiply(ctx.divide(x, ctx.add(1, ctx.exp(-x))), decimal.Decimal(float(u)))
+
+
+def pin_silu_mul(o):
+    """v = silu(g) * u against 50-digit decimal arithmetic (relative error of
+    a few binary64 roundings), h = its binary16 rounding; closed forms
+    (silu(0) = 0, u = 0, silu(40) = 40 in binary64, silu(-40) ~ 0) and the
+    identity silu(x) - silu(-x) = x."""
+    rng = np.random.Generator(np.random.PCG64(72))
+    g = np.concatenate([rng.normal(0, 3, 60), [0.0, 1.0, -1.0, 40.0, -40.0, 0.5, -7.25, 12.0]]).astype(np.float32)
+    u = np.concatenate([rng.normal(0, 2, 60), [5.0, 0.0, 2.0, 1.5, 3.0, -4.0, 0.125, -1.0]]).astype(np.float32)
+    v, h = o.silu_mul(g, u)
+    for i in range(g.size):
+        ref = _decimal_silu_mul(g[i], u[i])
+        rf = float(ref)
+        assert abs(v[i] - rf) <= 8 * 2.0 ** -53 * abs(rf) + 1e-300, (g[i], u[i], v[i], rf)
+        # h: the binary16 rounding of the exact value, unless that value sits
+        # within the binary64 error of a binary16 rounding boundary
+        hq = np.float64(np.float16(rf))
+        lo, hi = sorted((hq, np.float64(np.nextafter(np.float16(hq), np.float16(np.sign(rf - hq) or 1)))))
+        near = abs(abs(rf) - abs((lo + hi) / 2)) <= 16 * 2.0 ** -53 * abs(rf)
+        if not near:
+            assert h[i] == np.float16(rf).view(np.uint16), (g[i], u[i], hex(h[i]))
+    assert v[g.size - 8] == 0.0 and v[g.size - 7] == 0.0       # silu(0) * 5, silu(1) * 0
+    assert v[g.size - 5] == 40.0 * 1.5                          # silu(40) = 40 in binary64
+    assert abs(v[g.size - 4]) < 1e-15 and h[g.size - 4] & 0x7FFF == 0
+    # values just above a binary16 rounding midpoint by less than half a
+    # binary32 ulp (g = 40, so silu(g) = 40 exactly and v = 40 u): rounded
+    # straight from binary64 they go up; through binary32 they would land on
+    # the midpoint and go to the even, lower neighbour
+    found = 0
+    for base in (1.0, 3.0, 100.0, 0.3, 7.0, 2000.0, 0.01, 40000.0):
+        lo = np.float16(base)
+        if lo.view(np.uint16) & 1:
+            lo = np.nextafter(lo, np.float16(np.inf))
+        hi = np.nextafter(lo, np.float16(np.inf))
+        mid = (np.float64(lo) + np.float64(hi)) / 2
+        half_ulp32 = np.float64(np.spacing(np.float32(mid))) / 2
+        u0 = np.float32(mid / 40.0)
+        for k in range(-4, 5):
+            uk = np.float32(u0 + np.float32(k) * np.spacing(u0))
+            v40 = 40.0 * np.float64(uk)
+            if mid < v40 < mid + half_ulp32:
+                vk, hk = o.silu_mul(np.array([40.0], np.float32), np.array([uk], np.float32))
+                assert vk[0] == v40 and hk[0] == hi.view(np.uint16), (base, uk, hex(hk[0]))
+                found += 1
+    assert found >= 3, found
+    x = rng.normal(0, 4, 200).astype(np.float32)
+    one = np.ones_like(x)
+    vp, _ = o.silu_mul(x, one)
+    vm, _ = o.silu_mul(-x, one)
+    assert np.all(np.abs((vp - vm) - x.astype(np.float64)) <= 8 * 2.0 ** -53 * (np.abs(x) + 1.0))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -54,6 +54,14 @@ MUTATIONS = [
     ("w4g_ref_group_bytes", "for (int64_t j = g * (gs / 2); j < (g + 1) * (gs / 2); ++j)",
      "for (int64_t j = 0; j < gs / 2; ++j)"),
     ("w4g_ref_dropped_high", "acc += p0 + p1;", "acc += p0;"),
+    ("silu_sign_of_exp", "double p = x / (1.0 + exp(-x)) * (double)u[i];", "double p = x / (1.0 + exp(x)) * (double)u[i];"),
+    ("silu_dropped_up", "double p = x / (1.0 + exp(-x)) * (double)u[i];", "double p = x / (1.0 + exp(-x));"),
+    ("silu_sigmoid_only", "double p = x / (1.0 + exp(-x)) * (double)u[i];", "double p = 1.0 / (1.0 + exp(-x)) * (double)u[i];"),
+    ("silu_half_via_float", "h[i] = oracle_double_to_half(p);", "h[i] = oracle_float_to_half((float)p);"),
+    ("d2h_truncate", "double n = rint(ldexp(a, 10 - eh));", "double n = floor(ldexp(a, 10 - eh));"),
+    ("d2h_ties_away", "double n = rint(ldexp(a, 10 - eh));", "double n = round(ldexp(a, 10 - eh));"),
+    ("d2h_subnormal_exponent", "int eh = e - 1 < -14 ? -14 : e - 1;", "int eh = e - 1 < -15 ? -15 : e - 1;"),
+    ("d2h_overflow_threshold", "if (eh > 15) return (uint16_t)(sign | 0x7C00u);", "if (eh > 16) return (uint16_t)(sign | 0x7C00u);"),
     ("isx_lut_scale_254", "(uint8_t)round(255.0 * exp(", "(uint8_t)round(254.0 * exp("),
     ("isx_lut_step_2b", "exp(-c * (double)i / (double)(n - 1))", "exp(-c * (double)i / (double)n)"),
     ("isx_lut_last_not_zero", "lut[n - 1] = 0;", "lut[n - 1] = (uint8_t)round(255.0 * exp(-c));"),

@@ -46,3 +46,16 @@ def test_seeds_differ():
     b = synth.normal(2, (4, 64))
     assert not np.array_equal(a, b)
     assert np.array_equal(a, synth.normal(1, (4, 64)))
+
+
+def test_host_twin_matches_numpy():
+    """The C host twin draws the same bits as the numpy definition, whatever
+    the thread split and the counter offset."""
+    for seed, shape, sigma, offset, threads in [(3, (37, 96), 0.02, 0, 1), (1004, (5, 3584), 0.02, 12345, 3),
+                                                (7, (1000,), 1.0, 2 ** 32 - 1000, 8), (0, (1, 1), 0.5, 0, 4)]:
+        a = synth.normal_host(seed, shape, sigma, offset=offset, threads=threads)
+        b = synth.normal(seed, shape, sigma, offset=offset)
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    rows = [0, 511, 1999]
+    full = synth.normal_host(1006, (2000, 512), 0.02)
+    assert np.array_equal(full[rows].view(np.uint32), synth.weight_rows(1006, 2000, 512, rows).view(np.uint32))
