@@ -30,6 +30,7 @@ EXPORTS = [
     "w4g_quantize_weights", "w4a8g_workspace_bytes", "w4a8g_gemv", "w4a8g_linear",
     "w4a8g_linear_grouped", "w4a8g_plan_info",
     "index_softmax_lut", "index_softmax_c_int", "index_softmax_u8",
+    "w4_interleave_rows", "w4a8_gate_up_silu_workspace_bytes", "w4a8_gate_up_silu", "w4a8_silu_mul",
 ]
 
 
@@ -43,7 +44,8 @@ class _Tuning(ctypes.Structure):
     _fields_ = [("force_splits", ctypes.c_int), ("force_threads_per_row", ctypes.c_int),
                 ("ring_bytes", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
                 ("mma_min_m", ctypes.c_int), ("rowdot_max_m", ctypes.c_int),
-                ("mma_e4m3", ctypes.c_int)]
+                ("mma_e4m3", ctypes.c_int), ("qmma_max_m", ctypes.c_int),
+                ("qmma_tiles_per_warp", ctypes.c_int), ("stall_test_us", ctypes.c_int)]
 
 
 _i64, _p, _u = ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint
@@ -77,6 +79,10 @@ _SIGS = {
     "index_softmax_lut": (ctypes.c_int, [ctypes.c_int, ctypes.c_double, _p]),
     "index_softmax_c_int": (_i64, [ctypes.c_double, _i64, ctypes.c_float, ctypes.c_float]),
     "index_softmax_u8": (ctypes.c_int, [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _p]),
+    "w4_interleave_rows": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _p, _p, _p]),
+    "w4a8_gate_up_silu_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
+    "w4a8_gate_up_silu": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _p, _p, ctypes.c_size_t, _u, _p]),
+    "w4a8_silu_mul": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _u, _p]),
 }
 
 _lib = None
@@ -300,6 +306,59 @@ def w8a16_gemv(X, Wq8, sw16, Y=None, ws=None, flags: int = 0):
     return Y
 
 
+# -- the MLP's gated product ---------------------------------------------------
+
+def w4_interleave_rows(Wq_a, sw_a, Wq_b, sw_b, Wq_out=None, sw_out=None):
+    """Rows of two packed matrices interleaved: (Wq [2N][K/2], sw [2N])."""
+    N, half = Wq_a.shape
+    for t, dt, nm, shp in ((Wq_a, torch.uint8, "Wq_a", (N, half)), (Wq_b, torch.uint8, "Wq_b", (N, half)),
+                           (sw_a, torch.float32, "sw_a", (N,)), (sw_b, torch.float32, "sw_b", (N,))):
+        _want(t, dt, nm, shp)
+    Wq_out = torch.empty((2 * N, half), dtype=torch.uint8, device=Wq_a.device) if Wq_out is None else Wq_out
+    sw_out = torch.empty((2 * N,), dtype=torch.float32, device=Wq_a.device) if sw_out is None else sw_out
+    _want(Wq_out, torch.uint8, "Wq_out", (2 * N, half))
+    _want(sw_out, torch.float32, "sw_out", (2 * N,))
+    _check(lib().w4_interleave_rows(_ptr(Wq_a), _ptr(sw_a), _ptr(Wq_b), _ptr(sw_b), N, 2 * half,
+                                    _ptr(Wq_out), _ptr(sw_out), _stream(Wq_a)))
+    return Wq_out, sw_out
+
+
+def w4a8_gate_up_silu_workspace_bytes(M: int, K: int, N: int) -> int:
+    return int(lib().w4a8_gate_up_silu_workspace_bytes(M, K, N))
+
+
+def w4a8_gate_up_silu(X, Wq_gu, sw_gu, H=None, Y_gu=None, ws=None, flags: int = 0):
+    """Gate/up projections of interleaved weights with the gated product in
+    the epilogue; returns (H [M][N] fp16, Y_gu [M][2N] fp32)."""
+    _want(X, torch.float16, "X")
+    M, K = X.shape
+    N2 = Wq_gu.shape[0]
+    if N2 % 2:
+        raise ValueError("Wq_gu must have an even number of rows (gate/up pairs)")
+    N = N2 // 2
+    _want(Wq_gu, torch.uint8, "Wq_gu", (N2, K // 2))
+    _want(sw_gu, torch.float32, "sw_gu", (N2,))
+    H = torch.empty((M, N), dtype=torch.float16, device=X.device) if H is None else H
+    Y_gu = torch.empty((M, N2), dtype=torch.float32, device=X.device) if Y_gu is None else Y_gu
+    _want(H, torch.float16, "H", (M, N))
+    _want(Y_gu, torch.float32, "Y_gu", (M, N2))
+    ws = _workspace(w4a8_gate_up_silu_workspace_bytes(M, K, N), X.device, ws)
+    _check(lib().w4a8_gate_up_silu(_ptr(X), M, K, _ptr(Wq_gu), _ptr(sw_gu), N, _ptr(Y_gu), _ptr(H), _ptr(ws),
+                                   0 if ws is None else ws.numel() * ws.element_size(), flags, _stream(X)))
+    return H, Y_gu
+
+
+def w4a8_silu_mul(g, u, H=None, flags: int = 0):
+    """H = fp16(silu(g) * u), g and u [M][N] fp32; returns H."""
+    _want(g, torch.float32, "g")
+    M, N = g.shape
+    _want(u, torch.float32, "u", (M, N))
+    H = torch.empty((M, N), dtype=torch.float16, device=g.device) if H is None else H
+    _want(H, torch.float16, "H", (M, N))
+    _check(lib().w4a8_silu_mul(_ptr(g), _ptr(u), M, N, _ptr(H), flags, _stream(g)))
+    return H
+
+
 # -- group-wise INT4 scales -------------------------------------------------
 
 def w4g_scale_stride(K: int, group: int) -> int:
@@ -446,12 +505,13 @@ def w4a8_device_error(device=None) -> int:
 
 def w4a8_set_tuning(force_splits: int = 0, force_threads_per_row: int = 0,
                     ring_bytes: int = 0, ctas_per_sm: int = 0, mma_min_m: int = 0,
-                    rowdot_max_m: int = 0, mma_e4m3: int = 0, reset: bool = False):
+                    rowdot_max_m: int = 0, mma_e4m3: int = 0, qmma_max_m: int = 0,
+                    qmma_tiles_per_warp: int = 0, stall_test_us: int = 0, reset: bool = False):
     if reset:
         _check(lib().w4a8_set_tuning(None))
         return
     t = _Tuning(force_splits, force_threads_per_row, ring_bytes, ctas_per_sm, mma_min_m,
-                rowdot_max_m, mma_e4m3)
+                rowdot_max_m, mma_e4m3, qmma_max_m, qmma_tiles_per_warp, stall_test_us)
     _check(lib().w4a8_set_tuning(ctypes.byref(t)))
 
 

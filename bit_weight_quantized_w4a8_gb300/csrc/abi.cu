@@ -48,6 +48,11 @@ std::atomic<int> g_ctas_per_sm{0};
 std::atomic<int> g_mma_min_m{0};
 std::atomic<int> g_rowdot_max_m{0};
 std::atomic<int> g_mma_e4m3{0};
+std::atomic<int> g_qmma_max_m{0};
+std::atomic<int> g_qmma_r{0};
+std::atomic<int> g_stall_test_us{0};
+// Test of the bounded waits (w4a8_tuning_t.stall_test_us): 0 = off.
+unsigned long long qmma_stall_ns() { return (unsigned long long)g_stall_test_us.load() * 1000ull; }
 // Row-wise tensor-core calls use binary16 operands by default (measured
 // faster than the e4m3 path at every batch size).
 constexpr bool kDefaultMmaE4m3 = false;
@@ -63,6 +68,16 @@ constexpr int kDefaultRowdotMaxM = 8;
 // the dp4a GEMV is faster at 1-2 rows, the tensor cores from 3; with the
 // row-per-thread kernel taking 2..8 rows, the tensor cores start at 9).
 constexpr int kDefaultMmaMinM = 3;
+// Batch rows for which row-wise W4A8 calls take the warp-level e4m3 MMA
+// kernel by default; it takes precedence over the two kernels above.
+// Measured on GB300 (graphs of ten calls, two weight copies): from 4 to 8
+// rows it matches the row-per-thread kernel on gate and down and beats it
+// on lm_head (4 rows: 69 vs 84 us; 8 rows: 87 vs 108 us); at 2 rows the
+// row-per-thread kernel is faster (gate 8.9 vs 11.0 us), from 16 rows the
+// tensor cores (gate 19.8 vs 20.7 us).  An explicit qmma_max_m extends it
+// down to 2 rows.
+constexpr int kDefaultQmmaMinM = 4;
+constexpr int kDefaultQmmaMaxM = 8;
 
 int sm_count(int* out) {
     static std::atomic<int> cache[64];
@@ -95,12 +110,12 @@ w4a8::Tuning tuning() {
 
 // gshift >= 0: group-wise scales, one per 2^gshift granules, rows of gld floats.
 int plan_for(bool w4, bool fused, int64_t M, int64_t K, int64_t N, w4a8::GemvPlan* pl,
-             int sms = 0, int gshift = -1, int gld = 0) {
+             int sms = 0, int gshift = -1, int gld = 0, bool pair = false) {
     if (sms <= 0) {
         int st = sm_count(&sms);
         if (st != W4A8_OK) return st;
     }
-    if (!w4a8::make_gemv_plan(w4, fused, (int)M, K, N, sms, tuning(), pl, gshift, gld))
+    if (!w4a8::make_gemv_plan(w4, fused, (int)M, K, N, sms, tuning(), pl, gshift, gld, pair))
         return fail(W4A8_ERR_SHAPE, "no launch plan for M=%lld K=%lld N=%lld",
                     (long long)M, (long long)K, (long long)N);
     return W4A8_OK;
@@ -132,6 +147,17 @@ bool mma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::MmaPlan* pl, int sms = 
     if (group > 0 && (group % 128 || group > 16384)) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
     return w4a8::make_mma_plan((int)M, K, N, sms, pl, (int)(group / 64));
+}
+
+// Warp-level e4m3 MMA plan for an M-row row-wise W4A8 call, or false when
+// another kernel serves it.
+bool qmma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::QmmaPlan* pl, int sms = 0) {
+    const int t = g_qmma_max_m.load();
+    const int hi = t > 0 ? t : kDefaultQmmaMaxM;
+    const int lo = t > 0 ? 2 : kDefaultQmmaMinM;
+    if (M < lo || M > hi) return false;
+    if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
+    return w4a8::make_qmma_plan((int)M, K, N, sms, pl, g_qmma_r.load());
 }
 
 // Row-per-thread plan for an M-row W4A8 call, or false when another kernel
@@ -210,6 +236,8 @@ int check_workspace(const w4a8::GemvPlan& pl, void* ws, size_t ws_bytes) {
 
 }  // namespace
 
+cudaError_t w4a8_noalloc_reset(cudaStream_t stream);  // defined with the static scratch below
+
 extern "C" {
 
 int w4_quantize_weights(const float* W, int64_t N, int64_t K, uint8_t* Wq, float* sw, void* stream) {
@@ -245,6 +273,8 @@ int act_quantize_i8(const uint16_t* X, int64_t M, int64_t K, int8_t* Xq, float* 
 
 size_t w4a8_workspace_bytes(int64_t M, int64_t K, int64_t N) {
     if (check_w4a8_shape(M, K, N) != W4A8_OK) return 0;
+    w4a8::QmmaPlan qp;
+    if (qmma_plan_for(M, K, N, &qp)) return qp.ws_bytes;
     w4a8::RowdotPlan rp;
     if (rowdot_plan_for(M, K, N, &rp)) return rp.ws_bytes;
     w4a8::MmaPlan mp;
@@ -300,6 +330,14 @@ int w4a8_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, const uin
     if (!aligned(Xq, 16) || !aligned(Wq, 16) || !aligned(Y, 4) || !aligned(sw, 4) ||
         !aligned(sa, 4) || (acc_out && !aligned(acc_out, 4)))
         return fail(W4A8_ERR_ALIGN, "w4a8_gemv: Xq/Wq need 16-byte, Y/sw/sa/acc_out 4-byte alignment");
+    w4a8::QmmaPlan qp;
+    if (qmma_plan_for(M, K, N, &qp)) {
+        if ((st = check_ws(qp.ws_bytes, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_qmma(qp, nullptr, Xq, sa, (int)M, K, 1, &Wq, &sw, &N, &Y, acc_out,
+                                               nullptr, nullptr, ws, flags, static_cast<cudaStream_t>(stream),
+                                               qmma_stall_ns());
+        return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_gemv warp-MMA launch");
+    }
     w4a8::RowdotPlan rp;
     if (rowdot_plan_for(M, K, N, &rp)) {
         if ((st = check_ws(rp.ws_bytes, ws, ws_bytes)) != W4A8_OK) return st;
@@ -342,6 +380,14 @@ int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, cons
         (Xq_out && !aligned(Xq_out, 16)) || (sa_out && !aligned(sa_out, 4)) ||
         (acc_out && !aligned(acc_out, 4)))
         return fail(W4A8_ERR_ALIGN, "w4a8_linear: X/Wq/Xq_out need 16-byte, Y/sw/sa_out/acc_out 4-byte alignment");
+    w4a8::QmmaPlan qp;
+    if (qmma_plan_for(M, K, N, &qp)) {
+        if ((st = check_ws(qp.ws_bytes, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_qmma(qp, X, nullptr, nullptr, (int)M, K, 1, &Wq, &sw, &N, &Y,
+                                               acc_out, Xq_out, sa_out, ws, flags,
+                                               static_cast<cudaStream_t>(stream), qmma_stall_ns());
+        return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear warp-MMA launch");
+    }
     w4a8::RowdotPlan rp;
     if (rowdot_plan_for(M, K, N, &rp)) {
         if ((st = check_ws(rp.ws_bytes, ws, ws_bytes)) != W4A8_OK) return st;
@@ -392,6 +438,20 @@ int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const ui
     int st = check_w4a8_shape(M, K, total);
     if (st != W4A8_OK) return st;
     if (!aligned(X, 16)) return fail(W4A8_ERR_ALIGN, "w4a8_linear_grouped: X needs 16-byte alignment");
+    w4a8::QmmaPlan qp;
+    if (qmma_plan_for(M, K, total, &qp)) {
+        // one plan per matrix inside; the workspace bound covers every N[g] <= total
+        for (int g = 0; g < G; ++g) {
+            w4a8::QmmaPlan pg;
+            if (!w4a8::make_qmma_plan((int)M, K, N[g], qp.sms, &pg, qp.R) || pg.ws_bytes > qp.ws_bytes)
+                return fail(W4A8_ERR_SHAPE, "no warp-MMA plan for group %d", g);
+        }
+        if ((st = check_ws(qp.ws_bytes, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_qmma(qp, X, nullptr, nullptr, (int)M, K, G, Wq, sw, N, Y, nullptr,
+                                               nullptr, nullptr, ws, flags, static_cast<cudaStream_t>(stream),
+                                               qmma_stall_ns());
+        return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear_grouped warp-MMA launch");
+    }
     w4a8::RowdotPlan rp;
     if (rowdot_plan_for(M, K, total, &rp)) {
         // one plan per matrix inside; the workspace bound covers every N[g] <= total
@@ -600,10 +660,19 @@ const char* w4a8_last_error(void) { return g_last_error.c_str(); }
 
 int w4a8_device_error(unsigned* flags, void* stream) {
     if (!flags) return fail(W4A8_ERR_NULL, "w4a8_device_error: NULL pointer");
+    *flags = 0;
     cudaError_t e = w4a8::read_and_clear_device_error(flags, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = w4a8::read_and_clear_mma_error(flags, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = w4a8::read_and_clear_group_error(flags, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = w4a8::read_and_clear_rowdot_error(flags, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = w4a8::read_and_clear_qmma_error(flags, static_cast<cudaStream_t>(stream));
+    // a wait that gave up may leave split-K arrival counters non-zero; the
+    // static scratch of w4a8_linear_noalloc is cleared here (caller-owned
+    // workspaces must be re-zeroed by the caller)
+    if (e == cudaSuccess && *flags != 0) {
+        e = w4a8_noalloc_reset(static_cast<cudaStream_t>(stream));
+        if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    }
     return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_device_error");
 }
 
@@ -616,6 +685,9 @@ int w4a8_set_tuning(const w4a8_tuning_t* t) {
         g_mma_min_m = 0;
         g_rowdot_max_m = 0;
         g_mma_e4m3 = 0;
+        g_qmma_max_m = 0;
+        g_qmma_r = 0;
+        g_stall_test_us = 0;
         return ok();
     }
     if (t->force_splits < 0 || t->force_splits > 16)
@@ -639,6 +711,16 @@ int w4a8_set_tuning(const w4a8_tuning_t* t) {
     g_rowdot_max_m = t->rowdot_max_m;
     if (t->mma_e4m3 < 0 || t->mma_e4m3 > 2) return fail(W4A8_ERR_SHAPE, "mma_e4m3 must be 0, 1 or 2");
     g_mma_e4m3 = t->mma_e4m3;
+    if (t->qmma_max_m < 0 || t->qmma_max_m > w4a8::kQmmaMaxM)
+        return fail(W4A8_ERR_SHAPE, "qmma_max_m must be in [0, %d]", w4a8::kQmmaMaxM);
+    g_qmma_max_m = t->qmma_max_m;
+    if (t->qmma_tiles_per_warp != 0 && t->qmma_tiles_per_warp != 1 && t->qmma_tiles_per_warp != 2 &&
+        t->qmma_tiles_per_warp != 4)
+        return fail(W4A8_ERR_SHAPE, "qmma_tiles_per_warp must be 0, 1, 2 or 4");
+    g_qmma_r = t->qmma_tiles_per_warp;
+    if (t->stall_test_us < 0 || t->stall_test_us > 1000000)
+        return fail(W4A8_ERR_SHAPE, "stall_test_us must be in [0, 1000000]");
+    g_stall_test_us = t->stall_test_us;
     return ok();
 }
 
@@ -648,6 +730,14 @@ int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int*
     int st = w8a16 ? check_w8a16_shape(M, K, N) : check_w4a8_shape(M, K, N);
     if (st != W4A8_OK) return st;
     if (!w8a16) {
+        w4a8::QmmaPlan qp;
+        if (qmma_plan_for(M, K, N, &qp, num_sms)) {
+            const int ws = qp.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)qp.ws_bytes;
+            const int v[] = {qp.P, qp.R, 4 * qp.NT, 128, qp.tiles, qp.grid, 128, qp.NS, qp.stage_bytes,
+                             qp.smem, ws, 3};
+            for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
+            return ok();
+        }
         w4a8::RowdotPlan rp;
         if (rowdot_plan_for(M, K, N, &rp, num_sms)) {
             const int ws = rp.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)rp.ws_bytes;
@@ -716,44 +806,113 @@ int w4a8g_plan_info(int64_t M, int64_t K, int64_t N, int64_t group, int num_sms,
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// The MLP's gated product: gate/up projections with silu(gate) * up in the
+// epilogue, the stand-alone product, and the row interleaving it reads.
+// ---------------------------------------------------------------------------
+
+extern "C" {
+
+size_t w4a8_gate_up_silu_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+    if (N < 1 || N > 0x3FFFFFFF || check_w4a8_shape(M, K, 2 * N) != W4A8_OK) return 0;
+    if (M > 1) return w4a8_workspace_bytes(M, K, 2 * N);
+    w4a8::GemvPlan pl;
+    if (plan_for(true, true, 1, K, 2 * N, &pl, 0, -1, 0, true) != W4A8_OK) return 0;
+    return pl.ws_bytes;
+}
+
+int w4a8_gate_up_silu(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq_gu, const float* sw_gu,
+                      int64_t N, float* Y_gu, uint16_t* H, void* ws, size_t ws_bytes, unsigned flags,
+                      void* stream) {
+    if (!X || !Wq_gu || !sw_gu || !Y_gu || !H) return fail(W4A8_ERR_NULL, "w4a8_gate_up_silu: NULL pointer");
+    if (N < 1 || N > 0x3FFFFFFF) return fail(W4A8_ERR_SHAPE, "N=%lld outside [1, 2^30-1]", (long long)N);
+    int st = check_w4a8_shape(M, K, 2 * N);
+    if (st != W4A8_OK) return st;
+    if (!aligned(X, 16) || !aligned(Wq_gu, 16) || !aligned(Y_gu, 4) || !aligned(sw_gu, 4) || !aligned(H, 2))
+        return fail(W4A8_ERR_ALIGN, "w4a8_gate_up_silu: X/Wq need 16-byte, Y/sw 4-byte, H 2-byte alignment");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M == 1) {
+        w4a8::GemvPlan pl;
+        if ((st = plan_for(true, true, 1, K, 2 * N, &pl, 0, -1, 0, true)) != W4A8_OK) return st;
+        if ((st = check_workspace(pl, ws, ws_bytes)) != W4A8_OK) return st;
+        cudaError_t e = w4a8::launch_w4a8_silu(pl, X, 1, K, Wq_gu, sw_gu, 2 * N, Y_gu, H, ws, flags, s);
+        return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_gate_up_silu launch");
+    }
+    // batches: the linear on the interleaved matrix, then the product as a
+    // launch of its own
+    if ((st = w4a8_linear(X, M, K, Wq_gu, sw_gu, 2 * N, Y_gu, nullptr, nullptr, nullptr, ws, ws_bytes, flags,
+                          stream)) != W4A8_OK)
+        return st;
+    cudaError_t e = w4a8::launch_silu_mul(Y_gu, Y_gu + 1, N, M, 2, 2 * N, H, flags, s);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_gate_up_silu product launch");
+}
+
+int w4a8_silu_mul(const float* g, const float* u, int64_t M, int64_t N, uint16_t* H, unsigned flags,
+                  void* stream) {
+    if (!g || !u || !H) return fail(W4A8_ERR_NULL, "w4a8_silu_mul: NULL pointer");
+    if (M < 1 || M > 65535 || N < 1 || N > 0x7FFFFFFF)
+        return fail(W4A8_ERR_SHAPE, "w4a8_silu_mul: M=%lld, N=%lld out of range", (long long)M, (long long)N);
+    if (!aligned(g, 4) || !aligned(u, 4) || !aligned(H, 2))
+        return fail(W4A8_ERR_ALIGN, "w4a8_silu_mul: g/u need 4-byte, H 2-byte alignment");
+    cudaError_t e = w4a8::launch_silu_mul(g, u, N, M, 1, N, H, flags, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_silu_mul launch");
+}
+
+int w4_interleave_rows(const uint8_t* Wq_a, const float* sw_a, const uint8_t* Wq_b, const float* sw_b,
+                       int64_t N, int64_t K, uint8_t* Wq_out, float* sw_out, void* stream) {
+    if (!Wq_a || !sw_a || !Wq_b || !sw_b || !Wq_out || !sw_out)
+        return fail(W4A8_ERR_NULL, "w4_interleave_rows: NULL pointer");
+    if (N < 1 || N > 0x3FFFFFFF || K < 32 || K % 32 || K > (1LL << 30))
+        return fail(W4A8_ERR_SHAPE, "w4_interleave_rows: N=%lld, K=%lld out of range", (long long)N, (long long)K);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t rb = (size_t)(K / 2);
+    cudaError_t e = cudaMemcpy2DAsync(Wq_out, 2 * rb, Wq_a, rb, rb, (size_t)N, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(Wq_out + rb, 2 * rb, Wq_b, rb, rb, (size_t)N, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(sw_out, 8, sw_a, 4, 4, (size_t)N, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(sw_out + 1, 8, sw_b, 4, 4, (size_t)N, cudaMemcpyDeviceToDevice, s);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "w4_interleave_rows copy");
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
 // w4a8_linear_noalloc: the fused linear with its split-K scratch in a static
 // device array, for callers that cannot provide workspace memory.
 // ---------------------------------------------------------------------------
-
-#include <mutex>
 
 namespace {
 
 // Scratch of the split-K kernel: 4096 bytes of arrival counters, then the
 // int32 partial sums.  Every GPU that loads this library holds it until exit.
+// A __device__ array starts zeroed when the library's device code is loaded
+// on a device, and every completed call leaves the counters at zero.
 constexpr size_t kNoAllocScratchBytes = W4A8_NOALLOC_SCRATCH;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {};
-
-// Device address of this device's scratch array.  The first call on a device
-// looks it up (the host-side symbol is only a stand-in, never a device
-// address) and clears the arrival counters on `stream`.
-int noalloc_scratch(cudaStream_t stream, void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64) return fail(W4A8_ERR_CUDA, "device ordinal %d not supported", dev);
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-        e = cudaMemsetAsync(p, 0, w4a8::kTicketBytes, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch counters");
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+// Device address of the current device's scratch array.  In host code the
+// array's name is only a stand-in, never a device address, so it is looked
+// up on every call (the lookup allocates nothing and stays right if the
+// context, and with it the array, is ever created anew).
+int noalloc_scratch(void** out) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    *out = p;
     return W4A8_OK;
 }
 
 }  // namespace
+
+// Clears the static scratch's arrival counters on `stream` (after a call
+// that gave up on a wait they may be left non-zero).
+cudaError_t w4a8_noalloc_reset(cudaStream_t stream) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    return cudaMemsetAsync(p, 0, w4a8::kTicketBytes, stream);
+}
 
 extern "C" int w4a8_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                                    const float* sw, int64_t N, float* Y, unsigned flags,
@@ -773,9 +932,7 @@ extern "C" int w4a8_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, cons
                     "the %zu-byte static scratch; use w4a8_linear with a workspace",
                     pl.ws_bytes, kNoAllocScratchBytes);
     void* scratch = nullptr;
-    if (pl.ws_bytes > 0 &&
-        (st = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch)) != W4A8_OK)
-        return st;
+    if (pl.ws_bytes > 0 && (st = noalloc_scratch(&scratch)) != W4A8_OK) return st;
     cudaError_t e = w4a8::launch_w4a8(pl, true, X, nullptr, nullptr, (int)M, K, Wq, sw, N, Y,
                                       nullptr, nullptr, nullptr, scratch, flags,
                                       static_cast<cudaStream_t>(stream));

@@ -103,3 +103,34 @@ cudaError_t read_and_clear_device_error(unsigned* flags, cudaStream_t stream) {
 }
 
 }  // namespace w4a8
+
+namespace w4a8 {
+
+// One-row fused W4A8 linear on an interleaved gate/up matrix (rows 2i =
+// gate i, 2i + 1 = up i, N2 rows) whose epilogue also writes the gated
+// products H[m][i] = binary16(silu(Y[m][2i]) * Y[m][2i+1]).  The plan must
+// have been made with pair = true.
+cudaError_t launch_w4a8_silu(const GemvPlan& pl, const uint16_t* X, int M, int64_t K, const uint8_t* Wq,
+                             const float* sw, int64_t N2, float* Y, uint16_t* H, void* ws, unsigned flags,
+                             cudaStream_t stream) {
+    GemvArgs a = {};
+    const void* s0 = sw;
+    set_segments(a, 1, &Wq, &s0, &N2, &Y);
+    a.X = reinterpret_cast<const __half*>(X);
+    a.H = reinterpret_cast<__half*>(H);
+    a.tickets = static_cast<unsigned*>(ws);
+    a.part = ws ? static_cast<uint8_t*>(ws) + kTicketBytes : nullptr;
+    a.M = M;
+    a.K = (int)K;
+    a.N = (int)N2;
+    a.pl = pl;
+    switch (pl.MT) {
+        case 1: return launch_w4a8_m1_fused(a, flags, stream);
+        case 2: return launch_one<true, 2, 4, true>(a, flags, stream);
+        case 4: return launch_one<true, 4, 2, true>(a, flags, stream);
+        case 8: return launch_one<true, 8, 1, true>(a, flags, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace w4a8

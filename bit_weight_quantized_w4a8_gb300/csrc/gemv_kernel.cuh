@@ -38,6 +38,7 @@
 #include "plan.h"
 #include "actq.cuh"
 #include "ptx.cuh"
+#include "silu.cuh"
 
 namespace w4a8 {
 
@@ -60,6 +61,9 @@ struct GemvArgs {
     int32_t* acc_out;       // optional [M][N] (W4, one segment)
     int8_t* Xq_out;         // optional [M][K] (W4 fused)
     float* sa_out;          // optional [M] (W4 fused)
+    __half* H;              // optional [M][N/2] (W4, one segment of paired rows: row 2i is
+                            // gate i, row 2i + 1 up i): H[m][i] = binary16(silu(Y[m][2i]) * Y[m][2i+1]);
+                            // every CTA then owns whole pairs
     void* part;             // split partials [P][M][N] (int32 or fp32)
     unsigned* tickets;      // [Gs] arrival counters at the workspace start,
                             // zero between calls
@@ -70,6 +74,19 @@ struct GemvArgs {
     int gld;                // group scales: floats per scale row
     GemvPlan pl;
 };
+
+// Gated products of the rows row0 .. row0 + nrows - 1 (whole pairs) of a
+// paired-row call, from the outputs the CTA has just written.
+__device__ __forceinline__ void silu_pairs(const GemvArgs& a, int64_t row0, int nrows, int tid) {
+    const int np = nrows >> 1;
+    const int64_t N = a.N;
+    for (int q = tid; q < a.M * np; q += kConsumers) {
+        const int m = q / np, i = q - m * np;
+        const int64_t n = row0 + 2 * i;
+        const float* y = a.Yg[0] + (int64_t)m * N + n;
+        a.H[(int64_t)m * (N / 2) + (n >> 1)] = silu_mul_h(__ldcg(y), __ldcg(y + 1));
+    }
+}
 
 // Waits on an mbarrier phase unless the CTA has already given up.  On a
 // timeout it records `bit` in the device error word and tells the other
@@ -222,8 +239,10 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
     const int p = blockIdx.x % pl.P;
     const int rb = blockIdx.x / pl.P;
     const int64_t N = a.N;
-    const int64_t row0 = (int64_t)rb * N / pl.Gs;
-    const int nrows = (int)((int64_t)(rb + 1) * N / pl.Gs - row0);
+    // paired rows (H): whole pairs per CTA, so that its epilogue sees both rows
+    const int64_t row0 = a.H ? 2 * ((int64_t)rb * (N / 2) / pl.Gs) : (int64_t)rb * N / pl.Gs;
+    const int nrows = (int)((a.H ? 2 * ((int64_t)(rb + 1) * (N / 2) / pl.Gs) : (int64_t)(rb + 1) * N / pl.Gs) -
+                            row0);
     const int nstages = (nrows + pl.Rl - 1) / pl.Rl;
     const int NS = pl.NS;
     const int g0 = p * pl.Gq;                   // first granule of this piece
@@ -702,7 +721,15 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
             if (!mbar_wait(smem_u32(full + s2 % NS), (s2 / NS) & 1))
                 atomicOr(&g_device_error, kErrDrainWait);
     }
-    if (pl.P == 1) return;
+    if (pl.P == 1) {
+        if (a.H != nullptr) {
+            // the CTA's outputs were written by its own threads: a barrier makes
+            // them visible, then each pair of rows gives one gated product
+            named_bar_sync(1, kConsumers);
+            if (!*abort_flag) silu_pairs(a, row0, nrows, tid);
+        }
+        return;
+    }
 
     // ---------------------------------------------- split-K: last CTA sums
     __threadfence();
@@ -737,6 +764,10 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                 }
             }
         }
+    }
+    if (a.H != nullptr) {
+        named_bar_sync(1, kConsumers);
+        silu_pairs(a, row0, nrows, tid);
     }
     if (tid == 0) a.tickets[rb] = 0u;  // ready for the next call
 }

@@ -6,6 +6,7 @@
 #include <cstdint>
 
 #include "plan.h"
+#include "qmma_plan.h"
 #include "rowdot_plan.h"
 
 namespace w4a8 {
@@ -70,6 +71,28 @@ cudaError_t launch_w4a8_rowdot(const RowdotPlan& pl, const uint16_t* X, const in
                                unsigned flags, cudaStream_t stream, int gs = 0,
                                const float* const* sg = nullptr);
 cudaError_t read_and_clear_rowdot_error(unsigned* flags, cudaStream_t stream);
+
+// Warp-level e4m3 MMA kernel for small batches (qmma.cu).  make_qmma_plan
+// is host-only and needs no GPU; R = 16-row tiles per warp (1, 2 or 4; 0 =
+// the default for the batch size).
+bool make_qmma_plan(int M, int64_t K, int64_t N, int num_sms, QmmaPlan* out, int R = 0);
+cudaError_t launch_w4a8_qmma(const QmmaPlan& pl, const uint16_t* X, const int8_t* Xq, const float* sa,
+                             int M, int64_t K, int G, const uint8_t* const* Wq,
+                             const float* const* sw, const int64_t* Ns, float* const* Y,
+                             int32_t* acc_out, int8_t* Xq_out, float* sa_out, void* ws,
+                             unsigned flags, cudaStream_t stream,
+                             unsigned long long stall_ns = 0);
+cudaError_t read_and_clear_qmma_error(unsigned* flags, cudaStream_t stream);
+
+// The MLP's gated product (gemv.cu, silu.cu): the one-row GEMV over an
+// interleaved gate/up matrix with the product in its epilogue (a plan made
+// with pair = true), and the stand-alone kernel
+// h[m][i] = binary16(silu(g[m * ld + i * stride]) * u[m * ld + i * stride]).
+cudaError_t launch_w4a8_silu(const GemvPlan& pl, const uint16_t* X, int M, int64_t K, const uint8_t* Wq,
+                             const float* sw, int64_t N2, float* Y, uint16_t* H, void* ws, unsigned flags,
+                             cudaStream_t stream);
+cudaError_t launch_silu_mul(const float* g, const float* u, int64_t n, int64_t M, int64_t stride, int64_t ld,
+                            uint16_t* h, unsigned flags, cudaStream_t stream);
 
 // IndexSoftmax (isx.cu).  The host helpers need no GPU.
 constexpr int kIsxMaxEntries = 256;  // 2^b table entries, b <= 8

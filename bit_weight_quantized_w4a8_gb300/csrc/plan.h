@@ -98,8 +98,12 @@ inline int group_window_max(const GemvPlan& pl, int gshift, int gld) {
 // w4: INT4 weights (32 codes per granule) else INT8 (16 per granule).
 // gshift >= 0: INT4 with one scale per 2^gshift granules along K, scale rows
 // of gld floats (a multiple of 4); -1: one scale per row.
+// pair: the rows come in pairs (the gated product of gate/up rows 2i, 2i+1)
+// and every CTA takes whole pairs.
 inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int num_sms,
-                           const Tuning& tu, GemvPlan* out, int gshift = -1, int gld = 0) {
+                           const Tuning& tu, GemvPlan* out, int gshift = -1, int gld = 0,
+                           bool pair = false) {
+    if (pair && (N < 2 || N % 2)) return false;
     if (gshift >= 0 && (!w4 || gld <= 0 || gld % 4)) return false;
     GemvPlan pl = {};
     pl.MT = mt_of(M);
@@ -135,12 +139,13 @@ inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int
         }
         int64_t Gs = (int64_t)num_sms * cps / P;
         if (Gs < 1) Gs = 1;
-        if (Gs > N) Gs = N;
+        if (Gs > (pair ? N / 2 : N)) Gs = pair ? N / 2 : N;
         if (P > 1 && Gs > kTicketSlots) Gs = kTicketSlots;
-        int64_t rows_max = (N + Gs - 1) / Gs;
+        auto rows_of = [&](int64_t gs) { return pair ? 2 * ((N / 2 + gs - 1) / gs) : (N + gs - 1) / gs; };
+        int64_t rows_max = rows_of(Gs);
         while (P == 1 && rows_max > kMaxRowsPerCta) {  // keep the scale cache small
             Gs += (int64_t)num_sms * cps;
-            rows_max = (N + Gs - 1) / Gs;
+            rows_max = rows_of(Gs);
         }
         if (Gs * P > 0x7FFFFFFF) continue;
         // Streaming cost ~ granules per CTA; low lane utilisation only costs

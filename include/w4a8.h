@@ -134,7 +134,8 @@ int act_quantize_i8(const uint16_t* X, int64_t M, int64_t K, int8_t* Xq, float* 
  * tensor-core path the activation codes and int32 accumulators, which its
  * first kernel clears).  The counters must be zero before the first call
  * (zero-fill the buffer once); every call leaves them zero, so one
- * workspace can serve calls of any shape, in either precision.  Calls that share a workspace must not run
+ * workspace can serve calls of any shape, in either precision (after a
+ * non-zero w4a8_device_error, zero-fill it again).  Calls that share a workspace must not run
  * concurrently (same stream, or ordered by events).  Returns 0 for shapes
  * the linear entry points reject. */
 size_t w4a8_workspace_bytes(int64_t M, int64_t K, int64_t N);
@@ -194,16 +195,77 @@ int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const ui
  * bytes: 4096 bytes of arrival counters, then int32 partials) that every GPU
  * loading the library holds until the process exits.  Shapes whose plan
  * needs more scratch are rejected with W4A8_ERR_WORKSPACE (at M = 1 and four
- * K pieces that is N > 261,888).  The first call on a device that needs
- * scratch looks up the array's device address and clears its counters on
- * `stream`; make that first call before any stream capture.  Every call on a
- * device shares the one array, which keeps the last call's contents; the
- * kernels leave the counters at zero, so calls in order on one stream are
- * fine, but calls whose executions overlap on the GPU (different streams
- * without ordering between them) race and give wrong results. */
+ * K pieces that is N > 261,888).  Each call that needs scratch looks up the
+ * array's device address on the current device (a lookup, no allocation);
+ * the first call on a device may load the library's device code there, so
+ * make it before any stream capture.  Every call on a device shares the one
+ * array, which keeps the last call's contents; the array starts zeroed and
+ * the kernels leave its counters at zero, so calls in order on one stream
+ * are fine, but calls whose executions overlap on the GPU (different
+ * streams without ordering between them) race and give wrong results.  A
+ * call whose kernel gave up on a bounded wait may leave the counters
+ * non-zero; w4a8_device_error, which reports that, also clears them. */
 #define W4A8_NOALLOC_SCRATCH (4u << 20)
 int w4a8_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                         const float* sw, int64_t N, float* Y, unsigned flags, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* The MLP's gated product: gate/up projections -> down projection          */
+/* ---------------------------------------------------------------------- */
+
+/* The INT4 page's model (HIDDEN 3584, INTERMEDIATE 18944) has the MLP
+ * down(silu(gate(x)) * up(x)); section 后续优化方向 asks to cut the
+ * quantization overhead of the MLP.  The page does not print the
+ * activation; the reading is that model family's SwiGLU, silu(g) = g / (1 +
+ * exp(-g)).  The calls below produce the down projection's binary16 input h
+ * where gate and up are produced, so down (w4a8_linear on h) quantizes one
+ * binary16 vector and no separate launch sits between the two linears.
+ *
+ * Contract, per element: h = binary16(silu(g) * u) computed in fp32 (expf
+ * within 2 ulp, then one add, one division, one multiply, each rounded to
+ * nearest, then one round-to-nearest-even conversion).  The fp32 value is
+ * within 2^-20 |v| of v = silu(g) * u in exact arithmetic, so h equals the
+ * binary16 rounding of v unless v lies within 2^-20 |v| of a binary16
+ * rounding boundary (where either neighbour may result). */
+
+/* Interleaves the rows of two packed weight matrices of the same shape
+ * (gate and up): out row 2i = a row i, out row 2i + 1 = b row i, and the same
+ * for the scales.  Quantization is row-wise, so this equals quantizing the
+ * row-interleaved fp32 matrix.  Device-to-device copies on `stream`.
+ *   Wq_a, Wq_b [N][K/2] uint8, sw_a, sw_b [N] fp32 in;
+ *   Wq_out [2N][K/2] uint8, sw_out [2N] fp32 out.
+ * Requires 1 <= N <= 2^30 - 1, K >= 32, K % 32 == 0. */
+int w4_interleave_rows(const uint8_t* Wq_a, const float* sw_a, const uint8_t* Wq_b, const float* sw_b,
+                       int64_t N, int64_t K, uint8_t* Wq_out, float* sw_out, void* stream);
+
+/* Workspace bytes of w4a8_gate_up_silu (rules of w4a8_workspace_bytes). */
+size_t w4a8_gate_up_silu_workspace_bytes(int64_t M, int64_t K, int64_t N);
+
+/* Gate and up projections with the gated product in the epilogue.
+ *   X [M][K] binary16 in; Wq_gu [2N][K/2], sw_gu [2N]: gate and up
+ *   interleaved by rows (w4_interleave_rows);
+ *   Y_gu [M][2N] fp32 out: Y_gu[m][2i] = gate i, Y_gu[m][2i+1] = up i, each
+ *     bit-identical to w4a8_linear on that projection;
+ *   H [M][N] binary16 out: H[m][i] = binary16(silu(Y_gu[m][2i]) *
+ *     Y_gu[m][2i+1]) under the contract above;
+ *   ws, ws_bytes (w4a8_gate_up_silu_workspace_bytes), flags as w4a8_linear.
+ * One row: one launch of the fused GEMV, each CTA owning whole gate/up row
+ * pairs and writing their products after its outputs.  Batches of 2+ rows:
+ * the W4A8 linear on the interleaved matrix, then the product as a launch of
+ * its own (w4a8_silu_mul's kernel).
+ * Requires the w4a8_linear limits with 2N output rows; X and Wq_gu 16-byte,
+ * Y_gu and sw_gu 4-byte, H 2-byte aligned. */
+int w4a8_gate_up_silu(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq_gu, const float* sw_gu,
+                      int64_t N, float* Y_gu, uint16_t* H, void* ws, size_t ws_bytes, unsigned flags,
+                      void* stream);
+
+/* The gated product on its own (the unfused step):
+ *   H[m][i] = binary16(silu(g[m][i]) * u[m][i]), g, u [M][N] fp32,
+ *   H [M][N] binary16, same contract.  flags: 0 or W4A8_LAUNCH_PDL.
+ * Requires 1 <= M <= 65535, 1 <= N <= 2^31 - 1; g, u 4-byte, H 2-byte
+ * aligned. */
+int w4a8_silu_mul(const float* g, const float* u, int64_t M, int64_t N, uint16_t* H, unsigned flags,
+                  void* stream);
 
 /* ---------------------------------------------------------------------- */
 /* W4A8 with group-wise weight scales                                      */
@@ -357,7 +419,11 @@ const char* w4a8_last_error(void);
 
 /* Copies the current device's error word into *flags and clears it.  Bit 0:
  * a wait for weight data ran out; bit 1: unused; bit 2: a wait for
- * in-flight copies at exit ran out.
+ * in-flight copies at exit ran out.  A non-zero word means that some call's
+ * outputs are unspecified and that the split-K arrival counters of the
+ * workspace it used may be left non-zero: zero-fill that workspace again
+ * before reusing it.  (The static scratch of w4a8_linear_noalloc is cleared
+ * here, on `stream`, whenever the word is non-zero.)
  * Synchronises `stream` first.  Returns W4A8_OK or W4A8_ERR_CUDA. */
 int w4a8_device_error(unsigned* flags, void* stream);
 
@@ -383,6 +449,18 @@ int w4a8_device_error(unsigned* flags, void* stream);
  *   mma_e4m3: operands of the row-wise tensor-core kernel: 0 = default,
  *     1 = bf16 (kind::f16, K = 16 per MMA), 2 = e4m3 (kind::f8f6f4, K = 32
  *     per MMA, activation codes split as 16 a_hi + a_lo).
+ *   qmma_max_m: activation rows up to which row-wise W4A8 calls use the
+ *     warp-level e4m3 MMA kernel, from 2 rows (0 = the default 4..8 rows,
+ *     1 = never, <= 32); it takes precedence over rowdot_max_m and
+ *     mma_min_m.
+ *   qmma_tiles_per_warp: 16-row weight tiles per warp of that kernel (1, 2,
+ *     or 4 for at most 16 rows; 0 = default).
+ *   stall_test_us: for tests of the bounded waits (0 = off, <= 1 s): the
+ *     warp-level MMA kernel's warps first wait, with this limit in
+ *     microseconds, for a barrier phase that nothing completes.  The wait
+ *     runs out, sets bit 0 of the device error word and stops the call (its
+ *     outputs unspecified); copies already in flight are waited for (with
+ *     the usual limit) before the kernel exits.
  * w4a8_workspace_bytes reflects the overrides.  NULL restores the defaults.
  * Not synchronised with calls running on other threads. */
 typedef struct {
@@ -393,6 +471,9 @@ typedef struct {
     int mma_min_m;
     int rowdot_max_m;
     int mma_e4m3;
+    int qmma_max_m;
+    int qmma_tiles_per_warp;
+    int stall_test_us;
 } w4a8_tuning_t;
 
 int w4a8_set_tuning(const w4a8_tuning_t* tuning);

@@ -108,7 +108,8 @@ def test_tuning_validation():
 SHAPES = [(1, 896, 512), (1, 3584, 3584), (1, 3584, 512), (1, 3584, 18944), (1, 18944, 3584),
           (1, 3584, 152064), (2, 3584, 18944), (4, 18944, 3584), (8, 3584, 18944),
           (8, 18944, 3584), (3, 32, 1), (1, 64, 100000), (5, 131072, 3), (1, 4096, 7),
-          (16, 3584, 18944), (64, 18944, 3584), (33, 896, 100)]
+          (16, 3584, 18944), (64, 18944, 3584), (33, 896, 100), (32, 3584, 152064),
+          (24, 131072, 7), (17, 896, 100), (2, 32, 1)]
 
 
 @pytest.mark.parametrize("sms", [152, 148, 20, 1])
@@ -123,6 +124,9 @@ def test_plan_invariants(sms, w8):
             continue
         if p["kernel"] == 2:
             check_rowdot_plan(p, M, K, N, sms)
+            continue
+        if p["kernel"] == 3:
+            check_qmma_plan(p, M, K, N, sms)
             continue
         M = min(M, 4 if w8 else 8)  # the plan of the first launch of a row-group sequence
         kgran = 16 if w8 else 32
@@ -159,6 +163,28 @@ def check_mma_plan(p, M, K, N, sms):
     assert p["ws_bytes"] >= 4096 + 256 + M * K * 2
 
 
+def check_qmma_plan(p, M, K, N, sms):
+    """The warp-level MMA kernel: 4 batch rows per n-tile, 16-row tiles per
+    warp R, pieces of whole 256-code boxes, every warp's fp32 sums over at
+    most 65536 codes, stages of one weight box plus its activation slice."""
+    assert 2 <= M <= 32
+    tiles = -(-N // 128)
+    nbox = -(-K // 256)
+    NT = -(-M // 4)
+    P, R = p["splits"], p["threads_per_row"]
+    assert p["cols_per_thread"] == 4 * NT and R in (1, 2, 4) and (R < 4 or NT <= 4)
+    assert p["ctas_per_split"] == tiles and p["grid"] == tiles * P
+    bpp = -(-nbox // P)
+    assert (P - 1) * bpp < nbox                                  # no empty piece
+    assert -(-bpp // R) * 256 <= 65536                           # exact fp32 sums per warp
+    assert p["stage_bytes"] == 16384 + 2048 * NT
+    assert 2 <= p["stages"] <= 8 or p["stages"] == bpp
+    assert p["stages"] * p["stage_bytes"] + 128 * 4 * NT * 4 < p["smem_bytes"] <= 227 * 1024
+    assert P == 1 or tiles <= 1024
+    pre = -(-nbox * 256 // 2048)
+    assert p["ws_bytes"] >= 4096 + 256 + M * pre * 4 + nbox * 2048 * NT + (tiles * M * 512 if P > 1 else 0)
+
+
 def check_rowdot_plan(p, M, K, N, sms):
     assert 2 <= M <= 8
     tiles = -(-N // 128)
@@ -177,39 +203,53 @@ def check_rowdot_plan(p, M, K, N, sms):
 
 
 def test_kernel_routing():
-    """Row-wise calls: 1 row on the dp4a GEMV, 2..8 rows on the
-    row-per-thread kernel, 9+ on the tensor cores; the tuning moves both
-    thresholds."""
+    """Row-wise calls: 1 row on the dp4a GEMV, 2..3 rows on the
+    row-per-thread kernel, 4..8 on the warp-level MMA kernel, 9+ on the
+    tensor cores; an explicit qmma_max_m gives the warp-level kernel 2 rows
+    up to it; with it switched off, 2..8 rows on the row-per-thread kernel
+    and 9+ on the tensor cores; the tuning moves every threshold."""
     try:
         route = lambda M: w4.w4a8_plan_info(M, 3584, 18944, num_sms=152)["kernel"]
+        assert [route(M) for M in (1, 2, 3, 4, 8, 9, 32, 64)] == [0, 2, 2, 3, 3, 1, 1, 1]
+        w4.w4a8_set_tuning(qmma_max_m=16)
+        assert [route(M) for M in (2, 16, 17)] == [3, 3, 1]
+        w4.w4a8_set_tuning(qmma_max_m=32, qmma_tiles_per_warp=1)
+        assert w4.w4a8_plan_info(20, 3584, 18944, num_sms=152)["threads_per_row"] == 1
+        w4.w4a8_set_tuning(qmma_max_m=32, qmma_tiles_per_warp=4)   # 4 tiles a warp up to 16 rows
+        assert [route(M) for M in (16, 17)] == [3, 1]
+        with pytest.raises(w4.W4A8Error):
+            w4.w4a8_set_tuning(qmma_tiles_per_warp=3)
+        w4.w4a8_set_tuning(qmma_max_m=1)
         assert [route(M) for M in (1, 2, 3, 8, 9, 64)] == [0, 2, 2, 2, 1, 1]
-        w4.w4a8_set_tuning(rowdot_max_m=4)
+        with pytest.raises(w4.W4A8Error):
+            w4.w4a8_set_tuning(qmma_max_m=33)
+        w4.w4a8_set_tuning(rowdot_max_m=4, qmma_max_m=1)
         assert [route(M) for M in (2, 4, 5)] == [2, 2, 1]
-        w4.w4a8_set_tuning(rowdot_max_m=1)
+        w4.w4a8_set_tuning(rowdot_max_m=1, qmma_max_m=1)
         assert [route(M) for M in (2, 3)] == [0, 1]
         for tpr in (2, 4, 8):
-            w4.w4a8_set_tuning(force_threads_per_row=tpr)
+            w4.w4a8_set_tuning(force_threads_per_row=tpr, qmma_max_m=1)
             p = w4.w4a8_plan_info(5, 3584, 18944, num_sms=152)
             assert p["threads_per_row"] == tpr and p["kernel"] == 2
             check_rowdot_plan(p, 5, 3584, 18944, 152)
         with pytest.raises(w4.W4A8Error):
-            w4.w4a8_set_tuning(rowdot_max_m=9)
+            w4.w4a8_set_tuning(rowdot_max_m=9, qmma_max_m=1)
         with pytest.raises(w4.W4A8Error):
             w4.w4a8_set_tuning(mma_e4m3=3)
-        w4.w4a8_set_tuning(mma_e4m3=2, rowdot_max_m=1)  # operand type does not change the plan
+        w4.w4a8_set_tuning(mma_e4m3=2, rowdot_max_m=1, qmma_max_m=1)  # operand type does not change the plan
         assert w4.w4a8_plan_info(4, 3584, 18944, num_sms=152)["kernel"] == 1
         # group scales: the row-per-thread kernel at 2..8 rows, the tensor cores above
         w4.w4a8_set_tuning()
         assert w4.w4a8g_plan_info(4, 3584, 18944, 128, num_sms=152)["kernel"] == 2
         assert w4.w4a8g_plan_info(9, 3584, 18944, 128, num_sms=152)["kernel"] == 1
         assert w4.w4a8g_plan_info(4, 3584, 18944, 32, num_sms=152)["kernel"] == 2
-        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
+        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)
         assert w4.w4a8_plan_info(64, 3584, 18944, num_sms=152)["kernel"] == 0
-        w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1)
+        w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, qmma_max_m=1)
         assert w4.w4a8_plan_info(2, 3584, 18944, num_sms=152)["kernel"] == 1
         assert w4.w4a8_plan_info(1, 3584, 18944, num_sms=152)["kernel"] == 0
         with pytest.raises(w4.W4A8Error):
-            w4.w4a8_set_tuning(mma_min_m=1)
+            w4.w4a8_set_tuning(mma_min_m=1, qmma_max_m=1)
     finally:
         w4.w4a8_set_tuning(reset=True)
 
@@ -269,7 +309,7 @@ def test_group_plan_windows(sms, splits):
     and ends on 16-byte words inside the padded scale row, and the slot's
     scale area holds a whole stage of rows."""
     try:
-        w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65, rowdot_max_m=1)  # the dp4a kernel's plans
+        w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)  # the dp4a kernel's plans
         for (M, K, N, gs) in GROUP_SHAPES:
             if splits and splits > K // 32:
                 continue
@@ -345,7 +385,7 @@ def test_group_tensor_core_plans():
     hold whole groups and whole weight loads, and the workspace covers the
     fp32 partials of every piece."""
     try:
-        w4.w4a8_set_tuning(rowdot_max_m=1)  # 2..8 rows would take the row-per-thread kernel
+        w4.w4a8_set_tuning(rowdot_max_m=1, qmma_max_m=1)  # 2..8 rows would take the row-per-thread kernel
         for sms in (152, 148, 20):
             for (M, K, N, gs) in [(3, 3584, 300, 128), (16, 3584, 18944, 128), (64, 18944, 3584, 128),
                                   (4, 3584, 1000, 256), (8, 2048, 200, 512), (33, 896, 100, 128),
@@ -364,7 +404,7 @@ def test_group_tensor_core_plans():
                     assert p["ws_bytes"] >= 4096 + 256 + M * K * 2 + p["grid"] * M * 128 * 4
             for (M, K, N, gs) in [(3, 1024, 77, 32), (8, 3584, 100, 64), (2, 3584, 100, 128)]:
                 assert w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)["kernel"] == 0
-        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
+        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)
         assert w4.w4a8g_plan_info(16, 3584, 18944, 128, num_sms=152)["kernel"] == 0
     finally:
         w4.w4a8_set_tuning(reset=True)
@@ -393,14 +433,40 @@ def test_rowdot_workspace_covers_grouped_matrices():
     """A grouped call plans each matrix on its own inside the workspace sized
     for the total rows: every smaller matrix's plan needs no more, and plans
     that never split K do not reserve partial sums per tile."""
+    try:
+        w4.w4a8_set_tuning(qmma_max_m=1)
+        for sms in (152, 148, 20):
+            for (M, K) in [(2, 3584), (8, 3584), (8, 18944), (5, 131072), (3, 896)]:
+                N = 40000
+                full = w4.w4a8_plan_info(M, K, N, num_sms=sms)
+                assert full["kernel"] == 2
+                for Np in (1, 7, 128, 129, 1000, 4608, 18944, 39999):
+                    p = w4.w4a8_plan_info(M, K, Np, num_sms=sms)
+                    check_rowdot_plan(p, M, K, Np, sms)
+                    assert p["ws_bytes"] <= full["ws_bytes"], (M, K, Np, sms)
+        p = w4.w4a8_plan_info(8, 3584, 152064, num_sms=152)  # lm_head: one piece per tile
+        assert p["splits"] == 1 and p["ws_bytes"] < 2 * 1024 * 1024
+    finally:
+        w4.w4a8_set_tuning(reset=True)
+
+
+def test_qmma_workspace_covers_grouped_matrices():
+    """The same for the warp-level MMA kernel: each matrix of a grouped call
+    fits the workspace planned for the total rows."""
+    try:
+        w4.w4a8_set_tuning(qmma_max_m=32)
+        _qmma_grouped_cases()
+    finally:
+        w4.w4a8_set_tuning(reset=True)
+
+
+def _qmma_grouped_cases():
     for sms in (152, 148, 20):
-        for (M, K) in [(2, 3584), (8, 3584), (8, 18944), (5, 131072), (3, 896)]:
+        for (M, K) in [(2, 3584), (8, 3584), (16, 18944), (32, 131072), (3, 896), (32, 3584)]:
             N = 40000
             full = w4.w4a8_plan_info(M, K, N, num_sms=sms)
-            assert full["kernel"] == 2
+            assert full["kernel"] == 3
             for Np in (1, 7, 128, 129, 1000, 4608, 18944, 39999):
                 p = w4.w4a8_plan_info(M, K, Np, num_sms=sms)
-                check_rowdot_plan(p, M, K, Np, sms)
+                check_qmma_plan(p, M, K, Np, sms)
                 assert p["ws_bytes"] <= full["ws_bytes"], (M, K, Np, sms)
-    p = w4.w4a8_plan_info(8, 3584, 152064, num_sms=152)  # lm_head: one piece per tile
-    assert p["splits"] == 1 and p["ws_bytes"] < 2 * 1024 * 1024

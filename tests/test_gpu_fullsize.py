@@ -1,14 +1,26 @@
 """Full-size workloads in the launch configuration the benchmark times, checked
-against the CPU oracle on sampled output rows (the oracle regenerates just
-those weight rows from the counter-based generator).
+against the CPU oracle on EVERY output element.
+
+Weights are drawn on the host by the C twin of the seeded generator
+(synth.normal_host: the same bits as the numpy definition), quantized by the
+oracle (row chunks on host threads) and, separately, uploaded and quantized
+by the GPU; packed codes and scales are compared in full, then every output
+of the GPU linear against the oracle's.
 
 * Qwen2-7B-shaped decode linear set, M=1, W4A8 (q, k, v, o, gate, up, down,
-  lm_head), activations with 0.1% x20 outliers, fused activation quantization,
-  programmatic dependent launch.
+  lm_head), activations with 0.1% x20 outliers, fused activation
+  quantization, programmatic dependent launch; and the same step as the
+  benchmark launches it (q/k/v and gate/up grouped).
+* The full 28-layer decode step's own weights and activations (seeds
+  1000 * (layer + 1) + index) for layers 0, 13 and 27, all five launches of
+  each layer as the benchmark runs them.
 * Skinny-batch sweep on gate and down, M in {1, 2, 4, 8, 16, 32, 64}, and
   lm_head at 3, 8 and 16 rows.
-* ChatGLM2-6B-shaped W8A16 GEMVs.
+* ChatGLM2-6B-shaped W8A16 GEMVs (every output within the tolerance).
 """
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import pytest
 
@@ -23,10 +35,14 @@ pytestmark = pytest.mark.gpu
 QWEN2_7B_SET = [("q", 3584, 3584), ("k", 3584, 512), ("v", 3584, 512), ("o", 3584, 3584),
                 ("gate", 3584, 18944), ("up", 3584, 18944), ("down", 18944, 3584),
                 ("lm_head", 3584, 152064)]
+LAUNCHES = [("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")),
+            ("down", ("down",)), ("lm_head", ("lm_head",))]
 CHATGLM2_W8A16 = [("h_to_4h", 4096, 27392), ("qkv", 4096, 4608), ("4h_to_h", 13696, 4096)]
 WEIGHT_SEED0 = 1000
 ACT_SEED_OFFSET = 500
 OUTLIER_FRAC = 0.001
+NAMES = [s[0] for s in QWEN2_7B_SET]
+THREADS = os.cpu_count() or 4
 
 
 @pytest.fixture(scope="module")
@@ -48,92 +64,156 @@ def bits(a):
     return np.ascontiguousarray(a).view(np.uint32)
 
 
-def sample_rows(N, seed, n=48):
-    rng = np.random.Generator(np.random.PCG64(seed))
-    rows = set(rng.choice(N, size=min(n, N), replace=False).tolist()) | {0, N - 1}
-    return np.array(sorted(rows), np.int64)
+def chunks(n, parts):
+    step = max(1, -(-n // parts))
+    return [(i, min(n, i + step)) for i in range(0, n, step)]
+
+
+def oracle_quantize(orc, W):
+    """orc.w4_quantize over row chunks on host threads (rows are independent)."""
+    N, K = W.shape
+    Wq = np.empty((N, K // 2), np.uint8)
+    sw = np.empty(N, np.float32)
+
+    def one(c):
+        q, s = orc.w4_quantize(W[c[0]:c[1]])
+        Wq[c[0]:c[1]], sw[c[0]:c[1]] = q, s
+
+    with cf.ThreadPoolExecutor(THREADS) as ex:
+        list(ex.map(one, chunks(N, 4 * THREADS)))
+    return Wq, sw
+
+
+def oracle_linear(orc, X, Wq, sw):
+    """orc.w4a8_linear over output-row chunks on host threads: (Y, Xq, sa)."""
+    N = Wq.shape[0]
+    Y = np.empty((X.shape[0], N), np.float32)
+    first = {}
+
+    def one(c):
+        y, xq, sa, _ = orc.w4a8_linear(X, Wq[c[0]:c[1]], sw[c[0]:c[1]])
+        Y[:, c[0]:c[1]] = y
+        if c[0] == 0:
+            first["xq"], first["sa"] = xq, sa
+
+    with cf.ThreadPoolExecutor(THREADS) as ex:
+        list(ex.map(one, chunks(N, 4 * THREADS)))
+    return Y, first["xq"], first["sa"]
+
+
+_weights = {}
+
+
+def weights(w4, orc, seed, N, K):
+    """(Wq, sw) on the GPU and (Wq_ref, sw_ref) from the oracle for the
+    weight tensor normal(seed, (N, K), 0.02); the GPU quantizer is checked
+    against the oracle on every byte and scale.  Cached per tensor."""
+    key = (seed, N, K)
+    if key not in _weights:
+        W = synth.normal_host(seed, (N, K), 0.02)
+        Wd = torch.from_numpy(W).cuda()
+        Wq, sw = w4.w4_quantize_weights(Wd)
+        del Wd
+        Wq_ref, sw_ref = oracle_quantize(orc, W)
+        del W
+        assert np.array_equal(Wq.cpu().numpy(), Wq_ref), "packed weights differ (seed %d)" % seed
+        assert np.array_equal(bits(sw.cpu().numpy()), bits(sw_ref)), "weight scales differ (seed %d)" % seed
+        if len(_weights) > 24:
+            _weights.clear()
+        _weights[key] = (Wq, sw, Wq_ref, sw_ref)
+    return _weights[key]
 
 
 def run_w4(w4, orc, K, N, M, seed, flags):
-    W = synth.normal_gpu(seed, (N, K), 0.02)
-    Wq, sw = w4.w4_quantize_weights(W)
-    rows = sample_rows(N, seed)
-    W_rows_dev = W[torch.from_numpy(rows).cuda()].cpu().numpy()
-    del W
+    Wq, sw, Wq_ref, sw_ref = weights(w4, orc, seed, N, K)
     X = synth.activation(seed + ACT_SEED_OFFSET, M, K, outlier_frac=OUTLIER_FRAC)
     Xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
     sa = torch.empty((M,), dtype=torch.float32, device="cuda")
     Y = w4.w4a8_linear(torch.from_numpy(X).cuda(), Wq, sw, Xq_out=Xq, sa_out=sa, flags=flags)
     torch.cuda.synchronize()
-
-    W_rows = synth.weight_rows(seed, N, K, rows)
-    assert np.array_equal(bits(W_rows_dev), bits(W_rows))  # generator twins agree
-    Wq_ref, sw_ref = orc.w4_quantize(W_rows)
-    assert np.array_equal(Wq[torch.from_numpy(rows).cuda()].cpu().numpy(), Wq_ref)
-    assert np.array_equal(bits(sw.cpu().numpy()[rows]), bits(sw_ref))
-    Y_ref, Xq_ref, sa_ref, _ = orc.w4a8_linear(X, Wq_ref, sw_ref)
+    Y_ref, Xq_ref, sa_ref = oracle_linear(orc, X, Wq_ref, sw_ref)
     assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
     assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
-    assert np.array_equal(bits(Y.cpu().numpy()[:, rows]), bits(Y_ref))
-    assert np.isfinite(Y.cpu().numpy()).all()
+    Yh = Y.cpu().numpy()
+    bad = np.argwhere(bits(Yh) != bits(Y_ref))
+    assert bad.size == 0, ("%d outputs differ" % len(bad), bad[:5])
+    assert np.isfinite(Yh).all()
 
 
-@pytest.mark.parametrize("idx", range(len(QWEN2_7B_SET)), ids=[s[0] for s in QWEN2_7B_SET])
+@pytest.mark.parametrize("idx", range(len(QWEN2_7B_SET)), ids=NAMES)
 def test_qwen2_7b_linear_set_m1(w4, orc, idx):
     name, K, N = QWEN2_7B_SET[idx]
     run_w4(w4, orc, K, N, 1, WEIGHT_SEED0 + idx, flags=w4.LAUNCH_PDL)
     assert w4.w4a8_device_error() == 0
 
 
-def test_decode_step_as_benchmarked(w4, orc):
-    """One step exactly as bench.py runs it (grouped q/k/v and gate/up, PDL),
-    sampled rows of every output checked against the oracle."""
-    import bench
-    names = [l[0] for l in bench.LINEARS]
-    Wqs, sws, Ys = {}, {}, {}
-    for i, (name, K, N) in enumerate(bench.LINEARS):
-        W = synth.normal_gpu(bench.WEIGHT_SEED0 + i, (N, K), 0.02)
-        Wqs[name], sws[name] = w4.w4_quantize_weights(W)
-        del W
-    Xs = {}
-    for lname, members in bench.LAUNCHES:
-        K = bench.LINEARS[names.index(members[0])][1]
-        X = synth.activation(bench.activation_seed(members[0]), 1, K, outlier_frac=bench.OUTLIER_FRAC)
-        Xs[lname] = X
-        Xd = torch.from_numpy(X).cuda()
+def run_step(w4, orc, wseed, aseed, launches, check_every=True):
+    """The launches of one decode layer (q/k/v and gate/up grouped, PDL) on
+    weights wseed(i) and activations aseed(first member); every output is
+    compared with the oracle."""
+    Wd, refs, Xs, Ys = {}, {}, {}, {}
+    for lname, members in launches:
+        for n in members:
+            i = NAMES.index(n)
+            _, K, N = QWEN2_7B_SET[i]
+            Wq, sw, Wq_ref, sw_ref = weights(w4, orc, wseed(i), N, K)
+            Wd[n] = (Wq, sw)
+            refs[n] = (Wq_ref, sw_ref)
+        K = QWEN2_7B_SET[NAMES.index(members[0])][1]
+        Xs[lname] = synth.activation(aseed(NAMES.index(members[0])), 1, K, outlier_frac=OUTLIER_FRAC)
+    for lname, members in launches:
+        Xd = torch.from_numpy(Xs[lname]).cuda()
         if len(members) == 1:
-            Ys[members[0]] = w4.w4a8_linear(Xd, Wqs[members[0]], sws[members[0]], flags=w4.LAUNCH_PDL)
+            Wq, sw = Wd[members[0]]
+            Ys[members[0]] = w4.w4a8_linear(Xd, Wq, sw, flags=w4.LAUNCH_PDL)
         else:
-            out = w4.w4a8_linear_grouped(Xd, [Wqs[n] for n in members], [sws[n] for n in members],
+            out = w4.w4a8_linear_grouped(Xd, [Wd[n][0] for n in members], [Wd[n][1] for n in members],
                                          flags=w4.LAUNCH_PDL)
             Ys.update(dict(zip(members, out)))
     torch.cuda.synchronize()
-    for lname, members in bench.LAUNCHES:
-        for name in members:
-            i = names.index(name)
-            _, K, N = bench.LINEARS[i]
-            rows = sample_rows(N, 7000 + i, n=24)
-            Wq_ref, sw_ref = orc.w4_quantize(synth.weight_rows(bench.WEIGHT_SEED0 + i, N, K, rows))
-            Y_ref = orc.w4a8_linear(Xs[lname], Wq_ref, sw_ref)[0]
-            assert np.array_equal(bits(Ys[name].cpu().numpy()[:, rows]), bits(Y_ref)), name
+    for lname, members in launches:
+        for n in members:
+            Y_ref = oracle_linear(orc, Xs[lname], *refs[n])[0]
+            assert np.array_equal(bits(Ys[n].cpu().numpy()), bits(Y_ref)), n
     assert w4.w4a8_device_error() == 0
+
+
+def test_decode_step_as_benchmarked(w4, orc):
+    """One step exactly as bench.py runs it (grouped q/k/v and gate/up, PDL),
+    every output of every linear checked against the oracle."""
+    import bench
+    assert [l[0] for l in bench.LINEARS] == NAMES and bench.LAUNCHES == LAUNCHES
+    run_step(w4, orc, lambda i: WEIGHT_SEED0 + i, lambda i: WEIGHT_SEED0 + i + ACT_SEED_OFFSET, LAUNCHES)
+
+
+@pytest.mark.parametrize("layer", [0, 13, 27])
+def test_decode_28_layers_own_inputs(w4, orc, layer):
+    """Layers of the 28-layer decode step at their own seeds (weights
+    1000 * (layer + 1) + index, activations that + 500, as the benchmark
+    draws them): q/k/v, o, gate/up and down launched as the benchmark does,
+    every output element against the oracle."""
+    import bench
+    assert bench.DECODE_LAYERS == 28
+    base = 1000 * (layer + 1)
+    run_step(w4, orc, lambda i: base + i, lambda i: base + i + ACT_SEED_OFFSET, LAUNCHES[:-1])
 
 
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
 @pytest.mark.parametrize("name", ["gate", "down"])
 def test_skinny_batch_sweep(w4, orc, M, name):
-    idx = [s[0] for s in QWEN2_7B_SET].index(name)
+    idx = NAMES.index(name)
     _, K, N = QWEN2_7B_SET[idx]
     run_w4(w4, orc, K, N, M, WEIGHT_SEED0 + idx, flags=w4.LAUNCH_PDL)
 
 
 @pytest.mark.parametrize("M", [3, 8, 16])
 def test_lm_head_small_batches(w4, orc, M):
-    """lm_head at batch sizes that take the row-per-thread kernel (3, 8: a
-    1188-tile grid in several waves) and the tensor cores (16)."""
-    idx = [s[0] for s in QWEN2_7B_SET].index("lm_head")
+    """lm_head at small batch sizes: the row-per-thread kernel at 3 rows,
+    the warp-level MMA kernel at 8 (a 1188-tile grid in several waves), the
+    tensor cores at 16."""
+    idx = NAMES.index("lm_head")
     _, K, N = QWEN2_7B_SET[idx]
-    assert w4.w4a8_plan_info(M, K, N)["kernel"] == (2 if M <= 8 else 1)
+    assert w4.w4a8_plan_info(M, K, N)["kernel"] == {3: 2, 8: 3, 16: 1}[M]
     run_w4(w4, orc, K, N, M, WEIGHT_SEED0 + idx, flags=w4.LAUNCH_PDL)
 
 
@@ -150,19 +230,25 @@ def test_batch_above_limit_rejected(w4):
 def test_chatglm2_w8a16(w4, orc, idx):
     name, K, N = CHATGLM2_W8A16[idx]
     seed = 2000 + idx
-    W = synth.normal_gpu(seed, (N, K), 0.02)
-    Wq8, sw16 = w4.w8_quantize_weights(W)
-    del W
+    W = synth.normal_host(seed, (N, K), 0.02)
+    Wq8, sw16 = w4.w8_quantize_weights(torch.from_numpy(W).cuda())
     X = synth.activation(seed + ACT_SEED_OFFSET, 1, K)
     Y = w4.w8a16_gemv(torch.from_numpy(X).cuda(), Wq8, sw16, flags=w4.LAUNCH_PDL)
     torch.cuda.synchronize()
-    rows = sample_rows(N, seed)
-    Wq_ref, sw_ref = orc.w8_quantize(synth.weight_rows(seed, N, K, rows))
-    rdev = torch.from_numpy(rows).cuda()
-    assert np.array_equal(Wq8[rdev].cpu().numpy(), Wq_ref)
-    assert np.array_equal(sw16[rdev].cpu().numpy().view(np.uint16), sw_ref.view(np.uint16))
-    Y_ref = orc.w8a16_ref(X, Wq_ref, sw_ref)
-    got = Y.cpu().numpy()[:, rows].astype(np.float64)
+    Wq_ref = np.empty((N, K), np.int8)
+    sw_ref = np.empty(N, np.uint16)
+    Y_ref = np.empty((1, N), np.float64)
+
+    def one(c):
+        q, s = orc.w8_quantize(W[c[0]:c[1]])
+        Wq_ref[c[0]:c[1]], sw_ref[c[0]:c[1]] = q, s.view(np.uint16)
+        Y_ref[:, c[0]:c[1]] = orc.w8a16_ref(X, q, s)
+
+    with cf.ThreadPoolExecutor(THREADS) as ex:
+        list(ex.map(one, chunks(N, 4 * THREADS)))
+    assert np.array_equal(Wq8.cpu().numpy(), Wq_ref)
+    assert np.array_equal(sw16.cpu().numpy().view(np.uint16), sw_ref)
+    got = Y.cpu().numpy().astype(np.float64)
     err = np.abs(got - Y_ref)
     assert np.sqrt((err ** 2).sum() / (Y_ref ** 2).sum()) <= 5e-4
     assert np.all(err <= 1e-3 * (np.abs(Y_ref) + 1))

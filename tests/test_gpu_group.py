@@ -13,6 +13,7 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+import guards  # noqa: E402
 import oracle  # noqa: E402
 import synth  # noqa: E402
 
@@ -81,14 +82,17 @@ def check_group(w4, orc, M, K, N, gs, seed, fused=True, flags=0):
     Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
     assert np.array_equal(Wq.cpu().numpy(), Wq_ref)
     assert np.array_equal(bits(sg.cpu().numpy()), bits(sg_ref))
+    gY = guards.out((M, N), torch.float32)
+    gXq, gsa = guards.out((M, K), torch.int8), guards.out((M,), torch.float32)
+    gws = guards.workspace(w4.w4a8g_workspace_bytes(M, K, N, gs))
+    Xq, sa = gXq.t, gsa.t
     if fused:
-        Xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
-        sa = torch.empty((M,), dtype=torch.float32, device="cuda")
-        Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs, Xq_out=Xq, sa_out=sa, flags=flags)
+        Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs, Y=gY.t, Xq_out=Xq, sa_out=sa,
+                            ws=guards.t(gws), flags=flags)
     else:
-        Xq, sa = w4.act_quantize_i8(to_dev(X))
-        Y = w4.w4a8g_gemv(Xq, sa, Wq, sg, gs, flags=flags)
-    torch.cuda.synchronize()
+        w4.act_quantize_i8(to_dev(X), Xq=Xq, sa=sa)
+        Y = w4.w4a8g_gemv(Xq, sa, Wq, sg, gs, Y=gY.t, ws=guards.t(gws), flags=flags)
+    guards.check_all(gY, gXq, gsa, gws)
     assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
     assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
     Yh = Y.cpu().numpy()

@@ -13,6 +13,7 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+import guards  # noqa: E402
 import oracle  # noqa: E402
 import synth  # noqa: E402
 
@@ -46,8 +47,9 @@ def logits(seed, rows, cols, std_real=4.0, d=128):
 def check(w4, orc, A, c_int, b=5, lut=None):
     P_ref = orc.index_softmax(A, c_int, b, lut)
     Ad = torch.from_numpy(np.ascontiguousarray(A)).cuda()
-    P = w4.index_softmax_u8(Ad, c_int, b, None if lut is None else bytes(lut))
-    torch.cuda.synchronize()
+    gP = guards.out(A.shape, torch.uint8)
+    P = w4.index_softmax_u8(Ad, c_int, b, None if lut is None else bytes(lut), P=gP.t)
+    guards.check_all(gP)
     got = P.cpu().numpy()
     bad = np.argwhere(got != P_ref)
     assert bad.size == 0, (bad[:5], got[tuple(bad[0])], P_ref[tuple(bad[0])])

@@ -11,6 +11,7 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+import guards  # noqa: E402
 import oracle  # noqa: E402
 import synth  # noqa: E402
 
@@ -69,15 +70,20 @@ def check_w4a8(w4, orc, M, K, N, seed, fused=True, outliers=0.001, flags=0, zero
     Wq, sw = w4.w4_quantize_weights(to_dev(W))
     assert np.array_equal(Wq.cpu().numpy(), Wq_ref)
     assert np.array_equal(bits(sw.cpu().numpy()), bits(sw_ref))
-    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    # every output and the workspace sit between guard bytes
+    gacc, gY = guards.out((M, N), torch.int32), guards.out((M, N), torch.float32)
+    gws = guards.workspace(w4.w4a8_workspace_bytes(M, K, N))
     if fused:
-        Xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
-        sa = torch.empty((M,), dtype=torch.float32, device="cuda")
-        Y = w4.w4a8_linear(to_dev(X), Wq, sw, Xq_out=Xq, sa_out=sa, acc_out=acc, flags=flags)
+        gXq, gsa = guards.out((M, K), torch.int8), guards.out((M,), torch.float32)
+        Xq, sa = gXq.t, gsa.t
+        Y = w4.w4a8_linear(to_dev(X), Wq, sw, Y=gY.t, Xq_out=Xq, sa_out=sa, acc_out=gacc.t,
+                           ws=guards.t(gws), flags=flags)
     else:
-        Xq, sa = w4.act_quantize_i8(to_dev(X))
-        Y = w4.w4a8_gemv(Xq, sa, Wq, sw, acc_out=acc, flags=flags)
-    torch.cuda.synchronize()
+        gXq, gsa = guards.out((M, K), torch.int8), guards.out((M,), torch.float32)
+        Xq, sa = w4.act_quantize_i8(to_dev(X), Xq=gXq.t, sa=gsa.t)
+        Y = w4.w4a8_gemv(Xq, sa, Wq, sw, Y=gY.t, acc_out=gacc.t, ws=guards.t(gws), flags=flags)
+    guards.check_all(gacc, gY, gws, gXq, gsa)
+    acc = gacc.t
     assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
     assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
     assert np.array_equal(acc.cpu().numpy(), acc_ref)
@@ -168,7 +174,7 @@ W4A8_SHAPES = [
 @pytest.mark.parametrize("M,K,N,seed", W4A8_SHAPES)
 def test_w4a8_linear_fused(w4, orc, M, K, N, seed, path):
     if path == "dp4a":
-        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)  # batches of 3+ rows would take the tensor cores
+        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)  # batches of 3+ rows would take the tensor cores
     check_w4a8(w4, orc, M, K, N, seed, fused=True, zero_rows=(1,))
 
 
@@ -176,7 +182,7 @@ def test_w4a8_linear_fused(w4, orc, M, K, N, seed, path):
 @pytest.mark.parametrize("M,K,N,seed", W4A8_SHAPES[:8] + W4A8_SHAPES[-3:-1])
 def test_w4a8_gemv_unfused(w4, orc, M, K, N, seed, path):
     if path == "dp4a":
-        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
+        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)
     check_w4a8(w4, orc, M, K, N, seed, fused=False)
 
 
@@ -193,7 +199,7 @@ def test_w4a8_one_row_plans_fused_and_unfused(w4, orc, M, K, N, seed, fused):
 @pytest.mark.parametrize("splits", [2, 3, 5, 16])
 @pytest.mark.parametrize("fused", [True, False])
 def test_w4a8_split_k(w4, orc, splits, fused):
-    w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65, rowdot_max_m=1)  # the dp4a kernel's split plans
+    w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)  # the dp4a kernel's split plans
     for (M, K, N, seed) in [(1, 3584, 700, 30), (3, 18944, 150, 31), (8, 1024, 64, 32)]:
         if (K // 32) < splits:
             continue
@@ -247,14 +253,14 @@ def test_w4a8_fused_ties(w4, orc, M, K, N, splits):
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("ops", [1, 2], ids=["bf16", "e4m3"])
 def test_w4a8_tensor_cores(w4, orc, M, K, N, seed, fused, ops):
-    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, mma_e4m3=ops)
+    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, mma_e4m3=ops, qmma_max_m=1)
     assert w4.w4a8_plan_info(M, K, N)["kernel"] == 1
     check_w4a8(w4, orc, M, K, N, seed, fused=fused, zero_rows=(0,))
 
 
 @pytest.mark.parametrize("ops", [1, 2], ids=["bf16", "e4m3"])
 def test_w4a8_tensor_cores_grouped(w4, orc, ops):
-    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, mma_e4m3=ops)
+    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, mma_e4m3=ops, qmma_max_m=1)
     M, K, Ns = 18, 1024, (300, 7, 129)
     X = synth.activation(110, M, K, outlier_frac=0.001)
     Wqs, sws, refs = [], [], []
@@ -279,7 +285,7 @@ def test_w4a8_tensor_cores_largest_sums(w4, K, ops):
     codes +127 and -127: each K piece's partial sum reaches 8 * 127 * 16384 =
     16,646,144, just below 2^24, which the fp32 accumulator must hold
     exactly; the pieces are added as int32."""
-    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, mma_e4m3=ops)
+    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, mma_e4m3=ops, qmma_max_m=1)
     M, N = 16, 130
     Wq = torch.full((N, K // 2), 0x88, dtype=torch.uint8, device="cuda")
     sw = torch.ones((N,), dtype=torch.float32, device="cuda")
@@ -300,10 +306,10 @@ def test_w4a8_tensor_cores_match_dp4a(w4, orc):
     W = weights(N, K, 120)
     X = to_dev(synth.activation(121, M, K, outlier_frac=0.001))
     Wq, sw = w4.w4_quantize_weights(to_dev(W))
-    w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
+    w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)
     assert w4.w4a8_plan_info(M, K, N)["kernel"] == 0
     Y0 = w4.w4a8_linear(X, Wq, sw)
-    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1)
+    w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, qmma_max_m=1)
     Y1 = w4.w4a8_linear(X, Wq, sw)
     torch.cuda.synchronize()
     assert np.array_equal(bits(Y0.cpu().numpy()), bits(Y1.cpu().numpy()))
@@ -311,7 +317,7 @@ def test_w4a8_tensor_cores_match_dp4a(w4, orc):
 
 @pytest.mark.parametrize("cl", [1, 2, 8, 32, 64, 128, 256])
 def test_w4a8_threads_per_row(w4, orc, cl):
-    w4.w4a8_set_tuning(force_threads_per_row=cl, rowdot_max_m=1)  # the dp4a kernel's plans
+    w4.w4a8_set_tuning(force_threads_per_row=cl, rowdot_max_m=1, qmma_max_m=1)  # the dp4a kernel's plans
     for (M, K, N, seed) in [(1, 3584, 300, 40), (2, 2048, 99, 41), (1, 256, 513, 42)]:
         try:
             plan = w4.w4a8_plan_info(M, K, N)
@@ -326,7 +332,7 @@ def test_w4a8_two_stage_ring(w4, orc):
     w4.w4a8_set_tuning(ring_bytes=8192)
     assert w4.w4a8_plan_info(1, 3584, 5000)["stages"] == 2
     check_w4a8(w4, orc, 1, 3584, 5000, 50)
-    w4.w4a8_set_tuning(ring_bytes=8192, force_splits=3, rowdot_max_m=1)
+    w4.w4a8_set_tuning(ring_bytes=8192, force_splits=3, rowdot_max_m=1, qmma_max_m=1)
     check_w4a8(w4, orc, 2, 18944, 300, 51)
 
 
@@ -392,7 +398,11 @@ def check_w8a16(w4, orc, M, K, N, seed):
     Y_ref = orc.w8a16_ref(X, Wq_ref, sw_ref)
     Wq8, sw16 = w4.w8_quantize_weights(to_dev(W))
     assert np.array_equal(Wq8.cpu().numpy(), Wq_ref)
-    Y = w4.w8a16_gemv(to_dev(X), Wq8, sw16).cpu().numpy().astype(np.float64)
+    gY = guards.out((M, N), torch.float32)
+    gws = guards.workspace(w4.w8a16_workspace_bytes(M, K, N))
+    w4.w8a16_gemv(to_dev(X), Wq8, sw16, Y=gY.t, ws=guards.t(gws))
+    guards.check_all(gY, gws)
+    Y = gY.t.cpu().numpy().astype(np.float64)
     err = np.abs(Y - Y_ref)
     assert np.sqrt((err ** 2).sum() / max((Y_ref ** 2).sum(), 1e-300)) <= W8_REL_L2
     assert np.all(err <= W8_ELEM * (np.abs(Y_ref) + 1))
@@ -444,7 +454,7 @@ def test_gpu_generator_matches_host(w4):
 ])
 def test_w4a8_linear_grouped(w4, orc, M, K, Ns, splits):
     w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65 if splits else 0,
-                      rowdot_max_m=1 if splits else 0)
+                      rowdot_max_m=1 if splits else 0, qmma_max_m=1)
     X = synth.activation(500 + K, M, K, outlier_frac=0.001)
     refs, Wqs, sws = [], [], []
     for g, N in enumerate(Ns):

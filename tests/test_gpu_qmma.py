@@ -1,0 +1,223 @@
+"""The warp-level e4m3 MMA kernel (2..32 batch rows) against the CPU oracle,
+element by element, through the C ABI.
+
+The kernel encodes INT4 weight codes as e4m3 bytes v = q + 8 (exactly
+v * 2^-9) and INT8 activation codes as two exact e4m3 integers
+(a = 16 a_hi + a_lo); the fp32 sums of the MMAs are exact, so the int32
+accumulators, Xq, s_a and Y must equal the oracle's bit for bit.  Shapes
+span one and several 128-row tiles, ragged row and K tails (a partial last
+256-code box), split K, every n-tile count (1..8) and the largest sums.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import guards  # noqa: E402
+import oracle  # noqa: E402
+import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+QMMA = 3  # w4a8_plan_info "kernel" of the warp-level MMA kernel
+
+
+@pytest.fixture(scope="module")
+def w4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bit_weight_quantized_w4a8_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+@pytest.fixture(autouse=True)
+def _reset_tuning(w4):
+    w4.w4a8_set_tuning(qmma_max_m=32)  # by default the kernel serves 4..8 rows
+    yield
+    w4.w4a8_set_tuning(reset=True)
+    assert w4.w4a8_device_error() == 0
+
+
+def bits(a):
+    return np.ascontiguousarray(a).view(np.uint32)
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def check(w4, orc, M, K, N, seed, fused=True, flags=0):
+    plan = w4.w4a8_plan_info(M, K, N)
+    assert plan["kernel"] == QMMA, plan
+    W = synth.normal(seed, (N, K), 0.02)
+    W[0] = 0  # a zero weight row: scale 0, outputs 0
+    X = synth.activation(seed + 7, M, K, outlier_frac=0.001)
+    X[M - 1] = 0  # a zero activation row
+    Wq_ref, sw_ref = orc.w4_quantize(W)
+    Y_ref, Xq_ref, sa_ref, acc_ref = orc.w4a8_linear(X, Wq_ref, sw_ref)
+    Wq, sw = w4.w4_quantize_weights(to_dev(W))
+    gacc, gY = guards.out((M, N), torch.int32), guards.out((M, N), torch.float32)
+    gXq, gsa = guards.out((M, K), torch.int8), guards.out((M,), torch.float32)
+    gws = guards.workspace(w4.w4a8_workspace_bytes(M, K, N))
+    Xq, sa, acc = gXq.t, gsa.t, gacc.t
+    if fused:
+        Y = w4.w4a8_linear(to_dev(X), Wq, sw, Y=gY.t, Xq_out=Xq, sa_out=sa, acc_out=acc,
+                           ws=guards.t(gws), flags=flags)
+    else:
+        w4.act_quantize_i8(to_dev(X), Xq=Xq, sa=sa)
+        Y = w4.w4a8_gemv(Xq, sa, Wq, sw, Y=gY.t, acc_out=acc, ws=guards.t(gws), flags=flags)
+    guards.check_all(gacc, gY, gXq, gsa, gws)
+    assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
+    assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
+    assert np.array_equal(acc.cpu().numpy(), acc_ref)
+    assert np.array_equal(bits(Y.cpu().numpy()), bits(Y_ref))
+    return plan
+
+
+QMMA_SHAPES = [
+    (2, 3584, 1000, 0),      # split K (8 tiles), one n-tile
+    (3, 896, 129, 1),        # one row past a tile
+    (4, 18944, 300, 2),      # long rows, many pieces
+    (5, 96, 77, 3),          # one partial box, two n-tiles
+    (8, 3584, 256, 4),       # exactly two tiles
+    (9, 1024, 1500, 5),      # three n-tiles
+    (12, 2048, 640, 6),
+    (16, 18944, 200, 7),     # four tiles per warp, split K
+    (17, 3584, 129, 8),      # five n-tiles
+    (24, 512, 4000, 9),
+    (31, 288, 7, 10),        # a partial last box, seven rows
+    (32, 3584, 1100, 11),    # eight n-tiles
+]
+
+
+@pytest.mark.parametrize("M,K,N,seed", QMMA_SHAPES)
+@pytest.mark.parametrize("fused", [True, False])
+def test_qmma_parity(w4, orc, M, K, N, seed, fused):
+    check(w4, orc, M, K, N, 900 + seed, fused=fused)
+
+
+@pytest.mark.parametrize("M", [2, 6, 32])
+def test_qmma_longest_rows(w4, orc, M):
+    """K = 131072: every warp sums 65536 codes (the exactness limit of its
+    fp32 sums), the pieces meet in int32."""
+    p = check(w4, orc, M, 131072, 5, 950 + M)
+    assert p["splits"] >= 2
+
+
+@pytest.mark.parametrize("M", [4, 32])
+@pytest.mark.parametrize("K", [4096, 131072])
+def test_qmma_largest_sums(w4, M, K):
+    """Weight codes 7 and -8 (nibble 0x8, legal on input) against activation
+    codes +127 and -127: the largest products of both encodings (v = 15 and
+    v = 0) and the bias correction 8 * sum(a) at its extremes."""
+    N = 256
+    Wq = torch.full((N, K // 2), 0x77, dtype=torch.uint8, device="cuda")
+    Wq[1::2] = 0x88                            # odd rows: every code -8
+    sw = torch.ones((N,), dtype=torch.float32, device="cuda")
+    Xq = torch.full((M, K), 127, dtype=torch.int8, device="cuda")
+    Xq[1::2] = -127
+    sa = torch.ones((M,), dtype=torch.float32, device="cuda")
+    assert w4.w4a8_plan_info(M, K, N)["kernel"] == QMMA
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    Y = w4.w4a8_gemv(Xq, sa, Wq, sw, acc_out=acc)
+    torch.cuda.synchronize()
+    a = np.where(np.arange(M) % 2 == 0, 127, -127).astype(np.int64)[:, None]
+    q = np.where(np.arange(N) % 2 == 0, 7, -8).astype(np.int64)[None, :]
+    want = a * q * K
+    assert np.array_equal(acc.cpu().numpy(), want)
+    assert np.array_equal(Y.cpu().numpy(), want.astype(np.float32))
+
+
+def test_qmma_grouped(w4, orc):
+    M, K, Ns = 10, 1024, (300, 7, 129)
+    X = synth.activation(960, M, K, outlier_frac=0.001)
+    Wqs, sws, refs = [], [], []
+    for g, N in enumerate(Ns):
+        W = synth.normal(961 + g, (N, K), 0.02)
+        Wq_ref, sw_ref = orc.w4_quantize(W)
+        refs.append(orc.w4a8_linear(X, Wq_ref, sw_ref)[0])
+        Wq, sw = w4.w4_quantize_weights(to_dev(W))
+        Wqs.append(Wq)
+        sws.append(sw)
+    assert w4.w4a8_plan_info(M, K, sum(Ns))["kernel"] == QMMA
+    for rep in range(2):
+        gYs = [guards.out((M, N), torch.float32) for N in Ns]
+        gws = guards.workspace(w4.w4a8_workspace_bytes(M, K, sum(Ns)))
+        Ys = w4.w4a8_linear_grouped(to_dev(X), Wqs, sws, Ys=[g.t for g in gYs], ws=guards.t(gws),
+                                    flags=w4.LAUNCH_PDL if rep else 0)
+        guards.check_all(gws, *gYs)
+        for Y, ref in zip(Ys, refs):
+            assert np.array_equal(bits(Y.cpu().numpy()), bits(ref))
+
+
+def test_qmma_matches_other_kernels(w4):
+    """The same call on the warp-level MMA kernel, the row-per-thread kernel,
+    the tensor cores and the dp4a GEMV gives the same bits."""
+    M, K, N = 6, 3584, 1000
+    W = synth.normal(970, (N, K), 0.02)
+    X = to_dev(synth.activation(971, M, K, outlier_frac=0.001))
+    Wq, sw = w4.w4_quantize_weights(to_dev(W))
+    outs = []
+    for kw, kind in ((dict(qmma_max_m=8), QMMA), (dict(qmma_max_m=1), 2), (dict(qmma_max_m=1, rowdot_max_m=1), 1),
+                     (dict(qmma_max_m=1, rowdot_max_m=1, mma_min_m=65), 0)):
+        w4.w4a8_set_tuning(**kw)
+        assert w4.w4a8_plan_info(M, K, N)["kernel"] == kind
+        outs.append(w4.w4a8_linear(X, Wq, sw).cpu().numpy())
+    for o in outs[1:]:
+        assert np.array_equal(bits(outs[0]), bits(o))
+
+
+def test_qmma_pdl_chain_and_graph(w4, orc):
+    """Programmatically dependent launches back to back on one workspace,
+    then the same chain replayed from a CUDA graph: identical bits."""
+    M, K, N = 8, 3584, 700
+    W = synth.normal(980, (N, K), 0.02)
+    Wq_ref, sw_ref = orc.w4_quantize(W)
+    Wq, sw = w4.w4_quantize_weights(to_dev(W))
+    Xs = [synth.activation(981 + i, M, K, outlier_frac=0.001) for i in range(3)]
+    refs = [orc.w4a8_linear(X, Wq_ref, sw_ref)[0] for X in Xs]
+    Xd = [to_dev(X) for X in Xs]
+    Ys = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in Xs]
+    ws = torch.zeros(w4.w4a8_workspace_bytes(M, K, N), dtype=torch.uint8, device="cuda")
+
+    def chain():
+        for X, Y in zip(Xd, Ys):
+            w4.w4a8_linear(X, Wq, sw, Y=Y, ws=ws, flags=w4.LAUNCH_PDL)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.synchronize()
+    for Y, ref in zip(Ys, refs):
+        assert np.array_equal(bits(Y.cpu().numpy()), bits(ref))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        chain()
+    for Y in Ys:
+        Y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for Y, ref in zip(Ys, refs):
+        assert np.array_equal(bits(Y.cpu().numpy()), bits(ref))
+
+
+@pytest.mark.parametrize("R", [1, 2, 4])
+@pytest.mark.parametrize("M,K,N,seed", [(3, 3584, 300, 20), (8, 18944, 129, 21), (16, 1024, 777, 22),
+                                        (25, 2304, 260, 23)])
+def test_qmma_tiles_per_warp(w4, orc, R, M, K, N, seed):
+    """Every tiles-per-warp choice (boxes interleaved over R warp groups)
+    gives the oracle's bits; 4 tiles a warp exist up to 16 rows (past that
+    the call takes the next kernel)."""
+    w4.w4a8_set_tuning(qmma_tiles_per_warp=R, qmma_max_m=32)
+    if R == 4 and M > 16:  # no such kernel: the call goes to the tensor cores
+        assert w4.w4a8_plan_info(M, K, N)["kernel"] == 1
+        return
+    assert w4.w4a8_plan_info(M, K, N)["threads_per_row"] == R
+    check(w4, orc, M, K, N, 990 + seed)

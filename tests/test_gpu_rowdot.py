@@ -11,6 +11,7 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+import guards  # noqa: E402
 import oracle  # noqa: E402
 import synth  # noqa: E402
 
@@ -34,7 +35,7 @@ def orc():
 
 @pytest.fixture(autouse=True)
 def _reset_tuning(w4):
-    w4.w4a8_set_tuning(reset=True)
+    w4.w4a8_set_tuning(qmma_max_m=1)  # 2..32 rows would take the warp-level MMA kernel
     yield
     w4.w4a8_set_tuning(reset=True)
     assert w4.w4a8_device_error() == 0
@@ -58,15 +59,17 @@ def check(w4, orc, M, K, N, seed, fused=True, flags=0):
     Wq_ref, sw_ref = orc.w4_quantize(W)
     Y_ref, Xq_ref, sa_ref, acc_ref = orc.w4a8_linear(X, Wq_ref, sw_ref)
     Wq, sw = w4.w4_quantize_weights(to_dev(W))
-    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    gacc, gY = guards.out((M, N), torch.int32), guards.out((M, N), torch.float32)
+    gXq, gsa = guards.out((M, K), torch.int8), guards.out((M,), torch.float32)
+    gws = guards.workspace(w4.w4a8_workspace_bytes(M, K, N))
+    Xq, sa, acc = gXq.t, gsa.t, gacc.t
     if fused:
-        Xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
-        sa = torch.empty((M,), dtype=torch.float32, device="cuda")
-        Y = w4.w4a8_linear(to_dev(X), Wq, sw, Xq_out=Xq, sa_out=sa, acc_out=acc, flags=flags)
+        Y = w4.w4a8_linear(to_dev(X), Wq, sw, Y=gY.t, Xq_out=Xq, sa_out=sa, acc_out=acc,
+                           ws=guards.t(gws), flags=flags)
     else:
-        Xq, sa = w4.act_quantize_i8(to_dev(X))
-        Y = w4.w4a8_gemv(Xq, sa, Wq, sw, acc_out=acc, flags=flags)
-    torch.cuda.synchronize()
+        w4.act_quantize_i8(to_dev(X), Xq=Xq, sa=sa)
+        Y = w4.w4a8_gemv(Xq, sa, Wq, sw, Y=gY.t, acc_out=acc, ws=guards.t(gws), flags=flags)
+    guards.check_all(gacc, gY, gXq, gsa, gws)
     assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
     assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
     assert np.array_equal(acc.cpu().numpy(), acc_ref)
@@ -92,7 +95,7 @@ ROWDOT_SHAPES = [
 @pytest.mark.parametrize("M,K,N,seed", ROWDOT_SHAPES)
 def test_rowdot_parity(w4, orc, M, K, N, seed, fused, tpr):
     if tpr:
-        w4.w4a8_set_tuning(force_threads_per_row=tpr)
+        w4.w4a8_set_tuning(force_threads_per_row=tpr, qmma_max_m=1)
     plan = check(w4, orc, M, K, N, seed, fused=fused)
     assert plan["threads_per_row"] == (tpr or 4)
 
@@ -208,7 +211,7 @@ def test_rowdot_matches_other_kernels(w4):
     Wq, sw = w4.w4_quantize_weights(to_dev(W))
     outs = []
     for kw in (dict(), dict(rowdot_max_m=1), dict(rowdot_max_m=1, mma_min_m=65)):
-        w4.w4a8_set_tuning(**kw)
+        w4.w4a8_set_tuning(qmma_max_m=1, **kw)
         outs.append(w4.w4a8_linear(X, Wq, sw).cpu().numpy())
     assert np.array_equal(bits(outs[0]), bits(outs[1]))
     assert np.array_equal(bits(outs[0]), bits(outs[2]))
@@ -231,14 +234,17 @@ def check_group(w4, orc, M, K, N, gs, seed, fused=True, flags=0):
     Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
     Y_ref, B, Xq_ref, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
     Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
+    gY = guards.out((M, N), torch.float32)
+    gXq, gsa = guards.out((M, K), torch.int8), guards.out((M,), torch.float32)
+    gws = guards.workspace(w4.w4a8g_workspace_bytes(M, K, N, gs))
+    Xq, sa = gXq.t, gsa.t
     if fused:
-        Xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
-        sa = torch.empty((M,), dtype=torch.float32, device="cuda")
-        Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs, Xq_out=Xq, sa_out=sa, flags=flags)
+        Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs, Y=gY.t, Xq_out=Xq, sa_out=sa,
+                            ws=guards.t(gws), flags=flags)
     else:
-        Xq, sa = w4.act_quantize_i8(to_dev(X))
-        Y = w4.w4a8g_gemv(Xq, sa, Wq, sg, gs, flags=flags)
-    torch.cuda.synchronize()
+        w4.act_quantize_i8(to_dev(X), Xq=Xq, sa=sa)
+        Y = w4.w4a8g_gemv(Xq, sa, Wq, sg, gs, Y=gY.t, ws=guards.t(gws), flags=flags)
+    guards.check_all(gY, gXq, gsa, gws)
     assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
     assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
     Yh = Y.cpu().numpy().astype(np.float64)

@@ -53,7 +53,9 @@ def call_noalloc(w4, X, Wq, sw, Y):
 @pytest.mark.parametrize("M,K,N,splits", [(1, 3584, 3000, 4), (3, 18944, 500, 3), (1, 896, 512, 0),
                                           (8, 1024, 700, 16)])
 def test_noalloc_matches_workspace_path_twice(w4, M, K, N, splits):
-    w4.w4a8_set_tuning(force_splits=splits)
+    # the reference call takes the same dp4a plan the entry point launches,
+    # so `need` is that plan's scratch and the comparison is plan for plan
+    w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)
     try:
         need = w4.w4a8_workspace_bytes(M, K, N)
         assert need <= SCRATCH_BYTES
@@ -75,7 +77,7 @@ def test_noalloc_matches_workspace_path_twice(w4, M, K, N, splits):
 
 def test_noalloc_rejects_plans_beyond_the_static_scratch(w4):
     M, K, N = 8, 4096, 10000
-    w4.w4a8_set_tuning(force_splits=16, mma_min_m=65, rowdot_max_m=1)  # the dp4a plan the entry point uses
+    w4.w4a8_set_tuning(force_splits=16, mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)  # the dp4a plan the entry point uses
     try:
         assert w4.w4a8_workspace_bytes(M, K, N) > SCRATCH_BYTES
         X = torch.zeros((M, K), dtype=torch.float16, device="cuda")
