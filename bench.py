@@ -89,8 +89,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sample-stride", type=int, default=CPU_SAMPLE_STRIDE,
-                    help="the oracle's sample: every n-th output row of each linear")
+    ap.add_argument("--sample-stride", type=int, default=0,
+                    help="the oracle's sample: every n-th output row of each linear (default: "
+                         "%d for our arm's cpu_baseline, 1 = the whole set for --impl reference)"
+                         % CPU_SAMPLE_STRIDE)
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the 28-layer step, the skinny-batch sweep and the W8A16 set")
     ap.add_argument("--min-busy-s", type=float, default=0.6,
@@ -245,21 +247,30 @@ def profiled_traffic():
 
 def cpu_sample_inputs(dev, stride=CPU_SAMPLE_STRIDE):
     """Every stride-th output row of each linear, quantized by the oracle on
-    the host (weights drawn by the generator's GPU twin, or on the host when
-    dev is None: the same bits)."""
+    the host.  Weights are drawn on the host by the C twin of the generator
+    (the same bits as the numpy definition and the GPU twin), so no GPU is
+    involved; the oracle quantizes row chunks on host threads (set-up, not
+    timed)."""
+    import concurrent.futures as cf
     import oracle
     import synth
     orc = oracle.load()
     out = []
+    threads = os.cpu_count() or 4
     for idx, (name, K, N) in enumerate(LINEARS):
         seed = WEIGHT_SEED0 + idx
-        if dev is None:
-            W_rows = synth.weight_rows(seed, N, K, range(0, N, stride))
-        else:
-            W = synth.normal_gpu(seed, (N, K), 0.02, device=dev)
-            W_rows = W[::stride].cpu().numpy()
-            del W
-        Wq, sw = orc.w4_quantize(W_rows)
+        W_rows = np.ascontiguousarray(synth.normal_host(seed, (N, K), 0.02)[::stride])
+        n = W_rows.shape[0]
+        Wq = np.empty((n, K // 2), np.uint8)
+        sw = np.empty(n, np.float32)
+        step = -(-n // (4 * threads))
+
+        def quant(r0):
+            Wq[r0:r0 + step], sw[r0:r0 + step] = orc.w4_quantize(W_rows[r0:r0 + step])
+
+        with cf.ThreadPoolExecutor(threads) as ex:
+            list(ex.map(quant, range(0, n, step)))
+        del W_rows
         X = synth.activation(activation_seed(name), 1, K, outlier_frac=OUTLIER_FRAC)
         out.append((X, Wq, sw, N))
     return orc, out
@@ -309,13 +320,12 @@ def time_oracle_sample_threads(orc, inputs, threads, min_s=2.0, max_reps=50):
 # ---------------------------------------------------------------------------
 
 def run_reference(args, world, rank):
-    import torch
     if rank != 0:
         return
-    dev = torch.device("cuda") if torch.cuda.is_available() else None
-    orc, inputs = cpu_sample_inputs(dev, args.sample_stride)
-    sample = "every %dth output row of each linear (%.2f%% of the set's weights)" % (
-        args.sample_stride, 100.0 / args.sample_stride)
+    stride = args.sample_stride or 1
+    orc, inputs = cpu_sample_inputs(None, stride)
+    sample = ("the whole set (every output row of each linear)" if stride == 1 else
+              "every %dth output row of each linear (%.2f%% of the set's weights)" % (stride, 100.0 / stride))
     for _ in range(args.warmup):
         for (X, Wq, sw, _) in inputs:
             orc.w4a8_linear(X, Wq, sw)
@@ -325,7 +335,8 @@ def run_reference(args, world, rank):
     for _ in range(args.steps):
         for (X, Wq, sw, _) in inputs:
             orc.w4a8_linear(X, Wq, sw)
-    dt = (time.perf_counter() - t0) / args.steps * rows_total / rows_sampled
+    measured = (time.perf_counter() - t0) / args.steps
+    dt = measured * rows_total / rows_sampled
     value = SET_BYTES / dt / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
@@ -334,7 +345,9 @@ def run_reference(args, world, rank):
         "vs_baseline": None, "dtype": "int4xint8->int32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "set_weight_bytes": SET_BYTES},
         "cpu_baseline": {"kind": "oracle", "value": round(value, 4), "unit": "GB/s", "cores": 1,
-                         "sample": sample + "; per step, scaled to the full set"},
+                         "sample": sample + ("; timed per step" if stride == 1 else
+                                             "; per step, scaled to the full set"),
+                         "measured_s_per_step": round(measured, 4)},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -514,6 +527,7 @@ def run_ours(args, world, rank):
     extra = {}
     if not args.no_extra:
         extra["skinny_batch"] = measure_skinny(torch, w4, synth, dev, stream, copies, lin)
+        extra["mlp_m1"] = measure_mlp(torch, w4, synth, dev, stream, lin)
         extra["w8a16_set"] = measure_w8a16(torch, w4, synth, dev, stream)
         extra["group_scale_set"] = measure_group_set(torch, w4, synth, dev, stream, lin)
         extra["index_softmax"] = measure_index_softmax(torch, w4, synth, dev, stream, peak)
@@ -563,13 +577,14 @@ def run_ours(args, world, rank):
     }
     line.update(extra)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        orc, inputs = cpu_sample_inputs(dev, args.sample_stride)
+        stride = args.sample_stride or CPU_SAMPLE_STRIDE
+        orc, inputs = cpu_sample_inputs(dev, stride)
         t_set, reps = time_oracle_sample(orc, inputs)
         line["cpu_baseline"] = {
             "value": round(SET_BYTES / t_set / 1e9, 4), "unit": "GB/s", "cores": 1,
             "kind": "oracle", "us_per_set": round(t_set * 1e6, 1),
             "sample": "every %dth output row of each linear, %d repetitions, scaled to the full set"
-                      % (args.sample_stride, reps)}
+                      % (stride, reps)}
         threads = os.cpu_count() or 1
         t_all, reps_all = time_oracle_sample_threads(orc, inputs, threads)
         line["cpu_baseline"]["all_cores"] = {
@@ -660,14 +675,16 @@ SKINNY_M = (1, 2, 4, 8, 16, 32, 64)
 
 
 def measure_skinny(torch, w4, synth, dev, stream, copies, lin):
-    """gate 3584->18944 and down 18944->3584 at M = 1 ... 64 rows: a graph of
-    ten calls on the two alternating weight copies; more than 8 rows run as
-    consecutive launches of 8-row groups."""
+    """gate 3584->18944 and down 18944->3584 at M = 1 ... 64 rows, and
+    lm_head 3584->152064 at 2 ... 16: a graph of ten calls on the two
+    alternating weight copies, each row with the kernel that served it
+    (0 dp4a GEMV, 1 tcgen05 tensor cores, 2 row-per-thread dp4a, 3 warp-level
+    e4m3 MMA)."""
     out = {}
-    for name in ("gate", "down"):
+    for name in ("gate", "down", "lm_head"):
         i, K, N = lin[name]
         res = {}
-        for M in SKINNY_M:
+        for M in (SKINNY_M if name != "lm_head" else (2, 4, 8, 16)):
             X = torch.from_numpy(synth.activation(WEIGHT_SEED0 + i + ACT_SEED_OFFSET, M, K,
                                                   outlier_frac=OUTLIER_FRAC)).to(dev)
             Y = torch.empty((M, N), dtype=torch.float32, device=dev)
@@ -680,9 +697,62 @@ def measure_skinny(torch, w4, synth, dev, stream, copies, lin):
                     w4.w4a8_linear(X, Wqs[i], sws[i], Y=Y, ws=ws, flags=w4.LAUNCH_PDL)
 
             us = _graph_us(torch, stream, calls, 10)
-            res[str(M)] = {"us": round(us, 2), "GBps": round(weight_bytes(K, N) / us / 1e3, 1)}
+            res[str(M)] = {"us": round(us, 2), "GBps": round(weight_bytes(K, N) / us / 1e3, 1),
+                           "kernel": w4.w4a8_plan_info(M, K, N)["kernel"]}
         out[name] = res
     return out
+
+
+def measure_mlp(torch, w4, synth, dev, stream, lin):
+    """The Qwen2-7B-shaped MLP at one row, gate/up 3584 -> 18944 and down
+    18944 -> 3584 (102 MB of weights): fused, the gate/up launch writing
+    h = fp16(silu(g) * u) from its epilogue (row-interleaved gate/up weights)
+    and down reading h; unfused, the grouped gate/up launch, the gated
+    product as a launch of its own, then down.  PDL, two weight copies
+    alternating, graphs of ten MLPs."""
+    ig, K, N = lin["gate"]
+    iu = lin["up"][0]
+    idn = lin["down"][0]
+    mats = []
+    for c in range(2):
+        q = {}
+        for i in (ig, iu, idn):
+            n_, k_ = LINEARS[i][2], LINEARS[i][1]
+            W = synth.normal_gpu(WEIGHT_SEED0 + i + 100 * c, (n_, k_), 0.02, device=dev)
+            q[i] = w4.w4_quantize_weights(W)
+            del W
+        q["gu"] = w4.w4_interleave_rows(q[ig][0], q[ig][1], q[iu][0], q[iu][1])
+        mats.append(q)
+    X = torch.from_numpy(synth.activation(activation_seed("gate"), 1, K, outlier_frac=OUTLIER_FRAC)).to(dev)
+    H = torch.empty((1, N), dtype=torch.float16, device=dev)
+    Ygu = torch.empty((1, 2 * N), dtype=torch.float32, device=dev)
+    Yg = torch.empty((1, N), dtype=torch.float32, device=dev)
+    Yu = torch.empty((1, N), dtype=torch.float32, device=dev)
+    Yd = torch.empty((1, K), dtype=torch.float32, device=dev)
+    ws = torch.zeros(max(w4.w4a8_gate_up_silu_workspace_bytes(1, K, N), w4.w4a8_workspace_bytes(1, K, 2 * N),
+                         w4.w4a8_workspace_bytes(1, N, K), 4096), dtype=torch.uint8, device=dev)
+    PDL = w4.LAUNCH_PDL
+
+    def fused():
+        for k in range(10):
+            q = mats[k % 2]
+            w4.w4a8_gate_up_silu(X, q["gu"][0], q["gu"][1], H=H, Y_gu=Ygu, ws=ws, flags=PDL)
+            w4.w4a8_linear(H, q[idn][0], q[idn][1], Y=Yd, ws=ws, flags=PDL)
+
+    def unfused():
+        for k in range(10):
+            q = mats[k % 2]
+            w4.w4a8_linear_grouped(X, [q[ig][0], q[iu][0]], [q[ig][1], q[iu][1]], Ys=[Yg, Yu], ws=ws, flags=PDL)
+            w4.w4a8_silu_mul(Yg, Yu, H=H, flags=PDL)
+            w4.w4a8_linear(H, q[idn][0], q[idn][1], Y=Yd, ws=ws, flags=PDL)
+
+    nbytes = 2 * weight_bytes(K, N) + weight_bytes(N, K)
+    res = {"workload": "Qwen2-7B MLP, M=1: gate/up 3584->18944, silu(g)*u, down 18944->3584", "weight_bytes": nbytes}
+    for name, fn in (("fused", fused), ("unfused", unfused)):
+        us = _graph_us(torch, stream, fn, 10, reps=10)
+        res[name] = {"us": round(us, 2), "GBps": round(nbytes / us / 1e3, 1), "launches": 2 if name == "fused" else 3}
+    del mats
+    return res
 
 
 GROUP_SIZE = 128

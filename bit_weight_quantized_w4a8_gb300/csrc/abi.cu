@@ -53,31 +53,36 @@ std::atomic<int> g_qmma_r{0};
 std::atomic<int> g_stall_test_us{0};
 // Test of the bounded waits (w4a8_tuning_t.stall_test_us): 0 = off.
 unsigned long long qmma_stall_ns() { return (unsigned long long)g_stall_test_us.load() * 1000ull; }
-// Row-wise tensor-core calls use binary16 operands by default (measured
-// faster than the e4m3 path at every batch size).
-constexpr bool kDefaultMmaE4m3 = false;
+// Row-wise tensor-core calls use e4m3 operands by default: weight bytes
+// q + 8 (exactly (q + 8) * 2^-9, three instructions per 8 codes) and K = 32
+// per MMA, half the MMAs and TMEM stores of the binary16 path.  Measured on
+// GB300 (graphs of ten calls): lm_head at 8 rows 59.7 vs 88.2 us, gate at
+// 16 rows 15.9 vs 19.7 us, down at 8 rows 14.8 vs 18.8 us.
+constexpr bool kDefaultMmaE4m3 = true;
 bool mma_e4m3() {
     const int v = g_mma_e4m3.load();
     return v == 0 ? kDefaultMmaE4m3 : v == 2;
 }
 // Batch rows up to which row-wise W4A8 calls take the row-per-thread dp4a
-// kernel (from 2 rows).
-constexpr int kDefaultRowdotMaxM = 8;
+// kernel (from 2 rows) by default, on matrices of at most two tiles per SM:
+// measured on GB300 at 2 rows, gate 8.8 vs 12.6 us and down 11.9 vs 13.7 us
+// on the tensor cores, but lm_head (1188 tiles) 62.3 vs 57.9 us.
+constexpr int kDefaultRowdotMaxM = 3;
 // Batch rows from which the W4A8 entry points take the tensor-core kernel
-// when the row-per-thread kernel does not serve the call (measured on GB300:
-// the dp4a GEMV is faster at 1-2 rows, the tensor cores from 3; with the
-// row-per-thread kernel taking 2..8 rows, the tensor cores start at 9).
-constexpr int kDefaultMmaMinM = 3;
-// Batch rows for which row-wise W4A8 calls take the warp-level e4m3 MMA
-// kernel by default; it takes precedence over the two kernels above.
-// Measured on GB300 (graphs of ten calls, two weight copies): from 4 to 8
-// rows it matches the row-per-thread kernel on gate and down and beats it
-// on lm_head (4 rows: 69 vs 84 us; 8 rows: 87 vs 108 us); at 2 rows the
-// row-per-thread kernel is faster (gate 8.9 vs 11.0 us), from 16 rows the
-// tensor cores (gate 19.8 vs 20.7 us).  An explicit qmma_max_m extends it
-// down to 2 rows.
-constexpr int kDefaultQmmaMinM = 4;
-constexpr int kDefaultQmmaMaxM = 8;
+// when the row-per-thread kernel does not serve the call: row-wise scales
+// from 2 rows (e4m3 operands), group-wise scales from 3 (binary16 operands;
+// the dp4a GEMV is faster at 2 rows, and the row-per-thread kernel serves
+// group-wise calls of 2..8 rows).
+constexpr int kDefaultMmaMinM = 2;
+constexpr int kDefaultMmaMinMGroup = 3;
+// Group-wise scales: the row-per-thread kernel serves 2..8 rows by default
+// (the tensor cores' per-group readouts make them slower there).
+constexpr int kDefaultRowdotMaxMGroup = 8;
+// The warp-level e4m3 MMA kernel serves row-wise W4A8 calls only when
+// w4a8_tuning_t.qmma_max_m asks for it (2 rows up to that); it then takes
+// precedence over the two kernels above.  Measured on GB300 (graphs of ten
+// calls, two weight copies) it beats the e4m3 tensor cores only on gate at
+// 4 rows (11.5 vs 12.6 us); lm_head at 8 rows takes 86.9 vs 59.7 us.
 
 int sm_count(int* out) {
     static std::atomic<int> cache[64];
@@ -143,7 +148,7 @@ int check_w8a16_shape(int64_t M, int64_t K, int64_t N) {
 bool mma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::MmaPlan* pl, int sms = 0,
                   int64_t group = 0) {
     const int t = g_mma_min_m.load();
-    if (M < (t > 0 ? t : kDefaultMmaMinM)) return false;
+    if (M < (t > 0 ? t : group > 0 ? kDefaultMmaMinMGroup : kDefaultMmaMinM)) return false;
     if (group > 0 && (group % 128 || group > 16384)) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
     return w4a8::make_mma_plan((int)M, K, N, sms, pl, (int)(group / 64));
@@ -153,9 +158,7 @@ bool mma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::MmaPlan* pl, int sms = 
 // another kernel serves it.
 bool qmma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::QmmaPlan* pl, int sms = 0) {
     const int t = g_qmma_max_m.load();
-    const int hi = t > 0 ? t : kDefaultQmmaMaxM;
-    const int lo = t > 0 ? 2 : kDefaultQmmaMinM;
-    if (M < lo || M > hi) return false;
+    if (t <= 1 || M < 2 || M > t) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
     return w4a8::make_qmma_plan((int)M, K, N, sms, pl, g_qmma_r.load());
 }
@@ -165,9 +168,11 @@ bool qmma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::QmmaPlan* pl, int sms 
 bool rowdot_plan_for(int64_t M, int64_t K, int64_t N, w4a8::RowdotPlan* pl, int sms = 0,
                      int gshift = -1) {
     const int t = g_rowdot_max_m.load();
-    const int hi = t > 0 ? t : kDefaultRowdotMaxM;
+    const int hi = t > 0 ? t : gshift >= 0 ? kDefaultRowdotMaxMGroup : kDefaultRowdotMaxM;
     if (M < 2 || M > hi) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
+    // row-wise scales on many tiles: the tensor cores
+    if (t == 0 && gshift < 0 && (N + 127) / 128 > 2 * (int64_t)sms) return false;
     const int cl = g_force_cl.load();
     return w4a8::make_rowdot_plan((int)M, K, N, sms, pl, (cl == 2 || cl == 4 || cl == 8) ? cl : 0,
                                   g_ctas_per_sm.load(), gshift);

@@ -74,7 +74,8 @@ constexpr int kOffW = kOffB + kStages * kBStageMax;
 constexpr int kOffBars = kOffW + kWStages * kWTileBytes;
 constexpr int kNumBars = 2 * kWStages + 3 * kStages + 5;  // + accfull, dfull[2], dfree[2]
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kMmaSmem = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+constexpr int kOffSaSum = kOffMisc + 16;       // e4m3 path: exact code sums of the batch rows
+constexpr int kMmaSmem = kOffSaSum + 256 + 1024;  // + slack to align the base to 1024
 constexpr int kAQThreads = 256;
 
 static_assert(kWBlocks % kStageK == 0, "stage geometry");
@@ -107,6 +108,9 @@ struct MmaArgs {
     float* part_f;
     int gld, gkb;
     int M, N, K, BN, P, nkb, kbp;
+    // e4m3 path: the activation pass's per-piece code sums [M][pre_pieces]
+    const int32_t* sum_part;
+    int pre_pieces;
 };
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -225,9 +229,12 @@ __global__ void __launch_bounds__(kAQThreads) act_codes_kernel(
 // a_hi = a >> 4 in [-8, 7] and a_lo = a & 15 in [0, 15], both exact in
 // e4m3.  Per 128-code K tile t the B operand is [2 BN][128] bytes at
 // t * 2 BN * 128: rows 0..BN-1 hold a_hi of the batch rows, BN..2BN-1 a_lo,
-// 128-byte swizzled (16-byte chunk c of row m at m * 128 + (c ^ (m % 8)) * 16).
-// One MMA then yields W.A_hi and W.A_lo side by side in D, and the integer
-// product is 16 D_hi + D_lo.  Thread u handles 16 codes (one chunk).
+// 128-byte swizzled (16-byte chunk c of row m at m * 128 + (c ^ (m % 8)) * 16),
+// each group of 8 codes in the order (0, 2, 4, 6, 1, 3, 5, 7) that the
+// weight converters produce.  One MMA then yields W.A_hi and W.A_lo side by
+// side in D.  Thread u handles 16 codes (one chunk); each CTA also writes the
+// exact sum of its piece's codes of row m (sum_part[m][piece]), which removes
+// the +8 bias of the weight encoding.
 __device__ __forceinline__ uint32_t e4m3x4(int v0, int v1, int v2, int v3) {
     return (uint32_t)__nv_cvt_float_to_fp8((float)v0, __NV_SATFINITE, __NV_E4M3) |
            ((uint32_t)__nv_cvt_float_to_fp8((float)v1, __NV_SATFINITE, __NV_E4M3) << 8) |
@@ -239,8 +246,9 @@ __global__ void __launch_bounds__(kAQThreads) act_codes_e4m3_kernel(
     const __half* __restrict__ X, const int8_t* __restrict__ Xq, const float* __restrict__ sa_in,
     int M, int64_t K, int BN, uint8_t* __restrict__ B, float* __restrict__ sa_ws,
     int8_t* __restrict__ Xq_out, float* __restrict__ sa_out, int32_t* __restrict__ acc,
-    int64_t acc_words) {
+    int64_t acc_words, int32_t* __restrict__ sum_part) {
     __shared__ float red[kAQThreads / 32];
+    __shared__ int isum[kAQThreads / 32];
     griddep_launch_dependents();
     griddep_wait();
     for (int64_t e = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * kAQThreads + threadIdx.x; e < acc_words;
@@ -283,6 +291,7 @@ __global__ void __launch_bounds__(kAQThreads) act_codes_e4m3_kernel(
         for (int w = 0; w < kAQThreads / 32; ++w) mx = fmaxf(mx, red[w]);
         s = __fdiv_rn(mx, 127.f);
     }
+    int rsum = 0;
     if (u < nchunks) {
         uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
         if (u < kchunks) {
@@ -306,12 +315,18 @@ __global__ void __launch_bounds__(kAQThreads) act_codes_e4m3_kernel(
                 c8[2] = cq.z;
                 c8[3] = cq.w;
             }
+            // each 8-code group in the converters' order (0, 2, 4, 6, 1, 3, 5, 7)
+            const uint32_t p8[4] = {__byte_perm(c8[0], c8[1], 0x6420), __byte_perm(c8[0], c8[1], 0x7531),
+                                    __byte_perm(c8[2], c8[3], 0x6420), __byte_perm(c8[2], c8[3], 0x7531)};
             uint32_t h4[4], l4[4];
             #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 int a[4];
                 #pragma unroll
-                for (int b = 0; b < 4; ++b) a[b] = (int)(int8_t)((c8[w] >> (8 * b)) & 0xFFu);
+                for (int b = 0; b < 4; ++b) {
+                    a[b] = (int)(int8_t)((p8[w] >> (8 * b)) & 0xFFu);
+                    rsum += a[b];
+                }
                 h4[w] = e4m3x4(a[0] >> 4, a[1] >> 4, a[2] >> 4, a[3] >> 4);
                 l4[w] = e4m3x4(a[0] & 15, a[1] & 15, a[2] & 15, a[3] & 15);
             }
@@ -320,6 +335,17 @@ __global__ void __launch_bounds__(kAQThreads) act_codes_e4m3_kernel(
         }
         *dhi = hi;
         *dlo = lo;
+    }
+    // the piece's exact sum of codes (|sum| <= 127 * 4096)
+    #pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) rsum += __shfl_xor_sync(0xFFFFFFFFu, rsum, o);
+    if ((threadIdx.x & 31) == 0) isum[threadIdx.x >> 5] = rsum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int tsum = 0;
+        #pragma unroll
+        for (int w = 0; w < kAQThreads / 32; ++w) tsum += isum[w];
+        sum_part[(int64_t)m * gridDim.y + blockIdx.y] = tsum;
     }
     if (blockIdx.y == 0 && threadIdx.x == 0) {
         sa_ws[m] = s;
@@ -352,22 +378,13 @@ __device__ __forceinline__ uint4 int4x8_to_f16(uint32_t w) {
                       *reinterpret_cast<const uint32_t*>(&v2), *reinterpret_cast<const uint32_t*>(&v3));
 }
 
-// One packed word (8 INT4 codes) -> 8 e4m3 values in K order (two words):
-// each code pair as binary16 (n ^ 8 in the mantissa of 1024.0, minus 1032:
-// exact), then a pair conversion to e4m3 (exact for -8..7).
+// One packed word (8 INT4 codes) -> 8 e4m3 bytes in the K order (0, 2, 4, 6,
+// 1, 3, 5, 7): code q becomes the byte v = n ^ 8 = q + 8 in [0, 15], which as
+// e4m3 is exactly v * 2^-9 (bytes 0..7 are the subnormals m * 2^-9, bytes
+// 8..15 the first binade (8 + m) * 2^-9).  One xor, one shift, two masks.
 __device__ __forceinline__ uint2 int4x8_to_e4m3(uint32_t w) {
-    const uint32_t u = w ^ 0x88888888u;
-    const uint32_t h = u >> 4;
-    const __half2 bias = __floats2half2_rn(1032.f, 1032.f);
-    uint32_t e[4];
-    #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t x = (__byte_perm(u, h, (uint32_t)(j | ((4 + j) << 8))) & 0x000F000Fu) | 0x64006400u;
-        const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
-        e[j] = (uint32_t)__nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&v),
-                                                     __NV_SATFINITE, __NV_E4M3);
-    }
-    return make_uint2(e[0] | (e[1] << 16), e[2] | (e[3] << 16));
+    const uint32_t x = w ^ 0x88888888u;
+    return make_uint2(x & 0x0F0F0F0Fu, (x >> 4) & 0x0F0F0F0Fu);
 }
 
 // Two CTAs per SM (shared memory < 113 KB, 256 TMEM columns, <= 93
@@ -690,11 +707,20 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
         } else {
             // ---- epilogue: TMEM lanes = weight rows, columns = batch rows
             griddep_wait();  // scales and outputs
+            const int ct = tid - kFirstConvWarp * 32;
+            int* sa_sum = reinterpret_cast<int*>(smem + kOffSaSum);
+            if constexpr (kF8) {
+                // the batch rows' exact code sums (the +8 bias of the weight bytes)
+                for (int e = ct; e < a.M; e += kConvWarps * 32) sa_sum[e] = 0;
+                named_bar_sync(1, kConvWarps * 32);
+                for (int e = ct; e < a.M * a.pre_pieces; e += kConvWarps * 32)
+                    atomicAdd(sa_sum + e / a.pre_pieces, __ldcg(a.sum_part + e));
+                named_bar_sync(1, kConvWarps * 32);
+            }
             const bool ok = __all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(accfull), 0, abort_flag));
             tc_fence_after_sync();
             // the TMEM lanes this warp may read are its converter lanes (q, r);
             // the two warps of a quarter split the columns
-            const int ct = tid - kFirstConvWarp * 32;
             const int n = n0 + r;
             const float swv = (ok && n < a.N) ? a.sw[n] : 0.f;
             for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
@@ -706,15 +732,18 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                 for (int t = 0; t < 8; ++t) {
                     const int m = 8 * ch + t;
                     if (m >= a.M) break;
-                    const int32_t acc = kF8 ? 16 * __float2int_rn(__uint_as_float(v[t])) +
-                                                  __float2int_rn(__uint_as_float(vl[t]))
+                    // e4m3: D = 2^-9 sum v b (weight bytes v = q + 8), so 512 D is an
+                    // exact integer and sum q a = 16 U_hi + U_lo - 8 sum a
+                    const int32_t raw = kF8 ? 16 * __float2int_rn(__uint_as_float(v[t]) * 512.f) +
+                                                  __float2int_rn(__uint_as_float(vl[t]) * 512.f)
                                             : __float2int_rn(__uint_as_float(v[t]));
                     const int64_t o = (int64_t)m * a.N + n;
                     if (a.P == 1) {
+                        const int32_t acc = kF8 ? raw - 8 * sa_sum[m] : raw;
                         a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), swv), a.sa[m]);
                         if (a.acc_out != nullptr) a.acc_out[o] = acc;
                     } else {
-                        atomicAdd(a.part + ((int64_t)tile * a.M + m) * kTileRows + r, acc);  // exact, order-free
+                        atomicAdd(a.part + ((int64_t)tile * a.M + m) * kTileRows + r, raw);  // exact, order-free
                     }
                 }
             }
@@ -745,8 +774,9 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                             const int m = e / kTileRows, rr = e % kTileRows, nn = n0 + rr;
                             if (rr >= rows) continue;
                             const int64_t o = (int64_t)m * a.N + nn;
-                            a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(v[b]), a.sw[nn]), a.sa[m]);
-                            if (a.acc_out != nullptr) a.acc_out[o] = v[b];
+                            const int32_t acc = kF8 ? v[b] - 8 * sa_sum[m] : v[b];
+                            a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), a.sw[nn]), a.sa[m]);
+                            if (a.acc_out != nullptr) a.acc_out[o] = acc;
                         }
                     }
                     if (ct == 0) a.tickets[tile] = 0u;  // ready for the next call
@@ -861,7 +891,8 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int g
     // per weight matrix): K is split when the exactness limit forces it
     // (every tile) or when a matrix has fewer tiles than 4/5 of the CTA slots.
     pl.off_sa = kTicketBytes;
-    pl.off_codes = pl.off_sa + 256;
+    pl.off_sum = pl.off_sa + 256;  // e4m3 path: code sums [M][pieces of 4096 codes]
+    pl.off_codes = round_up_sz(pl.off_sum + (size_t)M * ((K + 4095) / 4096) * 4, 256);
     // (K blocks rounded up to an even count: the e4m3 tiles cover 128 codes)
     pl.off_part = round_up_sz(pl.off_codes + (size_t)((pl.nkb + 1) / 2 * 2) * pl.BN * kKBlock * 2, 256);
     const int64_t small = 2 * num_sms * 4 / 5;
@@ -885,15 +916,19 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     float* sa_ws = reinterpret_cast<float*>(wsb + pl.off_sa);
     uint8_t* codes = wsb + pl.off_codes;
+    int pre_pieces = 0;
     {
         const __half* xh = reinterpret_cast<const __half*>(X);
         int Mi = M, BNi = pl.BN;
         int64_t Kk = K;
         int32_t* acc = reinterpret_cast<int32_t*>(wsb + pl.off_part);
         int64_t acc_words = (int64_t)((pl.ws_bytes - pl.off_part) / 4);
-        void* args[] = {&xh, &Xq, &sa, &Mi, &Kk, &BNi, &codes, &sa_ws, &Xq_out, &sa_out, &acc, &acc_words};
+        int32_t* sum_part = reinterpret_cast<int32_t*>(wsb + pl.off_sum);
+        void* args[] = {&xh, &Xq, &sa, &Mi, &Kk, &BNi, &codes, &sa_ws, &Xq_out, &sa_out, &acc, &acc_words,
+                        &sum_part};
         const int64_t vecs = e4m3 ? (K + 127) / 128 * 8 : (int64_t)pl.nkb * 8;  // per batch row
         const unsigned pieces = (unsigned)((vecs + kAQThreads - 1) / kAQThreads);
+        pre_pieces = (int)pieces;
         const void* pre = e4m3 ? reinterpret_cast<const void*>(act_codes_e4m3_kernel)
                                : reinterpret_cast<const void*>(act_codes_kernel);
         cudaError_t e = launch_pdl(pre, dim3(pl.BN, pieces), dim3(kAQThreads), 0, stream, flags, args);
@@ -940,6 +975,8 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
         a.P = pg.P;
         a.nkb = pg.nkb;
         a.kbp = pg.kbp;
+        a.sum_part = reinterpret_cast<const int32_t*>(wsb + pl.off_sum);
+        a.pre_pieces = pre_pieces;
         void* args[] = {&a};
         const void* fn = gkb ? reinterpret_cast<const void*>(mma_kernel<true, false>)
                        : e4m3 ? reinterpret_cast<const void*>(mma_kernel<false, true>)

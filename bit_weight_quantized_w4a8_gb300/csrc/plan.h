@@ -70,7 +70,7 @@ struct MmaPlan {
     int P, kbp;        // K pieces, K blocks per piece
     int grid, smem, sms;
     int stages, stage_bytes;             // weight ring
-    size_t off_sa, off_codes, off_part;  // workspace layout
+    size_t off_sa, off_sum, off_codes, off_part;  // workspace layout
     size_t ws_bytes;
 };
 

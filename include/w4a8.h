@@ -73,23 +73,32 @@ typedef enum {
    workspace are only touched after the wait. */
 #define W4A8_LAUNCH_PDL 1u
 
-/* Maximum activation rows (decode batch) per call.  Row-wise W4A8 calls
- * with 2 to 8 rows (w4a8_tuning_t.rowdot_max_m) run on the row-per-thread
- * integer kernel: an activation-quantization launch writes the codes into
- * the workspace split by parity, then each weight row is walked by four
- * threads (of four warps) that unpack its INT4 codes once for all batch rows and
- * sum exact int32 dp4a products against activation words that the whole CTA
- * reads as shared-memory broadcasts.  Other W4A8 calls with at
- * least 3 rows (see w4a8_tuning_t.mma_min_m) run on the tensor cores: an
- * activation-quantization launch writes binary16 codes into the workspace, then
- * tcgen05 MMAs of 128 weight rows x the batch accumulate the integer
- * products exactly in fp32 (every partial sum of one K piece of at most
- * 16384 is an integer below 2^24) and the rescale matches the dp4a path
- * bit for bit.  One row (and larger batches when the other kernels are
- * switched off) runs on the dp4a GEMV, one launch per group of up to 8 rows
- * (W8A16: 4 rows, always dp4a-free fp32 FMAs), each streaming the whole
- * weight matrix.  w4a8_linear_noalloc takes at most 8 rows, always on the
- * dp4a GEMV. */
+/* Maximum activation rows (decode batch) per call.  Which kernel serves a
+ * call (w4a8_plan_info reports it; w4a8_tuning_t moves the thresholds):
+ *  - 1 row: the dp4a GEMV (fused activation quantization, weights streamed
+ *    by bulk copies into a shared-memory ring).
+ *  - row-wise scales, 2 or 3 rows on matrices of at most 2 x SMs 128-row
+ *    tiles: the row-per-thread integer kernel (an activation pass writes the
+ *    codes split by parity; four threads of four warps walk each weight row,
+ *    unpack its INT4 codes once for all batch rows and sum exact int32 dp4a
+ *    products against shared-memory broadcasts of the activations).
+ *  - other row-wise calls from 2 rows: the tcgen05 tensor cores.  An
+ *    activation pass writes each INT8 code as two exact e4m3 integers
+ *    (a = 16 a_hi + a_lo); converter warps turn each INT4 code into the e4m3
+ *    byte q + 8, which is exactly (q + 8) * 2^-9, and store it into TMEM;
+ *    kind::f8f6f4 MMAs of 128 weight rows x 32 codes x the batch accumulate
+ *    exactly in fp32 (every partial sum of one K piece of at most 16384 is
+ *    an integer multiple of 2^-9 below 2^15), and the bias 8 * sum(a) is
+ *    removed with the exact code sum, so the rescale matches the dp4a path
+ *    bit for bit.
+ *  - group-wise scales: the row-per-thread kernel for 2..8 rows, the tensor
+ *    cores (binary16 operands) from 9, the dp4a GEMV otherwise.
+ *  - the warp-level e4m3 MMA kernel (mma.sync m16n8k32, operands built in
+ *    registers) serves 2..32 rows when w4a8_tuning_t.qmma_max_m asks for it.
+ * When the other kernels are switched off the dp4a GEMV serves batches too,
+ * one launch per group of up to 8 rows (W8A16: always, 4 rows, fp32 FMAs),
+ * each streaming the whole weight matrix.  w4a8_linear_noalloc takes at most
+ * 8 rows, always on the dp4a GEMV. */
 #define W4A8_MAX_M 64
 #define W8A16_MAX_M 64
 
@@ -440,19 +449,22 @@ int w4a8_device_error(unsigned* flags, void* stream);
  *     row-per-thread kernel, CTAs per SM (0 = 1 at 4 or 8 threads per
  *     row, 2 at 2).
  *   mma_min_m: activation rows from which the W4A8 entry points use the
- *     tensor-core kernel (2..65; 0 = default, 65 = never).
- *   rowdot_max_m: activation rows up to which row-wise W4A8 calls use the
- *     row-per-thread kernel, from 2 rows (0 = default 8, 1 = never, <= 8);
- *     it takes precedence over mma_min_m.  force_threads_per_row 2, 4 or 8
+ *     tensor-core kernel (2..65; 0 = default: 2 rows for row-wise scales,
+ *     3 for group-wise scales; 65 = never).
+ *   rowdot_max_m: activation rows up to which W4A8 calls use the
+ *     row-per-thread kernel, from 2 rows (0 = default: 3 rows for row-wise
+ *     scales on matrices of at most 2 x SMs 128-row tiles, 8 rows for
+ *     group-wise scales; 1 = never, <= 8); it takes precedence over
+ *     mma_min_m.  force_threads_per_row 2, 4 or 8
  *     sets that kernel's threads per weight row (row-wise scales; calls
  *     with group-wise scales always use 4).
- *   mma_e4m3: operands of the row-wise tensor-core kernel: 0 = default,
- *     1 = bf16 (kind::f16, K = 16 per MMA), 2 = e4m3 (kind::f8f6f4, K = 32
- *     per MMA, activation codes split as 16 a_hi + a_lo).
+ *   mma_e4m3: operands of the row-wise tensor-core kernel: 0 = default
+ *     (e4m3), 1 = binary16 (kind::f16, K = 16 per MMA), 2 = e4m3
+ *     (kind::f8f6f4, K = 32 per MMA: weight bytes q + 8 read as (q + 8) *
+ *     2^-9, activation codes split as 16 a_hi + a_lo).
  *   qmma_max_m: activation rows up to which row-wise W4A8 calls use the
- *     warp-level e4m3 MMA kernel, from 2 rows (0 = the default 4..8 rows,
- *     1 = never, <= 32); it takes precedence over rowdot_max_m and
- *     mma_min_m.
+ *     warp-level e4m3 MMA kernel, from 2 rows (0 or 1 = never, the default;
+ *     <= 32); it takes precedence over rowdot_max_m and mma_min_m.
  *   qmma_tiles_per_warp: 16-row weight tiles per warp of that kernel (1, 2,
  *     or 4 for at most 16 rows; 0 = default).
  *   stall_test_us: for tests of the bounded waits (0 = off, <= 1 s): the

@@ -151,7 +151,7 @@ def test_plan_invariants(sms, w8):
 
 
 def check_mma_plan(p, M, K, N, sms):
-    assert M >= 3
+    assert M >= 2
     tiles = -(-N // 128)
     nkb = -(-K // 64)
     P = p["splits"]
@@ -204,13 +204,14 @@ def check_rowdot_plan(p, M, K, N, sms):
 
 def test_kernel_routing():
     """Row-wise calls: 1 row on the dp4a GEMV, 2..3 rows on the
-    row-per-thread kernel, 4..8 on the warp-level MMA kernel, 9+ on the
-    tensor cores; an explicit qmma_max_m gives the warp-level kernel 2 rows
-    up to it; with it switched off, 2..8 rows on the row-per-thread kernel
-    and 9+ on the tensor cores; the tuning moves every threshold."""
+    row-per-thread kernel for matrices of at most 2 x SMs tiles, the tensor
+    cores otherwise; an explicit qmma_max_m gives the warp-level kernel 2 rows
+    up to it; with the tensor cores switched off the row-per-thread kernel
+    takes up to rowdot_max_m rows; the tuning moves every threshold."""
     try:
-        route = lambda M: w4.w4a8_plan_info(M, 3584, 18944, num_sms=152)["kernel"]
-        assert [route(M) for M in (1, 2, 3, 4, 8, 9, 32, 64)] == [0, 2, 2, 3, 3, 1, 1, 1]
+        route = lambda M, N=18944: w4.w4a8_plan_info(M, 3584, N, num_sms=152)["kernel"]
+        assert [route(M) for M in (1, 2, 3, 4, 8, 9, 32, 64)] == [0, 2, 2, 1, 1, 1, 1, 1]
+        assert [route(M, 152064) for M in (1, 2, 3, 4)] == [0, 1, 1, 1]   # lm_head: many tiles
         w4.w4a8_set_tuning(qmma_max_m=16)
         assert [route(M) for M in (2, 16, 17)] == [3, 3, 1]
         w4.w4a8_set_tuning(qmma_max_m=32, qmma_tiles_per_warp=1)
@@ -219,16 +220,19 @@ def test_kernel_routing():
         assert [route(M) for M in (16, 17)] == [3, 1]
         with pytest.raises(w4.W4A8Error):
             w4.w4a8_set_tuning(qmma_tiles_per_warp=3)
-        w4.w4a8_set_tuning(qmma_max_m=1)
+        w4.w4a8_set_tuning(qmma_max_m=1, rowdot_max_m=8)
         assert [route(M) for M in (1, 2, 3, 8, 9, 64)] == [0, 2, 2, 2, 1, 1]
+        assert route(8, 152064) == 2                                       # explicit: any matrix
         with pytest.raises(w4.W4A8Error):
             w4.w4a8_set_tuning(qmma_max_m=33)
         w4.w4a8_set_tuning(rowdot_max_m=4, qmma_max_m=1)
         assert [route(M) for M in (2, 4, 5)] == [2, 2, 1]
         w4.w4a8_set_tuning(rowdot_max_m=1, qmma_max_m=1)
+        assert [route(M) for M in (2, 3)] == [1, 1]   # row-wise: the tensor cores from 2 rows
+        w4.w4a8_set_tuning(rowdot_max_m=1, qmma_max_m=1, mma_min_m=3)
         assert [route(M) for M in (2, 3)] == [0, 1]
         for tpr in (2, 4, 8):
-            w4.w4a8_set_tuning(force_threads_per_row=tpr, qmma_max_m=1)
+            w4.w4a8_set_tuning(force_threads_per_row=tpr, qmma_max_m=1, rowdot_max_m=8)
             p = w4.w4a8_plan_info(5, 3584, 18944, num_sms=152)
             assert p["threads_per_row"] == tpr and p["kernel"] == 2
             check_rowdot_plan(p, 5, 3584, 18944, 152)
@@ -434,7 +438,7 @@ def test_rowdot_workspace_covers_grouped_matrices():
     for the total rows: every smaller matrix's plan needs no more, and plans
     that never split K do not reserve partial sums per tile."""
     try:
-        w4.w4a8_set_tuning(qmma_max_m=1)
+        w4.w4a8_set_tuning(qmma_max_m=1, rowdot_max_m=8)
         for sms in (152, 148, 20):
             for (M, K) in [(2, 3584), (8, 3584), (8, 18944), (5, 131072), (3, 896)]:
                 N = 40000

@@ -208,12 +208,11 @@ def test_skinny_batch_sweep(w4, orc, M, name):
 
 @pytest.mark.parametrize("M", [3, 8, 16])
 def test_lm_head_small_batches(w4, orc, M):
-    """lm_head at small batch sizes: the row-per-thread kernel at 3 rows,
-    the warp-level MMA kernel at 8 (a 1188-tile grid in several waves), the
-    tensor cores at 16."""
+    """lm_head at small batch sizes, on the e4m3 tensor cores (a 1188-tile
+    grid in several waves)."""
     idx = NAMES.index("lm_head")
     _, K, N = QWEN2_7B_SET[idx]
-    assert w4.w4a8_plan_info(M, K, N)["kernel"] == {3: 2, 8: 3, 16: 1}[M]
+    assert w4.w4a8_plan_info(M, K, N)["kernel"] == 1
     run_w4(w4, orc, K, N, M, WEIGHT_SEED0 + idx, flags=w4.LAUNCH_PDL)
 
 

@@ -317,7 +317,7 @@ def test_w4a8_tensor_cores_match_dp4a(w4, orc):
 
 @pytest.mark.parametrize("cl", [1, 2, 8, 32, 64, 128, 256])
 def test_w4a8_threads_per_row(w4, orc, cl):
-    w4.w4a8_set_tuning(force_threads_per_row=cl, rowdot_max_m=1, qmma_max_m=1)  # the dp4a kernel's plans
+    w4.w4a8_set_tuning(force_threads_per_row=cl, rowdot_max_m=1, qmma_max_m=1, mma_min_m=65)  # the dp4a kernel's plans
     for (M, K, N, seed) in [(1, 3584, 300, 40), (2, 2048, 99, 41), (1, 256, 513, 42)]:
         try:
             plan = w4.w4a8_plan_info(M, K, N)
@@ -332,7 +332,7 @@ def test_w4a8_two_stage_ring(w4, orc):
     w4.w4a8_set_tuning(ring_bytes=8192)
     assert w4.w4a8_plan_info(1, 3584, 5000)["stages"] == 2
     check_w4a8(w4, orc, 1, 3584, 5000, 50)
-    w4.w4a8_set_tuning(ring_bytes=8192, force_splits=3, rowdot_max_m=1, qmma_max_m=1)
+    w4.w4a8_set_tuning(ring_bytes=8192, force_splits=3, rowdot_max_m=1, qmma_max_m=1, mma_min_m=65)
     check_w4a8(w4, orc, 2, 18944, 300, 51)
 
 

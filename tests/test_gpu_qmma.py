@@ -165,7 +165,7 @@ def test_qmma_matches_other_kernels(w4):
     X = to_dev(synth.activation(971, M, K, outlier_frac=0.001))
     Wq, sw = w4.w4_quantize_weights(to_dev(W))
     outs = []
-    for kw, kind in ((dict(qmma_max_m=8), QMMA), (dict(qmma_max_m=1), 2), (dict(qmma_max_m=1, rowdot_max_m=1), 1),
+    for kw, kind in ((dict(qmma_max_m=8), QMMA), (dict(qmma_max_m=1, rowdot_max_m=8), 2), (dict(qmma_max_m=1, rowdot_max_m=1), 1),
                      (dict(qmma_max_m=1, rowdot_max_m=1, mma_min_m=65), 0)):
         w4.w4a8_set_tuning(**kw)
         assert w4.w4a8_plan_info(M, K, N)["kernel"] == kind

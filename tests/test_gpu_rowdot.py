@@ -35,7 +35,7 @@ def orc():
 
 @pytest.fixture(autouse=True)
 def _reset_tuning(w4):
-    w4.w4a8_set_tuning(qmma_max_m=1)  # 2..32 rows would take the warp-level MMA kernel
+    w4.w4a8_set_tuning(qmma_max_m=1, rowdot_max_m=8)  # the row-per-thread kernel for 2..8 rows
     yield
     w4.w4a8_set_tuning(reset=True)
     assert w4.w4a8_device_error() == 0
@@ -95,7 +95,7 @@ ROWDOT_SHAPES = [
 @pytest.mark.parametrize("M,K,N,seed", ROWDOT_SHAPES)
 def test_rowdot_parity(w4, orc, M, K, N, seed, fused, tpr):
     if tpr:
-        w4.w4a8_set_tuning(force_threads_per_row=tpr, qmma_max_m=1)
+        w4.w4a8_set_tuning(force_threads_per_row=tpr, qmma_max_m=1, rowdot_max_m=8)
     plan = check(w4, orc, M, K, N, seed, fused=fused)
     assert plan["threads_per_row"] == (tpr or 4)
 
@@ -210,7 +210,7 @@ def test_rowdot_matches_other_kernels(w4):
     X = to_dev(synth.activation(731, M, K, outlier_frac=0.001))
     Wq, sw = w4.w4_quantize_weights(to_dev(W))
     outs = []
-    for kw in (dict(), dict(rowdot_max_m=1), dict(rowdot_max_m=1, mma_min_m=65)):
+    for kw in (dict(rowdot_max_m=8), dict(rowdot_max_m=1), dict(rowdot_max_m=1, mma_min_m=65)):
         w4.w4a8_set_tuning(qmma_max_m=1, **kw)
         outs.append(w4.w4a8_linear(X, Wq, sw).cpu().numpy())
     assert np.array_equal(bits(outs[0]), bits(outs[1]))

@@ -1,6 +1,7 @@
 """Bounded device waits, run out on purpose without faulting or hanging the GPU.
 
-With w4a8_tuning_t.stall_test_us the warp-level MMA kernel's warps first
+With w4a8_tuning_t.stall_test_us the warp-level MMA kernel's warps (the
+kernel is selected with qmma_max_m) first
 wait, with that short limit, for a barrier phase that nothing completes (a
 flag that nothing sets).  The wait runs out, the kernel records bit 0 in the
 device error word, waits (bounded) for the weight copies it already issued
@@ -43,7 +44,7 @@ def test_stalled_wait_reports_and_next_call_is_exact(w4, M, K, N):
     Xd = torch.from_numpy(X).cuda()
     assert w4.w4a8_device_error() == 0
     try:
-        w4.w4a8_set_tuning(stall_test_us=20000)  # 20 ms
+        w4.w4a8_set_tuning(stall_test_us=20000, qmma_max_m=32)  # 20 ms; the warp-level MMA kernel
         assert w4.w4a8_plan_info(M, K, N)["kernel"] == 3
         ws = torch.zeros(w4.w4a8_workspace_bytes(M, K, N), dtype=torch.uint8, device="cuda")
         w4.w4a8_linear(Xd, Wq, sw, ws=ws)           # returns: the wait runs out
@@ -53,8 +54,10 @@ def test_stalled_wait_reports_and_next_call_is_exact(w4, M, K, N):
     finally:
         w4.w4a8_set_tuning(reset=True)
     ws.zero_()                                      # as the header asks after an error
+    w4.w4a8_set_tuning(qmma_max_m=32)
     for _ in range(2):
         Y = w4.w4a8_linear(Xd, Wq, sw, ws=ws)
         torch.cuda.synchronize()
         assert np.array_equal(Y.cpu().numpy().view(np.uint32), Y_ref.view(np.uint32))
+    w4.w4a8_set_tuning(reset=True)
     assert w4.w4a8_device_error() == 0
