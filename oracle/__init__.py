@@ -75,6 +75,8 @@ class Oracle:
             "oracle_w4g_quantize": [_p, _i64, _i64, _i64, _p, _p],
             "oracle_w4a8g_ref": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p],
             "oracle_w4a8g_linear": [_p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _p, _p],
+            "oracle_w4a8g_f32": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p],
+            "oracle_w4a8g_linear_f32": [_p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _p],
             "oracle_isx_lut": [ctypes.c_int, ctypes.c_double, _p],
             "oracle_index_softmax": [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p],
         }.items():
@@ -233,6 +235,38 @@ class Oracle:
         if st != OK:
             raise ValueError("oracle_w4a8g_linear status %d" % st)
         return Y, B, Xq, sa
+
+    def w4a8g_f32(self, Xq: np.ndarray, sa: np.ndarray, Wq: np.ndarray, sg: np.ndarray, gs: int):
+        """The group-wise product in the fixed binary32 order: Y [M][N] fp32."""
+        Xq = np.ascontiguousarray(Xq, dtype=np.int8)
+        sa = np.ascontiguousarray(sa, dtype=np.float32)
+        Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+        sg = np.ascontiguousarray(sg, dtype=np.float32)
+        M, K = Xq.shape
+        N = Wq.shape[0]
+        assert Wq.shape[1] * 2 == K and sg.shape == (N, self.w4g_scale_stride(K, gs))
+        Y = np.empty((M, N), np.float32)
+        st = self._lib.oracle_w4a8g_f32(_ptr(Xq), _ptr(sa), M, K, gs, _ptr(Wq), _ptr(sg), N, _ptr(Y))
+        if st != OK:
+            raise ValueError("oracle_w4a8g_f32 status %d" % st)
+        return Y
+
+    def w4a8g_linear_f32(self, X: np.ndarray, Wq: np.ndarray, sg: np.ndarray, gs: int):
+        """Returns (Y fp32 in the fixed order, Xq, sa)."""
+        X = np.ascontiguousarray(X, dtype=np.float16)
+        Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+        sg = np.ascontiguousarray(sg, dtype=np.float32)
+        M, K = X.shape
+        N = Wq.shape[0]
+        assert Wq.shape[1] * 2 == K and sg.shape == (N, self.w4g_scale_stride(K, gs))
+        Y = np.empty((M, N), np.float32)
+        Xq = np.empty((M, K), np.int8)
+        sa = np.empty(M, np.float32)
+        st = self._lib.oracle_w4a8g_linear_f32(_ptr(X), M, K, gs, _ptr(Wq), _ptr(sg), N, _ptr(Y),
+                                               _ptr(Xq), _ptr(sa))
+        if st != OK:
+            raise ValueError("oracle_w4a8g_linear_f32 status %d" % st)
+        return Y, Xq, sa
 
     # -- IndexSoftmax -----------------------------------------------------
     def isx_lut(self, b: int = 5, c: float = 6.6) -> np.ndarray:

@@ -26,7 +26,10 @@
  * function (symmetric codes, divisors 7 and 127, round half away from zero,
  * true division, low-nibble-first two's-complement packing, fp32 rescale in
  * the order (acc * s_w) * s_a; for group scales a binary64 reference plus
- * the magnitude that bounds any fp32 evaluation of it).
+ * the magnitude that bounds any fp32 evaluation of it, and the binary32
+ * evaluation in the library's fixed order: exact group sums folded with one
+ * fused multiply-add each inside chunks of max(gs, 1024) codes, chunk
+ * results added in ascending order).
  *
  * Build: gcc -std=c11 -O2 -ffp-contract=off -fPIC -shared (no fast-math, no
  * FMA contraction, so every float operation is one IEEE binary32 operation).
@@ -373,6 +376,67 @@ int oracle_w4a8g_ref(const int8_t* Xq, const float* sa, int64_t M, int64_t K, in
         }
     }
     return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* g3: group-wise W4A8 product in binary32, in the library's fixed order     */
+/*     [P1 当前实现方式: int32 accumulate times the weight scale times the    */
+/*     activation scale, applied per group as 后续优化方向 suggests]          */
+/* ------------------------------------------------------------------------ */
+
+/* The page gives the arithmetic but no summation order for the per-group
+   products, and an fp32 sum depends on its order.  This is the order the
+   library fixes (a function of K and gs only, never of a launch plan):
+     acc_g   = exact integer sum of group g (as in g2), converted to binary32
+               with one round-to-nearest (exact for gs <= 16384)
+     L       = max(gs, 1024) codes: the fold chunk; chunk c holds the
+               groups whose codes lie in [c*L, (c+1)*L)
+     f_c     = +0, then for every group g of chunk c in ascending order
+               f_c = fmaf(acc_g, s_g, f_c)         (one rounding each)
+     F       = +0, then for every chunk c in ascending order F = F + f_c
+     Y[m][n] = F * s_a[m]
+   fmaf is C99's fused multiply-add (a single IEEE rounding); the other
+   operations are single binary32 operations (no contraction).  Chunks let
+   the K dimension be split at chunk boundaries without changing a bit. */
+int oracle_w4a8g_f32(const int8_t* Xq, const float* sa, int64_t M, int64_t K, int64_t gs,
+                     const uint8_t* Wq, const float* sg, int64_t N, float* Y)
+{
+    if (M < 0 || N < 0 || K < 0 || gs < 2 || (gs & 1) || K % gs || gs > 65536)
+        return ORACLE_ERR_SHAPE;
+    int64_t ld = oracle_w4g_scale_stride(K, gs);
+    int64_t L = gs > 1024 ? gs : 1024;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            float F = 0.0f;
+            for (int64_t c0 = 0; c0 < K; c0 += L) {
+                int64_t c1 = c0 + L < K ? c0 + L : K;
+                float f = 0.0f;
+                for (int64_t k0 = c0; k0 < c1; k0 += gs) {
+                    int64_t acc = 0;
+                    for (int64_t j = k0 / 2; j < (k0 + gs) / 2; ++j) {
+                        uint8_t byte = Wq[n * (K / 2) + j];
+                        acc += (int64_t)Xq[m * K + 2 * j] * nibble_value(byte & 0xFu);
+                        acc += (int64_t)Xq[m * K + 2 * j + 1] * nibble_value(byte >> 4);
+                    }
+                    f = fmaf((float)acc, sg[n * ld + k0 / gs], f);
+                }
+                F = F + f;
+            }
+            Y[m * N + n] = F * sa[m];
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* The whole group-wise linear in the fixed binary32 order: the activation
+   quantizer of a2, then g3. */
+int oracle_w4a8g_linear_f32(const uint16_t* X, int64_t M, int64_t K, int64_t gs,
+                            const uint8_t* Wq, const float* sg, int64_t N, float* Y,
+                            int8_t* Xq_out, float* sa_out)
+{
+    int st = oracle_act_quantize(X, M, K, Xq_out, sa_out);
+    if (st != ORACLE_OK) return st;
+    return oracle_w4a8g_f32(Xq_out, sa_out, M, K, gs, Wq, sg, N, Y);
 }
 
 /* The whole group-wise linear: the per-row activation quantizer of a2, then

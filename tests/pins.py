@@ -482,6 +482,123 @@ def pin_w4a8g_error_bound(o):
         assert err_g < err_r, (err_g, err_r)
 
 
+def pack_nibbles(q: np.ndarray) -> np.ndarray:
+    """[N][K] codes in [-8, 7] -> [N][K/2] bytes, q[2j] in the low nibble."""
+    u = (np.asarray(q, np.int64) & 0xF).astype(np.uint8)
+    return (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
+
+
+def _fold_exact(acc, sg_row, gs, K, chunk=None, descending=False, fused=True):
+    """The fixed binary32 order of the group-wise product for one output,
+    evaluated in exact rationals with every step rounded by ``f32_nearest``
+    (a single rounding for each fused multiply-add).  The keyword arguments
+    give the plausible wrong orders the pins must tell apart."""
+    L = chunk if chunk is not None else max(gs, 1024)
+    F = Fraction(0)
+    for c0 in range(0, K, L):
+        groups = list(range(c0 // gs, min(c0 + L, K) // gs))
+        if descending:
+            groups.reverse()
+        f = Fraction(0)
+        for g in groups:
+            a = Fraction(float(f32_nearest(Fraction(int(acc[g])))))
+            p = a * Fraction(float(sg_row[g]))
+            if not fused:
+                p = Fraction(float(f32_nearest(p)))
+            f = Fraction(float(f32_nearest(p + f)))
+        F = Fraction(float(f32_nearest(F + f)))
+    return F
+
+
+def pin_w4a8g_f32_golden(o):
+    """Hand-derived outputs of the fixed order (tests/golden/w4g_fold_order.txt):
+    ascending groups, one rounding per fused step, chunks of max(gs, 1024)
+    codes, the activation scale last."""
+    cases = read_cases("w4g_fold_order.txt")
+    assert len(cases) >= 6
+    for c in cases:
+        gs, K = int(c["gs"][0]), int(c["K"][0])
+        ng = K // gs
+        Xq = np.zeros((1, K), np.int8)
+        q = np.zeros((1, K), np.int64)
+        for t in c["acc"]:
+            g, a = (int(v) for v in t.split(":"))
+            Xq[0, g * gs], q[0, g * gs] = a, 1
+        sg = np.zeros((1, o.w4g_scale_stride(K, gs)), np.float32)
+        sg[0, :ng] = 1.0
+        for t in c.get("s", []):
+            g, v = t.split(":")
+            sg[0, int(g)] = np.float32(v)
+            assert Fraction(float(sg[0, int(g)])) == Fraction(v), v   # exact in binary32
+        sa = np.array([np.float32(c["sa"][0])], np.float32)
+        assert Fraction(float(sa[0])) == Fraction(c["sa"][0])
+        Y = o.w4a8g_f32(Xq, sa, pack_nibbles(q), sg, gs)
+        assert Fraction(float(Y[0, 0])) == Fraction(c["want"][0]), (c["name"], float(Y[0, 0]))
+        for v in c["not"]:
+            assert Fraction(v) != Fraction(c["want"][0])
+
+
+def pin_w4a8g_f32_exact_rational(o):
+    """Brute force on small seeded operands: every output equals the fixed
+    order evaluated in exact rationals, and the operands separate that order
+    from a descending fold, an unchunked fold, chunks of 512 codes and an
+    unfused multiply-add (so a pin failure localises the mistake)."""
+    seps = {"descending": 0, "unchunked": 0, "chunk512": 0, "unfused": 0}
+    for (M, N, K, gs, seed) in [(2, 3, 2048, 32, 71), (1, 3, 3072, 128, 72), (2, 2, 2560, 64, 73),
+                                (1, 3, 4096, 2048, 74), (2, 2, 1536, 512, 75)]:
+        W = synth.normal(seed, (N, K), 0.02)
+        Wq, sg = o.w4g_quantize(W, gs)
+        Xq, sa = o.act_quantize(synth.activation(seed + 100, M, K, outlier_frac=0.002))
+        Y = o.w4a8g_f32(Xq, sa, Wq, sg, gs)
+        q = decode_nibbles(Wq)
+        ng = K // gs
+        acc = (Xq.astype(np.int64)[:, None, :] * q[None, :, :]).reshape(M, N, ng, gs).sum(-1)
+        for m in range(M):
+            for n in range(N):
+                F = _fold_exact(acc[m, n], sg[n], gs, K)
+                want = f32_nearest(F * Fraction(float(sa[m])))
+                assert Y[m, n].view(np.uint32) == want.view(np.uint32), (gs, K, m, n, Y[m, n], want)
+                seps["descending"] += _fold_exact(acc[m, n], sg[n], gs, K, descending=True) != F
+                seps["unchunked"] += _fold_exact(acc[m, n], sg[n], gs, K, chunk=K) != F
+                seps["chunk512"] += gs < 512 and _fold_exact(acc[m, n], sg[n], gs, K, chunk=512) != F
+                seps["unfused"] += _fold_exact(acc[m, n], sg[n], gs, K, fused=False) != F
+    assert all(v > 0 for v in seps.values()), seps
+
+
+def pin_w4a8g_f32_closed_form(o):
+    """Every code +7, group scales 2^-g, activations all 1 (codes 127):
+    every group product and partial sum is exact, so Y is one rounding of
+    889 * gs * sum_g 2^-g * s_a; alternating activation signs give +0."""
+    gs, G = 64, 40
+    K = gs * G
+    W = np.concatenate([np.full(gs, 7.0 * 2.0 ** -(g % 8)) for g in range(G)]).astype(np.float32)
+    W = np.stack([W, -W])
+    Wq, sg = o.w4g_quantize(W, gs)
+    X = np.ones((1, K), np.float16)
+    Y, Xq, sa = o.w4a8g_linear_f32(X, Wq, sg, gs)
+    exact = Fraction(889 * gs) * sum(Fraction(1, 2 ** (g % 8)) for g in range(G))
+    want = f32_nearest(exact * Fraction(float(sa[0])))
+    assert Y[0, 0] == want and Y[0, 1] == -want, (Y, want)
+    Xa = np.tile(np.array([1, -1], np.float16), K // 2)[None, :]
+    Y0, _, _ = o.w4a8g_linear_f32(Xa, Wq, sg, gs)
+    assert np.all(Y0.view(np.uint32) == 0), Y0   # +0, never -0
+
+
+def pin_w4a8g_f32_bound(o):
+    """The fixed-order binary32 result against the binary64 reference: within
+    the recursive-summation bound (groups per chunk + chunks + 1) * 2^-24 * B
+    at the shapes of the benchmark (K = 3584 and 18944, gs = 128 and 32)."""
+    for (M, N, K, gs, seed) in [(2, 16, 3584, 128, 81), (1, 8, 18944, 128, 82), (1, 4, 3584, 32, 83)]:
+        W = synth.normal(seed, (N, K), 0.02)
+        X = synth.activation(seed + 50, M, K, outlier_frac=0.001)
+        Wq, sg = o.w4g_quantize(W, gs)
+        Y32, Xq, sa = o.w4a8g_linear_f32(X, Wq, sg, gs)
+        Y64, B = o.w4a8g_ref(Xq, sa, Wq, sg, gs)
+        L = max(gs, 1024)
+        n_round = L // gs + (K + L - 1) // L + 1
+        assert np.all(np.abs(Y32.astype(np.float64) - Y64) <= n_round * 2.0 ** -24 * 1.001 * B + 1e-300)
+
+
 # --------------------------------------------------------------------------
 # s1-s3: IndexSoftmax
 # --------------------------------------------------------------------------

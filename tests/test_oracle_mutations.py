@@ -54,6 +54,16 @@ MUTATIONS = [
     ("w4g_ref_group_bytes", "for (int64_t j = g * (gs / 2); j < (g + 1) * (gs / 2); ++j)",
      "for (int64_t j = 0; j < gs / 2; ++j)"),
     ("w4g_ref_dropped_high", "acc += p0 + p1;", "acc += p0;"),
+    ("w4g_f32_descending", "for (int64_t k0 = c0; k0 < c1; k0 += gs) {",
+     "for (int64_t k0 = c1 - gs; k0 >= c0; k0 -= gs) {"),
+    ("w4g_f32_unfused", "f = fmaf((float)acc, sg[n * ld + k0 / gs], f);",
+     "f = f + (float)acc * sg[n * ld + k0 / gs];"),
+    ("w4g_f32_unchunked", "int64_t L = gs > 1024 ? gs : 1024;", "int64_t L = K > 0 ? K : 1;"),
+    ("w4g_f32_chunk_512", "int64_t L = gs > 1024 ? gs : 1024;", "int64_t L = gs > 512 ? gs : 512;"),
+    ("w4g_f32_dropped_chunks", "F = F + f;", "F = f;"),
+    ("w4g_f32_dropped_sa", "Y[m * N + n] = F * sa[m];", "Y[m * N + n] = F;"),
+    ("w4g_f32_scale_group0", "sg[n * ld + k0 / gs], f);", "sg[n * ld], f);"),
+    ("w4g_f32_dropped_high", "acc += (int64_t)Xq[m * K + 2 * j + 1] * nibble_value(byte >> 4);", ""),
     ("silu_sign_of_exp", "double p = x / (1.0 + exp(-x)) * (double)u[i];", "double p = x / (1.0 + exp(x)) * (double)u[i];"),
     ("silu_dropped_up", "double p = x / (1.0 + exp(-x)) * (double)u[i];", "double p = x / (1.0 + exp(-x));"),
     ("silu_sigmoid_only", "double p = x / (1.0 + exp(-x)) * (double)u[i];", "double p = 1.0 / (1.0 + exp(-x)) * (double)u[i];"),
