@@ -527,7 +527,8 @@ def w4a8_plan_info(M: int, K: int, N: int, w8a16: bool = False, num_sms: int = 0
     return dict(zip(PLAN_FIELDS, list(arr)))
 
 
-GROUP_PLAN_FIELDS = PLAN_FIELDS + ("scale_window", "scale_stage_bytes")
+# group scales: the fold chunks of the fixed-order contract (count, codes each)
+GROUP_PLAN_FIELDS = PLAN_FIELDS + ("chunks", "chunk_codes")
 
 
 def w4a8g_plan_info(M: int, K: int, N: int, group: int, num_sms: int = 0) -> dict:

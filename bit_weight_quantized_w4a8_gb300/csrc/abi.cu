@@ -71,12 +71,12 @@ constexpr int kDefaultRowdotMaxM = 3;
 // Batch rows from which the W4A8 entry points take the tensor-core kernel
 // when the row-per-thread kernel does not serve the call: row-wise scales
 // from 2 rows (e4m3 operands), group-wise scales from 3 (binary16 operands;
-// the dp4a GEMV is faster at 2 rows, and the row-per-thread kernel serves
-// group-wise calls of 2..8 rows).
+// by default the one-thread-per-row kernel serves group-wise calls of 1..8
+// rows, so the tensor cores take them from 9).
 constexpr int kDefaultMmaMinM = 2;
 constexpr int kDefaultMmaMinMGroup = 3;
-// Group-wise scales: the row-per-thread kernel serves 2..8 rows by default
-// (the tensor cores' per-group readouts make them slower there).
+// Group-wise scales: the one-thread-per-row kernel serves 1..8 rows by
+// default (the tensor cores' per-group readouts make them slower there).
 constexpr int kDefaultRowdotMaxMGroup = 8;
 // The warp-level e4m3 MMA kernel serves row-wise W4A8 calls only when
 // w4a8_tuning_t.qmma_max_m asks for it (2 rows up to that); it then takes
@@ -113,14 +113,14 @@ w4a8::Tuning tuning() {
     return t;
 }
 
-// gshift >= 0: group-wise scales, one per 2^gshift granules, rows of gld floats.
+// pair: paired gate/up rows (the gated product in the epilogue).
 int plan_for(bool w4, bool fused, int64_t M, int64_t K, int64_t N, w4a8::GemvPlan* pl,
-             int sms = 0, int gshift = -1, int gld = 0, bool pair = false) {
+             int sms = 0, bool pair = false) {
     if (sms <= 0) {
         int st = sm_count(&sms);
         if (st != W4A8_OK) return st;
     }
-    if (!w4a8::make_gemv_plan(w4, fused, (int)M, K, N, sms, tuning(), pl, gshift, gld, pair))
+    if (!w4a8::make_gemv_plan(w4, fused, (int)M, K, N, sms, tuning(), pl, pair))
         return fail(W4A8_ERR_SHAPE, "no launch plan for M=%lld K=%lld N=%lld",
                     (long long)M, (long long)K, (long long)N);
     return W4A8_OK;
@@ -164,18 +164,19 @@ bool qmma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::QmmaPlan* pl, int sms 
 }
 
 // Row-per-thread plan for an M-row W4A8 call, or false when another kernel
-// serves it.  gshift >= 0: group-wise scales, groups of 2^gshift codes.
+// serves it.  gshift >= 0: group-wise scales, groups of 2^gshift codes, on
+// the one-thread-per-row kernel from 1 row (rowdot_max_m = 1: never).
 bool rowdot_plan_for(int64_t M, int64_t K, int64_t N, w4a8::RowdotPlan* pl, int sms = 0,
                      int gshift = -1) {
     const int t = g_rowdot_max_m.load();
     const int hi = t > 0 ? t : gshift >= 0 ? kDefaultRowdotMaxMGroup : kDefaultRowdotMaxM;
-    if (M < 2 || M > hi) return false;
+    if (M < (gshift >= 0 ? 1 : 2) || M > hi || (gshift >= 0 && t == 1)) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
     // row-wise scales on many tiles: the tensor cores
     if (t == 0 && gshift < 0 && (N + 127) / 128 > 2 * (int64_t)sms) return false;
     const int cl = g_force_cl.load();
     return w4a8::make_rowdot_plan((int)M, K, N, sms, pl, (cl == 2 || cl == 4 || cl == 8) ? cl : 0,
-                                  g_ctas_per_sm.load(), gshift);
+                                  g_ctas_per_sm.load(), gshift, gshift >= 0 ? g_force_splits.load() : 0);
 }
 
 // log2 of a group size already checked by check_group.
@@ -183,6 +184,23 @@ int log2_group(int64_t group) {
     int s = 0;
     while ((1LL << s) < group) ++s;
     return s;
+}
+
+// Group-wise calls that neither single launch serves: the one-thread-per-row
+// kernel, one launch per group of up to 8 rows (each streams the weights);
+// `full` plans 8 rows, `tail` a shorter last group.
+bool group_row_plans(int64_t M, int64_t K, int64_t N, int64_t group, w4a8::RowdotPlan* full,
+                     w4a8::RowdotPlan* tail, int sms = 0) {
+    if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
+    const int rg = w4a8::kRowdotMaxM;
+    const int gshift = log2_group(group);
+    const int fp = g_force_splits.load();
+    if (!w4a8::make_rowdot_plan((int)(M < rg ? M : rg), K, N, sms, full, 1, g_ctas_per_sm.load(), gshift, fp))
+        return false;
+    *tail = *full;
+    if (M > rg && M % rg)
+        return w4a8::make_rowdot_plan((int)(M % rg), K, N, sms, tail, 1, g_ctas_per_sm.load(), gshift, fp);
+    return true;
 }
 
 int check_ws(size_t need, void* ws, size_t ws_bytes) {
@@ -209,12 +227,11 @@ constexpr int kRowGroupW8 = 4;
 // Plans of the row groups of an M-row call: `full` for groups of `rg`
 // rows, `tail` for a shorter last group (equal to `full` when there is none).
 int plan_row_groups(bool w4, bool fused, int64_t M, int64_t K, int64_t N, int rg,
-                    w4a8::GemvPlan* full, w4a8::GemvPlan* tail, int sms = 0, int gshift = -1,
-                    int gld = 0) {
-    int st = plan_for(w4, fused, M < rg ? M : rg, K, N, full, sms, gshift, gld);
+                    w4a8::GemvPlan* full, w4a8::GemvPlan* tail, int sms = 0) {
+    int st = plan_for(w4, fused, M < rg ? M : rg, K, N, full, sms);
     if (st != W4A8_OK) return st;
     *tail = *full;
-    if (M > rg && M % rg) st = plan_for(w4, fused, M % rg, K, N, tail, sms, gshift, gld);
+    if (M > rg && M % rg) st = plan_for(w4, fused, M % rg, K, N, tail, sms);
     return st;
 }
 
@@ -313,9 +330,8 @@ size_t w4a8g_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t group) {
     if (rowdot_plan_for(M, K, N, &rp, 0, log2_group(group))) return rp.ws_bytes;
     w4a8::MmaPlan mp;
     if (mma_plan_for(M, K, N, &mp, 0, group)) return mp.ws_bytes;
-    w4a8::GemvPlan pf, pt;
-    if (plan_row_groups(true, true, M, K, N, kRowGroupW4, &pf, &pt, 0, gshift, gld) != W4A8_OK)
-        return 0;
+    w4a8::RowdotPlan pf, pt;
+    if (!group_row_plans(M, K, N, group, &pf, &pt)) return 0;
     return pf.ws_bytes > pt.ws_bytes ? pf.ws_bytes : pt.ws_bytes;
 }
 
@@ -530,13 +546,7 @@ int w4a8g_run(const char* name, const uint16_t* X, const int8_t* Xq, const float
         return fail(W4A8_ERR_ALIGN, "%s: X/Xq/Xq_out need 16-byte, sa/sa_out 4-byte alignment", name);
     w4a8::RowdotPlan rp;
     if (rowdot_plan_for(M, K, total, &rp, 0, log2_group(group))) {
-        // one plan per matrix inside; the workspace bound covers every N[g] <= total
-        for (int g = 0; g < G; ++g) {
-            w4a8::RowdotPlan pg;
-            if (!w4a8::make_rowdot_plan((int)M, K, N[g], rp.sms, &pg, rp.tpr, rp.cps, rp.gshift) ||
-                pg.ws_bytes > rp.ws_bytes)
-                return fail(W4A8_ERR_SHAPE, "%s: no row-per-thread plan for group %d", name, g);
-        }
+        // one launch for every matrix; its plan (whole tiles per matrix) fits this workspace
         if ((st = check_ws(rp.ws_bytes, ws, ws_bytes)) != W4A8_OK) return st;
         cudaError_t e = w4a8::launch_w4a8_rowdot(rp, X, Xq, sa, (int)M, K, G, Wq, nullptr, N, Y, nullptr,
                                                  Xq_out, sa_out, ws, flags,
@@ -558,20 +568,22 @@ int w4a8g_run(const char* name, const uint16_t* X, const int8_t* Xq, const float
                                               static_cast<cudaStream_t>(stream), (int)group, sg);
         return e == cudaSuccess ? ok() : cuda_fail(e, name);
     }
-    w4a8::GemvPlan pf, pt;
-    if ((st = plan_row_groups(true, true, M, K, total, kRowGroupW4, &pf, &pt, 0, gshift, gld)) != W4A8_OK)
+    w4a8::RowdotPlan pf, pt;
+    if (!group_row_plans(M, K, total, group, &pf, &pt))
+        return fail(W4A8_ERR_SHAPE, "%s: no launch plan for M=%lld K=%lld N=%lld", name, (long long)M,
+                    (long long)K, (long long)total);
+    if ((st = check_ws(pf.ws_bytes > pt.ws_bytes ? pf.ws_bytes : pt.ws_bytes, ws, ws_bytes)) != W4A8_OK)
         return st;
-    if ((st = check_workspace(pf, ws, ws_bytes)) != W4A8_OK) return st;
-    if ((st = check_workspace(pt, ws, ws_bytes)) != W4A8_OK) return st;
+    const int rg = w4a8::kRowdotMaxM;
     float* Yg[W4A8_MAX_GROUP];
-    for (int64_t m0 = 0; m0 < M; m0 += kRowGroupW4) {
-        const int64_t mg = M - m0 < kRowGroupW4 ? M - m0 : kRowGroupW4;
+    for (int64_t m0 = 0; m0 < M; m0 += rg) {
+        const int64_t mg = M - m0 < rg ? M - m0 : rg;
         for (int g = 0; g < G; ++g) Yg[g] = Y[g] + m0 * N[g];
-        cudaError_t e = w4a8::launch_w4a8g(
-            mg == kRowGroupW4 || M < kRowGroupW4 ? pf : pt, X != nullptr,
-            X ? X + m0 * K : nullptr, Xq ? Xq + m0 * K : nullptr, sa ? sa + m0 : nullptr, (int)mg,
-            K, (int)group, G, Wq, sg, N, Yg, Xq_out ? Xq_out + m0 * K : nullptr,
-            sa_out ? sa_out + m0 : nullptr, ws, flags, static_cast<cudaStream_t>(stream));
+        cudaError_t e = w4a8::launch_w4a8_rowdot(
+            mg == rg || M < rg ? pf : pt, X ? X + m0 * K : nullptr, Xq ? Xq + m0 * K : nullptr,
+            sa ? sa + m0 : nullptr, (int)mg, K, G, Wq, nullptr, N, Yg, nullptr,
+            Xq_out ? Xq_out + m0 * K : nullptr, sa_out ? sa_out + m0 : nullptr, ws, flags,
+            static_cast<cudaStream_t>(stream), (int)group, sg);
         if (e != cudaSuccess) return cuda_fail(e, name);
     }
     return ok();
@@ -668,7 +680,6 @@ int w4a8_device_error(unsigned* flags, void* stream) {
     *flags = 0;
     cudaError_t e = w4a8::read_and_clear_device_error(flags, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = w4a8::read_and_clear_mma_error(flags, static_cast<cudaStream_t>(stream));
-    if (e == cudaSuccess) e = w4a8::read_and_clear_group_error(flags, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = w4a8::read_and_clear_rowdot_error(flags, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = w4a8::read_and_clear_qmma_error(flags, static_cast<cudaStream_t>(stream));
     // a wait that gave up may leave split-K arrival counters non-zero; the
@@ -780,30 +791,28 @@ int w4a8g_plan_info(int64_t M, int64_t K, int64_t N, int64_t group, int num_sms,
     if (st != W4A8_OK) return st;
     int gshift, gld;
     if ((st = check_group(K, group, &gshift, &gld)) != W4A8_OK) return st;
-    w4a8::RowdotPlan rp;
-    if (rowdot_plan_for(M, K, N, &rp, num_sms, log2_group(group))) {
-        const int ws = rp.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)rp.ws_bytes;
-        const int v[] = {rp.P, rp.tpr, rp.MT, 128, rp.tiles, rp.grid, 128, rp.NS, 16384,
-                         rp.smem, ws, 2, rp.gwin, rp.gstride * 128 * 4};
-        for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
-        return ok();
-    }
+    // the last two entries: the fold chunks of the group-scale contract
+    // (count, codes per chunk)
+    const int64_t chunk = group > 1024 ? group : 1024;
+    const int nch = (int)((K + chunk - 1) / chunk);
+    w4a8::RowdotPlan rp, rt;
+    const bool single = rowdot_plan_for(M, K, N, &rp, num_sms, log2_group(group));
     w4a8::MmaPlan mp;
-    if (mma_plan_for(M, K, N, &mp, num_sms, group)) {
+    if (!single && mma_plan_for(M, K, N, &mp, num_sms, group)) {
         const int ws = mp.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)mp.ws_bytes;
         const int v[] = {mp.P, 0, mp.BN, 128, mp.tiles, mp.grid, 128, mp.stages, mp.stage_bytes,
-                         mp.smem, ws, 1, 0, 0};
+                         mp.smem, ws, 1, nch, (int)chunk};
         for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
         return ok();
     }
-    w4a8::GemvPlan pl, pt;
-    if ((st = plan_row_groups(true, true, M, K, N, kRowGroupW4, &pl, &pt, num_sms, gshift, gld)) !=
-        W4A8_OK)
-        return st;
-    const size_t wsb = pl.ws_bytes > pt.ws_bytes ? pl.ws_bytes : pt.ws_bytes;
+    // one launch, or the plan of the first group of 8 rows; workspace for the whole call
+    if (!single && !group_row_plans(M, K, N, group, &rp, &rt, num_sms))
+        return fail(W4A8_ERR_SHAPE, "no launch plan for M=%lld K=%lld N=%lld", (long long)M, (long long)K,
+                    (long long)N);
+    const size_t wsb = single ? rp.ws_bytes : rp.ws_bytes > rt.ws_bytes ? rp.ws_bytes : rt.ws_bytes;
     const int ws = wsb > 0x7FFFFFFF ? 0x7FFFFFFF : (int)wsb;
-    const int v[] = {pl.P, pl.Cl, pl.S, pl.Rl, pl.Gs, pl.grid, pl.rows_max, pl.NS,
-                     pl.stage_stride, pl.smem, ws, 0, pl.gwin, pl.gstage};
+    const int v[] = {rp.P, rp.tpr, rp.MT, 128, rp.tiles, rp.grid, 128, rp.NS, 16384,
+                     rp.smem, ws, 2, nch, (int)chunk};
     for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
     return ok();
 }
@@ -821,7 +830,7 @@ size_t w4a8_gate_up_silu_workspace_bytes(int64_t M, int64_t K, int64_t N) {
     if (N < 1 || N > 0x3FFFFFFF || check_w4a8_shape(M, K, 2 * N) != W4A8_OK) return 0;
     if (M > 1) return w4a8_workspace_bytes(M, K, 2 * N);
     w4a8::GemvPlan pl;
-    if (plan_for(true, true, 1, K, 2 * N, &pl, 0, -1, 0, true) != W4A8_OK) return 0;
+    if (plan_for(true, true, 1, K, 2 * N, &pl, 0, true) != W4A8_OK) return 0;
     return pl.ws_bytes;
 }
 
@@ -837,7 +846,7 @@ int w4a8_gate_up_silu(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (M == 1) {
         w4a8::GemvPlan pl;
-        if ((st = plan_for(true, true, 1, K, 2 * N, &pl, 0, -1, 0, true)) != W4A8_OK) return st;
+        if ((st = plan_for(true, true, 1, K, 2 * N, &pl, 0, true)) != W4A8_OK) return st;
         if ((st = check_workspace(pl, ws, ws_bytes)) != W4A8_OK) return st;
         cudaError_t e = w4a8::launch_w4a8_silu(pl, X, 1, K, Wq_gu, sw_gu, 2 * N, Y_gu, H, ws, flags, s);
         return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_gate_up_silu launch");

@@ -70,8 +70,6 @@ struct GemvArgs {
     int M;
     int K;
     int N;
-    int gshift;             // group scales: log2(granules per group)
-    int gld;                // group scales: floats per scale row
     GemvPlan pl;
 };
 
@@ -155,28 +153,10 @@ __device__ __forceinline__ int segment_of(const GemvArgs& a, int64_t n) {
     return g;
 }
 
-// Window of group scales a K piece needs: groups [gb, gb + win) of each scale
-// row, widened to whole 16-byte words (gb and win multiples of 4; the scale
-// rows are padded to a multiple of 4 floats, so the window stays in the row).
-struct GroupWindow {
-    int gb, win;
-};
-
-__device__ __forceinline__ GroupWindow group_window(const GemvArgs& a, int g0, int gp) {
-    GroupWindow w;
-    w.gb = (g0 >> a.gshift) & ~3;
-    const int ge = min((((g0 + gp - 1) >> a.gshift) + 4) & ~3, a.gld);
-    w.win = ge - w.gb;
-    return w;
-}
-
 // Stage `st` of a CTA's weight stream (rows row0 + st * Rl ...) into ring
 // slot `slot`: one 1-D bulk copy per run of whole rows, cut where a segment
-// ends, or one copy per row-piece when K is split.  With group scales (kG)
-// the rows' scale windows follow into the slot's scale area, as one copy
-// per run (whole rows) or one per row.  (Inlined: a call on the refill path
-// costs register spills and delays the refill.)
-template <bool kG>
+// ends, or one copy per row-piece when K is split.  (Inlined: a call on the
+// refill path costs register spills and delays the refill.)
 __device__ __forceinline__ void issue_stage(const GemvArgs& a, uint8_t* smem, int st, int slot,
                                          int64_t row0, int nrows, int g0, uint64_t pol) {
     const GemvPlan& pl = a.pl;
@@ -187,10 +167,7 @@ __device__ __forceinline__ void issue_stage(const GemvArgs& a, uint8_t* smem, in
     const int nr = min(pl.Rl, nrows - r0);
     const uint32_t dst = smem_u32(smem + slot * pl.stage_stride);
     const uint32_t bar = smem_u32(smem + pl.off_bars + 8 * slot);
-    GroupWindow gw = {0, 0};
-    if constexpr (kG) gw = group_window(a, g0, gp);
-    const uint32_t gdst = smem_u32(smem + pl.off_gsc + slot * pl.gstage);
-    mbar_arrive_expect_tx(bar, (uint32_t)(nr * RBp + (kG ? nr * gw.win * 4 : 0)));
+    mbar_arrive_expect_tx(bar, (uint32_t)(nr * RBp));
     int64_t n = row0 + r0;
     const int64_t n_end = n + nr;
     while (n < n_end) {
@@ -204,31 +181,15 @@ __device__ __forceinline__ void issue_stage(const GemvArgs& a, uint8_t* smem, in
             for (int r = 0; r < run; ++r)
                 bulk_g2s(d + r * RBp, src + (int64_t)r * RB, (uint32_t)RBp, bar, pol);
         }
-        if constexpr (kG) {
-            const float* ssrc = static_cast<const float*>(a.wscale[sg]) +
-                                (n - a.off[sg]) * a.gld + gw.gb;
-            const uint32_t sd = gdst + (uint32_t)((n - row0 - r0) * gw.win * 4);
-            if (pl.P == 1) {  // whole padded rows: the run is contiguous
-                bulk_g2s(sd, ssrc, (uint32_t)(run * gw.win * 4), bar, pol);
-            } else {
-                for (int r = 0; r < run; ++r)
-                    bulk_g2s(sd + r * gw.win * 4, ssrc + (int64_t)r * a.gld, (uint32_t)(gw.win * 4),
-                             bar, pol);
-            }
-        }
         n += run;
     }
 }
 
 // SMAX bounds the granule columns per thread; kExactS says the plan uses
-// exactly SMAX of them (no per-column test in the loop).  kG (INT4 only):
-// one fp32 scale per group of 2^gshift granules along K instead of one per
-// row; the int32 sum of each granule is scaled by its group's scale and
-// summed in fp32, and the activation scale multiplies that sum once.
-template <bool kW4, int MT, int SMAX, bool kFused, bool kExactS, bool kG>
+// exactly SMAX of them (no per-column test in the loop).
+template <bool kW4, int MT, int SMAX, bool kFused, bool kExactS>
 __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
-    static_assert(kW4 || !kG, "group scales are for INT4 weights");
-    using AccT = typename std::conditional<kW4 && !kG, int, float>::type;
+    using AccT = typename std::conditional<kW4, int, float>::type;
     constexpr int kActWords = 8;  // registers per granule per activation row (W8: binary16 pairs)
 
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -257,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
     float* sw_s = reinterpret_cast<float*>(smem + pl.off_sw);
 
     const uint64_t pol = l2_evict_first_policy();
-    auto issue = [&](int st, int slot) { issue_stage<kG>(a, smem, st, slot, row0, nrows, g0, pol); };
+    auto issue = [&](int st, int slot) { issue_stage(a, smem, st, slot, row0, nrows, g0, pol); };
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -293,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
     // Weight scales of this CTA's rows (weights may be read before the wait):
     // asynchronous 4-byte copies whose completion arrives on sw_bar; only the
     // threads that write outputs wait for it, right before their first one.
-    if constexpr (kW4 && !kG) {
+    if constexpr (kW4) {
         if (pl.P == 1)
             for (int r = tid; r < nrows; r += kConsumers)
             {
@@ -302,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                 cp_async_4(smem_u32(sw_s + r), static_cast<const float*>(a.wscale[sg]) + (n - a.off[sg]));
             }
         cp_async_mbar_arrive(smem_u32(sw_bar));
-    } else if constexpr (!kW4) {
+    } else {
         // binary16 scales (one segment): the 4-byte words covering rows
         // row0 & ~1 ... row0 + nrows - 1; a word past the last scale reads
         // only its first half
@@ -316,8 +277,6 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
             }
         }
         cp_async_mbar_arrive(smem_u32(sw_bar));
-    } else {
-        mbar_arrive(smem_u32(sw_bar));
     }
 
     griddep_wait();  // activations, outputs and workspace from here on
@@ -475,33 +434,18 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
 
 
     // W4: the low nibbles enter the dot product biased by +8 (n ^ 8 = q + 8),
-    // so each row's sum carries 8 * (sum of the even-k codes) too much: per
-    // thread (row-wise scales) or per granule (group scales).
-    constexpr int kCorr = kG ? SMAX : 1;
-    int corr[MT][kCorr];
+    // so each row's sum carries 8 * (sum of the even-k codes) too much.
+    int corr[MT];
     #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        #pragma unroll
-        for (int s = 0; s < kCorr; ++s) corr[m][s] = 0;
+        corr[m] = 0;
         if constexpr (kW4) {
             #pragma unroll
             for (int s = 0; s < SMAX; ++s)
                 #pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    corr[m][kG ? s : 0] = __dp4a((int)act[m][s][t], 0x08080808, corr[m][kG ? s : 0]);
+                for (int t = 0; t < 4; ++t) corr[m] = __dp4a((int)act[m][s][t], 0x08080808, corr[m]);
         }
     }
-    // Group scales: this thread's granule columns map to fixed groups; their
-    // offsets inside the piece's scale window (gsw floats per row).
-    int goff[kG ? SMAX : 1];
-    int gsw = 0;
-    if constexpr (kG) {
-        const GroupWindow gw = group_window(a, g0, gp);
-        gsw = gw.win;
-        #pragma unroll
-        for (int s = 0; s < SMAX; ++s) goff[s] = ((g0 + min(j + s * Cl, gp - 1)) >> a.gshift) - gw.gb;
-    }
-
     // the weight-scale cache must have landed before any output is written
     wait_or_abort(smem_u32(sw_bar), 0, abort_flag, kErrFullWait);
 
@@ -536,12 +480,6 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                 #pragma unroll
                 for (int s = 0; s < SMAX; ++s)
                     wg[s] = *reinterpret_cast<const uint4*>(stage + coff[s]);
-                float gsc[kG ? SMAX : 1];
-                if constexpr (kG) {
-                    const float* srow = reinterpret_cast<const float*>(smem + pl.off_gsc + slot * pl.gstage) + i * gsw;
-                    #pragma unroll
-                    for (int s = 0; s < SMAX; ++s) gsc[s] = srow[goff[s]];
-                }
                 __syncwarp();
                 if (lane == 0) {
                     // the last warp done with this slot refills it with the
@@ -557,22 +495,14 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
 
                 using LaneT = typename std::conditional<kW4, int, float>::type;
                 LaneT alo[MT][NCH], ahi[MT][NCH];
-                float gacc[MT][NCH];  // group scales: fp32 sums of scaled granules
                 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     #pragma unroll
-                    for (int h = 0; h < NCH; ++h) { alo[m][h] = 0; ahi[m][h] = 0; gacc[m][h] = 0.f; }
+                    for (int h = 0; h < NCH; ++h) { alo[m][h] = 0; ahi[m][h] = 0; }
                 }
                 #pragma unroll
                 for (int s = 0; s < SMAX; ++s) {
                     if (kExactS || s < pl.S) {  // uniform over the CTA
-                        if constexpr (kG) {
-                            #pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                #pragma unroll
-                                for (int h = 0; h < NCH; ++h) { alo[m][h] = 0; ahi[m][h] = 0; }
-                            }
-                        }
                         const uint32_t wv[4] = {wg[s].x, wg[s].y, wg[s].z, wg[s].w};
                         #pragma unroll
                         for (int t = 0; t < 4; ++t) {
@@ -609,31 +539,15 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                                 }
                             }
                         }
-                        if constexpr (kG) {
-                            // the granule's exact int32 sum times its group scale
-                            #pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                int lo_sum = 0, hi_sum = 0;
-                                #pragma unroll
-                                for (int h = 0; h < NCH; ++h) { lo_sum += alo[m][h]; hi_sum += ahi[m][h]; }
-                                const int v = lo_sum - corr[m][s] + (hi_sum >> 4);
-                                gacc[m][s % NCH] = __fmaf_rn(__int2float_rn(v), gsc[s], gacc[m][s % NCH]);
-                            }
-                        }
                     }
                 }
                 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    if constexpr (kG) {
-                        float sum = 0.f;
-                        #pragma unroll
-                        for (int h = 0; h < NCH; ++h) sum += gacc[m][h];
-                        part[d][m] = sum;
-                    } else if constexpr (kW4) {
+                    if constexpr (kW4) {
                         int lo_sum = 0, hi_sum = 0;
                         #pragma unroll
                         for (int h = 0; h < NCH; ++h) { lo_sum += alo[m][h]; hi_sum += ahi[m][h]; }
-                        part[d][m] = lo_sum - corr[m][0] + (hi_sum >> 4);  // exact: hi_sum = 16 * sum
+                        part[d][m] = lo_sum - corr[m] + (hi_sum >> 4);  // exact: hi_sum = 16 * sum
                     } else {
                         float sum = 0.f;
                         #pragma unroll
@@ -684,8 +598,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                 if (sb + d < nstages && r < nrows) {
                     const int64_t n = row0 + r;
                     if (pl.P == 1) {
-                        const float swv = kG ? 0.f
-                                        : kW4 ? sw_s[r]
+                        const float swv = kW4 ? sw_s[r]
                                               : __half2float(reinterpret_cast<const __half*>(sw_s)[r + (row0 & 1)]);
                         const int sg = segment_of(a, n);
                         const int64_t Ng = a.off[sg + 1] - a.off[sg];
@@ -693,9 +606,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
                         #pragma unroll
                         for (int m = 0; m < MT; ++m) {
                             if (m < M) {
-                                if constexpr (kG) {
-                                    Yp[m * Ng] = __fmul_rn(part[d][m], sa_r[m]);
-                                } else if constexpr (kW4) {
+                                if constexpr (kW4) {
                                     Yp[m * Ng] = __fmul_rn(__fmul_rn(__int2float_rn(part[d][m]), swv), sa_r[m]);
                                     if (a.acc_out != nullptr) a.acc_out[m * N + n] = part[d][m];
                                 } else {
@@ -745,18 +656,16 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
         const int64_t ng = n - a.off[sg];
         const int64_t Ng = a.off[sg + 1] - a.off[sg];
         float swv = 0.f;
-        if constexpr (kW4 && !kG)
+        if constexpr (kW4)
             swv = static_cast<const float*>(a.wscale[sg])[ng];
-        else if constexpr (!kW4)
+        else
             swv = __half2float(static_cast<const __half*>(a.wscale[sg])[ng]);
         #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m < M) {
                 AccT t = 0;
                 for (int q = 0; q < pl.P; ++q) t += __ldcg(part + ((int64_t)q * M + m) * N + n);
-                if constexpr (kG) {
-                    a.Yg[sg][m * Ng + ng] = __fmul_rn(t, sa_r[m]);
-                } else if constexpr (kW4) {
+                if constexpr (kW4) {
                     a.Yg[sg][m * Ng + ng] = __fmul_rn(__fmul_rn(__int2float_rn(t), swv), sa_r[m]);
                     if (a.acc_out != nullptr) a.acc_out[m * N + n] = t;
                 } else {
@@ -774,9 +683,9 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
 
 // --------------------------------------------------------------- launching
 
-template <bool kW4, int MT, int SMAX, bool kFused, bool kExactS = false, bool kG = false>
+template <bool kW4, int MT, int SMAX, bool kFused, bool kExactS = false>
 static cudaError_t launch_one(const GemvArgs& args, unsigned flags, cudaStream_t stream) {
-    auto* fn = gemv_kernel<kW4, MT, SMAX, kFused, kExactS, kG>;
+    auto* fn = gemv_kernel<kW4, MT, SMAX, kFused, kExactS>;
     static int attr_set[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

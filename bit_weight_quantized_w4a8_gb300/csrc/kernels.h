@@ -34,15 +34,6 @@ cudaError_t launch_w8a16(const GemvPlan& pl, const uint16_t* X, int M, int64_t K
 
 cudaError_t read_and_clear_device_error(unsigned* flags, cudaStream_t stream);
 
-// Group-wise INT4 scales (gemv_group.cu): G weight matrices sharing the
-// activation (G = 1 for a single linear); X (fused) or Xq + sa (unfused).
-cudaError_t launch_w4a8g(const GemvPlan& pl, bool fused, const uint16_t* X, const int8_t* Xq,
-                         const float* sa, int M, int64_t K, int gs, int G,
-                         const uint8_t* const* Wq, const float* const* sg, const int64_t* Ns,
-                         float* const* Y, int8_t* Xq_out, float* sa_out, void* ws,
-                         unsigned flags, cudaStream_t stream);
-// ORs the group-scale kernels' device error word into *flags and clears it.
-cudaError_t read_and_clear_group_error(unsigned* flags, cudaStream_t stream);
 
 // Tensor-core path (mma.cu).  make_mma_plan is host-only and needs no GPU.
 // gkb > 0: group-wise scales, groups of gkb 64-code K blocks (gs = 64 gkb).
@@ -63,7 +54,7 @@ bool make_w4_tile_map(void* map, const uint8_t* Wq, int64_t K, int64_t N);
 
 // Row-per-thread dp4a kernel for small batches (rowdot.cu).
 bool make_rowdot_plan(int M, int64_t K, int64_t N, int num_sms, RowdotPlan* out, int tpr = 0,
-                      int cps = 0, int gshift = -1);
+                      int cps = 0, int gshift = -1, int force_p = 0);
 cudaError_t launch_w4a8_rowdot(const RowdotPlan& pl, const uint16_t* X, const int8_t* Xq,
                                const float* sa, int M, int64_t K, int G, const uint8_t* const* Wq,
                                const float* const* sw, const int64_t* Ns, float* const* Y,

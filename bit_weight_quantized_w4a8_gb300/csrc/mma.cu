@@ -77,6 +77,8 @@ constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffSaSum = kOffMisc + 16;       // e4m3 path: exact code sums of the batch rows
 constexpr int kMmaSmem = kOffSaSum + 256 + 1024;  // + slack to align the base to 1024
 constexpr int kAQThreads = 256;
+// Group scales: the most workspace the chunk sums of a split call may take.
+constexpr size_t kGroupPartBytes = 32u << 20;
 
 static_assert(kWBlocks % kStageK == 0, "stage geometry");
 static_assert(kOffB % 1024 == 0 && kOffW % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -102,11 +104,12 @@ struct MmaArgs {
     int32_t* acc_out;       // optional [M][N]
     int32_t* part;          // [tiles][M][128] int32 accumulators when P > 1 (zeroed by the pre-pass)
     unsigned* tickets;      // [tiles] when P > 1, zero between calls
-    // group scales: sg [N][gld] fp32, gkb K blocks per group; fp32 partials
-    // [tiles][P][M][128] when P > 1
+    // group scales: sg [N][gld] fp32, gkb K blocks per group; with P > 1 the
+    // fold's chunk sums go to part_f [tiles][nch][M][128] (chunks of
+    // max(gkb, 16) K blocks)
     const float* sg;
     float* part_f;
-    int gld, gkb;
+    int gld, gkb, nch;
     int M, N, K, BN, P, nkb, kbp;
     // e4m3 path: the activation pass's per-piece code sums [M][pre_pieces]
     const int32_t* sum_part;
@@ -392,11 +395,15 @@ __device__ __forceinline__ uint2 int4x8_to_e4m3(uint32_t w) {
 // the issue rate of one.
 //
 // kG: group-wise weight scales (groups of gkb K blocks, a whole number of
-// stages).  The MMAs of each group start a fresh accumulator D (exact
-// integer sums); when a group's last stage is committed (dfull), every
-// converter warp folds its share of D into fp32 running sums F in TMEM,
-// F += D * s_g with one fused multiply-add, and releases D (dfree) for the
-// next group.  A converter warp does the readout of a group before it
+// stages; K pieces of whole fold chunks).  The MMAs of each group start a
+// fresh accumulator D (exact integer sums); when a group's last stage is
+// committed (dfull), every converter warp folds its share of D in the fixed
+// order of the group-scale contract: inside each chunk of max(group, 1024)
+// codes f = fma(D, s_g, f) with f in TMEM (F, +0 at the chunk's first
+// group), and at the chunk's last group T = T + f into the thread's
+// registers (one piece: Y = T * s_a at the end), or f to the workspace
+// (split K: the CTA that finishes a tile last adds the chunks in order).
+// Then it releases D (dfree) for the next group.  A converter warp does the readout of a group before it
 // converts the stage `lag` stages past the group's end, so every wait
 // points at earlier work.
 //
@@ -567,30 +574,55 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
         const int q = warp & 3;         // TMEM lanes 32q .. 32q + 31
         const int r = 32 * q + lane;    // weight row within the tile
         const uint32_t lanes = tmem + ((uint32_t)(32 * q) << 16);
-        // group scales: fold group g's sums into F (this warp's lanes, its
-        // column chunks); false when a wait gave up
+        // group scales: fold group g's sums (this warp's lanes, its column
+        // chunks ch = cg + 2j) into the chunk sum f in TMEM, and at a chunk's
+        // last group into the totals T; false when a wait gave up
         int next_g = 0;
         const int ngroups = kG ? nst / spg : 0;
-        auto readout = [&](int g) -> bool {
+        const int gpc = kG ? max(1, 16 / a.gkb) : 1;  // groups per 1024-code (or one-group) chunk
+        float T[kG ? 4 : 1][8];
+        #pragma unroll
+        for (int j = 0; j < (kG ? 4 : 1); ++j)
+            #pragma unroll
+            for (int t = 0; t < 8; ++t) T[j][t] = 0.f;
+        const int g0 = kG ? kb0 / a.gkb : 0;  // first group of the piece (a chunk's first)
+        auto readout = [&](int gl) -> bool {
             const int n = n0 + r;
-            const float sc = n < a.N ? __ldg(a.sg + (int64_t)n * a.gld + kb0 / a.gkb + g) : 0.f;
-            const int b = g % nbuf;
-            if (!__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(dfull + b), (g / nbuf) & 1, abort_flag)))
+            const int g = g0 + gl;  // group index in the row
+            const float sc = n < a.N ? __ldg(a.sg + (int64_t)n * a.gld + g) : 0.f;
+            const int b = gl % nbuf;
+            if (!__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(dfull + b), (gl / nbuf) & 1, abort_flag)))
                 return false;
             tc_fence_after_sync();
-            for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
-                uint32_t d[8], f[8];
-                tmem_ld8(lanes + (uint32_t)(32 * b + 8 * ch), d);
-                if (g > 0) {
-                    tmem_ld8(lanes + kTmemF + (uint32_t)(8 * ch), f);
-                } else {
+            const bool cfirst = (g % gpc) == 0;
+            const bool clast = (g % gpc) == gpc - 1 || gl == ngroups - 1;
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int ch = cg + kConvGroups * j;
+                if (ch < BN / 8) {
+                    uint32_t d[8], f[8];
+                    tmem_ld8(lanes + (uint32_t)(32 * b + 8 * ch), d);
+                    if (!cfirst) {
+                        tmem_ld8(lanes + kTmemF + (uint32_t)(8 * ch), f);
+                    } else {
+                        #pragma unroll
+                        for (int t = 0; t < 8; ++t) f[t] = 0u;
+                    }
                     #pragma unroll
-                    for (int t = 0; t < 8; ++t) f[t] = 0u;
+                    for (int t = 0; t < 8; ++t)  // D holds an exact integer
+                        f[t] = __float_as_uint(__fmaf_rn(__uint_as_float(d[t]), sc, __uint_as_float(f[t])));
+                    if (clast && a.P == 1) {
+                        #pragma unroll
+                        for (int t = 0; t < 8; ++t) T[kG ? j : 0][t] = __fadd_rn(T[kG ? j : 0][t], __uint_as_float(f[t]));
+                    } else if (clast) {
+                        float* dst = a.part_f + ((int64_t)(tile * a.nch + g / gpc) * a.M) * kTileRows + r;
+                        #pragma unroll
+                        for (int t = 0; t < 8; ++t)
+                            if (8 * ch + t < a.M) dst[(int64_t)(8 * ch + t) * kTileRows] = __uint_as_float(f[t]);
+                    } else {
+                        tmem_st8(lanes + kTmemF + (uint32_t)(8 * ch), f);
+                    }
                 }
-                #pragma unroll
-                for (int t = 0; t < 8; ++t)  // D holds an exact integer
-                    f[t] = __float_as_uint(__fmaf_rn(__uint_as_float(d[t]), sc, __uint_as_float(f[t])));
-                tmem_st8(lanes + kTmemF + (uint32_t)(8 * ch), f);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -662,33 +694,34 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
 
         if constexpr (kG) {
             // ---- epilogue, group scales: the remaining groups, then
-            // Y = F * s_a, or this K piece's fp32 partials for the last CTA
+            // Y = T * s_a
             while (next_g < ngroups && readout(next_g)) ++next_g;
             griddep_wait();  // activation scales and outputs
             const bool ok = __all_sync(0xFFFFFFFFu, next_g == ngroups);
             tc_fence_after_sync();
-            const int ct = tid - kFirstConvWarp * 32;
             const int n = n0 + r;
-            for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
-                uint32_t f[8];
-                tmem_ld8(lanes + kTmemF + (uint32_t)(8 * ch), f);
-                if (!ok || n >= a.N) continue;
-                #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const int m = 8 * ch + t;
-                    if (m >= a.M) break;
-                    const float v = __uint_as_float(f[t]);
-                    if (a.P == 1)
-                        a.Y[(int64_t)m * a.N + n] = __fmul_rn(v, a.sa[m]);
-                    else
-                        a.part_f[(((int64_t)tile * a.P + p) * a.M + m) * kTileRows + r] = v;
+            if (a.P == 1) {
+                if (ok && n < a.N) {
+                    #pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int ch = cg + kConvGroups * j;
+                        if (ch < BN / 8) {
+                            #pragma unroll
+                            for (int t = 0; t < 8; ++t) {
+                                const int m = 8 * ch + t;
+                                if (m < a.M) a.Y[(int64_t)m * a.N + n] = __fmul_rn(T[j][t], a.sa[m]);
+                            }
+                        }
+                    }
                 }
-            }
-            if (a.P > 1) {
-                // the last CTA of the tile adds the pieces' partials in piece order
+            } else {
+                // the last CTA of the tile adds the chunk sums in chunk order;
+                // every converter warp meets at the barrier, and after a wait
+                // gave up (the CTA's abort flag) nothing is written
+                const int ct = tid - kFirstConvWarp * 32;
                 __threadfence();
                 named_bar_sync(1, kConvWarps * 32);
-                if (ct == 0) *last_flag = (atomicAdd(a.tickets + tile, 1u) == (unsigned)(a.P - 1));
+                if (ct == 0) *last_flag = !*abort_flag && (atomicAdd(a.tickets + tile, 1u) == (unsigned)(a.P - 1));
                 named_bar_sync(1, kConvWarps * 32);
                 if (*last_flag) {
                     __threadfence();
@@ -696,9 +729,18 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                     for (int e = ct; e < a.M * kTileRows; e += kConvWarps * 32) {
                         const int m = e / kTileRows, rr = e % kTileRows;
                         if (rr >= rows) continue;
+                        const float* src = a.part_f + ((int64_t)tile * a.nch * a.M + m) * kTileRows + rr;
+                        // chunk order; loads issued 8 at a time ahead of the adds
                         float t = 0.f;
-                        for (int pp = 0; pp < a.P; ++pp)
-                            t += __ldcg(a.part_f + (((int64_t)tile * a.P + pp) * a.M + m) * kTileRows + rr);
+                        for (int c0 = 0; c0 < a.nch; c0 += 8) {
+                            float v[8];
+                            #pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                v[k] = c0 + k < a.nch ? __ldcg(src + (int64_t)(c0 + k) * a.M * kTileRows) : 0.f;
+                            #pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                if (c0 + k < a.nch) t = __fadd_rn(t, v[k]);
+                        }
                         a.Y[(int64_t)m * a.N + n0 + rr] = __fmul_rn(t, a.sa[m]);
                     }
                     if (ct == 0) a.tickets[tile] = 0u;  // ready for the next call
@@ -867,13 +909,21 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int g
     if (pl.tiles < slots * 4 / 5) P = slots / pl.tiles;
     if (P < 1) P = 1;
     // row-wise scales: pieces of at most 256 K blocks keep the integer sums
-    // exact; group scales: each group's D is exact on its own
+    // exact; group scales: each group's D is exact on its own, pieces hold
+    // whole fold chunks (max(gkb, 16) K blocks), and a split writes one fp32
+    // chunk sum per output and chunk, allowed up to kGroupPartBytes
     const int pmin = gkb ? 1 : (pl.nkb + 255) / 256;
     if (P < pmin) P = pmin;
+    const int cb = gkb > 16 ? gkb : 16;             // K blocks per fold chunk
+    const int nch = gkb ? (pl.nkb + cb - 1) / cb : 0;
+    if (gkb) {
+        if (P > nch) P = nch;
+        if ((size_t)pl.tiles * nch * M * kTileRows * 4 > kGroupPartBytes) P = 1;
+    }
     if (P > pl.nkb) P = pl.nkb;
     if (P > 64) P = 64;
-    // pieces of whole weight loads (kWBlocks K blocks) and whole groups, none empty
-    const int align = gkb > kWBlocks ? gkb : kWBlocks;
+    // pieces of whole weight loads (kWBlocks K blocks) and whole fold chunks, none empty
+    const int align = gkb ? cb : kWBlocks;
     pl.kbp = (pl.nkb + P - 1) / P;
     pl.kbp = (pl.kbp + align - 1) / align * align;
     pl.P = (pl.nkb + pl.kbp - 1) / pl.kbp;
@@ -897,9 +947,14 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int g
     pl.off_part = round_up_sz(pl.off_codes + (size_t)((pl.nkb + 1) / 2 * 2) * pl.BN * kKBlock * 2, 256);
     const int64_t small = 2 * num_sms * 4 / 5;
     const int64_t tmax = pmin > 1 ? pl.tiles : (pl.tiles < small ? pl.tiles : small);
-    // group scales: fp32 partials per tile and piece; a matrix split into
-    // P pieces has tiles * P <= the 2 * SMs CTA slots
-    const size_t part = gkb ? (size_t)(2 * num_sms) * M * kTileRows * 4 : (size_t)tmax * M * kTileRows * 4;
+    // group scales: the chunk sums of a split matrix (a split needs fewer
+    // tiles than 4/5 of the CTA slots and at most kGroupPartBytes of sums)
+    size_t part = (size_t)tmax * M * kTileRows * 4;
+    if (gkb) {
+        const size_t tb = (size_t)(pl.tiles < small ? pl.tiles : small);
+        part = nch > 1 ? tb * nch * M * kTileRows * 4 : 0;
+        if (part > kGroupPartBytes) part = kGroupPartBytes;
+    }
     pl.ws_bytes = pl.off_part + round_up_sz(part, 256);
     *out = pl;
     return true;
@@ -922,7 +977,9 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
         int Mi = M, BNi = pl.BN;
         int64_t Kk = K;
         int32_t* acc = reinterpret_cast<int32_t*>(wsb + pl.off_part);
-        int64_t acc_words = (int64_t)((pl.ws_bytes - pl.off_part) / 4);
+        // row-wise split plans accumulate int32 partials with atomics: zeroed here
+        // (group scales write their chunk sums whole)
+        int64_t acc_words = gkb ? 0 : (int64_t)((pl.ws_bytes - pl.off_part) / 4);
         int32_t* sum_part = reinterpret_cast<int32_t*>(wsb + pl.off_sum);
         void* args[] = {&xh, &Xq, &sa, &Mi, &Kk, &BNi, &codes, &sa_ws, &Xq_out, &sa_out, &acc, &acc_words,
                         &sum_part};
@@ -962,6 +1019,7 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
             a.gld = (int)((K / gs + 3) / 4 * 4);
             a.gkb = gkb;
             a.part_f = reinterpret_cast<float*>(wsb + pg.off_part);
+            a.nch = (pg.nkb + (gkb > 16 ? gkb : 16) - 1) / (gkb > 16 ? gkb : 16);
         }
         a.sa = sa_ws;
         a.Y = Y[g];

@@ -46,9 +46,6 @@ struct GemvPlan {
     int stage_stride;  // bytes per ring stage (multiple of 128)
     int cps;           // CTAs per SM the grid was sized for
     int x_bytes;       // staged activation row (0: read from global memory)
-    int gwin;          // group scales: widest scale window of a K piece (floats)
-    int gstage;        // group scales: bytes of one slot's scale area (0: none)
-    int off_gsc;       // group scales: the NS slots' scale areas
     int off_bars, off_sw, off_x, off_act, off_red, off_max, off_flag;
     int smem;          // dynamic shared memory bytes
     size_t ws_bytes;   // workspace: kTicketBytes of counters + [P][M][N] x 4
@@ -79,32 +76,14 @@ inline size_t round_up_sz(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 inline int mt_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 
-// Widest window of group scales (floats, whole 16-byte words) any K piece of
-// the plan reads: groups of 2^gshift granules, scale rows of gld floats.
-inline int group_window_max(const GemvPlan& pl, int gshift, int gld) {
-    int w = 0;
-    for (int p = 0; p < pl.P; ++p) {
-        const int g0 = p * pl.Gq;
-        const int gp = pl.Gt - g0 < pl.Gq ? pl.Gt - g0 : pl.Gq;
-        const int gb = (g0 >> gshift) & ~3;
-        int ge = (((g0 + gp - 1) >> gshift) + 4) & ~3;
-        if (ge > gld) ge = gld;
-        if (ge - gb > w) w = ge - gb;
-    }
-    return w;
-}
-
 // Builds the plan; returns false when no valid plan exists for the shape.
 // w4: INT4 weights (32 codes per granule) else INT8 (16 per granule).
-// gshift >= 0: INT4 with one scale per 2^gshift granules along K, scale rows
-// of gld floats (a multiple of 4); -1: one scale per row.
 // pair: the rows come in pairs (the gated product of gate/up rows 2i, 2i+1)
 // and every CTA takes whole pairs.
 inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int num_sms,
-                           const Tuning& tu, GemvPlan* out, int gshift = -1, int gld = 0,
+                           const Tuning& tu, GemvPlan* out,
                            bool pair = false) {
     if (pair && (N < 2 || N % 2)) return false;
-    if (gshift >= 0 && (!w4 || gld <= 0 || gld % 4)) return false;
     GemvPlan pl = {};
     pl.MT = mt_of(M);
     pl.smax = 8 / pl.MT;  // 8 activation registers per granule and row (W4 codes, W8 binary16 pairs)
@@ -180,11 +159,7 @@ inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int
     if (NS < 2) NS = 2;
     if (NS > 16) NS = 16;
 
-    const int sw_bytes = (pl.P == 1 && gshift < 0) ? round_up(pl.rows_max * 4 + 8, 16) : 0;
-    if (gshift >= 0) {
-        pl.gwin = group_window_max(pl, gshift, gld);
-        pl.gstage = round_up(pl.Rl * pl.gwin * 4, 128);
-    }
+    const int sw_bytes = pl.P == 1 ? round_up(pl.rows_max * 4 + 8, 16) : 0;
     const int act_bytes = (w4 && fused) ? round_up(pl.MT * pl.Gq * 32, 128) : 0;
     // the K piece of the activation rows a W8 CTA reads, staged once per CTA
     const int w8_x = w4 ? 0 : M * pl.Gq * kGranBytes * 2;
@@ -197,8 +172,6 @@ inline bool make_gemv_plan(bool w4, bool fused, int M, int64_t K, int64_t N, int
     const int limit = (pl.cps >= 2) ? kMaxSmem2 : kMaxSmem;
     for (;; --NS) {
         int off = NS * pl.stage_stride;
-        pl.off_gsc = off;
-        off += NS * pl.gstage;
         pl.off_bars = off;
         off += NS * 8 + 8 + NS * 4;  // full[NS], scale-cache mbarrier, released[NS]
         pl.off_sw = round_up(off, 16);

@@ -95,6 +95,10 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Programmatic dependent launch: block until the preceding kernel on the
 // stream has completed and its writes are visible (no-op without PDL).
 __device__ __forceinline__ void griddep_wait() {

@@ -36,9 +36,10 @@
 //    once; each thread group accumulates its row's dot products with all
 //    MT batch rows; pieces are summed in int32 by the CTA that finishes a
 //    tile last (exact, so the result is bit-identical to the integer
-//    definition whatever the split).  With group-wise scales (kG) every
-//    32-code granule's exact sum is folded into an fp32 sum with its group
-//    scale (staged per CTA), and the sums are added in a fixed order.
+//    definition whatever the split).
+//  * rowdot_group_kernel<MT> (group-wise scales, 1..8 batch rows): one
+//    thread per weight row, so that each row's per-group sums are folded by
+//    one thread in the fixed order of the group-scale contract (below).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -75,13 +76,30 @@ struct RowdotArgs {
     const float* sa;        // [M]
     float* Y;               // [M][N]
     int32_t* acc_out;       // optional [M][N]
-    int32_t* part;          // [tiles][P][M][128] piece sums when P > 1 (int32; fp32 with group scales)
+    int32_t* part;          // [tiles][P][M][128] piece sums when P > 1 (int32)
     unsigned* tickets;      // [tiles] when P > 1, zero between calls
-    // group scales: sg [N][gld] fp32, one per 2^gshift codes, ngroups = K >> gshift;
-    // a piece's window of gwin groups is staged per CTA as [128][gstride]
-    const float* sg;
-    int gshift, gld, ngroups, gwin, gstride;
     int M, N, nbox, bpp, P, NS;
+};
+
+// Group-wise scales: up to kGroupMats weight matrices reading the same
+// activation in one launch; their 128-row tiles are numbered consecutively
+// (matrix g owns tiles tile0[g] .. tile0[g + 1] - 1).
+constexpr int kGroupMats = 4;
+constexpr int kMaxPhases = 4;
+struct GroupArgs {
+    CUtensorMap tmW[kGroupMats];  // packed weights [N_g][K/2], box 128 bytes x 128 rows, 128B swizzle
+    const float* sg[kGroupMats];  // [N_g][gld] fp32, one scale per 2^gshift codes
+    float* Y[kGroupMats];         // [M][N_g]
+    int N[kGroupMats];
+    int tile0[kGroupMats + 1];    // unused matrices: tile0[g] = tile0[G]
+    const uint8_t* codes;         // activation codes [nbox][8][M][32 bytes]
+    const float* sa;              // [M]
+    float* part_f;                // [tiles][nch][M][128] chunk sums when P > 1
+    unsigned* tickets;            // [tiles] when P > 1, zero between calls
+    int gshift, gld, ngroups;     // ngroups = K >> gshift
+    int lshift, nch, abox;        // chunks of 2^lshift = max(group, 1024) codes, abox boxes each
+    int K, M, nbox, bpp, P, NS;
+    int nph;                      // thread phases (128 threads each), 1, 2 or 4
 };
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -91,6 +109,26 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
         #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(&g_rowdot_error, kErrFullWait);
+            return false;
+        }
+    }
+}
+
+// Waits (bounded) until ring slot `slot` holds the fill of box i: the
+// thread phases of the group-scale kernel consume boxes out of order, and a
+// barrier's parity alone cannot tell fill i from the fill two before it.
+// last_box[slot] is the box whose fill was last issued into the slot.
+__device__ __forceinline__ bool wait_slot_box(volatile int* last_box, int i, volatile int* abort_flag) {
+    if (*last_box == i) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        #pragma unroll 1
+        for (int k = 0; k < 32; ++k)
+            if (*last_box == i) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
@@ -164,10 +202,9 @@ __global__ void __launch_bounds__(kPreThreads) rowdot_codes_kernel(
 
 // Shared memory (base aligned to 1024 for the swizzled boxes): the weight
 // ring [NS][16384], the piece's activation codes [bpp][8][MT][32 bytes], the
-// cross-warp sums [TPR - 1][MT][128] (int32; fp32 with group scales), with
-// group scales the piece's scale window [128][gstride] fp32, NS + 1 mbarriers
-// (ring slots, activations), and per slot the number of warps done with it
-// and the last box copied into it.
+// cross-warp sums [TPR - 1][MT][128] int32, NS + 1 mbarriers (ring slots,
+// activations), and per slot the number of warps done with it and the last
+// box copied into it.
 //
 // Thread mapping: warp w takes the 16-byte chunks c = w / 4 + TPR * i of
 // every 128-byte box row, lane l the weight row r = (w % 4) * 32 + l.  With
@@ -175,13 +212,7 @@ __global__ void __launch_bounds__(kPreThreads) rowdot_codes_kernel(
 // * 16)) the eight lanes of each quarter-warp read eight different bank
 // groups (conflict-free), and every activation load of a warp is one
 // address (a broadcast).
-//
-// kG (group-wise scales, groups of 2^gshift >= 32 codes): a 32-code chunk is
-// one granule of one group; its exact int32 sum v is folded into an fp32 sum
-// per batch row with one fma(v, s_g, sum), the four threads of a row add
-// their fp32 sums in a fixed order, pieces add theirs in piece order, and
-// the result is multiplied by s_a.
-template <int MT, int TPR, bool kG>
+template <int MT, int TPR>
 __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_constant__ RowdotArgs a) {
     constexpr int kThreads = kTile * TPR;
     constexpr int kWarps = kThreads / 32;
@@ -195,8 +226,7 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
     uint8_t* ring = smem;
     uint8_t* act = smem + NS * kBoxBytes;
     int* red = reinterpret_cast<int*>(act + a.bpp * kBoxAct);
-    float* sgs = reinterpret_cast<float*>(red + (TPR - 1) * MT * kTile);  // group scales
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sgs + (kG ? kTile * a.gstride : 0));  // full[NS], activations
+    uint64_t* bars = reinterpret_cast<uint64_t*>(red + (TPR - 1) * MT * kTile);  // full[NS], activations
     int* released = reinterpret_cast<int*>(bars + NS + 1);
     int* last_box = released + NS;
     volatile int* abort_flag = last_box + NS;
@@ -209,7 +239,6 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
     const int t = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint64_t pol = l2_evict_first_policy();
-    const int g0 = kG ? (box0 * kBoxCodes) >> a.gshift : 0;  // first group of the piece
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -232,18 +261,6 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
             last_box[i] = i;
         }
     }
-    if constexpr (kG) {
-        // the piece's scale window; zero for rows past N and groups past K
-        for (int e = tid; e < kTile * a.gwin; e += kThreads) {
-            const int rr = e / a.gwin, j = e - rr * a.gwin;
-            const int64_t n = (int64_t)tile * kTile + rr;
-            float* dst = sgs + rr * a.gstride + j;
-            if (n < a.N && g0 + j < a.ngroups)
-                cp_async_4(smem_u32(dst), a.sg + n * a.gld + g0 + j);
-            else
-                *dst = 0.f;
-        }
-    }
     griddep_wait();  // activation codes, scales, outputs and workspace from here on
     if (tid == 0) {
         const uint32_t bytes = (uint32_t)nb * kBoxAct;
@@ -251,23 +268,18 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
         bulk_g2s(smem_u32(act), reinterpret_cast<const uint8_t*>(a.codes) + (int64_t)box0 * kBoxAct, bytes,
                  smem_u32(bars + NS), l2_evict_last_policy());
     }
-    if constexpr (kG) {
-        cp_async_wait_all();
-        __syncthreads();
-    }
 
     int acc[MT][2];  // 16 x the even / odd products of each batch row
-    float gacc[kG ? MT : 1];  // group scales: fp32 sums of scaled granules
     #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = 0;
-    #pragma unroll
-    for (int m = 0; m < (kG ? MT : 1); ++m) gacc[m] = 0.f;
     const uint8_t* wrow = ring + r * 128;
-    bool ok = wait_bounded(smem_u32(bars + NS), 0, abort_flag);
+    // waits end with a warp-uniform outcome (a lane may time out while
+    // another sees the phase), so the warp's __syncwarp below never splits
+    bool ok = __all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(bars + NS), 0, abort_flag));
     int slot = 0;
     uint32_t ph = 0;
     for (int i = 0; ok && i < nb; ++i) {
-        if (!wait_bounded(smem_u32(bars + slot), ph, abort_flag)) break;
+        if (!__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(bars + slot), ph, abort_flag))) break;
         uint4 wv[CPT];
         #pragma unroll
         for (int ci = 0; ci < CPT; ++ci) {
@@ -305,10 +317,6 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
                 lo[j] = (int)((w[j] << 4) & 0xF0F0F0F0u);
                 hi[j] = (int)(w[j] & 0xF0F0F0F0u);
             }
-            if constexpr (kG) {
-                #pragma unroll
-                for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = 0;
-            }
             #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 const uint4 a0 = *reinterpret_cast<const uint4*>(ac + m * 32);
@@ -322,28 +330,14 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
                 acc[m][0] = __dp4a(lo[3], (int)a1.z, acc[m][0]);
                 acc[m][1] = __dp4a(hi[3], (int)a1.w, acc[m][1]);
             }
-            if constexpr (kG) {
-                // the granule's group scale; |v| <= 1016 * 32 is exact in fp32
-                const int g = (((box0 + i) * kBoxCodes + c * 32) >> a.gshift) - g0;
-                const float sgv = sgs[r * a.gstride + g];
-                #pragma unroll
-                for (int m = 0; m < MT; ++m)
-                    gacc[m] = __fmaf_rn(__int2float_rn((acc[m][0] >> 4) + (acc[m][1] >> 4)), sgv, gacc[m]);
-            }
         }
     }
 
-    // The row's sums: integers (the two dp4a sums are 16 x integers), or fp32
-    // with group scales; the warps of chunk phases t > 0 hand theirs to
-    // phase 0, which adds them in phase order.
+    // The row's sums (the two dp4a sums are 16 x integers); the warps of
+    // chunk phases t > 0 hand theirs to phase 0, which adds them.
     int v[MT];
-    if constexpr (kG) {
-        #pragma unroll
-        for (int m = 0; m < MT; ++m) v[m] = __float_as_int(gacc[m]);
-    } else {
-        #pragma unroll
-        for (int m = 0; m < MT; ++m) v[m] = (acc[m][0] >> 4) + (acc[m][1] >> 4);
-    }
+    #pragma unroll
+    for (int m = 0; m < MT; ++m) v[m] = (acc[m][0] >> 4) + (acc[m][1] >> 4);
     if (t > 0) {
         #pragma unroll
         for (int m = 0; m < MT; ++m) red[((t - 1) * MT + m) * kTile + r] = v[m];
@@ -362,26 +356,18 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
         for (int tt = 1; tt < TPR; ++tt) {
             #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                const int o = red[((tt - 1) * MT + m) * kTile + r];
-                if constexpr (kG)
-                    v[m] = __float_as_int(__fadd_rn(__int_as_float(v[m]), __int_as_float(o)));
-                else
-                    v[m] += o;
+                v[m] += red[((tt - 1) * MT + m) * kTile + r];
             }
         }
     }
     const int n = tile * kTile + r;
     if (a.P == 1) {
         if (t == 0 && n < a.N) {
-            const float swv = kG ? 0.f : a.sw[n];
+            const float swv = a.sw[n];
             #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                if constexpr (kG) {
-                    a.Y[(int64_t)m * a.N + n] = __fmul_rn(__int_as_float(v[m]), a.sa[m]);
-                } else {
-                    a.Y[(int64_t)m * a.N + n] = __fmul_rn(__fmul_rn(__int2float_rn(v[m]), swv), a.sa[m]);
-                    if (a.acc_out != nullptr) a.acc_out[(int64_t)m * a.N + n] = v[m];
-                }
+                a.Y[(int64_t)m * a.N + n] = __fmul_rn(__fmul_rn(__int2float_rn(v[m]), swv), a.sa[m]);
+                if (a.acc_out != nullptr) a.acc_out[(int64_t)m * a.N + n] = v[m];
             }
         }
         return;
@@ -403,19 +389,274 @@ __global__ void __launch_bounds__(kTile * TPR) rowdot_kernel(const __grid_consta
     for (int e = tid; e < MT * kTile; e += kThreads) {
         const int m = e / kTile, rr = e % kTile, nn = tile * kTile + rr;
         if (nn >= a.N) continue;
-        if constexpr (kG) {
-            float sum = 0.f;
-            for (int q = 0; q < a.P; ++q)
-                sum = __fadd_rn(sum, __int_as_float(__ldcg(src + (int64_t)q * MT * kTile + e)));
-            a.Y[(int64_t)m * a.N + nn] = __fmul_rn(sum, a.sa[m]);
-        } else {
-            int32_t sum = 0;
-            for (int q = 0; q < a.P; ++q) sum += __ldcg(src + (int64_t)q * MT * kTile + e);
-            a.Y[(int64_t)m * a.N + nn] = __fmul_rn(__fmul_rn(__int2float_rn(sum), a.sw[nn]), a.sa[m]);
-            if (a.acc_out != nullptr) a.acc_out[(int64_t)m * a.N + nn] = sum;
-        }
+        int32_t sum = 0;
+        for (int q = 0; q < a.P; ++q) sum += __ldcg(src + (int64_t)q * MT * kTile + e);
+        a.Y[(int64_t)m * a.N + nn] = __fmul_rn(__fmul_rn(__int2float_rn(sum), a.sw[nn]), a.sa[m]);
+        if (a.acc_out != nullptr) a.acc_out[(int64_t)m * a.N + nn] = sum;
     }
     if (tid == 0) a.tickets[tile] = 0u;  // ready for the next call
+}
+
+// Group-wise scales (groups of gs = 2^gshift codes, 32 <= gs <= K): the
+// order of the fp32 arithmetic is fixed by K and gs alone, so the result is
+// the same bits whatever the launch plan:
+//   acc_g = the exact int32 sum of group g,
+//   per chunk of L = max(gs, 1024) codes: f = +0, then for its groups in
+//   ascending order f = fma((float)acc_g, s_g, f),
+//   T = +0, then for the chunks in ascending order T = T + f,
+//   Y = T * s_a.
+// Each chunk of a weight row is walked in K order by one thread, so its
+// fold needs no exchange: a CTA has nph phases of 128 threads (one per
+// weight row), phase h taking the piece's chunks h, h + nph, ...; each
+// thread reads all eight 16-byte chunks of its row from every box of its
+// chunks (the swizzle keeps a quarter-warp's eight lanes on eight bank
+// groups).  A ring slot holds a box of weights and that box's activation
+// codes ([8][MT][32 bytes], one bulk copy on the same mbarrier), so no
+// piece length limit comes from the activations.  The chunk sums go to T
+// in registers (one phase, one piece), to shared memory for phase 0 to add
+// in chunk order (several phases, one piece), or to the workspace for the
+// CTA that finishes a tile last (K split into pieces of whole chunks).
+// The group scales are read from global memory one box ahead (prefetched
+// into L1 for the whole piece).
+template <int MT>
+__global__ void __launch_bounds__(kTile * kMaxPhases, 1) rowdot_group_kernel(const __grid_constant__ GroupArgs a) {
+    constexpr int kWarps = kTile / 32;  // warps of one phase
+    constexpr int kChunkAct = MT * 32;
+    constexpr int kBoxAct = 8 * kChunkAct;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const int NS = a.NS;
+    const int cpp = a.bpp / a.abox;                                // chunks per piece
+    uint8_t* ring = smem;                                          // [NS][16384] weights
+    uint8_t* acts = smem + NS * kBoxBytes;                         // [NS][kBoxAct] codes
+    float* cval = reinterpret_cast<float*>(acts + NS * kBoxAct);   // [MT][cpp][128] when nph > 1, P == 1
+    uint64_t* bars = reinterpret_cast<uint64_t*>(cval + (a.nph > 1 && a.P == 1 ? MT * cpp * kTile : 0));
+    int* released = reinterpret_cast<int*>(bars + NS);
+    volatile int* last_box = released + NS;  // box of each slot's latest fill
+    volatile int* abort_flag = last_box + NS;
+    int* last_flag = const_cast<int*>(last_box) + NS + 1;
+
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int r = tid & (kTile - 1);  // weight row within the tile
+    const int ph = tid / kTile;       // phase: chunks ph, ph + nph, ... of the piece
+    const int nph = a.nph;
+    const int tg = blockIdx.x / a.P, p = blockIdx.x % a.P;  // tile of all matrices, K piece
+    int g = 0;
+    #pragma unroll
+    for (int k = 1; k < kGroupMats; ++k) g += (tg >= a.tile0[k]) ? 1 : 0;
+    const int tile = tg - a.tile0[g];  // tile within matrix g
+    const CUtensorMap* tmW = &a.tmW[g];
+    const int Ng = a.N[g];
+    const int box0 = p * a.bpp;
+    const int nb = min(a.bpp, a.nbox - box0);
+    const uint64_t pol = l2_evict_first_policy();
+    const uint64_t pol_act = l2_evict_last_policy();
+    const uint8_t* codes = a.codes;
+    const int64_t n = (int64_t)tile * kTile + r;
+    const bool row_ok = n < Ng;
+    const float* srow = a.sg[g] + (row_ok ? n : 0) * a.gld;
+    const int gmask = (1 << a.gshift) - 1;
+    const int lmask = (1 << a.lshift) - 1;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(smem_u32(bars + s), 1);
+            released[s] = 0;
+            last_box[s] = -1;
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+    const int n0 = min(NS, nb);
+    if (tid == 0) {  // the weights do not depend on earlier launches
+        for (int i = 0; i < n0; ++i) {
+            mbar_arrive_expect_tx(smem_u32(bars + i), kBoxBytes + kBoxAct);
+            tma_load_2d_hint(smem_u32(ring + i * kBoxBytes), tmW, (box0 + i) * (kBoxCodes / 2),
+                             tile * kTile, smem_u32(bars + i), pol);
+            last_box[i] = i;
+        }
+    }
+    // the boxes of this phase: i = abox * (chunk) + j for chunks ph, ph + nph, ...
+    auto next_box = [&](int i) { return (i + 1) % a.abox ? i + 1 : i + 1 + (nph - 1) * a.abox; };
+    // the row's scales for the piece into L1 (128-byte lines), so that the
+    // loads one box ahead hit it
+    if (ph == 0) {
+        const int ga = min((box0 * kBoxCodes) >> a.gshift, a.ngroups - 1);
+        const int gb = min(((box0 + nb) * kBoxCodes - 1) >> a.gshift, a.ngroups - 1);
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(srow + ga) & ~(uintptr_t)127;
+        const uintptr_t hi = reinterpret_cast<uintptr_t>(srow + gb);
+        for (uintptr_t q = lo; q <= hi; q += 128) prefetch_l1(reinterpret_cast<const void*>(q));
+    }
+    // scales of the groups holding the 8 chunks of box i (rows past N read
+    // row 0's and write nothing; chunks past K clamp to the last group)
+    auto load_scales = [&](int i, float* sc) {
+        #pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int gi = min(((box0 + i) * kBoxCodes + 32 * c) >> a.gshift, a.ngroups - 1);
+            sc[c] = __ldg(srow + gi);
+        }
+    };
+    const int i_first = ph * a.abox;
+    float sc[8];
+    load_scales(min(i_first, nb - 1), sc);
+    griddep_wait();  // activation codes, outputs and workspace from here on
+    if (tid == 0) {
+        for (int i = 0; i < n0; ++i)
+            bulk_g2s(smem_u32(acts + i * kBoxAct), codes + (int64_t)(box0 + i) * kBoxAct, kBoxAct,
+                     smem_u32(bars + i), pol_act);
+    }
+
+    int acc[MT][2];  // 16 x the even / odd products of the current group
+    float f[MT], T[MT];
+    #pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        acc[m][0] = acc[m][1] = 0;
+        f[m] = 0.f;
+        T[m] = 0.f;
+    }
+    const uint8_t* wrow = ring + r * 128;
+    for (int i = i_first; i < nb; i = next_box(i)) {
+        const int slot = i % NS;
+        float scn[8];
+        const int in = next_box(i);
+        load_scales(in < nb ? in : i, scn);
+        // the slot must hold box i's fill before its parity means anything;
+        // warp-uniform outcome, so the warp's __syncwarp below never splits
+        if (!__all_sync(0xFFFFFFFFu, wait_slot_box(last_box + slot, i, abort_flag) &&
+                                         wait_bounded(smem_u32(bars + slot), (uint32_t)(i / NS) & 1u, abort_flag)))
+            break;
+        uint4 wv[8];
+        #pragma unroll
+        for (int c = 0; c < 8; ++c)
+            wv[c] = *reinterpret_cast<const uint4*>(wrow + slot * kBoxBytes + ((c ^ (r & 7)) << 4));
+        const uint8_t* ab = acts + slot * kBoxAct;
+        const int pos = (box0 + i) * kBoxCodes;  // first code of the box
+        #pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint8_t* ac = ab + c * kChunkAct;
+            const uint32_t w[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
+            int lo[4], hi[4];
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                lo[j] = (int)((w[j] << 4) & 0xF0F0F0F0u);
+                hi[j] = (int)(w[j] & 0xF0F0F0F0u);
+            }
+            #pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const uint4 a0 = *reinterpret_cast<const uint4*>(ac + m * 32);
+                const uint4 a1 = *reinterpret_cast<const uint4*>(ac + m * 32 + 16);
+                acc[m][0] = __dp4a(lo[0], (int)a0.x, acc[m][0]);
+                acc[m][1] = __dp4a(hi[0], (int)a0.y, acc[m][1]);
+                acc[m][0] = __dp4a(lo[1], (int)a0.z, acc[m][0]);
+                acc[m][1] = __dp4a(hi[1], (int)a0.w, acc[m][1]);
+                acc[m][0] = __dp4a(lo[2], (int)a1.x, acc[m][0]);
+                acc[m][1] = __dp4a(hi[2], (int)a1.y, acc[m][1]);
+                acc[m][0] = __dp4a(lo[3], (int)a1.z, acc[m][0]);
+                acc[m][1] = __dp4a(hi[3], (int)a1.w, acc[m][1]);
+            }
+            const int end = pos + 32 * (c + 1);  // codes done after this chunk
+            if ((end & gmask) == 0 && end <= a.K) {  // a group ends (uniform over the CTA)
+                #pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    f[m] = __fmaf_rn(__int2float_rn((acc[m][0] >> 4) + (acc[m][1] >> 4)), sc[c], f[m]);
+                    acc[m][0] = acc[m][1] = 0;
+                }
+                if ((end & lmask) == 0 || end == a.K) {  // so does a fold chunk
+                    if (a.P == 1 && nph == 1) {
+                        #pragma unroll
+                        for (int m = 0; m < MT; ++m) T[m] = __fadd_rn(T[m], f[m]);
+                    } else if (a.P == 1) {
+                        const int cl = i / a.abox;  // chunk within the piece
+                        #pragma unroll
+                        for (int m = 0; m < MT; ++m) cval[(m * cpp + cl) * kTile + r] = f[m];
+                    } else {
+                        float* dst = a.part_f + ((int64_t)(tg * a.nch + ((end - 1) >> a.lshift)) * MT) * kTile + r;
+                        #pragma unroll
+                        for (int m = 0; m < MT; ++m) dst[m * kTile] = f[m];
+                    }
+                    #pragma unroll
+                    for (int m = 0; m < MT; ++m) f[m] = 0.f;
+                }
+            }
+        }
+        #pragma unroll
+        for (int c = 0; c < 8; ++c) sc[c] = scn[c];
+        __syncwarp();
+        if (lane == 0) {
+            // the last of the phase's warps done with this slot (weights and
+            // codes) refills it with the box NS further on
+            __threadfence_block();
+            if (atomicAdd(released + slot, 1) == kWarps - 1) {
+                released[slot] = 0;
+                __threadfence_block();
+                if (i + NS < nb && !*abort_flag) {
+                    const uint32_t bar = smem_u32(bars + slot);
+                    mbar_arrive_expect_tx(bar, kBoxBytes + kBoxAct);
+                    tma_load_2d_hint(smem_u32(ring + slot * kBoxBytes), tmW, (box0 + i + NS) * (kBoxCodes / 2),
+                                     tile * kTile, bar, pol);
+                    bulk_g2s(smem_u32(acts + slot * kBoxAct), codes + (int64_t)(box0 + i + NS) * kBoxAct, kBoxAct,
+                             bar, pol_act);
+                    last_box[slot] = i + NS;  // box i's fill is consumed: the parity now tracks box i + NS
+                    __threadfence_block();
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag && tid == 0) {
+        // copies may still be landing after an abandoned wait: wait for the
+        // last one of each slot (bounded) so none writes shared memory after exit
+        for (int s = 0; s < NS; ++s)
+            if (last_box[s] >= 0 && !mbar_wait(smem_u32(bars + s), (uint32_t)(last_box[s] / NS) & 1u))
+                atomicOr(&g_rowdot_error, kErrDrainWait);
+    }
+    if (*abort_flag) return;
+    float* Y = a.Y[g];
+    if (a.P == 1) {
+        if (ph == 0 && row_ok) {
+            #pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float t = T[m];
+                if (nph > 1) {  // the phases' chunk sums, in chunk order
+                    t = 0.f;
+                    for (int cl = 0; cl < cpp; ++cl) t = __fadd_rn(t, cval[(m * cpp + cl) * kTile + r]);
+                }
+                Y[(int64_t)m * Ng + n] = __fmul_rn(t, a.sa[m]);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------ split K: the last CTA adds the chunks
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) *last_flag = (atomicAdd(a.tickets + tg, 1u) == (unsigned)(a.P - 1));
+    __syncthreads();
+    if (!*last_flag) return;
+    __threadfence();
+    if (ph == 0 && row_ok) {
+        // chunk sums in chunk order; loads issued 8 at a time ahead of the adds
+        const float* src = a.part_f + (int64_t)tg * a.nch * MT * kTile + r;
+        #pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            float t = 0.f;
+            for (int c0 = 0; c0 < a.nch; c0 += 8) {
+                float v[8];
+                #pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    v[k] = c0 + k < a.nch ? __ldcg(src + ((int64_t)(c0 + k) * MT + m) * kTile) : 0.f;
+                #pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (c0 + k < a.nch) t = __fadd_rn(t, v[k]);
+            }
+            Y[(int64_t)m * Ng + n] = __fmul_rn(t, a.sa[m]);
+        }
+    }
+    if (tid == 0) a.tickets[tg] = 0u;  // ready for the next call
 }
 
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
@@ -435,32 +676,47 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-template <int MT, int TPR, bool kG>
+template <int MT, int TPR>
 const void* kernel_for() {
-    return reinterpret_cast<const void*>(rowdot_kernel<MT, TPR, kG>);
+    return reinterpret_cast<const void*>(rowdot_kernel<MT, TPR>);
 }
 
-template <int TPR, bool kG>
+template <int TPR>
 const void* kernel_for_rows(int M) {
     switch (M) {
-        case 2: return kernel_for<2, TPR, kG>();
-        case 3: return kernel_for<3, TPR, kG>();
-        case 4: return kernel_for<4, TPR, kG>();
-        case 5: return kernel_for<5, TPR, kG>();
-        case 6: return kernel_for<6, TPR, kG>();
-        case 7: return kernel_for<7, TPR, kG>();
-        case 8: return kernel_for<8, TPR, kG>();
+        case 2: return kernel_for<2, TPR>();
+        case 3: return kernel_for<3, TPR>();
+        case 4: return kernel_for<4, TPR>();
+        case 5: return kernel_for<5, TPR>();
+        case 6: return kernel_for<6, TPR>();
+        case 7: return kernel_for<7, TPR>();
+        case 8: return kernel_for<8, TPR>();
         default: return nullptr;
     }
 }
 
-// Row-wise scales: 2, 4 or 8 threads per row; group scales: 4.
+const void* group_kernel_for(int M) {
+    switch (M) {
+        case 1: return reinterpret_cast<const void*>(rowdot_group_kernel<1>);
+        case 2: return reinterpret_cast<const void*>(rowdot_group_kernel<2>);
+        case 3: return reinterpret_cast<const void*>(rowdot_group_kernel<3>);
+        case 4: return reinterpret_cast<const void*>(rowdot_group_kernel<4>);
+        case 5: return reinterpret_cast<const void*>(rowdot_group_kernel<5>);
+        case 6: return reinterpret_cast<const void*>(rowdot_group_kernel<6>);
+        case 7: return reinterpret_cast<const void*>(rowdot_group_kernel<7>);
+        case 8: return reinterpret_cast<const void*>(rowdot_group_kernel<8>);
+        default: return nullptr;
+    }
+}
+
+// Row-wise scales: 2, 4 or 8 threads per row; group scales: 1, 2 or 4
+// phases (one kernel).
 const void* kernel_for(int M, int tpr, bool group) {
-    if (group) return tpr == 4 ? kernel_for_rows<4, true>(M) : nullptr;
+    if (group) return (tpr == 1 || tpr == 2 || tpr == 4) ? group_kernel_for(M) : nullptr;
     switch (tpr) {
-        case 2: return kernel_for_rows<2, false>(M);
-        case 4: return kernel_for_rows<4, false>(M);
-        case 8: return kernel_for_rows<8, false>(M);
+        case 2: return kernel_for_rows<2>(M);
+        case 4: return kernel_for_rows<4>(M);
+        case 8: return kernel_for_rows<8>(M);
         default: return nullptr;
     }
 }
@@ -475,8 +731,9 @@ cudaError_t set_attributes() {
     if (e != cudaSuccess) return e;
     if (dev < 64 && done[dev]) return cudaSuccess;
     for (int k = 0; k < 4; ++k) {
-        for (int M = 2; M <= kRowdotMaxM; ++M) {
-            const void* fn = k < 3 ? kernel_for(M, 2 << k, false) : kernel_for(M, 4, true);
+        for (int M = 1; M <= kRowdotMaxM; ++M) {
+            const void* fn = k < 3 ? kernel_for(M, 2 << k, false) : kernel_for(M, 1, true);
+            if (fn == nullptr) continue;
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerSM - 1024);
             if (e != cudaSuccess) return e;
             e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -488,10 +745,91 @@ cudaError_t set_attributes() {
     return cudaSuccess;
 }
 
-size_t smem_bytes(int M, int NS, int bpp, int tpr, int gstride) {
+size_t smem_bytes(int M, int NS, int bpp, int tpr) {
     return 1024 + (size_t)NS * kBoxBytes + (size_t)M * bpp * kActBoxBytes +
-           (size_t)(tpr - 1) * M * kTile * 4 + (size_t)kTile * gstride * 4 + (size_t)(NS + 1) * 8 +
+           (size_t)(tpr - 1) * M * kTile * 4 + (size_t)(NS + 1) * 8 + (size_t)(2 * NS + 2) * 4;
+}
+
+// Group-scale kernel: NS slots of one weight box and its activation codes,
+// and cval_bytes of chunk sums.
+size_t group_smem_bytes(int M, int NS, size_t cval_bytes) {
+    return 1024 + (size_t)NS * (kBoxBytes + (size_t)M * kActBoxBytes) + cval_bytes + (size_t)NS * 8 +
            (size_t)(2 * NS + 2) * 4;
+}
+
+constexpr int kMaxNSGroup = 16;
+
+// Group scales (groups of 2^gshift codes): 1..8 batch rows, phases of 128
+// threads (one per weight row).  K is split into pieces of whole chunks
+// (max(group, 1024) codes) while the tiles cover less than 4/5 of the SMs
+// (or into min(force_p, chunks) pieces when force_p > 0); then as many CTAs
+// per SM as the grid fills (at most 4, or cps when given), 4 / cps phases
+// per CTA (at most one per chunk of a piece), and the ring takes the shared
+// memory left, so that every SM keeps 16 warps and about 12 boxes in flight.  N counts
+// the rows of all matrices of a launch (each padded to whole tiles by the
+// caller when the plan is for a launch, or the sum of the rows for the
+// workspace bound, which then covers kGroupMats - 1 partial tiles more).
+bool make_group_plan(int M, int64_t K, int64_t N, int num_sms, RowdotPlan* out, int cps, int gshift,
+                     int force_p) {
+    if (M < 1 || M > kRowdotMaxM || K < 32 || K % 32 || K > 131072 || N < 1 || N > 0x7FFFFFFF)
+        return false;
+    if (gshift < 5 || gshift > 17 || K % (1LL << gshift)) return false;
+    if (cps < 0 || cps > 4 || num_sms < 1) return false;
+    RowdotPlan pl = {};
+    pl.tpr = 1;
+    pl.MT = M;
+    pl.force_p = force_p;
+    pl.cps_req = cps;
+    pl.gshift = gshift;
+    pl.lshift = gshift > 10 ? gshift : 10;
+    pl.tiles = (int)((N + kTile - 1) / kTile);
+    pl.nbox = (int)((K + kBoxCodes - 1) / kBoxCodes);
+    pl.nch = (int)((K + (1LL << pl.lshift) - 1) >> pl.lshift);
+    const int abox = (1 << pl.lshift) / kBoxCodes;  // boxes per chunk
+    // split while the tiles cover less than 4/5 of the SMs
+    int P = (num_sms * 4 / 5 + pl.tiles - 1) / pl.tiles;
+    if (force_p > 0) P = force_p;
+    if (P > pl.nch) P = pl.nch;
+    if (P < 1 || pl.tiles > kTicketSlots) P = 1;  // one arrival counter per tile
+    const int cpp = (pl.nch + P - 1) / P;  // chunks per piece
+    pl.P = (pl.nch + cpp - 1) / cpp;
+    pl.bpp = cpp * abox;
+    if ((int64_t)pl.tiles * pl.P > 0x7FFFFFFF) return false;
+    const int64_t ctas = (int64_t)pl.tiles * pl.P;
+    pl.cps = cps > 0 ? cps : (int)((ctas + num_sms - 1) / num_sms < 4 ? (ctas + num_sms - 1) / num_sms : 4);
+    pl.abox = abox;
+    int nph = kMaxPhases / pl.cps;
+    while (nph > cpp) nph /= 2;
+    size_t cval = (nph > 1 && pl.P == 1) ? (size_t)M * cpp * kTile * 4 : 0;
+    if (cval > 32 * 1024) {  // chunk sums of a long row: one phase keeps them in registers
+        nph = 1;
+        cval = 0;
+    }
+    pl.nph = nph;
+    pl.tpr = nph;
+    const int budget = kSmemPerSM / pl.cps - 1024;
+    int NS = kMaxNSGroup;
+    while (NS > 1 && group_smem_bytes(M, NS, cval) > (size_t)budget) --NS;
+    if (group_smem_bytes(M, NS, cval) > (size_t)budget) return false;
+    pl.NS = NS;
+    pl.smem = (int)group_smem_bytes(M, NS, cval);
+    pl.grid = (int)ctas;
+    pl.sms = num_sms;
+    // workspace: tickets, scales, activation codes [nbox][8][M][32 bytes],
+    // then chunk sums [tiles][nch][M][128] fp32.  K is split only when the
+    // tiles are fewer than the SMs (or on request), and a launch of several
+    // matrices has at most kGroupMats - 1 tiles more than their summed rows.
+    pl.off_sa = kTicketBytes;
+    pl.off_codes = pl.off_sa + 256;
+    pl.off_part = round_up_sz(pl.off_codes + (size_t)M * pl.nbox * kActBoxBytes, 256);
+    int64_t tmax = 0;
+    if (pl.nch > 1) {
+        tmax = pl.tiles + kGroupMats - 1;
+        if (force_p <= 1 && tmax > num_sms * 4 / 5) tmax = num_sms * 4 / 5;
+    }
+    pl.ws_bytes = pl.off_part + round_up_sz((size_t)tmax * pl.nch * M * kTile * 4, 256);
+    *out = pl;
+    return true;
 }
 
 }  // namespace
@@ -501,15 +839,14 @@ size_t smem_bytes(int M, int NS, int bpp, int tpr, int gstride) {
 // into pieces of whole 256-code boxes when the tiles alone leave CTA slots
 // idle, and so that a piece's activation codes fit in kActMax bytes.  The
 // ring takes what shared memory is left, up to kMaxNS boxes.  gshift >= 0:
-// group scales (groups of 2^gshift codes, 4 threads per row), the piece's
-// scale window staged per CTA.
+// group scales (groups of 2^gshift codes), the one-thread-per-row kernel.
 bool make_rowdot_plan(int M, int64_t K, int64_t N, int num_sms, RowdotPlan* out, int tpr, int cps,
-                      int gshift) {
+                      int gshift, int force_p) {
+    if (gshift >= 0) return make_group_plan(M, K, N, num_sms, out, cps, gshift, force_p);
     if (M < 2 || M > kRowdotMaxM || K < 32 || K % 32 || K > 131072 || N < 1 || N > 0x7FFFFFFF)
         return false;
-    if (tpr == 0 || gshift >= 0) tpr = kRowdotDefaultTPR;
+    if (tpr == 0) tpr = kRowdotDefaultTPR;
     if (tpr != 2 && tpr != 4 && tpr != 8) return false;
-    if (gshift >= 0 && (gshift < 5 || gshift > 17 || K % (1LL << gshift))) return false;
     if (cps == 0) cps = tpr < 4 ? 4 / tpr : 1;
     if (cps < 1 || cps > 4) return false;
     RowdotPlan pl = {};
@@ -529,23 +866,17 @@ bool make_rowdot_plan(int M, int64_t K, int64_t N, int num_sms, RowdotPlan* out,
     pl.P = (pl.nbox + pl.bpp - 1) / pl.bpp;
     if (pl.P > 1 && pl.tiles > kTicketSlots) return false;
     if ((int64_t)pl.tiles * pl.P > 0x7FFFFFFF) return false;
-    pl.gshift = gshift;
-    if (gshift >= 0) {
-        // groups a piece touches: whole groups when boxes hold whole groups,
-        // else the piece may start and end inside one
-        pl.gwin = (int)(((int64_t)pl.bpp * kBoxCodes) >> gshift) + 2;
-        pl.gstride = pl.gwin | 1;  // odd: the 32 rows of a warp hit 32 banks
-    }
+    pl.gshift = -1;
     const int budget = kSmemPerSM / pl.cps - 1024;
     int NS = kMaxNS < pl.bpp ? kMaxNS : pl.bpp;
-    while (NS > 1 && smem_bytes(M, NS, pl.bpp, tpr, pl.gstride) > (size_t)budget) --NS;
-    if (smem_bytes(M, NS, pl.bpp, tpr, pl.gstride) > (size_t)budget) return false;
+    while (NS > 1 && smem_bytes(M, NS, pl.bpp, tpr) > (size_t)budget) --NS;
+    if (smem_bytes(M, NS, pl.bpp, tpr) > (size_t)budget) return false;
     pl.NS = NS;
-    pl.smem = (int)smem_bytes(M, NS, pl.bpp, tpr, pl.gstride);
+    pl.smem = (int)smem_bytes(M, NS, pl.bpp, tpr);
     pl.grid = pl.tiles * pl.P;
     pl.sms = num_sms;
     // workspace: tickets, scales, activation codes [nbox][8][M][32 bytes],
-    // then piece sums [tiles][P][M][128] (int32, or fp32 with group scales).
+    // then piece sums [tiles][P][M][128] int32.
     // Sized for any N' <= N (grouped launches plan each matrix on its own):
     // a matrix is split either because its tiles leave CTA slots idle
     // (then tiles' * P' <= slots) or because a piece's codes must fit in
@@ -586,22 +917,57 @@ cudaError_t launch_w4a8_rowdot(const RowdotPlan& pl, const uint16_t* X, const in
     if (fn == nullptr || group != (pl.gshift >= 0)) return cudaErrorInvalidValue;
     cudaError_t e = set_attributes();
     if (e != cudaSuccess) return e;
+    if (group) {
+        // every matrix in one launch, their tiles numbered consecutively
+        if (G < 1 || G > kGroupMats) return cudaErrorInvalidValue;
+        GroupArgs a;
+        memset(&a, 0, sizeof(a));
+        int64_t tiles = 0;
+        for (int g = 0; g < G; ++g) {
+            if (!make_w4_tile_map(&a.tmW[g], Wq[g], K, Ns[g])) return cudaErrorInvalidValue;
+            a.sg[g] = sg[g];
+            a.Y[g] = Y[g];
+            a.N[g] = (int)Ns[g];
+            a.tile0[g] = (int)tiles;
+            tiles += (Ns[g] + kTile - 1) / kTile;
+        }
+        for (int g = G; g <= kGroupMats; ++g) a.tile0[g] = (int)tiles;
+        RowdotPlan pg;
+        if (!make_group_plan(M, K, tiles * kTile, pl.sms, &pg, pl.cps_req, pl.gshift, pl.force_p))
+            return cudaErrorInvalidValue;
+        // the caller's workspace (planned for the summed rows) holds this launch's chunk sums
+        if (pg.off_part != pl.off_part ||
+            pl.off_part + (pg.P > 1 ? (size_t)tiles * pg.nch * M * kTile * 4 : 0) > pl.ws_bytes)
+            return cudaErrorInvalidValue;
+        a.codes = reinterpret_cast<const uint8_t*>(codes);
+        a.sa = sa_ws;
+        a.part_f = reinterpret_cast<float*>(wsb + pg.off_part);
+        a.tickets = reinterpret_cast<unsigned*>(wsb);
+        a.gshift = pg.gshift;
+        a.gld = (int)((K / gs + 3) / 4 * 4);
+        a.ngroups = (int)(K >> pg.gshift);
+        a.lshift = pg.lshift;
+        a.nch = pg.nch;
+        a.abox = pg.abox;
+        a.K = (int)K;
+        a.M = M;
+        a.nbox = pg.nbox;
+        a.bpp = pg.bpp;
+        a.P = pg.P;
+        a.NS = pg.NS;
+        a.nph = pg.nph;
+        void* args[] = {&a};
+        return launch_pdl(fn, dim3(pg.grid), dim3(kTile * pg.nph), pg.smem, stream, flags, args);
+    }
     for (int g = 0; g < G; ++g) {
         RowdotPlan pg;
-        if (!make_rowdot_plan(M, K, Ns[g], pl.sms, &pg, pl.tpr, pl.cps, pl.gshift)) return cudaErrorInvalidValue;
+        if (!make_rowdot_plan(M, K, Ns[g], pl.sms, &pg, pl.tpr, pl.cps, pl.gshift, pl.force_p))
+            return cudaErrorInvalidValue;
         RowdotArgs a;
         memset(&a, 0, sizeof(a));
         if (!make_w4_tile_map(&a.tmW, Wq[g], K, Ns[g])) return cudaErrorInvalidValue;
         a.codes = codes;
-        a.sw = group ? nullptr : sw[g];
-        if (group) {
-            a.sg = sg[g];
-            a.gshift = pg.gshift;
-            a.gld = (int)((K / gs + 3) / 4 * 4);
-            a.ngroups = (int)(K >> pg.gshift);
-            a.gwin = pg.gwin;
-            a.gstride = pg.gstride;
-        }
+        a.sw = sw[g];
         a.sa = sa_ws;
         a.Y = Y[g];
         a.acc_out = (G == 1) ? acc_out : nullptr;

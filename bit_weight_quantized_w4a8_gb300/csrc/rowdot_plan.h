@@ -1,5 +1,6 @@
-// rowdot_plan.h -- launch plan of the row-per-thread dp4a kernel
-// (rowdot.cu): W4A8 with row-wise scales for 2..8 activation rows.
+// rowdot_plan.h -- launch plan of the row-per-thread dp4a kernels
+// (rowdot.cu): W4A8 with row-wise scales for 2..8 activation rows, and with
+// group-wise scales for 1..8 (one thread per weight row).
 #pragma once
 
 #include <cstddef>
@@ -17,7 +18,10 @@ struct RowdotPlan {
     int P, bpp;        // K pieces, boxes per piece
     int NS;            // weight ring slots of 16 KB
     int gshift;        // group scales: groups of 2^gshift codes (-1: row-wise)
-    int gwin, gstride; // groups staged per CTA, floats per staged row
+    int lshift, nch;   // group scales: chunks of 2^lshift codes, nch of them
+    int force_p;       // group scales: requested K pieces (0 = by the tiles)
+    int cps_req;       // group scales: requested CTAs per SM (0 = by the grid)
+    int nph, abox;     // group scales: thread phases per CTA (= tpr), boxes per chunk
     int grid, smem, sms;
     size_t off_sa, off_codes, off_part;  // workspace layout
     size_t ws_bytes;

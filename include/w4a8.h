@@ -91,8 +91,11 @@ typedef enum {
  *    an integer multiple of 2^-9 below 2^15), and the bias 8 * sum(a) is
  *    removed with the exact code sum, so the rescale matches the dp4a path
  *    bit for bit.
- *  - group-wise scales: the row-per-thread kernel for 2..8 rows, the tensor
- *    cores (binary16 operands) from 9, the dp4a GEMV otherwise.
+ *  - group-wise scales: the one-thread-per-row integer kernel for 1..8 rows
+ *    (each thread folds its weight row's group sums in the fixed order of
+ *    the group-scale contract), the tensor cores (binary16 operands) from 9
+ *    rows for groups of whole 128-code stages up to 16384 codes, otherwise
+ *    the one-thread-per-row kernel once per group of up to 8 rows.
  *  - the warp-level e4m3 MMA kernel (mma.sync m16n8k32, operands built in
  *    registers) serves 2..32 rows when w4a8_tuning_t.qmma_max_m asks for it.
  * When the other kernels are switched off the dp4a GEMV serves batches too,
@@ -307,28 +310,31 @@ size_t w4a8g_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t group);
 /* INT4 x INT8 product with group-wise weight scales:
  *   Y[m][n] = sa[m] * sum_g sg[n][g] * acc_g[m][n],
  *   acc_g[m][n] = sum over the codes k of group g of Xq[m][k] * q[n][k].
- * Arithmetic: the int32 sum of every 32-code granule is exact; it is
- * multiplied by its group's scale and added into an fp32 sum with one
- * fused multiply-add, the partial sums are added in fp32 in an order fixed
- * by the launch plan (the same on every call with the same shape and
- * device), and the total is multiplied by sa[m].  The result therefore
- * lies within (K/32 + 4) * 2^-24 * sa[m] * sum_g sg[n][g] * |acc|_g of the
- * exact value, |acc|_g being the sum of |Xq * q| over group g.
+ * Arithmetic, in an order fixed by K and group alone (the page gives the
+ * output as the integer sum times the weight and activation scales, per
+ * group, and fixes no summation order):
+ *   acc_g is exact (int32; converted to fp32 with one round-to-nearest,
+ *     exact for groups of at most 16384 codes);
+ *   the fold chunks are L = max(group, 1024) codes: per chunk, f = +0, then
+ *     for its groups in ascending order f = fmaf(acc_g, s_g, f) (one
+ *     rounding each);
+ *   T = +0, then for the chunks in ascending order T = T + f;
+ *   Y[m][n] = T * sa[m].
+ * So Y is the same bits whatever the batch size, kernel or K split, and
+ * lies within (L / group + ceil(K / L) + 1) * 2^-24 * sa[m] * sum_g sg[n][g]
+ * * |acc|_g of the exact value, |acc|_g being the sum of |Xq * q| over
+ * group g.  Kernels: 1..8 rows (w4a8_tuning_t.rowdot_max_m) one thread per
+ * weight row, which walks the row's codes in order (K pieces of whole
+ * chunks; with split K each chunk's f goes to the workspace and the CTA that
+ * finishes a tile last adds them in chunk order).  From 9 rows
+ * (w4a8_tuning_t.mma_min_m) with a group of a multiple of 128 codes up to
+ * 16384: the tensor cores, each group's products summed exactly in an fp32
+ * TMEM accumulator, the fold run by the epilogue threads (K not split).
+ * Other calls: the one-thread-per-row kernel once per group of up to 8 rows.
  *   Xq [M][K] int8, sa [M] fp32    quantized activation (act_quantize_i8)
  *   Wq [N][K/2] uint8, sg [N][stride] fp32   (w4g_quantize_weights)
  *   Y [M][N] fp32 out; ws, ws_bytes (w4a8g_workspace_bytes) and flags as
  *   in w4a8_gemv.
- * Calls with 2 to 8 rows (w4a8_tuning_t.rowdot_max_m) run on the
- * row-per-thread kernel (any group size): each 32-code granule's exact sum
- * is folded with its group scale by one fused multiply-add per batch row,
- * the four threads of a weight row and the K pieces add their fp32 sums in
- * a fixed order.  Other calls with at least 3 rows
- * (w4a8_tuning_t.mma_min_m) and a group of a
- * multiple of 128 codes up to 16384 run on the tensor cores: each group's
- * products are summed exactly in an fp32 TMEM accumulator, multiplied by
- * the group scale and added into fp32 running sums with one fused
- * multiply-add (the same bound holds); K pieces are added in a fixed order.
- * Other calls run on the dp4a kernel, one launch per group of up to 8 rows.
  * Requires 1 <= M <= W4A8_MAX_M, the w4a8_gemv limits on K and N, the group
  * rule above; Xq, Wq and sg 16-byte aligned; Y and sa 4-byte aligned. */
 int w4a8g_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, int64_t group,
@@ -347,9 +353,9 @@ int w4a8g_linear(const uint16_t* X, int64_t M, int64_t K, int64_t group, const u
 /* Grouped fused linear with group-wise scales: G weight matrices reading
  * the same activation in one launch, as w4a8_linear_grouped.  Wq, sg, N, Y
  * are HOST arrays of G device pointers / sizes; ws covers
- * w4a8g_workspace_bytes(M, K, N[0] + ... + N[G-1], group).  Y[g] is within
- * the w4a8g_gemv bound of the exact product (its rounding may differ from
- * w4a8g_linear's, whose launch plan differs). */
+ * w4a8g_workspace_bytes(M, K, N[0] + ... + N[G-1], group).  Y[g] is
+ * bit-identical to w4a8g_linear's on matrix g (the order is fixed by K and
+ * group, not by the launch plan). */
 int w4a8g_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int64_t group, int G,
                          const uint8_t* const* Wq, const float* const* sg, const int64_t* N,
                          float* const* Y, void* ws, size_t ws_bytes, unsigned flags,
@@ -442,22 +448,25 @@ int w4a8_device_error(unsigned* flags, void* stream);
 
 /* Process-wide overrides of the launch plan, for A/B measurements and for
  * tests that must exercise a given plan.  Zero fields keep the heuristic.
- *   force_splits: number of K pieces (1..16); the shape must admit it.
+ *   force_splits: number of K pieces (1..16); the shape must admit it
+ *     (group-wise scales on the one-thread-per-row kernel: pieces of whole
+ *     fold chunks, so at most the chunk count, fewer when the chunks do not
+ *     divide evenly; tensor cores: never split).
  *   force_threads_per_row: threads sharing one row-piece (power of 2, <=256).
  *   ring_bytes: target size of the shared-memory weight ring (<= 204800).
  *   ctas_per_sm: CTAs per SM for each K piece (1..4; 0 = 1); for the
  *     row-per-thread kernel, CTAs per SM (0 = 1 at 4 or 8 threads per
- *     row, 2 at 2).
+ *     row, 2 at 2; 4 for the group-scale kernel).
  *   mma_min_m: activation rows from which the W4A8 entry points use the
  *     tensor-core kernel (2..65; 0 = default: 2 rows for row-wise scales,
  *     3 for group-wise scales; 65 = never).
  *   rowdot_max_m: activation rows up to which W4A8 calls use the
- *     row-per-thread kernel, from 2 rows (0 = default: 3 rows for row-wise
- *     scales on matrices of at most 2 x SMs 128-row tiles, 8 rows for
- *     group-wise scales; 1 = never, <= 8); it takes precedence over
- *     mma_min_m.  force_threads_per_row 2, 4 or 8
- *     sets that kernel's threads per weight row (row-wise scales; calls
- *     with group-wise scales always use 4).
+ *     row-per-thread kernel in one launch, from 2 rows (group-wise scales:
+ *     from 1) (0 = default: 3 rows for row-wise scales on matrices of at
+ *     most 2 x SMs 128-row tiles, 8 rows for group-wise scales; 1 = never,
+ *     <= 8); it takes precedence over mma_min_m.  force_threads_per_row 2,
+ *     4 or 8 sets that kernel's threads per weight row (row-wise scales;
+ *     the group-scale kernel always has one).
  *   mma_e4m3: operands of the row-wise tensor-core kernel: 0 = default
  *     (e4m3), 1 = binary16 (kind::f16, K = 16 per MMA), 2 = e4m3
  *     (kind::f8f6f4, K = 32 per MMA: weight bytes q + 8 read as (q + 8) *
@@ -507,11 +516,11 @@ int w4a8_set_tuning(const w4a8_tuning_t* tuning);
 int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int* info,
                    int n_info);
 
-/* The same for w4a8g_gemv / w4a8g_linear (the kernel field reads 0, 1 or
- * 2 as above), followed by two more: the widest scale window a K piece
- * reads (floats per row) and the bytes of one ring slot's scale area (the
- * dp4a GEMV) or of the CTA's staged scale window (the row-per-thread
- * kernel). */
+/* The same for w4a8g_gemv / w4a8g_linear (the kernel field reads 1 for the
+ * tensor cores, 2 for the one-thread-per-row kernel, whose threads-per-row
+ * field reads 1 and whose rows field gives the batch rows of one launch),
+ * followed by two more: the number of fold chunks and their length in
+ * codes (max(group, 1024)). */
 int w4a8g_plan_info(int64_t M, int64_t K, int64_t N, int64_t group, int num_sms, int* info,
                     int n_info);
 

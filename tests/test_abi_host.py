@@ -242,11 +242,15 @@ def test_kernel_routing():
             w4.w4a8_set_tuning(mma_e4m3=3)
         w4.w4a8_set_tuning(mma_e4m3=2, rowdot_max_m=1, qmma_max_m=1)  # operand type does not change the plan
         assert w4.w4a8_plan_info(4, 3584, 18944, num_sms=152)["kernel"] == 1
-        # group scales: the row-per-thread kernel at 2..8 rows, the tensor cores above
+        # group scales: the one-thread-per-row kernel at 1..8 rows, the tensor
+        # cores above for groups of whole 128-code stages, else launches of 8 rows
         w4.w4a8_set_tuning()
-        assert w4.w4a8g_plan_info(4, 3584, 18944, 128, num_sms=152)["kernel"] == 2
-        assert w4.w4a8g_plan_info(9, 3584, 18944, 128, num_sms=152)["kernel"] == 1
-        assert w4.w4a8g_plan_info(4, 3584, 18944, 32, num_sms=152)["kernel"] == 2
+        groute = lambda M, gs=128: w4.w4a8g_plan_info(M, 3584, 18944, gs, num_sms=152)
+        assert [groute(M)["kernel"] for M in (1, 4, 8, 9, 64)] == [2, 2, 2, 1, 1]
+        assert groute(4, 32)["kernel"] == 2 and groute(40, 32)["kernel"] == 2
+        assert groute(40, 32)["cols_per_thread"] == 8 and groute(5)["cols_per_thread"] == 5
+        w4.w4a8_set_tuning(rowdot_max_m=1, mma_min_m=65)
+        assert groute(1)["kernel"] == 2 and groute(20)["cols_per_thread"] == 8
         w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)
         assert w4.w4a8_plan_info(64, 3584, 18944, num_sms=152)["kernel"] == 0
         w4.w4a8_set_tuning(mma_min_m=2, rowdot_max_m=1, qmma_max_m=1)
@@ -303,46 +307,69 @@ def test_group_scale_stride_matches_header():
 
 GROUP_SHAPES = [(1, 896, 512, 128), (1, 3584, 152064, 128), (1, 18944, 3584, 128),
                 (1, 3584, 37888, 64), (2, 3584, 18944, 256), (8, 18944, 3584, 32), (1, 32, 7, 32),
-                (3, 131072, 5, 1024), (1, 4096, 9, 4096), (64, 2048, 100, 512)]
+                (3, 131072, 5, 1024), (1, 4096, 9, 4096), (8, 2048, 100, 512), (5, 8192, 40, 2048),
+                (8, 131072, 2, 131072)]
+
+
+def check_group_plan(p, M, K, N, gs, sms, splits=0):
+    """The one-thread-per-row group kernel's plan: whole chunks per K piece,
+    four CTAs of 128 threads per SM, and a workspace for the codes and the
+    chunk sums of split tiles."""
+    L = max(gs, 1024)
+    nch = -(-K // L)
+    nbox = -(-K // 256)
+    tiles = -(-N // 128)
+    P = p["splits"]
+    assert p["kernel"] == 2 and p["threads_per_row"] in (1, 2, 4) and p["cols_per_thread"] == M
+    assert p["chunks"] == nch and p["chunk_codes"] == L
+    if splits:  # pieces of whole chunks: the requested count, or fewer when chunks do not divide
+        want = -(-nch // -(-nch // min(splits, nch)))
+        assert P == (want if tiles <= 1024 else 1)
+    assert 1 <= P <= nch
+    cpp = -(-nch // P)
+    assert (P - 1) * cpp < nch                                   # no empty piece
+    assert p["ctas_per_split"] == tiles and p["grid"] == tiles * P
+    assert p["stage_bytes"] == 16384 and 1 <= p["stages"] <= 16
+    assert p["smem_bytes"] >= p["stages"] * (16384 + M * 256)
+    cps = min(4, -(-p["grid"] // sms))             # CTAs per SM the grid fills
+    nph = p["threads_per_row"]                     # thread phases, each whole chunks of a piece
+    assert p["smem_bytes"] * cps <= 227 * 1024
+    assert p["stages"] * cps >= 12 or p["smem_bytes"] * cps > 227 * 1024 - (16384 + M * 256) * cps
+    assert nph * cps <= 4 and nph <= cpp and (nph == 4 // cps or nph * 2 > cpp or nph == 1)
+    if tiles >= sms and not splits:
+        assert P == 1                              # every SM has a CTA already
+    assert P == 1 or tiles <= 1024
+    assert p["ws_bytes"] >= 4096 + 256 + M * nbox * 256 + (tiles * nch * M * 512 if P > 1 else 0)
 
 
 @pytest.mark.parametrize("sms", [152, 148, 20, 1])
 @pytest.mark.parametrize("splits", [0, 3, 7, 16])
-def test_group_plan_windows(sms, splits):
-    """Every K piece's scale window covers the groups of its granules, starts
-    and ends on 16-byte words inside the padded scale row, and the slot's
-    scale area holds a whole stage of rows."""
+def test_group_plans(sms, splits):
+    """Every group-scale shape of 1..8 rows plans on the one-thread-per-row
+    kernel, K pieces of whole fold chunks (a forced count is capped by the
+    chunks), and the workspace query agrees with the plan."""
     try:
-        w4.w4a8_set_tuning(force_splits=splits, mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)  # the dp4a kernel's plans
+        w4.w4a8_set_tuning(force_splits=splits)
         for (M, K, N, gs) in GROUP_SHAPES:
-            if splits and splits > K // 32:
-                continue
-            try:
-                p = w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)
-            except w4.W4A8Error:
-                assert splits, (M, K, N, gs)  # only a forced split may leave no plan
-                continue
-            P = p["splits"]
-            assert not splits or P == splits
-            Gt = K // 32
-            Gq = -(-Gt // P)
-            shift = (gs // 32).bit_length() - 1
-            ld = w4.w4g_scale_stride(K, gs)
-            win = p["scale_window"]
-            assert win % 4 == 0 and 4 <= win <= ld
-            for piece in range(P):
-                g0 = piece * Gq
-                gp = min(Gq, Gt - g0)
-                gb = (g0 >> shift) & ~3
-                first, last = g0 >> shift, (g0 + gp - 1) >> shift
-                assert gb <= first and last < gb + win or (gb + win == ld and last < ld)
-                assert gb % 4 == 0 and gb + min(win, ld - gb) <= ld
-            assert p["scale_stage_bytes"] % 16 == 0
-            assert p["scale_stage_bytes"] >= p["rows_per_stage"] * win * 4
-            assert p["smem_bytes"] <= 232448 and 2 <= p["stages"] <= 16
-            assert p["stage_bytes"] >= p["rows_per_stage"] * Gq * 16
-            assert (p["ws_bytes"] > 0) == (P > 1)
-            assert w4.w4a8g_workspace_bytes(M, K, N, gs) == p["ws_bytes"] or sms != 0
+            p = w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)
+            check_group_plan(p, M, K, N, gs, sms, splits)
+    finally:
+        w4.w4a8_set_tuning(reset=True)
+
+
+def test_group_workspace_covers_grouped_matrices():
+    """A grouped group-scale call plans each matrix on its own inside the
+    workspace sized for the total rows."""
+    try:
+        for splits in (0, 4):
+            w4.w4a8_set_tuning(force_splits=splits)
+            for sms in (152, 148, 20):
+                for (M, K, gs) in [(1, 3584, 128), (8, 18944, 128), (3, 131072, 1024), (2, 896, 32)]:
+                    full = w4.w4a8g_plan_info(M, K, 40000, gs, num_sms=sms)
+                    for Np in (1, 7, 128, 129, 1000, 4608, 18944, 39999):
+                        p = w4.w4a8g_plan_info(M, K, Np, gs, num_sms=sms)
+                        check_group_plan(p, M, K, Np, gs, sms, splits)
+                        assert p["ws_bytes"] <= full["ws_bytes"], (M, K, Np, sms)
     finally:
         w4.w4a8_set_tuning(reset=True)
 
@@ -385,52 +412,36 @@ def test_isx_argument_checks(L):
 
 def test_group_tensor_core_plans():
     """Group scales with 3..64 rows take the tensor cores when the group is a
-    whole number of 128-code stages (at most 16384 codes); the K pieces then
-    hold whole groups and whole weight loads, and the workspace covers the
-    fp32 partials of every piece."""
+    whole number of 128-code stages (at most 16384 codes); K pieces hold
+    whole fold chunks, and a split plan's workspace holds one fp32 sum per
+    output and chunk (at most 32 MB); other groups run launches of up to 8
+    rows on the one-thread-per-row kernel."""
     try:
-        w4.w4a8_set_tuning(rowdot_max_m=1, qmma_max_m=1)  # 2..8 rows would take the row-per-thread kernel
+        w4.w4a8_set_tuning(rowdot_max_m=1, qmma_max_m=1)  # 1..8 rows would take the one-thread-per-row kernel
         for sms in (152, 148, 20):
             for (M, K, N, gs) in [(3, 3584, 300, 128), (16, 3584, 18944, 128), (64, 18944, 3584, 128),
                                   (4, 3584, 1000, 256), (8, 2048, 200, 512), (33, 896, 100, 128),
-                                  (5, 32768, 64, 16384)]:
+                                  (5, 32768, 64, 16384), (40, 3072, 130, 1024)]:
                 p = w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)
                 assert p["kernel"] == 1, (M, K, N, gs)
-                nkb = K // 64
-                P = p["splits"]
-                kbp = -(-nkb // P)
-                align = max(4, gs // 64)
-                # the plan's pieces: kbp rounded up to whole groups and loads
-                kbp_al = -(-kbp // align) * align
-                assert -(-nkb // kbp_al) == P or P == 1
-                assert p["grid"] == p["ctas_per_split"] * P
-                if P > 1:
-                    assert p["ws_bytes"] >= 4096 + 256 + M * K * 2 + p["grid"] * M * 128 * 4
-            for (M, K, N, gs) in [(3, 1024, 77, 32), (8, 3584, 100, 64), (2, 3584, 100, 128)]:
-                assert w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)["kernel"] == 0
+                L = max(gs, 1024)
+                nch, tiles, P = -(-K // L), -(-N // 128), p["splits"]
+                assert p["chunks"] == nch and p["chunk_codes"] == L
+                assert 1 <= P <= nch and p["grid"] == tiles * P and p["ctas_per_split"] == tiles
+                cpp = -(-nch // P)                        # whole chunks per piece, none empty
+                assert (P - 1) * cpp < nch
+                part = tiles * nch * M * 512 if P > 1 else 0
+                assert part <= 32 << 20
+                assert p["ws_bytes"] >= 4096 + 256 + M * K * 2 + part
+                if tiles * 5 >= 2 * sms * 4 or nch == 1:
+                    assert P == 1
+            for (M, K, N, gs) in [(3, 1024, 77, 32), (8, 3584, 100, 64), (20, 3584, 100, 64)]:
+                p = w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)
+                assert p["kernel"] == 2 and p["cols_per_thread"] == min(M, 8)
         w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1, qmma_max_m=1)
-        assert w4.w4a8g_plan_info(16, 3584, 18944, 128, num_sms=152)["kernel"] == 0
+        assert w4.w4a8g_plan_info(16, 3584, 18944, 128, num_sms=152)["kernel"] == 2
     finally:
         w4.w4a8_set_tuning(reset=True)
-
-
-def test_group_rowdot_plans():
-    """Group scales with 2..8 rows take the row-per-thread kernel for every
-    power-of-two group from 32: the staged scale window covers every group a
-    K piece touches and fits beside the ring."""
-    for sms in (152, 148, 20):
-        for (M, K, N, gs) in [(2, 3584, 1000, 128), (3, 1024, 77, 32), (8, 18944, 700, 128),
-                              (8, 4096, 64, 4096), (4, 2048, 5, 1024), (2, 131072, 3, 32),
-                              (5, 131072, 7, 1024)]:
-            p = w4.w4a8g_plan_info(M, K, N, gs, num_sms=sms)
-            assert p["kernel"] == 2, (M, K, N, gs)
-            check_rowdot_plan(p, M, K, N, sms)
-            nbox = -(-K // 256)
-            bpp = -(-nbox // p["splits"])
-            # groups touched by any piece: at most bpp * 256 / gs + 1
-            assert p["scale_window"] >= bpp * 256 // gs + 1
-            assert p["scale_stage_bytes"] >= 128 * p["scale_window"] * 4
-            assert p["smem_bytes"] >= p["stages"] * 16384 + M * bpp * 256 + p["scale_stage_bytes"]
 
 
 def test_rowdot_workspace_covers_grouped_matrices():

@@ -1,12 +1,13 @@
 """Group-wise INT4 scales: CUDA path vs the CPU oracle through the C ABI.
 
-Codes, scales and the quantized activation are bit-exact.  The product is
-fp32 arithmetic on exact int32 granule sums, so Y is checked against the
-oracle's binary64 value within the bound the arithmetic gives:
-|Y - Y_ref| <= (K/32 + 4) * 2^-24 * B, B = s_a * sum_g s_g * sum |Xq * q|
-(K/32 granule terms, each folded with one rounding, the partial sums and the
-final multiply by s_a).  With power-of-two scales and integer activations
-every intermediate is exact and Y must equal the oracle bit for bit.
+Codes, scales and the quantized activation are bit-exact, and so is Y: the
+library fixes the order of the group-scale arithmetic by K and the group
+size alone (exact int32 group sums folded in ascending order with one fused
+multiply-add each inside chunks of max(gs, 1024) codes, chunk results added
+in ascending order, then times s_a), and the oracle evaluates that order
+(oracle_w4a8g_f32).  Y is also within the recursive-summation bound of the
+oracle's binary64 value, and a row gives the same bits at every batch size,
+split count and kernel.
 """
 import numpy as np
 import pytest
@@ -20,6 +21,12 @@ import synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 U = 2.0 ** -24
+
+# tuning of each routing: the default (one-thread-per-row kernel for 1..8
+# rows, tensor cores above), one launch per 8 rows on the one-thread-per-row
+# kernel, and the tensor cores from 3 rows
+PATHS = {"default": {}, "row_groups": dict(rowdot_max_m=1, mma_min_m=65),
+         "tensor_cores": dict(rowdot_max_m=1)}
 
 
 @pytest.fixture(scope="module")
@@ -54,13 +61,27 @@ def to_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def assert_within_bound(Y, Y_ref, B, K):
-    Y = Y.astype(np.float64)
-    bound = (K / 32 + 4) * U * B
-    err = np.abs(Y - Y_ref)
-    bad = np.argwhere(err > bound)
-    assert bad.size == 0, (bad[:5], Y[tuple(bad[0])], Y_ref[tuple(bad[0])], bound[tuple(bad[0])])
-    assert np.isfinite(Y).all()
+def assert_exact(Y, Y_ref):
+    Y, Y_ref = np.ascontiguousarray(Y, np.float32), np.ascontiguousarray(Y_ref, np.float32)
+    bad = np.argwhere(bits(Y) != bits(Y_ref))
+    assert bad.size == 0, (len(bad), bad[:5], Y[tuple(bad[0])], Y_ref[tuple(bad[0])])
+
+
+def assert_within_bound(Y, Y64, B, K, gs):
+    """The fixed order's rounding bound: (groups per chunk + chunks + 1)
+    roundings of at most 2^-24 relative each, in the magnitude B."""
+    L = max(gs, 1024)
+    n_round = L // gs + (K + L - 1) // L + 1
+    err = np.abs(Y.astype(np.float64) - Y64)
+    assert np.all(err <= n_round * U * 1.001 * B + 1e-300)
+
+
+def route(w4, path, M, gs):
+    """Sets the tuning of a routing; False when it cannot serve the call."""
+    if path == "tensor_cores" and (M < 3 or gs % 128 or gs > 16384):
+        return False
+    w4.w4a8_set_tuning(**PATHS[path])
+    return True
 
 
 def make_operands(M, K, N, gs, seed):
@@ -77,7 +98,7 @@ def make_operands(M, K, N, gs, seed):
 def check_group(w4, orc, M, K, N, gs, seed, fused=True, flags=0):
     W, X = make_operands(M, K, N, gs, seed)
     Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
-    Y_ref, B, Xq_ref, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
+    Y_ref, Xq_ref, sa_ref = orc.w4a8g_linear_f32(X, Wq_ref, sg_ref, gs)
 
     Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
     assert np.array_equal(Wq.cpu().numpy(), Wq_ref)
@@ -96,7 +117,9 @@ def check_group(w4, orc, M, K, N, gs, seed, fused=True, flags=0):
     assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
     assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
     Yh = Y.cpu().numpy()
-    assert_within_bound(Yh, Y_ref, B, K)
+    assert_exact(Yh, Y_ref)
+    Y64, B = orc.w4a8g_ref(Xq_ref, sa_ref, Wq_ref, sg_ref, gs)
+    assert_within_bound(Yh, Y64, B, K, gs)
     assert not Yh[:, 1 % N].any()
     if M > 1:
         assert not Yh[M - 1].any()
@@ -132,112 +155,102 @@ GROUP_SHAPES = [
     (2, 3584, 260, 64, 13), (3, 1024, 77, 32, 14), (4, 3584, 1000, 256, 15),
     (5, 896, 33, 128, 16), (8, 2048, 200, 512, 17), (1, 32, 7, 32, 18), (1, 4096, 64, 4096, 19),
     (11, 896, 100, 128, 20), (64, 384, 96, 128, 21),
+    (2, 3584, 1000, 128, 800),   # two chunks of 1024 and a partial one
+    (6, 4096, 40000, 512, 804),  # many tiles, one piece each
+    (7, 288, 7, 32, 805),        # a partial last box
+    (8, 18944, 700, 128, 806),   # long rows, chunk-aligned pieces
+    (8, 4096, 64, 4096, 807),    # one group per row: one chunk
+    (4, 2048, 5, 1024, 808),     # groups of a whole chunk
+    (3, 8192, 40, 2048, 809),    # chunks of one group larger than 1024 codes
+    (20, 3072, 300, 32, 810),    # batches of 8, 8, 4 rows (groups the tensor cores do not take)
 ]
 
 
-@pytest.mark.parametrize("path", ["default", "dp4a"])
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("M,K,N,gs,seed", GROUP_SHAPES)
 def test_w4a8g_linear(w4, orc, M, K, N, gs, seed, path):
-    if path == "dp4a":
-        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
+    if not route(w4, path, M, gs):
+        pytest.skip("the routing does not serve this call")
     check_group(w4, orc, M, K, N, gs, seed, fused=True)
 
 
-@pytest.mark.parametrize("path", ["default", "dp4a"])
-@pytest.mark.parametrize("M,K,N,gs,seed", GROUP_SHAPES[:6] + GROUP_SHAPES[-2:])
+@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("M,K,N,gs,seed", GROUP_SHAPES[:6] + GROUP_SHAPES[10:14])
 def test_w4a8g_gemv_unfused(w4, orc, M, K, N, gs, seed, path):
-    if path == "dp4a":
-        w4.w4a8_set_tuning(mma_min_m=65, rowdot_max_m=1)
+    if not route(w4, path, M, gs):
+        pytest.skip("the routing does not serve this call")
     check_group(w4, orc, M, K, N, gs, seed, fused=False)
 
 
 # the tensor-core path: groups of whole 128-code stages, 3..64 rows; small N
-# splits K into many pieces (fp32 partials summed by the last CTA)
+# splits K into pieces of whole chunks (chunk sums added by the last CTA)
 MMA_GROUP_SHAPES = [
     (3, 3584, 300, 128, 90), (16, 3584, 1000, 128, 91), (64, 896, 129, 128, 92),
     (33, 2048, 257, 256, 93), (8, 18944, 200, 128, 94), (5, 4096, 64, 4096, 95),
-    (24, 1024, 4096, 512, 96),
+    (24, 1024, 4096, 512, 96), (40, 3072, 130, 1024, 97), (17, 4096, 300, 2048, 98),
 ]
 
 
 @pytest.mark.parametrize("M,K,N,gs,seed", MMA_GROUP_SHAPES)
 @pytest.mark.parametrize("fused", [True, False])
 def test_w4a8g_tensor_cores(w4, orc, M, K, N, gs, seed, fused):
-    w4.w4a8_set_tuning(rowdot_max_m=1)  # 2..8 rows would take the row-per-thread kernel
-    assert w4.w4a8g_plan_info(M, K, N, gs)["kernel"] == 1
+    w4.w4a8_set_tuning(**PATHS["tensor_cores"])
+    p = w4.w4a8g_plan_info(M, K, N, gs)
+    assert p["kernel"] == 1
     check_group(w4, orc, M, K, N, gs, seed, fused=fused)
 
 
-@pytest.mark.parametrize("M,N", [(3, 300), (16, 5000), (64, 96)])
-def test_w4a8g_tensor_cores_exact(w4, orc, M, N):
-    """Power-of-two group scales and integer activations on the tensor cores:
-    each group's sums are exact in D and every fold is exact, so Y equals the
-    oracle bit for bit (small N: many K pieces and their fp32 partials)."""
-    K, gs = 1024, 128
-    rng = np.random.Generator(np.random.PCG64(78 + M))
-    G = K // gs
-    q = rng.integers(-7, 8, size=(N, G, gs))
-    q[:, :, 0] = 7 * rng.choice([-1, 1], size=(N, G))
-    e = rng.integers(0, 4, size=(N, G, 1))
-    W = (q * 2.0 ** -e).reshape(N, K).astype(np.float32)
-    X = rng.integers(-126, 127, size=(M, K)).astype(np.float16)
-    X[:, 5] = 127
-    Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
-    Y_ref, _, _, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
-    assert np.all(sa_ref == 1.0)
-    w4.w4a8_set_tuning(rowdot_max_m=1)
-    assert w4.w4a8g_plan_info(M, K, N, gs)["kernel"] == 1
-    Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
-    Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs)
-    torch.cuda.synchronize()
-    assert np.array_equal(Y.cpu().numpy().astype(np.float64), Y_ref)
+def test_w4a8g_tensor_cores_split_and_whole(w4, orc):
+    """The plans of the tensor-core group path include split K (few tiles)
+    and whole K (many tiles, or one chunk)."""
+    w4.w4a8_set_tuning(**PATHS["tensor_cores"])
+    assert w4.w4a8g_plan_info(8, 18944, 200, 128)["splits"] > 1
+    assert w4.w4a8g_plan_info(24, 1024, 4096, 512)["splits"] == 1
+    assert w4.w4a8g_plan_info(64, 3584, 40000, 128)["splits"] == 1
 
 
-def test_w4a8g_tensor_cores_grouped(w4, orc):
-    w4.w4a8_set_tuning(rowdot_max_m=1)
-    M, K, gs, Ns = 8, 3584, 128, [3584, 512, 512]
-    X = synth.activation(97, M, K, outlier_frac=0.001)
-    Wqs, sgs, refs = [], [], []
-    for g, N in enumerate(Ns):
-        W = synth.normal(180 + g, (N, K), 0.02)
-        Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
-        refs.append(orc.w4a8g_linear(X, Wq_ref, sg_ref, gs))
-        Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
-        Wqs.append(Wq)
-        sgs.append(sg)
-    Ys = w4.w4a8g_linear_grouped(to_dev(X), Wqs, sgs, gs, flags=w4.LAUNCH_PDL)
-    torch.cuda.synchronize()
-    for Y, (Y_ref, B, _, _) in zip(Ys, refs):
-        assert_within_bound(Y.cpu().numpy(), Y_ref, B, K)
-
-
-@pytest.mark.parametrize("splits", [2, 3, 5, 16])
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 16])
 @pytest.mark.parametrize("fused", [True, False])
 def test_w4a8g_split_k(w4, orc, splits, fused):
-    # pieces that start inside a scale word: the windows are widened to whole
-    # 16-byte words and indexed from their remainder
-    w4.w4a8_set_tuning(force_splits=splits, rowdot_max_m=1)  # the dp4a kernel's split plans
-    check_group(w4, orc, 2, 3584, 300, 128, 30 + splits, fused=fused)
-    check_group(w4, orc, 1, 18944, 70, 64, 40 + splits, fused=fused)
+    """K pieces of whole chunks, every count up to one chunk per piece: the
+    same bits as the oracle (the chunk sums are added in chunk order by the
+    CTA that finishes a tile last)."""
+    w4.w4a8_set_tuning(force_splits=splits)
+    for (M, K, N, gs, seed) in [(2, 3584, 300, 128, 30), (1, 18944, 70, 64, 40), (5, 8192, 200, 2048, 50)]:
+        p = w4.w4a8g_plan_info(M, K, N, gs)
+        nch = -(-K // max(gs, 1024))
+        assert p["kernel"] == 2 and p["splits"] == -(-nch // -(-nch // min(splits, nch)))
+        check_group(w4, orc, M, K, N, gs, seed + splits, fused=fused)
 
 
-@pytest.mark.parametrize("cl", [1, 4, 32, 256])
-def test_w4a8g_threads_per_row(w4, orc, cl):
-    w4.w4a8_set_tuning(force_threads_per_row=cl)
-    check_group(w4, orc, 1, 3584, 150, 128, 50)
+def test_w4a8g_same_bits_at_every_batch(w4, orc):
+    """One activation row inside batches of 1 to 64 rows, on every kernel
+    and split count: the same output bits, those of the oracle."""
+    K, N, gs = 3584, 1000, 128
+    W = synth.normal(120, (N, K), 0.02)
+    Xb = synth.activation(121, 64, K, outlier_frac=0.001)
+    Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
+    Y_ref = orc.w4a8g_linear_f32(Xb[:1], Wq_ref, sg_ref, gs)[0]
+    Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
+    seen = set()
+    for M in (1, 2, 5, 8, 9, 16, 40, 64):
+        for path in PATHS:
+            for splits in (0, 1, 4):
+                if not route(w4, path, M, gs):
+                    continue
+                w4.w4a8_set_tuning(force_splits=splits, **PATHS[path])
+                p = w4.w4a8g_plan_info(M, K, N, gs)
+                seen.add((p["kernel"], p["splits"]))
+                Y = w4.w4a8g_linear(to_dev(Xb[:M]), Wq, sg, gs)
+                assert_exact(Y.cpu().numpy()[:1], Y_ref)
+    assert {k for k, _ in seen} == {1, 2} and {P for _, P in seen} >= {1, 4}
 
 
-def test_w4a8g_two_stage_ring(w4, orc):
-    w4.w4a8_set_tuning(ring_bytes=8192)
-    check_group(w4, orc, 1, 3584, 700, 128, 51)
-
-
-@pytest.mark.parametrize("path", ["default", "dp4a"])
-def test_w4a8g_exact_powers_of_two(w4, orc, path):
+def test_w4a8g_exact_powers_of_two(w4, orc):
     """Group scales 2^-e (e in 0..3) and integer activations with max 127
-    (s_a = 1): every granule sum, product and partial sum is exact in fp32,
-    so Y equals the oracle's binary64 value bit for bit."""
-    M, K, N, gs = 3, 1024, 300, 64
+    (s_a = 1): every group sum, product and partial sum is exact in fp32,
+    so Y equals the oracle's binary64 value bit for bit on every path."""
+    M, K, N, gs = 3, 1024, 300, 128
     rng = np.random.Generator(np.random.PCG64(77))
     G = K // gs
     q = rng.integers(-7, 8, size=(N, G, gs))
@@ -249,13 +262,9 @@ def test_w4a8g_exact_powers_of_two(w4, orc, path):
     Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
     Y_ref, B, _, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
     assert np.all(sa_ref == 1.0)
-    for splits in (0, 3):
-        if path == "dp4a":
-            w4.w4a8_set_tuning(force_splits=splits, rowdot_max_m=1, mma_min_m=65)
-        else:
-            w4.w4a8_set_tuning()
-            assert w4.w4a8g_plan_info(M, K, N, gs)["kernel"] == 2
-        Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
+    Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
+    for path in PATHS:
+        route(w4, path, M, gs)
         Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs)
         torch.cuda.synchronize()
         assert np.array_equal(Y.cpu().numpy().astype(np.float64), Y_ref)
@@ -271,25 +280,31 @@ def test_w4a8g_deterministic(w4, orc):
     assert torch.equal(Y1, Y2)
 
 
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("M,K,Ns,gs,splits", [
     (1, 3584, [3584, 512, 512], 128, 0), (1, 3584, [300, 17], 128, 3),
     (2, 896, [64, 100, 33, 5], 128, 0), (4, 1024, [100, 60], 32, 2),
+    (8, 3584, [3584, 512, 512], 128, 0), (16, 3584, [1000, 300], 128, 0),
 ])
-def test_w4a8g_linear_grouped(w4, orc, M, K, Ns, gs, splits):
-    w4.w4a8_set_tuning(force_splits=splits)
+def test_w4a8g_linear_grouped(w4, orc, M, K, Ns, gs, splits, path):
+    if not route(w4, path, M, gs):
+        pytest.skip("the routing does not serve this call")
+    w4.w4a8_set_tuning(force_splits=splits, **PATHS[path])
     X = synth.activation(70 + len(Ns), M, K, outlier_frac=0.001)
     Wqs, sgs, refs = [], [], []
     for g, N in enumerate(Ns):
         W = synth.normal(80 + g, (N, K), 0.02)
         Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
-        refs.append(orc.w4a8g_linear(X, Wq_ref, sg_ref, gs))
+        refs.append(orc.w4a8g_linear_f32(X, Wq_ref, sg_ref, gs)[0])
         Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
         Wqs.append(Wq)
         sgs.append(sg)
-    Ys = w4.w4a8g_linear_grouped(to_dev(X), Wqs, sgs, gs)
+    gws = guards.workspace(w4.w4a8g_workspace_bytes(M, K, sum(Ns), gs))
+    Ys = w4.w4a8g_linear_grouped(to_dev(X), Wqs, sgs, gs, ws=guards.t(gws), flags=w4.LAUNCH_PDL)
     torch.cuda.synchronize()
-    for Y, (Y_ref, B, _, _) in zip(Ys, refs):
-        assert_within_bound(Y.cpu().numpy(), Y_ref, B, K)
+    guards.check_all(gws)
+    for Y, Y_ref in zip(Ys, refs):
+        assert_exact(Y.cpu().numpy(), Y_ref)
 
 
 def test_w4a8g_rejects(w4):
@@ -320,7 +335,7 @@ QWEN2_LAUNCHES = [[("q", 3584, 3584), ("k", 3584, 512), ("v", 3584, 512)], [("o"
                   [("lm_head", 3584, 152064)]]
 
 
-def sample_rows(N, seed, n=40):
+def sample_rows(N, seed, n=64):
     rng = np.random.Generator(np.random.PCG64(seed))
     rows = set(rng.choice(N, size=min(n, N), replace=False).tolist()) | {0, N - 1}
     return np.array(sorted(rows), np.int64)
@@ -333,7 +348,7 @@ def test_w4a8g_qwen2_fullsize(w4, orc, li):
     K = mats[0][1]
     seed0 = 2000 + 10 * li
     X = synth.activation(seed0 + 500, 1, K, outlier_frac=0.001)
-    Wqs, sgs, rows_all = [], [], []
+    Wqs, sgs = [], []
     for g, (_, _, N) in enumerate(mats):
         W = synth.normal_gpu(seed0 + g, (N, K), 0.02)
         Wq, sg = w4.w4g_quantize_weights(W, gs)
@@ -352,21 +367,20 @@ def test_w4a8g_qwen2_fullsize(w4, orc, li):
         idx = torch.from_numpy(rows).cuda()
         assert np.array_equal(Wqs[g][idx].cpu().numpy(), Wq_ref)
         assert np.array_equal(bits(sgs[g][idx].cpu().numpy()), bits(sg_ref))
-        Y_ref, B, _, _ = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
-        assert_within_bound(Ys[g].cpu().numpy()[:, rows], Y_ref, B, K)
+        Y_ref = orc.w4a8g_linear_f32(X, Wq_ref, sg_ref, gs)[0]
+        assert_exact(Ys[g].cpu().numpy()[:, rows], Y_ref)
 
 
-@pytest.mark.parametrize("path", ["default", "tensor_cores"])
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("M,K,N,gs,seed", [
-    (1, 131072, 5, 128, 110),     # longest rows, dp4a
-    (2, 131072, 3, 32, 111),      # longest rows, smallest groups (dp4a when forced)
-    (5, 131072, 7, 1024, 112),    # longest rows (row-per-thread; the tensor cores when forced)
+    (1, 131072, 5, 128, 110),     # longest rows
+    (2, 131072, 3, 32, 111),      # longest rows, smallest groups
+    (5, 131072, 7, 1024, 112),    # longest rows, one-group chunks
     (4, 131072, 1, 16384, 113),   # largest tensor-core group, one output row
+    (8, 131072, 2, 65536, 115),   # two groups per row, each a chunk of its own
     (1, 3584, 1, 128, 114),       # one output row
 ])
 def test_w4a8g_maximum_sizes(w4, orc, M, K, N, gs, seed, path):
-    if path == "tensor_cores":
-        if M == 1:
-            pytest.skip("one row runs on the dp4a kernel on both paths")
-        w4.w4a8_set_tuning(rowdot_max_m=1)
+    if not route(w4, path, M, gs):
+        pytest.skip("the routing does not serve this call")
     check_group(w4, orc, M, K, N, gs, seed)

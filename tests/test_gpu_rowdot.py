@@ -215,133 +215,3 @@ def test_rowdot_matches_other_kernels(w4):
         outs.append(w4.w4a8_linear(X, Wq, sw).cpu().numpy())
     assert np.array_equal(bits(outs[0]), bits(outs[1]))
     assert np.array_equal(bits(outs[0]), bits(outs[2]))
-
-
-# ---------------------------------------------------------------------------
-# group-wise scales on the row-per-thread kernel: one fp32 fold per 32-code
-# granule, checked against the oracle's binary64 value within
-# (K/32 + 4) * 2^-24 * B (B = s_a * sum_g s_g * sum |Xq * q|)
-# ---------------------------------------------------------------------------
-
-def check_group(w4, orc, M, K, N, gs, seed, fused=True, flags=0):
-    assert w4.w4a8g_plan_info(M, K, N, gs)["kernel"] == 2
-    W = synth.normal(seed, (N, K), 0.02)
-    W[1 % N] = 0.0                        # a zero row
-    if K // gs > 1:
-        W[0, gs:2 * gs] = 0.0             # a zero group inside a non-zero row
-    X = synth.activation(seed + 7, M, K, outlier_frac=0.001)
-    X[M - 1] = 0
-    Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
-    Y_ref, B, Xq_ref, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
-    Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
-    gY = guards.out((M, N), torch.float32)
-    gXq, gsa = guards.out((M, K), torch.int8), guards.out((M,), torch.float32)
-    gws = guards.workspace(w4.w4a8g_workspace_bytes(M, K, N, gs))
-    Xq, sa = gXq.t, gsa.t
-    if fused:
-        Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs, Y=gY.t, Xq_out=Xq, sa_out=sa,
-                            ws=guards.t(gws), flags=flags)
-    else:
-        w4.act_quantize_i8(to_dev(X), Xq=Xq, sa=sa)
-        Y = w4.w4a8g_gemv(Xq, sa, Wq, sg, gs, Y=gY.t, ws=guards.t(gws), flags=flags)
-    guards.check_all(gY, gXq, gsa, gws)
-    assert np.array_equal(Xq.cpu().numpy(), Xq_ref)
-    assert np.array_equal(bits(sa.cpu().numpy()), bits(sa_ref))
-    Yh = Y.cpu().numpy().astype(np.float64)
-    bound = (K / 32 + 4) * 2.0 ** -24 * B
-    bad = np.argwhere(np.abs(Yh - Y_ref) > bound)
-    assert bad.size == 0, (bad[:5], Yh[tuple(bad[0])], Y_ref[tuple(bad[0])])
-    assert np.isfinite(Yh).all()
-    assert not Yh[:, 1 % N].any() and not Yh[M - 1].any()
-
-
-ROWDOT_GROUP_SHAPES = [
-    (2, 3584, 1000, 128, 800),   # split K, groups of half a box
-    (3, 1024, 77, 32, 801),      # the smallest groups
-    (4, 3584, 300, 64, 802),
-    (5, 768, 129, 256, 803),     # one group per box, one row past a tile
-    (6, 4096, 40000, 512, 804),  # one piece per tile, groups of two boxes
-    (7, 288, 7, 32, 805),        # a partial last box
-    (8, 18944, 700, 128, 806),   # long rows, pieces
-    (8, 4096, 64, 4096, 807),    # one group per row, pieces inside it
-    (4, 2048, 5, 1024, 808),     # pieces that start inside a group
-]
-
-
-@pytest.mark.parametrize("fused", [True, False])
-@pytest.mark.parametrize("M,K,N,gs,seed", ROWDOT_GROUP_SHAPES)
-def test_rowdot_group_parity(w4, orc, M, K, N, gs, seed, fused):
-    check_group(w4, orc, M, K, N, gs, seed, fused=fused)
-
-
-@pytest.mark.parametrize("M,N", [(2, 300), (5, 5000), (8, 96)])
-def test_rowdot_group_exact(w4, orc, M, N):
-    """Power-of-two group scales and integer activations: every granule
-    term, fold and partial sum is exact in fp32, so Y equals the oracle bit
-    for bit (small N: many K pieces and their fp32 partials)."""
-    K, gs = 2048, 64
-    rng = np.random.Generator(np.random.PCG64(820 + M))
-    G = K // gs
-    q = rng.integers(-7, 8, size=(N, G, gs))
-    q[:, :, 0] = 7 * rng.choice([-1, 1], size=(N, G))
-    e = rng.integers(0, 4, size=(N, G, 1))
-    W = (q * 2.0 ** -e).reshape(N, K).astype(np.float32)
-    X = rng.integers(-126, 127, size=(M, K)).astype(np.float16)
-    X[:, 5] = 127
-    Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
-    Y_ref, _, _, sa_ref = orc.w4a8g_linear(X, Wq_ref, sg_ref, gs)
-    assert np.all(sa_ref == 1.0)
-    assert w4.w4a8g_plan_info(M, K, N, gs)["kernel"] == 2
-    Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
-    Y = w4.w4a8g_linear(to_dev(X), Wq, sg, gs)
-    torch.cuda.synchronize()
-    assert np.array_equal(Y.cpu().numpy().astype(np.float64), Y_ref)
-
-
-def test_rowdot_group_grouped_graph_and_tickets(w4, orc):
-    """Grouped group-scale launches (eager, PDL, a replayed graph) on one
-    workspace; the tickets of the split plans are handed back each call."""
-    M, K, gs, Ns = 4, 3584, 128, (1000, 129, 7)
-    X = synth.activation(830, M, K, outlier_frac=0.001)
-    Wqs, sgs, refs = [], [], []
-    for g, N in enumerate(Ns):
-        W = synth.normal(831 + g, (N, K), 0.02)
-        Wq_ref, sg_ref = orc.w4g_quantize(W, gs)
-        refs.append(orc.w4a8g_linear(X, Wq_ref, sg_ref, gs))
-        Wq, sg = w4.w4g_quantize_weights(to_dev(W), gs)
-        Wqs.append(Wq)
-        sgs.append(sg)
-    Xd = to_dev(X)
-
-    def check(Ys):
-        for Y, (Y_ref, B, _, _) in zip(Ys, refs):
-            Yh = Y.cpu().numpy().astype(np.float64)
-            assert np.all(np.abs(Yh - Y_ref) <= (K / 32 + 4) * 2.0 ** -24 * B)
-
-    first = None
-    for rep in range(2):
-        Ys = w4.w4a8g_linear_grouped(Xd, Wqs, sgs, gs, flags=w4.LAUNCH_PDL if rep else 0)
-        torch.cuda.synchronize()
-        check(Ys)
-        if first is None:
-            first = [y.clone() for y in Ys]
-        else:
-            assert all(torch.equal(a, b) for a, b in zip(first, Ys))  # deterministic
-    Ys = [torch.empty((M, N), dtype=torch.float32, device="cuda") for N in Ns]
-    ws = torch.zeros((w4.w4a8g_workspace_bytes(M, K, sum(Ns), gs),), dtype=torch.uint8, device="cuda")
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        w4.w4a8g_linear_grouped(Xd, Wqs, sgs, gs, Ys=Ys, ws=ws, flags=w4.LAUNCH_PDL)
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        w4.w4a8g_linear_grouped(Xd, Wqs, sgs, gs, Ys=Ys, ws=ws, flags=w4.LAUNCH_PDL)
-    for _ in range(2):
-        for Y in Ys:
-            Y.zero_()
-        g.replay()
-        torch.cuda.synchronize()
-        check(Ys)
-        assert all(torch.equal(a, b) for a, b in zip(first, Ys))
