@@ -226,7 +226,7 @@ def measured_peak():
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_weight_quantized_w4a8_gb300", "csrc")
-    for name in ("gemv_kernel.cuh", "gemv.cu", "gemv_group.cu", "plan.h", "ptx.cuh", "actq.cuh"):
+    for name in ("gemv_kernel.cuh", "gemv.cu", "plan.h", "ptx.cuh", "actq.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
