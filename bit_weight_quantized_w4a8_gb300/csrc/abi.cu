@@ -151,7 +151,7 @@ bool mma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::MmaPlan* pl, int sms = 
     if (M < (t > 0 ? t : group > 0 ? kDefaultMmaMinMGroup : kDefaultMmaMinM)) return false;
     if (group > 0 && (group % 128 || group > 16384)) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
-    return w4a8::make_mma_plan((int)M, K, N, sms, pl, (int)(group / 64));
+    return w4a8::make_mma_plan((int)M, K, N, sms, pl, (int)(group / 64), g_force_splits.load());
 }
 
 // Warp-level e4m3 MMA plan for an M-row row-wise W4A8 call, or false when
@@ -493,7 +493,7 @@ int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const ui
         // one plan per matrix inside; the workspace bound covers every N[g] <= total
         for (int g = 0; g < G; ++g) {
             w4a8::MmaPlan pg;
-            if (!w4a8::make_mma_plan((int)M, K, N[g], mp.sms, &pg) || pg.ws_bytes > mp.ws_bytes)
+            if (!w4a8::make_mma_plan((int)M, K, N[g], mp.sms, &pg, 0, mp.force_p) || pg.ws_bytes > mp.ws_bytes)
                 return fail(W4A8_ERR_SHAPE, "no tensor-core plan for group %d", g);
         }
         if ((st = check_mma_workspace(mp, ws, ws_bytes)) != W4A8_OK) return st;
@@ -558,7 +558,7 @@ int w4a8g_run(const char* name, const uint16_t* X, const int8_t* Xq, const float
         // one plan per matrix inside; the workspace bound covers every N[g] <= total
         for (int g = 0; g < G; ++g) {
             w4a8::MmaPlan pg;
-            if (!w4a8::make_mma_plan((int)M, K, N[g], mp.sms, &pg, (int)(group / 64)) ||
+            if (!w4a8::make_mma_plan((int)M, K, N[g], mp.sms, &pg, (int)(group / 64), mp.force_p) ||
                 pg.ws_bytes > mp.ws_bytes)
                 return fail(W4A8_ERR_SHAPE, "%s: no tensor-core plan for group %d", name, g);
         }
@@ -938,6 +938,15 @@ extern "C" int w4a8_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, cons
         return fail(W4A8_ERR_SHAPE, "w4a8_linear_noalloc: M=%lld outside [1, %d]", (long long)M, kRowGroupW4);
     if (!aligned(X, 16) || !aligned(Wq, 16) || !aligned(Y, 4) || !aligned(sw, 4))
         return fail(W4A8_ERR_ALIGN, "w4a8_linear_noalloc: X/Wq need 16-byte, Y/sw 4-byte alignment");
+    // the kernel w4a8_linear picks, when its workspace fits the scratch
+    const size_t need = w4a8_workspace_bytes(M, K, N);
+    if (need > 0 && need <= kNoAllocScratchBytes) {
+        void* scratch = nullptr;
+        if ((st = noalloc_scratch(&scratch)) != W4A8_OK) return st;
+        return w4a8_linear(X, M, K, Wq, sw, N, Y, nullptr, nullptr, nullptr, scratch, kNoAllocScratchBytes,
+                           flags, stream);
+    }
+    // else the dp4a GEMV, one launch, when its split-K scratch fits
     w4a8::GemvPlan pl;
     if ((st = plan_for(true, true, M, K, N, &pl)) != W4A8_OK) return st;
     if (pl.ws_bytes > kNoAllocScratchBytes)

@@ -37,7 +37,7 @@ cudaError_t read_and_clear_device_error(unsigned* flags, cudaStream_t stream);
 
 // Tensor-core path (mma.cu).  make_mma_plan is host-only and needs no GPU.
 // gkb > 0: group-wise scales, groups of gkb 64-code K blocks (gs = 64 gkb).
-bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int gkb = 0);
+bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int gkb = 0, int force_p = 0);
 // gs > 0: group-wise scales sg[g] ([N][stride] fp32, gs a multiple of 128,
 // at most 16384); sw is then unused.
 cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* Xq, const float* sa,

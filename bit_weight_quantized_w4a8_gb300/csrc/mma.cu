@@ -79,6 +79,11 @@ constexpr int kMmaSmem = kOffSaSum + 256 + 1024;  // + slack to align the base t
 constexpr int kAQThreads = 256;
 // Group scales: the most workspace the chunk sums of a split call may take.
 constexpr size_t kGroupPartBytes = 32u << 20;
+// Row-wise split K: up to this many pieces store int32 slices that the last
+// CTA of a tile adds to the sums it holds; more pieces add into one int32
+// accumulator per tile with atomics (the reduction spread over every CTA),
+// which the last CTA reads and clears.
+constexpr int kSliceMaxP = 3;
 
 static_assert(kWBlocks % kStageK == 0, "stage geometry");
 static_assert(kOffB % 1024 == 0 && kOffW % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -102,7 +107,8 @@ struct MmaArgs {
     const float* sa;        // [M]
     float* Y;               // [M][N]
     int32_t* acc_out;       // optional [M][N]
-    int32_t* part;          // [tiles][M][128] int32 accumulators when P > 1 (zeroed by the pre-pass)
+    int32_t* part;          // [tiles][P][M][128] int32 piece slices when 1 < P <= kSliceMaxP
+    int32_t* acc;           // [tiles][M][128] int32 accumulators when P > kSliceMaxP (zero between calls)
     unsigned* tickets;      // [tiles] when P > 1, zero between calls
     // group scales: sg [N][gld] fp32, gkb K blocks per group; with P > 1 the
     // fold's chunk sums go to part_f [tiles][nch][M][128] (chunks of
@@ -147,7 +153,8 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
 // max|x| (exact in binary16), s_a = max/127 by IEEE division, and quantizes
 // its piece with the fast exact quantizer (actq.cuh); when X is null it
 // widens the given int8 codes Xq instead.  Optional int8 codes and scale
-// outputs for the caller.  It also zeroes the int32 split-K accumulators.
+// outputs for the caller.  It also zeroes the int32 accumulators of the
+// atomic split plans that follow (acc_words of them).
 __global__ void __launch_bounds__(kAQThreads) act_codes_kernel(
     const __half* __restrict__ X, const int8_t* __restrict__ Xq, const float* __restrict__ sa_in,
     int M, int64_t K, int BN, uint8_t* __restrict__ B, float* __restrict__ sa_ws,
@@ -156,7 +163,6 @@ __global__ void __launch_bounds__(kAQThreads) act_codes_kernel(
     __shared__ float red[kAQThreads / 32];
     griddep_launch_dependents();
     griddep_wait();
-    // clear the split-K accumulators of the launches that follow
     for (int64_t e = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * kAQThreads + threadIdx.x; e < acc_words;
          e += (int64_t)gridDim.x * gridDim.y * kAQThreads)
         acc[e] = 0;
@@ -413,9 +419,13 @@ __device__ __forceinline__ uint2 int4x8_to_e4m3(uint32_t w) {
 // MMA (kind::f8f6f4, K = 32) covers twice the weights of a kind::f16 MMA;
 // D holds W.A_hi in columns 0..BN-1 and W.A_lo in BN..2BN-1, both exact
 // integers in fp32, and acc = 16 D_hi + D_lo.
-template <bool kG, bool kF8>
+// kAtomic (row-wise plans with more than kSliceMaxP K pieces): the atomic
+// split epilogue, compiled apart so that the register-held epilogue of the
+// other plans does not raise this variant's register allocation.
+template <bool kG, bool kF8, bool kAtomic>
 __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_constant__ MmaArgs a) {
     static_assert(!(kG && kF8), "the e4m3 path has row-wise scales only");
+    static_assert(!(kG && kAtomic), "group scales add their chunk sums in order");
     constexpr int S = kG ? kStagesG : kStages;          // stage ring in use
     constexpr uint32_t kA0 = kF8 ? kTmemAF8 : kG ? kTmemAG : kTmemA;  // first A stage column
     constexpr uint32_t kAStage = kF8 ? 32 : kTmemAStage;               // A columns per stage
@@ -762,44 +772,46 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
             const bool ok = __all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(accfull), 0, abort_flag));
             tc_fence_after_sync();
             // the TMEM lanes this warp may read are its converter lanes (q, r);
-            // the two warps of a quarter split the columns
+            // the two warps of a quarter split the columns: ch = cg + 2j
             const int n = n0 + r;
             const float swv = (ok && n < a.N) ? a.sw[n] : 0.f;
-            for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
-                uint32_t v[8], vl[8];
-                tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(8 * ch), v);
-                if constexpr (kF8) tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN + 8 * ch), vl);
-                if (!ok || n >= a.N) continue;
-                #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const int m = 8 * ch + t;
-                    if (m >= a.M) break;
-                    // e4m3: D = 2^-9 sum v b (weight bytes v = q + 8), so 512 D is an
-                    // exact integer and sum q a = 16 U_hi + U_lo - 8 sum a
-                    const int32_t raw = kF8 ? 16 * __float2int_rn(__uint_as_float(v[t]) * 512.f) +
-                                                  __float2int_rn(__uint_as_float(vl[t]) * 512.f)
-                                            : __float2int_rn(__uint_as_float(v[t]));
-                    const int64_t o = (int64_t)m * a.N + n;
-                    if (a.P == 1) {
-                        const int32_t acc = kF8 ? raw - 8 * sa_sum[m] : raw;
-                        a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), swv), a.sa[m]);
-                        if (a.acc_out != nullptr) a.acc_out[o] = acc;
-                    } else {
-                        atomicAdd(a.part + ((int64_t)tile * a.M + m) * kTileRows + r, raw);  // exact, order-free
+            // e4m3: D = 2^-9 sum v b (weight bytes v = q + 8), so 512 D is an
+            // exact integer and sum q a = 16 U_hi + U_lo - 8 sum a
+            auto exact_sum = [&](uint32_t v, uint32_t vl) -> int32_t {
+                return kF8 ? 16 * __float2int_rn(__uint_as_float(v) * 512.f) + __float2int_rn(__uint_as_float(vl) * 512.f)
+                           : __float2int_rn(__uint_as_float(v));
+            };
+            auto rescale = [&](int m, int64_t o, int32_t raw, float swn) {
+                const int32_t acc = kF8 ? raw - 8 * sa_sum[m] : raw;
+                a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), swn), a.sa[m]);
+                if (a.acc_out != nullptr) a.acc_out[o] = acc;
+            };
+            if constexpr (kAtomic) {
+                // split K into many pieces: every piece adds its sums into the
+                // tile's int32 accumulator [M][128] (integer addition: exact,
+                // order-free; the reduction spread over every CTA); the last
+                // CTA rescales the totals and clears them for the next matrix
+                // or call.  Every converter warp meets at the barrier.
+                int32_t* acc_t = a.acc + (int64_t)tile * a.M * kTileRows;
+                for (int ch = cg; ch < BN / 8; ch += kConvGroups) {
+                    uint32_t v[8], vl[8];
+                    tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(8 * ch), v);
+                    if constexpr (kF8) tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN + 8 * ch), vl);
+                    if (!ok) continue;
+                    #pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const int m = 8 * ch + t;
+                        if (m >= a.M) break;
+                        atomicAdd(acc_t + (int64_t)m * kTileRows + r, exact_sum(v[t], vl[t]));
                     }
                 }
-            }
-            if (a.P > 1) {
-                // the pieces' int32 sums were added atomically (integer addition
-                // is exact and order-free); the last CTA of the tile rescales them
                 __threadfence();
                 named_bar_sync(1, kConvWarps * 32);
-                if (ct == 0) *last_flag = (atomicAdd(a.tickets + tile, 1u) == (unsigned)(a.P - 1));
+                if (ct == 0) *last_flag = !*abort_flag && (atomicAdd(a.tickets + tile, 1u) == (unsigned)(a.P - 1));
                 named_bar_sync(1, kConvWarps * 32);
                 if (*last_flag) {
                     __threadfence();
                     const int rows = min(kTileRows, a.N - n0);
-                    int32_t* acc_t = a.part + (int64_t)tile * a.M * kTileRows;
                     constexpr int kBatch = 8;  // loads in flight per thread
                     for (int e0 = ct; e0 < a.M * kTileRows; e0 += kConvWarps * 32 * kBatch) {
                         int32_t v[kBatch];
@@ -812,16 +824,85 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
                         for (int b = 0; b < kBatch; ++b) {
                             const int e = e0 + b * kConvWarps * 32;
                             if (e >= a.M * kTileRows) break;
-                            __stcg(acc_t + e, 0);  // clear for the next matrix of a grouped call
+                            __stcg(acc_t + e, 0);
                             const int m = e / kTileRows, rr = e % kTileRows, nn = n0 + rr;
-                            if (rr >= rows) continue;
-                            const int64_t o = (int64_t)m * a.N + nn;
-                            const int32_t acc = kF8 ? v[b] - 8 * sa_sum[m] : v[b];
-                            a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(acc), a.sw[nn]), a.sa[m]);
-                            if (a.acc_out != nullptr) a.acc_out[o] = acc;
+                            if (rr < rows) rescale(m, (int64_t)m * a.N + nn, v[b], a.sw[nn]);
                         }
                     }
                     if (ct == 0) a.tickets[tile] = 0u;  // ready for the next call
+                }
+            } else {
+                int32_t raw[4][8];  // this thread's exact sums (e4m3: before the bias)
+                #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int ch = cg + kConvGroups * j;
+                    #pragma unroll
+                    for (int t = 0; t < 8; ++t) raw[j][t] = 0;
+                    if (ch < BN / 8) {  // uniform over the warp
+                        uint32_t v[8], vl[8];
+                        tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(8 * ch), v);
+                        if constexpr (kF8) tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN + 8 * ch), vl);
+                        #pragma unroll
+                        for (int t = 0; t < 8; ++t) raw[j][t] = exact_sum(v[t], vl[t]);
+                    }
+                }
+                // the outputs of this thread's row and columns from its exact sums
+                auto write_out = [&]() {
+                    if (!ok || n >= a.N) return;
+                    #pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        #pragma unroll
+                        for (int t = 0; t < 8; ++t) {
+                            const int m = 8 * (cg + kConvGroups * j) + t;
+                            if (m < a.M) rescale(m, (int64_t)m * a.N + n, raw[j][t], swv);
+                        }
+                    }
+                };
+                if (a.P == 1) {
+                    write_out();
+                } else {
+                    // split K into a few pieces: every piece stores its int32
+                    // slice [M][128] with plain stores; the CTA that takes the
+                    // tile's last ticket adds the other pieces' values to the
+                    // sums it holds (integer addition: exact, order-free), each
+                    // thread for its own outputs with all its loads of a piece
+                    // in flight at once.  Every converter warp meets at the
+                    // barrier.
+                    int32_t* part_t = a.part + (int64_t)tile * a.P * a.M * kTileRows + r;
+                    const int64_t slice = (int64_t)a.M * kTileRows;
+                    if (ok) {
+                        #pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            #pragma unroll
+                            for (int t = 0; t < 8; ++t) {
+                                const int m = 8 * (cg + kConvGroups * j) + t;
+                                if (m < a.M) __stcg(part_t + p * slice + (int64_t)m * kTileRows, raw[j][t]);
+                            }
+                    }
+                    __threadfence();
+                    named_bar_sync(1, kConvWarps * 32);
+                    if (ct == 0) *last_flag = !*abort_flag && (atomicAdd(a.tickets + tile, 1u) == (unsigned)(a.P - 1));
+                    named_bar_sync(1, kConvWarps * 32);
+                    if (*last_flag) {
+                        __threadfence();
+                        for (int pp = 0; pp < a.P; ++pp) {
+                            if (pp == p) continue;
+                            int32_t o[4][8];
+                            #pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                #pragma unroll
+                                for (int t = 0; t < 8; ++t) {
+                                    const int m = 8 * (cg + kConvGroups * j) + t;
+                                    o[j][t] = m < a.M ? __ldcg(part_t + pp * slice + (int64_t)m * kTileRows) : 0;
+                                }
+                            #pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                #pragma unroll
+                                for (int t = 0; t < 8; ++t) raw[j][t] += o[j][t];
+                        }
+                        write_out();
+                        if (ct == 0) a.tickets[tile] = 0u;  // ready for the next call
+                    }
                 }
             }
         }
@@ -892,7 +973,7 @@ bool make_w4_tile_map(void* map, const uint8_t* Wq, int64_t K, int64_t N) {
                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int gkb) {
+bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int gkb, int force_p) {
     if (M < 1 || M > 64 || K < 32 || K % 32 || N < 1 || N > 0x7FFFFFFF) return false;
     // group scales: groups of gkb K blocks, whole stages, each group's sums
     // exact in fp32 (at most 256 K blocks)
@@ -907,6 +988,11 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int g
     int P = 1;
     const int slots = 2 * num_sms;  // resident CTAs
     if (pl.tiles < slots * 4 / 5) P = slots / pl.tiles;
+    // a split pays a fixed tail (the partials, a ticket, the last CTA's
+    // adds): for a second CTA per SM (at most 2 pieces) worth it only for
+    // pieces of at least 16 K blocks (1024 codes), else of at least 8
+    if (P > (P <= 2 ? pl.nkb / 16 : pl.nkb / 8)) P = P <= 2 ? pl.nkb / 16 : pl.nkb / 8;
+    if (force_p > 0) P = force_p;
     if (P < 1) P = 1;
     // row-wise scales: pieces of at most 256 K blocks keep the integer sums
     // exact; group scales: each group's D is exact on its own, pieces hold
@@ -931,12 +1017,13 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int g
     if (pl.P > 1 && pl.tiles > kTicketSlots) return false;
     if ((int64_t)pl.tiles * pl.P > 0x7FFFFFFF) return false;
     pl.grid = pl.tiles * pl.P;
+    pl.force_p = force_p;
     pl.smem = kMmaSmem;
     pl.sms = num_sms;
     pl.stages = kWStages;
     pl.stage_bytes = kWTileBytes;
     // workspace: tickets, scales (64 floats), bf16 code tiles [nkb][BN][64], then
-    // int32 [M][128] accumulators per tile for split plans.  The region is
+    // int32 [P][M][128] piece sums per tile for split plans.  The region is
     // sized for any N' <= N on this device (grouped launches run one plan
     // per weight matrix): K is split when the exactness limit forces it
     // (every tile) or when a matrix has fewer tiles than 4/5 of the CTA slots.
@@ -946,16 +1033,26 @@ bool make_mma_plan(int M, int64_t K, int64_t N, int num_sms, MmaPlan* out, int g
     // (K blocks rounded up to an even count: the e4m3 tiles cover 128 codes)
     pl.off_part = round_up_sz(pl.off_codes + (size_t)((pl.nkb + 1) / 2 * 2) * pl.BN * kKBlock * 2, 256);
     const int64_t small = 2 * num_sms * 4 / 5;
-    const int64_t tmax = pmin > 1 ? pl.tiles : (pl.tiles < small ? pl.tiles : small);
+    // row-wise scales: an int32 slice [M][128] per tile and K piece.  A split
+    // by the tiles keeps tiles' * P' <= the CTA slots; one forced by the
+    // exactness limit or the tuning has at most tiles * max(pmin, force_p).
+    int64_t units = slots;
+    if (pmin > 1 && units < (int64_t)pl.tiles * pmin) units = (int64_t)pl.tiles * pmin;
+    if (force_p > 1 && units < (int64_t)pl.tiles * force_p) units = (int64_t)pl.tiles * force_p;
+    if (pl.P > 1 && units < (int64_t)pl.tiles * pl.P) units = (int64_t)pl.tiles * pl.P;
     // group scales: the chunk sums of a split matrix (a split needs fewer
     // tiles than 4/5 of the CTA slots and at most kGroupPartBytes of sums)
-    size_t part = (size_t)tmax * M * kTileRows * 4;
+    size_t part = (size_t)units * M * kTileRows * 4;
     if (gkb) {
         const size_t tb = (size_t)(pl.tiles < small ? pl.tiles : small);
         part = nch > 1 ? tb * nch * M * kTileRows * 4 : 0;
         if (part > kGroupPartBytes) part = kGroupPartBytes;
     }
-    pl.ws_bytes = pl.off_part + round_up_sz(part, 256);
+    pl.off_acc = pl.off_part + round_up_sz(part, 256);
+    // the atomic accumulators (row-wise plans with more than kSliceMaxP
+    // pieces), apart from the slices so that a grouped call may mix both
+    const size_t accb = gkb ? 0 : (size_t)units * M * kTileRows * 4;
+    pl.ws_bytes = pl.off_acc + round_up_sz(accb, 256);
     *out = pl;
     return true;
 }
@@ -976,11 +1073,16 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
         const __half* xh = reinterpret_cast<const __half*>(X);
         int Mi = M, BNi = pl.BN;
         int64_t Kk = K;
-        int32_t* acc = reinterpret_cast<int32_t*>(wsb + pl.off_part);
-        // row-wise split plans accumulate int32 partials with atomics: zeroed here
-        // (group scales write their chunk sums whole)
-        int64_t acc_words = gkb ? 0 : (int64_t)((pl.ws_bytes - pl.off_part) / 4);
         int32_t* sum_part = reinterpret_cast<int32_t*>(wsb + pl.off_sum);
+        // the atomic split plans' accumulators: the most tiles of any matrix
+        int32_t* acc = reinterpret_cast<int32_t*>(wsb + pl.off_acc);
+        int64_t acc_words = 0;
+        for (int g = 0; g < G && !gkb; ++g) {
+            MmaPlan pg;
+            if (!make_mma_plan(M, K, Ns[g], pl.sms, &pg, 0, pl.force_p)) return cudaErrorInvalidValue;
+            if (pg.P > kSliceMaxP && (int64_t)pg.tiles * M * kTileRows > acc_words)
+                acc_words = (int64_t)pg.tiles * M * kTileRows;
+        }
         void* args[] = {&xh, &Xq, &sa, &Mi, &Kk, &BNi, &codes, &sa_ws, &Xq_out, &sa_out, &acc, &acc_words,
                         &sum_part};
         const int64_t vecs = e4m3 ? (K + 127) / 128 * 8 : (int64_t)pl.nkb * 8;  // per batch row
@@ -996,17 +1098,21 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(mma_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(mma_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(mma_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+        const void* fns[] = {reinterpret_cast<const void*>(mma_kernel<false, false, false>),
+                             reinterpret_cast<const void*>(mma_kernel<false, false, true>),
+                             reinterpret_cast<const void*>(mma_kernel<false, true, false>),
+                             reinterpret_cast<const void*>(mma_kernel<false, true, true>),
+                             reinterpret_cast<const void*>(mma_kernel<true, false, false>)};
+        for (const void* f : fns) {
+            e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+            if (e != cudaSuccess) return e;
+        }
         if (e != cudaSuccess) return e;
         attr_set[dev] = 1;
     }
     for (int g = 0; g < G; ++g) {
         MmaPlan pg;
-        if (!make_mma_plan(M, K, Ns[g], pl.sms, &pg, gkb)) return cudaErrorInvalidValue;
+        if (!make_mma_plan(M, K, Ns[g], pl.sms, &pg, gkb, pl.force_p)) return cudaErrorInvalidValue;
         MmaArgs a;
         memset(&a, 0, sizeof(a));
         if (!encode_2d(&a.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq[g], (uint64_t)(K / 2), (uint64_t)Ns[g],
@@ -1025,6 +1131,7 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
         a.Y = Y[g];
         a.acc_out = (G == 1) ? acc_out : nullptr;
         a.part = reinterpret_cast<int32_t*>(wsb + pg.off_part);
+        a.acc = reinterpret_cast<int32_t*>(wsb + pg.off_acc);
         a.tickets = reinterpret_cast<unsigned*>(wsb);
         a.M = M;
         a.N = (int)Ns[g];
@@ -1036,9 +1143,12 @@ cudaError_t launch_w4a8_mma(const MmaPlan& pl, const uint16_t* X, const int8_t* 
         a.sum_part = reinterpret_cast<const int32_t*>(wsb + pl.off_sum);
         a.pre_pieces = pre_pieces;
         void* args[] = {&a};
-        const void* fn = gkb ? reinterpret_cast<const void*>(mma_kernel<true, false>)
-                       : e4m3 ? reinterpret_cast<const void*>(mma_kernel<false, true>)
-                              : reinterpret_cast<const void*>(mma_kernel<false, false>);
+        const bool atomic = !gkb && pg.P > kSliceMaxP;
+        const void* fn = gkb ? reinterpret_cast<const void*>(mma_kernel<true, false, false>)
+                       : e4m3 ? (atomic ? reinterpret_cast<const void*>(mma_kernel<false, true, true>)
+                                        : reinterpret_cast<const void*>(mma_kernel<false, true, false>))
+                              : (atomic ? reinterpret_cast<const void*>(mma_kernel<false, false, true>)
+                                        : reinterpret_cast<const void*>(mma_kernel<false, false, false>));
         e = launch_pdl(fn, dim3(pg.grid), dim3(kMmaThreads),
                        kMmaSmem, stream, flags, args);
         if (e != cudaSuccess) return e;

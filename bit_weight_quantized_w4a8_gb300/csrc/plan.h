@@ -65,9 +65,10 @@ struct MmaPlan {
     int tiles;         // 128-row weight tiles
     int nkb;           // 64-wide K blocks
     int P, kbp;        // K pieces, K blocks per piece
+    int force_p;       // requested K pieces (0 = by the tiles)
     int grid, smem, sms;
     int stages, stage_bytes;             // weight ring
-    size_t off_sa, off_sum, off_codes, off_part;  // workspace layout
+    size_t off_sa, off_sum, off_codes, off_part, off_acc;  // workspace layout
     size_t ws_bytes;
 };
 

@@ -101,7 +101,8 @@ typedef enum {
  * When the other kernels are switched off the dp4a GEMV serves batches too,
  * one launch per group of up to 8 rows (W8A16: always, 4 rows, fp32 FMAs),
  * each streaming the whole weight matrix.  w4a8_linear_noalloc takes at most
- * 8 rows, always on the dp4a GEMV. */
+ * 8 rows, on the kernel above whose workspace fits its static scratch, else
+ * on the dp4a GEMV in one launch. */
 #define W4A8_MAX_M 64
 #define W8A16_MAX_M 64
 
@@ -201,13 +202,15 @@ int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const ui
  * engine's per-token execute step or a framework plugin whose enqueue
  * function is not allowed to, because cudaMalloc can synchronise the device
  * and take unbounded time.
- *   Same arguments and results as w4a8_linear without the optional outputs:
- *   Y is bit-identical to w4a8_linear's for the same plan.
- * The split-K scratch is a static 4 MiB device array (W4A8_NOALLOC_SCRATCH
- * bytes: 4096 bytes of arrival counters, then int32 partials) that every GPU
- * loading the library holds until the process exits.  Shapes whose plan
- * needs more scratch are rejected with W4A8_ERR_WORKSPACE (at M = 1 and four
- * K pieces that is N > 261,888).  Each call that needs scratch looks up the
+ *   Same arguments and results as w4a8_linear without the optional outputs,
+ *   for 1 <= M <= 8: Y is bit-identical to w4a8_linear's.  The call runs the
+ *   kernel w4a8_linear would (the routing above) when that plan's workspace
+ *   fits the static scratch, else the dp4a GEMV in one launch.
+ * The scratch is a static 4 MiB device array (W4A8_NOALLOC_SCRATCH bytes:
+ * 4096 bytes of arrival counters, then the kernels' workspace) that every GPU
+ * loading the library holds until the process exits.  Shapes whose dp4a plan
+ * also needs more scratch are rejected with W4A8_ERR_WORKSPACE (at M = 1 and
+ * four K pieces that is N > 261,888).  Each call that needs scratch looks up the
  * array's device address on the current device (a lookup, no allocation);
  * the first call on a device may load the library's device code there, so
  * make it before any stream capture.  Every call on a device shares the one

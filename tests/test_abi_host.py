@@ -160,7 +160,8 @@ def check_mma_plan(p, M, K, N, sms):
     kbp = -(-nkb // P)
     assert kbp <= 256 and (P - 1) * kbp < nkb                   # pieces <= 16384, none empty
     assert p["smem_bytes"] <= 232448
-    assert p["ws_bytes"] >= 4096 + 256 + M * K * 2
+    # the codes, then one int32 slice [M][128] per tile and K piece of a split plan
+    assert p["ws_bytes"] >= 4096 + 256 + M * K * 2 + (tiles * P * M * 512 if P > 1 else 0)
 
 
 def check_qmma_plan(p, M, K, N, sms):
@@ -461,6 +462,28 @@ def test_rowdot_workspace_covers_grouped_matrices():
                     assert p["ws_bytes"] <= full["ws_bytes"], (M, K, Np, sms)
         p = w4.w4a8_plan_info(8, 3584, 152064, num_sms=152)  # lm_head: one piece per tile
         assert p["splits"] == 1 and p["ws_bytes"] < 2 * 1024 * 1024
+    finally:
+        w4.w4a8_set_tuning(reset=True)
+
+
+def test_mma_workspace_covers_grouped_matrices():
+    """The same for the tensor-core kernel: each matrix of a grouped call
+    (its own plan, its own K split) fits the workspace planned for the total
+    rows, with or without a forced split count."""
+    try:
+        for splits in (0, 3):
+            w4.w4a8_set_tuning(force_splits=splits, qmma_max_m=1)
+            for sms in (152, 148, 20):
+                for (M, K) in [(4, 3584), (16, 3584), (64, 18944), (9, 131072), (33, 896)]:
+                    N = 40000
+                    full = w4.w4a8_plan_info(M, K, N, num_sms=sms)
+                    assert full["kernel"] == 1
+                    for Np in (1, 7, 128, 129, 1000, 4608, 18944, 39999):
+                        p = w4.w4a8_plan_info(M, K, Np, num_sms=sms)
+                        if p["kernel"] != 1:
+                            continue
+                        check_mma_plan(p, M, K, Np, sms)
+                        assert p["ws_bytes"] <= full["ws_bytes"], (M, K, Np, sms)
     finally:
         w4.w4a8_set_tuning(reset=True)
 
