@@ -26,7 +26,7 @@ EXPORTS = [
     "w4a8_workspace_bytes", "w4a8_gemv", "w4a8_linear",
     "w8a16_workspace_bytes", "w8a16_gemv",
     "w4a8_last_error", "w4a8_device_error", "w4a8_set_tuning", "w4a8_plan_info",
-    "w4a8_linear_noalloc", "w4a8_linear_grouped",
+    "w4a8_linear_noalloc", "w4a8_linear_grouped", "w4a8_linear_prefetch", "w4a8_linear_grouped_prefetch",
     "w4g_quantize_weights", "w4a8g_workspace_bytes", "w4a8g_gemv", "w4a8g_linear",
     "w4a8g_linear_grouped", "w4a8g_plan_info",
     "index_softmax_lut", "index_softmax_c_int", "index_softmax_u8",
@@ -56,6 +56,10 @@ _SIGS = {
     "w4a8_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
     "w4a8_gemv": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, ctypes.c_size_t, _u, _p]),
     "w4a8_linear": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _p, _p, ctypes.c_size_t, _u, _p]),
+    "w4a8_linear_prefetch": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _p, ctypes.c_size_t, _u, _p, _p,
+                                            ctypes.c_size_t]),
+    "w4a8_linear_grouped_prefetch": (ctypes.c_int, [_p, _i64, _i64, ctypes.c_int, _p, _p, _p, _p, _p,
+                                                    ctypes.c_size_t, _u, _p, _p, ctypes.c_size_t]),
     "w4a8_linear_noalloc": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _i64, _p, _u, _p]),
     "w4a8_linear_grouped": (ctypes.c_int, [_p, _i64, _i64, ctypes.c_int, _p, _p, _p, _p, _p,
                                            ctypes.c_size_t, _u, _p]),
@@ -215,9 +219,21 @@ def w4a8_gemv(Xq, sa, Wq, sw, Y=None, acc_out=None, ws=None, flags: int = 0):
     return Y
 
 
+def _prefetch_arg(prefetch, prefetch_bytes):
+    if prefetch is None:
+        return None, 0
+    if not isinstance(prefetch, torch.Tensor) or not prefetch.is_cuda:
+        raise TypeError("prefetch must be a CUDA tensor")
+    nb = prefetch.numel() * prefetch.element_size()
+    return prefetch.data_ptr(), min(nb, int(prefetch_bytes) if prefetch_bytes else nb)
+
+
 def w4a8_linear(X, Wq, sw, Y=None, Xq_out=None, sa_out=None, acc_out=None, ws=None,
-                flags: int = 0):
-    """Fused activation quantization + W4A8 product; returns Y."""
+                flags: int = 0, prefetch=None, prefetch_bytes: int = 0):
+    """Fused activation quantization + W4A8 product; returns Y.  `prefetch`
+    (a CUDA tensor, e.g. the next launch's packed weights) and
+    `prefetch_bytes` (0 = all of it): an L2 prefetch hint for the next
+    launch (w4a8_linear_prefetch; the optional outputs are then not taken)."""
     _want(X, torch.float16, "X")
     M, K = X.shape
     N = Wq.shape[0]
@@ -233,16 +249,24 @@ def w4a8_linear(X, Wq, sw, Y=None, Xq_out=None, sa_out=None, acc_out=None, ws=No
         _want(acc_out, torch.int32, "acc_out", (M, N))
     nbytes = w4a8_workspace_bytes(M, K, N)
     ws = _workspace(nbytes, X.device, ws)
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    if prefetch is not None:
+        if Xq_out is not None or sa_out is not None or acc_out is not None:
+            raise ValueError("the prefetching call takes no optional outputs")
+        pp, pb = _prefetch_arg(prefetch, prefetch_bytes)
+        _check(lib().w4a8_linear_prefetch(_ptr(X), M, K, _ptr(Wq), _ptr(sw), N, _ptr(Y), _ptr(ws), wsb,
+                                          flags, _stream(X), pp, pb))
+        return Y
     _check(lib().w4a8_linear(_ptr(X), M, K, _ptr(Wq), _ptr(sw), N, _ptr(Y), _ptr(Xq_out),
-                             _ptr(sa_out), _ptr(acc_out), _ptr(ws),
-                             0 if ws is None else ws.numel() * ws.element_size(), flags,
-                             _stream(X)))
+                             _ptr(sa_out), _ptr(acc_out), _ptr(ws), wsb, flags, _stream(X)))
     return Y
 
 
-def w4a8_linear_grouped(X, Wqs, sws, Ys=None, ws=None, flags: int = 0):
+def w4a8_linear_grouped(X, Wqs, sws, Ys=None, ws=None, flags: int = 0, prefetch=None,
+                        prefetch_bytes: int = 0):
     """One launch for several weight matrices sharing X (e.g. q/k/v); returns
-    the list of outputs, each bit-identical to w4a8_linear on its own."""
+    the list of outputs, each bit-identical to w4a8_linear on its own.
+    `prefetch`, `prefetch_bytes`: as in w4a8_linear."""
     _want(X, torch.float16, "X")
     M, K = X.shape
     G = len(Wqs)
@@ -263,12 +287,15 @@ def w4a8_linear_grouped(X, Wqs, sws, Ys=None, ws=None, flags: int = 0):
     n_a = (ctypes.c_int64 * G)(*Ns)
     nbytes = w4a8_workspace_bytes(M, K, sum(Ns))
     ws = _workspace(nbytes, X.device, ws)
-    _check(lib().w4a8_linear_grouped(_ptr(X), M, K, G, ctypes.cast(wq_a, ctypes.c_void_p),
-                                     ctypes.cast(sw_a, ctypes.c_void_p),
-                                     ctypes.cast(n_a, ctypes.c_void_p),
-                                     ctypes.cast(y_a, ctypes.c_void_p), _ptr(ws),
-                                     0 if ws is None else ws.numel() * ws.element_size(), flags,
-                                     _stream(X)))
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    args = (_ptr(X), M, K, G, ctypes.cast(wq_a, ctypes.c_void_p), ctypes.cast(sw_a, ctypes.c_void_p),
+            ctypes.cast(n_a, ctypes.c_void_p), ctypes.cast(y_a, ctypes.c_void_p), _ptr(ws), wsb, flags,
+            _stream(X))
+    if prefetch is not None:
+        pp, pb = _prefetch_arg(prefetch, prefetch_bytes)
+        _check(lib().w4a8_linear_grouped_prefetch(*args, pp, pb))
+    else:
+        _check(lib().w4a8_linear_grouped(*args))
     return Ys
 
 

@@ -391,6 +391,29 @@ int w4a8_gemv(const int8_t* Xq, const float* sa, int64_t M, int64_t K, const uin
     return ok();
 }
 
+}  // extern "C"
+
+namespace {
+// The L2 prefetch hint of the *_prefetch entry points, passed to the dp4a
+// GEMV launch of the call that sets it (this thread only).
+thread_local const void* t_prefetch = nullptr;
+thread_local int64_t t_prefetch_bytes = 0;
+
+// Sets the hint for one call and clears it afterwards.
+struct PrefetchScope {
+    PrefetchScope(const void* p, size_t bytes) {
+        t_prefetch = p;
+        t_prefetch_bytes = p ? (int64_t)bytes : 0;
+    }
+    ~PrefetchScope() {
+        t_prefetch = nullptr;
+        t_prefetch_bytes = 0;
+    }
+};
+}  // namespace
+
+extern "C" {
+
 int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const float* sw,
                 int64_t N, float* Y, int8_t* Xq_out, float* sa_out, int32_t* acc_out, void* ws,
                 size_t ws_bytes, unsigned flags, void* stream) {
@@ -436,7 +459,7 @@ int w4a8_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, cons
                                           Y + m0 * N, acc_out ? acc_out + m0 * N : nullptr,
                                           Xq_out ? Xq_out + m0 * K : nullptr,
                                           sa_out ? sa_out + m0 : nullptr, ws, flags,
-                                          static_cast<cudaStream_t>(stream));
+                                          static_cast<cudaStream_t>(stream), t_prefetch, t_prefetch_bytes);
         if (e != cudaSuccess) return cuda_fail(e, "w4a8_linear launch");
     }
     return ok();
@@ -512,7 +535,8 @@ int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const ui
         for (int g = 0; g < G; ++g) Yg[g] = Y[g] + m0 * N[g];
         cudaError_t e = w4a8::launch_w4a8_grouped(mg == kRowGroupW4 || M < kRowGroupW4 ? pf : pt,
                                                   X + m0 * K, (int)mg, K, G, Wq, sw, N, Yg, ws,
-                                                  flags, static_cast<cudaStream_t>(stream));
+                                                  flags, static_cast<cudaStream_t>(stream), t_prefetch,
+                                                  t_prefetch_bytes);
         if (e != cudaSuccess) return cuda_fail(e, "w4a8_linear_grouped launch");
     }
     return ok();
@@ -961,3 +985,30 @@ extern "C" int w4a8_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, cons
                                       static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ok() : cuda_fail(e, "w4a8_linear_noalloc launch");
 }
+
+// ---------------------------------------------------------------------------
+// The linear with an L2 prefetch hint for the next launch's weights.
+// ---------------------------------------------------------------------------
+
+extern "C" {
+
+int w4a8_linear_prefetch(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const float* sw,
+                         int64_t N, float* Y, void* ws, size_t ws_bytes, unsigned flags, void* stream,
+                         const void* next, size_t next_bytes) {
+    if (next && !aligned(next, 16))
+        return fail(W4A8_ERR_ALIGN, "w4a8_linear_prefetch: next needs 16-byte alignment");
+    PrefetchScope scope(next, next_bytes);
+    return w4a8_linear(X, M, K, Wq, sw, N, Y, nullptr, nullptr, nullptr, ws, ws_bytes, flags, stream);
+}
+
+int w4a8_linear_grouped_prefetch(const uint16_t* X, int64_t M, int64_t K, int G, const uint8_t* const* Wq,
+                                 const float* const* sw, const int64_t* N, float* const* Y, void* ws,
+                                 size_t ws_bytes, unsigned flags, void* stream, const void* next,
+                                 size_t next_bytes) {
+    if (next && !aligned(next, 16))
+        return fail(W4A8_ERR_ALIGN, "w4a8_linear_grouped_prefetch: next needs 16-byte alignment");
+    PrefetchScope scope(next, next_bytes);
+    return w4a8_linear_grouped(X, M, K, G, Wq, sw, N, Y, ws, ws_bytes, flags, stream);
+}
+
+}  // extern "C"

@@ -15,8 +15,10 @@ static cudaError_t launch_w4a8_m1_fused(const GemvArgs& a, unsigned flags, cudaS
 cudaError_t launch_w4a8_grouped(const GemvPlan& pl, const uint16_t* X, int M, int64_t K, int G,
                                 const uint8_t* const* Wq, const float* const* sw,
                                 const int64_t* Ns, float* const* Y, void* ws, unsigned flags,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, const void* pf, int64_t pf_bytes) {
     GemvArgs a = {};
+    a.pf = static_cast<const uint8_t*>(pf);
+    a.pf_bytes = pf ? pf_bytes & ~(int64_t)15 : 0;
     const void* s[kMaxSegments] = {};
     for (int k = 0; k < G; ++k) s[k] = sw[k];
     set_segments(a, G, Wq, s, Ns, Y);
@@ -39,8 +41,10 @@ cudaError_t launch_w4a8_grouped(const GemvPlan& pl, const uint16_t* X, int M, in
 cudaError_t launch_w4a8(const GemvPlan& pl, bool fused, const uint16_t* X, const int8_t* Xq,
                         const float* sa, int M, int64_t K, const uint8_t* Wq, const float* sw,
                         int64_t N, float* Y, int32_t* acc_out, int8_t* Xq_out, float* sa_out,
-                        void* ws, unsigned flags, cudaStream_t stream) {
+                        void* ws, unsigned flags, cudaStream_t stream, const void* pf, int64_t pf_bytes) {
     GemvArgs a = {};
+    a.pf = static_cast<const uint8_t*>(pf);
+    a.pf_bytes = pf ? pf_bytes & ~(int64_t)15 : 0;
     const void* s0 = sw;
     set_segments(a, 1, &Wq, &s0, &N, &Y);
     a.Xq = Xq;

@@ -65,6 +65,8 @@ struct GemvArgs {
                             // gate i, row 2i + 1 up i): H[m][i] = binary16(silu(Y[m][2i]) * Y[m][2i+1]);
                             // every CTA then owns whole pairs
     void* part;             // split partials [P][M][N] (int32 or fp32)
+    const uint8_t* pf;      // optional: bytes [pf, pf + pf_bytes) of the next launch's
+    int64_t pf_bytes;       // weights to bring into L2 (a multiple of 16; 0 = none)
     unsigned* tickets;      // [Gs] arrival counters at the workspace start,
                             // zero between calls
     int M;
@@ -230,6 +232,14 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
         fence_mbar_init();
         // Fill the ring (weights may be read before the dependency wait).
         for (int st = 0; st < min(NS, nstages); ++st) issue(st, st);
+        // The next launch's first weight bytes into L2, this CTA's share: at
+        // one row the launch is latency-bound and leaves HBM idle meanwhile.
+        if (a.pf_bytes > 0) {
+            const int64_t share = ((a.pf_bytes + gridDim.x - 1) / gridDim.x + 15) & ~(int64_t)15;
+            const int64_t o1 = min((int64_t)(blockIdx.x + 1) * share, a.pf_bytes);
+            for (int64_t o = (int64_t)blockIdx.x * share; o < o1; o += 65536)
+                prefetch_bulk_l2(a.pf + o, (uint32_t)min((int64_t)65536, o1 - o));
+        }
     }
     griddep_launch_dependents();
     // Warm the L2 with the activation lines: a prefetch binds no value, so

@@ -23,11 +23,14 @@ cudaError_t launch_act_quantize(const uint16_t* X, int64_t M, int64_t K, int8_t*
 cudaError_t launch_w4a8(const GemvPlan& pl, bool fused, const uint16_t* X, const int8_t* Xq,
                         const float* sa, int M, int64_t K, const uint8_t* Wq, const float* sw,
                         int64_t N, float* Y, int32_t* acc_out, int8_t* Xq_out, float* sa_out,
-                        void* ws, unsigned flags, cudaStream_t stream);
+                        void* ws, unsigned flags, cudaStream_t stream, const void* pf = nullptr,
+                        int64_t pf_bytes = 0);
+// pf, pf_bytes: the next launch's first weight bytes to bring into L2 (see
+// w4a8_linear_prefetch); pf must be 16-byte aligned.
 cudaError_t launch_w4a8_grouped(const GemvPlan& pl, const uint16_t* X, int M, int64_t K, int G,
                                 const uint8_t* const* Wq, const float* const* sw,
                                 const int64_t* Ns, float* const* Y, void* ws, unsigned flags,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const void* pf = nullptr, int64_t pf_bytes = 0);
 cudaError_t launch_w8a16(const GemvPlan& pl, const uint16_t* X, int M, int64_t K,
                          const int8_t* Wq8, const uint16_t* sw16, int64_t N, float* Y, void* ws,
                          unsigned flags, cudaStream_t stream);

@@ -282,6 +282,23 @@ int w4a8_gate_up_silu(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq
 int w4a8_silu_mul(const float* g, const float* u, int64_t M, int64_t N, uint16_t* H, unsigned flags,
                   void* stream);
 
+/* Decode-step prefetch (no counterpart on the pages): w4a8_linear and
+ * w4a8_linear_grouped with a hint, `next`, `next_bytes`: the first bytes of
+ * the weights the following launch will read.  When the call runs the
+ * one-row dp4a GEMV, its CTAs bring that range into L2 at the start (a
+ * cp.async.bulk.prefetch.L2 of each CTA's share), while the launch, which at
+ * one row is bound by latency, leaves HBM idle; the following launch then
+ * finds those bytes in L2.  Other kernels ignore the hint.  A hint changes
+ * no result.  Requires next 16-byte aligned (NULL = none); next_bytes is
+ * rounded down to a multiple of 16. */
+int w4a8_linear_prefetch(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const float* sw,
+                         int64_t N, float* Y, void* ws, size_t ws_bytes, unsigned flags, void* stream,
+                         const void* next, size_t next_bytes);
+int w4a8_linear_grouped_prefetch(const uint16_t* X, int64_t M, int64_t K, int G, const uint8_t* const* Wq,
+                                 const float* const* sw, const int64_t* N, float* const* Y, void* ws,
+                                 size_t ws_bytes, unsigned flags, void* stream, const void* next,
+                                 size_t next_bytes);
+
 /* ---------------------------------------------------------------------- */
 /* W4A8 with group-wise weight scales                                      */
 /* ---------------------------------------------------------------------- */

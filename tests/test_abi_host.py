@@ -80,6 +80,16 @@ def test_misaligned_pointers_rejected(L):
     assert L.w8a16_gemv(P16, 1, 32, P16 + 4, P16, 4, P16, None, 0, 0, None) == E
 
 
+def test_prefetch_argument_checks(L):
+    """The prefetch hint must start on 16 bytes; checked before any launch."""
+    E_A = w4._binding.ERR_ALIGN
+    assert L.w4a8_linear_prefetch(P16, 1, 32, P16, P16, 4, P16, None, 0, 0, None, P16 + 8, 1024) == E_A
+    arr = (ctypes.c_void_p * 1)(P16)
+    ns = (ctypes.c_int64 * 1)(4)
+    assert L.w4a8_linear_grouped_prefetch(P16, 1, 32, 1, arr, arr, ns, arr, None, 0, 0, None,
+                                          P16 + 4, 64) == E_A
+
+
 def test_grouped_argument_checks(L):
     import ctypes
     arr = (ctypes.c_void_p * 2)(P16, P16)

@@ -482,3 +482,24 @@ def test_w4a8_linear_grouped_rejects_bad_groups(w4):
     with pytest.raises(w4.W4A8Error) as e:
         w4.w4a8_linear_grouped(X, [Wq, Wq_mis], [sw, sw])
     assert e.value.status == 2
+
+
+def test_prefetch_hint_changes_no_result(w4):
+    """The L2 prefetch entry points (a hint for the next launch's weights)
+    give the same bits as the plain calls, single and grouped, at one row
+    (the dp4a GEMV, which takes the hint) and at 16 rows (which ignores it);
+    the hinted range may be shorter or longer than the next matrix."""
+    K = 3584
+    Wq1, sw1 = w4.w4_quantize_weights(torch.from_numpy(synth.normal(940, (3000, K), 0.02)).cuda())
+    Wq2, sw2 = w4.w4_quantize_weights(torch.from_numpy(synth.normal(941, (700, K), 0.02)).cuda())
+    for M in (1, 16):
+        X = torch.from_numpy(synth.activation(942 + M, M, K, outlier_frac=0.001)).cuda()
+        ref = w4.w4a8_linear(X, Wq1, sw1).clone()
+        refg = [y.clone() for y in w4.w4a8_linear_grouped(X, [Wq1, Wq2], [sw1, sw2])]
+        for nb in (0, 4096, 1 << 20):
+            Y = w4.w4a8_linear(X, Wq1, sw1, prefetch=Wq2, prefetch_bytes=nb, flags=w4.LAUNCH_PDL)
+            Yg = w4.w4a8_linear_grouped(X, [Wq1, Wq2], [sw1, sw2], prefetch=Wq1, prefetch_bytes=nb)
+            torch.cuda.synchronize()
+            assert torch.equal(Y, ref)
+            assert all(torch.equal(a, b) for a, b in zip(Yg, refg))
+    assert w4.w4a8_device_error() == 0
