@@ -12,13 +12,19 @@ static cudaError_t launch_w4a8_m1_fused(const GemvArgs& a, unsigned flags, cudaS
     return launch_one<true, 1, 8, true>(a, flags, stream);
 }
 
+// The prefetch hint: whole 16-byte units, shared out over the grid's CTAs.
+static void set_prefetch(GemvArgs& a, const GemvPlan& pl, const void* pf, int64_t pf_bytes) {
+    a.pf = static_cast<const uint8_t*>(pf);
+    a.pf_bytes = pf ? pf_bytes & ~(int64_t)15 : 0;
+    a.pf_share = ((a.pf_bytes + pl.grid - 1) / pl.grid + 15) & ~(int64_t)15;
+}
+
 cudaError_t launch_w4a8_grouped(const GemvPlan& pl, const uint16_t* X, int M, int64_t K, int G,
                                 const uint8_t* const* Wq, const float* const* sw,
                                 const int64_t* Ns, float* const* Y, void* ws, unsigned flags,
                                 cudaStream_t stream, const void* pf, int64_t pf_bytes) {
     GemvArgs a = {};
-    a.pf = static_cast<const uint8_t*>(pf);
-    a.pf_bytes = pf ? pf_bytes & ~(int64_t)15 : 0;
+    set_prefetch(a, pl, pf, pf_bytes);
     const void* s[kMaxSegments] = {};
     for (int k = 0; k < G; ++k) s[k] = sw[k];
     set_segments(a, G, Wq, s, Ns, Y);
@@ -43,8 +49,7 @@ cudaError_t launch_w4a8(const GemvPlan& pl, bool fused, const uint16_t* X, const
                         int64_t N, float* Y, int32_t* acc_out, int8_t* Xq_out, float* sa_out,
                         void* ws, unsigned flags, cudaStream_t stream, const void* pf, int64_t pf_bytes) {
     GemvArgs a = {};
-    a.pf = static_cast<const uint8_t*>(pf);
-    a.pf_bytes = pf ? pf_bytes & ~(int64_t)15 : 0;
+    set_prefetch(a, pl, pf, pf_bytes);
     const void* s0 = sw;
     set_segments(a, 1, &Wq, &s0, &N, &Y);
     a.Xq = Xq;

@@ -66,7 +66,8 @@ struct GemvArgs {
                             // every CTA then owns whole pairs
     void* part;             // split partials [P][M][N] (int32 or fp32)
     const uint8_t* pf;      // optional: bytes [pf, pf + pf_bytes) of the next launch's
-    int64_t pf_bytes;       // weights to bring into L2 (a multiple of 16; 0 = none)
+    int64_t pf_bytes;       // weights to bring into L2 (a multiple of 16; 0 = none),
+    int64_t pf_share;       // pf_share bytes per CTA (a multiple of 16)
     unsigned* tickets;      // [Gs] arrival counters at the workspace start,
                             // zero between calls
     int M;
@@ -235,9 +236,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_kernel(const _
         // The next launch's first weight bytes into L2, this CTA's share: at
         // one row the launch is latency-bound and leaves HBM idle meanwhile.
         if (a.pf_bytes > 0) {
-            const int64_t share = ((a.pf_bytes + gridDim.x - 1) / gridDim.x + 15) & ~(int64_t)15;
-            const int64_t o1 = min((int64_t)(blockIdx.x + 1) * share, a.pf_bytes);
-            for (int64_t o = (int64_t)blockIdx.x * share; o < o1; o += 65536)
+            const int64_t o1 = min((int64_t)(blockIdx.x + 1) * a.pf_share, a.pf_bytes);
+            for (int64_t o = (int64_t)blockIdx.x * a.pf_share; o < o1; o += 65536)
                 prefetch_bulk_l2(a.pf + o, (uint32_t)min((int64_t)65536, o1 - o));
         }
     }
