@@ -503,3 +503,30 @@ def test_prefetch_hint_changes_no_result(w4):
             assert torch.equal(Y, ref)
             assert all(torch.equal(a, b) for a, b in zip(Yg, refg))
     assert w4.w4a8_device_error() == 0
+
+
+@pytest.mark.parametrize("M", [2, 9, 17, 32])
+def test_tensor_cores_many_tiles(w4, M):
+    """More 128-row tiles (313 for 40,000 rows) than two per SM, one K piece:
+    several waves of CTAs, ragged last tile; every output bit for bit, twice
+    in a row."""
+    orc = oracle.load()
+    K, N = 1024, 40000
+    W = synth.normal(960 + M, (N, K), 0.02)
+    X = synth.activation(961 + M, M, K, outlier_frac=0.001)
+    Wq_ref, sw_ref = orc.w4_quantize(W)
+    Y_ref = orc.w4a8_linear(X, Wq_ref, sw_ref)[0]
+    w4.w4a8_set_tuning(rowdot_max_m=1, qmma_max_m=1)
+    try:
+        p = w4.w4a8_plan_info(M, K, N)
+        assert p["kernel"] == 1 and p["splits"] == 1 and p["ctas_per_split"] > 2 * 152 * 0.9
+        Wq, sw = w4.w4_quantize_weights(torch.from_numpy(W).cuda())
+        for _ in range(2):
+            gY = guards.out((M, N), torch.float32)
+            Y = w4.w4a8_linear(torch.from_numpy(X).cuda(), Wq, sw, Y=gY.t, flags=w4.LAUNCH_PDL)
+            torch.cuda.synchronize()
+            guards.check_all(gY)
+            assert np.array_equal(Y.cpu().numpy().view(np.uint32), Y_ref.view(np.uint32))
+    finally:
+        w4.w4a8_set_tuning(reset=True)
+    assert w4.w4a8_device_error() == 0
