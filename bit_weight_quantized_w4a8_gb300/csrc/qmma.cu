@@ -80,7 +80,7 @@ struct QmmaArgs {
     int32_t* acc_out;       // optional [M][N]
     int32_t* part;          // [tiles][M][128] int32 sums when P > 1 (zeroed by the activation pass)
     unsigned* tickets;      // [tiles] when P > 1, zero between calls
-    int M, N, nbox, bpp, P, NS, pre_pieces;
+    int M, N, nbox, bpp, P, NS, pre_pieces, tiles;
     unsigned long long stall_ns;  // > 0: test of the bounded waits (see qmma_kernel)
 };
 
@@ -94,6 +94,26 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            atomicOr(&g_qmma_error, kErrFullWait);
+            return false;
+        }
+    }
+}
+
+// Waits (bounded) until the stage's copy of CTA box j has been issued:
+// tag is the box last issued into the stage.  A warp may reach box j while
+// its stage still holds box j - NS (the other warps have not released it);
+// the mbarrier parity alone cannot tell that phase from box j's.
+__device__ __forceinline__ bool wait_issued(const volatile int* tag, int j, volatile int* abort_flag) {
+    if (*tag == j) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        #pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (*tag == j) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
             atomicOr(&g_qmma_error, kErrFullWait);
             return false;
@@ -261,7 +281,14 @@ __device__ __forceinline__ void mma_e4m3(float* d, uint32_t a0, uint32_t a1, uin
 // independent MMA chains.  There is no copy warp: thread 0 fills the
 // ring at entry, and the last warp done with a stage refills it with the
 // box NS further on.
-template <int NT, int R>
+//
+// kPersist (one K piece, more tiles than SMs): CTA b takes the tiles
+// b, b + grid, ... and streams their boxes as one sequence j = ti * nb + i
+// (local tile ti, box i) through the ring, so the copies of the next tile
+// are in flight while a tile ends; after a tile's last box the warps' sums
+// meet in shared memory, the CTA writes the tile's outputs and clears the
+// sums.  Without it a CTA takes one tile and K piece (grid tiles x P).
+template <int NT, int R, bool kPersist>
 __global__ void __launch_bounds__(kQThreads, 1) qmma_kernel(const __grid_constant__ QmmaArgs a) {
     constexpr int C = 8 * NT;        // MMA columns
     constexpr int MP = 4 * NT;       // batch rows covered
@@ -284,11 +311,26 @@ __global__ void __launch_bounds__(kQThreads, 1) qmma_kernel(const __grid_constan
     uint64_t* never = reinterpret_cast<uint64_t*>(last_box + NS + 2);  // 8-byte aligned (16 NS + 8 past full)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = blockIdx.x / a.P, p = blockIdx.x % a.P;
+    const int tile = kPersist ? (int)blockIdx.x : (int)blockIdx.x / a.P;  // (first) tile
+    const int p = kPersist ? 0 : (int)blockIdx.x % a.P;
     const int box0 = p * a.bpp;
     const int nb = min(a.bpp, a.nbox - box0);
+    const int ntl = kPersist ? (a.tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 1;
+    const int total = ntl * nb;  // boxes this CTA streams
     const uint64_t pol_w = l2_evict_first_policy();
     const uint64_t pol_a = l2_evict_last_policy();
+    // CTA box j = ti * nb + i: box box0 + i of local tile ti, into stage j % NS
+    auto issue_w = [&](int j) {
+        const int ti = kPersist ? j / nb : 0;
+        const int i = j - ti * nb;
+        tma_load_2d_hint(smem_u32(smem + (j % NS) * kStage), &a.tmW, (box0 + i) * (kBoxCodes / 2),
+                         (tile + ti * (int)gridDim.x) * kTile, smem_u32(full + j % NS), pol_w);
+    };
+    auto issue_a = [&](int j) {
+        const int i = kPersist ? j % nb : j;
+        bulk_g2s(smem_u32(smem + (j % NS) * kStage + kBoxBytes), a.codes + (int64_t)(box0 + i) * kActBytes,
+                 kActBytes, smem_u32(full + j % NS), pol_a);
+    };
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -303,20 +345,17 @@ __global__ void __launch_bounds__(kQThreads, 1) qmma_kernel(const __grid_constan
     for (int e = tid; e < kTile * MP + MP; e += kQThreads) red[e] = 0;  // row sums, activation sums
     __syncthreads();
     griddep_launch_dependents();
-    const int pre = min(NS, nb);
+    const int pre = min(NS, total);
     if (tid == 0) {  // the weights do not depend on earlier launches
-        for (int i = 0; i < pre; ++i) {
-            mbar_arrive_expect_tx(smem_u32(full + i), kStage);
-            tma_load_2d_hint(smem_u32(smem + i * kStage), &a.tmW, (box0 + i) * (kBoxCodes / 2), tile * kTile,
-                             smem_u32(full + i), pol_w);
-            last_box[i] = i;
+        for (int j = 0; j < pre; ++j) {
+            mbar_arrive_expect_tx(smem_u32(full + j), kStage);
+            issue_w(j);
+            last_box[j] = j;
         }
     }
     griddep_wait();  // activation slices, sums, scales, outputs and workspace from here on
     if (tid == 0)
-        for (int i = 0; i < pre; ++i)
-            bulk_g2s(smem_u32(smem + i * kStage + kBoxBytes), a.codes + (int64_t)(box0 + i) * kActBytes, kActBytes,
-                     smem_u32(full + i), pol_a);
+        for (int j = 0; j < pre; ++j) issue_a(j);
     // the batch rows' exact code sums, from the activation pass's pieces
     // (one load per thread, added in shared memory; read after the loop)
     for (int e = tid; e < a.M * a.pre_pieces; e += kQThreads)
@@ -325,15 +364,6 @@ __global__ void __launch_bounds__(kQThreads, 1) qmma_kernel(const __grid_constan
     const int wr = warp % WR, wk = warp / WR;
     const int g = lane >> 2, t = lane & 3;
     const int pg = (g >> 1) + 4 * (g & 1);
-    float acc[KS][R][NT][4];
-    #pragma unroll
-    for (int k = 0; k < KS; ++k)
-        #pragma unroll
-        for (int rt = 0; rt < R; ++rt)
-            #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[k][rt][nt][i] = 0.f;
     // ldmatrix row of this lane: lanes 8 q .. 8 q + 7 address matrix q = (rows
     // g or g + 8) x (chunk 2 sp or 2 sp + 1) of tile rt; row pi(lane % 8)
     const int lg = lane & 7;
@@ -348,9 +378,22 @@ __global__ void __launch_bounds__(kQThreads, 1) qmma_kernel(const __grid_constan
         __all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(never), 0, abort_flag, a.stall_ns));
     }
     #pragma unroll 1
+    for (int ti = 0; ti < ntl; ++ti) {
+    float acc[KS][R][NT][4];
+    #pragma unroll
+    for (int k = 0; k < KS; ++k)
+        #pragma unroll
+        for (int rt = 0; rt < R; ++rt)
+            #pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) acc[k][rt][nt][i] = 0.f;
+    #pragma unroll 1
     for (int i = wk; i < nb; i += R) {
-        const int s = i % NS;
-        if (!__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(full + s), (uint32_t)(i / NS) & 1u, abort_flag, kWaitLimitNs)))
+        const int j = ti * nb + i;  // CTA box
+        const int s = j % NS;
+        if (!__all_sync(0xFFFFFFFFu, wait_issued(last_box + s, j, abort_flag))) break;
+        if (!__all_sync(0xFFFFFFFFu, wait_bounded(smem_u32(full + s), (uint32_t)(j / NS) & 1u, abort_flag, kWaitLimitNs)))
             break;
         const uint32_t wbox = smem_u32(smem + s * kStage) + lrow;
         const uint8_t* abox = smem + s * kStage + kBoxBytes + (g * 4 + t) * 8;
@@ -385,13 +428,12 @@ __global__ void __launch_bounds__(kQThreads, 1) qmma_kernel(const __grid_constan
             if (atomicAdd(released + s, 1) == WR - 1) {
                 released[s] = 0;
                 __threadfence_block();
-                if (i + NS < nb && !*abort_flag) {
+                if (j + NS < total && !*abort_flag) {
                     mbar_arrive_expect_tx(smem_u32(full + s), kStage);
-                    tma_load_2d_hint(smem_u32(smem + s * kStage), &a.tmW, (box0 + i + NS) * (kBoxCodes / 2),
-                                     tile * kTile, smem_u32(full + s), pol_w);
-                    bulk_g2s(smem_u32(smem + s * kStage + kBoxBytes),
-                             a.codes + (int64_t)(box0 + i + NS) * kActBytes, kActBytes, smem_u32(full + s), pol_a);
-                    last_box[s] = i + NS;
+                    issue_w(j + NS);
+                    issue_a(j + NS);
+                    __threadfence_block();
+                    last_box[s] = j + NS;
                 }
             }
         }
@@ -414,6 +456,23 @@ __global__ void __launch_bounds__(kQThreads, 1) qmma_kernel(const __grid_constan
         }
     }
     __syncthreads();
+    if constexpr (kPersist) {
+        // the abort flag is read by every thread between the two barriers,
+        // where no thread can set it: the break is CTA-uniform
+        if (*abort_flag) break;
+        const int n0 = (tile + ti * (int)gridDim.x) * kTile;
+        for (int e = tid; e < a.M * kTile; e += kQThreads) {
+            const int m = e / kTile, r = e % kTile, n = n0 + r;
+            const int32_t v = red[r * MP + m] - 8 * sa_sum[m];
+            red[r * MP + m] = 0;  // each sum is read and cleared by one thread; rows m >= M stay 0
+            if (n >= a.N) continue;
+            const int64_t o = (int64_t)m * a.N + n;
+            a.Y[o] = __fmul_rn(__fmul_rn(__int2float_rn(v), a.sw[n]), a.sa[m]);
+            if (a.acc_out != nullptr) a.acc_out[o] = v;
+        }
+        __syncthreads();
+    }
+    }  // tiles
     if (*abort_flag && tid == 0) {
         // copies may still be landing after an abandoned wait: wait for the
         // last one of each stage (bounded) so none writes shared memory after exit
@@ -421,6 +480,7 @@ __global__ void __launch_bounds__(kQThreads, 1) qmma_kernel(const __grid_constan
             if (last_box[s] >= 0 && !mbar_wait(smem_u32(full + s), (uint32_t)(last_box[s] / NS) & 1u))
                 atomicOr(&g_qmma_error, kErrDrainWait);
     }
+    if constexpr (kPersist) return;
     const bool ok = *abort_flag == 0;
     const int n0 = tile * kTile;
     if (a.P == 1) {
@@ -490,30 +550,35 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
 constexpr int default_r(int NT) { return NT <= 4 ? 4 : 2; }
 
 template <int NT, int R>
-const void* kernel_ntr() {
-    return reinterpret_cast<const void*>(qmma_kernel<NT, R>);
+const void* kernel_ntr(bool persist) {
+    // the persistent form exists for the default tiles per warp only
+    if (persist) {
+        if constexpr (R == default_r(NT)) return reinterpret_cast<const void*>(qmma_kernel<NT, R, true>);
+        return nullptr;
+    }
+    return reinterpret_cast<const void*>(qmma_kernel<NT, R, false>);
 }
 
 template <int NT>
-const void* kernel_nt(int R) {
-    if (R == 1) return kernel_ntr<NT, 1>();
-    if (R == 2) return kernel_ntr<NT, 2>();
+const void* kernel_nt(int R, bool persist) {
+    if (R == 1) return kernel_ntr<NT, 1>(persist);
+    if (R == 2) return kernel_ntr<NT, 2>(persist);
     if constexpr (NT <= 4) {  // 4 tiles a warp would spill past 4 n-tiles
-        if (R == 4) return kernel_ntr<NT, 4>();
+        if (R == 4) return kernel_ntr<NT, 4>(persist);
     }
     return nullptr;
 }
 
-const void* kernel_for(int NT, int R) {
+const void* kernel_for(int NT, int R, bool persist) {
     switch (NT) {
-        case 1: return kernel_nt<1>(R);
-        case 2: return kernel_nt<2>(R);
-        case 3: return kernel_nt<3>(R);
-        case 4: return kernel_nt<4>(R);
-        case 5: return kernel_nt<5>(R);
-        case 6: return kernel_nt<6>(R);
-        case 7: return kernel_nt<7>(R);
-        case 8: return kernel_nt<8>(R);
+        case 1: return kernel_nt<1>(R, persist);
+        case 2: return kernel_nt<2>(R, persist);
+        case 3: return kernel_nt<3>(R, persist);
+        case 4: return kernel_nt<4>(R, persist);
+        case 5: return kernel_nt<5>(R, persist);
+        case 6: return kernel_nt<6>(R, persist);
+        case 7: return kernel_nt<7>(R, persist);
+        case 8: return kernel_nt<8>(R, persist);
         default: return nullptr;
     }
 }
@@ -525,12 +590,13 @@ cudaError_t set_attributes() {
     if (e != cudaSuccess) return e;
     if (dev < 64 && done[dev]) return cudaSuccess;
     for (int nt = 1; nt <= kQmmaMaxM / 4; ++nt)
-        for (int r = 1; r <= 4; r *= 2) {
-            const void* fn = kernel_for(nt, r);
-            if (fn == nullptr) continue;
-            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-            if (e != cudaSuccess) return e;
-        }
+        for (int r = 1; r <= 4; r *= 2)
+            for (int persist = 0; persist < 2; ++persist) {
+                const void* fn = kernel_for(nt, r, persist != 0);
+                if (fn == nullptr) continue;
+                e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+                if (e != cudaSuccess) return e;
+            }
     if (dev < 64) done[dev] = true;
     return cudaSuccess;
 }
@@ -547,7 +613,9 @@ size_t smem_bytes(int NT, int NS) {
 // idle, and so that each MMA warp sums at most ceil(bpp / R) <= 256 boxes
 // (65536 codes), which keeps its fp32 sums exact.  The ring takes up to
 // kMaxNS stages of the shared memory.  R = 0 takes the default tiles per
-// warp.
+// warp.  With one K piece, more tiles than SMs and the default R, one
+// persistent CTA per SM walks the tiles (no waves of CTAs, each paying the
+// ring's fill).
 bool make_qmma_plan(int M, int64_t K, int64_t N, int num_sms, QmmaPlan* out, int R) {
     if (M < 2 || M > kQmmaMaxM || K < 32 || K % 32 || K > 131072 || N < 1 || N > 0x7FFFFFFF ||
         num_sms < 1)
@@ -578,7 +646,8 @@ bool make_qmma_plan(int M, int64_t K, int64_t N, int num_sms, QmmaPlan* out, int
     pl.NS = NS;
     pl.stage_bytes = kBoxBytes + 2048 * pl.NT;
     pl.smem = (int)smem_bytes(pl.NT, NS);
-    pl.grid = pl.tiles * pl.P;
+    pl.persist = (pl.P == 1 && pl.tiles > num_sms && pl.R == default_r(pl.NT)) ? 1 : 0;
+    pl.grid = pl.persist ? num_sms : pl.tiles * pl.P;
     pl.sms = num_sms;
     pl.pre_pieces = (int)(((int64_t)pl.nbox * kBoxCodes + kPreCodes - 1) / kPreCodes);
     // workspace: tickets, scales (64 floats), activation sums [M][pre_pieces],
@@ -619,8 +688,6 @@ cudaError_t launch_w4a8_qmma(const QmmaPlan& pl, const uint16_t* X, const int8_t
                                    dim3(4 * pl.NT, pl.pre_pieces), dim3(kPreThreads), 0, stream, flags, args);
         if (e != cudaSuccess) return e;
     }
-    const void* fn = kernel_for(pl.NT, pl.R);
-    if (fn == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = set_attributes();
     if (e != cudaSuccess) return e;
     for (int g = 0; g < G; ++g) {
@@ -644,7 +711,10 @@ cudaError_t launch_w4a8_qmma(const QmmaPlan& pl, const uint16_t* X, const int8_t
         a.P = pg.P;
         a.NS = pg.NS;
         a.pre_pieces = pg.pre_pieces;
+        a.tiles = pg.tiles;
         a.stall_ns = stall_ns;
+        const void* fn = kernel_for(pg.NT, pg.R, pg.persist != 0);
+        if (fn == nullptr) return cudaErrorInvalidValue;
         void* args[] = {&a};
         e = launch_pdl(fn, dim3(pg.grid), dim3(kQThreads), pg.smem, stream, flags, args);
         if (e != cudaSuccess) return e;

@@ -18,6 +18,7 @@ struct QmmaPlan {
     int NS;            // ring stages (weight box + activation slice)
     int stage_bytes;   // 16384 + activation slice
     int pre_pieces;    // CTAs per batch row of the activation pass
+    int persist;       // 1: one CTA per SM walks the tiles b, b + grid, ... (one K piece)
     int grid, smem, sms;
     size_t off_sa, off_sum, off_codes, off_part;  // workspace layout
     size_t ws_bytes;

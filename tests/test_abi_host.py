@@ -184,7 +184,11 @@ def check_qmma_plan(p, M, K, N, sms):
     NT = -(-M // 4)
     P, R = p["splits"], p["threads_per_row"]
     assert p["cols_per_thread"] == 4 * NT and R in (1, 2, 4) and (R < 4 or NT <= 4)
-    assert p["ctas_per_split"] == tiles and p["grid"] == tiles * P
+    assert p["ctas_per_split"] == tiles
+    # one K piece, more tiles than SMs, the default tiles per warp: one
+    # persistent CTA per SM walks the tiles
+    persist = P == 1 and tiles > sms and R == (4 if NT <= 4 else 2)
+    assert p["grid"] == (sms if persist else tiles * P)
     bpp = -(-nbox // P)
     assert (P - 1) * bpp < nbox                                  # no empty piece
     assert -(-bpp // R) * 256 <= 65536                           # exact fp32 sums per warp

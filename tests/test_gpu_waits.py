@@ -33,7 +33,8 @@ def w4():
 
 
 @pytest.mark.parametrize("M,K,N", [(6, 3584, 300),      # three tiles, K split (tickets)
-                                   (8, 1024, 2000)])    # one piece per tile
+                                   (8, 1024, 2000),     # one piece per tile
+                                   (4, 1024, 40000)])   # persistent CTAs, several tiles each
 def test_stalled_wait_reports_and_next_call_is_exact(w4, M, K, N):
     orc = oracle.load()
     W = synth.normal(1200 + M, (N, K), 0.02)
