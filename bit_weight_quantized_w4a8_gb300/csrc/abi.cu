@@ -78,11 +78,16 @@ constexpr int kDefaultMmaMinMGroup = 3;
 // Group-wise scales: the one-thread-per-row kernel serves 1..8 rows by
 // default (the tensor cores' per-group readouts make them slower there).
 constexpr int kDefaultRowdotMaxMGroup = 8;
-// The warp-level e4m3 MMA kernel serves row-wise W4A8 calls only when
-// w4a8_tuning_t.qmma_max_m asks for it (2 rows up to that); it then takes
-// precedence over the two kernels above.  Measured on GB300 (graphs of ten
-// calls, two weight copies) it beats the e4m3 tensor cores only on gate at
-// 4 rows (11.5 vs 12.6 us); lm_head at 8 rows takes 86.9 vs 59.7 us.
+// The warp-level e4m3 MMA kernel serves row-wise W4A8 calls of 2..4 rows
+// whose plan is persistent (one K piece) with at least kQmmaMinTilesPerSm
+// tiles per SM: lm_head-sized matrices, where two persistent CTAs per SM
+// beat the e4m3 tensor cores (GB300, graphs of ten calls, two weight
+// copies: lm_head 3584 -> 152064 at 2 / 4 rows 57.3 / 59.6 vs 60.1 / 60.4
+// us; at 8 rows 75.0 vs 61.6, at gate's 148 tiles slower).
+// w4a8_tuning_t.qmma_max_m = 1 switches it off, >= 2 gives it every call of
+// 2 rows up to that (any matrix), ahead of the two kernels above.
+constexpr int kDefaultQmmaMaxM = 4;
+constexpr int kQmmaMinTilesPerSm = 4;
 
 int sm_count(int* out) {
     static std::atomic<int> cache[64];
@@ -158,9 +163,11 @@ bool mma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::MmaPlan* pl, int sms = 
 // another kernel serves it.
 bool qmma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::QmmaPlan* pl, int sms = 0) {
     const int t = g_qmma_max_m.load();
-    if (t <= 1 || M < 2 || M > t) return false;
+    if (t == 1 || M < 2 || M > (t > 1 ? t : kDefaultQmmaMaxM)) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
-    return w4a8::make_qmma_plan((int)M, K, N, sms, pl, g_qmma_r.load());
+    if (!w4a8::make_qmma_plan((int)M, K, N, sms, pl, g_qmma_r.load())) return false;
+    // default routing: persistent plans on many tiles only
+    return t > 1 || (pl->persist && pl->tiles >= kQmmaMinTilesPerSm * sms);
 }
 
 // Row-per-thread plan for an M-row W4A8 call, or false when another kernel

@@ -69,6 +69,7 @@ constexpr int kPreThreads = 256;
 constexpr int kPreCodes = kPreThreads * 8;        // codes per activation-pass CTA
 constexpr int kMaxNS = 8;
 constexpr int kSmemMax = 227 * 1024;
+constexpr int kSmemMax2 = 233472 / 2 - 1024;      // per CTA with two CTAs on an SM
 
 struct QmmaArgs {
     CUtensorMap tmW;        // packed weights [N][K/2] uint8, box 128 bytes x 128 rows, 128B swizzle
@@ -288,8 +289,12 @@ __device__ __forceinline__ void mma_e4m3(float* d, uint32_t a0, uint32_t a1, uin
 // are in flight while a tile ends; after a tile's last box the warps' sums
 // meet in shared memory, the CTA writes the tile's outputs and clears the
 // sums.  Without it a CTA takes one tile and K piece (grid tiles x P).
+// Persistent CTAs of up to 8 batch rows (at most 2 n-tiles) run two to an
+// SM: their latency-bound warps then have twice the company (128 registers
+// a thread, which those instantiations fit without spilling).
 template <int NT, int R, bool kPersist>
-__global__ void __launch_bounds__(kQThreads, 1) qmma_kernel(const __grid_constant__ QmmaArgs a) {
+__global__ void __launch_bounds__(kQThreads, (kPersist && NT <= 2) ? 2 : 1)
+    qmma_kernel(const __grid_constant__ QmmaArgs a) {
     constexpr int C = 8 * NT;        // MMA columns
     constexpr int MP = 4 * NT;       // batch rows covered
     constexpr int kActBytes = 256 * C;
@@ -613,9 +618,9 @@ size_t smem_bytes(int NT, int NS) {
 // idle, and so that each MMA warp sums at most ceil(bpp / R) <= 256 boxes
 // (65536 codes), which keeps its fp32 sums exact.  The ring takes up to
 // kMaxNS stages of the shared memory.  R = 0 takes the default tiles per
-// warp.  With one K piece, more tiles than SMs and the default R, one
-// persistent CTA per SM walks the tiles (no waves of CTAs, each paying the
-// ring's fill).
+// warp.  With one K piece, more tiles than SMs and the default R,
+// persistent CTAs walk the tiles (no waves of CTAs, each paying the ring's
+// fill): two per SM up to 8 rows (shared memory for both), else one.
 bool make_qmma_plan(int M, int64_t K, int64_t N, int num_sms, QmmaPlan* out, int R) {
     if (M < 2 || M > kQmmaMaxM || K < 32 || K % 32 || K > 131072 || N < 1 || N > 0x7FFFFFFF ||
         num_sms < 1)
@@ -640,14 +645,16 @@ bool make_qmma_plan(int M, int64_t K, int64_t N, int num_sms, QmmaPlan* out, int
     if ((pl.bpp + pl.R - 1) / pl.R > 256) return false;
     if (pl.P > 1 && pl.tiles > kTicketSlots) return false;
     if ((int64_t)pl.tiles * pl.P > 0x7FFFFFFF) return false;
+    pl.persist = (pl.P == 1 && pl.tiles > num_sms && pl.R == default_r(pl.NT)) ? 1 : 0;
+    const bool two = pl.persist && pl.NT <= 2;  // two persistent CTAs per SM
+    const size_t cap = two ? (size_t)kSmemMax2 : (size_t)kSmemMax;
     int NS = kMaxNS < pl.bpp ? kMaxNS : pl.bpp;
-    while (NS > 2 && smem_bytes(pl.NT, NS) > (size_t)kSmemMax) --NS;
-    if (smem_bytes(pl.NT, NS) > (size_t)kSmemMax) return false;
+    while (NS > 2 && smem_bytes(pl.NT, NS) > cap) --NS;
+    if (smem_bytes(pl.NT, NS) > cap) return false;
     pl.NS = NS;
     pl.stage_bytes = kBoxBytes + 2048 * pl.NT;
     pl.smem = (int)smem_bytes(pl.NT, NS);
-    pl.persist = (pl.P == 1 && pl.tiles > num_sms && pl.R == default_r(pl.NT)) ? 1 : 0;
-    pl.grid = pl.persist ? num_sms : pl.tiles * pl.P;
+    pl.grid = !pl.persist ? pl.tiles * pl.P : two ? (pl.tiles < 2 * num_sms ? pl.tiles : 2 * num_sms) : num_sms;
     pl.sms = num_sms;
     pl.pre_pieces = (int)(((int64_t)pl.nbox * kBoxCodes + kPreCodes - 1) / kPreCodes);
     // workspace: tickets, scales (64 floats), activation sums [M][pre_pieces],

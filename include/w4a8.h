@@ -97,7 +97,10 @@ typedef enum {
  *    rows for groups of whole 128-code stages up to 16384 codes, otherwise
  *    the one-thread-per-row kernel once per group of up to 8 rows.
  *  - the warp-level e4m3 MMA kernel (mma.sync m16n8k32, operands built in
- *    registers) serves 2..32 rows when w4a8_tuning_t.qmma_max_m asks for it.
+ *    registers) serves row-wise calls of 2..4 rows on matrices of at least
+ *    4 x SMs 128-row tiles in one K piece (lm_head-sized: persistent CTAs,
+ *    two per SM, walk the tiles), ahead of the tensor cores; and 2..32 rows
+ *    on any matrix when w4a8_tuning_t.qmma_max_m asks for it.
  * When the other kernels are switched off the dp4a GEMV serves batches too,
  * one launch per group of up to 8 rows (W8A16: always, 4 rows, fp32 FMAs),
  * each streaming the whole weight matrix.  w4a8_linear_noalloc takes at most
@@ -492,8 +495,9 @@ int w4a8_device_error(unsigned* flags, void* stream);
  *     (kind::f8f6f4, K = 32 per MMA: weight bytes q + 8 read as (q + 8) *
  *     2^-9, activation codes split as 16 a_hi + a_lo).
  *   qmma_max_m: activation rows up to which row-wise W4A8 calls use the
- *     warp-level e4m3 MMA kernel, from 2 rows (0 or 1 = never, the default;
- *     <= 32); it takes precedence over rowdot_max_m and mma_min_m.
+ *     warp-level e4m3 MMA kernel, from 2 rows, on any matrix (<= 32); it
+ *     takes precedence over rowdot_max_m and mma_min_m.  0 = default (2..4
+ *     rows on matrices of at least 4 x SMs tiles in one K piece), 1 = never.
  *   qmma_tiles_per_warp: 16-row weight tiles per warp of that kernel (1, 2,
  *     or 4 for at most 16 rows; 0 = default).
  *   stall_test_us: for tests of the bounded waits (0 = off, <= 1 s): the

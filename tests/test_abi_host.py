@@ -185,10 +185,14 @@ def check_qmma_plan(p, M, K, N, sms):
     P, R = p["splits"], p["threads_per_row"]
     assert p["cols_per_thread"] == 4 * NT and R in (1, 2, 4) and (R < 4 or NT <= 4)
     assert p["ctas_per_split"] == tiles
-    # one K piece, more tiles than SMs, the default tiles per warp: one
-    # persistent CTA per SM walks the tiles
+    # one K piece, more tiles than SMs, the default tiles per warp:
+    # persistent CTAs walk the tiles, two per SM up to 8 rows (each within
+    # half the SM's shared memory), else one
     persist = P == 1 and tiles > sms and R == (4 if NT <= 4 else 2)
-    assert p["grid"] == (sms if persist else tiles * P)
+    two = persist and NT <= 2
+    assert p["grid"] == (min(tiles, 2 * sms) if two else sms if persist else tiles * P)
+    if two:
+        assert p["smem_bytes"] <= 233472 // 2 - 1024
     bpp = -(-nbox // P)
     assert (P - 1) * bpp < nbox                                  # no empty piece
     assert -(-bpp // R) * 256 <= 65536                           # exact fp32 sums per warp
@@ -220,13 +224,22 @@ def check_rowdot_plan(p, M, K, N, sms):
 def test_kernel_routing():
     """Row-wise calls: 1 row on the dp4a GEMV, 2..3 rows on the
     row-per-thread kernel for matrices of at most 2 x SMs tiles, the tensor
-    cores otherwise; an explicit qmma_max_m gives the warp-level kernel 2 rows
-    up to it; with the tensor cores switched off the row-per-thread kernel
-    takes up to rowdot_max_m rows; the tuning moves every threshold."""
+    cores otherwise, except lm_head-sized matrices (at least 4 x SMs tiles in
+    one K piece) at 2..4 rows: the warp-level kernel's persistent plan; an
+    explicit qmma_max_m gives the warp-level kernel 2 rows up to it (any
+    matrix), 1 switches it off; with the tensor cores switched off the
+    row-per-thread kernel takes up to rowdot_max_m rows; the tuning moves
+    every threshold."""
     try:
         route = lambda M, N=18944: w4.w4a8_plan_info(M, 3584, N, num_sms=152)["kernel"]
         assert [route(M) for M in (1, 2, 3, 4, 8, 9, 32, 64)] == [0, 2, 2, 1, 1, 1, 1, 1]
-        assert [route(M, 152064) for M in (1, 2, 3, 4)] == [0, 1, 1, 1]   # lm_head: many tiles
+        assert [route(M, 152064) for M in (1, 2, 3, 4, 5, 8)] == [0, 3, 3, 3, 1, 1]   # lm_head: many tiles
+        p = w4.w4a8_plan_info(4, 3584, 152064, num_sms=152)
+        assert p["grid"] == 2 * 152 and p["splits"] == 1                 # two persistent CTAs per SM
+        assert route(2, 77824 - 128) == 1 and route(2, 77824) == 3       # from 4 x 152 tiles
+        w4.w4a8_set_tuning(qmma_max_m=1)
+        assert [route(M, 152064) for M in (2, 3, 4)] == [1, 1, 1]         # switched off
+        w4.w4a8_set_tuning()
         w4.w4a8_set_tuning(qmma_max_m=16)
         assert [route(M) for M in (2, 16, 17)] == [3, 3, 1]
         w4.w4a8_set_tuning(qmma_max_m=32, qmma_tiles_per_warp=1)

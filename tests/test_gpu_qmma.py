@@ -104,8 +104,9 @@ def test_qmma_parity(w4, orc, M, K, N, seed, fused):
 
 
 @pytest.mark.parametrize("M,K,N,seed", [
-    (2, 1024, 40000, 40),    # 313 tiles: two or three per CTA, ragged last tile
+    (2, 1024, 40000, 40),    # 313 tiles: one or two per CTA (two CTAs per SM), ragged last tile
     (7, 3584, 19457, 41),    # one tile more than 152 SMs, the last of one row
+    (9, 1024, 20000, 45),    # three n-tiles: one CTA per SM
     (16, 512, 30000, 42),    # two boxes per tile
     (20, 288, 20000, 43),    # one partial box per tile, two tiles per warp
     (32, 1024, 25600, 44),   # eight n-tiles
@@ -115,8 +116,9 @@ def test_qmma_persistent_tiles(w4, orc, M, K, N, seed):
     ... with one ring across tile boundaries; every output bit for bit."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     p = w4.w4a8_plan_info(M, K, N)
-    assert p["splits"] == 1
-    assert p["grid"] == (sms if p["ctas_per_split"] > sms else p["ctas_per_split"])
+    tiles = p["ctas_per_split"]
+    assert p["splits"] == 1 and tiles > sms
+    assert p["grid"] == (min(tiles, 2 * sms) if M <= 8 else sms)  # two CTAs per SM up to 8 rows
     check(w4, orc, M, K, N, 900 + seed)
     check(w4, orc, M, K, N, 900 + seed, fused=False, flags=w4.LAUNCH_PDL)
 
