@@ -45,7 +45,8 @@ class _Tuning(ctypes.Structure):
                 ("ring_bytes", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
                 ("mma_min_m", ctypes.c_int), ("rowdot_max_m", ctypes.c_int),
                 ("mma_e4m3", ctypes.c_int), ("qmma_max_m", ctypes.c_int),
-                ("qmma_tiles_per_warp", ctypes.c_int), ("stall_test_us", ctypes.c_int)]
+                ("qmma_tiles_per_warp", ctypes.c_int), ("stall_test_us", ctypes.c_int),
+                ("qmma_operands", ctypes.c_int)]
 
 
 _i64, _p, _u = ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint
@@ -533,12 +534,13 @@ def w4a8_device_error(device=None) -> int:
 def w4a8_set_tuning(force_splits: int = 0, force_threads_per_row: int = 0,
                     ring_bytes: int = 0, ctas_per_sm: int = 0, mma_min_m: int = 0,
                     rowdot_max_m: int = 0, mma_e4m3: int = 0, qmma_max_m: int = 0,
-                    qmma_tiles_per_warp: int = 0, stall_test_us: int = 0, reset: bool = False):
+                    qmma_tiles_per_warp: int = 0, stall_test_us: int = 0, qmma_operands: int = 0,
+                    reset: bool = False):
     if reset:
         _check(lib().w4a8_set_tuning(None))
         return
     t = _Tuning(force_splits, force_threads_per_row, ring_bytes, ctas_per_sm, mma_min_m,
-                rowdot_max_m, mma_e4m3, qmma_max_m, qmma_tiles_per_warp, stall_test_us)
+                rowdot_max_m, mma_e4m3, qmma_max_m, qmma_tiles_per_warp, stall_test_us, qmma_operands)
     _check(lib().w4a8_set_tuning(ctypes.byref(t)))
 
 

@@ -51,6 +51,7 @@ std::atomic<int> g_mma_e4m3{0};
 std::atomic<int> g_qmma_max_m{0};
 std::atomic<int> g_qmma_r{0};
 std::atomic<int> g_stall_test_us{0};
+std::atomic<int> g_qmma_ops{0};  // 0 default (e4m3), 1 binary16, 2 e4m3
 // Test of the bounded waits (w4a8_tuning_t.stall_test_us): 0 = off.
 unsigned long long qmma_stall_ns() { return (unsigned long long)g_stall_test_us.load() * 1000ull; }
 // Row-wise tensor-core calls use e4m3 operands by default: weight bytes
@@ -165,7 +166,7 @@ bool qmma_plan_for(int64_t M, int64_t K, int64_t N, w4a8::QmmaPlan* pl, int sms 
     const int t = g_qmma_max_m.load();
     if (t == 1 || M < 2 || M > (t > 1 ? t : kDefaultQmmaMaxM)) return false;
     if (sms <= 0 && sm_count(&sms) != W4A8_OK) return false;
-    if (!w4a8::make_qmma_plan((int)M, K, N, sms, pl, g_qmma_r.load())) return false;
+    if (!w4a8::make_qmma_plan((int)M, K, N, sms, pl, g_qmma_r.load(), g_qmma_ops.load() == 1)) return false;
     // default routing: persistent plans on many tiles only
     return t > 1 || (pl->persist && pl->tiles >= kQmmaMinTilesPerSm * sms);
 }
@@ -494,7 +495,7 @@ int w4a8_linear_grouped(const uint16_t* X, int64_t M, int64_t K, int G, const ui
         // one plan per matrix inside; the workspace bound covers every N[g] <= total
         for (int g = 0; g < G; ++g) {
             w4a8::QmmaPlan pg;
-            if (!w4a8::make_qmma_plan((int)M, K, N[g], qp.sms, &pg, qp.R) || pg.ws_bytes > qp.ws_bytes)
+            if (!w4a8::make_qmma_plan((int)M, K, N[g], qp.sms, &pg, qp.R, qp.h16 != 0) || pg.ws_bytes > qp.ws_bytes)
                 return fail(W4A8_ERR_SHAPE, "no warp-MMA plan for group %d", g);
         }
         if ((st = check_ws(qp.ws_bytes, ws, ws_bytes)) != W4A8_OK) return st;
@@ -735,6 +736,7 @@ int w4a8_set_tuning(const w4a8_tuning_t* t) {
         g_qmma_max_m = 0;
         g_qmma_r = 0;
         g_stall_test_us = 0;
+        g_qmma_ops = 0;
         return ok();
     }
     if (t->force_splits < 0 || t->force_splits > 16)
@@ -768,6 +770,9 @@ int w4a8_set_tuning(const w4a8_tuning_t* t) {
     if (t->stall_test_us < 0 || t->stall_test_us > 1000000)
         return fail(W4A8_ERR_SHAPE, "stall_test_us must be in [0, 1000000]");
     g_stall_test_us = t->stall_test_us;
+    if (t->qmma_operands < 0 || t->qmma_operands > 2)
+        return fail(W4A8_ERR_SHAPE, "qmma_operands must be 0, 1 or 2");
+    g_qmma_ops = t->qmma_operands;
     return ok();
 }
 
@@ -780,7 +785,7 @@ int w4a8_plan_info(int64_t M, int64_t K, int64_t N, int w8a16, int num_sms, int*
         w4a8::QmmaPlan qp;
         if (qmma_plan_for(M, K, N, &qp, num_sms)) {
             const int ws = qp.ws_bytes > 0x7FFFFFFF ? 0x7FFFFFFF : (int)qp.ws_bytes;
-            const int v[] = {qp.P, qp.R, 4 * qp.NT, 128, qp.tiles, qp.grid, 128, qp.NS, qp.stage_bytes,
+            const int v[] = {qp.P, qp.R, (qp.h16 ? 8 : 4) * qp.NT, 128, qp.tiles, qp.grid, 128, qp.NS, qp.stage_bytes,
                              qp.smem, ws, 3};
             for (int k = 0; k < n_info && k < (int)(sizeof(v) / sizeof(v[0])); ++k) info[k] = v[k];
             return ok();

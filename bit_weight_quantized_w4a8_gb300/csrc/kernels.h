@@ -69,7 +69,7 @@ cudaError_t read_and_clear_rowdot_error(unsigned* flags, cudaStream_t stream);
 // Warp-level e4m3 MMA kernel for small batches (qmma.cu).  make_qmma_plan
 // is host-only and needs no GPU; R = 16-row tiles per warp (1, 2 or 4; 0 =
 // the default for the batch size).
-bool make_qmma_plan(int M, int64_t K, int64_t N, int num_sms, QmmaPlan* out, int R = 0);
+bool make_qmma_plan(int M, int64_t K, int64_t N, int num_sms, QmmaPlan* out, int R = 0, bool h16 = false);
 cudaError_t launch_w4a8_qmma(const QmmaPlan& pl, const uint16_t* X, const int8_t* Xq, const float* sa,
                              int M, int64_t K, int G, const uint8_t* const* Wq,
                              const float* const* sw, const int64_t* Ns, float* const* Y,

@@ -135,6 +135,38 @@ __device__ __forceinline__ uint32_t e4m3_int4(int v0, int v1, int v2, int v3) {
     return e4m3_small(v0) | (e4m3_small(v1) << 8) | (e4m3_small(v2) << 16) | (e4m3_small(v3) << 24);
 }
 
+// Two small integers (|v| <= 2048, exact) as a binary16 pair: lo in bits 0..15.
+__device__ __forceinline__ uint32_t half2_bits(int lo, int hi) {
+    const __half2 h = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Eight packed INT4 codes (a 32-bit word, code i in bits 4i..4i+3, two's
+// complement) as four binary16 pairs of the codes themselves, exactly:
+// p[0] = (c0, c4), p[1] = (c1, c5), p[2] = (c2, c6), p[3] = (c3, c7).  The
+// nibble n ^ 8 = q + 8 is placed under the exponent of 1024 (bits 0x6400 of
+// each half): 1024 + (q + 8), minus 1032, is q; the odd codes sit 4 bits
+// higher, 1024 + 16 (q + 8), and one fused multiply-add by 1/16 and -72
+// gives q (every step exact in binary16).
+__device__ __forceinline__ void int4x8_to_h2(uint32_t w, uint32_t p[4]) {
+    const uint32_t x = w ^ 0x88888888u;
+    const uint32_t y = x >> 8;
+    const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6408u),
+                                        __ushort_as_half((unsigned short)0x6408u));  // 1032
+    const __half2 sc = __halves2half2(__ushort_as_half((unsigned short)0x2C00u),
+                                      __ushort_as_half((unsigned short)0x2C00u));    // 1/16
+    const __half2 off = __halves2half2(__ushort_as_half((unsigned short)0xD480u),
+                                       __ushort_as_half((unsigned short)0xD480u));   // -72
+    uint32_t u[4] = {(x & 0x000F000Fu) | 0x64006400u, (x & 0x00F000F0u) | 0x64006400u,
+                     (y & 0x000F000Fu) | 0x64006400u, (y & 0x00F000F0u) | 0x64006400u};
+    #pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 h = *reinterpret_cast<const __half2*>(&u[i]);
+        const __half2 r = (i & 1) ? __hfma2(h, sc, off) : __hsub2(h, bias);
+        p[i] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+}
+
 // Activation pass.  Grid (MP rows, pieces of 2048 codes covering whole
 // boxes); thread u of piece y handles the 8 codes 8w..8w+7 of its row,
 // w = 256 y + u.  Codes are quantized as in the other paths (or taken from
@@ -147,6 +179,14 @@ __device__ __forceinline__ uint32_t e4m3_int4(int v0, int v1, int v2, int v3) {
 // Rows m >= M and codes past K are zero.  Each CTA also writes the sum of
 // its piece's codes of row m (exact int32) and clears the split-K
 // accumulators.
+// kH (binary16 operands): the codes themselves, exact binary16 integers, in
+// the order of the m16n8k16 B fragments: C = 8 NT columns are NT n-tiles of
+// 8 batch rows (row m: n-tile m / 8, fragment column g = m % 8); 16-byte
+// chunk cc of a box holds K sub-steps s = 0, 1, and lane (g, t) of sub-step
+// s takes codes (8t + 2s, 8t + 2s + 4) as b0 and (8t + 2s + 1, 8t + 2s + 5)
+// as b1 of the chunk (the pairs the weight conversion forms).  Slice
+// layout: [box][cc][s][n-tile][lane][b0, b1], 512 C bytes a box.
+template <bool kH>
 __global__ void __launch_bounds__(kPreThreads) qmma_codes_kernel(
     const __half* __restrict__ X, const int8_t* __restrict__ Xq, const float* __restrict__ sa_in,
     int M, int64_t K, int C, int64_t words, uint8_t* __restrict__ codes, float* __restrict__ sa_ws,
@@ -217,14 +257,24 @@ __global__ void __launch_bounds__(kPreThreads) qmma_codes_kernel(
         // word w of the row: box b, K step (16-byte chunk) sidx, lane column t
         const int64_t b = w >> 5;
         const int sidx = (int)(w >> 2) & 7, t = (int)w & 3;
-        const int col = 8 * (m >> 2) + 2 * (m & 3);
-        uint8_t* base = codes + b * ((int64_t)256 * C) + ((int64_t)(sidx * C + col) * 4 + t) * 8;
-        const uint2 hi = make_uint2(e4m3_int4(e[0] >> 4, e[1] >> 4, e[2] >> 4, e[3] >> 4),
-                                    e4m3_int4(o[0] >> 4, o[1] >> 4, o[2] >> 4, o[3] >> 4));
-        const uint2 lo = make_uint2(e4m3_int4(e[0] & 15, e[1] & 15, e[2] & 15, e[3] & 15),
-                                    e4m3_int4(o[0] & 15, o[1] & 15, o[2] & 15, o[3] & 15));
-        *reinterpret_cast<uint2*>(base) = hi;
-        *reinterpret_cast<uint2*>(base + 32) = lo;  // the next column
+        if constexpr (kH) {
+            // code 2i is e[i], code 2i + 1 is o[i]
+            const int nt = m >> 3, g = m & 7;
+            uint8_t* base = codes + b * ((int64_t)512 * C) + (int64_t)nt * 256 + (g * 4 + t) * 8;
+            #pragma unroll
+            for (int sub = 0; sub < 2; ++sub)
+                *reinterpret_cast<uint2*>(base + (int64_t)(sidx * 2 + sub) * (C / 8) * 256) =
+                    make_uint2(half2_bits(e[sub], e[sub + 2]), half2_bits(o[sub], o[sub + 2]));
+        } else {
+            const int col = 8 * (m >> 2) + 2 * (m & 3);
+            uint8_t* base = codes + b * ((int64_t)256 * C) + ((int64_t)(sidx * C + col) * 4 + t) * 8;
+            const uint2 hi = make_uint2(e4m3_int4(e[0] >> 4, e[1] >> 4, e[2] >> 4, e[3] >> 4),
+                                        e4m3_int4(o[0] >> 4, o[1] >> 4, o[2] >> 4, o[3] >> 4));
+            const uint2 lo = make_uint2(e4m3_int4(e[0] & 15, e[1] & 15, e[2] & 15, e[3] & 15),
+                                        e4m3_int4(o[0] & 15, o[1] & 15, o[2] & 15, o[3] & 15));
+            *reinterpret_cast<uint2*>(base) = hi;
+            *reinterpret_cast<uint2*>(base + 32) = lo;  // the next column
+        }
     }
     // the piece's exact sum of codes (|sum| <= 127 * 2048)
     #pragma unroll
@@ -250,6 +300,15 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t* d, uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
                  : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void mma_e4m3(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -292,12 +351,21 @@ __device__ __forceinline__ void mma_e4m3(float* d, uint32_t a0, uint32_t a1, uin
 // Persistent CTAs of up to 8 batch rows (at most 2 n-tiles) run two to an
 // SM: their latency-bound warps then have twice the company (128 registers
 // a thread, which those instantiations fit without spilling).
-template <int NT, int R, bool kPersist>
+//
+// kH (binary16 operands, mma.sync m16n8k16 f16 -> f32): a weight word
+// becomes four pairs of the codes themselves (int4x8_to_h2), the
+// activation codes are exact binary16 integers, an n-tile covers 8 batch
+// rows (no high / low split) and no bias is removed.  Products |q a| <=
+// 1016 and every fp32 sum of one warp's boxes (at most 16384 codes, which
+// the plan guarantees) stay below 2^24: exact.  Of a 16-byte chunk, K
+// sub-step s pairs (c 2s, c 2s + 4) of word t as fragment columns 2t, 2t + 1
+// and (c 2s + 1, c 2s + 5) as 2t + 8, 2t + 9.
+template <int NT, int R, bool kPersist, bool kH>
 __global__ void __launch_bounds__(kQThreads, (kPersist && NT <= 2) ? 2 : 1)
     qmma_kernel(const __grid_constant__ QmmaArgs a) {
     constexpr int C = 8 * NT;        // MMA columns
-    constexpr int MP = 4 * NT;       // batch rows covered
-    constexpr int kActBytes = 256 * C;
+    constexpr int MP = (kH ? 8 : 4) * NT;  // batch rows covered
+    constexpr int kActBytes = (kH ? 512 : 256) * C;
     constexpr int kStage = kBoxBytes + kActBytes;
     constexpr int WR = kMmaWarps / R;  // warps per box
     constexpr int KS = R * NT <= 2 ? 2 : 1;  // accumulator sets (alternate K steps)
@@ -363,8 +431,9 @@ __global__ void __launch_bounds__(kQThreads, (kPersist && NT <= 2) ? 2 : 1)
         for (int j = 0; j < pre; ++j) issue_a(j);
     // the batch rows' exact code sums, from the activation pass's pieces
     // (one load per thread, added in shared memory; read after the loop)
-    for (int e = tid; e < a.M * a.pre_pieces; e += kQThreads)
-        atomicAdd(sa_sum + e / a.pre_pieces, __ldcg(a.sum_part + e));
+    if constexpr (!kH)  // binary16 codes carry no bias: the sums stay 0
+        for (int e = tid; e < a.M * a.pre_pieces; e += kQThreads)
+            atomicAdd(sa_sum + e / a.pre_pieces, __ldcg(a.sum_part + e));
 
     const int wr = warp % WR, wk = warp / WR;
     const int g = lane >> 2, t = lane & 3;
@@ -408,6 +477,32 @@ __global__ void __launch_bounds__(kQThreads, (kPersist && NT <= 2) ? 2 : 1)
             #pragma unroll
             for (int rt = 0; rt < R; ++rt)
                 ldmatrix_x4(wv[rt], wbox + rt * 2048 + (((2 * sp + lchunk) ^ lsw) << 4));
+            if constexpr (kH) {
+                #pragma unroll
+                for (int h = 0; h < 2; ++h) {  // chunk cc = 2 sp + h of rows g (word 2h) and g + 8 (2h + 1)
+                    const int cc = 2 * sp + h;
+                    uint32_t pg_[R][4], p8_[R][4];
+                    #pragma unroll
+                    for (int rt = 0; rt < R; ++rt) {
+                        int4x8_to_h2(wv[rt][2 * h], pg_[rt]);
+                        int4x8_to_h2(wv[rt][2 * h + 1], p8_[rt]);
+                    }
+                    #pragma unroll
+                    for (int sub = 0; sub < 2; ++sub) {
+                        uint2 b[NT];
+                        #pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            b[nt] = *reinterpret_cast<const uint2*>(abox + ((cc * 2 + sub) * NT + nt) * 256);
+                        #pragma unroll
+                        for (int rt = 0; rt < R; ++rt)
+                            #pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                mma_f16(acc[KS == 2 ? sub : 0][rt][nt], pg_[rt][2 * sub], p8_[rt][2 * sub],
+                                        pg_[rt][2 * sub + 1], p8_[rt][2 * sub + 1], b[nt].x, b[nt].y);
+                    }
+                }
+                continue;
+            }
             #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int ks = 2 * sp + h;
@@ -443,10 +538,28 @@ __global__ void __launch_bounds__(kQThreads, (kPersist && NT <= 2) ? 2 : 1)
             }
         }
     }
-    // exact integers: U = 512 D, row value 16 U_hi + U_lo (batch row 4 nt + t)
+    // exact integers: U = 512 D, row value 16 U_hi + U_lo (batch row 4 nt + t);
+    // binary16: D itself, columns 2t and 2t + 1 of n-tile nt are batch rows
+    // 8 nt + 2t and 8 nt + 2t + 1
     #pragma unroll
     for (int rt = 0; rt < R; ++rt) {
         const int r0 = 16 * (R * wr + rt) + pg;
+        if constexpr (kH) {
+            #pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int m = 8 * nt + 2 * t;
+                int v[4] = {0, 0, 0, 0};
+                #pragma unroll
+                for (int k = 0; k < KS; ++k)
+                    #pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] += __float2int_rn(acc[k][rt][nt][i]);
+                atomicAdd(red + r0 * MP + m, v[0]);
+                atomicAdd(red + r0 * MP + m + 1, v[1]);
+                atomicAdd(red + (r0 + 8) * MP + m, v[2]);
+                atomicAdd(red + (r0 + 8) * MP + m + 1, v[3]);
+            }
+            continue;
+        }
         #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int m = 4 * nt + t;
@@ -554,36 +667,46 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
 // 11.5 / 14.6; past 4 n-tiles 4 tiles a warp would spill.
 constexpr int default_r(int NT) { return NT <= 4 ? 4 : 2; }
 
-template <int NT, int R>
+template <int NT, int R, bool kH>
 const void* kernel_ntr(bool persist) {
     // the persistent form exists for the default tiles per warp only
     if (persist) {
-        if constexpr (R == default_r(NT)) return reinterpret_cast<const void*>(qmma_kernel<NT, R, true>);
+        if constexpr (R == default_r(NT)) return reinterpret_cast<const void*>(qmma_kernel<NT, R, true, kH>);
         return nullptr;
     }
-    return reinterpret_cast<const void*>(qmma_kernel<NT, R, false>);
+    return reinterpret_cast<const void*>(qmma_kernel<NT, R, false, kH>);
 }
 
-template <int NT>
+template <int NT, bool kH>
 const void* kernel_nt(int R, bool persist) {
-    if (R == 1) return kernel_ntr<NT, 1>(persist);
-    if (R == 2) return kernel_ntr<NT, 2>(persist);
+    if (R == 1) return kernel_ntr<NT, 1, kH>(persist);
+    if (R == 2) return kernel_ntr<NT, 2, kH>(persist);
     if constexpr (NT <= 4) {  // 4 tiles a warp would spill past 4 n-tiles
-        if (R == 4) return kernel_ntr<NT, 4>(persist);
+        if (R == 4) return kernel_ntr<NT, 4, kH>(persist);
     }
     return nullptr;
 }
 
-const void* kernel_for(int NT, int R, bool persist) {
+// NT: n-tiles of 4 batch rows (e4m3) or of 8 (binary16, at most 4)
+const void* kernel_for(int NT, int R, bool persist, bool h16) {
+    if (h16) {
+        switch (NT) {
+            case 1: return kernel_nt<1, true>(R, persist);
+            case 2: return kernel_nt<2, true>(R, persist);
+            case 3: return kernel_nt<3, true>(R, persist);
+            case 4: return kernel_nt<4, true>(R, persist);
+            default: return nullptr;
+        }
+    }
     switch (NT) {
-        case 1: return kernel_nt<1>(R, persist);
-        case 2: return kernel_nt<2>(R, persist);
-        case 3: return kernel_nt<3>(R, persist);
-        case 4: return kernel_nt<4>(R, persist);
-        case 5: return kernel_nt<5>(R, persist);
-        case 6: return kernel_nt<6>(R, persist);
-        case 7: return kernel_nt<7>(R, persist);
-        case 8: return kernel_nt<8>(R, persist);
+        case 1: return kernel_nt<1, false>(R, persist);
+        case 2: return kernel_nt<2, false>(R, persist);
+        case 3: return kernel_nt<3, false>(R, persist);
+        case 4: return kernel_nt<4, false>(R, persist);
+        case 5: return kernel_nt<5, false>(R, persist);
+        case 6: return kernel_nt<6, false>(R, persist);
+        case 7: return kernel_nt<7, false>(R, persist);
+        case 8: return kernel_nt<8, false>(R, persist);
         default: return nullptr;
     }
 }
@@ -596,8 +719,8 @@ cudaError_t set_attributes() {
     if (dev < 64 && done[dev]) return cudaSuccess;
     for (int nt = 1; nt <= kQmmaMaxM / 4; ++nt)
         for (int r = 1; r <= 4; r *= 2)
-            for (int persist = 0; persist < 2; ++persist) {
-                const void* fn = kernel_for(nt, r, persist != 0);
+            for (int v = 0; v < 4; ++v) {  // persist x binary16
+                const void* fn = kernel_for(nt, r, (v & 1) != 0, (v & 2) != 0);
                 if (fn == nullptr) continue;
                 e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
                 if (e != cudaSuccess) return e;
@@ -606,8 +729,13 @@ cudaError_t set_attributes() {
     return cudaSuccess;
 }
 
-size_t smem_bytes(int NT, int NS) {
-    return 1024 + (size_t)NS * (kBoxBytes + 2048 * NT) + (size_t)kTile * 4 * NT * 4 + (size_t)4 * NT * 4 +
+// activation slice of one box, batch rows an n-tile covers
+constexpr int act_box_bytes(int NT, bool h16) { return (h16 ? 4096 : 2048) * NT; }
+constexpr int rows_per_tile(bool h16) { return h16 ? 8 : 4; }
+
+size_t smem_bytes(int NT, int NS, bool h16) {
+    const int MP = rows_per_tile(h16) * NT;
+    return 1024 + (size_t)NS * (kBoxBytes + act_box_bytes(NT, h16)) + (size_t)kTile * MP * 4 + (size_t)MP * 4 +
            (size_t)NS * 8 + (size_t)(2 * NS + 2) * 4 + 16;
 }
 
@@ -621,13 +749,14 @@ size_t smem_bytes(int NT, int NS) {
 // warp.  With one K piece, more tiles than SMs and the default R,
 // persistent CTAs walk the tiles (no waves of CTAs, each paying the ring's
 // fill): two per SM up to 8 rows (shared memory for both), else one.
-bool make_qmma_plan(int M, int64_t K, int64_t N, int num_sms, QmmaPlan* out, int R) {
+bool make_qmma_plan(int M, int64_t K, int64_t N, int num_sms, QmmaPlan* out, int R, bool h16) {
     if (M < 2 || M > kQmmaMaxM || K < 32 || K % 32 || K > 131072 || N < 1 || N > 0x7FFFFFFF ||
         num_sms < 1)
         return false;
     QmmaPlan pl = {};
     pl.M = M;
-    pl.NT = (M + 3) / 4;
+    pl.h16 = h16 ? 1 : 0;
+    pl.NT = (M + rows_per_tile(h16) - 1) / rows_per_tile(h16);
     pl.R = R == 0 ? default_r(pl.NT) : R;
     if (pl.R != 1 && pl.R != 2 && pl.R != 4) return false;
     if (pl.R == 4 && pl.NT > 4) return false;
@@ -635,30 +764,33 @@ bool make_qmma_plan(int M, int64_t K, int64_t N, int num_sms, QmmaPlan* out, int
     pl.nbox = (int)((K + kBoxCodes - 1) / kBoxCodes);
     int P = 1;
     if (pl.tiles < num_sms * 4 / 5) P = num_sms / pl.tiles;
-    // each warp sums at most 256 boxes (65536 codes): exact fp32 sums
-    const int pmin = (pl.nbox + 256 * pl.R - 1) / (256 * pl.R);
+    // each warp sums at most 256 boxes (65536 codes) of e4m3 products
+    // (|v a_lo| <= 225) or 64 boxes (16384 codes) of binary16 ones (|q a| <=
+    // 1016): exact fp32 sums
+    const int wmax = h16 ? 64 : 256;
+    const int pmin = (pl.nbox + wmax * pl.R - 1) / (wmax * pl.R);
     if (P < pmin) P = pmin;
     if (P > pl.nbox) P = pl.nbox;
     if (P < 1) P = 1;
     pl.bpp = (pl.nbox + P - 1) / P;
     pl.P = (pl.nbox + pl.bpp - 1) / pl.bpp;
-    if ((pl.bpp + pl.R - 1) / pl.R > 256) return false;
+    if ((pl.bpp + pl.R - 1) / pl.R > wmax) return false;
     if (pl.P > 1 && pl.tiles > kTicketSlots) return false;
     if ((int64_t)pl.tiles * pl.P > 0x7FFFFFFF) return false;
     pl.persist = (pl.P == 1 && pl.tiles > num_sms && pl.R == default_r(pl.NT)) ? 1 : 0;
     const bool two = pl.persist && pl.NT <= 2;  // two persistent CTAs per SM
     const size_t cap = two ? (size_t)kSmemMax2 : (size_t)kSmemMax;
     int NS = kMaxNS < pl.bpp ? kMaxNS : pl.bpp;
-    while (NS > 2 && smem_bytes(pl.NT, NS) > cap) --NS;
-    if (smem_bytes(pl.NT, NS) > cap) return false;
+    while (NS > 2 && smem_bytes(pl.NT, NS, h16) > cap) --NS;
+    if (smem_bytes(pl.NT, NS, h16) > cap) return false;
     pl.NS = NS;
-    pl.stage_bytes = kBoxBytes + 2048 * pl.NT;
-    pl.smem = (int)smem_bytes(pl.NT, NS);
+    pl.stage_bytes = kBoxBytes + act_box_bytes(pl.NT, h16);
+    pl.smem = (int)smem_bytes(pl.NT, NS, h16);
     pl.grid = !pl.persist ? pl.tiles * pl.P : two ? (pl.tiles < 2 * num_sms ? pl.tiles : 2 * num_sms) : num_sms;
     pl.sms = num_sms;
     pl.pre_pieces = (int)(((int64_t)pl.nbox * kBoxCodes + kPreCodes - 1) / kPreCodes);
     // workspace: tickets, scales (64 floats), activation sums [M][pre_pieces],
-    // activation slices [nbox][2048 NT], then int32 [M][128] accumulators per
+    // activation slices [nbox][act_box_bytes], then int32 [M][128] accumulators per
     // tile for split plans.  Sized for any N' <= N on this device (grouped
     // launches plan each matrix on its own): a matrix is split only when its
     // tiles are fewer than 4/5 of the SMs or when K is longer than the
@@ -666,7 +798,7 @@ bool make_qmma_plan(int M, int64_t K, int64_t N, int num_sms, QmmaPlan* out, int
     pl.off_sa = kTicketBytes;
     pl.off_sum = pl.off_sa + 256;
     pl.off_codes = round_up_sz(pl.off_sum + (size_t)M * pl.pre_pieces * 4, 256);
-    pl.off_part = round_up_sz(pl.off_codes + (size_t)pl.nbox * 2048 * pl.NT, 256);
+    pl.off_part = round_up_sz(pl.off_codes + (size_t)pl.nbox * act_box_bytes(pl.NT, h16), 256);
     const int64_t small = num_sms * 4 / 5;
     const int64_t tmax = pmin > 1 ? pl.tiles : (pl.tiles < small ? pl.tiles : small);
     pl.ws_bytes = pl.off_part + round_up_sz((size_t)tmax * M * kTile * 4, 256);
@@ -691,15 +823,17 @@ cudaError_t launch_w4a8_qmma(const QmmaPlan& pl, const uint16_t* X, const int8_t
         int64_t acc_words = (int64_t)((pl.ws_bytes - pl.off_part) / 4);
         void* args[] = {&xh, &Xq, &sa, &Mi, &Kk, &Ci, &words, &codes, &sa_ws, &sum_part, &Xq_out, &sa_out,
                         &acc, &acc_words};
-        cudaError_t e = launch_pdl(reinterpret_cast<const void*>(qmma_codes_kernel),
-                                   dim3(4 * pl.NT, pl.pre_pieces), dim3(kPreThreads), 0, stream, flags, args);
+        const void* pre = pl.h16 ? reinterpret_cast<const void*>(qmma_codes_kernel<true>)
+                                 : reinterpret_cast<const void*>(qmma_codes_kernel<false>);
+        cudaError_t e = launch_pdl(pre, dim3(rows_per_tile(pl.h16 != 0) * pl.NT, pl.pre_pieces), dim3(kPreThreads), 0,
+                                   stream, flags, args);
         if (e != cudaSuccess) return e;
     }
     cudaError_t e = set_attributes();
     if (e != cudaSuccess) return e;
     for (int g = 0; g < G; ++g) {
         QmmaPlan pg;
-        if (!make_qmma_plan(M, K, Ns[g], pl.sms, &pg, pl.R)) return cudaErrorInvalidValue;
+        if (!make_qmma_plan(M, K, Ns[g], pl.sms, &pg, pl.R, pl.h16 != 0)) return cudaErrorInvalidValue;
         QmmaArgs a;
         memset(&a, 0, sizeof(a));
         if (!make_w4_tile_map(&a.tmW, Wq[g], K, Ns[g])) return cudaErrorInvalidValue;
@@ -720,7 +854,7 @@ cudaError_t launch_w4a8_qmma(const QmmaPlan& pl, const uint16_t* X, const int8_t
         a.pre_pieces = pg.pre_pieces;
         a.tiles = pg.tiles;
         a.stall_ns = stall_ns;
-        const void* fn = kernel_for(pg.NT, pg.R, pg.persist != 0);
+        const void* fn = kernel_for(pg.NT, pg.R, pg.persist != 0, pg.h16 != 0);
         if (fn == nullptr) return cudaErrorInvalidValue;
         void* args[] = {&a};
         e = launch_pdl(fn, dim3(pg.grid), dim3(kQThreads), pg.smem, stream, flags, args);

@@ -10,13 +10,15 @@ constexpr int kQmmaMaxM = 32;  // batch rows the kernel is instantiated for: 2..
 
 struct QmmaPlan {
     int M;             // activation rows (2..kQmmaMaxM)
-    int NT;            // n-tiles of 8 MMA columns: ceil(M / 4) (4 batch rows x {high, low} each)
+    int h16;           // 1: binary16 operands (m16n8k16), 0: e4m3 (m16n8k32)
+    int NT;            // n-tiles of 8 MMA columns: ceil(M / 8) batch rows (binary16) or
+                       // ceil(M / 4) (e4m3: 4 batch rows x {high, low} each)
     int R;             // 16-row MMA tiles per warp (= boxes interleaved over R warp groups)
     int tiles;         // 128-row weight tiles
     int nbox;          // 256-code K boxes (K rounded up)
     int P, bpp;        // K pieces, boxes per piece
     int NS;            // ring stages (weight box + activation slice)
-    int stage_bytes;   // 16384 + activation slice
+    int stage_bytes;   // 16384 + activation slice (4096 NT binary16, 2048 NT e4m3)
     int pre_pieces;    // CTAs per batch row of the activation pass
     int persist;       // 1: one CTA per SM walks the tiles b, b + grid, ... (one K piece)
     int grid, smem, sms;

@@ -506,6 +506,15 @@ int w4a8_device_error(unsigned* flags, void* stream);
  *     runs out, sets bit 0 of the device error word and stops the call (its
  *     outputs unspecified); copies already in flight are waited for (with
  *     the usual limit) before the kernel exits.
+ *   qmma_operands: operand type of the warp-level MMA kernel: 0 = default
+ *     (e4m3), 1 = binary16 (mma.sync m16n8k16: each weight code and
+ *     activation code an exact binary16 integer, 8 batch rows an n-tile),
+ *     2 = e4m3 (m16n8k32: weight bytes q + 8 read as (q + 8) * 2^-9,
+ *     activation codes split as 16 a_hi + a_lo, 4 batch rows an n-tile).
+ *     Measured on GB300: e4m3 is faster on lm_head at 2..4 rows (the
+ *     default route: 57.5 vs 65.8 us at 2 rows), binary16 at 5..32 rows
+ *     (gate 3584 -> 18944 at 8 rows 12.5 vs 14.8 us, lm_head at 16 rows
+ *     84.5 vs 126.0), where the tensor cores lead on every matrix but gate.
  * w4a8_workspace_bytes reflects the overrides.  NULL restores the defaults.
  * Not synchronised with calls running on other threads. */
 typedef struct {
@@ -519,6 +528,7 @@ typedef struct {
     int qmma_max_m;
     int qmma_tiles_per_warp;
     int stall_test_us;
+    int qmma_operands;
 } w4a8_tuning_t;
 
 int w4a8_set_tuning(const w4a8_tuning_t* tuning);

@@ -174,19 +174,22 @@ def check_mma_plan(p, M, K, N, sms):
     assert p["ws_bytes"] >= 4096 + 256 + M * K * 2 + (tiles * P * M * 512 if P > 1 else 0)
 
 
-def check_qmma_plan(p, M, K, N, sms):
-    """The warp-level MMA kernel: 4 batch rows per n-tile, 16-row tiles per
-    warp R, pieces of whole 256-code boxes, every warp's fp32 sums over at
-    most 65536 codes, stages of one weight box plus its activation slice."""
+def check_qmma_plan(p, M, K, N, sms, h16=False):
+    """The warp-level MMA kernel: n-tiles of 8 batch rows (binary16 operands)
+    or 4 (e4m3, high and low halves), 16-row tiles per warp R, pieces of
+    whole 256-code boxes, every warp's fp32 sums over at most 16384
+    (binary16) or 65536 (e4m3) codes, stages of one weight box plus its
+    activation slice."""
     assert 2 <= M <= 32
     tiles = -(-N // 128)
     nbox = -(-K // 256)
-    NT = -(-M // 4)
+    rows = 8 if h16 else 4
+    NT = -(-M // rows)
     P, R = p["splits"], p["threads_per_row"]
-    assert p["cols_per_thread"] == 4 * NT and R in (1, 2, 4) and (R < 4 or NT <= 4)
+    assert p["cols_per_thread"] == rows * NT and R in (1, 2, 4) and (R < 4 or NT <= 4)
     assert p["ctas_per_split"] == tiles
     # one K piece, more tiles than SMs, the default tiles per warp:
-    # persistent CTAs walk the tiles, two per SM up to 8 rows (each within
+    # persistent CTAs walk the tiles, two per SM up to 2 n-tiles (each within
     # half the SM's shared memory), else one
     persist = P == 1 and tiles > sms and R == (4 if NT <= 4 else 2)
     two = persist and NT <= 2
@@ -195,13 +198,14 @@ def check_qmma_plan(p, M, K, N, sms):
         assert p["smem_bytes"] <= 233472 // 2 - 1024
     bpp = -(-nbox // P)
     assert (P - 1) * bpp < nbox                                  # no empty piece
-    assert -(-bpp // R) * 256 <= 65536                           # exact fp32 sums per warp
-    assert p["stage_bytes"] == 16384 + 2048 * NT
+    assert -(-bpp // R) * 256 <= (16384 if h16 else 65536)       # exact fp32 sums per warp
+    slice_bytes = (4096 if h16 else 2048) * NT
+    assert p["stage_bytes"] == 16384 + slice_bytes
     assert 2 <= p["stages"] <= 8 or p["stages"] == bpp
-    assert p["stages"] * p["stage_bytes"] + 128 * 4 * NT * 4 < p["smem_bytes"] <= 227 * 1024
+    assert p["stages"] * p["stage_bytes"] + 128 * rows * NT * 4 < p["smem_bytes"] <= 227 * 1024
     assert P == 1 or tiles <= 1024
     pre = -(-nbox * 256 // 2048)
-    assert p["ws_bytes"] >= 4096 + 256 + M * pre * 4 + nbox * 2048 * NT + (tiles * M * 512 if P > 1 else 0)
+    assert p["ws_bytes"] >= 4096 + 256 + M * pre * 4 + nbox * slice_bytes + (tiles * M * 512 if P > 1 else 0)
 
 
 def check_rowdot_plan(p, M, K, N, sms):
@@ -244,8 +248,14 @@ def test_kernel_routing():
         assert [route(M) for M in (2, 16, 17)] == [3, 3, 1]
         w4.w4a8_set_tuning(qmma_max_m=32, qmma_tiles_per_warp=1)
         assert w4.w4a8_plan_info(20, 3584, 18944, num_sms=152)["threads_per_row"] == 1
-        w4.w4a8_set_tuning(qmma_max_m=32, qmma_tiles_per_warp=4)   # 4 tiles a warp up to 16 rows
+        w4.w4a8_set_tuning(qmma_max_m=32, qmma_tiles_per_warp=4, qmma_operands=1)  # binary16: 4 tiles a warp up to 32 rows
+        assert [route(M) for M in (16, 17, 32)] == [3, 3, 3]
+        p = w4.w4a8_plan_info(24, 3584, 18944, num_sms=152)
+        check_qmma_plan(p, 24, 3584, 18944, 152, h16=True)
+        w4.w4a8_set_tuning(qmma_max_m=32, qmma_tiles_per_warp=4)  # e4m3 (the default): up to 16 rows
         assert [route(M) for M in (16, 17)] == [3, 1]
+        with pytest.raises(w4.W4A8Error):
+            w4.w4a8_set_tuning(qmma_operands=3)
         with pytest.raises(w4.W4A8Error):
             w4.w4a8_set_tuning(qmma_tiles_per_warp=3)
         w4.w4a8_set_tuning(qmma_max_m=1, rowdot_max_m=8)
@@ -535,3 +545,20 @@ def _qmma_grouped_cases():
                 p = w4.w4a8_plan_info(M, K, Np, num_sms=sms)
                 check_qmma_plan(p, M, K, Np, sms)
                 assert p["ws_bytes"] <= full["ws_bytes"], (M, K, Np, sms)
+
+
+def test_qmma_binary16_plans():
+    """Warp-level MMA plans with binary16 operands (qmma_operands = 1) for
+    every shape of the plan table: n-tiles of 8 rows, 4096-byte slices per
+    n-tile, at most 64 boxes (16384 codes) per warp accumulator."""
+    try:
+        w4.w4a8_set_tuning(qmma_max_m=32, qmma_operands=1)
+        for sms in (152, 20):
+            for (M, K, N) in SHAPES + [(7, 131072, 300), (12, 65536, 2000), (32, 512, 200000)]:
+                if not 2 <= M <= 32:
+                    continue
+                p = w4.w4a8_plan_info(M, K, N, num_sms=sms)
+                assert p["kernel"] == 3
+                check_qmma_plan(p, M, K, N, sms, h16=True)
+    finally:
+        w4.w4a8_set_tuning(reset=True)

@@ -1,12 +1,14 @@
-"""The warp-level e4m3 MMA kernel (2..32 batch rows) against the CPU oracle,
-element by element, through the C ABI.
+"""The warp-level MMA kernel (2..32 batch rows) against the CPU oracle,
+element by element, through the C ABI, with both operand types.
 
-The kernel encodes INT4 weight codes as e4m3 bytes v = q + 8 (exactly
-v * 2^-9) and INT8 activation codes as two exact e4m3 integers
-(a = 16 a_hi + a_lo); the fp32 sums of the MMAs are exact, so the int32
-accumulators, Xq, s_a and Y must equal the oracle's bit for bit.  Shapes
-span one and several 128-row tiles, ragged row and K tails (a partial last
-256-code box), split K, every n-tile count (1..8) and the largest sums.
+binary16: every INT4 weight code and INT8 activation code is an exact
+binary16 integer (m16n8k16).  e4m3: weight codes become the bytes v = q + 8
+(exactly v * 2^-9) and activation codes two exact e4m3 integers
+(a = 16 a_hi + a_lo, m16n8k32).  Either way the fp32 sums of the MMAs are
+exact, so the int32 accumulators, Xq, s_a and Y must equal the oracle's bit
+for bit.  Shapes span one and several 128-row tiles, ragged row and K tails
+(a partial last 256-code box), split K, every n-tile count and the largest
+sums.
 """
 import numpy as np
 import pytest
@@ -37,9 +39,15 @@ def orc():
     return oracle.load()
 
 
+@pytest.fixture(params=[1, 2], ids=["binary16", "e4m3"])
+def ops(request):
+    """Operand type of the kernel (w4a8_tuning_t.qmma_operands)."""
+    return request.param
+
+
 @pytest.fixture(autouse=True)
-def _reset_tuning(w4):
-    w4.w4a8_set_tuning(qmma_max_m=32)  # by default the kernel serves 4..8 rows
+def _reset_tuning(w4, ops):
+    w4.w4a8_set_tuning(qmma_max_m=32, qmma_operands=ops)  # every matrix, 2..32 rows
     yield
     w4.w4a8_set_tuning(reset=True)
     assert w4.w4a8_device_error() == 0
@@ -111,22 +119,23 @@ def test_qmma_parity(w4, orc, M, K, N, seed, fused):
     (20, 288, 20000, 43),    # one partial box per tile, two tiles per warp
     (32, 1024, 25600, 44),   # eight n-tiles
 ])
-def test_qmma_persistent_tiles(w4, orc, M, K, N, seed):
+def test_qmma_persistent_tiles(w4, orc, ops, M, K, N, seed):
     """One K piece and more tiles than SMs: each CTA walks tiles b, b + grid,
     ... with one ring across tile boundaries; every output bit for bit."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     p = w4.w4a8_plan_info(M, K, N)
     tiles = p["ctas_per_split"]
     assert p["splits"] == 1 and tiles > sms
-    assert p["grid"] == (min(tiles, 2 * sms) if M <= 8 else sms)  # two CTAs per SM up to 8 rows
+    two = M <= (16 if ops == 1 else 8)  # two CTAs per SM up to two n-tiles
+    assert p["grid"] == (min(tiles, 2 * sms) if two else sms)
     check(w4, orc, M, K, N, 900 + seed)
     check(w4, orc, M, K, N, 900 + seed, fused=False, flags=w4.LAUNCH_PDL)
 
 
 @pytest.mark.parametrize("M", [2, 6, 32])
 def test_qmma_longest_rows(w4, orc, M):
-    """K = 131072: every warp sums 65536 codes (the exactness limit of its
-    fp32 sums), the pieces meet in int32."""
+    """K = 131072: every warp sums the most codes its fp32 sums hold exactly
+    (16384 binary16 products, 65536 e4m3 ones), the pieces meet in int32."""
     p = check(w4, orc, M, 131072, 5, 950 + M)
     assert p["splits"] >= 2
 
@@ -135,8 +144,9 @@ def test_qmma_longest_rows(w4, orc, M):
 @pytest.mark.parametrize("K", [4096, 131072])
 def test_qmma_largest_sums(w4, M, K):
     """Weight codes 7 and -8 (nibble 0x8, legal on input) against activation
-    codes +127 and -127: the largest products of both encodings (v = 15 and
-    v = 0) and the bias correction 8 * sum(a) at its extremes."""
+    codes +127 and -127: the largest products (binary16 |q a| = 1016; e4m3
+    bytes v = 15 and v = 0) and the e4m3 bias correction 8 * sum(a) at its
+    extremes."""
     N = 256
     Wq = torch.full((N, K // 2), 0x77, dtype=torch.uint8, device="cuda")
     Wq[1::2] = 0x88                            # odd rows: every code -8
@@ -177,7 +187,7 @@ def test_qmma_grouped(w4, orc):
             assert np.array_equal(bits(Y.cpu().numpy()), bits(ref))
 
 
-def test_qmma_matches_other_kernels(w4):
+def test_qmma_matches_other_kernels(w4, ops):
     """The same call on the warp-level MMA kernel, the row-per-thread kernel,
     the tensor cores and the dp4a GEMV gives the same bits."""
     M, K, N = 6, 3584, 1000
@@ -185,7 +195,7 @@ def test_qmma_matches_other_kernels(w4):
     X = to_dev(synth.activation(971, M, K, outlier_frac=0.001))
     Wq, sw = w4.w4_quantize_weights(to_dev(W))
     outs = []
-    for kw, kind in ((dict(qmma_max_m=8), QMMA), (dict(qmma_max_m=1, rowdot_max_m=8), 2), (dict(qmma_max_m=1, rowdot_max_m=1), 1),
+    for kw, kind in ((dict(qmma_max_m=8, qmma_operands=ops), QMMA), (dict(qmma_max_m=1, rowdot_max_m=8), 2), (dict(qmma_max_m=1, rowdot_max_m=1), 1),
                      (dict(qmma_max_m=1, rowdot_max_m=1, mma_min_m=65), 0)):
         w4.w4a8_set_tuning(**kw)
         assert w4.w4a8_plan_info(M, K, N)["kernel"] == kind
@@ -231,12 +241,12 @@ def test_qmma_pdl_chain_and_graph(w4, orc):
 @pytest.mark.parametrize("R", [1, 2, 4])
 @pytest.mark.parametrize("M,K,N,seed", [(3, 3584, 300, 20), (8, 18944, 129, 21), (16, 1024, 777, 22),
                                         (25, 2304, 260, 23)])
-def test_qmma_tiles_per_warp(w4, orc, R, M, K, N, seed):
+def test_qmma_tiles_per_warp(w4, orc, ops, R, M, K, N, seed):
     """Every tiles-per-warp choice (boxes interleaved over R warp groups)
-    gives the oracle's bits; 4 tiles a warp exist up to 16 rows (past that
-    the call takes the next kernel)."""
-    w4.w4a8_set_tuning(qmma_tiles_per_warp=R, qmma_max_m=32)
-    if R == 4 and M > 16:  # no such kernel: the call goes to the tensor cores
+    gives the oracle's bits; with e4m3 operands 4 tiles a warp exist up to 16
+    rows (past that the call takes the next kernel)."""
+    w4.w4a8_set_tuning(qmma_tiles_per_warp=R, qmma_max_m=32, qmma_operands=ops)
+    if R == 4 and M > 16 and ops == 2:  # no such e4m3 kernel: the call goes to the tensor cores
         assert w4.w4a8_plan_info(M, K, N)["kernel"] == 1
         return
     assert w4.w4a8_plan_info(M, K, N)["threads_per_row"] == R
