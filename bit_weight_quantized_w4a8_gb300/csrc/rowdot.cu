@@ -490,13 +490,22 @@ __global__ void __launch_bounds__(kTile * kMaxPhases, 1) rowdot_group_kernel(con
         const uintptr_t hi = reinterpret_cast<uintptr_t>(srow + gb);
         for (uintptr_t q = lo; q <= hi; q += 128) prefetch_l1(reinterpret_cast<const void*>(q));
     }
-    // scales of the groups holding the 8 chunks of box i (rows past N read
-    // row 0's and write nothing; chunks past K clamp to the last group)
+    // scales of the groups that end in the 8 chunks of box i (rows past N
+    // read row 0's and write nothing; chunks past K clamp to the last group).
+    // Only a chunk that ends a group uses its scale: boxes start on 256-code
+    // boundaries, so for groups of at most 256 codes that is every chunk
+    // with 32 (c + 1) a multiple of the group, for longer groups at most the
+    // last chunk (uniform over the CTA; 2 loads a box instead of 8 at
+    // groups of 128 codes)
     auto load_scales = [&](int i, float* sc) {
         #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const int gi = min(((box0 + i) * kBoxCodes + 32 * c) >> a.gshift, a.ngroups - 1);
-            sc[c] = __ldg(srow + gi);
+            if (((32 * (c + 1)) & gmask) == 0 || c == 7) {
+                const int gi = min(((box0 + i) * kBoxCodes + 32 * c) >> a.gshift, a.ngroups - 1);
+                sc[c] = __ldg(srow + gi);
+            } else {
+                sc[c] = 0.f;
+            }
         }
     };
     const int i_first = ph * a.abox;
