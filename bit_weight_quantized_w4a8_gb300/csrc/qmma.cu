@@ -1,12 +1,12 @@
 // qmma.cu -- W4A8 linear for decode batches of 2..32 rows on the warp-level
-// e4m3 MMA (mma.sync m16n8k32, fp32 accumulation), operands built in
-// registers.
+// MMA (mma.sync, fp32 accumulation), operands built in registers: e4m3
+// (m16n8k32, the default) or binary16 (m16n8k16).
 //
 // The arithmetic is the W4A8 contract of the Jetson INT4 page (sections
 // 正确方向 / 当前实现方式): INT8 activation codes times INT4 weight codes,
 // summed exactly in integers, y = ((float)acc * s_w) * s_a.
 //
-// Operand encodings (all exact):
+// e4m3 operand encodings (all exact):
 //  * weights: a packed nibble n (two's complement code q) becomes the byte
 //    v = n ^ 8 = q + 8 in [0, 15].  Read as e4m3, a byte whose bits 4..6
 //    are zero is exactly v * 2^-9: bytes 0..7 are the subnormals m * 2^-9
@@ -25,20 +25,24 @@
 //    removes the +8 bias of the weight encoding (S_a is computed exactly
 //    by the activation pass).  The result is bit-identical to the integer
 //    definition, whatever the order of the hardware's sums.
+// binary16 operands: the weight and activation codes themselves, exact
+// binary16 integers (int4x8_to_h2 below); an n-tile covers 8 batch rows, no
+// bias; |q a| <= 1016, so each warp sums at most 16384 codes.
 //
 // Two kernels:
-//  * qmma_codes_kernel (grid: padded batch rows x pieces of 2048 codes):
-//    the per-row INT8 quantization (actq.cuh) or the given int8 codes,
-//    split into e4m3 high / low bytes in the order the MMA fragments read
-//    them (one contiguous activation slice per 256-code box), and per
-//    piece the exact partial sum of the row's codes.
-//  * qmma_kernel<NT, R> (one CTA of 8 MMA warps + 1 copy warp per 128
-//    weight rows and K piece): the copy warp streams 2-D TMA boxes of 128
-//    rows x 256 codes (128-byte swizzle) and the matching activation slice
-//    into a ring; MMA warp (wr, wk) owns R 16-row tiles and every R-th box,
-//    so the activation fragments it loads serve R weight tiles; at the end
-//    the warps' exact integer sums meet in shared memory and K pieces meet
-//    in int32 through the workspace (order-free).
+//  * qmma_codes_kernel<kH> (grid: padded batch rows x pieces of 2048
+//    codes): the per-row INT8 quantization (actq.cuh) or the given int8
+//    codes, written in the order the MMA fragments read them (one
+//    contiguous activation slice per 256-code box), and per piece the exact
+//    partial sum of the row's codes.
+//  * qmma_kernel<NT, R, kPersist, kH> (8 MMA warps; thread 0 fills a ring
+//    of 2-D TMA boxes of 128 rows x 256 codes (128-byte swizzle) plus the
+//    matching activation slices, the last warp done with a stage refills
+//    it): MMA warp (wr, wk) owns R 16-row tiles and every R-th box, so the
+//    activation fragments it loads serve R weight tiles; the warps' exact
+//    integer sums meet in shared memory and K pieces meet in int32 through
+//    the workspace (order-free).  A CTA takes one 128-row tile and K piece,
+//    or (kPersist) walks tiles b, b + grid, ... through one ring.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
