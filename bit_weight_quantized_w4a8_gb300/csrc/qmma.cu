@@ -505,23 +505,23 @@ __global__ void __launch_bounds__(kQThreads, (kPersist && NT <= 2) ? 2 : 1)
                                         pg_[rt][2 * sub + 1], p8_[rt][2 * sub + 1], b[nt].x, b[nt].y);
                     }
                 }
-                continue;
-            }
-            #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int ks = 2 * sp + h;
-                uint2 b[NT];
+            } else {
                 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    b[nt] = *reinterpret_cast<const uint2*>(abox + (ks * C + 8 * nt) * 32);
-                #pragma unroll
-                for (int rt = 0; rt < R; ++rt) {
-                    const uint32_t x0 = wv[rt][2 * h] ^ 0x88888888u, x1 = wv[rt][2 * h + 1] ^ 0x88888888u;
-                    const uint32_t a0 = x0 & 0x0F0F0F0Fu, a2 = (x0 >> 4) & 0x0F0F0F0Fu;
-                    const uint32_t a1 = x1 & 0x0F0F0F0Fu, a3 = (x1 >> 4) & 0x0F0F0F0Fu;
+                for (int h = 0; h < 2; ++h) {
+                    const int ks = 2 * sp + h;
+                    uint2 b[NT];
                     #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        mma_e4m3(acc[KS == 2 ? h : 0][rt][nt], a0, a1, a2, a3, b[nt].x, b[nt].y);
+                        b[nt] = *reinterpret_cast<const uint2*>(abox + (ks * C + 8 * nt) * 32);
+                    #pragma unroll
+                    for (int rt = 0; rt < R; ++rt) {
+                        const uint32_t x0 = wv[rt][2 * h] ^ 0x88888888u, x1 = wv[rt][2 * h + 1] ^ 0x88888888u;
+                        const uint32_t a0 = x0 & 0x0F0F0F0Fu, a2 = (x0 >> 4) & 0x0F0F0F0Fu;
+                        const uint32_t a1 = x1 & 0x0F0F0F0Fu, a3 = (x1 >> 4) & 0x0F0F0F0Fu;
+                        #pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_e4m3(acc[KS == 2 ? h : 0][rt][nt], a0, a1, a2, a3, b[nt].x, b[nt].y);
+                    }
                 }
             }
         }
@@ -562,19 +562,19 @@ __global__ void __launch_bounds__(kQThreads, (kPersist && NT <= 2) ? 2 : 1)
                 atomicAdd(red + (r0 + 8) * MP + m, v[2]);
                 atomicAdd(red + (r0 + 8) * MP + m + 1, v[3]);
             }
-            continue;
-        }
-        #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int m = 4 * nt + t;
-            int v0 = 0, v1 = 0;
+        } else {
             #pragma unroll
-            for (int k = 0; k < KS; ++k) {
-                v0 += 16 * __float2int_rn(acc[k][rt][nt][0] * 512.f) + __float2int_rn(acc[k][rt][nt][1] * 512.f);
-                v1 += 16 * __float2int_rn(acc[k][rt][nt][2] * 512.f) + __float2int_rn(acc[k][rt][nt][3] * 512.f);
+            for (int nt = 0; nt < NT; ++nt) {
+                const int m = 4 * nt + t;
+                int v0 = 0, v1 = 0;
+                #pragma unroll
+                for (int k = 0; k < KS; ++k) {
+                    v0 += 16 * __float2int_rn(acc[k][rt][nt][0] * 512.f) + __float2int_rn(acc[k][rt][nt][1] * 512.f);
+                    v1 += 16 * __float2int_rn(acc[k][rt][nt][2] * 512.f) + __float2int_rn(acc[k][rt][nt][3] * 512.f);
+                }
+                atomicAdd(red + r0 * MP + m, v0);
+                atomicAdd(red + (r0 + 8) * MP + m, v1);
             }
-            atomicAdd(red + r0 * MP + m, v0);
-            atomicAdd(red + (r0 + 8) * MP + m, v1);
         }
     }
     __syncthreads();
