@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import bit_weight_quantized_w4a8_gb300 as w4
@@ -128,36 +129,66 @@ def test_plan_invariants(sms, w8):
     for (M, K, N) in SHAPES:
         if w8 and K > 65536:
             continue
-        p = w4.w4a8_plan_info(M, K, N, w8a16=w8, num_sms=sms)
-        if p["kernel"] == 1:
-            check_mma_plan(p, M, K, N, sms)
-            continue
-        if p["kernel"] == 2:
-            check_rowdot_plan(p, M, K, N, sms)
-            continue
-        if p["kernel"] == 3:
-            check_qmma_plan(p, M, K, N, sms)
-            continue
-        M = min(M, 4 if w8 else 8)  # the plan of the first launch of a row-group sequence
-        kgran = 16 if w8 else 32
-        Gt = K // kgran
-        P = p["splits"]
-        Gq = -(-Gt // P)
-        assert 1 <= P <= 16 and (P - 1) * Gq < Gt
-        Cl, S = p["threads_per_row"], p["cols_per_thread"]
-        assert Cl & (Cl - 1) == 0 and Cl * S >= Gq and Cl * (S - 1) < Gq
-        mt = 1 if M <= 1 else 2 if M <= 2 else 4 if M <= 4 else 8
-        assert S <= 8 // mt
-        assert p["rows_per_stage"] * Cl == 256
-        assert p["grid"] == p["ctas_per_split"] * P
-        assert p["ctas_per_split"] <= N
-        assert p["rows_per_cta"] * p["ctas_per_split"] >= N
-        assert p["rows_per_cta"] <= 4096 or P > 1
-        assert 2 <= p["stages"] <= 16
-        assert p["stage_bytes"] % 128 == 0 and p["stage_bytes"] >= p["rows_per_stage"] * Gq * 16
-        assert p["smem_bytes"] <= 232448
-        if P > 1:
-            assert p["ws_bytes"] > 0
+        check_any_plan(M, K, N, sms, w8)
+
+
+def test_plan_invariants_random():
+    """The same invariants on 400 seeded random shapes (batch 1..64, K a
+    multiple of 32 up to 131072, N up to 300000, 1..160 SMs), under the
+    default routing and with the warp-level kernel at every batch it takes
+    (both operand types).  Every kernel kind is reached."""
+    rng = np.random.default_rng(20261202)
+    seen = set()
+    tunings = [dict(), dict(qmma_max_m=32), dict(qmma_max_m=32, qmma_operands=1)]
+    try:
+        for i in range(400):
+            M = int(rng.choice([1, 2, 3, 4, 8, rng.integers(1, 65)]))
+            K = 32 * int(rng.choice([rng.integers(1, 129), rng.integers(1, 4097)]))
+            N = int(rng.choice([rng.integers(1, 5000), rng.integers(1, 300001)]))
+            sms = int(rng.choice([152, 148, int(rng.integers(1, 161))]))
+            w8 = bool(rng.integers(0, 4) == 0) and K <= 65536 and K % 16 == 0
+            tun = tunings[i % len(tunings)]
+            w4.w4a8_set_tuning(**tun)
+            seen.add(check_any_plan(M, K, N, sms, w8, h16=tun.get("qmma_operands") == 1))
+    finally:
+        w4.w4a8_set_tuning(reset=True)
+    assert seen == {0, 1, 2, 3}, seen
+
+
+def check_any_plan(M, K, N, sms, w8, h16=False):
+    """Checks the plan w4a8_plan_info reports for one call, whichever kernel
+    the routing picks (h16: the warp-level kernel has binary16 operands)."""
+    p = w4.w4a8_plan_info(M, K, N, w8a16=w8, num_sms=sms)
+    if p["kernel"] == 1:
+        check_mma_plan(p, M, K, N, sms)
+        return 1
+    if p["kernel"] == 2:
+        check_rowdot_plan(p, M, K, N, sms)
+        return 2
+    if p["kernel"] == 3:
+        check_qmma_plan(p, M, K, N, sms, h16=h16)
+        return 3
+    M = min(M, 4 if w8 else 8)  # the plan of the first launch of a row-group sequence
+    kgran = 16 if w8 else 32
+    Gt = K // kgran
+    P = p["splits"]
+    Gq = -(-Gt // P)
+    assert 1 <= P <= 16 and (P - 1) * Gq < Gt
+    Cl, S = p["threads_per_row"], p["cols_per_thread"]
+    assert Cl & (Cl - 1) == 0 and Cl * S >= Gq and Cl * (S - 1) < Gq
+    mt = 1 if M <= 1 else 2 if M <= 2 else 4 if M <= 4 else 8
+    assert S <= 8 // mt
+    assert p["rows_per_stage"] * Cl == 256
+    assert p["grid"] == p["ctas_per_split"] * P
+    assert p["ctas_per_split"] <= N
+    assert p["rows_per_cta"] * p["ctas_per_split"] >= N
+    assert p["rows_per_cta"] <= 4096 or P > 1
+    assert 2 <= p["stages"] <= 16
+    assert p["stage_bytes"] % 128 == 0 and p["stage_bytes"] >= p["rows_per_stage"] * Gq * 16
+    assert p["smem_bytes"] <= 232448
+    if P > 1:
+        assert p["ws_bytes"] > 0
+    return 0
 
 
 def check_mma_plan(p, M, K, N, sms):
